@@ -1,0 +1,107 @@
+"""Oracle: plain fp64 CPU reference of the Q-Delta / QED forward and decode step.
+
+TEST INFRASTRUCTURE.  Only `tests/`, `__graft_entry__.smoke()` and `bench.py`'s
+CPU-baseline / reference leg may import this package.  It shares no code with
+the CUDA path and the CUDA path never calls it.
+
+The arithmetic lives in `qdelta_oracle.c` (sequential recurrences in the pages'
+step order; citations in its header).  This module only marshals numpy arrays to
+fp64 and calls it.  `build()` compiles the C file with gcc (no CUDA involved).
+
+Array layouts (all numpy, any float dtype; converted to fp64):
+  q, k [B,T,H,dk]; v [B,T,H,dv]; Q-Delta gates [B,T,H]; QED g, b [B,T,H,dk],
+  w [B,T,H,dv], lam_h [H]; states [B,H,dv,dk] (QED: its K x V state transposed).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "qdelta_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile qdelta_oracle.c into liboracle.so (gcc, -O2, portable flags)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-D_POSIX_C_SOURCE=200809L", "-shared",
+                               "-fPIC", "-o", tmp, _SRC, "-lpthread", "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        lib.oracle_qdelta_fwd.argtypes = [I] * 5 + [P] * 9 + [I]
+        lib.oracle_qed_fwd.argtypes = [I] * 5 + [P] * 10 + [I]
+        lib.oracle_qdelta_step.argtypes = [I] * 4 + [P] * 8 + [I]
+        for f in (lib.oracle_qdelta_fwd, lib.oracle_qed_fwd, lib.oracle_qdelta_step):
+            f.restype = I
+        _lib = lib
+    return _lib
+
+
+def _f64(x):
+    if x is None:
+        return None
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _ptr(x):
+    return None if x is None else x.ctypes.data_as(ctypes.c_void_p)
+
+
+def qdelta_fwd(q, k, v, alpha, beta, lam, S0=None, nthreads: int = 0):
+    """Sequential Q-Delta forward.  alpha None = 1, lam None = 0, S0 None = 0.
+    Returns (o [B,T,H,dv], S_final [B,H,dv,dk]) in fp64."""
+    q, k, v, alpha, beta, lam, S0 = map(_f64, (q, k, v, alpha, beta, lam, S0))
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    o = np.zeros((B, T, H, dv))
+    S = np.zeros((B, H, dv, dk))
+    rc = _load().oracle_qdelta_fwd(B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+                                   _ptr(beta), _ptr(lam), _ptr(S0), _ptr(o), _ptr(S), nthreads)
+    if rc:
+        raise MemoryError("oracle_qdelta_fwd failed")
+    return o, S
+
+
+def qed_fwd(q, k, v, g, b, w, lam_h, S0=None, nthreads: int = 0):
+    """Sequential QED forward (GDN-2 with the query-derived erase direction).
+    Returns (o [B,T,H,dv], S_final [B,H,dv,dk] = QED's K x V state transposed)."""
+    q, k, v, g, b, w, lam_h, S0 = map(_f64, (q, k, v, g, b, w, lam_h, S0))
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    o = np.zeros((B, T, H, dv))
+    S = np.zeros((B, H, dv, dk))
+    rc = _load().oracle_qed_fwd(B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b),
+                                _ptr(w), _ptr(lam_h), _ptr(S0), _ptr(o), _ptr(S), nthreads)
+    if rc:
+        raise MemoryError("oracle_qed_fwd failed")
+    return o, S
+
+
+def qdelta_step(S, q, k, v, alpha, beta, lam, nthreads: int = 0):
+    """One decode step.  S [N,H,dv,dk] fp64 numpy array, updated IN PLACE;
+    tokens [N,H,d], gates [N,H].  Returns o [N,H,dv]."""
+    if not (isinstance(S, np.ndarray) and S.dtype == np.float64 and S.flags.c_contiguous):
+        raise TypeError("S must be a C-contiguous float64 numpy array (updated in place)")
+    q, k, v, alpha, beta, lam = map(_f64, (q, k, v, alpha, beta, lam))
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    o = np.zeros((N, H, dv))
+    rc = _load().oracle_qdelta_step(N, H, dk, dv, _ptr(S), _ptr(q), _ptr(k), _ptr(v),
+                                    _ptr(alpha), _ptr(beta), _ptr(lam), _ptr(o), nthreads)
+    if rc:
+        raise MemoryError("oracle_qdelta_step failed")
+    return o

@@ -1,0 +1,233 @@
+/*
+ * Oracle for the Q-Delta / QED forward and the Q-Delta decode step:
+ * plain fp64 sequential recurrences on the CPU.
+ *
+ * TEST INFRASTRUCTURE.  Only the tests, the package smoke check and the bench's
+ * CPU-baseline / reference leg load this library.  It shares no code with the
+ * CUDA path (no headers, helpers or tables) and the CUDA path never calls it.
+ *
+ * It computes the definition, not the chunked algorithm: one token at a time,
+ * in the order the pages state the steps, with no blocking or reordering.
+ *
+ *  - Q-Delta, gated recurrence: "Q-Delta: Beyond Key-Value Associative State
+ *    Evolution", Sec. 3.3.1, Eqs. 17-20 (the boxed gated form and the teaching
+ *    pseudocode under it).  State S is d_v x d_k, output o_t = S_t q_t.
+ *      x = k + lambda q;  S_prior = alpha S;  e = v - S_prior x;
+ *      S = S_prior + beta e k^T;  o = S q.
+ *    Absent alpha means 1 and absent lambda means 0 (Gated DeltaNet, DeltaNet).
+ *    No 1+lambda normalisation of the residual (same section).
+ *  - QED over GDN-2: "The Query Knows What to Forget", Sec. 2 Eqs. 4 and 8
+ *    (GDN-2 update) and Sec. 3.1 Eq. 6 (erase vector).  State S is K x V,
+ *    output o_t = S_t^T q_t.
+ *      Sbar = Diag(exp g) S;  u = b*q;  d = u - k (k^T u);  a = b*k + lambda_h d;
+ *      r = w*v - Sbar^T a;  S = Sbar + k r^T;  o = S^T q.
+ *    d is formed with the given k as it is (the pages' projection assumes
+ *    |k| = 1; no renormalisation is done here).
+ *  - Decode step: one iteration of the Q-Delta loop per call, state in place.
+ *
+ * Storage of every state buffer, both methods: [B][H][d_v][d_k] row-major.  For
+ * Q-Delta that is S itself; for QED it is S^T (QED's K x V state transposed), so
+ * both share one format.  Token tensors are [B][T][H][d], gates [B][T][H],
+ * QED's per-channel g, b [B][T][H][d_k] and w [B][T][H][d_v], lambda_h [H].
+ *
+ * Parity pins: see tests/test_oracle_pins.py (worked examples, closed forms,
+ * special cases, brute force on tiny inputs).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+typedef struct {
+    int B, T, H, dk, dv;
+    const double *q, *k, *v, *alpha, *beta, *lam;   /* Q-Delta gates */
+    const double *g, *bgate, *w, *lam_h;            /* QED gates */
+    const double *S0;
+    double *o, *S_final;
+    int method;          /* 0 = Q-Delta, 1 = QED */
+    int first, stride;   /* this worker's (b,h) streams: first, first+stride, ... */
+    int status;
+} job_t;
+
+/* One Q-Delta stream (b, h), t = 0..T-1. */
+static int qdelta_stream(const job_t *J, int b, int h)
+{
+    const int T = J->T, H = J->H, dk = J->dk, dv = J->dv;
+    double *S = malloc(sizeof(double) * (size_t)dv * dk);
+    double *x = malloc(sizeof(double) * (size_t)dk);
+    double *e = malloc(sizeof(double) * (size_t)dv);
+    if (!S || !x || !e) { free(S); free(x); free(e); return 1; }
+    const size_t sh = ((size_t)b * H + h) * dv * dk;
+    if (J->S0) memcpy(S, J->S0 + sh, sizeof(double) * (size_t)dv * dk);
+    else memset(S, 0, sizeof(double) * (size_t)dv * dk);
+
+    for (int t = 0; t < T; ++t) {
+        const size_t tok = ((size_t)b * T + t) * H + h;
+        const double *qt = J->q + tok * dk, *kt = J->k + tok * dk, *vt = J->v + tok * dv;
+        const double alpha = J->alpha ? J->alpha[tok] : 1.0;
+        const double beta = J->beta[tok];
+        const double lam = J->lam ? J->lam[tok] : 0.0;
+        double *ot = J->o + tok * dv;
+
+        for (int j = 0; j < dk; ++j) x[j] = kt[j] + lam * qt[j];          /* x = k + lambda q */
+        for (size_t n = 0; n < (size_t)dv * dk; ++n) S[n] *= alpha;       /* S_prior = alpha S */
+        for (int i = 0; i < dv; ++i) {                                     /* e = v - S_prior x */
+            const double *Si = S + (size_t)i * dk;
+            double acc = 0.0;
+            for (int j = 0; j < dk; ++j) acc += Si[j] * x[j];
+            e[i] = vt[i] - acc;
+        }
+        for (int i = 0; i < dv; ++i) {                                     /* S += beta e k^T */
+            double *Si = S + (size_t)i * dk;
+            const double be = beta * e[i];
+            for (int j = 0; j < dk; ++j) Si[j] += be * kt[j];
+        }
+        for (int i = 0; i < dv; ++i) {                                     /* o = S q */
+            const double *Si = S + (size_t)i * dk;
+            double acc = 0.0;
+            for (int j = 0; j < dk; ++j) acc += Si[j] * qt[j];
+            ot[i] = acc;
+        }
+    }
+    if (J->S_final) memcpy(J->S_final + sh, S, sizeof(double) * (size_t)dv * dk);
+    free(S); free(x); free(e);
+    return 0;
+}
+
+/* One QED stream (b, h).  S is held K x V here (S[c*dv + j], c over keys). */
+static int qed_stream(const job_t *J, int b, int h)
+{
+    const int T = J->T, H = J->H, K = J->dk, V = J->dv;
+    double *S = malloc(sizeof(double) * (size_t)K * V);
+    double *u = malloc(sizeof(double) * (size_t)K);
+    double *a = malloc(sizeof(double) * (size_t)K);
+    double *r = malloc(sizeof(double) * (size_t)V);
+    if (!S || !u || !a || !r) { free(S); free(u); free(a); free(r); return 1; }
+    const size_t sh = ((size_t)b * H + h) * K * V;
+    for (int c = 0; c < K; ++c)                   /* stored [V][K] = S^T -> S[c][j] */
+        for (int j = 0; j < V; ++j)
+            S[(size_t)c * V + j] = J->S0 ? J->S0[sh + (size_t)j * K + c] : 0.0;
+    const double lam_h = J->lam_h[h];
+
+    for (int t = 0; t < T; ++t) {
+        const size_t tok = ((size_t)b * T + t) * H + h;
+        const double *qt = J->q + tok * K, *kt = J->k + tok * K, *vt = J->v + tok * V;
+        const double *gt = J->g + tok * K, *bt = J->bgate + tok * K, *wt = J->w + tok * V;
+        double *ot = J->o + tok * V;
+
+        for (int c = 0; c < K; ++c) {                                      /* Sbar = Diag(exp g) S */
+            const double dc = exp(gt[c]);
+            double *Sc = S + (size_t)c * V;
+            for (int j = 0; j < V; ++j) Sc[j] *= dc;
+        }
+        double ku = 0.0;
+        for (int c = 0; c < K; ++c) { u[c] = bt[c] * qt[c]; ku += kt[c] * u[c]; }  /* u = b*q, k^T u */
+        for (int c = 0; c < K; ++c) {
+            const double d = u[c] - kt[c] * ku;                            /* d = u - k (k^T u) */
+            a[c] = bt[c] * kt[c] + lam_h * d;                              /* a = b*k + lambda_h d */
+        }
+        for (int j = 0; j < V; ++j) {                                      /* r = w*v - Sbar^T a */
+            double acc = 0.0;
+            for (int c = 0; c < K; ++c) acc += S[(size_t)c * V + j] * a[c];
+            r[j] = wt[j] * vt[j] - acc;
+        }
+        for (int c = 0; c < K; ++c) {                                      /* S = Sbar + k r^T */
+            double *Sc = S + (size_t)c * V;
+            for (int j = 0; j < V; ++j) Sc[j] += kt[c] * r[j];
+        }
+        for (int j = 0; j < V; ++j) {                                      /* o = S^T q */
+            double acc = 0.0;
+            for (int c = 0; c < K; ++c) acc += S[(size_t)c * V + j] * qt[c];
+            ot[j] = acc;
+        }
+    }
+    if (J->S_final)
+        for (int c = 0; c < K; ++c)
+            for (int j = 0; j < V; ++j)
+                J->S_final[sh + (size_t)j * K + c] = S[(size_t)c * V + j];
+    free(S); free(u); free(a); free(r);
+    return 0;
+}
+
+static void *worker(void *arg)
+{
+    job_t *J = (job_t *)arg;
+    const int n = J->B * J->H;
+    for (int s = J->first; s < n; s += J->stride) {
+        const int b = s / J->H, h = s % J->H;
+        int rc = J->method == 0 ? qdelta_stream(J, b, h) : qed_stream(J, b, h);
+        if (rc) J->status = rc;
+    }
+    return NULL;
+}
+
+/* Runs the streams of one call over `nthreads` threads (<= 0: all cores). */
+static int run(job_t *proto, int nthreads)
+{
+    const int n = proto->B * proto->H;
+    if (n <= 0 || proto->T < 0) return 0;
+    if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > n) nthreads = n;
+    job_t *jobs = calloc((size_t)nthreads, sizeof(job_t));
+    pthread_t *th = calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !th) { free(jobs); free(th); return 1; }
+    int status = 0;
+    for (int i = 0; i < nthreads; ++i) {
+        jobs[i] = *proto;
+        jobs[i].first = i;
+        jobs[i].stride = nthreads;
+        jobs[i].status = 0;
+        if (i > 0 && pthread_create(&th[i], NULL, worker, &jobs[i]) != 0) {
+            worker(&jobs[i]);          /* could not spawn: run inline */
+            th[i] = 0;
+        }
+    }
+    worker(&jobs[0]);
+    for (int i = 1; i < nthreads; ++i)
+        if (th[i]) pthread_join(th[i], NULL);
+    for (int i = 0; i < nthreads; ++i)
+        if (jobs[i].status) status = jobs[i].status;
+    free(jobs); free(th);
+    return status;
+}
+
+/* Q-Delta forward.  alpha, lam, S0, S_final may be NULL.  Returns 0 on success. */
+int oracle_qdelta_fwd(int B, int T, int H, int dk, int dv,
+                      const double *q, const double *k, const double *v,
+                      const double *alpha, const double *beta, const double *lam,
+                      const double *S0, double *o, double *S_final, int nthreads)
+{
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.B = B; J.T = T; J.H = H; J.dk = dk; J.dv = dv;
+    J.q = q; J.k = k; J.v = v; J.alpha = alpha; J.beta = beta; J.lam = lam;
+    J.S0 = S0; J.o = o; J.S_final = S_final; J.method = 0;
+    return run(&J, nthreads);
+}
+
+/* QED forward over GDN-2.  S0, S_final may be NULL; stored as [B][H][dv][dk]. */
+int oracle_qed_fwd(int B, int T, int H, int dk, int dv,
+                   const double *q, const double *k, const double *v,
+                   const double *g, const double *b, const double *w, const double *lam_h,
+                   const double *S0, double *o, double *S_final, int nthreads)
+{
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.B = B; J.T = T; J.H = H; J.dk = dk; J.dv = dv;
+    J.q = q; J.k = k; J.v = v; J.g = g; J.bgate = b; J.w = w; J.lam_h = lam_h;
+    J.S0 = S0; J.o = o; J.S_final = S_final; J.method = 1;
+    return run(&J, nthreads);
+}
+
+/* One Q-Delta decode step for N sequences x H heads: S [N][H][dv][dk] updated in
+ * place, tokens [N][H][d], gates [N][H] (alpha, lam may be NULL), o [N][H][dv].
+ * It is the T = 1 case of the forward, with the state carried in and out. */
+int oracle_qdelta_step(int N, int H, int dk, int dv, double *S,
+                       const double *q, const double *k, const double *v,
+                       const double *alpha, const double *beta, const double *lam,
+                       double *o, int nthreads)
+{
+    return oracle_qdelta_fwd(N, 1, H, dk, dv, q, k, v, alpha, beta, lam, S, o, S, nthreads);
+}

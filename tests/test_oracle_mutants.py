@@ -1,0 +1,134 @@
+"""The pins are discriminative: plausible mistakes in a recurrence fail them.
+
+Each mutant is a one-step recurrence with one planted mistake (CPU only, never
+the GPU path).  The same pin predicates that the oracle passes must reject every
+mutant, so a mistake of that kind in the oracle could not go unnoticed.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+rng = np.random.default_rng(99)
+
+
+def _unit(x):
+    return x / np.linalg.norm(x)
+
+
+def oracle_qdelta_step(Sp, q, k, v, al, be, lm):
+    sh = lambda x: np.asarray(x, dtype=np.float64).reshape(1, 1, 1, -1)
+    g = lambda x: np.array([[[x]]])
+    o, S = oracle.qdelta_fwd(sh(q), sh(k), sh(v), g(al), g(be), g(lm), Sp[None, None])
+    return S[0, 0], o[0, 0, 0]
+
+
+def _qdelta_mutant(kind):
+    def step(Sp, q, k, v, al, be, lm):
+        x = k + lm * q
+        Sb = al * Sp
+        if kind == "normalised_residual":
+            e = (v - Sb @ x) / (1 + lm)
+        elif kind == "decay_after_error":
+            e = v - Sp @ x
+        elif kind == "lambda_sign":
+            e = v - Sb @ (k - lm * q)
+        else:
+            e = v - Sb @ x
+        w = x if kind == "write_along_x" else k
+        S = Sb + be * np.outer(e, w)
+        o = Sb @ q if kind == "output_before_update" else S @ q
+        return S, o
+    return step
+
+
+def qdelta_pins_hold(step):
+    """Gated error identity and closed-form output (Q-Delta notes sec. 2.4, 2.7)."""
+    dk, dv = 6, 5
+    for _ in range(5):
+        q, k = _unit(rng.standard_normal(dk)), _unit(rng.standard_normal(dk))
+        v = rng.standard_normal(dv)
+        al, be, lm = rng.uniform(0.8, 0.99), rng.uniform(0.1, 0.9), rng.uniform(0.1, 0.9)
+        Sp = rng.standard_normal((dv, dk))
+        S, o = step(Sp, q, k, v, al, be, lm)
+        x = k + lm * q
+        ok1 = np.allclose(v - S @ x, (1 - be * (k @ x)) * (v - al * Sp @ x), atol=1e-10)
+        ok2 = np.allclose(o, al * Sp @ q + be * (v - al * Sp @ x) * (k @ q), atol=1e-10)
+        if not (ok1 and ok2):
+            return False
+    return True
+
+
+def test_oracle_passes_qdelta_pins():
+    assert qdelta_pins_hold(oracle_qdelta_step)
+
+
+@pytest.mark.parametrize("kind", ["normalised_residual", "decay_after_error", "lambda_sign",
+                                  "write_along_x", "output_before_update"])
+def test_qdelta_mutant_rejected(kind):
+    assert not qdelta_pins_hold(_qdelta_mutant(kind))
+
+
+def oracle_qed_step(Sbar, q, k, b, w, v, lam):
+    K, V = Sbar.shape
+    sh = lambda x: np.asarray(x, dtype=np.float64).reshape(1, 1, 1, -1)
+    o, S = oracle.qed_fwd(sh(q), sh(k), sh(v), sh(np.zeros(K)), sh(b), sh(w), np.array([lam]),
+                          Sbar.T.reshape(1, 1, V, K))
+    return S[0, 0].T, o[0, 0, 0]
+
+
+def _qed_mutant(kind):
+    def step(Sbar, q, k, b, w, v, lam):
+        if kind == "no_projection":
+            d = b * q
+        elif kind == "project_then_gate":
+            d = b * (q - k * (k @ q))
+        elif kind == "ungated_query":
+            d = q - k * (k @ q)
+        else:
+            u = b * q
+            d = u - k * (k @ u)
+        a = b * k + lam * d
+        if kind == "lambda_on_base":
+            a = lam * b * k + d
+        r = w * v - Sbar.T @ a
+        S = Sbar + np.outer(k, r)
+        return S, S.T @ q
+    return step
+
+
+def qed_pins_hold(step):
+    """Printed 2-D example and Eqs. 11-12 (QED notes sec. 2.3-2.4)."""
+    ex = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "qed_2d_example.json")))
+    i, e = ex["inputs"], ex["expected"]
+    S, o = step(np.array(i["S_bar_KxV"]), np.array(i["q"]), np.array(i["k"]), np.array(i["b"]),
+                np.ones(1), np.array([i["w_times_v"]]), i["lambda_h"])
+    if abs(o - e["o_qed"]) > 1e-12:
+        return False
+    K, V = 6, 4
+    for _ in range(3):
+        q, k = _unit(rng.standard_normal(K)), _unit(rng.standard_normal(K))
+        b, w = rng.uniform(0.1, 0.9, K), rng.uniform(0.1, 0.9, V)
+        v, Sbar, lam = rng.standard_normal(V), rng.standard_normal((K, V)), 0.45
+        Sq, oq = step(Sbar, q, k, b, w, v, lam)
+        Sg, og = step(Sbar, q, k, b, w, v, 0.0)
+        u = b * q
+        d = u - k * (k @ u)
+        if not np.allclose(Sq - Sg, -lam * np.outer(k, Sbar.T @ d), atol=1e-10):
+            return False
+        if not np.allclose(oq - og, -lam * (q @ k) * (Sbar.T @ d), atol=1e-10):
+            return False
+    return True
+
+
+def test_oracle_passes_qed_pins():
+    assert qed_pins_hold(oracle_qed_step)
+
+
+@pytest.mark.parametrize("kind", ["no_projection", "project_then_gate", "ungated_query",
+                                  "lambda_on_base"])
+def test_qed_mutant_rejected(kind):
+    assert not qed_pins_hold(_qed_mutant(kind))

@@ -1,0 +1,383 @@
+"""Pins of the fp64 oracle to what the pages and the mathematics fix.
+
+None of these re-types the oracle's own update: each checks it against a
+printed worked example, a closed form or identity derived on the pages, a
+special case that reduces to another page's formulation, an invariant, or a
+brute-force expansion by explicit transition-matrix products.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(12345)
+
+
+def _unit(x):
+    return x / np.linalg.norm(x, axis=-1, keepdims=True)
+
+
+def _rand_qdelta(B, T, H, dk, dv, gated=True, lam=True, s0=True, unit=True):
+    q = rng.standard_normal((B, T, H, dk))
+    k = rng.standard_normal((B, T, H, dk))
+    if unit:
+        q, k = _unit(q), _unit(k)
+    v = rng.standard_normal((B, T, H, dv))
+    beta = rng.uniform(0.05, 1.0, (B, T, H))
+    alpha = rng.uniform(0.8, 1.0, (B, T, H)) if gated else None
+    lm = rng.uniform(0.0, 1.0, (B, T, H)) if lam else None
+    S0 = rng.standard_normal((B, H, dv, dk)) * 0.3 if s0 else None
+    return q, k, v, alpha, beta, lm, S0
+
+
+def _states_per_step(q, k, v, alpha, beta, lam, S0):
+    """S_0..S_T for a single stream (B=H=1) by carrying the oracle's state."""
+    T = q.shape[1]
+    dk, dv = q.shape[-1], v.shape[-1]
+    S = np.zeros((1, 1, dv, dk)) if S0 is None else S0.copy()
+    states, outs = [S[0, 0].copy()], []
+    for t in range(T):
+        sl = slice(t, t + 1)
+        o, S = oracle.qdelta_fwd(q[:, sl], k[:, sl], v[:, sl],
+                                 None if alpha is None else alpha[:, sl], beta[:, sl],
+                                 None if lam is None else lam[:, sl], S)
+        states.append(S[0, 0].copy())
+        outs.append(o[0, 0, 0])
+    return states, outs
+
+
+# ---------------------------------------------------------------- QED (page 3)
+
+def _qed_one_step(k, q, b, Sbar_KxV, w, v, lam_h, g=None):
+    """One oracle QED step with S0 = Sbar (g = 0 unless given). Returns (S_KxV, o)."""
+    K, V = Sbar_KxV.shape
+    sh = lambda x: np.asarray(x, dtype=np.float64).reshape(1, 1, 1, -1)
+    g = np.zeros(K) if g is None else g
+    S0 = Sbar_KxV.T.reshape(1, 1, V, K)
+    o, S = oracle.qed_fwd(sh(q), sh(k), sh(v), sh(g), sh(b), sh(w), np.array([lam_h]), S0)
+    return S[0, 0].T, o[0, 0, 0]
+
+
+def test_qed_worked_example_2d():
+    """QED notes, sec. 2.4: the printed 2-D example, exactly."""
+    ex = json.load(open(os.path.join(GOLDEN, "qed_2d_example.json")))
+    i, e = ex["inputs"], ex["expected"]
+    Sbar = np.array(i["S_bar_KxV"])
+    S, o = _qed_one_step(i["k"], i["q"], i["b"], Sbar, [1.0], [i["w_times_v"]], i["lambda_h"])
+    np.testing.assert_allclose(S, np.array(e["S_qed_KxV"]), rtol=0, atol=1e-14)
+    assert abs(o - e["o_qed"]) < 1e-14
+    np.testing.assert_allclose(S - Sbar, np.array(e["delta_S_KxV"]), atol=1e-14)
+    S2, o2 = _qed_one_step(i["k"], i["q"], i["b"], Sbar, [1.0], [i["w_times_v"]], 0.0)
+    assert abs(o2 - e["o_gdn2"]) < 1e-14
+    np.testing.assert_allclose(S2, Sbar, atol=1e-14)   # baseline residual is exactly zero
+    assert abs((o2 - o) - e["o_difference"]) < 1e-14
+    # the printed decomposition 0.144 = lambda * rho * (Sbar^T d)
+    rho = float(np.dot(i["q"], i["k"]))
+    assert abs(i["lambda_h"] * rho * e["S_bar_T_d"] - e["o_difference"]) < 1e-14
+
+
+def _erase_factor(k, q, b, lam_h, g=None):
+    """M = I - k a^T read off the oracle: v = 0 and S0 = I (V = K) give S_1 = M Sbar."""
+    K = len(k)
+    S, _ = _qed_one_step(k, q, b, np.eye(K), np.ones(K), np.zeros(K), lam_h, g)
+    return S
+
+
+def test_qed_erase_factor_counterexample():
+    """QED notes, sec. 2.5: M = [[0.5,-0.1],[0,1]], spec {0.5, 1}, |M e2|^2 = 1.01."""
+    ex = json.load(open(os.path.join(GOLDEN, "qed_erase_factor.json")))
+    i, e = ex["inputs"], ex["expected"]
+    M = _erase_factor(i["k"], i["q"], i["b"], i["lambda_h"])
+    np.testing.assert_allclose(M, np.array(e["M"]), atol=1e-15)
+    np.testing.assert_allclose(np.sort(np.linalg.eigvals(M).real), e["spectrum"], atol=1e-14)
+    assert abs(np.sum((M @ np.array([0.0, 1.0])) ** 2) - e["norm_M_e2_squared"]) < 1e-14
+
+
+@pytest.mark.parametrize("lam_h", [0.0, 0.3, 1.0, 2.5])
+def test_qed_erase_spectrum_independent_of_lambda(lam_h):
+    """QED notes, sec. 2.5: M has K-1 unit eigenvalues and 1 - sum_i b_i k_i^2,
+    whatever lambda_h (d is orthogonal to k)."""
+    K = 8
+    k = _unit(rng.standard_normal(K))
+    q = _unit(rng.standard_normal(K))
+    b = rng.uniform(0.05, 0.95, K)
+    M = _erase_factor(k, q, b, lam_h)
+    ev = np.sort(np.linalg.eigvals(M).real)
+    expect = np.sort(np.r_[np.ones(K - 1), 1.0 - np.sum(b * k * k)])
+    np.testing.assert_allclose(ev, expect, atol=1e-10)
+
+
+def test_qed_difference_identities_and_gdn2():
+    """QED notes, sec. 2.3, Eqs. 11-12: against GDN-2 on the same Sbar,
+    S_QED - S_GDN2 = -lambda k (Sbar^T d)^T and o_QED - o_GDN2 = -lambda rho Sbar^T d,
+    with per-channel decay in play; lambda_h = 0 is the GDN-2 update of Eqs. 4/8."""
+    K, V = 6, 5
+    k = _unit(rng.standard_normal(K))
+    q = _unit(rng.standard_normal(K))
+    b = rng.uniform(0.05, 0.95, K)
+    w = rng.uniform(0.05, 0.95, V)
+    v = rng.standard_normal(V)
+    g = -rng.uniform(0.0, 0.5, K)
+    S_prev = rng.standard_normal((K, V))
+    lam = 0.37
+    S_q, o_q = _qed_one_step(k, q, b, S_prev, w, v, lam, g)
+    S_g, o_g = _qed_one_step(k, q, b, S_prev, w, v, 0.0, g)
+    Sbar = np.exp(g)[:, None] * S_prev
+    # GDN-2 written from its own equations (the base erase vector b*k)
+    r_base = w * v - Sbar.T @ (b * k)
+    np.testing.assert_allclose(S_g, Sbar + np.outer(k, r_base), atol=1e-13)
+    u = b * q
+    d = u - k * np.dot(k, u)
+    assert abs(np.dot(d, k)) < 1e-14                       # d is orthogonal to k
+    np.testing.assert_allclose(S_q - S_g, -lam * np.outer(k, Sbar.T @ d), atol=1e-13)
+    np.testing.assert_allclose(o_q - o_g, -lam * np.dot(q, k) * (Sbar.T @ d), atol=1e-13)
+
+
+def test_qed_key_orthogonal_response_and_gdn2_decomposition():
+    """QED notes, sec. 2.3: Eq. 9 (a probe x orthogonal to k sees no change:
+    S_t^T x = Sbar^T x) and Eq. 10 (GDN-2 output split along k and q_perp)."""
+    K, V = 7, 4
+    k = _unit(rng.standard_normal(K))
+    q = _unit(rng.standard_normal(K))
+    b = rng.uniform(0.05, 0.95, K)
+    w = rng.uniform(0.05, 0.95, V)
+    v = rng.standard_normal(V)
+    S_prev = rng.standard_normal((K, V))
+    for lam in (0.0, 0.8):
+        S, o = _qed_one_step(k, q, b, S_prev, w, v, lam)
+        x = rng.standard_normal(K)
+        x -= k * np.dot(k, x)
+        np.testing.assert_allclose(S.T @ x, S_prev.T @ x, atol=1e-13)
+    S, o = _qed_one_step(k, q, b, S_prev, w, v, 0.0)
+    rho = np.dot(q, k)
+    q_perp = q - rho * k
+    expect = rho * (w * v + S_prev.T @ ((1.0 - b) * k)) + S_prev.T @ q_perp
+    np.testing.assert_allclose(o, expect, atol=1e-13)
+
+
+def test_qed_decay_only():
+    """With v = 0 and b = 0 (nothing erased, nothing written), each key row of the
+    state decays by exp(sum of its g) and o = S^T q."""
+    K, V, T = 5, 3, 6
+    S0 = rng.standard_normal((1, 1, V, K))
+    g = -rng.uniform(0, 0.3, (1, T, 1, K))
+    q = rng.standard_normal((1, T, 1, K))
+    k = _unit(rng.standard_normal((1, T, 1, K)))
+    z = np.zeros((1, T, 1, K))
+    o, S = oracle.qed_fwd(q, k, np.zeros((1, T, 1, V)), g, z, np.ones((1, T, 1, V)),
+                          np.array([0.7]), S0)
+    np.testing.assert_allclose(S[0, 0], S0[0, 0] * np.exp(g.sum(axis=1))[0, 0][None, :], atol=1e-14)
+
+
+# ------------------------------------------------------------ Q-Delta (page 1)
+
+def test_deltanet_special_case():
+    """lambda = 0, alpha = 1 is DeltaNet: compared with the DeltaNet notes' own
+    read / blend / replace form (sec. 2.5): v_old = S k, v_new = beta v + (1-beta) v_old,
+    S <- S - v_old k^T + v_new k^T."""
+    q, k, v, _, beta, _, S0 = _rand_qdelta(1, 12, 1, 6, 5, gated=False, lam=False)
+    o, S = oracle.qdelta_fwd(q, k, v, None, beta, None, S0)
+    St = S0[0, 0].copy()
+    for t in range(12):
+        kt, vt, bt = k[0, t, 0], v[0, t, 0], beta[0, t, 0]
+        v_old = St @ kt
+        v_new = bt * vt + (1 - bt) * v_old
+        St = St - np.outer(v_old, kt) + np.outer(v_new, kt)
+        np.testing.assert_allclose(o[0, t, 0], St @ q[0, t, 0], atol=1e-12)
+    np.testing.assert_allclose(S[0, 0], St, atol=1e-12)
+
+
+def test_gated_deltanet_special_case():
+    """lambda = 0 is Gated DeltaNet: S_t = S_{t-1} alpha_t (I - beta_t k k^T) + beta_t v k^T
+    (DeltaNet notes sec. 6.2), as explicit matrix products."""
+    q, k, v, alpha, beta, _, S0 = _rand_qdelta(1, 10, 1, 5, 4, lam=False)
+    o, S = oracle.qdelta_fwd(q, k, v, alpha, beta, None, S0)
+    St = S0[0, 0].copy()
+    I = np.eye(5)
+    for t in range(10):
+        kt, vt = k[0, t, 0], v[0, t, 0]
+        St = St @ (alpha[0, t, 0] * (I - beta[0, t, 0] * np.outer(kt, kt))) + beta[0, t, 0] * np.outer(vt, kt)
+        np.testing.assert_allclose(o[0, t, 0], St @ q[0, t, 0], atol=1e-12)
+    np.testing.assert_allclose(S[0, 0], St, atol=1e-12)
+
+
+def test_beta_zero_pure_decay():
+    """beta = 0: nothing is written, S_T = (prod alpha) S_0 and o_t = gamma_t S_0 q_t."""
+    q, k, v, alpha, beta, lam, S0 = _rand_qdelta(2, 9, 3, 6, 4)
+    beta = np.zeros_like(beta)
+    o, S = oracle.qdelta_fwd(q, k, v, alpha, beta, lam, S0)
+    gam = np.cumprod(alpha, axis=1)                      # [B,T,H]
+    np.testing.assert_allclose(S, S0 * gam[:, -1][:, :, None, None], atol=1e-13)
+    expect = np.einsum("bth,bhij,bthj->bthi", gam, S0, q)
+    np.testing.assert_allclose(o, expect, atol=1e-13)
+    o0, S00 = oracle.qdelta_fwd(q, k, v, alpha, beta, lam, None)
+    assert np.all(o0 == 0) and np.all(S00 == 0)          # beta = 0 from S_0 = 0 stays 0
+
+
+def test_exact_retrieval_orthonormal_keys():
+    """beta = 1, alpha = 1, lambda = 0 with orthonormal keys: S k_j = v_j for every
+    key written (DeltaNet notes sec. 2.5: beta = 1 replaces the value)."""
+    d, dv = 8, 5
+    Qm, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    k = Qm.T.reshape(1, d, 1, d)
+    v = rng.standard_normal((1, d, 1, dv))
+    q = _unit(rng.standard_normal((1, d, 1, d)))
+    beta = np.ones((1, d, 1))
+    S0 = rng.standard_normal((1, 1, dv, d))
+    _, S = oracle.qdelta_fwd(q, k, v, None, beta, None, S0)
+    np.testing.assert_allclose(S[0, 0] @ k[0, :, 0].T, v[0, :, 0].T, atol=1e-12)
+
+
+def test_exact_write_beta_inverse_norm():
+    """DeltaNet notes sec. 2.6: with beta = 1/|k|^2 one step gives S_t k_t = v_t."""
+    d, dv = 6, 4
+    k = rng.standard_normal((1, 1, 1, d)) * 1.7
+    v = rng.standard_normal((1, 1, 1, dv))
+    q = rng.standard_normal((1, 1, 1, d))
+    beta = np.array([[[1.0 / np.sum(k ** 2)]]])
+    _, S = oracle.qdelta_fwd(q, k, v, None, beta, None, rng.standard_normal((1, 1, dv, d)))
+    np.testing.assert_allclose(S[0, 0] @ k[0, 0, 0], v[0, 0, 0], atol=1e-12)
+
+
+def test_deltanet_transition_eigenvalues():
+    """DeltaNet notes sec. 3.8: I - beta k k^T has eigenvalue 1 (d-1 times) and
+    1 - beta |k|^2.  Read off the oracle with v = 0 and S_0 = I."""
+    d = 6
+    k = rng.standard_normal((1, 1, 1, d))
+    beta = np.array([[[0.6]]])
+    _, S = oracle.qdelta_fwd(np.zeros((1, 1, 1, d)), k, np.zeros((1, 1, 1, d)), None, beta,
+                             None, np.eye(d).reshape(1, 1, d, d))
+    ev = np.sort(np.linalg.eigvals(S[0, 0]).real)
+    expect = np.sort(np.r_[np.ones(d - 1), 1 - 0.6 * np.sum(k ** 2)])
+    np.testing.assert_allclose(ev, expect, atol=1e-12)
+
+
+def _value_mixture(q, k, v, alpha, beta, lam, S0):
+    """Q-Delta notes sec. 2.2 (Eqs. 8-15): for S_t = S_{t-1} P_t + eta_t v_t k_t^T,
+    S_t = S_0 P_1..P_t + sum_tau v_tau b_{tau,t}^T with b_{tau,t} = P_t^T b_{tau,t-1},
+    b_{tau,tau} = eta_tau k_tau.  Here P_t = alpha_t (I - beta_t x_t k_t^T), eta = beta."""
+    T, dk = q.shape[1], q.shape[-1]
+    I = np.eye(dk)
+    P = []
+    for t in range(T):
+        x = k[0, t, 0] + lam[0, t, 0] * q[0, t, 0]
+        P.append(alpha[0, t, 0] * (I - beta[0, t, 0] * np.outer(x, k[0, t, 0])))
+    outs, S_list = [], []
+    for t in range(T):
+        prod = I.copy()
+        for j in range(t + 1):
+            prod = prod @ P[j]
+        St = S0[0, 0] @ prod
+        for tau in range(t + 1):
+            bvec = beta[0, tau, 0] * k[0, tau, 0]
+            for j in range(tau + 1, t + 1):
+                bvec = P[j].T @ bvec
+            St = St + np.outer(v[0, tau, 0], bvec)
+        S_list.append(St)
+        outs.append(St @ q[0, t, 0])
+    return outs, S_list
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 8])
+def test_value_mixture_bruteforce(T):
+    q, k, v, alpha, beta, lam, S0 = _rand_qdelta(1, T, 1, 5, 4)
+    o, S = oracle.qdelta_fwd(q, k, v, alpha, beta, lam, S0)
+    outs, S_list = _value_mixture(q, k, v, alpha, beta, lam, S0)
+    for t in range(T):
+        np.testing.assert_allclose(o[0, t, 0], outs[t], atol=1e-12)
+    np.testing.assert_allclose(S[0, 0], S_list[-1], atol=1e-12)
+
+
+def test_gated_error_identity_and_closed_form_output():
+    """Q-Delta notes sec. 2.7 (gated): v_t - S_t x_t = (1 - beta_t a_t)(v_t - alpha_t S_{t-1} x_t),
+    a_t = k_t^T x_t; sec. 2.4: o_t = alpha S_{t-1} q + beta (v - alpha S_{t-1} x)(k^T q)."""
+    q, k, v, alpha, beta, lam, S0 = _rand_qdelta(1, 10, 1, 6, 5)
+    states, outs = _states_per_step(q, k, v, alpha, beta, lam, S0)
+    for t in range(10):
+        qt, kt, vt = q[0, t, 0], k[0, t, 0], v[0, t, 0]
+        al, be, lm = alpha[0, t, 0], beta[0, t, 0], lam[0, t, 0]
+        x = kt + lm * qt
+        Sp, S = states[t], states[t + 1]
+        a = kt @ x
+        np.testing.assert_allclose(vt - S @ x, (1 - be * a) * (vt - al * Sp @ x), atol=1e-12)
+        o_cf = al * Sp @ qt + be * (vt - al * Sp @ x) * (kt @ qt)
+        np.testing.assert_allclose(outs[t], o_cf, atol=1e-12)
+
+
+def test_lemma31_ungated_contraction():
+    """Q-Delta notes sec. 2.7, Lemma 3.1 (alpha = 1): e_t = (1 - beta_t a_t) e~_t with
+    e~_t = v_t - S_{t-1} x_t; for unit q, k also 1 - lambda <= a_t <= 1 + lambda."""
+    q, k, v, _, beta, lam, S0 = _rand_qdelta(1, 10, 1, 6, 5, gated=False)
+    states, _ = _states_per_step(q, k, v, None, beta, lam, S0)
+    for t in range(10):
+        x = k[0, t, 0] + lam[0, t, 0] * q[0, t, 0]
+        a = k[0, t, 0] @ x
+        e_tilde = v[0, t, 0] - states[t] @ x
+        e = v[0, t, 0] - states[t + 1] @ x
+        np.testing.assert_allclose(e, (1 - beta[0, t, 0] * a) * e_tilde, atol=1e-12)
+        assert 1 - lam[0, t, 0] - 1e-12 <= a <= 1 + lam[0, t, 0] + 1e-12
+
+
+def test_online_surrogate_minimiser():
+    """Q-Delta notes sec. 2.5 (Table 1): the minimiser of
+    J(S) = |S - alpha S_{t-1}|_F^2 - 2 beta <S k, delta>, delta = v - alpha S_{t-1} x,
+    found by a generic least-squares solve of the quadratic, is the oracle's step."""
+    dk, dv = 4, 3
+    q, k, v, alpha, beta, lam, S0 = _rand_qdelta(1, 1, 1, dk, dv)
+    _, S1 = oracle.qdelta_fwd(q, k, v, alpha, beta, lam, S0)
+    Sp = S0[0, 0]
+    al, be = alpha[0, 0, 0], beta[0, 0, 0]
+    x = k[0, 0, 0] + lam[0, 0, 0] * q[0, 0, 0]
+    delta = v[0, 0, 0] - al * Sp @ x
+    # J(s) = s^T s - 2 s^T (alpha vec(Sp)) - 2 beta s^T (delta kron k) + const  (s = vec(S), row-major)
+    # as least squares: min |s - c|^2 with c the stationary point of the linear terms
+    n = dv * dk
+    A = np.eye(n)
+    lin = al * Sp.reshape(-1) + be * np.array([delta[i] * k[0, 0, 0][j] for i in range(dv) for j in range(dk)])
+    s, *_ = np.linalg.lstsq(A, lin, rcond=None)
+    # independent check that s is the minimiser: J increases along random directions
+    J = lambda S: np.sum((S - al * Sp) ** 2) - 2 * be * np.dot(S @ k[0, 0, 0], delta)
+    Smin = s.reshape(dv, dk)
+    for _ in range(5):
+        D = rng.standard_normal((dv, dk)) * 1e-3
+        assert J(Smin + D) > J(Smin) and J(Smin - D) > J(Smin)
+    np.testing.assert_allclose(S1[0, 0], Smin, atol=1e-12)
+
+
+# -------------------------------------------------- equivalences of the oracle
+
+def test_step_equals_forward():
+    q, k, v, alpha, beta, lam, S0 = _rand_qdelta(3, 7, 2, 6, 5)
+    o, S = oracle.qdelta_fwd(q, k, v, alpha, beta, lam, S0)
+    St = S0.copy()
+    for t in range(7):
+        ot = oracle.qdelta_step(St, q[:, t], k[:, t], v[:, t], alpha[:, t], beta[:, t], lam[:, t])
+        np.testing.assert_allclose(ot, o[:, t], atol=1e-12)
+    np.testing.assert_allclose(St, S, atol=1e-12)
+
+
+@pytest.mark.parametrize("split", [1, 5, 11])
+def test_split_call_carries_state(split):
+    q, k, v, alpha, beta, lam, S0 = _rand_qdelta(2, 12, 2, 5, 4)
+    o, S = oracle.qdelta_fwd(q, k, v, alpha, beta, lam, S0)
+    a = slice(0, split)
+    b = slice(split, 12)
+    o1, S1 = oracle.qdelta_fwd(q[:, a], k[:, a], v[:, a], alpha[:, a], beta[:, a], lam[:, a], S0)
+    o2, S2 = oracle.qdelta_fwd(q[:, b], k[:, b], v[:, b], alpha[:, b], beta[:, b], lam[:, b], S1)
+    np.testing.assert_allclose(np.concatenate([o1, o2], axis=1), o, atol=1e-12)
+    np.testing.assert_allclose(S2, S, atol=1e-12)
+
+
+def test_heads_and_batches_independent_and_thread_count_invariant():
+    q, k, v, alpha, beta, lam, S0 = _rand_qdelta(3, 6, 4, 5, 3)
+    o, S = oracle.qdelta_fwd(q, k, v, alpha, beta, lam, S0, nthreads=1)
+    o4, S4 = oracle.qdelta_fwd(q, k, v, alpha, beta, lam, S0, nthreads=5)
+    assert np.array_equal(o, o4) and np.array_equal(S, S4)
+    b, h = 2, 1
+    sl = lambda x: x[b:b + 1, :, h:h + 1]
+    o1, S1 = oracle.qdelta_fwd(sl(q), sl(k), sl(v), sl(alpha), sl(beta), sl(lam), S0[b:b + 1, h:h + 1])
+    assert np.array_equal(o1[0, :, 0], o[b, :, h]) and np.array_equal(S1[0, 0], S[b, h])
