@@ -1,0 +1,421 @@
+"""Benchmark of the chunked Q-Delta forward on GB300 (one JSON line on rank 0).
+
+Workload of a step: one qdelta_fwd over one batch of the 1.3B-model layer shape,
+B=8, H=16, T=2048, dk=dv=128, bf16 inputs, fp32 state, full Q-Delta gates
+(alpha, beta, lambda), synthetic seeded inputs (synth.layer_1p3b).
+
+  value    tokens/s (B*T per step, summed over ranks) from CUDA events around
+           exactly K steps on the launching stream, inputs resident in HBM and
+           larger than L2, rotated over several buffer sets between steps
+  e2e      the same metric through the C ABI with pinned HOST buffers: every step
+           copies its inputs host->device and its outputs (o, S_final) back
+  roofline the dominant kernel against the measured HBM copy bandwidth
+  tensor   its GEMM work against the measured bf16 tensor peak
+  decode   qdelta_step on 512 sequences x 16 heads (fp32 128x128 state), GB/s
+  qed      qed_fwd at B=4, H=8, T=4096, d=128 bf16, tokens/s
+  cpu_baseline  the fp64 oracle timed on this host's cores on a bounded sample
+
+--impl reference times the oracle itself (the CPU reference of this build) on
+a bounded sample of the same workload each step, and prints the same line.
+Multi-GPU: replicas (each rank runs its own batch; no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "chunked Q-Delta fwd tokens/s at H=16,d=128,T=2048; % tensor peak; step GB/s"
+B, T, H, DK, DV, CHUNK = 8, 2048, 16, 128, 128, 64
+TOKEN_HEADS = B * T * H
+# algorithmic bytes of one forward: q, k, v, o in bf16 + alpha, beta, lambda in bf16
+# per token-head, + the fp32 final state
+BYTES_PER_TOKEN_HEAD = 2 * (DK + DK + DV + DV) + 3 * 2
+ALG_BYTES = TOKEN_HEADS * BYTES_PER_TOKEN_HEAD + B * H * DV * DK * 4
+# GEMM work per token-head at chunk C: Grams 4Cd + solve-apply 2Cd + intra output 2Cd
+# + the three state products 6 d^2  (= 8Cd + 6d^2 with d = dk = dv)
+FLOPS_PER_TOKEN_HEAD = 8 * CHUNK * DK + 6 * DK * DV
+ALG_FLOPS = TOKEN_HEADS * FLOPS_PER_TOKEN_HEAD
+N_BUFFERS = 3
+DOMINANT_KERNEL_SOURCES = ["delta_rule_linear_qdelta_gb300/csrc/chunk_simt.cu"]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def kernel_hash():
+    h = hashlib.sha256()
+    for rel in DOMINANT_KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile():
+    """DRAM bytes per launch from the committed ncu summary, if it matches the kernel."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    ent = d.get("qdelta_fwd_bf16_B8_H16_T2048_d128")
+    if not ent or ent.get("source_hash") != kernel_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled in the background."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        win = [s for t, s in self.samples if t0 - 0.15 <= t <= t1 + 0.15]
+        if not win:   # a timed region shorter than the sampling period: nearest samples
+            mid = 0.5 * (t0 + t1)
+            win = [min(self.samples, key=lambda ts: abs(ts[0] - mid))[1]]
+        sm = [float(s[1]) for s in win if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in win if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for s in win for n, v in zip(names, s[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(win)}
+
+
+def dist_setup(n_gpus):
+    import torch
+    if n_gpus > 1 or int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch.distributed as dist
+        rank = int(os.environ["RANK"])
+        local = int(os.environ.get("LOCAL_RANK", rank))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        return rank, int(os.environ["WORLD_SIZE"]), local
+    torch.cuda.set_device(0)
+    return 0, 1, 0
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def to_dev(x, dtype):
+    import torch
+    return None if x is None else torch.from_numpy(np.ascontiguousarray(x)).to("cuda", dtype)
+
+
+def make_buffers(n_sets, seed_base=1):
+    """n_sets independent input sets of the workload, resident on the device."""
+    import torch
+    sets = []
+    for i in range(n_sets):
+        d = synth.qdelta_inputs(B, T, H, DK, DV, seed=seed_base + 1000 * i, dtype="bf16", mode="qdelta")
+        sets.append({k: to_dev(d[k], torch.bfloat16) for k in ("q", "k", "v", "alpha", "beta", "lam")})
+    return sets
+
+
+def time_device(qd, sets, steps, warmup, world):
+    import torch
+    o = torch.empty(B, T, H, DV, dtype=torch.bfloat16, device="cuda")
+    S = torch.empty(B, H, DV, DK, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        s = sets[i % len(sets)]
+        qd.qdelta_fwd(s["q"], s["k"], s["v"], s["alpha"], s["beta"], s["lam"], None, o=o, S_final=S,
+                      stream=stream)
+        return qd.last_launch_count()
+
+    for i in range(warmup):
+        step(i)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    launches = 0
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        launches += step(warmup + i)
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier(world)
+    total_ms = start.elapsed_time(end)
+    per_launch_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    return total_ms, per_launch_ms, launches, (t_wall0, t_wall1)
+
+
+def time_e2e(qd, steps, warmup, world):
+    """Host buffers in pinned memory; each step copies inputs in and results out."""
+    import torch
+    d = synth.qdelta_inputs(B, T, H, DK, DV, seed=5, dtype="bf16", mode="qdelta")
+    host = {k: torch.from_numpy(d[k]).to(torch.bfloat16).pin_memory() for k in ("q", "k", "v", "alpha", "beta", "lam")}
+    devb = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
+    o = torch.empty(B, T, H, DV, dtype=torch.bfloat16, device="cuda")
+    S = torch.empty(B, H, DV, DK, dtype=torch.float32, device="cuda")
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    S_h = torch.empty(S.shape, dtype=S.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o.numel() * o.element_size() + S.numel() * S.element_size()
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for k in host:
+            devb[k].copy_(host[k], non_blocking=True)
+        qd.qdelta_fwd(devb["q"], devb["k"], devb["v"], devb["alpha"], devb["beta"], devb["lam"], None,
+                      o=o, S_final=S, stream=stream)
+        o_h.copy_(o, non_blocking=True)
+        S_h.copy_(S, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(start.elapsed_time(end) / steps, world)
+    return {"value": B * T * world / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+
+
+def time_decode(qd, steps=50, warmup=5, N=512):
+    import torch
+    d = synth.decode_inputs(N, 16, 128, 128, 4, seed=4, dtype="bf16", s0_var=None)
+    S = torch.empty(N, 16, 128, 128, dtype=torch.float32, device="cuda").normal_(0, 0.1)
+    tok = [{k: to_dev(d[k][i], torch.bfloat16) for k in ("q", "k", "v", "alpha", "beta", "lam")} for i in range(4)]
+    o = torch.empty(N, 16, 128, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        t = tok[i % 4]
+        qd.qdelta_step(S, t["q"], t["k"], t["v"], t["alpha"], t["beta"], t["lam"], o=o, stream=stream)
+
+    for i in range(warmup):
+        step(i)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(steps):
+        step(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    heads = N * 16
+    nbytes = heads * (2 * 128 * 128 * 4 + 2 * (128 + 128 + 128 + 128) + 3 * 2)
+    return {"workload": f"qdelta_step_bf16_N{N}_H16_d128", "ms_per_step": ms, "tokens_per_s": N / (ms * 1e-3),
+            "bytes_per_step": nbytes, "GBps": nbytes / (ms * 1e-3) / 1e9}
+
+
+def time_qed(qd, steps=20, warmup=3):
+    import torch
+    _, d = synth.qed_gdn2()
+    bf = torch.bfloat16
+    args = [to_dev(d[k], bf) for k in ("q", "k", "v", "g", "b", "w")] + [to_dev(d["lam_h"], torch.float32)]
+    o = torch.empty(4, 4096, 8, 128, dtype=bf, device="cuda")
+    S = torch.empty(4, 8, 128, 128, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        qd.qed_fwd(*args, o=o, S_final=S, stream=stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        qd.qed_fwd(*args, o=o, S_final=S, stream=stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    th = 4 * 4096 * 8
+    nbytes = th * (2 * (128 * 5 + 128)) + 4 * 8 * 128 * 128 * 4
+    return {"workload": "qed_bf16_B4_H8_T4096_d128", "ms_per_step": ms, "tokens_per_s": 4 * 4096 / (ms * 1e-3),
+            "GBps": nbytes / (ms * 1e-3) / 1e9,
+            "tensor_TFLOPs": th * FLOPS_PER_TOKEN_HEAD / (ms * 1e-3) / 1e12}
+
+
+def oracle_sample(n_streams, seed=1):
+    """Runs the fp64 oracle on the first n_streams (b, h) streams of the workload
+    (full T) on all host cores; returns (tokens/s equivalent, seconds, cores)."""
+    import oracle
+    d = synth.qdelta_inputs(1, T, n_streams, DK, DV, seed=seed, dtype="bf16", mode="qdelta")
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle.qdelta_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["lam"], None, nthreads=cores)
+    dt = time.perf_counter() - t0
+    return (n_streams * T / H) / dt, dt, min(cores, n_streams)
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    n_streams = 16
+    for _ in range(args.warmup):
+        oracle_sample(n_streams)
+    times = []
+    for _ in range(args.steps):
+        _, dt, cores = oracle_sample(n_streams)
+        times.append(dt)
+    sec = sum(times) / len(times)
+    value = (n_streams * T / H) / sec
+    sample = f"{n_streams} of {B * H} (b,h) streams at full T={T} per step (fp64, all host cores)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"qdelta_bf16_B{B}_H{H}_T{T}_d{DK}", "B": B, "T": T, "H": H, "dk": DK,
+                       "dv": DV, "chunk": CHUNK},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="skip the decode / QED / e2e / CPU legs")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    import delta_rule_linear_qdelta_gb300 as qd
+    if not os.path.exists(qd.LIB_PATH):
+        from delta_rule_linear_qdelta_gb300 import build
+        build.build()
+    rank, world, local = dist_setup(args.gpus)
+    hbm_peak, tc_peak, tc_sustained, peak_kind = load_peaks()
+
+    sets = make_buffers(N_BUFFERS, seed_base=1 + rank)
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    smi_index = int(vis.split(",")[local]) if vis and vis.split(",")[local].isdigit() else local
+    sampler = ClockSampler(smi_index)
+    sampler.start()
+    time.sleep(0.3)
+    total_ms, launch_ms, launches, (tw0, tw1) = time_device(qd, sets, args.steps, args.warmup, world)
+    sampler.stop()
+    clocks = sampler.summary(tw0, tw1)
+    ms_step = max_over_ranks(total_ms / args.steps, world)
+    value = B * T * world / (ms_step * 1e-3)
+    launch_ms = max_over_ranks(launch_ms, world)
+    achieved_gbs = ALG_BYTES / (launch_ms * 1e-3) / 1e9
+    achieved_tf = ALG_FLOPS / (launch_ms * 1e-3) / 1e12
+
+    extras = {}
+    if not args.no_extras:
+        extras["e2e"] = time_e2e(qd, max(3, min(args.steps, 20)), 3, world)
+        if rank == 0:
+            dec = time_decode(qd)
+            dec["frac_hbm"] = dec["GBps"] / hbm_peak
+            extras["decode"] = dec
+            extras["qed"] = time_qed(qd)
+    del sets
+    torch.cuda.synchronize()
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"qdelta_bf16_B{B}_H{H}_T{T}_d{DK}", "B": B, "T": T, "H": H, "dk": DK,
+                       "dv": DV, "chunk": CHUNK, "gates": "alpha,beta,lambda bf16",
+                       "l2": f"inputs > L2 (q,k,v 192 MiB per set), rotated over {N_BUFFERS} sets",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved_gbs / hbm_peak, "traffic": traffic_from_profile(),
+                         "peak_kind": peak_kind, "alg_bytes_per_launch": ALG_BYTES,
+                         "kernel_ms": launch_ms},
+            "tensor": {"achieved": achieved_tf, "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved_tf / tc_peak,
+                       "alg_flops_per_launch": ALG_FLOPS, "peak_kind": peak_kind},
+            "gpu_launches": launches,
+            "clocks": clocks}
+    if "e2e" in extras:
+        line["e2e"] = extras.pop("e2e")
+    line.update(extras)
+    if rank == 0 and not args.no_extras:
+        import oracle
+        oracle.build()
+        v, sec, cores = oracle_sample(32)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                "sample": f"32 of {B * H} (b,h) streams at full T={T} (fp64), {sec:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

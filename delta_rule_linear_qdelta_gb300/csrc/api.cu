@@ -1,0 +1,151 @@
+// The C ABI of include/qdelta.h: argument validation, kernel selection and
+// error reporting.  No allocation happens here; all buffers belong to the caller.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/qdelta.h"
+#include "qd_internal.cuh"
+
+namespace {
+
+thread_local char g_err[512] = "";
+thread_local int g_launches = 0;
+
+qd_status fail(qd_status s, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+qd_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(QD_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+bool head_dim_ok(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+// Common checks for the chunked forwards.  Returns QD_OK or an error with message.
+qd_status check_fwd(const char *fn, const void *const *req, int nreq, const void *const *opt, int nopt,
+                    int B, int T, int H, int dk, int dv, int chunk, qd_dtype dt) {
+    if (B < 0 || T < 0 || H < 0) return fail(QD_ERR_ARG, "%s: negative size B=%d T=%d H=%d", fn, B, T, H);
+    if (dt != QD_F32 && dt != QD_BF16) return fail(QD_ERR_UNSUPPORTED, "%s: unknown dtype %d", fn, (int)dt);
+    if (!head_dim_ok(dk) || !head_dim_ok(dv))
+        return fail(QD_ERR_UNSUPPORTED, "%s: head dims dk=%d dv=%d not in {16,32,64,128}", fn, dk, dv);
+    if (chunk != 64) return fail(QD_ERR_UNSUPPORTED, "%s: chunk=%d (only 64 is supported)", fn, chunk);
+    const double elems = (double)B * T * H * (dk > dv ? dk : dv);
+    if (elems > 9.0e15) return fail(QD_ERR_ARG, "%s: sizes overflow", fn);
+    if ((double)B * H > 2147483647.0) return fail(QD_ERR_ARG, "%s: B*H exceeds the grid limit", fn);
+    const bool empty = (B == 0 || H == 0 || T == 0);
+    for (int i = 0; i < nreq; ++i) {
+        if (!req[i] && !empty) return fail(QD_ERR_ARG, "%s: required pointer argument #%d is NULL", fn, i);
+        if (!aligned16(req[i])) return fail(QD_ERR_ARG, "%s: pointer argument #%d not 16-byte aligned", fn, i);
+    }
+    for (int i = 0; i < nopt; ++i)
+        if (!aligned16(opt[i])) return fail(QD_ERR_ARG, "%s: optional pointer #%d not 16-byte aligned", fn, i);
+    return QD_OK;
+}
+
+// T == 0: the final state is the initial state.
+qd_status empty_sequence(const float *S0, float *S_final, int B, int H, int dk, int dv, cudaStream_t s) {
+    if (!S_final || B == 0 || H == 0) return QD_OK;
+    const size_t bytes = (size_t)B * H * dk * dv * sizeof(float);
+    cudaError_t e = cudaSuccess;
+    if (!S0) e = cudaMemsetAsync(S_final, 0, bytes, s);
+    else if (S0 != S_final) e = cudaMemcpyAsync(S_final, S0, bytes, cudaMemcpyDeviceToDevice, s);
+    return e == cudaSuccess ? QD_OK : cuda_fail(e, "state copy for T=0");
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *qd_last_error(void) { return g_err; }
+
+int qd_last_launch_count(void) { return g_launches; }
+
+size_t qdelta_workspace_bytes(int, int, int, int, int, int, qd_dtype) { return 0; }
+
+size_t qed_workspace_bytes(int, int, int, int, int, int, qd_dtype) { return 0; }
+
+qd_status qdelta_fwd(const void *q, const void *k, const void *v, const void *alpha, const void *beta,
+                     const void *lam, const float *S0, void *o, float *S_final, int B, int T, int H,
+                     int dk, int dv, int chunk, qd_dtype dtype, void *workspace, size_t workspace_bytes,
+                     cudaStream_t stream) {
+    g_err[0] = 0;
+    const void *req[] = {q, k, v, beta, o};
+    const void *opt[] = {alpha, lam, S0, S_final, workspace};
+    qd_status st = check_fwd("qdelta_fwd", req, 5, opt, 5, B, T, H, dk, dv, chunk, dtype);
+    if (st != QD_OK) return st;
+    const size_t need = qdelta_workspace_bytes(B, T, H, dk, dv, chunk, dtype);
+    if (need && (!workspace || workspace_bytes < need))
+        return fail(QD_ERR_WORKSPACE, "qdelta_fwd: workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+    int n = 0;
+    if (B == 0 || H == 0) { g_launches = 0; return QD_OK; }
+    if (T == 0) { g_launches = 0; return empty_sequence(S0, S_final, B, H, dk, dv, stream); }
+    qd::QDeltaArgs a{q, k, v, alpha, beta, lam, S0, o, S_final, B, T, H, dk, dv, workspace, workspace_bytes};
+    cudaError_t e = qd::launch_qdelta_chunk_simt(a, dtype, stream, &n);
+    if (e != cudaSuccess) return cuda_fail(e, "qdelta_fwd launch");
+    g_launches = n;
+    return QD_OK;
+}
+
+qd_status qed_fwd(const void *q, const void *k, const void *v, const void *g, const void *b, const void *w,
+                  const float *lam_h, const float *S0, void *o, float *S_final, int B, int T, int H, int dk,
+                  int dv, int chunk, qd_dtype dtype, void *workspace, size_t workspace_bytes,
+                  cudaStream_t stream) {
+    g_err[0] = 0;
+    const void *req[] = {q, k, v, g, b, w, lam_h, o};
+    const void *opt[] = {S0, S_final, workspace};
+    qd_status st = check_fwd("qed_fwd", req, 8, opt, 3, B, T, H, dk, dv, chunk, dtype);
+    if (st != QD_OK) return st;
+    const size_t need = qed_workspace_bytes(B, T, H, dk, dv, chunk, dtype);
+    if (need && (!workspace || workspace_bytes < need))
+        return fail(QD_ERR_WORKSPACE, "qed_fwd: workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+    int n = 0;
+    if (B == 0 || H == 0) { g_launches = 0; return QD_OK; }
+    if (T == 0) { g_launches = 0; return empty_sequence(S0, S_final, B, H, dk, dv, stream); }
+    qd::QedArgs a{q, k, v, g, b, w, lam_h, S0, o, S_final, B, T, H, dk, dv, workspace, workspace_bytes};
+    cudaError_t e = qd::launch_qed_chunk_simt(a, dtype, stream, &n);
+    if (e != cudaSuccess) return cuda_fail(e, "qed_fwd launch");
+    g_launches = n;
+    return QD_OK;
+}
+
+qd_status qdelta_step(float *S, const void *q, const void *k, const void *v, const void *alpha,
+                      const void *beta, const void *lam, void *o, int N, int H, int dk, int dv,
+                      qd_dtype dtype, cudaStream_t stream) {
+    g_err[0] = 0;
+    if (N < 0 || H < 0) return fail(QD_ERR_ARG, "qdelta_step: negative size N=%d H=%d", N, H);
+    if (dtype != QD_F32 && dtype != QD_BF16) return fail(QD_ERR_UNSUPPORTED, "qdelta_step: unknown dtype");
+    if (!head_dim_ok(dk) || !head_dim_ok(dv))
+        return fail(QD_ERR_UNSUPPORTED, "qdelta_step: head dims dk=%d dv=%d not in {16,32,64,128}", dk, dv);
+    if ((double)N * H > 2147483647.0) return fail(QD_ERR_ARG, "qdelta_step: N*H exceeds the grid limit");
+    const bool empty = (N == 0 || H == 0);
+    const void *req[] = {S, q, k, v, beta, o};
+    for (int i = 0; i < 6; ++i) {
+        if (!req[i] && !empty) return fail(QD_ERR_ARG, "qdelta_step: required pointer argument #%d is NULL", i);
+        if (!aligned16(req[i])) return fail(QD_ERR_ARG, "qdelta_step: pointer argument #%d not 16-byte aligned", i);
+    }
+    if (!aligned16(alpha) || !aligned16(lam)) return fail(QD_ERR_ARG, "qdelta_step: gate pointer not 16-byte aligned");
+    g_launches = 0;
+    if (empty) return QD_OK;
+    int n = 0;
+    qd::StepArgs a{S, q, k, v, alpha, beta, lam, o, N, H, dk, dv};
+    cudaError_t e = qd::launch_qdelta_step(a, dtype, stream, &n);
+    if (e != cudaSuccess) return cuda_fail(e, "qdelta_step launch");
+    g_launches = n;
+    return QD_OK;
+}
+
+qd_status qd_device_status(cudaStream_t stream) {
+    g_err[0] = 0;
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "qd_device_status");
+    return QD_OK;
+}
+
+}  // extern "C"

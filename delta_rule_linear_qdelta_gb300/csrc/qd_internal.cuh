@@ -1,0 +1,59 @@
+// Internal declarations shared by the library's translation units (not part of
+// the C ABI).  Device helpers for dtype conversion and the launcher signatures.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qd {
+
+enum { kF32 = 0, kBF16 = 1 };
+
+template <typename T> __device__ __forceinline__ float to_f(T x);
+template <> __device__ __forceinline__ float to_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) {
+    return __bfloat162float(x);
+}
+template <typename T> __device__ __forceinline__ T from_f(float x);
+template <> __device__ __forceinline__ float from_f<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Arguments of one Q-Delta forward (layouts as in include/qdelta.h).
+struct QDeltaArgs {
+    const void *q, *k, *v, *alpha, *beta, *lam;
+    const float *S0;
+    void *o;
+    float *S_final;
+    int B, T, H, dk, dv;
+    void *ws;
+    size_t ws_bytes;
+};
+
+// Arguments of one QED forward.
+struct QedArgs {
+    const void *q, *k, *v, *g, *b, *w;
+    const float *lam_h, *S0;
+    void *o;
+    float *S_final;
+    int B, T, H, dk, dv;
+    void *ws;
+    size_t ws_bytes;
+};
+
+// Arguments of one decode step.
+struct StepArgs {
+    float *S;
+    const void *q, *k, *v, *alpha, *beta, *lam;
+    void *o;
+    int N, H, dk, dv;
+};
+
+// Launchers.  Each returns the first CUDA error and adds its launches to *nlaunch.
+cudaError_t launch_qdelta_chunk_simt(const QDeltaArgs &a, int dtype, cudaStream_t s, int *nlaunch);
+cudaError_t launch_qed_chunk_simt(const QedArgs &a, int dtype, cudaStream_t s, int *nlaunch);
+cudaError_t launch_qdelta_step(const StepArgs &a, int dtype, cudaStream_t s, int *nlaunch);
+
+}  // namespace qd

@@ -1,0 +1,136 @@
+// Decode step: one token of the gated Q-Delta recurrence per (sequence, head),
+// state updated in place.  Memory bound: the fp32 state is read once and
+// written once; everything else is a few hundred bytes per head.
+//
+// Per state row s (length dk), with x = k + lambda q and kq = k . q
+// ("Q-Delta: Beyond Key-Value Associative State Evolution", Sec. 3.3.1 Eq. 19 and
+// the single-pass output form derived in the notes' Sec. 2.4):
+//   p = s . x,  r = s . q,  e = v_row - alpha p
+//   s' = alpha s + beta e k,  o_row = alpha r + beta e kq
+//
+// Layout: a group of LANES lanes owns one row, VEC consecutive floats per lane
+// (a 16-byte access for dk = 128), so a warp's access to a row is one fully
+// coalesced 512-byte line.  Each warp keeps UNROLL rows in flight.  One CTA of
+// 4 warps per (sequence, head).
+#include "qd_internal.cuh"
+
+namespace qd {
+namespace {
+
+constexpr int kStepThreads = 128;
+constexpr int kUnroll = 4;
+
+template <int VEC> struct Vec;
+template <> struct Vec<1> { using T = float; };
+template <> struct Vec<2> { using T = float2; };
+template <> struct Vec<4> { using T = float4; };
+
+template <int VEC> __device__ __forceinline__ void vload(const float *p, float (&r)[VEC]) {
+    typename Vec<VEC>::T x = *reinterpret_cast<const typename Vec<VEC>::T *>(p);
+    const float *f = reinterpret_cast<const float *>(&x);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) r[e] = f[e];
+}
+template <int VEC> __device__ __forceinline__ void vstore(float *p, const float (&r)[VEC]) {
+    typename Vec<VEC>::T x;
+    float *f = reinterpret_cast<float *>(&x);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) f[e] = r[e];
+    *reinterpret_cast<typename Vec<VEC>::T *>(p) = x;
+}
+
+template <int LANES> __device__ __forceinline__ float group_sum(float x) {
+#pragma unroll
+    for (int off = LANES / 2; off; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off, LANES);
+    return x;
+}
+
+template <typename TIn, int DK>
+__global__ void __launch_bounds__(kStepThreads) qdelta_step_kernel(StepArgs a) {
+    constexpr int VEC = DK >= 128 ? 4 : (DK >= 64 ? 2 : 1);
+    constexpr int LANES = DK / VEC;             // 32, or 16 when dk = 16
+    constexpr int RPW = 32 / LANES;             // rows per warp per pass
+    constexpr int NW = kStepThreads / 32;
+    const int head = blockIdx.x;                // n * H + h
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane / LANES, l = lane % LANES;
+    const int dv = a.dv;
+
+    const TIn *q = (const TIn *)a.q + (size_t)head * DK;
+    const TIn *k = (const TIn *)a.k + (size_t)head * DK;
+    const TIn *v = (const TIn *)a.v + (size_t)head * dv;
+    const float alpha = a.alpha ? to_f(((const TIn *)a.alpha)[head]) : 1.f;
+    const float beta = to_f(((const TIn *)a.beta)[head]);
+    const float lam = a.lam ? to_f(((const TIn *)a.lam)[head]) : 0.f;
+    TIn *o = (TIn *)a.o + (size_t)head * dv;
+    float *S = a.S + (size_t)head * dv * DK;
+
+    float qv[VEC], kv[VEC], xv[VEC];
+    float kq = 0.f;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+        qv[e] = to_f(q[l * VEC + e]);
+        kv[e] = to_f(k[l * VEC + e]);
+        xv[e] = kv[e] + lam * qv[e];
+        kq = fmaf(kv[e], qv[e], kq);
+    }
+    kq = group_sum<LANES>(kq);
+
+    const int row_step = NW * RPW;              // rows covered by one pass of the CTA
+    for (int base = warp * RPW; base < dv; base += row_step * kUnroll) {   // warp-uniform
+        const int r0 = base + sub;
+        float s[kUnroll][VEC] = {};
+        float vr[kUnroll] = {};
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int row = r0 + u * row_step;
+            if (row < dv) {
+                vload<VEC>(S + (size_t)row * DK + l * VEC, s[u]);
+                vr[u] = to_f(v[row]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int row = r0 + u * row_step;
+            float p = 0.f, r = 0.f;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                p = fmaf(s[u][e], xv[e], p);
+                r = fmaf(s[u][e], qv[e], r);
+            }
+            p = group_sum<LANES>(p);
+            r = group_sum<LANES>(r);
+            if (row < dv) {
+                const float err = vr[u] - alpha * p;
+                const float be = beta * err;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) s[u][e] = fmaf(alpha, s[u][e], be * kv[e]);
+                vstore<VEC>(S + (size_t)row * DK + l * VEC, s[u]);
+                if (l == 0) o[row] = from_f<TIn>(fmaf(alpha, r, be * kq));
+            }
+        }
+    }
+}
+
+template <typename TIn>
+cudaError_t run_step(const StepArgs &a, cudaStream_t s) {
+    const unsigned grid = (unsigned)((size_t)a.N * a.H);
+    switch (a.dk) {
+        case 16: qdelta_step_kernel<TIn, 16><<<grid, kStepThreads, 0, s>>>(a); break;
+        case 32: qdelta_step_kernel<TIn, 32><<<grid, kStepThreads, 0, s>>>(a); break;
+        case 64: qdelta_step_kernel<TIn, 64><<<grid, kStepThreads, 0, s>>>(a); break;
+        case 128: qdelta_step_kernel<TIn, 128><<<grid, kStepThreads, 0, s>>>(a); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_qdelta_step(const StepArgs &a, int dtype, cudaStream_t s, int *nlaunch) {
+    cudaError_t e = dtype == kBF16 ? run_step<__nv_bfloat16>(a, s) : run_step<float>(a, s);
+    if (e == cudaSuccess) *nlaunch += 1;
+    return e;
+}
+
+}  // namespace qd

@@ -1,0 +1,130 @@
+/*
+ * qdelta.h -- C ABI of the GB300 (sm_103a) Q-Delta / QED forward and decode step.
+ *
+ * Every entry point takes plain device pointers and sizes; no C++ or framework
+ * types cross this boundary.  All device buffers are owned by the caller.  Every
+ * compute call is asynchronous on the caller's stream and does not synchronise.
+ * No call throws; each returns a qd_status and, on error, records a message
+ * retrievable with qd_last_error() (per host thread).
+ *
+ * Layouts (row-major, dense, no padding):
+ *   tokens    q, k        [B][T][H][dk]      in the call's dtype
+ *             v, o        [B][T][H][dv]      in the call's dtype
+ *   Q-Delta   alpha, beta, lam  [B][T][H]    in the call's dtype
+ *   QED       g, b        [B][T][H][dk], w [B][T][H][dv] in the call's dtype;
+ *             lam_h [H] fp32
+ *   state     S0, S_final, S    [B][H][dv][dk] fp32 (decode: [N][H][dv][dk])
+ *             Q-Delta's state is d_v x d_k (o = S q); QED's state is K x V
+ *             (o = S^T q) and is stored transposed, so both share this format.
+ * Every pointer must be 16-byte aligned.  S0 may alias S_final (in-place carry).
+ *
+ * Supported: dk, dv in {16, 32, 64, 128}; chunk = 64; any T >= 0 (a ragged last
+ * chunk is handled); dtype QD_F32 or QD_BF16 (math in fp32, state in fp32).
+ */
+#ifndef QDELTA_GB300_H
+#define QDELTA_GB300_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define QD_API __attribute__((visibility("default")))
+#else
+#define QD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QD_OK = 0,
+    QD_ERR_ARG = 1,          /* null / misaligned pointer, negative or overflowing size */
+    QD_ERR_UNSUPPORTED = 2,  /* valid but unsupported: head dim, chunk size, dtype */
+    QD_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+    QD_ERR_TIMEOUT = 4,      /* a kernel's bounded wait gave up (see qd_device_status) */
+    QD_ERR_WORKSPACE = 5     /* workspace missing or smaller than *_workspace_bytes() */
+} qd_status;
+
+typedef enum { QD_F32 = 0, QD_BF16 = 1 } qd_dtype;
+
+/*
+ * qdelta_fwd -- chunkwise-parallel forward of the gated Q-Delta recurrence.
+ *
+ * Defines (reading notes "Q-Delta: Beyond Key-Value Associative State
+ * Evolution", Sec. 3.3.1, Eqs. 17-20, the boxed gated form), per (b, h), for
+ * t = 1..T, starting from S_0 = S0 (or 0):
+ *     x_t = k_t + lambda_t q_t
+ *     S_t = alpha_t S_{t-1} (I - beta_t x_t k_t^T) + beta_t v_t k_t^T
+ *     o_t = S_t q_t
+ * computed chunk by chunk (Sec. 3.3.2, Eqs. 20-27: WY / UT-transform form, with
+ * the notes' corrections of the v1 transposes and decay factors).
+ * alpha == NULL means alpha = 1 and lam == NULL means lambda = 0: lam == NULL
+ * is Gated DeltaNet, both NULL is DeltaNet.  beta must not be NULL.
+ * S0 == NULL starts from zero; S_final == NULL skips writing the final state.
+ * o receives o_t in the call's dtype.
+ *
+ * workspace: device scratch of at least qdelta_workspace_bytes(...) bytes
+ * (may be NULL when that returns 0).  Calls that share a workspace must be
+ * ordered on one stream.
+ */
+QD_API qd_status qdelta_fwd(const void *q, const void *k, const void *v,
+                     const void *alpha, const void *beta, const void *lam,
+                     const float *S0, void *o, float *S_final,
+                     int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype,
+                     void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of device workspace qdelta_fwd needs for these sizes (0 if none). */
+QD_API size_t qdelta_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype);
+
+/*
+ * qed_fwd -- chunked forward of QED over GDN-2 (reading notes "The Query Knows
+ * What to Forget", Sec. 2.1-2.2: GDN-2 update of Eqs. 4/8, erase vector of
+ * Eq. 6).  With the paper's K x V state S (stored transposed, see above):
+ *     Sbar_t = Diag(exp g_t) S_{t-1}
+ *     u_t = b_t * q_t;  d_t = u_t - k_t (k_t^T u_t);  a_t = b_t * k_t + lam_h[h] d_t
+ *     S_t = Sbar_t + k_t (w_t * v_t - Sbar_t^T a_t)^T
+ *     o_t = S_t^T q_t
+ * g is the per-key-channel log-decay (g <= 0 expected).  The chunked kernel
+ * factors exp(G_t - G_i) into exp(G_t) exp(-G_i) within a chunk, G the in-chunk
+ * cumulative log-decay; it stays accurate while every channel's log-decay summed
+ * over one 64-token chunk is >= -80 (fp32 range).  lam_h must not be NULL.
+ */
+QD_API qd_status qed_fwd(const void *q, const void *k, const void *v,
+                  const void *g, const void *b, const void *w, const float *lam_h,
+                  const float *S0, void *o, float *S_final,
+                  int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype,
+                  void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+QD_API size_t qed_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype);
+
+/*
+ * qdelta_step -- one decode step of the same recurrence (T = 1), state in place.
+ * Uses the single-pass output form of the Q-Delta notes, Sec. 2.4:
+ *     o_t = alpha_t S_{t-1} q_t + beta_t (v_t - alpha_t S_{t-1} x_t)(k_t^T q_t)
+ * so each state row is read once and written once.
+ *   S  [N][H][dv][dk] fp32, updated in place from S_{t-1} to S_t
+ *   q, k [N][H][dk]; v, o [N][H][dv]; alpha, beta, lam [N][H] (alpha, lam nullable)
+ */
+QD_API qd_status qdelta_step(float *S, const void *q, const void *k, const void *v,
+                      const void *alpha, const void *beta, const void *lam, void *o,
+                      int N, int H, int dk, int dv, qd_dtype dtype, cudaStream_t stream);
+
+/*
+ * qd_device_status -- synchronises `stream`, then reports whether any kernel of
+ * this library gave up a bounded wait since the last call (QD_ERR_TIMEOUT) or the
+ * stream holds a CUDA error (QD_ERR_CUDA).  Clears the timeout flag.
+ */
+QD_API qd_status qd_device_status(cudaStream_t stream);
+
+/* Message of the last failed call on this host thread ("" if none). */
+QD_API const char *qd_last_error(void);
+
+/* Number of kernels the last successful compute call on this thread launched. */
+QD_API int qd_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QDELTA_GB300_H */

@@ -1,0 +1,79 @@
+"""The C-ABI library: it loads without a GPU, exports every symbol the header
+declares, and rejects bad arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import delta_rule_linear_qdelta_gb300 as qd
+from delta_rule_linear_qdelta_gb300 import build as qd_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qdelta.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    qd_build.build()
+    return qd.load_library()
+
+
+def header_functions():
+    txt = open(HEADER).read()
+    return sorted(set(re.findall(r"QD_API\s+[\w\s\*]+?\b(\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_entry_points():
+    names = header_functions()
+    assert set(names) == set(qd.EXPORTS), names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    P = ctypes.c_void_p
+    good = P(256)
+    st = lib.qdelta_fwd(None, good, good, None, good, None, None, good, None,
+                        1, 8, 1, 64, 64, 64, qd.QD_BF16, None, 0, None)
+    assert st == qd.QD_ERR_ARG and "NULL" in qd.qd_last_error()
+    st = lib.qdelta_fwd(P(258), good, good, None, good, None, None, good, None,
+                        1, 8, 1, 64, 64, 64, qd.QD_BF16, None, 0, None)
+    assert st == qd.QD_ERR_ARG and "aligned" in qd.qd_last_error()
+    st = lib.qdelta_step(good, good, good, good, None, None, None, good, 1, 1, 64, 64, qd.QD_BF16, None)
+    assert st == qd.QD_ERR_ARG
+
+
+@pytest.mark.parametrize("dk,dv,chunk,dt,code", [(48, 64, 64, 1, 2), (64, 256, 64, 1, 2), (64, 64, 32, 1, 2),
+                                                  (64, 64, 64, 7, 2)])
+def test_unsupported_shapes_rejected(lib, dk, dv, chunk, dt, code):
+    g = ctypes.c_void_p(256)
+    st = lib.qdelta_fwd(g, g, g, None, g, None, None, g, None, 1, 8, 1, dk, dv, chunk, dt, None, 0, None)
+    assert st == code, qd.qd_last_error()
+    st = lib.qed_fwd(g, g, g, g, g, g, g, None, g, None, 1, 8, 1, dk, dv, chunk, dt, None, 0, None)
+    assert st == code, qd.qd_last_error()
+
+
+def test_negative_sizes_rejected_and_empty_batch_is_a_noop(lib):
+    g = ctypes.c_void_p(256)
+    assert lib.qdelta_fwd(g, g, g, None, g, None, None, g, None, -1, 8, 1, 64, 64, 64, 1, None, 0, None) == qd.QD_ERR_ARG
+    # B = 0: nothing to do, no device call
+    assert lib.qdelta_fwd(None, None, None, None, None, None, None, None, None, 0, 8, 4, 64, 64, 64, 1,
+                          None, 0, None) == qd.QD_OK
+    assert lib.qdelta_step(None, None, None, None, None, None, None, None, 0, 4, 64, 64, 1, None) == qd.QD_OK
+
+
+def test_python_binding_refuses_cpu_tensors(lib):
+    import torch
+    x = torch.zeros(1, 4, 1, 16, dtype=torch.bfloat16)
+    gt = torch.zeros(1, 4, 1, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        qd.qdelta_fwd(x, x, x, gt, gt, gt)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="not built"):
+        qd.load_library(str(tmp_path / "nope.so"))

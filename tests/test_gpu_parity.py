@@ -1,0 +1,285 @@
+"""GPU vs oracle parity, through the C ABI (via the thin binding).
+
+Tolerances (element by element against the fp64 oracle on identical inputs):
+  bf16 inputs, fp32 accumulation: relative L2 <= 5e-3 and max abs <= 2e-2
+  fp32 path:                       relative L2 <= 1e-5
+Small cases compare every output; the full-size workloads run on the GPU in the
+same launch configuration the bench times, and compare sampled (b, h) streams
+that the oracle computes one by one over the full sequence.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+BF16_REL, BF16_ABS, F32_REL = 5e-3, 2e-2, 1e-5
+
+
+@pytest.fixture(scope="module")
+def qd():
+    import delta_rule_linear_qdelta_gb300 as m
+    from delta_rule_linear_qdelta_gb300 import build
+    build.build()
+    m.load_library()
+    assert torch.cuda.is_available()
+    return m
+
+
+def dev(x, dtype=torch.bfloat16):
+    if x is None:
+        return None
+    return torch.from_numpy(np.ascontiguousarray(x)).to("cuda", dtype)
+
+
+def tdt(d):
+    return torch.bfloat16 if d["dtype"] == "bf16" else torch.float32
+
+
+def check(got, ref, dtype, what):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    mx = np.abs(got - ref).max() if got.size else 0.0
+    if dtype == "bf16":
+        assert rel <= BF16_REL and mx <= BF16_ABS, f"{what}: rel L2 {rel:.3e}, max abs {mx:.3e}"
+    else:
+        assert rel <= F32_REL, f"{what}: rel L2 {rel:.3e}, max abs {mx:.3e}"
+    return rel, mx
+
+
+def run_qdelta(qd, d):
+    dt = tdt(d)
+    o, S = qd.qdelta_fwd(dev(d["q"], dt), dev(d["k"], dt), dev(d["v"], dt), dev(d["alpha"], dt),
+                         dev(d["beta"], dt), dev(d["lam"], dt), dev(d["S0"], torch.float32))
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy(), S.cpu().numpy()
+
+
+def run_qed(qd, d):
+    dt = tdt(d)
+    o, S = qd.qed_fwd(dev(d["q"], dt), dev(d["k"], dt), dev(d["v"], dt), dev(d["g"], dt), dev(d["b"], dt),
+                      dev(d["w"], dt), dev(d["lam_h"], torch.float32), dev(d["S0"], torch.float32))
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy(), S.cpu().numpy()
+
+
+def sel(x, pairs, gate=False):
+    """Stack streams (b, h) of [B,T,H,...] into [n,T,1,...] for the oracle."""
+    if x is None:
+        return None
+    return np.stack([x[b, :, h] for b, h in pairs])[:, :, None]
+
+
+# ------------------------------------------------------------------ Q-Delta
+
+def test_tiny_fp32_full(qd):
+    name, d = synth.tiny_fp32()
+    o, S = run_qdelta(qd, d)
+    o_ref, S_ref = oracle.qdelta_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["lam"], d["S0"])
+    check(o, o_ref, "f32", name + " o")
+    check(S, S_ref, "f32", name + " S")
+
+
+@pytest.mark.parametrize("mode", ["qdelta", "gdn", "deltanet"])
+def test_bf16_small_all_outputs(qd, mode):
+    d = synth.qdelta_inputs(2, 200, 3, 128, 128, seed=21, dtype="bf16", mode=mode, s0_var=0.01)
+    o, S = run_qdelta(qd, d)
+    o_ref, S_ref = oracle.qdelta_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["lam"], d["S0"])
+    check(o, o_ref, "bf16", f"{mode} o")
+    check(S, S_ref, "bf16", f"{mode} S")
+
+
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 100, 191])
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_ragged_lengths(qd, T, dt):
+    d = synth.qdelta_inputs(1, T, 2, 128, 128, seed=30 + T, dtype=dt, mode="qdelta", s0_var=0.01)
+    o, S = run_qdelta(qd, d)
+    o_ref, S_ref = oracle.qdelta_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["lam"], d["S0"])
+    check(o, o_ref, dt, f"T={T} o")
+    check(S, S_ref, dt, f"T={T} S")
+
+
+@pytest.mark.parametrize("dk,dv", [(16, 16), (32, 64), (64, 32), (64, 64), (128, 64), (64, 128)])
+def test_head_dims_fp32(qd, dk, dv):
+    d = synth.qdelta_inputs(2, 130, 2, dk, dv, seed=40 + dk + dv, dtype="f32", mode="qdelta", s0_var=0.01)
+    o, S = run_qdelta(qd, d)
+    o_ref, S_ref = oracle.qdelta_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["lam"], d["S0"])
+    check(o, o_ref, "f32", f"dk={dk} dv={dv} o")
+    check(S, S_ref, "f32", f"dk={dk} dv={dv} S")
+
+
+@pytest.mark.parametrize("mode", ["qdelta", "gdn", "deltanet"])
+def test_layer_1p3b_full_size_sampled(qd, mode):
+    """B=8, H=16, T=2048, d=128 bf16: the benchmarked workload; 6 streams checked."""
+    name, d = synth.layer_1p3b(mode)
+    o, S = run_qdelta(qd, d)
+    pairs = [(0, 0), (0, 15), (3, 7), (5, 2), (7, 9), (7, 15)]
+    o_ref, S_ref = oracle.qdelta_fwd(sel(d["q"], pairs), sel(d["k"], pairs), sel(d["v"], pairs),
+                                     sel(d["alpha"], pairs), sel(d["beta"], pairs), sel(d["lam"], pairs))
+    check(sel(o, pairs), o_ref, "bf16", name + " o")
+    check(np.stack([S[b, h] for b, h in pairs])[:, None], S_ref, "bf16", name + " S")
+
+
+def test_long_context_full_size_sampled(qd):
+    """B=1, H=16, T=32768, mean alpha 0.995, S0 ~ N(0, 0.01); 2 heads checked."""
+    name, d = synth.long_context()
+    o, S = run_qdelta(qd, d)
+    pairs = [(0, 3), (0, 12)]
+    S0 = np.stack([d["S0"][b, h] for b, h in pairs])[:, None]
+    o_ref, S_ref = oracle.qdelta_fwd(sel(d["q"], pairs), sel(d["k"], pairs), sel(d["v"], pairs),
+                                     sel(d["alpha"], pairs), sel(d["beta"], pairs), sel(d["lam"], pairs), S0)
+    check(sel(o, pairs), o_ref, "bf16", name + " o")
+    check(np.stack([S[b, h] for b, h in pairs])[:, None], S_ref, "bf16", name + " S")
+
+
+def test_split_call_carries_state_in_place(qd):
+    """fwd(T1) then fwd(T2, S0 = S_T1) equals one fwd(T1+T2); S0 aliases S_final."""
+    d = synth.qdelta_inputs(2, 300, 2, 128, 128, seed=50, dtype="bf16", mode="qdelta", s0_var=0.01)
+    dt = torch.bfloat16
+    o_ref, S_ref = oracle.qdelta_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["lam"], d["S0"])
+    S = dev(d["S0"], torch.float32)
+    outs = []
+    for a, b in ((0, 100), (100, 300)):   # split at a non-multiple of the chunk
+        sl = lambda x: None if x is None else x[:, a:b]
+        o, _ = qd.qdelta_fwd(dev(sl(d["q"]), dt), dev(sl(d["k"]), dt), dev(sl(d["v"]), dt),
+                             dev(sl(d["alpha"]), dt), dev(sl(d["beta"]), dt), dev(sl(d["lam"]), dt), S, S_final=S)
+        outs.append(o.float().cpu().numpy())
+    torch.cuda.synchronize()
+    check(np.concatenate(outs, axis=1), o_ref, "bf16", "split o")
+    check(S.cpu().numpy(), S_ref, "bf16", "split S")
+
+
+def test_empty_sequence_and_batch(qd):
+    S0 = torch.randn(2, 3, 64, 64, device="cuda")
+    z = torch.empty(2, 0, 3, 64, device="cuda", dtype=torch.bfloat16)
+    zg = torch.empty(2, 0, 3, device="cuda", dtype=torch.bfloat16)
+    o, S = qd.qdelta_fwd(z, z, z, zg, zg, zg, S0)
+    torch.cuda.synchronize()
+    assert o.shape == (2, 0, 3, 64) and torch.equal(S, S0)
+    o, S = qd.qdelta_fwd(z, z, z, None, zg, None, None)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(S) == 0
+
+
+def test_deterministic(qd):
+    d = synth.qdelta_inputs(1, 300, 4, 128, 128, seed=60, dtype="bf16", mode="qdelta")
+    o1, S1 = run_qdelta(qd, d)
+    o2, S2 = run_qdelta(qd, d)
+    assert np.array_equal(o1, o2) and np.array_equal(S1, S2)
+
+
+# ---------------------------------------------------------------------- QED
+
+@pytest.mark.parametrize("T,dt", [(1, "bf16"), (70, "bf16"), (200, "bf16"), (130, "f32")])
+def test_qed_small_all_outputs(qd, T, dt):
+    d = synth.qed_inputs(2, T, 2, 128, 128, seed=70 + T, dtype=dt, s0_var=0.01)
+    o, S = run_qed(qd, d)
+    o_ref, S_ref = oracle.qed_fwd(d["q"], d["k"], d["v"], d["g"], d["b"], d["w"], d["lam_h"], d["S0"])
+    check(o, o_ref, dt, f"qed T={T} o")
+    check(S, S_ref, dt, f"qed T={T} S")
+
+
+def test_qed_lambda_zero_is_gdn2(qd):
+    """lam_h = 0 reduces QED to GDN-2; compared with the oracle at lam_h = 0."""
+    d = synth.qed_inputs(1, 150, 2, 64, 64, seed=80, dtype="f32")
+    d["lam_h"] = np.zeros_like(d["lam_h"])
+    o, S = run_qed(qd, d)
+    o_ref, S_ref = oracle.qed_fwd(d["q"], d["k"], d["v"], d["g"], d["b"], d["w"], d["lam_h"])
+    check(o, o_ref, "f32", "gdn2 o")
+    check(S, S_ref, "f32", "gdn2 S")
+
+
+def test_qed_full_size_sampled(qd):
+    """B=4, H=8, T=4096, d=128 bf16; 4 streams checked."""
+    name, d = synth.qed_gdn2()
+    o, S = run_qed(qd, d)
+    pairs = [(0, 0), (1, 5), (2, 7), (3, 3)]
+    lam = np.array([d["lam_h"][h] for _, h in pairs])
+    # the oracle takes one lambda_h per head: run each stream as its own head
+    o_ref = np.zeros((len(pairs), 4096, 1, 128))
+    S_ref = np.zeros((len(pairs), 1, 128, 128))
+    for i, (b, h) in enumerate(pairs):
+        s = [(b, h)]
+        o1, S1 = oracle.qed_fwd(sel(d["q"], s), sel(d["k"], s), sel(d["v"], s), sel(d["g"], s), sel(d["b"], s),
+                                sel(d["w"], s), lam[i:i + 1])
+        o_ref[i], S_ref[i] = o1[0], S1[0]
+    check(sel(o, pairs), o_ref, "bf16", name + " o")
+    check(np.stack([S[b, h] for b, h in pairs])[:, None], S_ref, "bf16", name + " S")
+
+
+# ------------------------------------------------------------------- decode
+
+def test_decode_small_all_outputs(qd):
+    d = synth.decode_inputs(3, 2, 128, 128, 20, seed=90)
+    S = dev(d["S0"], torch.float32)
+    S_ref = d["S0"].astype(np.float64).copy()
+    for t in range(20):
+        o = qd.qdelta_step(S, dev(d["q"][t]), dev(d["k"][t]), dev(d["v"][t]), dev(d["alpha"][t]),
+                           dev(d["beta"][t]), dev(d["lam"][t]))
+        o_ref = oracle.qdelta_step(S_ref, d["q"][t], d["k"][t], d["v"][t], d["alpha"][t], d["beta"][t],
+                                   d["lam"][t])
+        check(o.float().cpu().numpy(), o_ref, "bf16", f"step {t} o")
+    check(S.cpu().numpy(), S_ref, "f32", "decode S")
+
+
+@pytest.mark.parametrize("dk,dv", [(16, 16), (32, 64), (64, 128)])
+def test_decode_head_dims_fp32(qd, dk, dv):
+    d = synth.decode_inputs(2, 3, dk, dv, 5, seed=91, dtype="f32")
+    S = dev(d["S0"], torch.float32)
+    S_ref = d["S0"].astype(np.float64).copy()
+    for t in range(5):
+        o = qd.qdelta_step(S, dev(d["q"][t], torch.float32), dev(d["k"][t], torch.float32),
+                           dev(d["v"][t], torch.float32), None, dev(d["beta"][t], torch.float32), None)
+        o_ref = oracle.qdelta_step(S_ref, d["q"][t], d["k"][t], d["v"][t], None, d["beta"][t], None)
+        check(o.cpu().numpy(), o_ref, "f32", f"step {t} o")
+    check(S.cpu().numpy(), S_ref, "f32", "decode S")
+
+
+def test_decode_512x16_100_steps_sampled(qd):
+    """N=512 x H=16, 128x128 fp32 state, 100 consecutive steps in place; 96 heads
+    followed by the oracle step by step."""
+    name, d = synth.decode_512x16()
+    S = dev(d["S0"], torch.float32)
+    heads = [(n, h) for n in (0, 1, 77, 255, 256, 400, 510, 511) for h in range(0, 16, 4)] + \
+            [(n, h) for n in (3, 300) for h in range(16)] + [(100 + i, i % 16) for i in range(32)]
+    ns = np.array([n for n, _ in heads])
+    hs = np.array([h for _, h in heads])
+    S_ref = d["S0"][ns, hs].astype(np.float64)[:, None].copy()
+    tok = lambda x, t: x[t][ns, hs][:, None]
+    q_d, k_d, v_d = dev(d["q"]), dev(d["k"]), dev(d["v"])
+    a_d, b_d, l_d = dev(d["alpha"]), dev(d["beta"]), dev(d["lam"])
+    for t in range(100):
+        o = qd.qdelta_step(S, q_d[t], k_d[t], v_d[t], a_d[t], b_d[t], l_d[t])
+        o_ref = oracle.qdelta_step(S_ref, tok(d["q"], t), tok(d["k"], t), tok(d["v"], t), tok(d["alpha"], t),
+                                   tok(d["beta"], t), tok(d["lam"], t))
+        if t % 10 == 9:
+            got = o[torch.from_numpy(ns).cuda(), torch.from_numpy(hs).cuda()].float().cpu().numpy()[:, None]
+            check(got, o_ref, "bf16", f"{name} step {t} o")
+    got = S[torch.from_numpy(ns).cuda(), torch.from_numpy(hs).cuda()].cpu().numpy()[:, None]
+    check(got, S_ref, "f32", name + " S after 100 steps")
+
+
+def test_step_sequence_matches_forward(qd):
+    d = synth.qdelta_inputs(2, 40, 2, 64, 64, seed=95, dtype="f32", mode="qdelta", s0_var=0.01)
+    f = torch.float32
+    o_fwd, S_fwd = qd.qdelta_fwd(dev(d["q"], f), dev(d["k"], f), dev(d["v"], f), dev(d["alpha"], f),
+                                 dev(d["beta"], f), dev(d["lam"], f), dev(d["S0"], f))
+    S = dev(d["S0"], f)
+    outs = []
+    for t in range(40):
+        outs.append(qd.qdelta_step(S, dev(d["q"][:, t], f), dev(d["k"][:, t], f), dev(d["v"][:, t], f),
+                                   dev(d["alpha"][:, t], f), dev(d["beta"][:, t], f), dev(d["lam"][:, t], f)))
+    o_step = torch.stack(outs, dim=1)
+    torch.cuda.synchronize()
+    check(o_step.cpu().numpy(), o_fwd.cpu().numpy(), "f32", "step vs fwd o")
+    check(S.cpu().numpy(), S_fwd.cpu().numpy(), "f32", "step vs fwd S")
+
+
+def test_device_status_ok(qd):
+    assert qd.qd_device_status() == qd.QD_OK
