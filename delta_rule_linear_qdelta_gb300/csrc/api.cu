@@ -87,7 +87,8 @@ qd_status qdelta_fwd(const void *q, const void *k, const void *v, const void *al
     if (B == 0 || H == 0) { g_launches = 0; return QD_OK; }
     if (T == 0) { g_launches = 0; return empty_sequence(S0, S_final, B, H, dk, dv, stream); }
     qd::QDeltaArgs a{q, k, v, alpha, beta, lam, S0, o, S_final, B, T, H, dk, dv, workspace, workspace_bytes};
-    cudaError_t e = qd::launch_qdelta_chunk_simt(a, dtype, stream, &n);
+    cudaError_t e = qd::qdelta_tc_supported(a, dtype) ? qd::launch_qdelta_chunk_tc(a, stream, &n)
+                                                      : qd::launch_qdelta_chunk_simt(a, dtype, stream, &n);
     if (e != cudaSuccess) return cuda_fail(e, "qdelta_fwd launch");
     g_launches = n;
     return QD_OK;
@@ -145,6 +146,8 @@ qd_status qd_device_status(cudaStream_t stream) {
     g_err[0] = 0;
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "qd_device_status");
+    if (qd::tc_read_and_clear_timeout())
+        return fail(QD_ERR_TIMEOUT, "a tensor-core kernel gave up a bounded wait (results of that call are invalid)");
     return QD_OK;
 }
 

@@ -1,0 +1,595 @@
+// Fused chunked Q-Delta forward on the sm_103a tensor cores (tcgen05 + TMEM + TMA),
+// bf16 inputs, dk = dv = 128, chunk C = 64, fp32 state held on chip for the whole
+// sequence.  One CTA of 8 warps per (b, h).
+//
+// Algorithm ("Q-Delta: Beyond Key-Value Associative State Evolution", Sec. 3.3.2,
+// Eqs. 20-27, with the corrected transposes and gamma_r/gamma_i decay; the two UT
+// solves folded into one).  Per chunk, rows stacked, l_i = sum_{j<=i} log alpha_j,
+// gamma_i = e^{l_i}, kappa_i = e^{l_C - l_i}, X = K + diag(lambda) Q:
+//   G      = [X; Q] K^T                                   (one M=128 MMA)
+//   A      = strictly_lower(beta_t e^{l_t - l_i} (X K^T)_ti);  P = incl_lower(e^{l_t-l_i} (Q K^T)_ti)
+//   Tinv   = (I + A)^{-1}                                  (block-doubling solve, fp32)
+//   U^T    = V^T (Tinv diag(beta))^T;   W^T = X^T (Tinv diag(beta gamma))^T
+//   Z^T    = U^T - S W^T                                   (S = state entering the chunk)
+//   O^T    = diag-scaled S Q^T + Z^T P^T,  i.e. o_t = gamma_t S q_t + sum_i P_ti z_i
+//   S     <- gamma_C S + Z^T diag(kappa) K
+// Every product is written "transposed" so that the 128 TMEM lanes index d_v (or
+// d_k) and every MMA has M = 128.  The master state stays in registers in fp32;
+// its bf16 copy in shared memory feeds the MMAs.
+//
+// Shared memory (offsets from a 1024-aligned base):
+//   stage s in {0,1}: XQ 32 KB (per 64-column panel: X rows 0-63 | Q rows 64-127),
+//                     K 16 KB (overwritten in place by kappa*K), V 16 KB
+//   S_in 32 KB   bf16 state [dv][dk]
+//   R1   17 KB   A/Tinv fp32 [64][65]  ->  Tinv*beta, Tinv*beta*gamma (bf16)
+//   R2   16 KB   -W [64][dk]  ->  Z^T [dv][64]  ->  O staging [64][dv]
+//   P     8 KB   bf16 [64][64]
+// All MMA operands use the 128-byte swizzle (TMA layout): 128-byte rows, 8-row
+// groups 1024 bytes apart, 64-column panels.
+// TMEM (512 columns): G 0-63, O1 64-127, U/Z 128-191, W 192-255, O2 256-319, dS 320-447.
+//
+// Every wait is bounded; on a timeout the kernel sets the library's error word,
+// drains its own copies and MMAs, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "qd_internal.cuh"
+#include "sm103_ptx.cuh"
+
+namespace qd {
+
+__device__ unsigned int g_tc_timeout = 0;
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kC = 64, kD = 128, kThreads = 256;
+constexpr uint32_t kStageBytes = 65536;
+constexpr uint32_t OFF_XQ = 0, OFF_K = 32768, OFF_V = 49152;
+constexpr uint32_t OFF_S = 2 * kStageBytes;          // 131072
+constexpr uint32_t OFF_R1 = OFF_S + 32768;           // 163840
+constexpr uint32_t OFF_R2 = OFF_R1 + 17408;          // 181248
+constexpr uint32_t OFF_P = OFF_R2 + 16384;           // 197632
+constexpr uint32_t kSmemUsed = OFF_P + 8192;         // 205824
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
+constexpr int LA = 65;                               // fp32 row stride of A
+constexpr uint32_t kTmaBytes = 3 * kC * kD * 2;      // Q, K, V tiles per chunk
+constexpr uint64_t kWaitNs = 2000000000ull;          // 2 s per wait
+
+constexpr uint32_t TM_G = 0, TM_O1 = 64, TM_U = 128, TM_W = 192, TM_O2 = 256, TM_DS = 320;
+
+struct TcParams {
+    const __nv_bfloat16 *alpha, *beta, *lam;
+    const float *S0;
+    float *S_final;
+    int B, T, H;
+};
+
+__device__ __forceinline__ float bf(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+    uint4 u;
+    u.x = pack_bf16x2(f[0], f[1]);
+    u.y = pack_bf16x2(f[2], f[3]);
+    u.z = pack_bf16x2(f[4], f[5]);
+    u.w = pack_bf16x2(f[6], f[7]);
+    return u;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
+                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmO) {
+    extern __shared__ uint8_t smraw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t bar_full[2], bar_mma;
+    __shared__ uint32_t tmem_base;
+    __shared__ int abort_flag;
+    __shared__ float g_ell[kC], g_beta[kC], g_lam[kC], g_gam[kC], g_kap[kC];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q4 = warp & 3, hf = warp >> 2;          // TMEM lane quarter, column half
+    const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
+    const int T = p.T, H = p.H;
+    const int nchunks = (T + kC - 1) / kC;
+    const bool producer = (tid == 0), issuer = (tid == 32);
+
+    if (tid == 0) {
+        mbar_init(&bar_full[0], 1);
+        mbar_init(&bar_full[1], 1);
+        mbar_init(&bar_mma, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmO);
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_base, 512);
+        tmem_relinquish();
+    }
+
+    // master state rows d = 32*q4 + lane, columns 64*hf .. 64*hf+63 (fp32, registers)
+    const int d_row = 32 * q4 + lane;
+    float S[64];
+    {
+        const size_t base = ((size_t)bh * kD + d_row) * kD + 64 * hf;
+        if (p.S0) {
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+                float4 v = *reinterpret_cast<const float4 *>(p.S0 + base + j);
+                S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 64; ++j) S[j] = 0.f;
+        }
+        uint8_t *sp = sm + OFF_S + hf * 16384;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = S[8 * ch + e];
+            *reinterpret_cast<uint4 *>(sp + sw128_off(d_row, 8 * ch)) = pack8(f);
+        }
+    }
+
+    auto issue_loads = [&](int c) {
+        const int s = c & 1;
+        uint8_t *st = sm + s * kStageBytes;
+        const int t0 = c * kC;
+        mbar_arrive_expect_tx(&bar_full[s], kTmaBytes);
+#pragma unroll
+        for (int pnl = 0; pnl < 2; ++pnl) {
+            tma_load_4d(st + OFF_XQ + pnl * 16384 + 8192, &tmQ, &bar_full[s], 64 * pnl, h, t0, b);
+            tma_load_4d(st + OFF_K + pnl * 8192, &tmK, &bar_full[s], 64 * pnl, h, t0, b);
+            tma_load_4d(st + OFF_V + pnl * 8192, &tmV, &bar_full[s], 64 * pnl, h, t0, b);
+        }
+    };
+
+    // gates of a chunk: lane l of warp 0 holds tokens 2l and 2l+1
+    float ga[2], gb[2], gl[2];
+    auto load_gates = [&](int c) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int t = c * kC + 2 * lane + u;
+            const bool ok = t < T;
+            const size_t tok = ((size_t)b * T + t) * H + h;
+            ga[u] = (ok && p.alpha) ? bf(p.alpha[tok]) : 1.f;
+            gb[u] = ok ? bf(p.beta[tok]) : 0.f;
+            gl[u] = (ok && p.lam) ? bf(p.lam[tok]) : 0.f;
+        }
+    };
+
+    if (producer) {
+        issue_loads(0);
+        if (nchunks > 1) issue_loads(1);
+    }
+    if (warp == 0) load_gates(0);
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_base;
+    const uint32_t tl = tm + ((uint32_t)(32 * q4) << 16);   // this warp's TMEM lane quarter
+    uint32_t mma_phase = 0;
+    bool ok = true;
+
+    auto wait_mma = [&]() {
+        if (!mbar_wait(&bar_mma, mma_phase, kWaitNs)) { ok = false; abort_flag = 1; }
+        mma_phase ^= 1;
+        tc_fence_after();
+    };
+    auto sync_for_mma = [&]() {   // generic smem writes -> visible to the tensor core / TMA
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    };
+
+    const uint32_t sbase = smem_u32(sm);
+    for (int c = 0; c < nchunks; ++c) {
+        const int s = c & 1;
+        const int t0 = c * kC;
+        uint8_t *st = sm + s * kStageBytes;
+        const uint32_t sXQ = sbase + s * kStageBytes + OFF_XQ, sK = sbase + s * kStageBytes + OFF_K;
+        const uint32_t sV = sbase + s * kStageBytes + OFF_V, sS = sbase + OFF_S;
+        const uint32_t sR1 = sbase + OFF_R1, sR2 = sbase + OFF_R2, sP = sbase + OFF_P;
+
+        // (1) gates -> log-prefix, gamma, kappa (warp 0); prefetch the next chunk's gates
+        if (warp == 0) {
+            const float l0 = __logf(ga[0]), l1 = __logf(ga[1]);
+            float sum = l0 + l1;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float n = __shfl_up_sync(0xffffffffu, sum, off);
+                if (lane >= off) sum += n;
+            }
+            const float e1 = sum, e0 = sum - l1;
+            const float eC = __shfl_sync(0xffffffffu, sum, 31);
+            g_ell[2 * lane] = e0;
+            g_ell[2 * lane + 1] = e1;
+            g_beta[2 * lane] = gb[0];
+            g_beta[2 * lane + 1] = gb[1];
+            g_lam[2 * lane] = gl[0];
+            g_lam[2 * lane + 1] = gl[1];
+            g_gam[2 * lane] = __expf(e0);
+            g_gam[2 * lane + 1] = __expf(e1);
+            g_kap[2 * lane] = __expf(eC - e0);
+            g_kap[2 * lane + 1] = __expf(eC - e1);
+            if (c + 1 < nchunks) load_gates(c + 1);
+        }
+        if (producer) tma_store_wait_read0();   // O staging (R2) of the previous chunk is read out
+        if (!mbar_wait(&bar_full[s], (uint32_t)((c >> 1) & 1), kWaitNs)) { ok = false; abort_flag = 1; }
+        __syncthreads();
+        if (abort_flag) break;
+
+        // (2) X = K + lambda Q into rows 0-63 of the XQ panels
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int u = tid + kThreads * r;             // 16-byte chunk index, 0..1023
+            const int pnl = u >> 9;
+            const uint32_t off = (uint32_t)(u & 511) << 4;
+            const int row = off >> 7;
+            float kf[8], qf[8], xf[8];
+            unpack8(*reinterpret_cast<const uint4 *>(st + OFF_K + pnl * 8192 + off), kf);
+            unpack8(*reinterpret_cast<const uint4 *>(st + OFF_XQ + pnl * 16384 + 8192 + off), qf);
+            const float lm = g_lam[row];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xf[e] = fmaf(lm, qf[e], kf[e]);
+            *reinterpret_cast<uint4 *>(st + OFF_XQ + pnl * 16384 + off) = pack8(xf);
+        }
+        sync_for_mma();
+
+        // (3) G = [X;Q] K^T and O1 = S Q^T
+        if (issuer) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
+                umma_bf16(tm + TM_G, smem_desc(sXQ + ko, 16, 1024),
+                          smem_desc(sK + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), idesc_bf16(128, 64, false, false),
+                          k > 0);
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
+                umma_bf16(tm + TM_O1, smem_desc(sS + ko, 16, 1024), smem_desc(sXQ + ko + 8192, 16, 1024),
+                          idesc_bf16(128, 64, false, false), k > 0);
+            }
+            umma_commit(&bar_mma);
+        }
+        wait_mma();
+
+        // (4) decay masks: A (fp32, R1) from X K^T rows, P (bf16) from Q K^T rows; K -> kappa K
+        {
+            float g[32];
+            tmem_ld32(tl + TM_G + 32 * hf, g);
+            tmem_ld_wait();
+            if (q4 < 2) {
+                const int t = 32 * q4 + lane;
+                const float lt = g_ell[t], bt = g_beta[t];
+                float *Arow = reinterpret_cast<float *>(sm + OFF_R1) + t * LA;
+#pragma unroll
+                for (int cc = 0; cc < 32; ++cc) {
+                    const int i = 32 * hf + cc;
+                    Arow[i] = (i < t) ? bt * __expf(lt - g_ell[i]) * g[cc] : 0.f;
+                }
+            } else {
+                const int t = 32 * (q4 - 2) + lane;
+                const float lt = g_ell[t];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int i = 32 * hf + 8 * ch + e;
+                        f[e] = (i <= t) ? __expf(lt - g_ell[i]) * g[8 * ch + e] : 0.f;
+                    }
+                    *reinterpret_cast<uint4 *>(sm + OFF_P + sw128_off(t, 32 * hf + 8 * ch)) = pack8(f);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int u = tid + kThreads * r;
+                const uint32_t off = (uint32_t)u << 4;       // 0 .. 16 KB across both K panels
+                const int row = (off & 8191) >> 7;
+                uint4 *pk = reinterpret_cast<uint4 *>(st + OFF_K + off);
+                float kf[8];
+                unpack8(*pk, kf);
+                const float ka = g_kap[row];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) kf[e] *= ka;
+                *pk = pack8(kf);
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+
+        // (5) Tinv = (I + A)^{-1} in place by block doubling: for each pair of diagonal
+        // blocks of size bs, T21 = -T22 (A21 T11).
+        {
+            float *M = reinterpret_cast<float *>(sm + OFF_R1);
+            for (int bs = 1; bs < kC; bs <<= 1) {
+                const int total = 32 * bs;            // (64 / 2bs) pairs x bs^2
+                float y[4];
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    const int o = tid + kThreads * n;
+                    if (o < total) {
+                        const int pr = o / (bs * bs), rem = o % (bs * bs), r = rem / bs, cc = rem % bs;
+                        const int base = 2 * bs * pr, row = base + bs + r, col = base + cc;
+                        float acc = M[row * LA + col];
+                        for (int k = cc + 1; k < bs; ++k) acc = fmaf(M[row * LA + base + k], M[(base + k) * LA + col], acc);
+                        y[n] = acc;
+                    }
+                }
+                __syncthreads();
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    const int o = tid + kThreads * n;
+                    if (o < total) {
+                        const int pr = o / (bs * bs), rem = o % (bs * bs), r = rem / bs, cc = rem % bs;
+                        M[(2 * bs * pr + bs + r) * LA + 2 * bs * pr + cc] = y[n];
+                    }
+                }
+                __syncthreads();
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    const int o = tid + kThreads * n;
+                    if (o < total) {
+                        const int pr = o / (bs * bs), rem = o % (bs * bs), r = rem / bs, cc = rem % bs;
+                        const int base = 2 * bs * pr, row = base + bs + r, col = base + cc;
+                        float acc = M[row * LA + col];
+                        for (int k = 0; k < r; ++k) acc = fmaf(M[row * LA + base + bs + k], M[(base + bs + k) * LA + col], acc);
+                        y[n] = -acc;
+                    }
+                }
+                __syncthreads();
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    const int o = tid + kThreads * n;
+                    if (o < total) {
+                        const int pr = o / (bs * bs), rem = o % (bs * bs), r = rem / bs, cc = rem % bs;
+                        M[(2 * bs * pr + bs + r) * LA + 2 * bs * pr + cc] = y[n];
+                    }
+                }
+                __syncthreads();
+            }
+            // Tinv*beta and Tinv*beta*gamma as bf16 [64][64] (128B swizzle) over R1
+            float tv[2][8];
+            int rows[2], chs[2];
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                const int u = tid + kThreads * n;          // 512 chunks of 8
+                rows[n] = u >> 3;
+                chs[n] = u & 7;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int j = 8 * chs[n] + e;
+                    tv[n][e] = (j < rows[n]) ? M[rows[n] * LA + j] : (j == rows[n] ? 1.f : 0.f);
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                float f1[8], f2[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int j = 8 * chs[n] + e;
+                    f1[e] = tv[n][e] * g_beta[j];
+                    f2[e] = f1[e] * g_gam[j];
+                }
+                *reinterpret_cast<uint4 *>(sm + OFF_R1 + sw128_off(rows[n], 8 * chs[n])) = pack8(f1);
+                *reinterpret_cast<uint4 *>(sm + OFF_R1 + 8192 + sw128_off(rows[n], 8 * chs[n])) = pack8(f2);
+            }
+        }
+        sync_for_mma();
+
+        // (6) U^T = V^T T1^T, W^T = X^T T2^T
+        if (issuer) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                umma_bf16(tm + TM_U, smem_desc(sV + k * 2048, 8192, 1024), smem_desc(sR1 + k * 32, 16, 1024),
+                          idesc_bf16(128, 64, true, false), k > 0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                umma_bf16(tm + TM_W, smem_desc(sXQ + k * 2048, 16384, 1024), smem_desc(sR1 + 8192 + k * 32, 16, 1024),
+                          idesc_bf16(128, 64, true, false), k > 0);
+            umma_commit(&bar_mma);
+        }
+        wait_mma();
+
+        // (7) -W -> R2 as [64 tokens][dk] (two 64-column panels)
+        {
+            float w[32];
+            tmem_ld32(tl + TM_W + 32 * hf, w);
+            tmem_ld_wait();
+            const int j = d_row;                            // lane index = dk index
+            uint8_t *dst = sm + OFF_R2 + (j >> 6) * 8192;
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+                const int i = 32 * hf + cc;
+                *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(i, j & 63)) = __float2bfloat16_rn(-w[cc]);
+            }
+        }
+        sync_for_mma();
+
+        // (8) Z^T = U^T - S W^T  (accumulate into the U columns)
+        if (issuer) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
+                umma_bf16(tm + TM_U, smem_desc(sS + ko, 16, 1024), smem_desc(sR2 + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024),
+                          idesc_bf16(128, 64, false, false), 1);
+            }
+            umma_commit(&bar_mma);
+        }
+        wait_mma();
+
+        // (9) Z^T (bf16) -> R2 as [dv][64 tokens]
+        {
+            float z[32];
+            tmem_ld32(tl + TM_U + 32 * hf, z);
+            tmem_ld_wait();
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = z[8 * ch + e];
+                *reinterpret_cast<uint4 *>(sm + OFF_R2 + sw128_off(d_row, 32 * hf + 8 * ch)) = pack8(f);
+            }
+        }
+        sync_for_mma();
+
+        // (10) O2 = Z^T P^T ; dS = Z^T (kappa K)
+        if (issuer) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                umma_bf16(tm + TM_O2, smem_desc(sR2 + k * 32, 16, 1024), smem_desc(sP + k * 32, 16, 1024),
+                          idesc_bf16(128, 64, false, false), k > 0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                umma_bf16(tm + TM_DS, smem_desc(sR2 + k * 32, 16, 1024), smem_desc(sK + k * 2048, 8192, 1024),
+                          idesc_bf16(128, 128, false, true), k > 0);
+            umma_commit(&bar_mma);
+        }
+        wait_mma();
+
+        // (11) o = gamma_t O1 + O2 -> staging (R2) ; S = gamma_C S + dS -> registers and bf16 S_in
+        {
+            float o1[32], o2[32];
+            tmem_ld32(tl + TM_O1 + 32 * hf, o1);
+            tmem_ld32(tl + TM_O2 + 32 * hf, o2);
+            tmem_ld_wait();
+            uint8_t *dst = sm + OFF_R2 + (d_row >> 6) * 8192;
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+                const int t = 32 * hf + cc;
+                *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(t, d_row & 63)) =
+                    __float2bfloat16_rn(fmaf(g_gam[t], o1[cc], o2[cc]));
+            }
+            const float gC = g_gam[kC - 1];
+            uint8_t *sp = sm + OFF_S + hf * 16384;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float ds[32];
+                tmem_ld32(tl + TM_DS + 64 * hf + 32 * half, ds);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) S[32 * half + e] = fmaf(gC, S[32 * half + e], ds[e]);
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    float f[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = S[32 * half + 8 * ch + e];
+                    *reinterpret_cast<uint4 *>(sp + sw128_off(d_row, 32 * half + 8 * ch)) = pack8(f);
+                }
+            }
+        }
+        sync_for_mma();
+        if (producer) {
+            tma_store_4d(&tmO, sm + OFF_R2, 0, h, t0, b);
+            tma_store_4d(&tmO, sm + OFF_R2 + 8192, 64, h, t0, b);
+            tma_store_commit();
+            if (c + 2 < nchunks) issue_loads(c + 2);
+        }
+    }
+
+    // final state
+    if (ok && !abort_flag && p.S_final) {
+        float *dst = p.S_final + ((size_t)bh * kD + d_row) * kD + 64 * hf;
+#pragma unroll
+        for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
+    }
+    if (producer) {
+        tma_store_wait_all();
+        if (abort_flag) {
+            // drain loads that may still be landing in shared memory
+            for (int c = 0; c < 2 && c < nchunks; ++c) mbar_wait(&bar_full[c], 0, kWaitNs);
+        }
+    }
+    if (issuer && abort_flag) {
+        umma_commit(&bar_mma);
+        mbar_wait(&bar_mma, mma_phase, kWaitNs);
+    }
+    if (!ok || abort_flag) {
+        if (lane == 0) atomicExch(&g_tc_timeout, 1u);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 512);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// [B][T][H][128] bf16 tensor, boxes of 64 columns x 64 tokens of one head.
+bool make_token_map(CUtensorMap *m, const void *ptr, int B, int T, int H) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2, (cuuint64_t)T * H * kD * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)kC, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool qdelta_tc_supported(const QDeltaArgs &a, int dtype) {
+    return dtype == kBF16 && a.dk == kD && a.dv == kD && (long long)a.T * a.H * kD * 2 < (1ll << 40);
+}
+
+cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nlaunch) {
+    CUtensorMap mq, mk, mv, mo;
+    if (!make_token_map(&mq, a.q, a.B, a.T, a.H) || !make_token_map(&mk, a.k, a.B, a.T, a.H) ||
+        !make_token_map(&mv, a.v, a.B, a.T, a.H) || !make_token_map(&mo, a.o, a.B, a.T, a.H))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(qdelta_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    TcParams p{(const __nv_bfloat16 *)a.alpha, (const __nv_bfloat16 *)a.beta, (const __nv_bfloat16 *)a.lam,
+               a.S0, a.S_final, a.B, a.T, a.H};
+    qdelta_fwd_tc_kernel<<<a.B * a.H, kThreads, kSmemBytes, s>>>(p, mq, mk, mv, mo);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) *nlaunch += 1;
+    return e;
+}
+
+bool tc_read_and_clear_timeout() {
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_tc_timeout, sizeof v) != cudaSuccess) return false;
+    if (v) cudaMemcpyToSymbol(g_tc_timeout, &zero, sizeof zero);
+    return v != 0;
+}
+
+}  // namespace qd

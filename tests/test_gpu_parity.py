@@ -114,6 +114,15 @@ def test_head_dims_fp32(qd, dk, dv):
     check(S, S_ref, "f32", f"dk={dk} dv={dv} S")
 
 
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 64), (64, 128)])
+def test_head_dims_bf16(qd, dk, dv):
+    d = synth.qdelta_inputs(2, 150, 2, dk, dv, seed=45 + dk + dv, dtype="bf16", mode="qdelta", s0_var=0.01)
+    o, S = run_qdelta(qd, d)
+    o_ref, S_ref = oracle.qdelta_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["lam"], d["S0"])
+    check(o, o_ref, "bf16", f"dk={dk} dv={dv} o")
+    check(S, S_ref, "bf16", f"dk={dk} dv={dv} S")
+
+
 @pytest.mark.parametrize("mode", ["qdelta", "gdn", "deltanet"])
 def test_layer_1p3b_full_size_sampled(qd, mode):
     """B=8, H=16, T=2048, d=128 bf16: the benchmarked workload; 6 streams checked."""
