@@ -14,8 +14,9 @@
 //   O^T    = diag-scaled S Q^T + Z^T P^T,  i.e. o_t = gamma_t S q_t + sum_i P_ti z_i
 //   S     <- gamma_C S + Z^T diag(kappa) K
 // Every product is written "transposed" so that the 128 TMEM lanes index d_v (or
-// d_k) and every MMA has M = 128.  The master state stays in registers in fp32;
-// its bf16 copy in shared memory feeds the MMAs.
+// d_k) and every MMA has M = 128.  The master state stays in TMEM in fp32 (the
+// MMA accumulates Z^T (kappa K) onto it after the epilogue has scaled it by the
+// chunk's gamma_C); its bf16 copy in shared memory feeds the MMAs.
 //
 // Shared memory (offsets from a 1024-aligned base):
 //   stage s in {0,1}: XQ 32 KB (per 64-column panel: X rows 0-63 | Q rows 64-127),
@@ -26,7 +27,7 @@
 //   P     8 KB   bf16 [64][64]
 // All MMA operands use the 128-byte swizzle (TMA layout): 128-byte rows, 8-row
 // groups 1024 bytes apart, 64-column panels.
-// TMEM (512 columns): G 0-63, O1 64-127, U/Z 128-191, W 192-255, O2 256-319, dS 320-447.
+// TMEM (512 columns): G 0-63, O1 64-127, U/Z 128-191, W 192-255, O2 256-319, S 320-447.
 //
 // Every wait is bounded; on a timeout the kernel sets the library's error word,
 // drains its own copies and MMAs, frees TMEM and returns.
@@ -50,15 +51,15 @@ constexpr uint32_t kStageBytes = 65536;
 constexpr uint32_t OFF_XQ = 0, OFF_K = 32768, OFF_V = 49152;
 constexpr uint32_t OFF_S = 2 * kStageBytes;          // 131072
 constexpr uint32_t OFF_R1 = OFF_S + 32768;           // 163840
-constexpr uint32_t OFF_R2 = OFF_R1 + 17408;          // 181248
+constexpr uint32_t OFF_R2 = OFF_R1 + 17408;          // 181248 (A needs 64 * 68 * 4 = 17408)
 constexpr uint32_t OFF_P = OFF_R2 + 16384;           // 197632
 constexpr uint32_t kSmemUsed = OFF_P + 8192;         // 205824
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
-constexpr int LA = 65;                               // fp32 row stride of A
+constexpr int LA = 68;                               // fp32 row stride of A (16-byte rows)
 constexpr uint32_t kTmaBytes = 3 * kC * kD * 2;      // Q, K, V tiles per chunk
 constexpr uint64_t kWaitNs = 2000000000ull;          // 2 s per wait
 
-constexpr uint32_t TM_G = 0, TM_O1 = 64, TM_U = 128, TM_W = 192, TM_O2 = 256, TM_DS = 320;
+constexpr uint32_t TM_G = 0, TM_O1 = 64, TM_U = 128, TM_W = 192, TM_O2 = 256, TM_S = 320;
 
 struct TcParams {
     const __nv_bfloat16 *alpha, *beta, *lam;
@@ -96,7 +97,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     __shared__ uint64_t bar_full[2], bar_mma;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
-    __shared__ float g_ell[kC], g_beta[kC], g_lam[kC], g_gam[kC], g_kap[kC];
+    __shared__ float g_ell[2][kC], g_beta[2][kC], g_lam[2][kC], g_gam[2][kC], g_kap[2][kC], g_igam[2][kC];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, hf = warp >> 2;          // TMEM lane quarter, column half
@@ -121,30 +122,8 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         tmem_relinquish();
     }
 
-    // master state rows d = 32*q4 + lane, columns 64*hf .. 64*hf+63 (fp32, registers)
+    // this thread's TMEM lane / state row and its 64-column half
     const int d_row = 32 * q4 + lane;
-    float S[64];
-    {
-        const size_t base = ((size_t)bh * kD + d_row) * kD + 64 * hf;
-        if (p.S0) {
-#pragma unroll
-            for (int j = 0; j < 64; j += 4) {
-                float4 v = *reinterpret_cast<const float4 *>(p.S0 + base + j);
-                S[j] = v.x; S[j + 1] = v.y; S[j + 2] = v.z; S[j + 3] = v.w;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 64; ++j) S[j] = 0.f;
-        }
-        uint8_t *sp = sm + OFF_S + hf * 16384;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = S[8 * ch + e];
-            *reinterpret_cast<uint4 *>(sp + sw128_off(d_row, 8 * ch)) = pack8(f);
-        }
-    }
 
     auto issue_loads = [&](int c) {
         const int s = c & 1;
@@ -159,31 +138,97 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         }
     };
 
-    // gates of a chunk: lane l of warp 0 holds tokens 2l and 2l+1
-    float ga[2], gb[2], gl[2];
+    // gates of a chunk: lane l of warp 4 holds tokens 2l and 2l+1.  The loads land in raw
+    // bf16 registers that nothing reads until compute_gates, so they do not stall the warp.
+    __nv_bfloat16 ra[2], rb[2], rl[2];
     auto load_gates = [&](int c) {
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-            const int t = c * kC + 2 * lane + u;
-            const bool ok = t < T;
+            const int t = min(c * kC + 2 * lane + u, T - 1);
             const size_t tok = ((size_t)b * T + t) * H + h;
-            ga[u] = (ok && p.alpha) ? bf(p.alpha[tok]) : 1.f;
-            gb[u] = ok ? bf(p.beta[tok]) : 0.f;
-            gl[u] = (ok && p.lam) ? bf(p.lam[tok]) : 0.f;
+            if (p.alpha) ra[u] = p.alpha[tok];
+            rb[u] = p.beta[tok];
+            if (p.lam) rl[u] = p.lam[tok];
         }
+    };
+    // warp-wide: log-prefix l, gamma = e^l, kappa = e^{l_C - l}, e^{-l} of one chunk into buffer buf
+    auto compute_gates = [&](int c, int buf) {
+        float ga[2], gb[2], gl[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {                  // tokens past T: alpha 1, beta 0, lambda 0
+            const bool ok = c * kC + 2 * lane + u < T;
+            ga[u] = (ok && p.alpha) ? bf(ra[u]) : 1.f;
+            gb[u] = ok ? bf(rb[u]) : 0.f;
+            gl[u] = (ok && p.lam) ? bf(rl[u]) : 0.f;
+        }
+        const float l0 = __logf(ga[0]), l1 = __logf(ga[1]);
+        float sum = l0 + l1;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, sum, off);
+            if (lane >= off) sum += n;
+        }
+        const float e1 = sum, e0 = sum - l1;
+        const float eC = __shfl_sync(0xffffffffu, sum, 31);
+        g_ell[buf][2 * lane] = e0;
+        g_ell[buf][2 * lane + 1] = e1;
+        g_beta[buf][2 * lane] = gb[0];
+        g_beta[buf][2 * lane + 1] = gb[1];
+        g_lam[buf][2 * lane] = gl[0];
+        g_lam[buf][2 * lane + 1] = gl[1];
+        g_gam[buf][2 * lane] = __expf(e0);
+        g_gam[buf][2 * lane + 1] = __expf(e1);
+        g_kap[buf][2 * lane] = __expf(eC - e0);
+        g_kap[buf][2 * lane + 1] = __expf(eC - e1);
+        // exp(l_t - l_i) = gamma_t * exp(-l_i) while exp(-l_C) stays in fp32 range
+        g_igam[buf][2 * lane] = eC > -80.f ? __expf(-e0) : 0.f;
+        g_igam[buf][2 * lane + 1] = eC > -80.f ? __expf(-e1) : 0.f;
     };
 
     if (producer) {
         issue_loads(0);
         if (nchunks > 1) issue_loads(1);
     }
-    if (warp == 0) load_gates(0);
-    fence_proxy_async();
+    if (warp == 4) {
+        load_gates(0);
+        compute_gates(0, 0);
+        if (nchunks > 1) load_gates(1);       // turned into arrays during chunk 0's solve
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = tmem_base;
     const uint32_t tl = tm + ((uint32_t)(32 * q4) << 16);   // this warp's TMEM lane quarter
+    {
+        const size_t base = ((size_t)bh * kD + d_row) * kD + 64 * hf;
+        const float g0 = g_gam[0][kC - 1];
+        uint8_t *sp = sm + OFF_S + hf * 16384;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float sv[32];
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                float4 v = p.S0 ? *reinterpret_cast<const float4 *>(p.S0 + base + 32 * half + j)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                sv[j] = v.x; sv[j + 1] = v.y; sv[j + 2] = v.z; sv[j + 3] = v.w;
+            }
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = sv[8 * ch + e];
+                *reinterpret_cast<uint4 *>(sp + sw128_off(d_row, 32 * half + 8 * ch)) = pack8(f);
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sv[e] *= g0;
+            tmem_st32(tl + TM_S + 64 * hf + 32 * half, sv);
+        }
+        tmem_st_wait();
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
     uint32_t mma_phase = 0;
     bool ok = true;
 
@@ -207,31 +252,11 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         const uint32_t sXQ = sbase + s * kStageBytes + OFF_XQ, sK = sbase + s * kStageBytes + OFF_K;
         const uint32_t sV = sbase + s * kStageBytes + OFF_V, sS = sbase + OFF_S;
         const uint32_t sR1 = sbase + OFF_R1, sR2 = sbase + OFF_R2, sP = sbase + OFF_P;
+        const float *g_ell_c = g_ell[c & 1], *g_beta_c = g_beta[c & 1], *g_lam_c = g_lam[c & 1];
+        const float *g_gam_c = g_gam[c & 1], *g_kap_c = g_kap[c & 1], *g_igam_c = g_igam[c & 1];
 
-        // (1) gates -> log-prefix, gamma, kappa (warp 0); prefetch the next chunk's gates
-        if (warp == 0) {
-            const float l0 = __logf(ga[0]), l1 = __logf(ga[1]);
-            float sum = l0 + l1;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const float n = __shfl_up_sync(0xffffffffu, sum, off);
-                if (lane >= off) sum += n;
-            }
-            const float e1 = sum, e0 = sum - l1;
-            const float eC = __shfl_sync(0xffffffffu, sum, 31);
-            g_ell[2 * lane] = e0;
-            g_ell[2 * lane + 1] = e1;
-            g_beta[2 * lane] = gb[0];
-            g_beta[2 * lane + 1] = gb[1];
-            g_lam[2 * lane] = gl[0];
-            g_lam[2 * lane + 1] = gl[1];
-            g_gam[2 * lane] = __expf(e0);
-            g_gam[2 * lane + 1] = __expf(e1);
-            g_kap[2 * lane] = __expf(eC - e0);
-            g_kap[2 * lane + 1] = __expf(eC - e1);
-            if (c + 1 < nchunks) load_gates(c + 1);
-        }
-        if (producer) tma_store_wait_read0();   // O staging (R2) of the previous chunk is read out
+        // (1) this chunk's tiles; warp 4 starts loading the next chunk's gates
+        if (warp == 4 && c + 1 < nchunks) load_gates(c + 1);
         if (!mbar_wait(&bar_full[s], (uint32_t)((c >> 1) & 1), kWaitNs)) { ok = false; abort_flag = 1; }
         __syncthreads();
         if (abort_flag) break;
@@ -246,7 +271,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             float kf[8], qf[8], xf[8];
             unpack8(*reinterpret_cast<const uint4 *>(st + OFF_K + pnl * 8192 + off), kf);
             unpack8(*reinterpret_cast<const uint4 *>(st + OFF_XQ + pnl * 16384 + 8192 + off), qf);
-            const float lm = g_lam[row];
+            const float lm = g_lam_c[row];
 #pragma unroll
             for (int e = 0; e < 8; ++e) xf[e] = fmaf(lm, qf[e], kf[e]);
             *reinterpret_cast<uint4 *>(st + OFF_XQ + pnl * 16384 + off) = pack8(xf);
@@ -277,25 +302,33 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             float g[32];
             tmem_ld32(tl + TM_G + 32 * hf, g);
             tmem_ld_wait();
+            const bool split = g_ell_c[kC - 1] > -80.f;        // uniform: gamma_t * exp(-l_i) is safe
             if (q4 < 2) {
                 const int t = 32 * q4 + lane;
-                const float lt = g_ell[t], bt = g_beta[t];
-                float *Arow = reinterpret_cast<float *>(sm + OFF_R1) + t * LA;
+                const float lt = g_ell_c[t], bt = g_beta_c[t], bg = bt * g_gam_c[t];
+                float *Arow = reinterpret_cast<float *>(sm + OFF_R1) + t * LA + 32 * hf;
 #pragma unroll
-                for (int cc = 0; cc < 32; ++cc) {
-                    const int i = 32 * hf + cc;
-                    Arow[i] = (i < t) ? bt * __expf(lt - g_ell[i]) * g[cc] : 0.f;
+                for (int c4 = 0; c4 < 8; ++c4) {
+                    float a[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int cc = 4 * c4 + e, i = 32 * hf + cc;
+                        const float v = split ? bg * g_igam_c[i] * g[cc] : bt * __expf(lt - g_ell_c[i]) * g[cc];
+                        a[e] = (i < t) ? v : 0.f;
+                    }
+                    *reinterpret_cast<float4 *>(Arow + 4 * c4) = make_float4(a[0], a[1], a[2], a[3]);
                 }
             } else {
                 const int t = 32 * (q4 - 2) + lane;
-                const float lt = g_ell[t];
+                const float lt = g_ell_c[t], gt = g_gam_c[t];
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                     float f[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int i = 32 * hf + 8 * ch + e;
-                        f[e] = (i <= t) ? __expf(lt - g_ell[i]) * g[8 * ch + e] : 0.f;
+                        const float pv = split ? gt * g_igam_c[i] * g[8 * ch + e] : __expf(lt - g_ell_c[i]) * g[8 * ch + e];
+                        f[e] = (i <= t) ? pv : 0.f;
                     }
                     *reinterpret_cast<uint4 *>(sm + OFF_P + sw128_off(t, 32 * hf + 8 * ch)) = pack8(f);
                 }
@@ -308,65 +341,135 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                 uint4 *pk = reinterpret_cast<uint4 *>(st + OFF_K + off);
                 float kf[8];
                 unpack8(*pk, kf);
-                const float ka = g_kap[row];
+                const float ka = g_kap_c[row];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) kf[e] *= ka;
                 *pk = pack8(kf);
             }
         }
+        if (producer) tma_store_wait_read0();   // R2 (last chunk's O staging) is free for scratch
         tc_fence_before();
         __syncthreads();
 
-        // (5) Tinv = (I + A)^{-1} in place by block doubling: for each pair of diagonal
-        // blocks of size bs, T21 = -T22 (A21 T11).
+        // (5) Tinv = (I + A)^{-1}.  A is fp32 in R1, zero on and above the diagonal.
+        //   a) the four 16x16 diagonal blocks by forward substitution (one column per lane)
+        //   b) 16 -> 32: T10 = -T11 (A10 T00) for the block pairs (0,1) and (2,3)
+        //   c) 32 -> 64: T21 = -T22 (A21 T11) on the two 32x32 halves
+        // Every inverted block keeps only the strict lower part of its inverse (the
+        // unit diagonal is implied, zeros above), so each product is a dense loop:
+        // Y = A21 + A21 T11s and T21 = -(Y + T22s Y).  R2 serves as scratch.
         {
             float *M = reinterpret_cast<float *>(sm + OFF_R1);
-            for (int bs = 1; bs < kC; bs <<= 1) {
-                const int total = 32 * bs;            // (64 / 2bs) pairs x bs^2
-                float y[4];
+            float *Y = reinterpret_cast<float *>(sm + OFF_R2);      // [32][36] fp32 scratch
+            constexpr int LY = 36;
+            if (warp < 4 && lane < 16) {
+                const int base = 16 * warp, j = lane;
+                float t[16];
 #pragma unroll
-                for (int n = 0; n < 4; ++n) {
-                    const int o = tid + kThreads * n;
-                    if (o < total) {
-                        const int pr = o / (bs * bs), rem = o % (bs * bs), r = rem / bs, cc = rem % bs;
-                        const int base = 2 * bs * pr, row = base + bs + r, col = base + cc;
-                        float acc = M[row * LA + col];
-                        for (int k = cc + 1; k < bs; ++k) acc = fmaf(M[row * LA + base + k], M[(base + k) * LA + col], acc);
-                        y[n] = acc;
-                    }
-                }
-                __syncthreads();
+                for (int i = 0; i < 16; ++i) {
+                    const float *Ai = M + (base + i) * LA + base;
+                    float acc = (i == j) ? 1.f : 0.f;
 #pragma unroll
-                for (int n = 0; n < 4; ++n) {
-                    const int o = tid + kThreads * n;
-                    if (o < total) {
-                        const int pr = o / (bs * bs), rem = o % (bs * bs), r = rem / bs, cc = rem % bs;
-                        M[(2 * bs * pr + bs + r) * LA + 2 * bs * pr + cc] = y[n];
+                    for (int m4 = 0; m4 < (i + 3) / 4; ++m4) {
+                        const float4 a = *reinterpret_cast<const float4 *>(Ai + 4 * m4);
+                        if (4 * m4 + 0 < i) acc = fmaf(-a.x, t[4 * m4 + 0], acc);
+                        if (4 * m4 + 1 < i) acc = fmaf(-a.y, t[4 * m4 + 1], acc);
+                        if (4 * m4 + 2 < i) acc = fmaf(-a.z, t[4 * m4 + 2], acc);
+                        if (4 * m4 + 3 < i) acc = fmaf(-a.w, t[4 * m4 + 3], acc);
                     }
+                    t[i] = acc;
                 }
-                __syncthreads();
+                __syncwarp(0x0000ffffu);
 #pragma unroll
-                for (int n = 0; n < 4; ++n) {
-                    const int o = tid + kThreads * n;
-                    if (o < total) {
-                        const int pr = o / (bs * bs), rem = o % (bs * bs), r = rem / bs, cc = rem % bs;
-                        const int base = 2 * bs * pr, row = base + bs + r, col = base + cc;
-                        float acc = M[row * LA + col];
-                        for (int k = 0; k < r; ++k) acc = fmaf(M[row * LA + base + bs + k], M[(base + bs + k) * LA + col], acc);
-                        y[n] = -acc;
-                    }
-                }
-                __syncthreads();
-#pragma unroll
-                for (int n = 0; n < 4; ++n) {
-                    const int o = tid + kThreads * n;
-                    if (o < total) {
-                        const int pr = o / (bs * bs), rem = o % (bs * bs), r = rem / bs, cc = rem % bs;
-                        M[(2 * bs * pr + bs + r) * LA + 2 * bs * pr + cc] = y[n];
-                    }
-                }
-                __syncthreads();
+                for (int i = 1; i < 16; ++i)
+                    if (i > j) M[(base + i) * LA + base + j] = t[i];
             }
+            if (warp == 4 && c + 1 < nchunks) compute_gates(c + 1, (c + 1) & 1);
+            __syncthreads();
+            // Y = L + L Rs (+= into out) for n x n blocks: thread owns rows r, r+n/2 and 4 columns.
+            // 16 -> 32: both pairs at once (threads 0..63 pair 0, 64..127 pair 1), 2x4 outputs each
+            if (tid < 128) {
+                const int pr = tid >> 6, u = tid & 63, r = u >> 2, c = 4 * (u & 3), base = 32 * pr;
+                const float *L0 = M + (base + 16 + r) * LA + base;        // A10 row r
+                float y[4];
+                {
+                    const float4 l0 = *reinterpret_cast<const float4 *>(L0 + c);
+                    y[0] = l0.x; y[1] = l0.y; y[2] = l0.z; y[3] = l0.w;
+                }
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const float4 a = *reinterpret_cast<const float4 *>(L0 + 4 * k4);
+                    const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 tr = *reinterpret_cast<const float4 *>(M + (base + 4 * k4 + e) * LA + base + c);
+                        y[0] = fmaf(av[e], tr.x, y[0]); y[1] = fmaf(av[e], tr.y, y[1]);
+                        y[2] = fmaf(av[e], tr.z, y[2]); y[3] = fmaf(av[e], tr.w, y[3]);
+                    }
+                }
+                *reinterpret_cast<float4 *>(Y + (16 * pr + r) * LY + c) = make_float4(y[0], y[1], y[2], y[3]);
+            }
+            __syncthreads();
+            if (tid < 128) {                                     // T10 = -(Y + T11s Y)
+                const int pr = tid >> 6, u = tid & 63, r = u >> 2, c = 4 * (u & 3), base = 32 * pr;
+                const float *T0 = M + (base + 16 + r) * LA + base + 16;
+                const float *Yp = Y + 16 * pr * LY;
+                float y[4];
+                {
+                    const float4 y0 = *reinterpret_cast<const float4 *>(Yp + r * LY + c);
+                    y[0] = y0.x; y[1] = y0.y; y[2] = y0.z; y[3] = y0.w;
+                }
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const float4 a = *reinterpret_cast<const float4 *>(T0 + 4 * k4);
+                    const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 yr = *reinterpret_cast<const float4 *>(Yp + (4 * k4 + e) * LY + c);
+                        y[0] = fmaf(av[e], yr.x, y[0]); y[1] = fmaf(av[e], yr.y, y[1]);
+                        y[2] = fmaf(av[e], yr.z, y[2]); y[3] = fmaf(av[e], yr.w, y[3]);
+                    }
+                }
+                *reinterpret_cast<float4 *>(M + (base + 16 + r) * LA + base + c) = make_float4(-y[0], -y[1], -y[2], -y[3]);
+            }
+            __syncthreads();
+            // 32 -> 64: row r of the 32x32 blocks, columns c..c+3 (256 threads)
+            {
+                const int r = tid >> 3, c = 4 * (tid & 7);
+                const float *L0 = M + (32 + r) * LA;                     // A21 row r
+                float y0[4];
+                {
+                    const float4 a0 = *reinterpret_cast<const float4 *>(L0 + c);
+                    y0[0] = a0.x; y0[1] = a0.y; y0[2] = a0.z; y0[3] = a0.w;
+                }
+#pragma unroll
+                for (int k4 = 0; k4 < 8; ++k4) {                 // Y = A21 + A21 T11s
+                    const float4 a0 = *reinterpret_cast<const float4 *>(L0 + 4 * k4);
+                    const float av0[4] = {a0.x, a0.y, a0.z, a0.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 tr = *reinterpret_cast<const float4 *>(M + (4 * k4 + e) * LA + c);
+                        y0[0] = fmaf(av0[e], tr.x, y0[0]); y0[1] = fmaf(av0[e], tr.y, y0[1]);
+                        y0[2] = fmaf(av0[e], tr.z, y0[2]); y0[3] = fmaf(av0[e], tr.w, y0[3]);
+                    }
+                }
+                *reinterpret_cast<float4 *>(Y + r * LY + c) = make_float4(y0[0], y0[1], y0[2], y0[3]);
+                __syncthreads();
+                const float *T0 = L0 + 32;                                // T22s row r
+#pragma unroll
+                for (int k4 = 0; k4 < 8; ++k4) {                 // T21 = -(Y + T22s Y)
+                    const float4 a0 = *reinterpret_cast<const float4 *>(T0 + 4 * k4);
+                    const float av0[4] = {a0.x, a0.y, a0.z, a0.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 yr = *reinterpret_cast<const float4 *>(Y + (4 * k4 + e) * LY + c);
+                        y0[0] = fmaf(av0[e], yr.x, y0[0]); y0[1] = fmaf(av0[e], yr.y, y0[1]);
+                        y0[2] = fmaf(av0[e], yr.z, y0[2]); y0[3] = fmaf(av0[e], yr.w, y0[3]);
+                    }
+                }
+                *reinterpret_cast<float4 *>(M + (32 + r) * LA + c) = make_float4(-y0[0], -y0[1], -y0[2], -y0[3]);
+            }
+            __syncthreads();
             // Tinv*beta and Tinv*beta*gamma as bf16 [64][64] (128B swizzle) over R1
             float tv[2][8];
             int rows[2], chs[2];
@@ -388,8 +491,8 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int j = 8 * chs[n] + e;
-                    f1[e] = tv[n][e] * g_beta[j];
-                    f2[e] = f1[e] * g_gam[j];
+                    f1[e] = tv[n][e] * g_beta_c[j];
+                    f2[e] = f1[e] * g_gam_c[j];
                 }
                 *reinterpret_cast<uint4 *>(sm + OFF_R1 + sw128_off(rows[n], 8 * chs[n])) = pack8(f1);
                 *reinterpret_cast<uint4 *>(sm + OFF_R1 + 8192 + sw128_off(rows[n], 8 * chs[n])) = pack8(f2);
@@ -453,7 +556,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         }
         sync_for_mma();
 
-        // (10) O2 = Z^T P^T ; dS = Z^T (kappa K)
+        // (10) O2 = Z^T P^T ; S += Z^T (kappa K)  (S in TMEM already scaled by gamma_C)
         if (issuer) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -461,13 +564,13 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                           idesc_bf16(128, 64, false, false), k > 0);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                umma_bf16(tm + TM_DS, smem_desc(sR2 + k * 32, 16, 1024), smem_desc(sK + k * 2048, 8192, 1024),
-                          idesc_bf16(128, 128, false, true), k > 0);
+                umma_bf16(tm + TM_S, smem_desc(sR2 + k * 32, 16, 1024), smem_desc(sK + k * 2048, 8192, 1024),
+                          idesc_bf16(128, 128, false, true), 1);
             umma_commit(&bar_mma);
         }
         wait_mma();
 
-        // (11) o = gamma_t O1 + O2 -> staging (R2) ; S = gamma_C S + dS -> registers and bf16 S_in
+        // (11) o = gamma_t O1 + O2 -> staging (R2); state -> bf16 S_in
         {
             float o1[32], o2[32];
             tmem_ld32(tl + TM_O1 + 32 * hf, o1);
@@ -478,25 +581,36 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             for (int cc = 0; cc < 32; ++cc) {
                 const int t = 32 * hf + cc;
                 *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(t, d_row & 63)) =
-                    __float2bfloat16_rn(fmaf(g_gam[t], o1[cc], o2[cc]));
+                    __float2bfloat16_rn(fmaf(g_gam_c[t], o1[cc], o2[cc]));
             }
-            const float gC = g_gam[kC - 1];
+            // state: bf16 copy for the next chunk's MMAs; rescale by the next chunk's gamma_C
+            // in TMEM, or write the final state after the last chunk
+            const bool last = (c + 1 == nchunks);
+            const float gN = last ? 1.f : g_gam[(c + 1) & 1][kC - 1];
             uint8_t *sp = sm + OFF_S + hf * 16384;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                float ds[32];
-                tmem_ld32(tl + TM_DS + 64 * hf + 32 * half, ds);
+                float sv[32];
+                tmem_ld32(tl + TM_S + 64 * hf + 32 * half, sv);
                 tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) S[32 * half + e] = fmaf(gC, S[32 * half + e], ds[e]);
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                     float f[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = S[32 * half + 8 * ch + e];
+                    for (int e = 0; e < 8; ++e) f[e] = sv[8 * ch + e];
                     *reinterpret_cast<uint4 *>(sp + sw128_off(d_row, 32 * half + 8 * ch)) = pack8(f);
                 }
+                if (!last) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) sv[e] *= gN;
+                    tmem_st32(tl + TM_S + 64 * hf + 32 * half, sv);
+                } else if (p.S_final && !abort_flag) {
+                    float *dst = p.S_final + ((size_t)bh * kD + d_row) * kD + 64 * hf + 32 * half;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+                }
             }
+            tmem_st_wait();
         }
         sync_for_mma();
         if (producer) {
@@ -507,12 +621,6 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         }
     }
 
-    // final state
-    if (ok && !abort_flag && p.S_final) {
-        float *dst = p.S_final + ((size_t)bh * kD + d_row) * kD + 64 * hf;
-#pragma unroll
-        for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
-    }
     if (producer) {
         tma_store_wait_all();
         if (abort_flag) {
