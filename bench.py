@@ -150,14 +150,20 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device="cuda"):
+    """Max of a per-rank scalar over all ranks (the slowest rank's time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_tokens_per_s(ms_per_step, world):
+    """Whole-job throughput: every rank processes its own B*T-token batch per step."""
+    return B * T * world / (ms_per_step * 1e-3)
 
 
 def to_dev(x, dtype):
@@ -377,7 +383,7 @@ def main():
     sampler.stop()
     clocks = sampler.summary(tw0, tw1)
     ms_step = max_over_ranks(total_ms / args.steps, world)
-    value = B * T * world / (ms_step * 1e-3)
+    value = job_tokens_per_s(ms_step, world)
     launch_ms = max_over_ranks(launch_ms, world)
     achieved_gbs = ALG_BYTES / (launch_ms * 1e-3) / 1e9
     achieved_tf = ALG_FLOPS / (launch_ms * 1e-3) / 1e12
