@@ -110,7 +110,8 @@ qd_status qed_fwd(const void *q, const void *k, const void *v, const void *g, co
     if (B == 0 || H == 0) { g_launches = 0; return QD_OK; }
     if (T == 0) { g_launches = 0; return empty_sequence(S0, S_final, B, H, dk, dv, stream); }
     qd::QedArgs a{q, k, v, g, b, w, lam_h, S0, o, S_final, B, T, H, dk, dv, workspace, workspace_bytes};
-    cudaError_t e = qd::launch_qed_chunk_simt(a, dtype, stream, &n);
+    cudaError_t e = qd::qed_tc_supported(a, dtype) ? qd::launch_qed_chunk_tc(a, stream, &n)
+                                                   : qd::launch_qed_chunk_simt(a, dtype, stream, &n);
     if (e != cudaSuccess) return cuda_fail(e, "qed_fwd launch");
     g_launches = n;
     return QD_OK;
@@ -146,7 +147,8 @@ qd_status qd_device_status(cudaStream_t stream) {
     g_err[0] = 0;
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "qd_device_status");
-    if (qd::tc_read_and_clear_timeout())
+    const bool t1 = qd::tc_read_and_clear_timeout(), t2 = qd::qed_tc_read_and_clear_timeout();
+    if (t1 || t2)
         return fail(QD_ERR_TIMEOUT, "a tensor-core kernel gave up a bounded wait (results of that call are invalid)");
     return QD_OK;
 }

@@ -37,6 +37,7 @@
 
 #include "qd_internal.cuh"
 #include "sm103_ptx.cuh"
+#include "tc_common.cuh"
 
 namespace qd {
 
@@ -45,8 +46,8 @@ __device__ unsigned int g_tc_timeout = 0;
 namespace {
 
 using namespace ptx;
+using namespace tc;
 
-constexpr int kC = 64, kD = 128, kThreads = 256;
 constexpr uint32_t kStageBytes = 65536;
 constexpr uint32_t OFF_XQ = 0, OFF_K = 32768, OFF_V = 49152;
 constexpr uint32_t OFF_S = 2 * kStageBytes;          // 131072
@@ -55,7 +56,6 @@ constexpr uint32_t OFF_R2 = OFF_R1 + 17408;          // 181248 (A needs 64 * 68 
 constexpr uint32_t OFF_P = OFF_R2 + 16384;           // 197632
 constexpr uint32_t kSmemUsed = OFF_P + 8192;         // 205824
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
-constexpr int LA = 68;                               // fp32 row stride of A (16-byte rows)
 constexpr uint32_t kTmaBytes = 3 * kC * kD * 2;      // Q, K, V tiles per chunk
 constexpr uint64_t kWaitNs = 2000000000ull;          // 2 s per wait
 
@@ -67,26 +67,6 @@ struct TcParams {
     float *S_final;
     int B, T, H;
 };
-
-__device__ __forceinline__ float bf(__nv_bfloat16 x) { return __bfloat162float(x); }
-
-__device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
-    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float2 t = __bfloat1622float2(h[i]);
-        f[2 * i] = t.x;
-        f[2 * i + 1] = t.y;
-    }
-}
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
-    uint4 u;
-    u.x = pack_bf16x2(f[0], f[1]);
-    u.y = pack_bf16x2(f[2], f[3]);
-    u.z = pack_bf16x2(f[4], f[5]);
-    u.w = pack_bf16x2(f[6], f[7]);
-    return u;
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
 qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
@@ -359,144 +339,10 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         // unit diagonal is implied, zeros above), so each product is a dense loop:
         // Y = A21 + A21 T11s and T21 = -(Y + T22s Y).  R2 serves as scratch.
         {
-            float *M = reinterpret_cast<float *>(sm + OFF_R1);
-            float *Y = reinterpret_cast<float *>(sm + OFF_R2);      // [32][36] fp32 scratch
-            constexpr int LY = 36;
-            if (warp < 4 && lane < 16) {
-                const int base = 16 * warp, j = lane;
-                float t[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float *Ai = M + (base + i) * LA + base;
-                    float acc = (i == j) ? 1.f : 0.f;
-#pragma unroll
-                    for (int m4 = 0; m4 < (i + 3) / 4; ++m4) {
-                        const float4 a = *reinterpret_cast<const float4 *>(Ai + 4 * m4);
-                        if (4 * m4 + 0 < i) acc = fmaf(-a.x, t[4 * m4 + 0], acc);
-                        if (4 * m4 + 1 < i) acc = fmaf(-a.y, t[4 * m4 + 1], acc);
-                        if (4 * m4 + 2 < i) acc = fmaf(-a.z, t[4 * m4 + 2], acc);
-                        if (4 * m4 + 3 < i) acc = fmaf(-a.w, t[4 * m4 + 3], acc);
-                    }
-                    t[i] = acc;
-                }
-                __syncwarp(0x0000ffffu);
-#pragma unroll
-                for (int i = 1; i < 16; ++i)
-                    if (i > j) M[(base + i) * LA + base + j] = t[i];
-            }
-            if (warp == 4 && c + 1 < nchunks) compute_gates(c + 1, (c + 1) & 1);
-            __syncthreads();
-            // Y = L + L Rs (+= into out) for n x n blocks: thread owns rows r, r+n/2 and 4 columns.
-            // 16 -> 32: both pairs at once (threads 0..63 pair 0, 64..127 pair 1), 2x4 outputs each
-            if (tid < 128) {
-                const int pr = tid >> 6, u = tid & 63, r = u >> 2, c = 4 * (u & 3), base = 32 * pr;
-                const float *L0 = M + (base + 16 + r) * LA + base;        // A10 row r
-                float y[4];
-                {
-                    const float4 l0 = *reinterpret_cast<const float4 *>(L0 + c);
-                    y[0] = l0.x; y[1] = l0.y; y[2] = l0.z; y[3] = l0.w;
-                }
-#pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                    const float4 a = *reinterpret_cast<const float4 *>(L0 + 4 * k4);
-                    const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float4 tr = *reinterpret_cast<const float4 *>(M + (base + 4 * k4 + e) * LA + base + c);
-                        y[0] = fmaf(av[e], tr.x, y[0]); y[1] = fmaf(av[e], tr.y, y[1]);
-                        y[2] = fmaf(av[e], tr.z, y[2]); y[3] = fmaf(av[e], tr.w, y[3]);
-                    }
-                }
-                *reinterpret_cast<float4 *>(Y + (16 * pr + r) * LY + c) = make_float4(y[0], y[1], y[2], y[3]);
-            }
-            __syncthreads();
-            if (tid < 128) {                                     // T10 = -(Y + T11s Y)
-                const int pr = tid >> 6, u = tid & 63, r = u >> 2, c = 4 * (u & 3), base = 32 * pr;
-                const float *T0 = M + (base + 16 + r) * LA + base + 16;
-                const float *Yp = Y + 16 * pr * LY;
-                float y[4];
-                {
-                    const float4 y0 = *reinterpret_cast<const float4 *>(Yp + r * LY + c);
-                    y[0] = y0.x; y[1] = y0.y; y[2] = y0.z; y[3] = y0.w;
-                }
-#pragma unroll
-                for (int k4 = 0; k4 < 4; ++k4) {
-                    const float4 a = *reinterpret_cast<const float4 *>(T0 + 4 * k4);
-                    const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float4 yr = *reinterpret_cast<const float4 *>(Yp + (4 * k4 + e) * LY + c);
-                        y[0] = fmaf(av[e], yr.x, y[0]); y[1] = fmaf(av[e], yr.y, y[1]);
-                        y[2] = fmaf(av[e], yr.z, y[2]); y[3] = fmaf(av[e], yr.w, y[3]);
-                    }
-                }
-                *reinterpret_cast<float4 *>(M + (base + 16 + r) * LA + base + c) = make_float4(-y[0], -y[1], -y[2], -y[3]);
-            }
-            __syncthreads();
-            // 32 -> 64: row r of the 32x32 blocks, columns c..c+3 (256 threads)
-            {
-                const int r = tid >> 3, c = 4 * (tid & 7);
-                const float *L0 = M + (32 + r) * LA;                     // A21 row r
-                float y0[4];
-                {
-                    const float4 a0 = *reinterpret_cast<const float4 *>(L0 + c);
-                    y0[0] = a0.x; y0[1] = a0.y; y0[2] = a0.z; y0[3] = a0.w;
-                }
-#pragma unroll
-                for (int k4 = 0; k4 < 8; ++k4) {                 // Y = A21 + A21 T11s
-                    const float4 a0 = *reinterpret_cast<const float4 *>(L0 + 4 * k4);
-                    const float av0[4] = {a0.x, a0.y, a0.z, a0.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float4 tr = *reinterpret_cast<const float4 *>(M + (4 * k4 + e) * LA + c);
-                        y0[0] = fmaf(av0[e], tr.x, y0[0]); y0[1] = fmaf(av0[e], tr.y, y0[1]);
-                        y0[2] = fmaf(av0[e], tr.z, y0[2]); y0[3] = fmaf(av0[e], tr.w, y0[3]);
-                    }
-                }
-                *reinterpret_cast<float4 *>(Y + r * LY + c) = make_float4(y0[0], y0[1], y0[2], y0[3]);
-                __syncthreads();
-                const float *T0 = L0 + 32;                                // T22s row r
-#pragma unroll
-                for (int k4 = 0; k4 < 8; ++k4) {                 // T21 = -(Y + T22s Y)
-                    const float4 a0 = *reinterpret_cast<const float4 *>(T0 + 4 * k4);
-                    const float av0[4] = {a0.x, a0.y, a0.z, a0.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float4 yr = *reinterpret_cast<const float4 *>(Y + (4 * k4 + e) * LY + c);
-                        y0[0] = fmaf(av0[e], yr.x, y0[0]); y0[1] = fmaf(av0[e], yr.y, y0[1]);
-                        y0[2] = fmaf(av0[e], yr.z, y0[2]); y0[3] = fmaf(av0[e], yr.w, y0[3]);
-                    }
-                }
-                *reinterpret_cast<float4 *>(M + (32 + r) * LA + c) = make_float4(-y0[0], -y0[1], -y0[2], -y0[3]);
-            }
-            __syncthreads();
-            // Tinv*beta and Tinv*beta*gamma as bf16 [64][64] (128B swizzle) over R1
-            float tv[2][8];
-            int rows[2], chs[2];
-#pragma unroll
-            for (int n = 0; n < 2; ++n) {
-                const int u = tid + kThreads * n;          // 512 chunks of 8
-                rows[n] = u >> 3;
-                chs[n] = u & 7;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int j = 8 * chs[n] + e;
-                    tv[n][e] = (j < rows[n]) ? M[rows[n] * LA + j] : (j == rows[n] ? 1.f : 0.f);
-                }
-            }
-            __syncthreads();
-#pragma unroll
-            for (int n = 0; n < 2; ++n) {
-                float f1[8], f2[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int j = 8 * chs[n] + e;
-                    f1[e] = tv[n][e] * g_beta_c[j];
-                    f2[e] = f1[e] * g_gam_c[j];
-                }
-                *reinterpret_cast<uint4 *>(sm + OFF_R1 + sw128_off(rows[n], 8 * chs[n])) = pack8(f1);
-                *reinterpret_cast<uint4 *>(sm + OFF_R1 + 8192 + sw128_off(rows[n], 8 * chs[n])) = pack8(f2);
-            }
+            unit_lower_inverse(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_R2),
+                               sm + OFF_R1, sm + OFF_R1 + 8192, g_beta_c, g_gam_c, [&]() {
+                                   if (warp == 4 && c + 1 < nchunks) compute_gates(c + 1, (c + 1) & 1);
+                               });
         }
         sync_for_mma();
 
@@ -638,37 +484,6 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 512);
-}
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
-                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
-                                  CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void *f = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(f);
-    }
-    return fn;
-}
-
-// [B][T][H][128] bf16 tensor, boxes of 64 columns x 64 tokens of one head.
-bool make_token_map(CUtensorMap *m, const void *ptr, int B, int T, int H) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)B};
-    cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2, (cuuint64_t)T * H * kD * 2};
-    cuuint32_t box[4] = {64, 1, (cuuint32_t)kC, 1};
-    cuuint32_t es[4] = {1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace

@@ -59,7 +59,11 @@ cudaError_t launch_qdelta_step(const StepArgs &a, int dtype, cudaStream_t s, int
 // Tensor-core (tcgen05) chunked Q-Delta forward: bf16, dk = dv = 128.
 bool qdelta_tc_supported(const QDeltaArgs &a, int dtype);
 cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nlaunch);
+// Tensor-core (tcgen05) chunked QED forward: bf16, dk = dv = 128.
+bool qed_tc_supported(const QedArgs &a, int dtype);
+cudaError_t launch_qed_chunk_tc(const QedArgs &a, cudaStream_t s, int *nlaunch);
 // Reads and clears the device word the tensor-core kernels set when a bounded wait runs out.
 bool tc_read_and_clear_timeout();
+bool qed_tc_read_and_clear_timeout();
 
 }  // namespace qd

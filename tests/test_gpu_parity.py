@@ -194,6 +194,41 @@ def test_qed_small_all_outputs(qd, T, dt):
     check(S, S_ref, dt, f"qed T={T} S")
 
 
+@pytest.mark.parametrize("dk,dv", [(64, 64), (128, 64)])
+def test_qed_head_dims_bf16(qd, dk, dv):
+    d = synth.qed_inputs(2, 150, 2, dk, dv, seed=75 + dk + dv, dtype="bf16", s0_var=0.01)
+    o, S = run_qed(qd, d)
+    o_ref, S_ref = oracle.qed_fwd(d["q"], d["k"], d["v"], d["g"], d["b"], d["w"], d["lam_h"], d["S0"])
+    check(o, o_ref, "bf16", f"qed dk={dk} dv={dv} o")
+    check(S, S_ref, "bf16", f"qed dk={dk} dv={dv} S")
+
+
+def test_qed_strong_decay(qd):
+    """Per-channel log-decay near -0.5 per token (about -32 summed over a chunk): the
+    factored decay of the tensor-core kernel still inside its fp32 range."""
+    d = synth.qed_inputs(2, 200, 2, 128, 128, seed=78, dtype="bf16", g_mu=-0.3, s0_var=0.01)
+    o, S = run_qed(qd, d)
+    o_ref, S_ref = oracle.qed_fwd(d["q"], d["k"], d["v"], d["g"], d["b"], d["w"], d["lam_h"], d["S0"])
+    check(o, o_ref, "bf16", "qed strong decay o")
+    check(S, S_ref, "bf16", "qed strong decay S")
+
+
+def test_qed_split_call_carries_state_in_place(qd):
+    d = synth.qed_inputs(2, 300, 2, 128, 128, seed=79, dtype="bf16", s0_var=0.01)
+    bf = torch.bfloat16
+    o_ref, S_ref = oracle.qed_fwd(d["q"], d["k"], d["v"], d["g"], d["b"], d["w"], d["lam_h"], d["S0"])
+    S = dev(d["S0"], torch.float32)
+    outs = []
+    for a, b in ((0, 130), (130, 300)):
+        sl = lambda x: x[:, a:b]
+        o, _ = qd.qed_fwd(dev(sl(d["q"]), bf), dev(sl(d["k"]), bf), dev(sl(d["v"]), bf), dev(sl(d["g"]), bf),
+                          dev(sl(d["b"]), bf), dev(sl(d["w"]), bf), dev(d["lam_h"], torch.float32), S, S_final=S)
+        outs.append(o.float().cpu().numpy())
+    torch.cuda.synchronize()
+    check(np.concatenate(outs, axis=1), o_ref, "bf16", "qed split o")
+    check(S.cpu().numpy(), S_ref, "bf16", "qed split S")
+
+
 def test_qed_lambda_zero_is_gdn2(qd):
     """lam_h = 0 reduces QED to GDN-2; compared with the oracle at lam_h = 0."""
     d = synth.qed_inputs(1, 150, 2, 64, 64, seed=80, dtype="f32")
