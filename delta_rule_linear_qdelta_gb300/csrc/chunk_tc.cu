@@ -8,29 +8,39 @@
 // gamma_i = e^{l_i}, kappa_i = e^{l_C - l_i}, X = K + diag(lambda) Q:
 //   G      = [X; Q] K^T                                   (one M=128 MMA)
 //   A      = strictly_lower(beta_t e^{l_t - l_i} (X K^T)_ti);  P = incl_lower(e^{l_t-l_i} (Q K^T)_ti)
-//   Tinv   = (I + A)^{-1}                                  (block-doubling solve, fp32)
+//   Tinv   = (I + A)^{-1}                                  (fp32, tc_common.cuh)
 //   U^T    = V^T (Tinv diag(beta))^T;   W^T = X^T (Tinv diag(beta gamma))^T
 //   Z^T    = U^T - S W^T                                   (S = state entering the chunk)
-//   O^T    = diag-scaled S Q^T + Z^T P^T,  i.e. o_t = gamma_t S q_t + sum_i P_ti z_i
+//   o_t    = gamma_t (S Q^T)_t + (Z^T P^T)_t
 //   S     <- gamma_C S + Z^T diag(kappa) K
 // Every product is written "transposed" so that the 128 TMEM lanes index d_v (or
-// d_k) and every MMA has M = 128.  The master state stays in TMEM in fp32 (the
-// MMA accumulates Z^T (kappa K) onto it after the epilogue has scaled it by the
-// chunk's gamma_C); its bf16 copy in shared memory feeds the MMAs.
+// d_k) and every MMA has M = 128.  The master state stays in TMEM in fp32 (the MMA
+// accumulates Z^T (kappa K) onto it after the epilogue has scaled it by the chunk's
+// gamma_C); its bf16 copy in shared memory feeds the MMAs.
+//
+// Software pipeline: the state-independent work of chunk c+1 (X, its Gram, the
+// masks, the solve, U and W) is interleaved with the state chain of chunk c
+// (Z, the output and state products, the epilogue) so that each MMA's latency is
+// covered by thread work of the other chunk:
+//   issue Z(c) | X(c+1), issue G(c+1) | wait Z(c), Z^T(c) -> smem, issue O2/S(c)
+//   | wait G(c+1), masks(c+1) | solve(c+1), issue U/W(c+1) | wait O2/S(c), epilogue(c)
+//   | issue O1(c+1) | wait U/W(c+1), -W(c+1) -> smem
+// Each commit has its own mbarrier (one phase per chunk).
 //
 // Shared memory (offsets from a 1024-aligned base):
 //   stage s in {0,1}: XQ 32 KB (per 64-column panel: X rows 0-63 | Q rows 64-127),
 //                     K 16 KB (overwritten in place by kappa*K), V 16 KB
 //   S_in 32 KB   bf16 state [dv][dk]
-//   R1   17 KB   A/Tinv fp32 [64][65]  ->  Tinv*beta, Tinv*beta*gamma (bf16)
-//   R2   16 KB   -W [64][dk]  ->  Z^T [dv][64]  ->  O staging [64][dv]
-//   P     8 KB   bf16 [64][64]
+//   R1   17 KB   A fp32 [64][68]  ->  Tinv*beta, Tinv*beta*gamma (bf16)
+//   R2   16 KB   -W [64][dk]  ->  Z^T [dv][64]
+//   P    2x8 KB  bf16 [64][64], by chunk parity
+//   Y     5 KB   solve scratch
 // All MMA operands use the 128-byte swizzle (TMA layout): 128-byte rows, 8-row
 // groups 1024 bytes apart, 64-column panels.
 // TMEM (512 columns): G 0-63, O1 64-127, U/Z 128-191, W 192-255, O2 256-319, S 320-447.
 //
 // Every wait is bounded; on a timeout the kernel sets the library's error word,
-// drains its own copies and MMAs, frees TMEM and returns.
+// waits (bounded) for its own copies and MMAs, frees TMEM and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -52,9 +62,10 @@ constexpr uint32_t kStageBytes = 65536;
 constexpr uint32_t OFF_XQ = 0, OFF_K = 32768, OFF_V = 49152;
 constexpr uint32_t OFF_S = 2 * kStageBytes;          // 131072
 constexpr uint32_t OFF_R1 = OFF_S + 32768;           // 163840
-constexpr uint32_t OFF_R2 = OFF_R1 + 17408;          // 181248 (A needs 64 * 68 * 4 = 17408)
-constexpr uint32_t OFF_P = OFF_R2 + 16384;           // 197632
-constexpr uint32_t kSmemUsed = OFF_P + 8192;         // 205824
+constexpr uint32_t OFF_R2 = OFF_R1 + 17408;          // 181248
+constexpr uint32_t OFF_P = OFF_R2 + 16384;           // 197632 (two 8 KB buffers)
+constexpr uint32_t OFF_Y = OFF_P + 16384;            // 214016
+constexpr uint32_t kSmemUsed = OFF_Y + 5120;         // 219136
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
 constexpr uint32_t kTmaBytes = 3 * kC * kD * 2;      // Q, K, V tiles per chunk
 constexpr uint64_t kWaitNs = 2000000000ull;          // 2 s per wait
@@ -64,20 +75,22 @@ constexpr uint32_t TM_G = 0, TM_O1 = 64, TM_U = 128, TM_W = 192, TM_O2 = 256, TM
 struct TcParams {
     const __nv_bfloat16 *alpha, *beta, *lam;
     const float *S0;
+    __nv_bfloat16 *o;
     float *S_final;
     int B, T, H;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
 qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
-                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                     const __grid_constant__ CUtensorMap tmO) {
+                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t bar_full[2], bar_mma;
+    // one mbarrier per TMA stage and per kind of MMA commit (each completes once per chunk)
+    __shared__ uint64_t bar_full[2], bar_z, bar_g, bar_o2, bar_uw;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
-    __shared__ float g_ell[2][kC], g_beta[2][kC], g_lam[2][kC], g_gam[2][kC], g_kap[2][kC], g_igam[2][kC];
+    // per-chunk gate arrays, by chunk index mod 3
+    __shared__ float g_ell[3][kC], g_beta[3][kC], g_lam[3][kC], g_gam[3][kC], g_kap[3][kC], g_igam[3][kC];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, hf = warp >> 2;          // TMEM lane quarter, column half
@@ -85,25 +98,25 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     const int T = p.T, H = p.H;
     const int nchunks = (T + kC - 1) / kC;
     const bool producer = (tid == 0), issuer = (tid == 32);
+    const int d_row = 32 * q4 + lane;                  // this thread's TMEM lane / state row
 
     if (tid == 0) {
         mbar_init(&bar_full[0], 1);
         mbar_init(&bar_full[1], 1);
-        mbar_init(&bar_mma, 1);
+        mbar_init(&bar_z, 1);
+        mbar_init(&bar_g, 1);
+        mbar_init(&bar_o2, 1);
+        mbar_init(&bar_uw, 1);
         abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
-        tma_prefetch_desc(&tmO);
     }
     if (warp == 0) {
         tmem_alloc(&tmem_base, 512);
         tmem_relinquish();
     }
-
-    // this thread's TMEM lane / state row and its 64-column half
-    const int d_row = 32 * q4 + lane;
 
     auto issue_loads = [&](int c) {
         const int s = c & 1;
@@ -131,8 +144,9 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             if (p.lam) rl[u] = p.lam[tok];
         }
     };
-    // warp-wide: log-prefix l, gamma = e^l, kappa = e^{l_C - l}, e^{-l} of one chunk into buffer buf
-    auto compute_gates = [&](int c, int buf) {
+    // warp-wide: log-prefix l, gamma = e^l, kappa = e^{l_C - l}, e^{-l} of chunk c
+    auto compute_gates = [&](int c) {
+        const int buf = c % 3;
         float ga[2], gb[2], gl[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {                  // tokens past T: alpha 1, beta 0, lambda 0
@@ -171,7 +185,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     }
     if (warp == 4) {
         load_gates(0);
-        compute_gates(0, 0);
+        compute_gates(0);
         if (nchunks > 1) load_gates(1);       // turned into arrays during chunk 0's solve
     }
     tc_fence_before();
@@ -179,6 +193,231 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     tc_fence_after();
     const uint32_t tm = tmem_base;
     const uint32_t tl = tm + ((uint32_t)(32 * q4) << 16);   // this warp's TMEM lane quarter
+
+    bool ok = true;
+    auto wait_on = [&](uint64_t *bar, uint32_t parity) {
+        if (!mbar_wait(bar, parity, kWaitNs)) { ok = false; abort_flag = 1; }
+    };
+    auto wait_mma = [&](uint64_t *bar, int chunk) {
+        wait_on(bar, (uint32_t)(chunk & 1));
+        tc_fence_after();
+    };
+    auto sync_for_mma = [&]() {   // generic smem writes -> visible to the tensor core / TMA
+        fence_proxy_async();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+    };
+    const uint32_t sbase = smem_u32(sm);
+    const uint32_t sS = sbase + OFF_S, sR1 = sbase + OFF_R1, sR2 = sbase + OFF_R2;
+    auto stage_addr = [&](int c) { return sbase + (uint32_t)(c & 1) * kStageBytes; };
+
+    // X = K + lambda Q into rows 0-63 of the XQ panels of chunk c's stage
+    auto x_pass = [&](int c) {
+        uint8_t *st = sm + (c & 1) * kStageBytes;
+        const float *lam = g_lam[c % 3];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int u = tid + kThreads * r;             // 16-byte chunk index, 0..1023
+            const int pnl = u >> 9;
+            const uint32_t off = (uint32_t)(u & 511) << 4;
+            float kf[8], qf[8], xf[8];
+            unpack8(*reinterpret_cast<const uint4 *>(st + OFF_K + pnl * 8192 + off), kf);
+            unpack8(*reinterpret_cast<const uint4 *>(st + OFF_XQ + pnl * 16384 + 8192 + off), qf);
+            const float lm = lam[off >> 7];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xf[e] = fmaf(lm, qf[e], kf[e]);
+            *reinterpret_cast<uint4 *>(st + OFF_XQ + pnl * 16384 + off) = pack8(xf);
+        }
+    };
+    // G = [X; Q] K^T
+    auto issue_gram = [&](int c) {
+        if (!issuer) return;
+        const uint32_t sXQ = stage_addr(c) + OFF_XQ, sK = stage_addr(c) + OFF_K;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
+            umma_bf16(tm + TM_G, smem_desc(sXQ + ko, 16, 1024), smem_desc(sK + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024),
+                      idesc_bf16(128, 64, false, false), k > 0);
+        }
+        umma_commit(&bar_g);
+    };
+    // decay masks: A (fp32, R1) from the X K^T rows, P (bf16) from the Q K^T rows; K -> kappa K
+    auto masks = [&](int c) {
+        const int gi = c % 3;
+        const float *ell = g_ell[gi], *bet = g_beta[gi], *gam = g_gam[gi], *igam = g_igam[gi], *kap = g_kap[gi];
+        float g[32];
+        tmem_ld32(tl + TM_G + 32 * hf, g);
+        tmem_ld_wait();
+        const bool split = ell[kC - 1] > -80.f;       // uniform: gamma_t * exp(-l_i) is safe
+        if (q4 < 2) {
+            const int t = 32 * q4 + lane;
+            const float lt = ell[t], bt = bet[t], bg = bt * gam[t];
+            float *Arow = reinterpret_cast<float *>(sm + OFF_R1) + t * LA + 32 * hf;
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+                float a[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int cc = 4 * c4 + e, i = 32 * hf + cc;
+                    const float v = split ? bg * igam[i] * g[cc] : bt * __expf(lt - ell[i]) * g[cc];
+                    a[e] = (i < t) ? v : 0.f;
+                }
+                *reinterpret_cast<float4 *>(Arow + 4 * c4) = make_float4(a[0], a[1], a[2], a[3]);
+            }
+        } else {
+            const int t = 32 * (q4 - 2) + lane;
+            const float lt = ell[t], gt = gam[t];
+            uint8_t *P = sm + OFF_P + (c & 1) * 8192;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int i = 32 * hf + 8 * ch + e;
+                    const float pv = split ? gt * igam[i] * g[8 * ch + e] : __expf(lt - ell[i]) * g[8 * ch + e];
+                    f[e] = (i <= t) ? pv : 0.f;
+                }
+                *reinterpret_cast<uint4 *>(P + sw128_off(t, 32 * hf + 8 * ch)) = pack8(f);
+            }
+        }
+        uint8_t *st = sm + (c & 1) * kStageBytes;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const uint32_t off = (uint32_t)(tid + kThreads * r) << 4;   // both K panels
+            uint4 *pk = reinterpret_cast<uint4 *>(st + OFF_K + off);
+            float kf[8];
+            unpack8(*pk, kf);
+            const float ka = kap[(off & 8191) >> 7];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) kf[e] *= ka;
+            *pk = pack8(kf);
+        }
+    };
+    // Tinv -> Tinv*beta, Tinv*beta*gamma over R1; warp 4 meanwhile prepares the next gates
+    auto solve = [&](int c) {
+        const int gi = c % 3;
+        unit_lower_inverse(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_Y),
+                           sm + OFF_R1, sm + OFF_R1 + 8192, g_beta[gi], g_gam[gi], [&]() {
+                               if (warp == 4 && c + 1 < nchunks) compute_gates(c + 1);
+                           });
+    };
+    // U^T = V^T T1^T, W^T = X^T T2^T
+    auto issue_uw = [&](int c) {
+        if (!issuer) return;
+        const uint32_t sXQ = stage_addr(c) + OFF_XQ, sV = stage_addr(c) + OFF_V;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            umma_bf16(tm + TM_U, smem_desc(sV + k * 2048, 8192, 1024), smem_desc(sR1 + k * 32, 16, 1024),
+                      idesc_bf16(128, 64, true, false), k > 0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            umma_bf16(tm + TM_W, smem_desc(sXQ + k * 2048, 16384, 1024), smem_desc(sR1 + 8192 + k * 32, 16, 1024),
+                      idesc_bf16(128, 64, true, false), k > 0);
+        umma_commit(&bar_uw);
+    };
+    // -W -> R2 as [64 tokens][dk] (two 64-column panels)
+    auto w_store = [&]() {
+        float w[32];
+        tmem_ld32(tl + TM_W + 32 * hf, w);
+        tmem_ld_wait();
+        uint8_t *dst = sm + OFF_R2 + (d_row >> 6) * 8192;   // lane index = dk index
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc)
+            *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * hf + cc, d_row & 63)) = __float2bfloat16_rn(-w[cc]);
+    };
+    // O1 = S Q^T (no commit: the next Z commit covers it)
+    auto issue_o1 = [&](int c) {
+        if (!issuer) return;
+        const uint32_t sXQ = stage_addr(c) + OFF_XQ;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
+            umma_bf16(tm + TM_O1, smem_desc(sS + ko, 16, 1024), smem_desc(sXQ + ko + 8192, 16, 1024),
+                      idesc_bf16(128, 64, false, false), k > 0);
+        }
+    };
+    // Z^T = U^T - S W^T  (accumulate into the U columns)
+    auto issue_z = [&]() {
+        if (!issuer) return;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
+            umma_bf16(tm + TM_U, smem_desc(sS + ko, 16, 1024), smem_desc(sR2 + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024),
+                      idesc_bf16(128, 64, false, false), 1);
+        }
+        umma_commit(&bar_z);
+    };
+    // Z^T (bf16) -> R2 as [dv][64 tokens]
+    auto zt_store = [&]() {
+        float z[32];
+        tmem_ld32(tl + TM_U + 32 * hf, z);
+        tmem_ld_wait();
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = z[8 * ch + e];
+            *reinterpret_cast<uint4 *>(sm + OFF_R2 + sw128_off(d_row, 32 * hf + 8 * ch)) = pack8(f);
+        }
+    };
+    // O2 = Z^T P^T ; S += Z^T (kappa K)  (S in TMEM already scaled by gamma_C)
+    auto issue_mma2 = [&](int c) {
+        if (!issuer) return;
+        const uint32_t sK = stage_addr(c) + OFF_K, sP = sbase + OFF_P + (uint32_t)(c & 1) * 8192;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            umma_bf16(tm + TM_O2, smem_desc(sR2 + k * 32, 16, 1024), smem_desc(sP + k * 32, 16, 1024),
+                      idesc_bf16(128, 64, false, false), k > 0);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            umma_bf16(tm + TM_S, smem_desc(sR2 + k * 32, 16, 1024), smem_desc(sK + k * 2048, 8192, 1024),
+                      idesc_bf16(128, 128, false, true), 1);
+        umma_commit(&bar_o2);
+    };
+    // o_t = gamma_t O1 + O2 straight to global memory; state -> bf16 S_in for the next
+    // chunk, rescaled in TMEM by the next chunk's gamma_C (or written out after the last)
+    auto epilogue = [&](int c) {
+        const int t0 = c * kC;
+        const float *gam = g_gam[c % 3];
+        float o1[32], o2[32];
+        tmem_ld32(tl + TM_O1 + 32 * hf, o1);
+        tmem_ld32(tl + TM_O2 + 32 * hf, o2);
+        tmem_ld_wait();
+        __nv_bfloat16 *og = p.o + ((size_t)b * T + t0 + 32 * hf) * H * kD + (size_t)h * kD + d_row;
+        const int nvalid = T - t0 - 32 * hf;
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc)
+            if (cc < nvalid) og[(size_t)cc * H * kD] = __float2bfloat16_rn(fmaf(gam[32 * hf + cc], o1[cc], o2[cc]));
+        const bool last = (c + 1 == nchunks);
+        const float gN = last ? 1.f : g_gam[(c + 1) % 3][kC - 1];
+        uint8_t *sp = sm + OFF_S + hf * 16384;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float sv[32];
+            tmem_ld32(tl + TM_S + 64 * hf + 32 * half, sv);
+            tmem_ld_wait();
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = sv[8 * ch + e];
+                *reinterpret_cast<uint4 *>(sp + sw128_off(d_row, 32 * half + 8 * ch)) = pack8(f);
+            }
+            if (!last) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) sv[e] *= gN;
+                tmem_st32(tl + TM_S + 64 * hf + 32 * half, sv);
+            } else if (p.S_final && !abort_flag) {
+                float *dst = p.S_final + ((size_t)bh * kD + d_row) * kD + 64 * hf + 32 * half;
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+            }
+        }
+        tmem_st_wait();
+    };
+
+    // initial state: bf16 copy in S_in, fp32 in TMEM scaled by chunk 0's gamma_C
     {
         const size_t base = ((size_t)bh * kD + d_row) * kD + 64 * hf;
         const float g0 = g_gam[0][kC - 1];
@@ -205,280 +444,75 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         }
         tmem_st_wait();
     }
-    fence_proxy_async();
+
+    // chunk 0's state-independent work, then O1(0)
+    wait_on(&bar_full[0], 0);
+    x_pass(0);
+    sync_for_mma();
+    issue_gram(0);
+    wait_mma(&bar_g, 0);
+    masks(0);
     tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-    uint32_t mma_phase = 0;
-    bool ok = true;
+    solve(0);
+    sync_for_mma();
+    issue_uw(0);
+    wait_mma(&bar_uw, 0);
+    w_store();
+    sync_for_mma();
+    issue_o1(0);
 
-    auto wait_mma = [&]() {
-        if (!mbar_wait(&bar_mma, mma_phase, kWaitNs)) { ok = false; abort_flag = 1; }
-        mma_phase ^= 1;
-        tc_fence_after();
-    };
-    auto sync_for_mma = [&]() {   // generic smem writes -> visible to the tensor core / TMA
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-        tc_fence_after();
-    };
-
-    const uint32_t sbase = smem_u32(sm);
-    for (int c = 0; c < nchunks; ++c) {
-        const int s = c & 1;
-        const int t0 = c * kC;
-        uint8_t *st = sm + s * kStageBytes;
-        const uint32_t sXQ = sbase + s * kStageBytes + OFF_XQ, sK = sbase + s * kStageBytes + OFF_K;
-        const uint32_t sV = sbase + s * kStageBytes + OFF_V, sS = sbase + OFF_S;
-        const uint32_t sR1 = sbase + OFF_R1, sR2 = sbase + OFF_R2, sP = sbase + OFF_P;
-        const float *g_ell_c = g_ell[c & 1], *g_beta_c = g_beta[c & 1], *g_lam_c = g_lam[c & 1];
-        const float *g_gam_c = g_gam[c & 1], *g_kap_c = g_kap[c & 1], *g_igam_c = g_igam[c & 1];
-
-        // (1) this chunk's tiles; warp 4 starts loading the next chunk's gates
-        if (warp == 4 && c + 1 < nchunks) load_gates(c + 1);
-        if (!mbar_wait(&bar_full[s], (uint32_t)((c >> 1) & 1), kWaitNs)) { ok = false; abort_flag = 1; }
-        __syncthreads();
-        if (abort_flag) break;
-
-        // (2) X = K + lambda Q into rows 0-63 of the XQ panels
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int u = tid + kThreads * r;             // 16-byte chunk index, 0..1023
-            const int pnl = u >> 9;
-            const uint32_t off = (uint32_t)(u & 511) << 4;
-            const int row = off >> 7;
-            float kf[8], qf[8], xf[8];
-            unpack8(*reinterpret_cast<const uint4 *>(st + OFF_K + pnl * 8192 + off), kf);
-            unpack8(*reinterpret_cast<const uint4 *>(st + OFF_XQ + pnl * 16384 + 8192 + off), qf);
-            const float lm = g_lam_c[row];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) xf[e] = fmaf(lm, qf[e], kf[e]);
-            *reinterpret_cast<uint4 *>(st + OFF_XQ + pnl * 16384 + off) = pack8(xf);
+    int loads_issued = nchunks > 1 ? 2 : 1;              // producer's bookkeeping for a drain
+    for (int c = 0; c < nchunks && !abort_flag; ++c) {
+        const bool more = (c + 1 < nchunks);
+        issue_z();                                        // covers O1(c) too
+        if (warp == 4 && c + 2 < nchunks) load_gates(c + 2);
+        if (more) {
+            wait_on(&bar_full[(c + 1) & 1], (uint32_t)(((c + 1) >> 1) & 1));
+            x_pass(c + 1);
+            sync_for_mma();
+            issue_gram(c + 1);
         }
+        wait_mma(&bar_z, c);
+        zt_store();
         sync_for_mma();
-
-        // (3) G = [X;Q] K^T and O1 = S Q^T
-        if (issuer) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
-                umma_bf16(tm + TM_G, smem_desc(sXQ + ko, 16, 1024),
-                          smem_desc(sK + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), idesc_bf16(128, 64, false, false),
-                          k > 0);
-            }
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
-                umma_bf16(tm + TM_O1, smem_desc(sS + ko, 16, 1024), smem_desc(sXQ + ko + 8192, 16, 1024),
-                          idesc_bf16(128, 64, false, false), k > 0);
-            }
-            umma_commit(&bar_mma);
+        issue_mma2(c);
+        if (more) {
+            wait_mma(&bar_g, c + 1);
+            masks(c + 1);
+            tc_fence_before();
+            __syncthreads();
+            solve(c + 1);
+            sync_for_mma();
+            issue_uw(c + 1);
         }
-        wait_mma();
-
-        // (4) decay masks: A (fp32, R1) from X K^T rows, P (bf16) from Q K^T rows; K -> kappa K
-        {
-            float g[32];
-            tmem_ld32(tl + TM_G + 32 * hf, g);
-            tmem_ld_wait();
-            const bool split = g_ell_c[kC - 1] > -80.f;        // uniform: gamma_t * exp(-l_i) is safe
-            if (q4 < 2) {
-                const int t = 32 * q4 + lane;
-                const float lt = g_ell_c[t], bt = g_beta_c[t], bg = bt * g_gam_c[t];
-                float *Arow = reinterpret_cast<float *>(sm + OFF_R1) + t * LA + 32 * hf;
-#pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) {
-                    float a[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int cc = 4 * c4 + e, i = 32 * hf + cc;
-                        const float v = split ? bg * g_igam_c[i] * g[cc] : bt * __expf(lt - g_ell_c[i]) * g[cc];
-                        a[e] = (i < t) ? v : 0.f;
-                    }
-                    *reinterpret_cast<float4 *>(Arow + 4 * c4) = make_float4(a[0], a[1], a[2], a[3]);
-                }
-            } else {
-                const int t = 32 * (q4 - 2) + lane;
-                const float lt = g_ell_c[t], gt = g_gam_c[t];
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    float f[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int i = 32 * hf + 8 * ch + e;
-                        const float pv = split ? gt * g_igam_c[i] * g[8 * ch + e] : __expf(lt - g_ell_c[i]) * g[8 * ch + e];
-                        f[e] = (i <= t) ? pv : 0.f;
-                    }
-                    *reinterpret_cast<uint4 *>(sm + OFF_P + sw128_off(t, 32 * hf + 8 * ch)) = pack8(f);
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int u = tid + kThreads * r;
-                const uint32_t off = (uint32_t)u << 4;       // 0 .. 16 KB across both K panels
-                const int row = (off & 8191) >> 7;
-                uint4 *pk = reinterpret_cast<uint4 *>(st + OFF_K + off);
-                float kf[8];
-                unpack8(*pk, kf);
-                const float ka = g_kap_c[row];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) kf[e] *= ka;
-                *pk = pack8(kf);
-            }
+        wait_mma(&bar_o2, c);
+        if (producer && c + 2 < nchunks) {                // chunk c's stage is consumed
+            issue_loads(c + 2);
+            ++loads_issued;
         }
-        if (producer) tma_store_wait_read0();   // R2 (last chunk's O staging) is free for scratch
-        tc_fence_before();
-        __syncthreads();
-
-        // (5) Tinv = (I + A)^{-1}.  A is fp32 in R1, zero on and above the diagonal.
-        //   a) the four 16x16 diagonal blocks by forward substitution (one column per lane)
-        //   b) 16 -> 32: T10 = -T11 (A10 T00) for the block pairs (0,1) and (2,3)
-        //   c) 32 -> 64: T21 = -T22 (A21 T11) on the two 32x32 halves
-        // Every inverted block keeps only the strict lower part of its inverse (the
-        // unit diagonal is implied, zeros above), so each product is a dense loop:
-        // Y = A21 + A21 T11s and T21 = -(Y + T22s Y).  R2 serves as scratch.
-        {
-            unit_lower_inverse(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_R2),
-                               sm + OFF_R1, sm + OFF_R1 + 8192, g_beta_c, g_gam_c, [&]() {
-                                   if (warp == 4 && c + 1 < nchunks) compute_gates(c + 1, (c + 1) & 1);
-                               });
-        }
+        epilogue(c);
         sync_for_mma();
-
-        // (6) U^T = V^T T1^T, W^T = X^T T2^T
-        if (issuer) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                umma_bf16(tm + TM_U, smem_desc(sV + k * 2048, 8192, 1024), smem_desc(sR1 + k * 32, 16, 1024),
-                          idesc_bf16(128, 64, true, false), k > 0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                umma_bf16(tm + TM_W, smem_desc(sXQ + k * 2048, 16384, 1024), smem_desc(sR1 + 8192 + k * 32, 16, 1024),
-                          idesc_bf16(128, 64, true, false), k > 0);
-            umma_commit(&bar_mma);
-        }
-        wait_mma();
-
-        // (7) -W -> R2 as [64 tokens][dk] (two 64-column panels)
-        {
-            float w[32];
-            tmem_ld32(tl + TM_W + 32 * hf, w);
-            tmem_ld_wait();
-            const int j = d_row;                            // lane index = dk index
-            uint8_t *dst = sm + OFF_R2 + (j >> 6) * 8192;
-#pragma unroll
-            for (int cc = 0; cc < 32; ++cc) {
-                const int i = 32 * hf + cc;
-                *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(i, j & 63)) = __float2bfloat16_rn(-w[cc]);
-            }
-        }
-        sync_for_mma();
-
-        // (8) Z^T = U^T - S W^T  (accumulate into the U columns)
-        if (issuer) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
-                umma_bf16(tm + TM_U, smem_desc(sS + ko, 16, 1024), smem_desc(sR2 + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024),
-                          idesc_bf16(128, 64, false, false), 1);
-            }
-            umma_commit(&bar_mma);
-        }
-        wait_mma();
-
-        // (9) Z^T (bf16) -> R2 as [dv][64 tokens]
-        {
-            float z[32];
-            tmem_ld32(tl + TM_U + 32 * hf, z);
-            tmem_ld_wait();
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = z[8 * ch + e];
-                *reinterpret_cast<uint4 *>(sm + OFF_R2 + sw128_off(d_row, 32 * hf + 8 * ch)) = pack8(f);
-            }
-        }
-        sync_for_mma();
-
-        // (10) O2 = Z^T P^T ; S += Z^T (kappa K)  (S in TMEM already scaled by gamma_C)
-        if (issuer) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                umma_bf16(tm + TM_O2, smem_desc(sR2 + k * 32, 16, 1024), smem_desc(sP + k * 32, 16, 1024),
-                          idesc_bf16(128, 64, false, false), k > 0);
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                umma_bf16(tm + TM_S, smem_desc(sR2 + k * 32, 16, 1024), smem_desc(sK + k * 2048, 8192, 1024),
-                          idesc_bf16(128, 128, false, true), 1);
-            umma_commit(&bar_mma);
-        }
-        wait_mma();
-
-        // (11) o = gamma_t O1 + O2 -> staging (R2); state -> bf16 S_in
-        {
-            float o1[32], o2[32];
-            tmem_ld32(tl + TM_O1 + 32 * hf, o1);
-            tmem_ld32(tl + TM_O2 + 32 * hf, o2);
-            tmem_ld_wait();
-            uint8_t *dst = sm + OFF_R2 + (d_row >> 6) * 8192;
-#pragma unroll
-            for (int cc = 0; cc < 32; ++cc) {
-                const int t = 32 * hf + cc;
-                *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(t, d_row & 63)) =
-                    __float2bfloat16_rn(fmaf(g_gam_c[t], o1[cc], o2[cc]));
-            }
-            // state: bf16 copy for the next chunk's MMAs; rescale by the next chunk's gamma_C
-            // in TMEM, or write the final state after the last chunk
-            const bool last = (c + 1 == nchunks);
-            const float gN = last ? 1.f : g_gam[(c + 1) & 1][kC - 1];
-            uint8_t *sp = sm + OFF_S + hf * 16384;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float sv[32];
-                tmem_ld32(tl + TM_S + 64 * hf + 32 * half, sv);
-                tmem_ld_wait();
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    float f[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = sv[8 * ch + e];
-                    *reinterpret_cast<uint4 *>(sp + sw128_off(d_row, 32 * half + 8 * ch)) = pack8(f);
-                }
-                if (!last) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) sv[e] *= gN;
-                    tmem_st32(tl + TM_S + 64 * hf + 32 * half, sv);
-                } else if (p.S_final && !abort_flag) {
-                    float *dst = p.S_final + ((size_t)bh * kD + d_row) * kD + 64 * hf + 32 * half;
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
-                }
-            }
-            tmem_st_wait();
-        }
-        sync_for_mma();
-        if (producer) {
-            tma_store_4d(&tmO, sm + OFF_R2, 0, h, t0, b);
-            tma_store_4d(&tmO, sm + OFF_R2 + 8192, 64, h, t0, b);
-            tma_store_commit();
-            if (c + 2 < nchunks) issue_loads(c + 2);
+        if (more) {
+            issue_o1(c + 1);
+            wait_mma(&bar_uw, c + 1);
+            w_store();
+            sync_for_mma();
         }
     }
 
-    if (producer) {
-        tma_store_wait_all();
-        if (abort_flag) {
-            // drain loads that may still be landing in shared memory
-            for (int c = 0; c < 2 && c < nchunks; ++c) mbar_wait(&bar_full[c], 0, kWaitNs);
+    if (abort_flag) {
+        // wind down: let this CTA's copies and MMAs finish (bounded) before freeing TMEM
+        if (producer)
+            for (int s = 0; s < 2; ++s) {
+                const int n_s = (loads_issued + 1 - s) / 2;   // loads issued into stage s
+                if (n_s > 0) mbar_wait(&bar_full[s], (uint32_t)((n_s - 1) & 1), kWaitNs);
+            }
+        if (issuer) {
+            umma_commit(&bar_z);
+            mbar_wait(&bar_z, 0, kWaitNs);
+            mbar_wait(&bar_z, 1, kWaitNs);
         }
-    }
-    if (issuer && abort_flag) {
-        umma_commit(&bar_mma);
-        mbar_wait(&bar_mma, mma_phase, kWaitNs);
-    }
-    if (!ok || abort_flag) {
         if (lane == 0) atomicExch(&g_tc_timeout, 1u);
     }
     tc_fence_before();
@@ -493,16 +527,16 @@ bool qdelta_tc_supported(const QDeltaArgs &a, int dtype) {
 }
 
 cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nlaunch) {
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv;
     if (!make_token_map(&mq, a.q, a.B, a.T, a.H) || !make_token_map(&mk, a.k, a.B, a.T, a.H) ||
-        !make_token_map(&mv, a.v, a.B, a.T, a.H) || !make_token_map(&mo, a.o, a.B, a.T, a.H))
+        !make_token_map(&mv, a.v, a.B, a.T, a.H))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(qdelta_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     TcParams p{(const __nv_bfloat16 *)a.alpha, (const __nv_bfloat16 *)a.beta, (const __nv_bfloat16 *)a.lam,
-               a.S0, a.S_final, a.B, a.T, a.H};
-    qdelta_fwd_tc_kernel<<<a.B * a.H, kThreads, kSmemBytes, s>>>(p, mq, mk, mv, mo);
+               a.S0, (__nv_bfloat16 *)a.o, a.S_final, a.B, a.T, a.H};
+    qdelta_fwd_tc_kernel<<<a.B * a.H, kThreads, kSmemBytes, s>>>(p, mq, mk, mv);
     e = cudaGetLastError();
     if (e == cudaSuccess) *nlaunch += 1;
     return e;
