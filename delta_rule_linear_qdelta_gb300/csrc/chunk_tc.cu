@@ -18,26 +18,28 @@
 // accumulates Z^T (kappa K) onto it after the epilogue has scaled it by the chunk's
 // gamma_C); its bf16 copy in shared memory feeds the MMAs.
 //
-// Software pipeline: the state-independent work of chunk c+1 (X, its Gram, the
-// masks, the solve, U and W) is interleaved with the state chain of chunk c
-// (Z, the output and state products, the epilogue) so that each MMA's latency is
-// covered by thread work of the other chunk:
-//   issue Z(c) | X(c+1), issue G(c+1) | wait Z(c), Z^T(c) -> smem, issue O2/S(c)
-//   | wait G(c+1), masks(c+1) | solve(c+1), issue U/W(c+1) | wait O2/S(c), epilogue(c)
-//   | issue O1(c+1) | wait U/W(c+1), -W(c+1) -> smem
-// Each commit has its own mbarrier (one phase per chunk).
+// Warp specialisation: a prep group (warps 0-7) does the state-independent work of
+// each chunk -- X, its Gram, the decay masks, the solve, U and W -- and hands the
+// chunk to a chain group (warps 8-11) that carries the state: O1 and Z, Z^T, the
+// output and state products, the epilogue.  The two groups run concurrently, so the
+// chunk period is the longer of the two instead of their sum.  Each group
+// synchronises on its own named barrier; hand-offs are mbarriers:
+//   ready       prep -> chain: -W(c), P(c), U(c), kappa K(c) and the gates are in place
+//   cdone[c&1]  chain -> prep: the output and state products of chunk c have run, so
+//               R2, P[c&1], U[c&1] and chunk c's stage are free
+// The chain group also issues the TMA loads of chunk c+2 into chunk c's stage.
 //
 // Shared memory (offsets from a 1024-aligned base):
 //   stage s in {0,1}: XQ 32 KB (per 64-column panel: X rows 0-63 | Q rows 64-127),
 //                     K 16 KB (overwritten in place by kappa*K), V 16 KB
 //   S_in 32 KB   bf16 state [dv][dk]
 //   R1   17 KB   A fp32 [64][68]  ->  Tinv*beta, Tinv*beta*gamma (bf16)
-//   R2   16 KB   -W [64][dk]  ->  Z^T [dv][64]
+//   R2   16 KB   -W(c) [64][dk]  ->  Z^T(c) [dv][64]  ->  solve scratch and -W(c+1)
 //   P    2x8 KB  bf16 [64][64], by chunk parity
-//   Y     5 KB   solve scratch
 // All MMA operands use the 128-byte swizzle (TMA layout): 128-byte rows, 8-row
 // groups 1024 bytes apart, 64-column panels.
-// TMEM (512 columns): G 0-63, O1 64-127, U/Z 128-191, W 192-255, O2 256-319, S 320-447.
+// TMEM (512 columns): G 0-63, W 64-127, U[0] 128-191, U[1] 192-255, O1 256-319,
+// O2 320-383, S 384-511.
 //
 // Every wait is bounded; on a timeout the kernel sets the library's error word,
 // waits (bounded) for its own copies and MMAs, frees TMEM and returns.
@@ -58,19 +60,22 @@ namespace {
 using namespace ptx;
 using namespace tc;
 
+constexpr int kPrepThreads = kThreads;              // warps 0-7
+constexpr int kChainThreads = 128;                  // warps 8-11
+constexpr int kAllThreads = kPrepThreads + kChainThreads;
+constexpr int kBarPrep = 1, kBarChain = 2;          // named barrier ids
 constexpr uint32_t kStageBytes = 65536;
 constexpr uint32_t OFF_XQ = 0, OFF_K = 32768, OFF_V = 49152;
 constexpr uint32_t OFF_S = 2 * kStageBytes;          // 131072
 constexpr uint32_t OFF_R1 = OFF_S + 32768;           // 163840
 constexpr uint32_t OFF_R2 = OFF_R1 + 17408;          // 181248
 constexpr uint32_t OFF_P = OFF_R2 + 16384;           // 197632 (two 8 KB buffers)
-constexpr uint32_t OFF_Y = OFF_P + 16384;            // 214016
-constexpr uint32_t kSmemUsed = OFF_Y + 5120;         // 219136
+constexpr uint32_t kSmemUsed = OFF_P + 16384;        // 214016
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
 constexpr uint32_t kTmaBytes = 3 * kC * kD * 2;      // Q, K, V tiles per chunk
 constexpr uint64_t kWaitNs = 2000000000ull;          // 2 s per wait
 
-constexpr uint32_t TM_G = 0, TM_O1 = 64, TM_U = 128, TM_W = 192, TM_O2 = 256, TM_S = 320;
+constexpr uint32_t TM_G = 0, TM_W = 64, TM_U = 128, TM_O1 = 256, TM_O2 = 320, TM_S = 384;
 
 struct TcParams {
     const __nv_bfloat16 *alpha, *beta, *lam;
@@ -80,33 +85,39 @@ struct TcParams {
     int B, T, H;
 };
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kAllThreads, 1)
 qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-    // one mbarrier per TMA stage and per kind of MMA commit (each completes once per chunk)
-    __shared__ uint64_t bar_full[2], bar_z, bar_g, bar_o2, bar_uw;
+    __shared__ uint64_t bar_full[2], bar_g, bar_uw, bar_z, bar_o2, bar_ready, bar_cdone[2], bar_drain[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
-    // per-chunk gate arrays, by chunk index mod 3
+    // per-chunk gate arrays, by chunk index mod 3 (the prep group runs at most one
+    // chunk ahead of the chain group's epilogue)
     __shared__ float g_ell[3][kC], g_beta[3][kC], g_lam[3][kC], g_gam[3][kC], g_kap[3][kC], g_igam[3][kC];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int q4 = warp & 3, hf = warp >> 2;          // TMEM lane quarter, column half
+    const bool prep = tid < kPrepThreads;
+    const int q4 = warp & 3, hf = (warp >> 2) & 1;    // TMEM lane quarter; column half (prep)
     const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
     const int T = p.T, H = p.H;
     const int nchunks = (T + kC - 1) / kC;
-    const bool producer = (tid == 0), issuer = (tid == 32);
+    const bool p_issuer = (tid == 32), c_issuer = (tid == kPrepThreads);
     const int d_row = 32 * q4 + lane;                  // this thread's TMEM lane / state row
 
     if (tid == 0) {
         mbar_init(&bar_full[0], 1);
         mbar_init(&bar_full[1], 1);
-        mbar_init(&bar_z, 1);
         mbar_init(&bar_g, 1);
-        mbar_init(&bar_o2, 1);
         mbar_init(&bar_uw, 1);
+        mbar_init(&bar_z, 1);
+        mbar_init(&bar_o2, 1);
+        mbar_init(&bar_ready, 1);
+        mbar_init(&bar_cdone[0], 1);
+        mbar_init(&bar_cdone[1], 1);
+        mbar_init(&bar_drain[0], 1);
+        mbar_init(&bar_drain[1], 1);
         abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ);
@@ -130,7 +141,6 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             tma_load_4d(st + OFF_V + pnl * 8192, &tmV, &bar_full[s], 64 * pnl, h, t0, b);
         }
     };
-
     // gates of a chunk: lane l of warp 4 holds tokens 2l and 2l+1.  The loads land in raw
     // bf16 registers that nothing reads until compute_gates, so they do not stall the warp.
     __nv_bfloat16 ra[2], rb[2], rl[2];
@@ -179,14 +189,13 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         g_igam[buf][2 * lane + 1] = eC > -80.f ? __expf(-e1) : 0.f;
     };
 
-    if (producer) {
+    if (tid == 0) {
         issue_loads(0);
         if (nchunks > 1) issue_loads(1);
     }
     if (warp == 4) {
         load_gates(0);
         compute_gates(0);
-        if (nchunks > 1) load_gates(1);       // turned into arrays during chunk 0's solve
     }
     tc_fence_before();
     __syncthreads();
@@ -202,23 +211,31 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         wait_on(bar, (uint32_t)(chunk & 1));
         tc_fence_after();
     };
-    auto sync_for_mma = [&]() {   // generic smem writes -> visible to the tensor core / TMA
+    // a group's generic smem and TMEM work made visible to its next MMA / to the other group
+    auto psync = [&]() {
         fence_proxy_async();
         tc_fence_before();
-        __syncthreads();
+        named_sync(kBarPrep, kPrepThreads);
+        tc_fence_after();
+    };
+    auto csync = [&]() {
+        fence_proxy_async();
+        tc_fence_before();
+        named_sync(kBarChain, kChainThreads);
         tc_fence_after();
     };
     const uint32_t sbase = smem_u32(sm);
     const uint32_t sS = sbase + OFF_S, sR1 = sbase + OFF_R1, sR2 = sbase + OFF_R2;
     auto stage_addr = [&](int c) { return sbase + (uint32_t)(c & 1) * kStageBytes; };
 
+    // ---------------------------------------------------------------- prep group
     // X = K + lambda Q into rows 0-63 of the XQ panels of chunk c's stage
     auto x_pass = [&](int c) {
         uint8_t *st = sm + (c & 1) * kStageBytes;
         const float *lam = g_lam[c % 3];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            const int u = tid + kThreads * r;             // 16-byte chunk index, 0..1023
+            const int u = tid + kPrepThreads * r;         // 16-byte chunk index, 0..1023
             const int pnl = u >> 9;
             const uint32_t off = (uint32_t)(u & 511) << 4;
             float kf[8], qf[8], xf[8];
@@ -232,7 +249,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     };
     // G = [X; Q] K^T
     auto issue_gram = [&](int c) {
-        if (!issuer) return;
+        if (!p_issuer) return;
         const uint32_t sXQ = stage_addr(c) + OFF_XQ, sK = stage_addr(c) + OFF_K;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -284,7 +301,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         uint8_t *st = sm + (c & 1) * kStageBytes;
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-            const uint32_t off = (uint32_t)(tid + kThreads * r) << 4;   // both K panels
+            const uint32_t off = (uint32_t)(tid + kPrepThreads * r) << 4;   // both K panels
             uint4 *pk = reinterpret_cast<uint4 *>(st + OFF_K + off);
             float kf[8];
             unpack8(*pk, kf);
@@ -294,21 +311,23 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             *pk = pack8(kf);
         }
     };
-    // Tinv -> Tinv*beta, Tinv*beta*gamma over R1; warp 4 meanwhile prepares the next gates
+    // Tinv -> Tinv*beta, Tinv*beta*gamma over R1 (scratch in R2); warp 4 meanwhile
+    // turns the next chunk's raw gates into arrays
     auto solve = [&](int c) {
         const int gi = c % 3;
-        unit_lower_inverse(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_Y),
-                           sm + OFF_R1, sm + OFF_R1 + 8192, g_beta[gi], g_gam[gi], [&]() {
-                               if (warp == 4 && c + 1 < nchunks) compute_gates(c + 1);
-                           });
+        unit_lower_inverse(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_R2),
+                           sm + OFF_R1, sm + OFF_R1 + 8192, g_beta[gi], g_gam[gi],
+                           [&]() { if (warp == 4 && c + 1 < nchunks) compute_gates(c + 1); },
+                           []() { named_sync(kBarPrep, kPrepThreads); });
     };
-    // U^T = V^T T1^T, W^T = X^T T2^T
+    // U^T = V^T T1^T into U[c&1], W^T = X^T T2^T
     auto issue_uw = [&](int c) {
-        if (!issuer) return;
+        if (!p_issuer) return;
         const uint32_t sXQ = stage_addr(c) + OFF_XQ, sV = stage_addr(c) + OFF_V;
+        const uint32_t tu = tm + TM_U + 64 * (uint32_t)(c & 1);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            umma_bf16(tm + TM_U, smem_desc(sV + k * 2048, 8192, 1024), smem_desc(sR1 + k * 32, 16, 1024),
+            umma_bf16(tu, smem_desc(sV + k * 2048, 8192, 1024), smem_desc(sR1 + k * 32, 16, 1024),
                       idesc_bf16(128, 64, true, false), k > 0);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -326,44 +345,48 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         for (int cc = 0; cc < 32; ++cc)
             *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * hf + cc, d_row & 63)) = __float2bfloat16_rn(-w[cc]);
     };
-    // O1 = S Q^T (no commit: the next Z commit covers it)
-    auto issue_o1 = [&](int c) {
-        if (!issuer) return;
+
+    // --------------------------------------------------------------- chain group
+    // each chain thread owns TMEM lane d_row (a d_v row) and all of its columns
+    // O1 = S Q^T and Z^T = U^T - S W^T (accumulated into U[c&1])
+    auto issue_o1_z = [&](int c) {
+        if (!c_issuer) return;
         const uint32_t sXQ = stage_addr(c) + OFF_XQ;
+        const uint32_t tu = tm + TM_U + 64 * (uint32_t)(c & 1);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
             umma_bf16(tm + TM_O1, smem_desc(sS + ko, 16, 1024), smem_desc(sXQ + ko + 8192, 16, 1024),
                       idesc_bf16(128, 64, false, false), k > 0);
         }
-    };
-    // Z^T = U^T - S W^T  (accumulate into the U columns)
-    auto issue_z = [&]() {
-        if (!issuer) return;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
-            umma_bf16(tm + TM_U, smem_desc(sS + ko, 16, 1024), smem_desc(sR2 + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024),
+            umma_bf16(tu, smem_desc(sS + ko, 16, 1024), smem_desc(sR2 + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024),
                       idesc_bf16(128, 64, false, false), 1);
         }
         umma_commit(&bar_z);
     };
     // Z^T (bf16) -> R2 as [dv][64 tokens]
-    auto zt_store = [&]() {
-        float z[32];
-        tmem_ld32(tl + TM_U + 32 * hf, z);
-        tmem_ld_wait();
+    auto zt_store = [&](int c) {
+        const uint32_t tu = tl + TM_U + 64 * (uint32_t)(c & 1);
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-            float f[8];
+        for (int half = 0; half < 2; ++half) {
+            float z[32];
+            tmem_ld32(tu + 32 * half, z);
+            tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = z[8 * ch + e];
-            *reinterpret_cast<uint4 *>(sm + OFF_R2 + sw128_off(d_row, 32 * hf + 8 * ch)) = pack8(f);
+            for (int ch = 0; ch < 4; ++ch) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = z[8 * ch + e];
+                *reinterpret_cast<uint4 *>(sm + OFF_R2 + sw128_off(d_row, 32 * half + 8 * ch)) = pack8(f);
+            }
         }
     };
     // O2 = Z^T P^T ; S += Z^T (kappa K)  (S in TMEM already scaled by gamma_C)
     auto issue_mma2 = [&](int c) {
-        if (!issuer) return;
+        if (!c_issuer) return;
         const uint32_t sK = stage_addr(c) + OFF_K, sP = sbase + OFF_P + (uint32_t)(c & 1) * 8192;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -375,41 +398,50 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                       idesc_bf16(128, 128, false, true), 1);
         umma_commit(&bar_o2);
     };
+    // bf16 copy of 32 state columns (block q of 4) into S_in
+    auto write_s_in = [&](int q, const float (&sv)[32]) {
+        uint8_t *sp = sm + OFF_S + (q >> 1) * 16384;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = sv[8 * ch + e];
+            *reinterpret_cast<uint4 *>(sp + sw128_off(d_row, 32 * (q & 1) + 8 * ch)) = pack8(f);
+        }
+    };
     // o_t = gamma_t O1 + O2 straight to global memory; state -> bf16 S_in for the next
     // chunk, rescaled in TMEM by the next chunk's gamma_C (or written out after the last)
     auto epilogue = [&](int c) {
         const int t0 = c * kC;
         const float *gam = g_gam[c % 3];
-        float o1[32], o2[32];
-        tmem_ld32(tl + TM_O1 + 32 * hf, o1);
-        tmem_ld32(tl + TM_O2 + 32 * hf, o2);
-        tmem_ld_wait();
-        __nv_bfloat16 *og = p.o + ((size_t)b * T + t0 + 32 * hf) * H * kD + (size_t)h * kD + d_row;
-        const int nvalid = T - t0 - 32 * hf;
-#pragma unroll
-        for (int cc = 0; cc < 32; ++cc)
-            if (cc < nvalid) og[(size_t)cc * H * kD] = __float2bfloat16_rn(fmaf(gam[32 * hf + cc], o1[cc], o2[cc]));
-        const bool last = (c + 1 == nchunks);
-        const float gN = last ? 1.f : g_gam[(c + 1) % 3][kC - 1];
-        uint8_t *sp = sm + OFF_S + hf * 16384;
+        __nv_bfloat16 *og = p.o + ((size_t)b * T + t0) * H * kD + (size_t)h * kD + d_row;
+        const int nvalid = T - t0;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            float sv[32];
-            tmem_ld32(tl + TM_S + 64 * hf + 32 * half, sv);
+            float o1[32], o2[32];
+            tmem_ld32(tl + TM_O1 + 32 * half, o1);
+            tmem_ld32(tl + TM_O2 + 32 * half, o2);
             tmem_ld_wait();
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = sv[8 * ch + e];
-                *reinterpret_cast<uint4 *>(sp + sw128_off(d_row, 32 * half + 8 * ch)) = pack8(f);
+            for (int cc = 0; cc < 32; ++cc) {
+                const int t = 32 * half + cc;
+                if (t < nvalid) og[(size_t)t * H * kD] = __float2bfloat16_rn(fmaf(gam[t], o1[cc], o2[cc]));
             }
+        }
+        const bool last = (c + 1 == nchunks);
+        const float gN = last ? 1.f : g_gam[(c + 1) % 3][kC - 1];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float sv[32];
+            tmem_ld32(tl + TM_S + 32 * q, sv);
+            tmem_ld_wait();
+            write_s_in(q, sv);
             if (!last) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) sv[e] *= gN;
-                tmem_st32(tl + TM_S + 64 * hf + 32 * half, sv);
+                tmem_st32(tl + TM_S + 32 * q, sv);
             } else if (p.S_final && !abort_flag) {
-                float *dst = p.S_final + ((size_t)bh * kD + d_row) * kD + 64 * hf + 32 * half;
+                float *dst = p.S_final + ((size_t)bh * kD + d_row) * kD + 32 * q;
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
             }
@@ -417,101 +449,96 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         tmem_st_wait();
     };
 
-    // initial state: bf16 copy in S_in, fp32 in TMEM scaled by chunk 0's gamma_C
-    {
-        const size_t base = ((size_t)bh * kD + d_row) * kD + 64 * hf;
-        const float g0 = g_gam[0][kC - 1];
-        uint8_t *sp = sm + OFF_S + hf * 16384;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float sv[32];
-#pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                float4 v = p.S0 ? *reinterpret_cast<const float4 *>(p.S0 + base + 32 * half + j)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-                sv[j] = v.x; sv[j + 1] = v.y; sv[j + 2] = v.z; sv[j + 3] = v.w;
+    int loads_issued = nchunks > 1 ? 2 : 1;             // the chain issuer's bookkeeping for a drain
+    if (prep) {
+        for (int c = 0; c < nchunks; ++c) {
+            if (warp == 4 && c + 1 < nchunks) load_gates(c + 1);   // arrays built in solve(c)
+            wait_on(&bar_full[c & 1], (uint32_t)((c >> 1) & 1));
+            x_pass(c);
+            psync();
+            issue_gram(c);
+            wait_mma(&bar_g, c);
+            if (c >= 2) {                                 // P[c&1] and U[c&1] free
+                wait_on(&bar_cdone[c & 1], (uint32_t)(((c - 2) >> 1) & 1));
+                tc_fence_after();
             }
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = sv[8 * ch + e];
-                *reinterpret_cast<uint4 *>(sp + sw128_off(d_row, 32 * half + 8 * ch)) = pack8(f);
+            masks(c);
+            if (c >= 1) {                                 // R2 free (scratch, then -W)
+                wait_on(&bar_cdone[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1));
+                tc_fence_after();
             }
-#pragma unroll
-            for (int e = 0; e < 32; ++e) sv[e] *= g0;
-            tmem_st32(tl + TM_S + 64 * hf + 32 * half, sv);
-        }
-        tmem_st_wait();
-    }
-
-    // chunk 0's state-independent work, then O1(0)
-    wait_on(&bar_full[0], 0);
-    x_pass(0);
-    sync_for_mma();
-    issue_gram(0);
-    wait_mma(&bar_g, 0);
-    masks(0);
-    tc_fence_before();
-    __syncthreads();
-    solve(0);
-    sync_for_mma();
-    issue_uw(0);
-    wait_mma(&bar_uw, 0);
-    w_store();
-    sync_for_mma();
-    issue_o1(0);
-
-    int loads_issued = nchunks > 1 ? 2 : 1;              // producer's bookkeeping for a drain
-    for (int c = 0; c < nchunks && !abort_flag; ++c) {
-        const bool more = (c + 1 < nchunks);
-        issue_z();                                        // covers O1(c) too
-        if (warp == 4 && c + 2 < nchunks) load_gates(c + 2);
-        if (more) {
-            wait_on(&bar_full[(c + 1) & 1], (uint32_t)(((c + 1) >> 1) & 1));
-            x_pass(c + 1);
-            sync_for_mma();
-            issue_gram(c + 1);
-        }
-        wait_mma(&bar_z, c);
-        zt_store();
-        sync_for_mma();
-        issue_mma2(c);
-        if (more) {
-            wait_mma(&bar_g, c + 1);
-            masks(c + 1);
             tc_fence_before();
-            __syncthreads();
-            solve(c + 1);
-            sync_for_mma();
-            issue_uw(c + 1);
-        }
-        wait_mma(&bar_o2, c);
-        if (producer && c + 2 < nchunks) {                // chunk c's stage is consumed
-            issue_loads(c + 2);
-            ++loads_issued;
-        }
-        epilogue(c);
-        sync_for_mma();
-        if (more) {
-            issue_o1(c + 1);
-            wait_mma(&bar_uw, c + 1);
+            named_sync(kBarPrep, kPrepThreads);
+            tc_fence_after();
+            solve(c);
+            psync();
+            issue_uw(c);
+            wait_mma(&bar_uw, c);
             w_store();
-            sync_for_mma();
+            fence_proxy_async();
+            tc_fence_before();
+            const bool stop = named_sync_or(kBarPrep, kPrepThreads, abort_flag != 0);
+            if (tid == 0) mbar_arrive(&bar_ready);
+            if (stop) break;
+        }
+    } else {
+        // initial state: bf16 copy in S_in, fp32 in TMEM scaled by chunk 0's gamma_C
+        {
+            const size_t base = ((size_t)bh * kD + d_row) * kD;
+            const float g0 = g_gam[0][kC - 1];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float sv[32];
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    float4 v = p.S0 ? *reinterpret_cast<const float4 *>(p.S0 + base + 32 * q + j)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                    sv[j] = v.x; sv[j + 1] = v.y; sv[j + 2] = v.z; sv[j + 3] = v.w;
+                }
+                write_s_in(q, sv);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) sv[e] *= g0;
+                tmem_st32(tl + TM_S + 32 * q, sv);
+            }
+            tmem_st_wait();
+        }
+        csync();
+        for (int c = 0; c < nchunks; ++c) {
+            wait_on(&bar_ready, (uint32_t)(c & 1));
+            tc_fence_after();
+            issue_o1_z(c);
+            wait_mma(&bar_z, c);
+            zt_store(c);
+            csync();
+            issue_mma2(c);
+            wait_mma(&bar_o2, c);
+            if (c_issuer) {
+                mbar_arrive(&bar_cdone[c & 1]);
+                if (c + 2 < nchunks) {                    // chunk c's stage is consumed
+                    issue_loads(c + 2);
+                    ++loads_issued;
+                }
+            }
+            epilogue(c);
+            fence_proxy_async();
+            tc_fence_before();
+            const bool stop = named_sync_or(kBarChain, kChainThreads, abort_flag != 0);
+            tc_fence_after();
+            if (stop) break;
         }
     }
 
     if (abort_flag) {
         // wind down: let this CTA's copies and MMAs finish (bounded) before freeing TMEM
-        if (producer)
+        if (c_issuer)
             for (int s = 0; s < 2; ++s) {
                 const int n_s = (loads_issued + 1 - s) / 2;   // loads issued into stage s
                 if (n_s > 0) mbar_wait(&bar_full[s], (uint32_t)((n_s - 1) & 1), kWaitNs);
             }
-        if (issuer) {
-            umma_commit(&bar_z);
-            mbar_wait(&bar_z, 0, kWaitNs);
-            mbar_wait(&bar_z, 1, kWaitNs);
+        if (p_issuer || c_issuer) {
+            uint64_t *dr = &bar_drain[p_issuer ? 0 : 1];
+            umma_commit(dr);
+            mbar_wait(dr, 0, kWaitNs);
         }
         if (lane == 0) atomicExch(&g_tc_timeout, 1u);
     }
@@ -536,7 +563,7 @@ cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nla
     if (e != cudaSuccess) return e;
     TcParams p{(const __nv_bfloat16 *)a.alpha, (const __nv_bfloat16 *)a.beta, (const __nv_bfloat16 *)a.lam,
                a.S0, (__nv_bfloat16 *)a.o, a.S_final, a.B, a.T, a.H};
-    qdelta_fwd_tc_kernel<<<a.B * a.H, kThreads, kSmemBytes, s>>>(p, mq, mk, mv);
+    qdelta_fwd_tc_kernel<<<a.B * a.H, kAllThreads, kSmemBytes, s>>>(p, mq, mk, mv);
     e = cudaGetLastError();
     if (e == cudaSuccess) *nlaunch += 1;
     return e;

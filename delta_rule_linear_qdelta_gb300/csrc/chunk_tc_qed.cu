@@ -334,7 +334,7 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
 
         // (6) Tinv = (I + At)^{-1} -> R1 (twice: the U and W products read the same matrix)
         unit_lower_inverse(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_R2),
-                           sm + OFF_R1, sm + OFF_R1 + 8192, nullptr, nullptr, []() {});
+                           sm + OFF_R1, sm + OFF_R1 + 8192, nullptr, nullptr, []() {}, []() { __syncthreads(); });
         sync_for_mma();
 
         // (7) U^T = (W*V)^T Tinv^T, W^T = Ae^T Tinv^T

@@ -18,6 +18,25 @@ constexpr int kC = 64, kD = 128, kThreads = 256;
 constexpr int LA = 68;                 // fp32 row stride of the 64x64 chunk matrix (16-byte rows)
 constexpr int LY = 36;                 // fp32 row stride of the 32x32 scratch
 
+// Named barrier `id` over `count` threads (a multiple of 32).
+__device__ __forceinline__ void named_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Named barrier that also returns the OR of `pred` over the participating threads,
+// so that every thread of the group takes the same decision.
+__device__ __forceinline__ bool named_sync_or(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ float bf(__nv_bfloat16 x) { return __bfloat162float(x); }
 
 __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
@@ -48,11 +67,12 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
 //   c) 32 -> 64: T21 = -T22 (A21 T11) on the two 32x32 halves
 // Every inverted block keeps only the strict lower part of its inverse (the unit
 // diagonal is implied, zeros above), so each product is a dense loop:
-// Y = A21 + A21 T11s and T21 = -(Y + T22s Y).  Called by all kThreads threads;
-// idle() runs on every thread while warps 0-3 invert the diagonal blocks.
-template <typename Idle>
+// Y = A21 + A21 T11s and T21 = -(Y + T22s Y).  Called by kThreads threads (thread
+// indices 0..kThreads-1) that synchronise with sync(); idle() runs on every one of
+// them while warps 0-3 invert the diagonal blocks.
+template <typename Idle, typename Sync>
 __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *out1, uint8_t *out2,
-                                                   const float *s1, const float *s2, Idle idle) {
+                                                   const float *s1, const float *s2, Idle idle, Sync sync) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (warp < 4 && lane < 16) {
         const int base = 16 * warp, j = lane;
@@ -77,7 +97,7 @@ __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *
             if (i > j) M[(base + i) * LA + base + j] = t[i];
     }
     idle();
-    __syncthreads();
+    sync();
     // Y = L + L Rs (+= into out) for n x n blocks: thread owns rows r, r+n/2 and 4 columns.
     // 16 -> 32: both pairs at once (threads 0..63 pair 0, 64..127 pair 1), 2x4 outputs each
     if (tid < 128) {
@@ -101,7 +121,7 @@ __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *
         }
         *reinterpret_cast<float4 *>(Y + (16 * pr + r) * LY + c) = make_float4(y[0], y[1], y[2], y[3]);
     }
-    __syncthreads();
+    sync();
     if (tid < 128) {                                     // T10 = -(Y + T11s Y)
         const int pr = tid >> 6, u = tid & 63, r = u >> 2, c = 4 * (u & 3), base = 32 * pr;
         const float *T0 = M + (base + 16 + r) * LA + base + 16;
@@ -124,7 +144,7 @@ __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *
         }
         *reinterpret_cast<float4 *>(M + (base + 16 + r) * LA + base + c) = make_float4(-y[0], -y[1], -y[2], -y[3]);
     }
-    __syncthreads();
+    sync();
     // 32 -> 64: row r of the 32x32 blocks, columns c..c+3 (256 threads)
     {
         const int r = tid >> 3, c = 4 * (tid & 7);
@@ -146,7 +166,7 @@ __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *
             }
         }
         *reinterpret_cast<float4 *>(Y + r * LY + c) = make_float4(y0[0], y0[1], y0[2], y0[3]);
-        __syncthreads();
+        sync();
         const float *T0 = L0 + 32;                                // T22s row r
 #pragma unroll
         for (int k4 = 0; k4 < 8; ++k4) {                 // T21 = -(Y + T22s Y)
@@ -161,7 +181,7 @@ __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *
         }
         *reinterpret_cast<float4 *>(M + (32 + r) * LA + c) = make_float4(-y0[0], -y0[1], -y0[2], -y0[3]);
     }
-    __syncthreads();
+    sync();
     // Tinv*beta and Tinv*beta*gamma as bf16 [64][64] (128B swizzle) over R1
     float tv[2][8];
     int rows[2], chs[2];
@@ -176,7 +196,7 @@ __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *
             tv[n][e] = (j < rows[n]) ? M[rows[n] * LA + j] : (j == rows[n] ? 1.f : 0.f);
         }
     }
-    __syncthreads();
+    sync();
 #pragma unroll
     for (int n = 0; n < 2; ++n) {
         float f1[8], f2[8];
