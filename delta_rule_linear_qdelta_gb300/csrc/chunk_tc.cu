@@ -451,12 +451,13 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
 
     int loads_issued = nchunks > 1 ? 2 : 1;             // the chain issuer's bookkeeping for a drain
     if (prep) {
+        // chunk 0's X and Gram; afterwards chunk c+1's are issued under chunk c's U/W
+        wait_on(&bar_full[0], 0);
+        x_pass(0);
+        psync();
+        issue_gram(0);
         for (int c = 0; c < nchunks; ++c) {
             if (warp == 4 && c + 1 < nchunks) load_gates(c + 1);   // arrays built in solve(c)
-            wait_on(&bar_full[c & 1], (uint32_t)((c >> 1) & 1));
-            x_pass(c);
-            psync();
-            issue_gram(c);
             wait_mma(&bar_g, c);
             if (c >= 2) {                                 // P[c&1] and U[c&1] free
                 wait_on(&bar_cdone[c & 1], (uint32_t)(((c - 2) >> 1) & 1));
@@ -473,6 +474,12 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             solve(c);
             psync();
             issue_uw(c);
+            if (c + 1 < nchunks) {                        // TM_G was read by masks(c)
+                wait_on(&bar_full[(c + 1) & 1], (uint32_t)(((c + 1) >> 1) & 1));
+                x_pass(c + 1);
+                psync();
+                issue_gram(c + 1);
+            }
             wait_mma(&bar_uw, c);
             w_store();
             fence_proxy_async();
