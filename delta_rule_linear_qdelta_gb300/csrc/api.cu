@@ -67,7 +67,10 @@ const char *qd_last_error(void) { return g_err; }
 
 int qd_last_launch_count(void) { return g_launches; }
 
-size_t qdelta_workspace_bytes(int, int, int, int, int, int, qd_dtype) { return 0; }
+size_t qdelta_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype) {
+    if (B <= 0 || T <= 0 || H <= 0 || chunk != 64) return 0;
+    return qd::qdelta_segment_workspace(B, H, qd::qdelta_segments(B, T, H, dk, dv, dtype));
+}
 
 size_t qed_workspace_bytes(int, int, int, int, int, int, qd_dtype) { return 0; }
 
@@ -87,8 +90,13 @@ qd_status qdelta_fwd(const void *q, const void *k, const void *v, const void *al
     if (B == 0 || H == 0) { g_launches = 0; return QD_OK; }
     if (T == 0) { g_launches = 0; return empty_sequence(S0, S_final, B, H, dk, dv, stream); }
     qd::QDeltaArgs a{q, k, v, alpha, beta, lam, S0, o, S_final, B, T, H, dk, dv, workspace, workspace_bytes};
-    cudaError_t e = qd::qdelta_tc_supported(a, dtype) ? qd::launch_qdelta_chunk_tc(a, stream, &n)
-                                                      : qd::launch_qdelta_chunk_simt(a, dtype, stream, &n);
+    cudaError_t e;
+    if (qd::qdelta_tc_supported(a, dtype)) {
+        const int G = qd::qdelta_segments(B, T, H, dk, dv, dtype);
+        e = G > 1 ? qd::launch_qdelta_segmented(a, G, stream, &n) : qd::launch_qdelta_chunk_tc(a, stream, &n);
+    } else {
+        e = qd::launch_qdelta_chunk_simt(a, dtype, stream, &n);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "qdelta_fwd launch");
     g_launches = n;
     return QD_OK;

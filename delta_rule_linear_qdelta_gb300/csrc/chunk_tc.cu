@@ -83,6 +83,7 @@ struct TcParams {
     __nv_bfloat16 *o;
     float *S_final;
     int B, T, H;
+    int flags;   // kTcNoV | kTcS0Identity | kTcNoO (segment-scan passes)
 };
 
 __global__ void __launch_bounds__(kAllThreads, 1)
@@ -105,6 +106,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     const int nchunks = (T + kC - 1) / kC;
     const bool p_issuer = (tid == 32), c_issuer = (tid == kPrepThreads);
     const int d_row = 32 * q4 + lane;                  // this thread's TMEM lane / state row
+    const bool no_v = p.flags & kTcNoV, no_o = p.flags & kTcNoO, s0_id = p.flags & kTcS0Identity;
 
     if (tid == 0) {
         mbar_init(&bar_full[0], 1);
@@ -133,12 +135,12 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         const int s = c & 1;
         uint8_t *st = sm + s * kStageBytes;
         const int t0 = c * kC;
-        mbar_arrive_expect_tx(&bar_full[s], kTmaBytes);
+        mbar_arrive_expect_tx(&bar_full[s], no_v ? kTmaBytes / 3 * 2 : kTmaBytes);
 #pragma unroll
         for (int pnl = 0; pnl < 2; ++pnl) {
             tma_load_4d(st + OFF_XQ + pnl * 16384 + 8192, &tmQ, &bar_full[s], 64 * pnl, h, t0, b);
             tma_load_4d(st + OFF_K + pnl * 8192, &tmK, &bar_full[s], 64 * pnl, h, t0, b);
-            tma_load_4d(st + OFF_V + pnl * 8192, &tmV, &bar_full[s], 64 * pnl, h, t0, b);
+            if (!no_v) tma_load_4d(st + OFF_V + pnl * 8192, &tmV, &bar_full[s], 64 * pnl, h, t0, b);
         }
     };
     // gates of a chunk: lane l of warp 4 holds tokens 2l and 2l+1.  The loads land in raw
@@ -325,10 +327,11 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         if (!p_issuer) return;
         const uint32_t sXQ = stage_addr(c) + OFF_XQ, sV = stage_addr(c) + OFF_V;
         const uint32_t tu = tm + TM_U + 64 * (uint32_t)(c & 1);
+        if (!no_v)
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            umma_bf16(tu, smem_desc(sV + k * 2048, 8192, 1024), smem_desc(sR1 + k * 32, 16, 1024),
-                      idesc_bf16(128, 64, true, false), k > 0);
+            for (int k = 0; k < 4; ++k)
+                umma_bf16(tu, smem_desc(sV + k * 2048, 8192, 1024), smem_desc(sR1 + k * 32, 16, 1024),
+                          idesc_bf16(128, 64, true, false), k > 0);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
             umma_bf16(tm + TM_W, smem_desc(sXQ + k * 2048, 16384, 1024), smem_desc(sR1 + 8192 + k * 32, 16, 1024),
@@ -363,7 +366,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         for (int k = 0; k < 8; ++k) {
             const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
             umma_bf16(tu, smem_desc(sS + ko, 16, 1024), smem_desc(sR2 + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024),
-                      idesc_bf16(128, 64, false, false), 1);
+                      idesc_bf16(128, 64, false, false), (no_v && k == 0) ? 0u : 1u);
         }
         umma_commit(&bar_z);
     };
@@ -425,7 +428,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
             for (int cc = 0; cc < 32; ++cc) {
                 const int t = 32 * half + cc;
-                if (t < nvalid) og[(size_t)t * H * kD] = __float2bfloat16_rn(fmaf(gam[t], o1[cc], o2[cc]));
+                if (t < nvalid && !no_o) og[(size_t)t * H * kD] = __float2bfloat16_rn(fmaf(gam[t], o1[cc], o2[cc]));
             }
         }
         const bool last = (c + 1 == nchunks);
@@ -502,6 +505,9 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                                     : make_float4(0.f, 0.f, 0.f, 0.f);
                     sv[j] = v.x; sv[j + 1] = v.y; sv[j + 2] = v.z; sv[j + 3] = v.w;
                 }
+                if (s0_id)
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) sv[j] = (32 * q + j == d_row) ? 1.f : 0.f;
                 write_s_in(q, sv);
 #pragma unroll
                 for (int e = 0; e < 32; ++e) sv[e] *= g0;
@@ -557,10 +563,11 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
 }  // namespace
 
 bool qdelta_tc_supported(const QDeltaArgs &a, int dtype) {
+    if (a.T <= 0) return false;
     return dtype == kBF16 && a.dk == kD && a.dv == kD && (long long)a.T * a.H * kD * 2 < (1ll << 40);
 }
 
-cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nlaunch) {
+cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nlaunch, int flags) {
     CUtensorMap mq, mk, mv;
     if (!make_token_map(&mq, a.q, a.B, a.T, a.H) || !make_token_map(&mk, a.k, a.B, a.T, a.H) ||
         !make_token_map(&mv, a.v, a.B, a.T, a.H))
@@ -569,7 +576,7 @@ cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nla
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     TcParams p{(const __nv_bfloat16 *)a.alpha, (const __nv_bfloat16 *)a.beta, (const __nv_bfloat16 *)a.lam,
-               a.S0, (__nv_bfloat16 *)a.o, a.S_final, a.B, a.T, a.H};
+               a.S0, (__nv_bfloat16 *)a.o, a.S_final, a.B, a.T, a.H, flags};
     qdelta_fwd_tc_kernel<<<a.B * a.H, kAllThreads, kSmemBytes, s>>>(p, mq, mk, mv);
     e = cudaGetLastError();
     if (e == cudaSuccess) *nlaunch += 1;

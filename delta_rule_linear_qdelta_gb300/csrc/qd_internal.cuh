@@ -56,12 +56,21 @@ cudaError_t launch_qdelta_chunk_simt(const QDeltaArgs &a, int dtype, cudaStream_
 cudaError_t launch_qed_chunk_simt(const QedArgs &a, int dtype, cudaStream_t s, int *nlaunch);
 cudaError_t launch_qdelta_step(const StepArgs &a, int dtype, cudaStream_t s, int *nlaunch);
 
-// Tensor-core (tcgen05) chunked Q-Delta forward: bf16, dk = dv = 128.
+// Tensor-core (tcgen05) chunked Q-Delta forward: bf16, dk = dv = 128.  flags select the
+// segment-scan passes: kTcNoV (v taken as 0, v not read), kTcS0Identity (S0 = I per
+// head, needs dk = dv), kTcNoO (o not written).
+enum { kTcNoV = 1, kTcS0Identity = 2, kTcNoO = 4 };
 bool qdelta_tc_supported(const QDeltaArgs &a, int dtype);
-cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nlaunch);
+cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nlaunch, int flags = 0);
 // Tensor-core (tcgen05) chunked QED forward: bf16, dk = dv = 128.
 bool qed_tc_supported(const QedArgs &a, int dtype);
 cudaError_t launch_qed_chunk_tc(const QedArgs &a, cudaStream_t s, int *nlaunch);
+// Segment scan of the tensor-core forward for long sequences over few (b, h)
+// streams: the number of segments for these sizes (1 = a single pass), its
+// workspace, and the launch (three passes of the forward kernel and a combine).
+int qdelta_segments(int B, int T, int H, int dk, int dv, int dtype);
+size_t qdelta_segment_workspace(int B, int H, int G);
+cudaError_t launch_qdelta_segmented(const QDeltaArgs &a, int G, cudaStream_t s, int *nlaunch);
 // Reads and clears the device word the tensor-core kernels set when a bounded wait runs out.
 bool tc_read_and_clear_timeout();
 bool qed_tc_read_and_clear_timeout();

@@ -1,0 +1,139 @@
+// Segment scan for long sequences over few (b, h) streams.
+//
+// A chunk of the Q-Delta recurrence maps its entering state linearly
+// ("Q-Delta: Beyond Key-Value Associative State Evolution", Sec. 3.3.2: with the
+// chunk's WY factors, S_out = gamma_C S_in + (U - W S_in^T)^T K_out), so
+//     S_out = S_in Phi + Psi,   Phi = gamma_C I - W^T K_out  (d_k x d_k),  Psi = U^T K_out,
+// and so does any run of chunks: a segment's map is the product of its chunks' maps.
+// When B*H streams leave most SMs idle, each sequence is cut into G segments
+// that run side by side as a [B*G][T/G] batch of the same tensor-core kernel:
+//   pass 1  S0 = 0, v as given        ->  final state = Psi_g
+//   pass 2  S0 = I, v taken as 0      ->  final state = Phi_g
+//   combine (fp32, per (b, h), in segment order): S_start(g) = S, S <- S Phi_g + Psi_g
+//   pass 3  S0 = S_start(g)           ->  o, exactly as one pass over the whole sequence
+// The [B][T][H][d] layout makes the segment view free: [B][G*L][H][d] is [B*G][L][H][d].
+// The three per-segment state arrays live in caller-provided workspace.
+#include <cuda_runtime.h>
+
+#include "qd_internal.cuh"
+
+namespace qd {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kLS = 132;          // smem row stride (16-byte aligned rows)
+constexpr int kCombineThreads = 256;
+
+// one CTA per (b, h): S [128][kLS] and Phi [128][kLS] in shared memory; thread owns
+// rows r0..r0+3 and columns c0..c0+15 of the product
+__global__ void __launch_bounds__(kCombineThreads)
+segment_combine_kernel(const float *S0, const float *Phi, const float *Psi, float *S_start, float *S_final,
+                       int B, int H, int G) {
+    extern __shared__ float sm[];
+    float *Ss = sm, *Ps = sm + kD * kLS;
+    const int tid = threadIdx.x;
+    const int bh = blockIdx.x, b = bh / H, h = bh % H;
+    const int r0 = 4 * (tid >> 3), c0 = 16 * (tid & 7);
+    const size_t mat = (size_t)kD * kD;
+    for (int i = tid; i < kD * kD / 4; i += kCombineThreads) {
+        const int r = (4 * i) / kD, c = (4 * i) % kD;
+        const float4 v = S0 ? reinterpret_cast<const float4 *>(S0 + (size_t)bh * mat)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(Ss + r * kLS + c) = v;
+    }
+    __syncthreads();
+    for (int g = 0; g < G; ++g) {
+        const size_t seg = ((size_t)(b * G + g) * H + h) * mat;   // (b*G + g, h) in the segment batch
+        for (int i = tid; i < kD * kD / 4; i += kCombineThreads) {
+            const int r = (4 * i) / kD, c = (4 * i) % kD;
+            reinterpret_cast<float4 *>(S_start + seg)[i] = *reinterpret_cast<const float4 *>(Ss + r * kLS + c);
+            *reinterpret_cast<float4 *>(Ps + r * kLS + c) = reinterpret_cast<const float4 *>(Phi + seg)[i];
+        }
+        __syncthreads();
+        float acc[4][16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(Psi + seg + (size_t)(r0 + i) * kD + c0 + j);
+                acc[i][j] = v.x; acc[i][j + 1] = v.y; acc[i][j + 2] = v.z; acc[i][j + 3] = v.w;
+            }
+        for (int k = 0; k < kD; ++k) {
+            float a[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) a[i] = Ss[(r0 + i) * kLS + k];
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+                const float4 p = *reinterpret_cast<const float4 *>(Ps + k * kLS + c0 + j);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[i][j] = fmaf(a[i], p.x, acc[i][j]);
+                    acc[i][j + 1] = fmaf(a[i], p.y, acc[i][j + 1]);
+                    acc[i][j + 2] = fmaf(a[i], p.z, acc[i][j + 2]);
+                    acc[i][j + 3] = fmaf(a[i], p.w, acc[i][j + 3]);
+                }
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+                *reinterpret_cast<float4 *>(Ss + (r0 + i) * kLS + c0 + j) =
+                    make_float4(acc[i][j], acc[i][j + 1], acc[i][j + 2], acc[i][j + 3]);
+        __syncthreads();
+    }
+    if (S_final)
+        for (int i = tid; i < kD * kD / 4; i += kCombineThreads) {
+            const int r = (4 * i) / kD, c = (4 * i) % kD;
+            reinterpret_cast<float4 *>(S_final + (size_t)bh * mat)[i] = *reinterpret_cast<const float4 *>(Ss + r * kLS + c);
+        }
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+}  // namespace
+
+int qdelta_segments(int B, int T, int H, int dk, int dv, int dtype) {
+    if (dtype != kBF16 || dk != kD || dv != kD) return 1;
+    const long long streams = (long long)B * H;
+    const int nsm = sm_count();
+    int G = 1;
+    while (streams * 2 * G <= nsm && T % (2 * G) == 0 && T / (2 * G) >= 1024) G *= 2;
+    return G;
+}
+
+size_t qdelta_segment_workspace(int B, int H, int G) {
+    return G > 1 ? 3 * (size_t)B * G * H * kD * kD * sizeof(float) : 0;
+}
+
+cudaError_t launch_qdelta_segmented(const QDeltaArgs &a, int G, cudaStream_t s, int *nlaunch) {
+    const size_t n = (size_t)a.B * G * a.H * kD * kD;
+    float *S_start = static_cast<float *>(a.ws), *Psi = S_start + n, *Phi = Psi + n;
+    QDeltaArgs seg = a;
+    seg.B = a.B * G;
+    seg.T = a.T / G;
+    seg.S0 = nullptr;
+    seg.S_final = Psi;
+    cudaError_t e = launch_qdelta_chunk_tc(seg, s, nlaunch, kTcNoO);
+    if (e != cudaSuccess) return e;
+    seg.S_final = Phi;
+    e = launch_qdelta_chunk_tc(seg, s, nlaunch, kTcNoO | kTcNoV | kTcS0Identity);
+    if (e != cudaSuccess) return e;
+    const size_t smem = 2 * kD * kLS * sizeof(float);
+    e = cudaFuncSetAttribute(segment_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    segment_combine_kernel<<<a.B * a.H, kCombineThreads, smem, s>>>(a.S0, Phi, Psi, S_start, a.S_final, a.B, a.H, G);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    *nlaunch += 1;
+    seg.S0 = S_start;
+    seg.S_final = nullptr;
+    return launch_qdelta_chunk_tc(seg, s, nlaunch, 0);
+}
+
+}  // namespace qd

@@ -66,7 +66,11 @@ typedef enum { QD_F32 = 0, QD_BF16 = 1 } qd_dtype;
  *
  * workspace: device scratch of at least qdelta_workspace_bytes(...) bytes
  * (may be NULL when that returns 0).  Calls that share a workspace must be
- * ordered on one stream.
+ * ordered on one stream.  A workspace is needed when few (b, h) streams carry a
+ * long sequence (bf16, dk = dv = 128): each sequence is then cut into segments
+ * that run in parallel (the chunk map S -> S Phi + Psi is linear in the state)
+ * and are stitched together in fp32; the workspace holds three d_v x d_k fp32
+ * states per segment.
  */
 QD_API qd_status qdelta_fwd(const void *q, const void *k, const void *v,
                      const void *alpha, const void *beta, const void *lam,

@@ -147,6 +147,19 @@ def test_long_context_full_size_sampled(qd):
     check(np.stack([S[b, h] for b, h in pairs])[:, None], S_ref, "bf16", name + " S")
 
 
+@pytest.mark.parametrize("mode", ["qdelta", "deltanet"])
+def test_segmented_long_sequence_all_outputs(qd, mode):
+    """B=1, H=2, T=4096: few streams and a long sequence take the segment scan
+    (several segments in parallel, stitched by their linear state maps)."""
+    d = synth.qdelta_inputs(1, 4096, 2, 128, 128, seed=55, dtype="bf16", mode=mode, s0_var=0.01)
+    assert qd.qdelta_workspace_bytes(1, 4096, 2, 128, 128) > 0
+    o, S = run_qdelta(qd, d)
+    assert qd.last_launch_count() == 4
+    o_ref, S_ref = oracle.qdelta_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["lam"], d["S0"])
+    check(o, o_ref, "bf16", f"segmented {mode} o")
+    check(S, S_ref, "bf16", f"segmented {mode} S")
+
+
 def test_split_call_carries_state_in_place(qd):
     """fwd(T1) then fwd(T2, S0 = S_T1) equals one fwd(T1+T2); S0 aliases S_final."""
     d = synth.qdelta_inputs(2, 300, 2, 128, 128, seed=50, dtype="bf16", mode="qdelta", s0_var=0.01)
