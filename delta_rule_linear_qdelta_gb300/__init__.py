@@ -6,7 +6,7 @@ calls the library on the current CUDA stream.  Every step of the computation
 runs in the library's CUDA kernels; there is no CPU path.  If the shared
 library is missing this module raises instead of computing anything.
 
-Functions keep the C names: qdelta_fwd, qed_fwd, qdelta_step,
+Functions keep the C names: qdelta_fwd, qed_fwd, qdelta_step, qdelta_fwd_static_scratch,
 qdelta_workspace_bytes, qed_workspace_bytes, qd_device_status, qd_last_error.
 """
 from __future__ import annotations
@@ -24,7 +24,7 @@ QD_F32, QD_BF16 = 0, 1
 STATUS_NAMES = {0: "QD_OK", 1: "QD_ERR_ARG", 2: "QD_ERR_UNSUPPORTED", 3: "QD_ERR_CUDA",
                 4: "QD_ERR_TIMEOUT", 5: "QD_ERR_WORKSPACE"}
 EXPORTS = ("qdelta_fwd", "qdelta_workspace_bytes", "qed_fwd", "qed_workspace_bytes", "qdelta_step",
-           "qd_device_status", "qd_last_error", "qd_last_launch_count")
+           "qdelta_fwd_static_scratch", "qd_device_status", "qd_last_error", "qd_last_launch_count")
 
 
 class QDError(RuntimeError):
@@ -47,12 +47,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
     P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     lib.qdelta_fwd.argtypes = [P] * 9 + [I] * 7 + [P, Z, P]
+    lib.qdelta_fwd_static_scratch.argtypes = [P] * 9 + [I] * 7 + [P]
     lib.qed_fwd.argtypes = [P] * 10 + [I] * 7 + [P, Z, P]
     lib.qdelta_step.argtypes = [P] * 8 + [I] * 5 + [P]
     lib.qdelta_workspace_bytes.argtypes = [I] * 7
     lib.qed_workspace_bytes.argtypes = [I] * 7
     lib.qd_device_status.argtypes = [P]
-    for f in (lib.qdelta_fwd, lib.qed_fwd, lib.qdelta_step, lib.qd_device_status, lib.qd_last_launch_count):
+    for f in (lib.qdelta_fwd, lib.qed_fwd, lib.qdelta_step, lib.qdelta_fwd_static_scratch, lib.qd_device_status,
+              lib.qd_last_launch_count):
         f.restype = I
     lib.qdelta_workspace_bytes.restype = Z
     lib.qed_workspace_bytes.restype = Z
@@ -155,6 +157,35 @@ def qdelta_fwd(q, k, v, alpha, beta, lam, S0=None, *, o=None, S_final=None, retu
                                    _ptr(o), _ptr(S_final), B, T, H, dk, dv, chunk, code, _ptr(workspace),
                                    wsb, _stream(stream, q.device))
     _check(st, "qdelta_fwd")
+    return o, S_final
+
+
+def qdelta_fwd_static_scratch(q, k, v, alpha, beta, lam, S0=None, *, o=None, S_final=None, return_final=True,
+                              chunk=64, stream=None):
+    """qdelta_fwd without a workspace argument: for callers that cannot allocate
+    device memory at call time, any scratch comes from a fixed 24 MiB array inside
+    the library (sizes needing more raise QDError with QD_ERR_WORKSPACE).  Calls
+    whose work overlaps on the GPU share that array and race."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    _need(q, "q", dt, (B, T, H, dk))
+    _need(k, "k", dt, (B, T, H, dk))
+    _need(v, "v", dt, (B, T, H, dv))
+    _need(beta, "beta", dt, (B, T, H))
+    _need(alpha, "alpha", dt, (B, T, H), optional=True)
+    _need(lam, "lam", dt, (B, T, H), optional=True)
+    _need(S0, "S0", torch.float32, (B, H, dv, dk), optional=True)
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=dt, device=q.device)
+    _need(o, "o", dt, (B, T, H, dv))
+    if S_final is None and return_final:
+        S_final = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
+    _need(S_final, "S_final", torch.float32, (B, H, dv, dk), optional=True)
+    st = load_library().qdelta_fwd_static_scratch(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(lam),
+                                                  _ptr(S0), _ptr(o), _ptr(S_final), B, T, H, dk, dv, chunk,
+                                                  _dtype_code(q), _stream(stream, q.device))
+    _check(st, "qdelta_fwd_static_scratch")
     return o, S_final
 
 

@@ -61,6 +61,10 @@ qd_status empty_sequence(const float *S0, float *S_final, int B, int H, int dk, 
 
 }  // namespace
 
+namespace qd {
+qd_status report_error(qd_status status, const char *msg) { return fail(status, "%s", msg); }
+}  // namespace qd
+
 extern "C" {
 
 const char *qd_last_error(void) { return g_err; }

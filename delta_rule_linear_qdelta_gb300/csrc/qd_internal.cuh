@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/qdelta.h"
+
 namespace qd {
 
 enum { kF32 = 0, kBF16 = 1 };
@@ -74,5 +76,8 @@ cudaError_t launch_qdelta_segmented(const QDeltaArgs &a, int G, cudaStream_t s, 
 // Reads and clears the device word the tensor-core kernels set when a bounded wait runs out.
 bool tc_read_and_clear_timeout();
 bool qed_tc_read_and_clear_timeout();
+
+// Records `msg` as this host thread's last error (qd_last_error) and returns `status`.
+qd_status report_error(qd_status status, const char *msg);
 
 }  // namespace qd

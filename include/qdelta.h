@@ -115,6 +115,30 @@ QD_API qd_status qdelta_step(float *S, const void *q, const void *k, const void 
                       int N, int H, int dk, int dv, qd_dtype dtype, cudaStream_t stream);
 
 /*
+ * qdelta_fwd_static_scratch -- qdelta_fwd for callers that cannot allocate device
+ * memory at call time.  The pages have no counterpart: this is a property of the
+ * library, not of the method.
+ *
+ * Some callers cannot pass a workspace: plain C code that holds only the input and
+ * output pointers and no device allocator, or a serving loop whose device memory is
+ * reserved up front and that must not call cudaMalloc (which can synchronise the
+ * device and can fail under memory pressure) during a step.  This entry point takes
+ * no workspace and allocates nothing.  Arguments and results are those of
+ * qdelta_fwd.  When the segment scan needs scratch it uses a fixed 24 MiB array in
+ * the library's device image (room for 128 segment-heads, B * G * H, of three
+ * 128 x 128 fp32 states), which every GPU that loads the library holds until the
+ * process exits.  Sizes needing more return QD_ERR_WORKSPACE.
+ * The array's device address is looked up on the first call made on each device,
+ * so make that first call before any stream capture.  All calls share the array:
+ * calls whose work overlaps on the GPU race on it.
+ */
+QD_API qd_status qdelta_fwd_static_scratch(const void *q, const void *k, const void *v,
+                                           const void *alpha, const void *beta, const void *lam,
+                                           const float *S0, void *o, float *S_final,
+                                           int B, int T, int H, int dk, int dv, int chunk,
+                                           qd_dtype dtype, cudaStream_t stream);
+
+/*
  * qd_device_status -- synchronises `stream`, then reports whether any kernel of
  * this library gave up a bounded wait since the last call (QD_ERR_TIMEOUT) or the
  * stream holds a CUDA error (QD_ERR_CUDA).  Clears the timeout flag.
