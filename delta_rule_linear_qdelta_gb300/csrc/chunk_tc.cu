@@ -1,6 +1,6 @@
 // Fused chunked Q-Delta forward on the sm_103a tensor cores (tcgen05 + TMEM + TMA),
 // bf16 inputs, dk = dv = 128, chunk C = 64, fp32 state held on chip for the whole
-// sequence.  One CTA of 8 warps per (b, h).
+// sequence.  One CTA of 12 warps per (b, h).
 //
 // Algorithm ("Q-Delta: Beyond Key-Value Associative State Evolution", Sec. 3.3.2,
 // Eqs. 20-27, with the corrected transposes and gamma_r/gamma_i decay; the two UT
@@ -14,9 +14,12 @@
 //   o_t    = gamma_t (S Q^T)_t + (Z^T P^T)_t
 //   S     <- gamma_C S + Z^T diag(kappa) K
 // Every product is written "transposed" so that the 128 TMEM lanes index d_v (or
-// d_k) and every MMA has M = 128.  The master state stays in TMEM in fp32 (the MMA
-// accumulates Z^T (kappa K) onto it after the epilogue has scaled it by the chunk's
-// gamma_C); its bf16 copy in shared memory feeds the MMAs.
+// d_k) and every MMA has M = 128.  When the chunk's decay is mild (l_C > -30) the
+// kappa scaling moves onto Z^T, and P is divided by kappa to match:
+// (Z^T diag(kappa)) (P diag(1/kappa))^T = Z^T P^T with P_ti / kappa_i = e^{l_t - l_C} (Q K^T)_ti,
+// so K is used as loaded; otherwise K is scaled in place.  The master state stays in
+// TMEM in fp32 (the MMA accumulates Z^T diag(kappa) K onto it after the epilogue has
+// scaled it by the chunk's gamma_C); its bf16 copy in shared memory feeds the MMAs.
 //
 // Warp specialisation: a prep group (warps 0-7) does the state-independent work of
 // each chunk -- X, its Gram, the decay masks, the solve, U and W -- and hands the
@@ -24,18 +27,22 @@
 // output and state products, the epilogue.  The two groups run concurrently, so the
 // chunk period is the longer of the two instead of their sum.  Each group
 // synchronises on its own named barrier; hand-offs are mbarriers:
-//   ready       prep -> chain: -W(c), P(c), U(c), kappa K(c) and the gates are in place
+//   ready       prep -> chain: P(c) and the gates are in place, U/W(c) issued (the chain
+//               waits on their commit, then writes -W^T itself)
+//   wfree       chain -> prep: W(c) has been read out of TMEM, so U/W(c+1) may be issued
 //   cdone[c&1]  chain -> prep: the output and state products of chunk c have run, so
-//               R2, P[c&1], U[c&1] and chunk c's stage are free
+//               P[c&1], U[c&1] and chunk c's stage are free
 // The chain group also issues the TMA loads of chunk c+2 into chunk c's stage.
 //
 // Shared memory (offsets from a 1024-aligned base):
 //   stage s in {0,1}: XQ 32 KB (per 64-column panel: X rows 0-63 | Q rows 64-127),
-//                     K 16 KB (overwritten in place by kappa*K), V 16 KB
+//                     K 16 KB (scaled in place to kappa*K under strong decay), V 16 KB
 //   S_in 32 KB   bf16 state [dv][dk]
 //   R1   17 KB   A fp32 [64][68]  ->  Tinv*beta, Tinv*beta*gamma (bf16)
-//   R2   16 KB   -W(c) [64][dk]  ->  Z^T(c) [dv][64]  ->  solve scratch and -W(c+1)
+//   R2   16 KB   -W^T(c) [dk][64]  ->  Z^T(c) [dv][64]  ->  o(c) [64][dv] for the TMA store
+//                (chain group only)
 //   P    2x8 KB  bf16 [64][64], by chunk parity
+//   Y    4.5 KB  fp32 scratch of the solve (prep group only)
 // All MMA operands use the 128-byte swizzle (TMA layout): 128-byte rows, 8-row
 // groups 1024 bytes apart, 64-column panels.
 // TMEM (512 columns): G 0-63, W 64-127, U[0] 128-191, U[1] 192-255, O1 256-319,
@@ -70,10 +77,15 @@ constexpr uint32_t OFF_S = 2 * kStageBytes;          // 131072
 constexpr uint32_t OFF_R1 = OFF_S + 32768;           // 163840
 constexpr uint32_t OFF_R2 = OFF_R1 + 17408;          // 181248
 constexpr uint32_t OFF_P = OFF_R2 + 16384;           // 197632 (two 8 KB buffers)
-constexpr uint32_t kSmemUsed = OFF_P + 16384;        // 214016
+constexpr uint32_t OFF_Y = OFF_P + 16384;           // 214016 (solve scratch, 32 x LY fp32)
+constexpr uint32_t kSmemUsed = OFF_Y + 32 * LY * 4;  // 218624
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
 constexpr uint32_t kTmaBytes = 3 * kC * kD * 2;      // Q, K, V tiles per chunk
 constexpr uint64_t kWaitNs = 2000000000ull;          // 2 s per wait
+
+// fold kappa into Z^T (and 1/kappa into P) when the chunk's log-decay l_C exceeds this:
+// then kappa >= e^-30 and gamma_t / gamma_C <= e^30, far from bf16 under/overflow
+constexpr float kFoldLog = -30.f;
 
 constexpr uint32_t TM_G = 0, TM_W = 64, TM_U = 128, TM_O1 = 256, TM_O2 = 320, TM_S = 384;
 
@@ -88,15 +100,17 @@ struct TcParams {
 
 __global__ void __launch_bounds__(kAllThreads, 1)
 qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
-                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+                     const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const __grid_constant__ CUtensorMap tmO) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t bar_full[2], bar_g, bar_uw, bar_z, bar_o2, bar_ready, bar_cdone[2], bar_drain[2];
+    __shared__ uint64_t bar_full[2], bar_g, bar_uw, bar_z, bar_o2, bar_ready, bar_wfree, bar_cdone[2], bar_drain[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
-    // per-chunk gate arrays, by chunk index mod 3 (the prep group runs at most one
-    // chunk ahead of the chain group's epilogue)
-    __shared__ float g_ell[3][kC], g_beta[3][kC], g_lam[3][kC], g_gam[3][kC], g_kap[3][kC], g_igam[3][kC];
+    // per-chunk gate arrays, by chunk index mod 4: while the prep group builds chunk
+    // c+1's arrays (during the solve of chunk c) the chain group may still read those
+    // of chunks c-2 (its epilogue), c-1 and c
+    __shared__ float g_ell[4][kC], g_beta[4][kC], g_lam[4][kC], g_gam[4][kC], g_kap[4][kC], g_igam[4][kC];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool prep = tid < kPrepThreads;
@@ -116,6 +130,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         mbar_init(&bar_z, 1);
         mbar_init(&bar_o2, 1);
         mbar_init(&bar_ready, 1);
+        mbar_init(&bar_wfree, 1);
         mbar_init(&bar_cdone[0], 1);
         mbar_init(&bar_cdone[1], 1);
         mbar_init(&bar_drain[0], 1);
@@ -125,6 +140,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        if (!(p.flags & kTcNoO)) tma_prefetch_desc(&tmO);
     }
     if (warp == 0) {
         tmem_alloc(&tmem_base, 512);
@@ -158,7 +174,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     };
     // warp-wide: log-prefix l, gamma = e^l, kappa = e^{l_C - l}, e^{-l} of chunk c
     auto compute_gates = [&](int c) {
-        const int buf = c % 3;
+        const int buf = c & 3;
         float ga[2], gb[2], gl[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {                  // tokens past T: alpha 1, beta 0, lambda 0
@@ -234,7 +250,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     // X = K + lambda Q into rows 0-63 of the XQ panels of chunk c's stage
     auto x_pass = [&](int c) {
         uint8_t *st = sm + (c & 1) * kStageBytes;
-        const float *lam = g_lam[c % 3];
+        const float *lam = g_lam[c & 3];
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int u = tid + kPrepThreads * r;         // 16-byte chunk index, 0..1023
@@ -261,10 +277,10 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         }
         umma_commit(&bar_g);
     };
-    // decay masks: A (fp32, R1) from the X K^T rows, P (bf16) from the Q K^T rows; K -> kappa K
+    // decay masks: A (fp32, R1) from the X K^T rows, P (bf16) from the Q K^T rows
     auto masks = [&](int c) {
-        const int gi = c % 3;
-        const float *ell = g_ell[gi], *bet = g_beta[gi], *gam = g_gam[gi], *igam = g_igam[gi], *kap = g_kap[gi];
+        const int gi = c & 3;
+        const float *ell = g_ell[gi], *bet = g_beta[gi], *gam = g_gam[gi], *igam = g_igam[gi];
         float g[32];
         tmem_ld32(tl + TM_G + 32 * hf, g);
         tmem_ld_wait();
@@ -287,6 +303,8 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         } else {
             const int t = 32 * (q4 - 2) + lane;
             const float lt = ell[t], gt = gam[t];
+            const float gtc = gt * igam[kC - 1];          // gamma_t / gamma_C (fold mode)
+            const bool fold = ell[kC - 1] > kFoldLog;
             uint8_t *P = sm + OFF_P + (c & 1) * 8192;
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
@@ -294,30 +312,19 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int i = 32 * hf + 8 * ch + e;
-                    const float pv = split ? gt * igam[i] * g[8 * ch + e] : __expf(lt - ell[i]) * g[8 * ch + e];
+                    const float pv = fold ? gtc * g[8 * ch + e]
+                                   : split ? gt * igam[i] * g[8 * ch + e] : __expf(lt - ell[i]) * g[8 * ch + e];
                     f[e] = (i <= t) ? pv : 0.f;
                 }
                 *reinterpret_cast<uint4 *>(P + sw128_off(t, 32 * hf + 8 * ch)) = pack8(f);
             }
         }
-        uint8_t *st = sm + (c & 1) * kStageBytes;
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const uint32_t off = (uint32_t)(tid + kPrepThreads * r) << 4;   // both K panels
-            uint4 *pk = reinterpret_cast<uint4 *>(st + OFF_K + off);
-            float kf[8];
-            unpack8(*pk, kf);
-            const float ka = kap[(off & 8191) >> 7];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) kf[e] *= ka;
-            *pk = pack8(kf);
-        }
     };
-    // Tinv -> Tinv*beta, Tinv*beta*gamma over R1 (scratch in R2); warp 4 meanwhile
+    // Tinv -> Tinv*beta, Tinv*beta*gamma over R1 (scratch in Y); warp 4 meanwhile
     // turns the next chunk's raw gates into arrays
     auto solve = [&](int c) {
-        const int gi = c % 3;
-        unit_lower_inverse(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_R2),
+        const int gi = c & 3;
+        unit_lower_inverse(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_Y),
                            sm + OFF_R1, sm + OFF_R1 + 8192, g_beta[gi], g_gam[gi],
                            [&]() { if (warp == 4 && c + 1 < nchunks) compute_gates(c + 1); },
                            []() { named_sync(kBarPrep, kPrepThreads); });
@@ -338,19 +345,42 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                       idesc_bf16(128, 64, true, false), k > 0);
         umma_commit(&bar_uw);
     };
-    // -W -> R2 as [64 tokens][dk] (two 64-column panels)
-    auto w_store = [&]() {
-        float w[32];
-        tmem_ld32(tl + TM_W + 32 * hf, w);
-        tmem_ld_wait();
-        uint8_t *dst = sm + OFF_R2 + (d_row >> 6) * 8192;   // lane index = dk index
-#pragma unroll
-        for (int cc = 0; cc < 32; ++cc)
-            *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * hf + cc, d_row & 63)) = __float2bfloat16_rn(-w[cc]);
-    };
 
     // --------------------------------------------------------------- chain group
     // each chain thread owns TMEM lane d_row (a d_v row) and all of its columns
+    // -W -> R2 as W^T [dk][64 tokens] (the MN-major B operand of Z); the TMEM lane is the dk index
+    auto w_store = [&]() {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float w[32];
+            tmem_ld32(tl + TM_W + 32 * half, w);
+            tmem_ld_wait();
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = -w[8 * ch + e];
+                *reinterpret_cast<uint4 *>(sm + OFF_R2 + sw128_off(d_row, 32 * half + 8 * ch)) = pack8(f);
+            }
+        }
+    };
+    // K -> kappa K in place in chunk c's stage (the operand of the state product)
+    auto kappa_k = [&](int c) {
+        uint8_t *st = sm + (c & 1) * kStageBytes;
+        const float *kap = g_kap[c & 3];
+        const int ct = tid - kPrepThreads;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const uint32_t off = (uint32_t)(ct + kChainThreads * r) << 4;   // both K panels
+            uint4 *pk = reinterpret_cast<uint4 *>(st + OFF_K + off);
+            float kf[8];
+            unpack8(*pk, kf);
+            const float ka = kap[(off & 8191) >> 7];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) kf[e] *= ka;
+            *pk = pack8(kf);
+        }
+    };
     // O1 = S Q^T and Z^T = U^T - S W^T (accumulated into U[c&1])
     auto issue_o1_z = [&](int c) {
         if (!c_issuer) return;
@@ -365,14 +395,15 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
-            umma_bf16(tu, smem_desc(sS + ko, 16, 1024), smem_desc(sR2 + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024),
-                      idesc_bf16(128, 64, false, false), (no_v && k == 0) ? 0u : 1u);
+            umma_bf16(tu, smem_desc(sS + ko, 16, 1024), smem_desc(sR2 + k * 2048, 8192, 1024),
+                      idesc_bf16(128, 64, false, true), (no_v && k == 0) ? 0u : 1u);
         }
         umma_commit(&bar_z);
     };
-    // Z^T (bf16) -> R2 as [dv][64 tokens]
-    auto zt_store = [&](int c) {
+    // Z^T (bf16) -> R2 as [dv][64 tokens]; in fold mode as Z^T diag(kappa)
+    auto zt_store = [&](int c, bool fold) {
         const uint32_t tu = tl + TM_U + 64 * (uint32_t)(c & 1);
+        const float *kap = g_kap[c & 3];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             float z[32];
@@ -382,7 +413,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             for (int ch = 0; ch < 4; ++ch) {
                 float f[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = z[8 * ch + e];
+                for (int e = 0; e < 8; ++e) f[e] = fold ? z[8 * ch + e] * kap[32 * half + 8 * ch + e] : z[8 * ch + e];
                 *reinterpret_cast<uint4 *>(sm + OFF_R2 + sw128_off(d_row, 32 * half + 8 * ch)) = pack8(f);
             }
         }
@@ -416,23 +447,33 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     // chunk, rescaled in TMEM by the next chunk's gamma_C (or written out after the last)
     auto epilogue = [&](int c) {
         const int t0 = c * kC;
-        const float *gam = g_gam[c % 3];
-        __nv_bfloat16 *og = p.o + ((size_t)b * T + t0) * H * kD + (size_t)h * kD + d_row;
-        const int nvalid = T - t0;
+        const float *gam = g_gam[c & 3];
+        if (!no_o) {
+            // [64 tokens][dv] tile in R2 (free once the chunk's MMAs have run), two 64-column panels
+            uint8_t *ot = sm + OFF_R2 + (d_row >> 6) * 8192;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float o1[32], o2[32];
-            tmem_ld32(tl + TM_O1 + 32 * half, o1);
-            tmem_ld32(tl + TM_O2 + 32 * half, o2);
-            tmem_ld_wait();
+            for (int half = 0; half < 2; ++half) {
+                float o1[32], o2[32];
+                tmem_ld32(tl + TM_O1 + 32 * half, o1);
+                tmem_ld32(tl + TM_O2 + 32 * half, o2);
+                tmem_ld_wait();
 #pragma unroll
-            for (int cc = 0; cc < 32; ++cc) {
-                const int t = 32 * half + cc;
-                if (t < nvalid && !no_o) og[(size_t)t * H * kD] = __float2bfloat16_rn(fmaf(gam[t], o1[cc], o2[cc]));
+                for (int cc = 0; cc < 32; ++cc) {
+                    const int t = 32 * half + cc;
+                    *reinterpret_cast<__nv_bfloat16 *>(ot + sw128_off(t, d_row & 63)) =
+                        __float2bfloat16_rn(fmaf(gam[t], o1[cc], o2[cc]));
+                }
+            }
+            fence_proxy_async();
+            named_sync(kBarChain, kChainThreads);
+            if (c_issuer) {                               // rows past T are clipped by the copy
+                tma_store_4d(&tmO, sm + OFF_R2, 0, h, t0, b);
+                tma_store_4d(&tmO, sm + OFF_R2 + 8192, 64, h, t0, b);
+                tma_store_commit();
             }
         }
         const bool last = (c + 1 == nchunks);
-        const float gN = last ? 1.f : g_gam[(c + 1) % 3][kC - 1];
+        const float gN = last ? 1.f : g_gam[(c + 1) & 3][kC - 1];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             float sv[32];
@@ -462,33 +503,32 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         for (int c = 0; c < nchunks; ++c) {
             if (warp == 4 && c + 1 < nchunks) load_gates(c + 1);   // arrays built in solve(c)
             wait_mma(&bar_g, c);
+            if (c >= 1) wait_mma(&bar_uw, c - 1);         // R1 free: Tinv of chunk c-1 consumed
             if (c >= 2) {                                 // P[c&1] and U[c&1] free
                 wait_on(&bar_cdone[c & 1], (uint32_t)(((c - 2) >> 1) & 1));
                 tc_fence_after();
             }
             masks(c);
-            if (c >= 1) {                                 // R2 free (scratch, then -W)
-                wait_on(&bar_cdone[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1));
-                tc_fence_after();
-            }
             tc_fence_before();
             named_sync(kBarPrep, kPrepThreads);
             tc_fence_after();
             solve(c);
             psync();
+            if (p_issuer && c >= 1) {                     // TM_W free: the chain has read W(c-1)
+                wait_on(&bar_wfree, (uint32_t)((c - 1) & 1));
+                tc_fence_after();
+            }
             issue_uw(c);
             if (c + 1 < nchunks) {                        // TM_G was read by masks(c)
                 wait_on(&bar_full[(c + 1) & 1], (uint32_t)(((c + 1) >> 1) & 1));
                 x_pass(c + 1);
-                psync();
-                issue_gram(c + 1);
+                fence_proxy_async();
             }
-            wait_mma(&bar_uw, c);
-            w_store();
-            fence_proxy_async();
             tc_fence_before();
             const bool stop = named_sync_or(kBarPrep, kPrepThreads, abort_flag != 0);
-            if (tid == 0) mbar_arrive(&bar_ready);
+            tc_fence_after();
+            if (tid == 0) mbar_arrive(&bar_ready);        // P(c), gates(c+1), U/W(c) issued
+            if (c + 1 < nchunks) issue_gram(c + 1);
             if (stop) break;
         }
     } else {
@@ -518,10 +558,15 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         csync();
         for (int c = 0; c < nchunks; ++c) {
             wait_on(&bar_ready, (uint32_t)(c & 1));
-            tc_fence_after();
+            wait_mma(&bar_uw, c);
+            const bool fold = g_ell[c & 3][kC - 1] > kFoldLog;
+            w_store();
+            if (!fold) kappa_k(c);
+            csync();
+            if (c_issuer) mbar_arrive(&bar_wfree);
             issue_o1_z(c);
             wait_mma(&bar_z, c);
-            zt_store(c);
+            zt_store(c, fold);
             csync();
             issue_mma2(c);
             wait_mma(&bar_o2, c);
@@ -533,6 +578,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                 }
             }
             epilogue(c);
+            if (c_issuer) tma_store_wait_read0();         // R2 (the o tile) is free for -W(c+1)
             fence_proxy_async();
             tc_fence_before();
             const bool stop = named_sync_or(kBarChain, kChainThreads, abort_flag != 0);
@@ -541,6 +587,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         }
     }
 
+    if (c_issuer) tma_store_wait_all();
     if (abort_flag) {
         // wind down: let this CTA's copies and MMAs finish (bounded) before freeing TMEM
         if (c_issuer)
@@ -568,16 +615,18 @@ bool qdelta_tc_supported(const QDeltaArgs &a, int dtype) {
 }
 
 cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nlaunch, int flags) {
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if (!make_token_map(&mq, a.q, a.B, a.T, a.H) || !make_token_map(&mk, a.k, a.B, a.T, a.H) ||
         !make_token_map(&mv, a.v, a.B, a.T, a.H))
         return cudaErrorInvalidValue;
+    if (flags & kTcNoO) mo = mq;                      // not used
+    else if (!make_token_map(&mo, a.o, a.B, a.T, a.H)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(qdelta_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     TcParams p{(const __nv_bfloat16 *)a.alpha, (const __nv_bfloat16 *)a.beta, (const __nv_bfloat16 *)a.lam,
                a.S0, (__nv_bfloat16 *)a.o, a.S_final, a.B, a.T, a.H, flags};
-    qdelta_fwd_tc_kernel<<<a.B * a.H, kAllThreads, kSmemBytes, s>>>(p, mq, mk, mv);
+    qdelta_fwd_tc_kernel<<<a.B * a.H, kAllThreads, kSmemBytes, s>>>(p, mq, mk, mv, mo);
     e = cudaGetLastError();
     if (e == cudaSuccess) *nlaunch += 1;
     return e;

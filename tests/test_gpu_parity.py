@@ -95,6 +95,19 @@ def test_bf16_small_all_outputs(qd, mode):
     check(S, S_ref, "bf16", f"{mode} S")
 
 
+@pytest.mark.parametrize("alpha_mu", [-0.45, 0.3, 2.0])
+def test_qdelta_strong_decay(qd, alpha_mu):
+    """Log-decay per token about -0.5, -0.85 and -2.1 (chunk sums near -31, -55 and
+    -136): chunks on both sides of the tensor-core kernel's switch between folding
+    kappa into Z^T and scaling K, and past the range where e^{-l_i} stays finite."""
+    d = synth.qdelta_inputs(2, 200, 3, 128, 128, seed=23, dtype="bf16", mode="qdelta", alpha_mu=alpha_mu,
+                            s0_var=0.01)
+    o, S = run_qdelta(qd, d)
+    o_ref, S_ref = oracle.qdelta_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["lam"], d["S0"])
+    check(o, o_ref, "bf16", f"strong decay {alpha_mu} o")
+    check(S, S_ref, "bf16", f"strong decay {alpha_mu} S")
+
+
 @pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 100, 191])
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
 def test_ragged_lengths(qd, T, dt):
