@@ -110,7 +110,11 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     // per-chunk gate arrays, by chunk index mod 4: while the prep group builds chunk
     // c+1's arrays (during the solve of chunk c) the chain group may still read those
     // of chunks c-2 (its epilogue), c-1 and c
-    __shared__ float g_ell[4][kC], g_beta[4][kC], g_lam[4][kC], g_gam[4][kC], g_kap[4][kC], g_igam[4][kC];
+    // (Loops below read what they need of these into registers before they store to
+    // shared memory: the compiler cannot tell the two apart and would otherwise
+    // serialise every load behind the previous store.)
+    __shared__ __align__(16) float g_ell[4][kC], g_beta[4][kC], g_lam[4][kC], g_gam[4][kC], g_kap[4][kC],
+        g_igam[4][kC];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool prep = tid < kPrepThreads;
@@ -251,17 +255,27 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     auto x_pass = [&](int c) {
         uint8_t *st = sm + (c & 1) * kStageBytes;
         const float *lam = g_lam[c & 3];
+        uint4 kr[4], qr[4];
+        float lm[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
+        for (int r = 0; r < 4; ++r) {                     // all loads first
             const int u = tid + kPrepThreads * r;         // 16-byte chunk index, 0..1023
             const int pnl = u >> 9;
             const uint32_t off = (uint32_t)(u & 511) << 4;
-            float kf[8], qf[8], xf[8];
-            unpack8(*reinterpret_cast<const uint4 *>(st + OFF_K + pnl * 8192 + off), kf);
-            unpack8(*reinterpret_cast<const uint4 *>(st + OFF_XQ + pnl * 16384 + 8192 + off), qf);
-            const float lm = lam[off >> 7];
+            kr[r] = *reinterpret_cast<const uint4 *>(st + OFF_K + pnl * 8192 + off);
+            qr[r] = *reinterpret_cast<const uint4 *>(st + OFF_XQ + pnl * 16384 + 8192 + off);
+            lm[r] = lam[off >> 7];
+        }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xf[e] = fmaf(lm, qf[e], kf[e]);
+        for (int r = 0; r < 4; ++r) {
+            const int u = tid + kPrepThreads * r;
+            const int pnl = u >> 9;
+            const uint32_t off = (uint32_t)(u & 511) << 4;
+            float kf[8], qf[8], xf[8];
+            unpack8(kr[r], kf);
+            unpack8(qr[r], qf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xf[e] = fmaf(lm[r], qf[e], kf[e]);
             *reinterpret_cast<uint4 *>(st + OFF_XQ + pnl * 16384 + off) = pack8(xf);
         }
     };
@@ -285,39 +299,40 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         tmem_ld32(tl + TM_G + 32 * hf, g);
         tmem_ld_wait();
         const bool split = ell[kC - 1] > -80.f;       // uniform: gamma_t * exp(-l_i) is safe
+        const bool fold = ell[kC - 1] > kFoldLog;
+        // per-column factor of columns i = 32 hf .. 32 hf + 31: e^{-l_i}, or l_i itself
+        float fi[32];
+        const float *src = (split ? igam : ell) + 32 * hf;
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(src + j);
+            fi[j] = v.x; fi[j + 1] = v.y; fi[j + 2] = v.z; fi[j + 3] = v.w;
+        }
         if (q4 < 2) {
             const int t = 32 * q4 + lane;
             const float lt = ell[t], bt = bet[t], bg = bt * gam[t];
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+                const float v = split ? bg * fi[cc] * g[cc] : bt * __expf(lt - fi[cc]) * g[cc];
+                g[cc] = (32 * hf + cc < t) ? v : 0.f;
+            }
             float *Arow = reinterpret_cast<float *>(sm + OFF_R1) + t * LA + 32 * hf;
 #pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4) {
-                float a[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int cc = 4 * c4 + e, i = 32 * hf + cc;
-                    const float v = split ? bg * igam[i] * g[cc] : bt * __expf(lt - ell[i]) * g[cc];
-                    a[e] = (i < t) ? v : 0.f;
-                }
-                *reinterpret_cast<float4 *>(Arow + 4 * c4) = make_float4(a[0], a[1], a[2], a[3]);
-            }
+            for (int c4 = 0; c4 < 8; ++c4)
+                *reinterpret_cast<float4 *>(Arow + 4 * c4) = make_float4(g[4 * c4], g[4 * c4 + 1], g[4 * c4 + 2], g[4 * c4 + 3]);
         } else {
             const int t = 32 * (q4 - 2) + lane;
             const float lt = ell[t], gt = gam[t];
             const float gtc = gt * igam[kC - 1];          // gamma_t / gamma_C (fold mode)
-            const bool fold = ell[kC - 1] > kFoldLog;
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+                const float pv = fold ? gtc * g[cc] : split ? gt * fi[cc] * g[cc] : __expf(lt - fi[cc]) * g[cc];
+                g[cc] = (32 * hf + cc <= t) ? pv : 0.f;
+            }
             uint8_t *P = sm + OFF_P + (c & 1) * 8192;
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int i = 32 * hf + 8 * ch + e;
-                    const float pv = fold ? gtc * g[8 * ch + e]
-                                   : split ? gt * igam[i] * g[8 * ch + e] : __expf(lt - ell[i]) * g[8 * ch + e];
-                    f[e] = (i <= t) ? pv : 0.f;
-                }
-                *reinterpret_cast<uint4 *>(P + sw128_off(t, 32 * hf + 8 * ch)) = pack8(f);
-            }
+            for (int ch = 0; ch < 4; ++ch)
+                *reinterpret_cast<uint4 *>(P + sw128_off(t, 32 * hf + 8 * ch)) = pack8p(g + 8 * ch);
         }
     };
     // Tinv -> Tinv*beta, Tinv*beta*gamma over R1 (scratch in Y); warp 4 meanwhile
@@ -369,16 +384,22 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         uint8_t *st = sm + (c & 1) * kStageBytes;
         const float *kap = g_kap[c & 3];
         const int ct = tid - kPrepThreads;
+        uint4 kr[8];
+        float ka[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {                     // all loads first
+            const uint32_t off = (uint32_t)(ct + kChainThreads * r) << 4;   // both K panels
+            kr[r] = *reinterpret_cast<const uint4 *>(st + OFF_K + off);
+            ka[r] = kap[(off & 8191) >> 7];
+        }
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
-            const uint32_t off = (uint32_t)(ct + kChainThreads * r) << 4;   // both K panels
-            uint4 *pk = reinterpret_cast<uint4 *>(st + OFF_K + off);
+            const uint32_t off = (uint32_t)(ct + kChainThreads * r) << 4;
             float kf[8];
-            unpack8(*pk, kf);
-            const float ka = kap[(off & 8191) >> 7];
+            unpack8(kr[r], kf);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) kf[e] *= ka;
-            *pk = pack8(kf);
+            for (int e = 0; e < 8; ++e) kf[e] *= ka[r];
+            *reinterpret_cast<uint4 *>(st + OFF_K + off) = pack8(kf);
         }
     };
     // O1 = S Q^T and Z^T = U^T - S W^T (accumulated into U[c&1])
@@ -406,16 +427,22 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         const float *kap = g_kap[c & 3];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
+            float kv[32];
+            if (fold)
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {         // kappa read before this half's stores
+                    const float4 v = *reinterpret_cast<const float4 *>(kap + 32 * half + j);
+                    kv[j] = v.x; kv[j + 1] = v.y; kv[j + 2] = v.z; kv[j + 3] = v.w;
+                }
             float z[32];
             tmem_ld32(tu + 32 * half, z);
             tmem_ld_wait();
+            if (fold)
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                float f[8];
+                for (int j = 0; j < 32; ++j) z[j] *= kv[j];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = fold ? z[8 * ch + e] * kap[32 * half + 8 * ch + e] : z[8 * ch + e];
-                *reinterpret_cast<uint4 *>(sm + OFF_R2 + sw128_off(d_row, 32 * half + 8 * ch)) = pack8(f);
-            }
+            for (int ch = 0; ch < 4; ++ch)
+                *reinterpret_cast<uint4 *>(sm + OFF_R2 + sw128_off(d_row, 32 * half + 8 * ch)) = pack8p(z + 8 * ch);
         }
     };
     // O2 = Z^T P^T ; S += Z^T (kappa K)  (S in TMEM already scaled by gamma_C)
@@ -453,16 +480,19 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             uint8_t *ot = sm + OFF_R2 + (d_row >> 6) * 8192;
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                float o1[32], o2[32];
+                float gv[32], o1[32], o2[32];
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {         // gamma read before this half's stores
+                    const float4 v = *reinterpret_cast<const float4 *>(gam + 32 * half + j);
+                    gv[j] = v.x; gv[j + 1] = v.y; gv[j + 2] = v.z; gv[j + 3] = v.w;
+                }
                 tmem_ld32(tl + TM_O1 + 32 * half, o1);
                 tmem_ld32(tl + TM_O2 + 32 * half, o2);
                 tmem_ld_wait();
 #pragma unroll
-                for (int cc = 0; cc < 32; ++cc) {
-                    const int t = 32 * half + cc;
-                    *reinterpret_cast<__nv_bfloat16 *>(ot + sw128_off(t, d_row & 63)) =
-                        __float2bfloat16_rn(fmaf(gam[t], o1[cc], o2[cc]));
-                }
+                for (int cc = 0; cc < 32; ++cc)
+                    *reinterpret_cast<__nv_bfloat16 *>(ot + sw128_off(32 * half + cc, d_row & 63)) =
+                        __float2bfloat16_rn(fmaf(gv[cc], o1[cc], o2[cc]));
             }
             fence_proxy_async();
             named_sync(kBarChain, kChainThreads);

@@ -48,7 +48,8 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
         f[2 * i + 1] = t.y;
     }
 }
-__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+// eight consecutive floats (from f[0]) -> eight bf16
+__device__ __forceinline__ uint4 pack8p(const float *f) {
     uint4 u;
     u.x = pack_bf16x2(f[0], f[1]);
     u.y = pack_bf16x2(f[2], f[3]);
@@ -56,6 +57,7 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
     u.w = pack_bf16x2(f[6], f[7]);
     return u;
 }
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) { return pack8p(f); }
 
 
 // Tinv = (I + A)^{-1} for the 64x64 strictly lower fp32 matrix A held in M (row
@@ -196,20 +198,23 @@ __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *
             tv[n][e] = (j < rows[n]) ? M[rows[n] * LA + j] : (j == rows[n] ? 1.f : 0.f);
         }
     }
-    sync();
+    // the column scales, read before any store (the compiler cannot tell them apart)
+    float f1[2][8], f2[2][8];
 #pragma unroll
-    for (int n = 0; n < 2; ++n) {
-        float f1[8], f2[8];
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             const int j = 8 * chs[n] + e;
-            f1[e] = s1 ? tv[n][e] * s1[j] : tv[n][e];
-            f2[e] = s2 ? f1[e] * s2[j] : f1[e];
+            f1[n][e] = s1 ? tv[n][e] * s1[j] : tv[n][e];
+            f2[n][e] = s2 ? f1[n][e] * s2[j] : f1[n][e];
         }
-        *reinterpret_cast<uint4 *>(out1 + sw128_off(rows[n], 8 * chs[n])) = pack8(f1);
-        *reinterpret_cast<uint4 *>(out2 + sw128_off(rows[n], 8 * chs[n])) = pack8(f2);
+    sync();
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+        *reinterpret_cast<uint4 *>(out1 + sw128_off(rows[n], 8 * chs[n])) = pack8(f1[n]);
+        *reinterpret_cast<uint4 *>(out2 + sw128_off(rows[n], 8 * chs[n])) = pack8(f2[n]);
     }
-    }
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
