@@ -52,6 +52,7 @@ FLOPS_PER_TOKEN_HEAD = 8 * CHUNK * DK + 6 * DK * DV
 ALG_FLOPS = TOKEN_HEADS * FLOPS_PER_TOKEN_HEAD
 N_BUFFERS = 3
 DOMINANT_KERNEL_SOURCES = ["delta_rule_linear_qdelta_gb300/csrc/chunk_tc.cu",
+                           "delta_rule_linear_qdelta_gb300/csrc/tc_common.cuh",
                            "delta_rule_linear_qdelta_gb300/csrc/sm103_ptx.cuh"]
 
 
@@ -358,6 +359,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip the decode / QED / e2e / CPU legs")
+    ap.add_argument("--profile", action="store_true",
+                    help="profiling case: run warmup + steps forwards of the workload untimed, print no JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -372,6 +375,12 @@ def main():
         build.build()
     rank, world, local = dist_setup(args.gpus)
     hbm_peak, tc_peak, tc_sustained, peak_kind = load_peaks()
+    if args.profile:
+        sets = make_buffers(1, seed_base=1 + rank)
+        time_device(qd, sets, args.steps, args.warmup, world)
+        torch.cuda.synchronize()
+        print(f"profile case done: {args.warmup + args.steps} forwards, status {qd.qd_device_status()}", flush=True)
+        return
 
     sets = make_buffers(N_BUFFERS, seed_base=1 + rank)
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")

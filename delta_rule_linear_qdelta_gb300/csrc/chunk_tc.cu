@@ -311,11 +311,12 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         if (q4 < 2) {
             const int t = 32 * q4 + lane;
             const float lt = ell[t], bt = bet[t], bg = bt * gam[t];
+            if (split)                                    // uniform branches: no exp when not needed
 #pragma unroll
-            for (int cc = 0; cc < 32; ++cc) {
-                const float v = split ? bg * fi[cc] * g[cc] : bt * __expf(lt - fi[cc]) * g[cc];
-                g[cc] = (32 * hf + cc < t) ? v : 0.f;
-            }
+                for (int cc = 0; cc < 32; ++cc) g[cc] = (32 * hf + cc < t) ? bg * fi[cc] * g[cc] : 0.f;
+            else
+#pragma unroll
+                for (int cc = 0; cc < 32; ++cc) g[cc] = (32 * hf + cc < t) ? bt * __expf(lt - fi[cc]) * g[cc] : 0.f;
             float *Arow = reinterpret_cast<float *>(sm + OFF_R1) + t * LA + 32 * hf;
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4)
@@ -324,11 +325,15 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             const int t = 32 * (q4 - 2) + lane;
             const float lt = ell[t], gt = gam[t];
             const float gtc = gt * igam[kC - 1];          // gamma_t / gamma_C (fold mode)
+            if (fold)
 #pragma unroll
-            for (int cc = 0; cc < 32; ++cc) {
-                const float pv = fold ? gtc * g[cc] : split ? gt * fi[cc] * g[cc] : __expf(lt - fi[cc]) * g[cc];
-                g[cc] = (32 * hf + cc <= t) ? pv : 0.f;
-            }
+                for (int cc = 0; cc < 32; ++cc) g[cc] = (32 * hf + cc <= t) ? gtc * g[cc] : 0.f;
+            else if (split)
+#pragma unroll
+                for (int cc = 0; cc < 32; ++cc) g[cc] = (32 * hf + cc <= t) ? gt * fi[cc] * g[cc] : 0.f;
+            else
+#pragma unroll
+                for (int cc = 0; cc < 32; ++cc) g[cc] = (32 * hf + cc <= t) ? __expf(lt - fi[cc]) * g[cc] : 0.f;
             uint8_t *P = sm + OFF_P + (c & 1) * 8192;
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch)
