@@ -14,16 +14,22 @@
 //   o_t    = gamma_t (S Q^T)_t + (Z^T P^T)_t
 //   S     <- gamma_C S + Z^T diag(kappa) K
 // Every product is written "transposed" so that the 128 TMEM lanes index d_v (or
-// d_k) and every MMA has M = 128.  When the chunk's decay is mild (l_C > -30) the
-// kappa scaling moves onto Z^T, and P is divided by kappa to match:
-// (Z^T diag(kappa)) (P diag(1/kappa))^T = Z^T P^T with P_ti / kappa_i = e^{l_t - l_C} (Q K^T)_ti,
-// so K is used as loaded; otherwise K is scaled in place.  The master state stays in
-// TMEM in fp32 (the MMA accumulates Z^T diag(kappa) K onto it after the epilogue has
-// scaled it by the chunk's gamma_C); its bf16 copy in shared memory feeds the MMAs.
+// d_k) and every MMA has M = 128.  The two output terms share one accumulator O:
+// the MMAs form O = S Q^T + Zt^T Pt^T and the epilogue multiplies token t by gamma_t,
+// with Zt, Pt chosen by the chunk's log-decay l_C:
+//   l_C > -30 (fold):  Zt = Z diag(kappa), Pt_ti = e^{-l_C} (Q K^T)_ti   (K used as loaded)
+//   l_C > -80 (split): Zt = Z, Pt_ti = e^{-l_i} (Q K^T)_ti, K scaled in place to kappa K
+//   otherwise:         Zt = Z, Pt = P, kappa K in place, Q scaled in place to gamma Q after
+//                      the Gram and no gamma_t in the epilogue (no factor can overflow)
+// since (Z^T diag(kappa)) (P diag(1/kappa))^T = Z^T P^T and P_ti / gamma_t = e^{-l_i} (Q K^T)_ti.
+// The master state stays in TMEM in fp32 (the MMA accumulates Zt^T (kappa) K onto it
+// after the epilogue has scaled it by the chunk's gamma_C).  Its bf16 copy, and the
+// bf16 Zt^T, also live in TMEM and are the A operands of the state-dependent
+// products, so those MMAs read only their B operand from shared memory.
 //
 // Warp specialisation: a prep group (warps 0-7) does the state-independent work of
 // each chunk -- X, its Gram, the decay masks, the solve, U and W -- and hands the
-// chunk to a chain group (warps 8-11) that carries the state: O1 and Z, Z^T, the
+// chunk to a chain group (warps 8-11) that carries the state: Z and O, Zt^T, the
 // output and state products, the epilogue.  The two groups run concurrently, so the
 // chunk period is the longer of the two instead of their sum.  Each group
 // synchronises on its own named barrier; hand-offs are mbarriers:
@@ -37,16 +43,15 @@
 // Shared memory (offsets from a 1024-aligned base):
 //   stage s in {0,1}: XQ 32 KB (per 64-column panel: X rows 0-63 | Q rows 64-127),
 //                     K 16 KB (scaled in place to kappa*K under strong decay), V 16 KB
-//   S_in 32 KB   bf16 state [dv][dk]
 //   R1   17 KB   A fp32 [64][68]  ->  Tinv*beta, Tinv*beta*gamma (bf16)
-//   R2   16 KB   -W^T(c) [dk][64]  ->  Z^T(c) [dv][64]  ->  o(c) [64][dv] for the TMA store
-//                (chain group only)
-//   P    2x8 KB  bf16 [64][64], by chunk parity
+//   R2   16 KB   -W^T(c) [dk][64]  ->  o(c) [64][dv] for the TMA store (chain group only)
+//   P    2x8 KB  bf16 Pt [64][64], by chunk parity
 //   Y    4.5 KB  fp32 scratch of the solve (prep group only)
-// All MMA operands use the 128-byte swizzle (TMA layout): 128-byte rows, 8-row
-// groups 1024 bytes apart, 64-column panels.
-// TMEM (512 columns): G 0-63, W 64-127, U[0] 128-191, U[1] 192-255, O1 256-319,
-// O2 320-383, S 384-511.
+// All shared-memory MMA operands use the 128-byte swizzle (TMA layout): 128-byte
+// rows, 8-row groups 1024 bytes apart, 64-column panels.
+// TMEM (512 columns): G 0-63, W 64-127, U[0] 128-191, U[1] 192-255 (Z^T accumulates
+// there; its first 32 columns then hold the packed bf16 Zt^T), O 256-319, packed
+// bf16 state 320-383, fp32 state 384-511.
 //
 // Every wait is bounded; on a timeout the kernel sets the library's error word,
 // waits (bounded) for its own copies and MMAs, frees TMEM and returns.
@@ -73,21 +78,23 @@ constexpr int kAllThreads = kPrepThreads + kChainThreads;
 constexpr int kBarPrep = 1, kBarChain = 2;          // named barrier ids
 constexpr uint32_t kStageBytes = 65536;
 constexpr uint32_t OFF_XQ = 0, OFF_K = 32768, OFF_V = 49152;
-constexpr uint32_t OFF_S = 2 * kStageBytes;          // 131072
-constexpr uint32_t OFF_R1 = OFF_S + 32768;           // 163840
-constexpr uint32_t OFF_R2 = OFF_R1 + 17408;          // 181248
-constexpr uint32_t OFF_P = OFF_R2 + 16384;           // 197632 (two 8 KB buffers)
-constexpr uint32_t OFF_Y = OFF_P + 16384;           // 214016 (solve scratch, 32 x LY fp32)
-constexpr uint32_t kSmemUsed = OFF_Y + 32 * LY * 4;  // 218624
+constexpr uint32_t OFF_R1 = 2 * kStageBytes;         // 131072
+constexpr uint32_t OFF_R2 = OFF_R1 + 17408;          // 148480
+constexpr uint32_t OFF_P = OFF_R2 + 16384;           // 164864 (two 8 KB buffers)
+constexpr uint32_t OFF_Y = OFF_P + 16384;           // 181248 (solve scratch, 32 x LY fp32)
+constexpr uint32_t kSmemUsed = OFF_Y + 32 * LY * 4;  // 185856
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
 constexpr uint32_t kTmaBytes = 3 * kC * kD * 2;      // Q, K, V tiles per chunk
 constexpr uint64_t kWaitNs = 2000000000ull;          // 2 s per wait
 
 // fold kappa into Z^T (and 1/kappa into P) when the chunk's log-decay l_C exceeds this:
-// then kappa >= e^-30 and gamma_t / gamma_C <= e^30, far from bf16 under/overflow
+// then kappa >= e^-30 and Pt <= e^30 |Q K^T|, far from bf16 under/overflow
 constexpr float kFoldLog = -30.f;
+// below this log-decay e^{-l_i} leaves the fp32 range: the exponentials are taken
+// one by one and Q carries gamma instead
+constexpr float kSplitLog = -80.f;
 
-constexpr uint32_t TM_G = 0, TM_W = 64, TM_U = 128, TM_O1 = 256, TM_O2 = 320, TM_S = 384;
+constexpr uint32_t TM_G = 0, TM_W = 64, TM_U = 128, TM_O = 256, TM_SB = 320, TM_S = 384;
 
 struct TcParams {
     const __nv_bfloat16 *alpha, *beta, *lam;
@@ -247,7 +254,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         tc_fence_after();
     };
     const uint32_t sbase = smem_u32(sm);
-    const uint32_t sS = sbase + OFF_S, sR1 = sbase + OFF_R1, sR2 = sbase + OFF_R2;
+    const uint32_t sR1 = sbase + OFF_R1, sR2 = sbase + OFF_R2;
     auto stage_addr = [&](int c) { return sbase + (uint32_t)(c & 1) * kStageBytes; };
 
     // ---------------------------------------------------------------- prep group
@@ -291,53 +298,66 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         }
         umma_commit(&bar_g);
     };
-    // decay masks: A (fp32, R1) from the X K^T rows, P (bf16) from the Q K^T rows
+    // decay masks: A (fp32, R1) from the X K^T rows, Pt (bf16) from the Q K^T rows.
+    // Row t, column i of this thread's half: A_ti = beta_t e^{l_t - l_i} (X K^T)_ti for
+    // i < t; for i <= t, Pt_ti = e^{-l_C} (Q K^T)_ti (fold), e^{-l_i} (Q K^T)_ti (split)
+    // or e^{l_t - l_i} (Q K^T)_ti.  While l_C > -80 the decay factors as r_t * f_i with
+    // f_i = e^{-l_i} (or 1 for fold-mode Pt); otherwise each factor is its own exponential.
     auto masks = [&](int c) {
         const int gi = c & 3;
         const float *ell = g_ell[gi], *bet = g_beta[gi], *gam = g_gam[gi], *igam = g_igam[gi];
         float g[32];
         tmem_ld32(tl + TM_G + 32 * hf, g);
         tmem_ld_wait();
-        const bool split = ell[kC - 1] > -80.f;       // uniform: gamma_t * exp(-l_i) is safe
+        const bool split = ell[kC - 1] > kSplitLog;   // uniform: gamma_t * exp(-l_i) is safe
         const bool fold = ell[kC - 1] > kFoldLog;
-        // per-column factor of columns i = 32 hf .. 32 hf + 31: e^{-l_i}, or l_i itself
+        const bool arow = q4 < 2;                      // warp-uniform: A rows or P rows
+        const int t = 32 * (arow ? q4 : q4 - 2) + lane;
+        const int lim = arow ? t : t + 1;              // columns cc with 32 hf + cc < lim are kept
+        const bool ones = !arow && fold;
+        float r;
+        if (arow) r = split ? bet[t] * gam[t] : bet[t];
+        else r = fold ? igam[kC - 1] : 1.f;
         float fi[32];
         const float *src = (split ? igam : ell) + 32 * hf;
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(src + j);
+            const float4 v = ones ? make_float4(1.f, 1.f, 1.f, 1.f) : *reinterpret_cast<const float4 *>(src + j);
             fi[j] = v.x; fi[j + 1] = v.y; fi[j + 2] = v.z; fi[j + 3] = v.w;
         }
-        if (q4 < 2) {
-            const int t = 32 * q4 + lane;
-            const float lt = ell[t], bt = bet[t], bg = bt * gam[t];
-            if (split)                                    // uniform branches: no exp when not needed
+        if (split)                                    // uniform branches: no exp when not needed
 #pragma unroll
-                for (int cc = 0; cc < 32; ++cc) g[cc] = (32 * hf + cc < t) ? bg * fi[cc] * g[cc] : 0.f;
-            else
+            for (int cc = 0; cc < 32; ++cc) g[cc] = (32 * hf + cc < lim) ? r * fi[cc] * g[cc] : 0.f;
+        else {
+            const float lt = ell[t];
 #pragma unroll
-                for (int cc = 0; cc < 32; ++cc) g[cc] = (32 * hf + cc < t) ? bt * __expf(lt - fi[cc]) * g[cc] : 0.f;
+            for (int cc = 0; cc < 32; ++cc) g[cc] = (32 * hf + cc < lim) ? r * __expf(lt - fi[cc]) * g[cc] : 0.f;
+        }
+        if (arow) {
             float *Arow = reinterpret_cast<float *>(sm + OFF_R1) + t * LA + 32 * hf;
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4)
                 *reinterpret_cast<float4 *>(Arow + 4 * c4) = make_float4(g[4 * c4], g[4 * c4 + 1], g[4 * c4 + 2], g[4 * c4 + 3]);
         } else {
-            const int t = 32 * (q4 - 2) + lane;
-            const float lt = ell[t], gt = gam[t];
-            const float gtc = gt * igam[kC - 1];          // gamma_t / gamma_C (fold mode)
-            if (fold)
-#pragma unroll
-                for (int cc = 0; cc < 32; ++cc) g[cc] = (32 * hf + cc <= t) ? gtc * g[cc] : 0.f;
-            else if (split)
-#pragma unroll
-                for (int cc = 0; cc < 32; ++cc) g[cc] = (32 * hf + cc <= t) ? gt * fi[cc] * g[cc] : 0.f;
-            else
-#pragma unroll
-                for (int cc = 0; cc < 32; ++cc) g[cc] = (32 * hf + cc <= t) ? __expf(lt - fi[cc]) * g[cc] : 0.f;
             uint8_t *P = sm + OFF_P + (c & 1) * 8192;
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch)
                 *reinterpret_cast<uint4 *>(P + sw128_off(t, 32 * hf + 8 * ch)) = pack8p(g + 8 * ch);
+        }
+        if (!split) {                                 // Q -> gamma Q (the Gram has read Q)
+            uint8_t *st = sm + (c & 1) * kStageBytes;
+#pragma unroll 1
+            for (int r4 = 0; r4 < 4; ++r4) {
+                const int u = tid + kPrepThreads * r4;    // 16-byte chunk of the two Q panels
+                const uint32_t off = (uint32_t)(u & 511) << 4;
+                uint8_t *qp = st + OFF_XQ + (u >> 9) * 16384 + 8192 + off;
+                const float gq = gam[off >> 7];
+                float qf[8];
+                unpack8(*reinterpret_cast<const uint4 *>(qp), qf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) qf[e] *= gq;
+                *reinterpret_cast<uint4 *>(qp) = pack8(qf);
+            }
         }
     };
     // Tinv -> Tinv*beta, Tinv*beta*gamma over R1 (scratch in Y); warp 4 meanwhile
@@ -370,18 +390,16 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     // each chain thread owns TMEM lane d_row (a d_v row) and all of its columns
     // -W -> R2 as W^T [dk][64 tokens] (the MN-major B operand of Z); the TMEM lane is the dk index
     auto w_store = [&]() {
+        float w[64];
+        tmem_ld32(tl + TM_W, *reinterpret_cast<float(*)[32]>(w));
+        tmem_ld32(tl + TM_W + 32, *reinterpret_cast<float(*)[32]>(w + 32));
+        tmem_ld_wait();
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float w[32];
-            tmem_ld32(tl + TM_W + 32 * half, w);
-            tmem_ld_wait();
+        for (int ch = 0; ch < 8; ++ch) {
+            float f[8];
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = -w[8 * ch + e];
-                *reinterpret_cast<uint4 *>(sm + OFF_R2 + sw128_off(d_row, 32 * half + 8 * ch)) = pack8(f);
-            }
+            for (int e = 0; e < 8; ++e) f[e] = -w[8 * ch + e];
+            *reinterpret_cast<uint4 *>(sm + OFF_R2 + sw128_off(d_row, 8 * ch)) = pack8(f);
         }
     };
     // K -> kappa K in place in chunk c's stage (the operand of the state product)
@@ -407,97 +425,113 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             *reinterpret_cast<uint4 *>(st + OFF_K + off) = pack8(kf);
         }
     };
-    // O1 = S Q^T and Z^T = U^T - S W^T (accumulated into U[c&1])
-    auto issue_o1_z = [&](int c) {
+    // Z^T = U^T - S W^T (accumulated into U[c&1]), then O = S Q^T; A = the bf16 state in TMEM
+    auto issue_z_o = [&](int c) {
         if (!c_issuer) return;
         const uint32_t sXQ = stage_addr(c) + OFF_XQ;
         const uint32_t tu = tm + TM_U + 64 * (uint32_t)(c & 1);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
-            umma_bf16(tm + TM_O1, smem_desc(sS + ko, 16, 1024), smem_desc(sXQ + ko + 8192, 16, 1024),
-                      idesc_bf16(128, 64, false, false), k > 0);
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
-            umma_bf16(tu, smem_desc(sS + ko, 16, 1024), smem_desc(sR2 + k * 2048, 8192, 1024),
-                      idesc_bf16(128, 64, false, true), (no_v && k == 0) ? 0u : 1u);
-        }
+        for (int k = 0; k < 8; ++k)
+            umma_bf16_ta(tu, tm + TM_SB + 8 * k, smem_desc(sR2 + k * 2048, 8192, 1024),
+                         idesc_bf16(128, 64, false, true), (no_v && k == 0) ? 0u : 1u);
         umma_commit(&bar_z);
+        if (!no_o)
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
+                umma_bf16_ta(tm + TM_O, tm + TM_SB + 8 * k, smem_desc(sXQ + ko + 8192, 16, 1024),
+                             idesc_bf16(128, 64, false, false), k > 0);
+            }
     };
-    // Z^T (bf16) -> R2 as [dv][64 tokens]; in fold mode as Z^T diag(kappa)
-    auto zt_store = [&](int c, bool fold) {
+    // Z^T (fp32, U[c&1]) -> Zt^T as packed bf16 pairs of tokens in the first 32 columns
+    // of U[c&1]; in fold mode Zt^T = Z^T diag(kappa)
+    auto zt_pack = [&](int c, bool fold) {
         const uint32_t tu = tl + TM_U + 64 * (uint32_t)(c & 1);
         const float *kap = g_kap[c & 3];
+        float z[64];
+        tmem_ld32(tu, *reinterpret_cast<float(*)[32]>(z));
+        tmem_ld32(tu + 32, *reinterpret_cast<float(*)[32]>(z + 32));
+        tmem_ld_wait();
+        uint32_t zp[32];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float kv[32];
-            if (fold)
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) {         // kappa read before this half's stores
-                    const float4 v = *reinterpret_cast<const float4 *>(kap + 32 * half + j);
-                    kv[j] = v.x; kv[j + 1] = v.y; kv[j + 2] = v.z; kv[j + 3] = v.w;
-                }
-            float z[32];
-            tmem_ld32(tu + 32 * half, z);
-            tmem_ld_wait();
-            if (fold)
-#pragma unroll
-                for (int j = 0; j < 32; ++j) z[j] *= kv[j];
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch)
-                *reinterpret_cast<uint4 *>(sm + OFF_R2 + sw128_off(d_row, 32 * half + 8 * ch)) = pack8p(z + 8 * ch);
+        for (int j = 0; j < 32; j += 2) {              // no shared-memory stores here: kappa read as needed
+            const float4 kv = fold ? *reinterpret_cast<const float4 *>(kap + 2 * j) : make_float4(1.f, 1.f, 1.f, 1.f);
+            zp[j] = pack_bf16x2(z[2 * j] * kv.x, z[2 * j + 1] * kv.y);
+            zp[j + 1] = pack_bf16x2(z[2 * j + 2] * kv.z, z[2 * j + 3] * kv.w);
         }
+        tmem_st32(tu, zp);
+        tmem_st_wait();
     };
-    // O2 = Z^T P^T ; S += Z^T (kappa K)  (S in TMEM already scaled by gamma_C)
+    // O += Zt^T Pt^T ; S += Zt^T (kappa K)  (S in TMEM already scaled by gamma_C); A = Zt^T in TMEM
     auto issue_mma2 = [&](int c) {
         if (!c_issuer) return;
         const uint32_t sK = stage_addr(c) + OFF_K, sP = sbase + OFF_P + (uint32_t)(c & 1) * 8192;
+        const uint32_t tz = tm + TM_U + 64 * (uint32_t)(c & 1);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            umma_bf16(tm + TM_O2, smem_desc(sR2 + k * 32, 16, 1024), smem_desc(sP + k * 32, 16, 1024),
-                      idesc_bf16(128, 64, false, false), k > 0);
+            umma_bf16_ta(tm + TM_S, tz + 8 * k, smem_desc(sK + k * 2048, 8192, 1024),
+                         idesc_bf16(128, 128, false, true), 1);
+        if (!no_o)
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            umma_bf16(tm + TM_S, smem_desc(sR2 + k * 32, 16, 1024), smem_desc(sK + k * 2048, 8192, 1024),
-                      idesc_bf16(128, 128, false, true), 1);
+            for (int k = 0; k < 4; ++k)
+                umma_bf16_ta(tm + TM_O, tz + 8 * k, smem_desc(sP + k * 32, 16, 1024),
+                             idesc_bf16(128, 64, false, false), 1);
         umma_commit(&bar_o2);
     };
-    // bf16 copy of 32 state columns (block q of 4) into S_in
-    auto write_s_in = [&](int q, const float (&sv)[32]) {
-        uint8_t *sp = sm + OFF_S + (q >> 1) * 16384;
+    // the state of this thread's row, 64 columns from column 64 h: packed bf16 copy into
+    // the state A operand, fp32 scaled by g back into the master state
+    auto state_half = [&](int half, float (&sv)[64], float g, bool store_back) {
+        uint32_t sp[32];
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-            float f[8];
+        for (int j = 0; j < 32; ++j) sp[j] = pack_bf16x2(sv[2 * j], sv[2 * j + 1]);
+        tmem_st32(tl + TM_SB + 32 * half, sp);
+        if (store_back) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = sv[8 * ch + e];
-            *reinterpret_cast<uint4 *>(sp + sw128_off(d_row, 32 * (q & 1) + 8 * ch)) = pack8(f);
+            for (int e = 0; e < 64; ++e) sv[e] *= g;
+            tmem_st32(tl + TM_S + 64 * half, *reinterpret_cast<float(*)[32]>(sv));
+            tmem_st32(tl + TM_S + 64 * half + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
         }
     };
-    // o_t = gamma_t O1 + O2 straight to global memory; state -> bf16 S_in for the next
-    // chunk, rescaled in TMEM by the next chunk's gamma_C (or written out after the last)
+    // state -> packed bf16 state for the next chunk, rescaled in TMEM by the next chunk's
+    // gamma_C (or written out after the last); o_t = gamma_t O_t (or O_t) through a
+    // shared-memory tile and two TMA stores
     auto epilogue = [&](int c) {
         const int t0 = c * kC;
-        const float *gam = g_gam[c & 3];
+        const bool last = (c + 1 == nchunks);
+        const float gN = last ? 1.f : g_gam[(c + 1) & 3][kC - 1];
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+            float sv[64];
+            tmem_ld32(tl + TM_S + 64 * half, *reinterpret_cast<float(*)[32]>(sv));
+            tmem_ld32(tl + TM_S + 64 * half + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
+            tmem_ld_wait();
+            if (last && p.S_final && !abort_flag) {
+                float *dst = p.S_final + ((size_t)bh * kD + d_row) * kD + 64 * half;
+#pragma unroll
+                for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+            }
+            state_half(half, sv, gN, !last);
+        }
         if (!no_o) {
+            const bool gscale = g_ell[c & 3][kC - 1] > kSplitLog;
+            const float *gam = g_gam[c & 3];
             // [64 tokens][dv] tile in R2 (free once the chunk's MMAs have run), two 64-column panels
             uint8_t *ot = sm + OFF_R2 + (d_row >> 6) * 8192;
-#pragma unroll
+#pragma unroll 1
             for (int half = 0; half < 2; ++half) {
-                float gv[32], o1[32], o2[32];
+                float ov[32], gv[32];
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {         // gamma read before this half's stores
-                    const float4 v = *reinterpret_cast<const float4 *>(gam + 32 * half + j);
+                    const float4 v = gscale ? *reinterpret_cast<const float4 *>(gam + 32 * half + j)
+                                            : make_float4(1.f, 1.f, 1.f, 1.f);
                     gv[j] = v.x; gv[j + 1] = v.y; gv[j + 2] = v.z; gv[j + 3] = v.w;
                 }
-                tmem_ld32(tl + TM_O1 + 32 * half, o1);
-                tmem_ld32(tl + TM_O2 + 32 * half, o2);
+                tmem_ld32(tl + TM_O + 32 * half, ov);
                 tmem_ld_wait();
 #pragma unroll
                 for (int cc = 0; cc < 32; ++cc)
                     *reinterpret_cast<__nv_bfloat16 *>(ot + sw128_off(32 * half + cc, d_row & 63)) =
-                        __float2bfloat16_rn(fmaf(gv[cc], o1[cc], o2[cc]));
+                        __float2bfloat16_rn(gv[cc] * ov[cc]);
             }
             fence_proxy_async();
             named_sync(kBarChain, kChainThreads);
@@ -505,24 +539,6 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                 tma_store_4d(&tmO, sm + OFF_R2, 0, h, t0, b);
                 tma_store_4d(&tmO, sm + OFF_R2 + 8192, 64, h, t0, b);
                 tma_store_commit();
-            }
-        }
-        const bool last = (c + 1 == nchunks);
-        const float gN = last ? 1.f : g_gam[(c + 1) & 3][kC - 1];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            float sv[32];
-            tmem_ld32(tl + TM_S + 32 * q, sv);
-            tmem_ld_wait();
-            write_s_in(q, sv);
-            if (!last) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) sv[e] *= gN;
-                tmem_st32(tl + TM_S + 32 * q, sv);
-            } else if (p.S_final && !abort_flag) {
-                float *dst = p.S_final + ((size_t)bh * kD + d_row) * kD + 32 * q;
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
             }
         }
         tmem_st_wait();
@@ -567,26 +583,23 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             if (stop) break;
         }
     } else {
-        // initial state: bf16 copy in S_in, fp32 in TMEM scaled by chunk 0's gamma_C
+        // initial state: packed bf16 copy and fp32 state (scaled by chunk 0's gamma_C) in TMEM
         {
             const size_t base = ((size_t)bh * kD + d_row) * kD;
             const float g0 = g_gam[0][kC - 1];
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                float sv[64];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float sv[32];
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) {
-                    float4 v = p.S0 ? *reinterpret_cast<const float4 *>(p.S0 + base + 32 * q + j)
+                for (int j = 0; j < 64; j += 4) {
+                    float4 v = p.S0 ? *reinterpret_cast<const float4 *>(p.S0 + base + 64 * half + j)
                                     : make_float4(0.f, 0.f, 0.f, 0.f);
                     sv[j] = v.x; sv[j + 1] = v.y; sv[j + 2] = v.z; sv[j + 3] = v.w;
                 }
                 if (s0_id)
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) sv[j] = (32 * q + j == d_row) ? 1.f : 0.f;
-                write_s_in(q, sv);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) sv[e] *= g0;
-                tmem_st32(tl + TM_S + 32 * q, sv);
+                    for (int j = 0; j < 64; ++j) sv[j] = (64 * half + j == d_row) ? 1.f : 0.f;
+                state_half(half, sv, g0, true);
             }
             tmem_st_wait();
         }
@@ -599,9 +612,9 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             if (!fold) kappa_k(c);
             csync();
             if (c_issuer) mbar_arrive(&bar_wfree);
-            issue_o1_z(c);
+            issue_z_o(c);
             wait_mma(&bar_z, c);
-            zt_store(c, fold);
+            zt_pack(c, fold);
             csync();
             issue_mma2(c);
             wait_mma(&bar_o2, c);

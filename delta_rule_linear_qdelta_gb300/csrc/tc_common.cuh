@@ -64,9 +64,9 @@ __device__ __forceinline__ uint4 pack8(const float (&f)[8]) { return pack8p(f); 
 // The merge steps of the inverse are 16x8 output tiles with K = 16 or 32: too small
 // and too latency-bound for tcgen05 (its TMEM round trip alone exceeds the work),
 // so they run on the warp-synchronous m16n8k8 TF32 MMA with operands read straight
-// from shared memory.  Each fp32 operand is split into two TF32 parts, x = hi + lo,
-// and a b = a_hi b_hi + a_hi b_lo + a_lo b_hi (the a_lo b_lo term is below fp32
-// rounding), which keeps the products at about fp32 accuracy.
+// from shared memory.  One TF32 product per step: its rounding (unit roundoff
+// 2^-11) stays well below the bf16 rounding (2^-8) that every entry of the inverse
+// receives before it is used, so a split hi/lo product would buy no accuracy.
 // Fragment layout of m16n8k8 (lane = 4 g + t): A (16x8) a0 (g, t), a1 (g+8, t),
 // a2 (g, t+4), a3 (g+8, t+4); B (8x8) b0 (t, g), b1 (t+4, g); C/D (16x8) c0 (g, 2t),
 // c1 (g, 2t+1), c2 (g+8, 2t), c3 (g+8, 2t+1).
@@ -74,10 +74,6 @@ __device__ __forceinline__ uint32_t to_tf32(float x) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
     return r;
-}
-__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-    hi = to_tf32(x);
-    lo = to_tf32(x - __uint_as_float(hi));
 }
 __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -93,31 +89,24 @@ template <int K>
 __device__ __forceinline__ void tile_cab(float (&d)[4], const float *C, int ldc, const float *A, int lda,
                                          const float *B, int ldb) {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    d[0] = C[g * ldc + 2 * t];
-    d[1] = C[g * ldc + 2 * t + 1];
-    d[2] = C[(g + 8) * ldc + 2 * t];
-    d[3] = C[(g + 8) * ldc + 2 * t + 1];
-    float x[K / 8][4];                                 // one accumulator per k-step: short chains
+    uint32_t a[K / 8][4], b[K / 8][2];
 #pragma unroll
-    for (int s = 0; s < K / 8; ++s) {
+    for (int s = 0; s < K / 8; ++s) {                  // every operand load first
         const int k0 = 8 * s;
-        uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
-        split_tf32(A[g * lda + k0 + t], ah[0], al[0]);
-        split_tf32(A[(g + 8) * lda + k0 + t], ah[1], al[1]);
-        split_tf32(A[g * lda + k0 + t + 4], ah[2], al[2]);
-        split_tf32(A[(g + 8) * lda + k0 + t + 4], ah[3], al[3]);
-        split_tf32(B[(k0 + t) * ldb + g], bh0, bl0);
-        split_tf32(B[(k0 + t + 4) * ldb + g], bh1, bl1);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) x[s][i] = 0.f;
-        mma_tf32(x[s], ah, bl0, bl1);
-        mma_tf32(x[s], al, bh0, bh1);
-        mma_tf32(x[s], ah, bh0, bh1);
+        a[s][0] = to_tf32(A[g * lda + k0 + t]);
+        a[s][1] = to_tf32(A[(g + 8) * lda + k0 + t]);
+        a[s][2] = to_tf32(A[g * lda + k0 + t + 4]);
+        a[s][3] = to_tf32(A[(g + 8) * lda + k0 + t + 4]);
+        b[s][0] = to_tf32(B[(k0 + t) * ldb + g]);
+        b[s][1] = to_tf32(B[(k0 + t + 4) * ldb + g]);
     }
+    float x[2][4] = {{C[g * ldc + 2 * t], C[g * ldc + 2 * t + 1], C[(g + 8) * ldc + 2 * t],
+                      C[(g + 8) * ldc + 2 * t + 1]},
+                     {0.f, 0.f, 0.f, 0.f}};             // two accumulators: short chains
 #pragma unroll
-    for (int s = 0; s < K / 8; ++s)
+    for (int s = 0; s < K / 8; ++s) mma_tf32(x[s & 1], a[s], b[s][0], b[s][1]);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) d[i] += x[s][i];
+    for (int i = 0; i < 4; ++i) d[i] = x[0][i] + x[1][i];
 }
 // stores s * d into the 16x8 tile at D (row stride ldd)
 __device__ __forceinline__ void tile_store(float *D, int ldd, const float (&d)[4], float s) {
@@ -126,61 +115,92 @@ __device__ __forceinline__ void tile_store(float *D, int ldd, const float (&d)[4
     *reinterpret_cast<float2 *>(D + (g + 8) * ldd + 2 * t) = make_float2(s * d[2], s * d[3]);
 }
 
+// one 8x8 product on the m16n8k8 MMA (rows 8-15 of its A operand zero):
+// d = C + A B, A, B, C 8x8 fp32 in shared memory; this lane receives row g, columns
+// 2t and 2t+1 of d in d[0], d[1]
+__device__ __forceinline__ void tile8_cab(float (&d)[4], const float *C, int ldc, const float *A, int lda,
+                                          const float *B, int ldb) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const uint32_t a[4] = {to_tf32(A[g * lda + t]), 0u, to_tf32(A[g * lda + t + 4]), 0u};
+    const uint32_t b0 = to_tf32(B[t * ldb + g]), b1 = to_tf32(B[(t + 4) * ldb + g]);
+    d[0] = C[g * ldc + 2 * t];
+    d[1] = C[g * ldc + 2 * t + 1];
+    d[2] = 0.f;
+    d[3] = 0.f;
+    mma_tf32(d, a, b0, b1);
+}
+
 // Tinv = (I + A)^{-1} for the 64x64 strictly lower fp32 matrix A held in M (row
 // stride LA, zero on and above the diagonal), then Tinv diag(s1) -> out1 and
 // Tinv diag(s1 s2) -> out2 as bf16 [64][64] tiles in the 128-byte swizzle (out1
 // and out2 may overlay M; null scales mean 1).  Y is >= 32*LY floats of scratch.
-//   a) the four 16x16 diagonal blocks by forward substitution, one column per lane
-//   b) 16 -> 32: T10 = -T11 (A10 T00) for the block pairs (0,1) and (2,3)
-//   c) 32 -> 64: T21 = -T22 (A21 T11) on the two 32x32 halves
+//   a) the eight 8x8 diagonal blocks by forward substitution, one column per lane,
+//      the block held in registers
+//   b) 8 -> 16:  T10 = -T11 (A10 T00), one warp per block pair
+//   c) 16 -> 32: the same on 16x16 blocks, one warp per (pair, 8-column tile)
+//   d) 32 -> 64: the same on the two 32x32 halves, one warp per 16x8 tile
 // Every inverted block keeps only the strict lower part of its inverse (the unit
 // diagonal is implied, zeros above), so each merge is two products,
-// Y = A21 + A21 T11s and T21 = -(Y + T22s Y), run as 16x8 tiles on the warp MMA.
+// Y = A21 + A21 T11s and T21 = -(Y + T22s Y), run on the warp MMA.  Between the two
+// products only the warps that read the A21 being overwritten synchronise: the
+// warp itself (8 -> 16), the warp pair on named barrier 8 + pair (16 -> 32), all
+// warps (32 -> 64).
 // Called by kThreads threads (thread indices 0..kThreads-1) that synchronise with
-// sync(); idle() runs on every one of them while warps 0-3 invert the diagonal blocks.
+// sync(); idle() runs on every one of them while warps 0-1 invert the diagonal blocks.
 template <typename Idle, typename Sync>
 __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *out1, uint8_t *out2,
                                                    const float *s1, const float *s2, Idle idle, Sync sync) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (warp < 4 && lane < 16) {
-        const int base = 16 * warp, j = lane;
-        float t[16];
+    if (warp < 2) {
+        const int base = 8 * (4 * warp + (lane >> 3)), j = lane & 7;
+        float a[8][8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float *Ai = M + (base + i) * LA + base;
-            float acc[4] = {(i == j) ? 1.f : 0.f, 0.f, 0.f, 0.f};   // four partial sums
-#pragma unroll
-            for (int m4 = 0; m4 < (i + 3) / 4; ++m4) {
-                const float4 a = *reinterpret_cast<const float4 *>(Ai + 4 * m4);
-                if (4 * m4 + 0 < i) acc[0] = fmaf(-a.x, t[4 * m4 + 0], acc[0]);
-                if (4 * m4 + 1 < i) acc[1] = fmaf(-a.y, t[4 * m4 + 1], acc[1]);
-                if (4 * m4 + 2 < i) acc[2] = fmaf(-a.z, t[4 * m4 + 2], acc[2]);
-                if (4 * m4 + 3 < i) acc[3] = fmaf(-a.w, t[4 * m4 + 3], acc[3]);
-            }
-            t[i] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        for (int i = 1; i < 8; ++i) {                  // the block's rows 1-7, all loads first
+            const float4 lo = *reinterpret_cast<const float4 *>(M + (base + i) * LA + base);
+            const float4 hi = *reinterpret_cast<const float4 *>(M + (base + i) * LA + base + 4);
+            a[i][0] = lo.x; a[i][1] = lo.y; a[i][2] = lo.z; a[i][3] = lo.w;
+            a[i][4] = hi.x; a[i][5] = hi.y; a[i][6] = hi.z; a[i][7] = hi.w;
         }
-        __syncwarp(0x0000ffffu);
+        float t[8];
 #pragma unroll
-        for (int i = 1; i < 16; ++i)
+        for (int i = 0; i < 8; ++i) {
+            float acc0 = (i == j) ? 1.f : 0.f, acc1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < i; ++m) {
+                if (m & 1) acc1 = fmaf(-a[i][m], t[m], acc1);
+                else acc0 = fmaf(-a[i][m], t[m], acc0);
+            }
+            t[i] = (i < j) ? 0.f : acc0 + acc1;
+        }
+#pragma unroll
+        for (int i = 1; i < 8; ++i)
             if (i > j) M[(base + i) * LA + base + j] = t[i];
     }
     idle();
     sync();
+    // 8 -> 16: warp w < 4 merges the 8x8 blocks at 16 w
+    if (warp < 4) {
+        const int base = 16 * warp, g = lane >> 2, t = lane & 3;
+        float *Yw = Y + 8 * warp * LY;
+        float d[4];
+        tile8_cab(d, M + (base + 8) * LA + base, LA, M + (base + 8) * LA + base, LA, M + base * LA + base, LA);
+        *reinterpret_cast<float2 *>(Yw + g * LY + 2 * t) = make_float2(d[0], d[1]);
+        __syncwarp();
+        tile8_cab(d, Yw, LY, M + (base + 8) * LA + base + 8, LA, Yw, LY);
+        *reinterpret_cast<float2 *>(M + (base + 8 + g) * LA + base + 2 * t) = make_float2(-d[0], -d[1]);
+    }
+    sync();
     // 16 -> 32: warp w < 4 takes pair p = w / 2 (blocks at 32 p) and 8-column tile w % 2
-    {
-        const int p = (warp >> 1) & 1, n0 = 8 * (warp & 1), base = 32 * p;
+    if (warp < 4) {
+        const int p = warp >> 1, n0 = 8 * (warp & 1), base = 32 * p;
         float *Yp = Y + 16 * p * LY;
         float d[4];
-        if (warp < 4) {
-            tile_cab<16>(d, M + (base + 16) * LA + base + n0, LA, M + (base + 16) * LA + base, LA,
-                         M + base * LA + base + n0, LA);                // A10 + A10 T00s
-            tile_store(Yp + n0, LY, d, 1.f);
-        }
-        sync();
-        if (warp < 4) {
-            tile_cab<16>(d, Yp + n0, LY, M + (base + 16) * LA + base + 16, LA, Yp + n0, LY);   // Y + T11s Y
-            tile_store(M + (base + 16) * LA + base + n0, LA, d, -1.f);
-        }
+        tile_cab<16>(d, M + (base + 16) * LA + base + n0, LA, M + (base + 16) * LA + base, LA,
+                     M + base * LA + base + n0, LA);                // A10 + A10 T00s
+        tile_store(Yp + n0, LY, d, 1.f);
+        named_sync(8 + p, 64);        // the pair's A10 has been read before T10 overwrites it
+        tile_cab<16>(d, Yp + n0, LY, M + (base + 16) * LA + base + 16, LA, Yp + n0, LY);   // Y + T11s Y
+        tile_store(M + (base + 16) * LA + base + n0, LA, d, -1.f);
     }
     sync();
     // 32 -> 64: warp w takes rows 16 (w / 4) and columns 8 (w % 4) of the 32x32 block
@@ -189,7 +209,7 @@ __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *
         float d[4];
         tile_cab<32>(d, M + (32 + m0) * LA + n0, LA, M + (32 + m0) * LA, LA, M + n0, LA);   // A21 + A21 T11s
         tile_store(Y + m0 * LY + n0, LY, d, 1.f);
-        sync();
+        sync();                       // all of A21 has been read before T21 overwrites it
         tile_cab<32>(d, Y + m0 * LY + n0, LY, M + (32 + m0) * LA + 32, LA, Y + n0, LY);    // Y + T22s Y
         tile_store(M + (32 + m0) * LA + n0, LA, d, -1.f);
     }
