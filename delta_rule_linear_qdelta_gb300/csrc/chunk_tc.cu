@@ -43,10 +43,13 @@
 // Shared memory (offsets from a 1024-aligned base):
 //   stage s in {0,1}: XQ 32 KB (per 64-column panel: X rows 0-63 | Q rows 64-127),
 //                     K 16 KB (scaled in place to kappa*K under strong decay), V 16 KB
-//   R1   17 KB   A fp32 [64][68]  ->  Tinv*beta, Tinv*beta*gamma (bf16)
-//   R2   16 KB   -W^T(c) [dk][64]  ->  o(c) [64][dv] for the TMA store (chain group only)
+//   R1   17 KB   A fp32 [64][68], overwritten by the solve's intermediate blocks
+//   R2   16 KB   -W^T(c) [dk][64] (chain group only)
 //   P    2x8 KB  bf16 Pt [64][64], by chunk parity
+//   T    16 KB   Tinv*beta, Tinv*beta*gamma (bf16 [64][64] each), written block by
+//                block by the solve; zero above the 8x8 diagonal blocks
 //   Y    4.5 KB  fp32 scratch of the solve (prep group only)
+//   O    16 KB   o(c) [64][dv] bf16 for the TMA store (chain group only)
 // All shared-memory MMA operands use the 128-byte swizzle (TMA layout): 128-byte
 // rows, 8-row groups 1024 bytes apart, 64-column panels.
 // TMEM (512 columns): G 0-63, W 64-127, U[0] 128-191, U[1] 192-255 (Z^T accumulates
@@ -75,14 +78,20 @@ using namespace tc;
 constexpr int kPrepThreads = kThreads;              // warps 0-7
 constexpr int kChainThreads = 128;                  // warps 8-11
 constexpr int kAllThreads = kPrepThreads + kChainThreads;
-constexpr int kBarPrep = 1, kBarChain = 2;          // named barrier ids
+constexpr int kBarPrep = 1, kBarChain = 2;          // named barrier ids (8-13: inside the solve)
+constexpr int kBarLo = 14;                          // prep warps 0-3
 constexpr uint32_t kStageBytes = 65536;
 constexpr uint32_t OFF_XQ = 0, OFF_K = 32768, OFF_V = 49152;
 constexpr uint32_t OFF_R1 = 2 * kStageBytes;         // 131072
 constexpr uint32_t OFF_R2 = OFF_R1 + 17408;          // 148480
 constexpr uint32_t OFF_P = OFF_R2 + 16384;           // 164864 (two 8 KB buffers)
-constexpr uint32_t OFF_Y = OFF_P + 16384;           // 181248 (solve scratch, 32 x LY fp32)
-constexpr uint32_t kSmemUsed = OFF_Y + 32 * LY * 4;  // 185856
+constexpr uint32_t OFF_T = OFF_P + 16384;           // 181248 (Tinv*beta, Tinv*beta*gamma bf16)
+constexpr uint32_t OFF_Y = OFF_T + 16384;           // 197632 (solve scratch, 32 x LY fp32)
+constexpr uint32_t OFF_O = 203776;                   // o tile [64][dv] bf16 for the TMA store
+constexpr uint32_t kSmemUsed = OFF_O + 16384;        // 220160
+static_assert(OFF_O % 1024 == 0 && OFF_O >= OFF_Y + 32 * LY * 4, "o tile placement");
+static_assert(OFF_R2 % 1024 == 0 && OFF_P % 1024 == 0 && OFF_T % 1024 == 0 && kSmemUsed + 1024 <= 232448,
+              "128-byte-swizzled MMA operands start on 1024-byte boundaries");
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
 constexpr uint32_t kTmaBytes = 3 * kC * kD * 2;      // Q, K, V tiles per chunk
 constexpr uint64_t kWaitNs = 2000000000ull;          // 2 s per wait
@@ -131,7 +140,12 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     const int nchunks = (T + kC - 1) / kC;
     const bool p_issuer = (tid == 32), c_issuer = (tid == kPrepThreads);
     const int d_row = 32 * q4 + lane;                  // this thread's TMEM lane / state row
-    const bool no_v = p.flags & kTcNoV, no_o = p.flags & kTcNoO, s0_id = p.flags & kTcS0Identity;
+    // flags of the segment-scan passes; read through opaque() where they are tested
+    // inside the chunk loops (see tc_common.cuh)
+    const uint32_t flags = (uint32_t)p.flags;
+    const bool s0_id = flags & kTcS0Identity;
+    auto no_v = [&]() { return (opaque(flags) & kTcNoV) != 0; };
+    auto no_o = [&]() { return (opaque(flags) & kTcNoO) != 0; };
 
     if (tid == 0) {
         mbar_init(&bar_full[0], 1);
@@ -157,42 +171,47 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         tmem_alloc(&tmem_base, 512);
         tmem_relinquish();
     }
+    for (int i = tid; i < 16384 / 16; i += kAllThreads)   // T: zeros above the diagonal blocks
+        reinterpret_cast<uint4 *>(sm + OFF_T)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async();                                  // ... as the tensor core will read them
 
     auto issue_loads = [&](int c) {
         const int s = c & 1;
         uint8_t *st = sm + s * kStageBytes;
         const int t0 = c * kC;
-        mbar_arrive_expect_tx(&bar_full[s], no_v ? kTmaBytes / 3 * 2 : kTmaBytes);
+        mbar_arrive_expect_tx(&bar_full[s], no_v() ? kTmaBytes / 3 * 2 : kTmaBytes);
 #pragma unroll
         for (int pnl = 0; pnl < 2; ++pnl) {
             tma_load_4d(st + OFF_XQ + pnl * 16384 + 8192, &tmQ, &bar_full[s], 64 * pnl, h, t0, b);
             tma_load_4d(st + OFF_K + pnl * 8192, &tmK, &bar_full[s], 64 * pnl, h, t0, b);
-            if (!no_v) tma_load_4d(st + OFF_V + pnl * 8192, &tmV, &bar_full[s], 64 * pnl, h, t0, b);
+            if (!no_v()) tma_load_4d(st + OFF_V + pnl * 8192, &tmV, &bar_full[s], 64 * pnl, h, t0, b);
         }
     };
     // gates of a chunk: lane l of warp 4 holds tokens 2l and 2l+1.  The loads land in raw
     // bf16 registers that nothing reads until compute_gates, so they do not stall the warp.
     __nv_bfloat16 ra[2], rb[2], rl[2];
     auto load_gates = [&](int c) {
+        const __nv_bfloat16 *pa = opaque(p.alpha), *pl = opaque(p.lam);
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int t = min(c * kC + 2 * lane + u, T - 1);
             const size_t tok = ((size_t)b * T + t) * H + h;
-            if (p.alpha) ra[u] = p.alpha[tok];
+            if (pa) ra[u] = pa[tok];
             rb[u] = p.beta[tok];
-            if (p.lam) rl[u] = p.lam[tok];
+            if (pl) rl[u] = pl[tok];
         }
     };
     // warp-wide: log-prefix l, gamma = e^l, kappa = e^{l_C - l}, e^{-l} of chunk c
     auto compute_gates = [&](int c) {
         const int buf = c & 3;
+        const bool has_a = opaque(p.alpha) != nullptr, has_l = opaque(p.lam) != nullptr;
         float ga[2], gb[2], gl[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {                  // tokens past T: alpha 1, beta 0, lambda 0
             const bool ok = c * kC + 2 * lane + u < T;
-            ga[u] = (ok && p.alpha) ? bf(ra[u]) : 1.f;
+            ga[u] = (ok && has_a) ? bf(ra[u]) : 1.f;
             gb[u] = ok ? bf(rb[u]) : 0.f;
-            gl[u] = (ok && p.lam) ? bf(rl[u]) : 0.f;
+            gl[u] = (ok && has_l) ? bf(rl[u]) : 0.f;
         }
         const float l0 = __logf(ga[0]), l1 = __logf(ga[1]);
         float sum = l0 + l1;
@@ -254,7 +273,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         tc_fence_after();
     };
     const uint32_t sbase = smem_u32(sm);
-    const uint32_t sR1 = sbase + OFF_R1, sR2 = sbase + OFF_R2;
+    const uint32_t sT = sbase + OFF_T, sR2 = sbase + OFF_R2;
     auto stage_addr = [&](int c) { return sbase + (uint32_t)(c & 1) * kStageBytes; };
 
     // ---------------------------------------------------------------- prep group
@@ -360,28 +379,28 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             }
         }
     };
-    // Tinv -> Tinv*beta, Tinv*beta*gamma over R1 (scratch in Y); warp 4 meanwhile
+    // Tinv -> Tinv*beta, Tinv*beta*gamma into T (R1 and Y as scratch); warp 4 meanwhile
     // turns the next chunk's raw gates into arrays
     auto solve = [&](int c) {
         const int gi = c & 3;
         unit_lower_inverse(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_Y),
-                           sm + OFF_R1, sm + OFF_R1 + 8192, g_beta[gi], g_gam[gi],
+                           sm + OFF_T, sm + OFF_T + 8192, g_beta[gi], g_gam[gi],
                            [&]() { if (warp == 4 && c + 1 < nchunks) compute_gates(c + 1); },
-                           []() { named_sync(kBarPrep, kPrepThreads); });
+                           []() { named_sync(kBarPrep, kPrepThreads); }, []() { named_sync(kBarLo, 128); });
     };
     // U^T = V^T T1^T into U[c&1], W^T = X^T T2^T
     auto issue_uw = [&](int c) {
         if (!p_issuer) return;
         const uint32_t sXQ = stage_addr(c) + OFF_XQ, sV = stage_addr(c) + OFF_V;
         const uint32_t tu = tm + TM_U + 64 * (uint32_t)(c & 1);
-        if (!no_v)
+        if (!no_v())
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                umma_bf16(tu, smem_desc(sV + k * 2048, 8192, 1024), smem_desc(sR1 + k * 32, 16, 1024),
+                umma_bf16(tu, smem_desc(sV + k * 2048, 8192, 1024), smem_desc(sT + k * 32, 16, 1024),
                           idesc_bf16(128, 64, true, false), k > 0);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            umma_bf16(tm + TM_W, smem_desc(sXQ + k * 2048, 16384, 1024), smem_desc(sR1 + 8192 + k * 32, 16, 1024),
+            umma_bf16(tm + TM_W, smem_desc(sXQ + k * 2048, 16384, 1024), smem_desc(sT + 8192 + k * 32, 16, 1024),
                       idesc_bf16(128, 64, true, false), k > 0);
         umma_commit(&bar_uw);
     };
@@ -433,9 +452,9 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
         for (int k = 0; k < 8; ++k)
             umma_bf16_ta(tu, tm + TM_SB + 8 * k, smem_desc(sR2 + k * 2048, 8192, 1024),
-                         idesc_bf16(128, 64, false, true), (no_v && k == 0) ? 0u : 1u);
+                         idesc_bf16(128, 64, false, true), (no_v() && k == 0) ? 0u : 1u);
         umma_commit(&bar_z);
-        if (!no_o)
+        if (!no_o())
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
@@ -471,7 +490,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         for (int k = 0; k < 4; ++k)
             umma_bf16_ta(tm + TM_S, tz + 8 * k, smem_desc(sK + k * 2048, 8192, 1024),
                          idesc_bf16(128, 128, false, true), 1);
-        if (!no_o)
+        if (!no_o())
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 umma_bf16_ta(tm + TM_O, tz + 8 * k, smem_desc(sP + k * 32, 16, 1024),
@@ -505,18 +524,18 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             tmem_ld32(tl + TM_S + 64 * half, *reinterpret_cast<float(*)[32]>(sv));
             tmem_ld32(tl + TM_S + 64 * half + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
             tmem_ld_wait();
-            if (last && p.S_final && !abort_flag) {
+            if (last && opaque(p.S_final) && !abort_flag) {
                 float *dst = p.S_final + ((size_t)bh * kD + d_row) * kD + 64 * half;
 #pragma unroll
                 for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
             }
             state_half(half, sv, gN, !last);
         }
-        if (!no_o) {
+        if (!no_o()) {
             const bool gscale = g_ell[c & 3][kC - 1] > kSplitLog;
             const float *gam = g_gam[c & 3];
-            // [64 tokens][dv] tile in R2 (free once the chunk's MMAs have run), two 64-column panels
-            uint8_t *ot = sm + OFF_R2 + (d_row >> 6) * 8192;
+            // [64 tokens][dv] tile, two 64-column panels (the previous tile's store has read it)
+            uint8_t *ot = sm + OFF_O + (d_row >> 6) * 8192;
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
                 float ov[32], gv[32];
@@ -536,8 +555,8 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             fence_proxy_async();
             named_sync(kBarChain, kChainThreads);
             if (c_issuer) {                               // rows past T are clipped by the copy
-                tma_store_4d(&tmO, sm + OFF_R2, 0, h, t0, b);
-                tma_store_4d(&tmO, sm + OFF_R2 + 8192, 64, h, t0, b);
+                tma_store_4d(&tmO, sm + OFF_O, 0, h, t0, b);
+                tma_store_4d(&tmO, sm + OFF_O + 8192, 64, h, t0, b);
                 tma_store_commit();
             }
         }
@@ -554,7 +573,6 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         for (int c = 0; c < nchunks; ++c) {
             if (warp == 4 && c + 1 < nchunks) load_gates(c + 1);   // arrays built in solve(c)
             wait_mma(&bar_g, c);
-            if (c >= 1) wait_mma(&bar_uw, c - 1);         // R1 free: Tinv of chunk c-1 consumed
             if (c >= 2) {                                 // P[c&1] and U[c&1] free
                 wait_on(&bar_cdone[c & 1], (uint32_t)(((c - 2) >> 1) & 1));
                 tc_fence_after();
@@ -563,6 +581,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             tc_fence_before();
             named_sync(kBarPrep, kPrepThreads);
             tc_fence_after();
+            if (c >= 1) wait_mma(&bar_uw, c - 1);         // T free: U/W of chunk c-1 have run
             solve(c);
             psync();
             if (p_issuer && c >= 1) {                     // TM_W free: the chain has read W(c-1)
@@ -615,6 +634,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             issue_z_o(c);
             wait_mma(&bar_z, c);
             zt_pack(c, fold);
+            if (c_issuer) tma_store_wait_read0();         // the o tile of chunk c-1 has been read
             csync();
             issue_mma2(c);
             wait_mma(&bar_o2, c);
@@ -626,8 +646,6 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                 }
             }
             epilogue(c);
-            if (c_issuer) tma_store_wait_read0();         // R2 (the o tile) is free for -W(c+1)
-            fence_proxy_async();
             tc_fence_before();
             const bool stop = named_sync_or(kBarChain, kChainThreads, abort_flag != 0);
             tc_fence_after();

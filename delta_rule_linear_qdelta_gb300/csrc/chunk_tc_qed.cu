@@ -27,8 +27,9 @@
 // Shared memory (offsets from a 1024-aligned base):
 //   XQ 32 KB (per 64-column panel: Ae rows 0-63 | Q -> Qe rows 64-127)
 //   K 16 KB (K -> Ke -> Kd), V 16 KB (V -> W*V), G 16 KB, Bt 16 KB, Wt 16 KB (g, b, w tiles)
-//   S_in 32 KB bf16 state, R1 17 KB (At fp32 -> Tinv bf16), R2 16 KB (scratch, -W, Z^T,
-//   O staging), P 8 KB.
+//   S_in 32 KB bf16 state, R1 17 KB (At fp32, the solve's intermediate blocks), R2 16 KB
+//   (scratch, -W, Z^T, O staging), P 8 KB, T 8 KB (Tinv bf16, zero above the diagonal
+//   blocks).
 // TMEM (512 columns): G 0-63, O1 64-127, U/Z 128-191, W 192-255, O2 256-319, S 320-447.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -52,7 +53,10 @@ constexpr uint32_t OFF_S = 114688;
 constexpr uint32_t OFF_R1 = OFF_S + 32768;           // 147456
 constexpr uint32_t OFF_R2 = OFF_R1 + 17408;          // 164864
 constexpr uint32_t OFF_P = OFF_R2 + 16384;           // 181248
-constexpr uint32_t kSmemUsed = OFF_P + 8192;         // 189440
+constexpr uint32_t OFF_T = OFF_P + 8192;             // 189440 (Tinv, bf16 [64][64])
+constexpr uint32_t kSmemUsed = OFF_T + 8192;         // 197632
+static_assert(OFF_R2 % 1024 == 0 && OFF_P % 1024 == 0 && OFF_T % 1024 == 0 && OFF_S % 1024 == 0,
+              "128-byte-swizzled MMA operands start on 1024-byte boundaries");
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t TM_G = 0, TM_O1 = 64, TM_U = 128, TM_W = 192, TM_O2 = 256, TM_S = 320;
@@ -109,6 +113,9 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
         tmem_alloc(&tmem_base, 512);
         tmem_relinquish();
     }
+    for (int i = tid; i < 8192 / 16; i += kThreads)   // Tinv: zeros above the diagonal blocks
+        reinterpret_cast<uint4 *>(sm + OFF_T)[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async();                              // ... as the tensor core will read them
 
     auto load_gbw = [&](int c) {
         mbar_arrive_expect_tx(&bar_gbw, 3 * kC * kD * 2);
@@ -186,7 +193,7 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
 
     const uint32_t sbase = smem_u32(sm);
     const uint32_t sXQ = sbase + OFF_XQ, sK = sbase + OFF_K, sV = sbase + OFF_V, sS = sbase + OFF_S;
-    const uint32_t sR1 = sbase + OFF_R1, sR2 = sbase + OFF_R2, sP = sbase + OFF_P;
+    const uint32_t sT = sbase + OFF_T, sR2 = sbase + OFF_R2, sP = sbase + OFF_P;
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * kC;
         const uint32_t par = (uint32_t)(c & 1);
@@ -332,20 +339,21 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
         tc_fence_before();
         __syncthreads();
 
-        // (6) Tinv = (I + At)^{-1} -> R1 (twice: the U and W products read the same matrix)
+        // (6) Tinv = (I + At)^{-1} -> T (the U and W products read the same matrix)
         unit_lower_inverse(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_R2),
-                           sm + OFF_R1, sm + OFF_R1 + 8192, nullptr, nullptr, []() {}, []() { __syncthreads(); });
+                           sm + OFF_T, nullptr, nullptr, nullptr, []() {}, []() { __syncthreads(); },
+                           []() { named_sync(14, 128); });
         sync_for_mma();
 
         // (7) U^T = (W*V)^T Tinv^T, W^T = Ae^T Tinv^T
         if (issuer) {
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                umma_bf16(tm + TM_U, smem_desc(sV + k * 2048, 8192, 1024), smem_desc(sR1 + k * 32, 16, 1024),
+                umma_bf16(tm + TM_U, smem_desc(sV + k * 2048, 8192, 1024), smem_desc(sT + k * 32, 16, 1024),
                           idesc_bf16(128, 64, true, false), k > 0);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                umma_bf16(tm + TM_W, smem_desc(sXQ + k * 2048, 16384, 1024), smem_desc(sR1 + 8192 + k * 32, 16, 1024),
+                umma_bf16(tm + TM_W, smem_desc(sXQ + k * 2048, 16384, 1024), smem_desc(sT + k * 32, 16, 1024),
                           idesc_bf16(128, 64, true, false), k > 0);
             umma_commit(&bar_mma);
         }

@@ -39,6 +39,19 @@ __device__ __forceinline__ bool named_sync_or(int id, int count, bool pred) {
 
 __device__ __forceinline__ float bf(__nv_bfloat16 x) { return __bfloat162float(x); }
 
+// Returns v unchanged but hides it from the optimiser.  A loop-invariant flag or
+// nullable pointer tested inside a long loop would otherwise let the compiler copy
+// the whole loop once per value (loop unswitching), multiplying the kernel's code
+// size; instruction fetch is then a measurable share of the stall cycles.
+__device__ __forceinline__ uint32_t opaque(uint32_t v) {
+    asm volatile("" : "+r"(v));
+    return v;
+}
+template <typename T> __device__ __forceinline__ T *opaque(T *v) {
+    asm volatile("" : "+l"(v));
+    return v;
+}
+
 __device__ __forceinline__ void unpack8(const uint4 &u, float (&f)[8]) {
     const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
 #pragma unroll
@@ -130,12 +143,28 @@ __device__ __forceinline__ void tile8_cab(float (&d)[4], const float *C, int ldc
     mma_tf32(d, a, b0, b1);
 }
 
+// bf16 outputs of the inverse: s * Tinv(row, col) * s1[col] into out1 and, unless
+// out2 is null, times s2[col] into out2 (null scales mean 1); col is even and
+// (v0, v1) are columns col and col + 1 of the row.
+__device__ __forceinline__ void put_pair(uint8_t *out1, uint8_t *out2, const float *s1, const float *s2, int row,
+                                         int col, float v0, float v1) {
+    const float a0 = s1 ? v0 * s1[col] : v0, a1 = s1 ? v1 * s1[col + 1] : v1;
+    const uint32_t off = sw128_off(row, col);
+    *reinterpret_cast<uint32_t *>(out1 + off) = pack_bf16x2(a0, a1);
+    if (out2)
+        *reinterpret_cast<uint32_t *>(out2 + off) =
+            pack_bf16x2(s2 ? a0 * s2[col] : a0, s2 ? a1 * s2[col + 1] : a1);
+}
+
 // Tinv = (I + A)^{-1} for the 64x64 strictly lower fp32 matrix A held in M (row
-// stride LA, zero on and above the diagonal), then Tinv diag(s1) -> out1 and
-// Tinv diag(s1 s2) -> out2 as bf16 [64][64] tiles in the 128-byte swizzle (out1
-// and out2 may overlay M; null scales mean 1).  Y is >= 32*LY floats of scratch.
+// stride LA, zero on and above the diagonal).  Writes Tinv diag(s1) to out1 and
+// Tinv diag(s1 s2) to out2 as bf16 [64][64] tiles in the 128-byte swizzle, each
+// block as soon as it is final (null scales mean 1, null out2 skips it).  out1 and
+// out2 must not overlap M and must hold zeros above the 8x8 diagonal blocks (that
+// part of the inverse is zero and is never written).  Y is >= 32*LY floats of
+// scratch; M is overwritten with intermediate blocks.
 //   a) the eight 8x8 diagonal blocks by forward substitution, one column per lane,
-//      the block held in registers
+//      the block held in registers (warps 0-1)
 //   b) 8 -> 16:  T10 = -T11 (A10 T00), one warp per block pair
 //   c) 16 -> 32: the same on 16x16 blocks, one warp per (pair, 8-column tile)
 //   d) 32 -> 64: the same on the two 32x32 halves, one warp per 16x8 tile
@@ -143,109 +172,96 @@ __device__ __forceinline__ void tile8_cab(float (&d)[4], const float *C, int ldc
 // diagonal is implied, zeros above), so each merge is two products,
 // Y = A21 + A21 T11s and T21 = -(Y + T22s Y), run on the warp MMA.  Between the two
 // products only the warps that read the A21 being overwritten synchronise: the
-// warp itself (8 -> 16), the warp pair on named barrier 8 + pair (16 -> 32), all
-// warps (32 -> 64).
+// warp itself (8 -> 16), the warp pair on named barrier 8 + pair (16 -> 32); in
+// 32 -> 64 nothing is overwritten and warps w, w + 4 share their Y tiles on named
+// barrier 10 + w (w < 4).  The caller orders the bf16 writes before their use (proxy
+// fence and barrier).
 // Called by kThreads threads (thread indices 0..kThreads-1) that synchronise with
-// sync(); idle() runs on every one of them while warps 0-1 invert the diagonal blocks.
-template <typename Idle, typename Sync>
+// sync(); phases a-c run on warps 0-3 alone, which synchronise with sync_lo(), while
+// warps 4-7 run idle().
+template <typename Idle, typename Sync, typename SyncLo>
 __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *out1, uint8_t *out2,
-                                                   const float *s1, const float *s2, Idle idle, Sync sync) {
+                                                   const float *s1, const float *s2, Idle idle, Sync sync,
+                                                   SyncLo sync_lo) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    if (warp < 2) {
-        const int base = 8 * (4 * warp + (lane >> 3)), j = lane & 7;
-        float a[8][8];
+    if (warp >= 4) {
+        idle();
+    } else {
+        const int g = lane >> 2, t4 = lane & 3;
+        if (warp < 2) {
+            const int base = 8 * (4 * warp + (lane >> 3)), j = lane & 7;
+            float a[8][8];
 #pragma unroll
-        for (int i = 1; i < 8; ++i) {                  // the block's rows 1-7, all loads first
-            const float4 lo = *reinterpret_cast<const float4 *>(M + (base + i) * LA + base);
-            const float4 hi = *reinterpret_cast<const float4 *>(M + (base + i) * LA + base + 4);
-            a[i][0] = lo.x; a[i][1] = lo.y; a[i][2] = lo.z; a[i][3] = lo.w;
-            a[i][4] = hi.x; a[i][5] = hi.y; a[i][6] = hi.z; a[i][7] = hi.w;
-        }
-        float t[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float acc0 = (i == j) ? 1.f : 0.f, acc1 = 0.f;
-#pragma unroll
-            for (int m = 0; m < i; ++m) {
-                if (m & 1) acc1 = fmaf(-a[i][m], t[m], acc1);
-                else acc0 = fmaf(-a[i][m], t[m], acc0);
+            for (int i = 1; i < 8; ++i) {                  // the block's rows 1-7, all loads first
+                const float4 lo = *reinterpret_cast<const float4 *>(M + (base + i) * LA + base);
+                const float4 hi = *reinterpret_cast<const float4 *>(M + (base + i) * LA + base + 4);
+                a[i][0] = lo.x; a[i][1] = lo.y; a[i][2] = lo.z; a[i][3] = lo.w;
+                a[i][4] = hi.x; a[i][5] = hi.y; a[i][6] = hi.z; a[i][7] = hi.w;
             }
-            t[i] = (i < j) ? 0.f : acc0 + acc1;
-        }
+            const float c1 = s1 ? s1[base + j] : 1.f;
+            const float c2 = s2 ? c1 * s2[base + j] : c1;
+            float t[8];
 #pragma unroll
-        for (int i = 1; i < 8; ++i)
-            if (i > j) M[(base + i) * LA + base + j] = t[i];
-    }
-    idle();
-    sync();
-    // 8 -> 16: warp w < 4 merges the 8x8 blocks at 16 w
-    if (warp < 4) {
-        const int base = 16 * warp, g = lane >> 2, t = lane & 3;
-        float *Yw = Y + 8 * warp * LY;
-        float d[4];
-        tile8_cab(d, M + (base + 8) * LA + base, LA, M + (base + 8) * LA + base, LA, M + base * LA + base, LA);
-        *reinterpret_cast<float2 *>(Yw + g * LY + 2 * t) = make_float2(d[0], d[1]);
-        __syncwarp();
-        tile8_cab(d, Yw, LY, M + (base + 8) * LA + base + 8, LA, Yw, LY);
-        *reinterpret_cast<float2 *>(M + (base + 8 + g) * LA + base + 2 * t) = make_float2(-d[0], -d[1]);
-    }
-    sync();
-    // 16 -> 32: warp w < 4 takes pair p = w / 2 (blocks at 32 p) and 8-column tile w % 2
-    if (warp < 4) {
-        const int p = warp >> 1, n0 = 8 * (warp & 1), base = 32 * p;
-        float *Yp = Y + 16 * p * LY;
-        float d[4];
-        tile_cab<16>(d, M + (base + 16) * LA + base + n0, LA, M + (base + 16) * LA + base, LA,
-                     M + base * LA + base + n0, LA);                // A10 + A10 T00s
-        tile_store(Yp + n0, LY, d, 1.f);
-        named_sync(8 + p, 64);        // the pair's A10 has been read before T10 overwrites it
-        tile_cab<16>(d, Yp + n0, LY, M + (base + 16) * LA + base + 16, LA, Yp + n0, LY);   // Y + T11s Y
-        tile_store(M + (base + 16) * LA + base + n0, LA, d, -1.f);
+            for (int i = 0; i < 8; ++i) {
+                float acc0 = (i == j) ? 1.f : 0.f, acc1 = 0.f;
+#pragma unroll
+                for (int m = 0; m < i; ++m) {
+                    if (m & 1) acc1 = fmaf(-a[i][m], t[m], acc1);
+                    else acc0 = fmaf(-a[i][m], t[m], acc0);
+                }
+                t[i] = (i < j) ? 0.f : acc0 + acc1;
+            }
+#pragma unroll
+            for (int i = 1; i < 8; ++i)
+                if (i > j) M[(base + i) * LA + base + j] = t[i];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {                  // the whole block, zeros above the diagonal
+                const uint32_t off = sw128_off(base + i, base + j);
+                *reinterpret_cast<__nv_bfloat16 *>(out1 + off) = __float2bfloat16_rn(t[i] * c1);
+                if (out2) *reinterpret_cast<__nv_bfloat16 *>(out2 + off) = __float2bfloat16_rn(t[i] * c2);
+            }
+        }
+        sync_lo();
+        // 8 -> 16: warp w < 4 merges the 8x8 blocks at 16 w
+        {
+            const int base = 16 * warp;
+            float *Yw = Y + 8 * warp * LY;
+            float d[4];
+            tile8_cab(d, M + (base + 8) * LA + base, LA, M + (base + 8) * LA + base, LA, M + base * LA + base, LA);
+            *reinterpret_cast<float2 *>(Yw + g * LY + 2 * t4) = make_float2(d[0], d[1]);
+            __syncwarp();
+            tile8_cab(d, Yw, LY, M + (base + 8) * LA + base + 8, LA, Yw, LY);
+            *reinterpret_cast<float2 *>(M + (base + 8 + g) * LA + base + 2 * t4) = make_float2(-d[0], -d[1]);
+            put_pair(out1, out2, s1, s2, base + 8 + g, base + 2 * t4, -d[0], -d[1]);
+        }
+        sync_lo();
+        // 16 -> 32: warp w < 4 takes pair p = w / 2 (blocks at 32 p) and 8-column tile w % 2
+        {
+            const int p = warp >> 1, n0 = 8 * (warp & 1), base = 32 * p;
+            float *Yp = Y + 16 * p * LY;
+            float d[4];
+            tile_cab<16>(d, M + (base + 16) * LA + base + n0, LA, M + (base + 16) * LA + base, LA,
+                         M + base * LA + base + n0, LA);                // A10 + A10 T00s
+            tile_store(Yp + n0, LY, d, 1.f);
+            named_sync(8 + p, 64);        // the pair's A10 has been read before T10 overwrites it
+            tile_cab<16>(d, Yp + n0, LY, M + (base + 16) * LA + base + 16, LA, Yp + n0, LY);   // Y + T11s Y
+            tile_store(M + (base + 16) * LA + base + n0, LA, d, -1.f);
+            put_pair(out1, out2, s1, s2, base + 16 + g, base + n0 + 2 * t4, -d[0], -d[1]);
+            put_pair(out1, out2, s1, s2, base + 24 + g, base + n0 + 2 * t4, -d[2], -d[3]);
+        }
     }
     sync();
     // 32 -> 64: warp w takes rows 16 (w / 4) and columns 8 (w % 4) of the 32x32 block
     {
+        const int g = lane >> 2, t4 = lane & 3;
         const int m0 = 16 * (warp >> 2), n0 = 8 * (warp & 3);
         float d[4];
         tile_cab<32>(d, M + (32 + m0) * LA + n0, LA, M + (32 + m0) * LA, LA, M + n0, LA);   // A21 + A21 T11s
         tile_store(Y + m0 * LY + n0, LY, d, 1.f);
-        sync();                       // all of A21 has been read before T21 overwrites it
+        named_sync(10 + (warp & 3), 64);   // warps w and w ^ 4: Y columns n0..n0+7, all 32 rows
         tile_cab<32>(d, Y + m0 * LY + n0, LY, M + (32 + m0) * LA + 32, LA, Y + n0, LY);    // Y + T22s Y
-        tile_store(M + (32 + m0) * LA + n0, LA, d, -1.f);
-    }
-    sync();
-    // Tinv*beta and Tinv*beta*gamma as bf16 [64][64] (128B swizzle) over R1
-    float tv[2][8];
-    int rows[2], chs[2];
-#pragma unroll
-    for (int n = 0; n < 2; ++n) {
-        const int u = tid + kThreads * n;          // 512 chunks of 8
-        rows[n] = u >> 3;
-        chs[n] = u & 7;
-        const float4 lo = *reinterpret_cast<const float4 *>(M + rows[n] * LA + 8 * chs[n]);
-        const float4 hi = *reinterpret_cast<const float4 *>(M + rows[n] * LA + 8 * chs[n] + 4);
-        const float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int j = 8 * chs[n] + e;
-            tv[n][e] = (j < rows[n]) ? v[e] : (j == rows[n] ? 1.f : 0.f);
-        }
-    }
-    // the column scales, read before any store (the compiler cannot tell them apart)
-    float f1[2][8], f2[2][8];
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int j = 8 * chs[n] + e;
-            f1[n][e] = s1 ? tv[n][e] * s1[j] : tv[n][e];
-            f2[n][e] = s2 ? f1[n][e] * s2[j] : f1[n][e];
-        }
-    sync();
-#pragma unroll
-    for (int n = 0; n < 2; ++n) {
-        *reinterpret_cast<uint4 *>(out1 + sw128_off(rows[n], 8 * chs[n])) = pack8(f1[n]);
-        *reinterpret_cast<uint4 *>(out2 + sw128_off(rows[n], 8 * chs[n])) = pack8(f2[n]);
+        put_pair(out1, out2, s1, s2, 32 + m0 + g, n0 + 2 * t4, -d[0], -d[1]);
+        put_pair(out1, out2, s1, s2, 40 + m0 + g, n0 + 2 * t4, -d[2], -d[3]);
     }
 }
 
