@@ -50,6 +50,7 @@
 //                block by the solve; zero above the 8x8 diagonal blocks
 //   Y    4.5 KB  fp32 scratch of the solve (prep group only)
 //   O    16 KB   o(c) [64][dv] bf16 for the TMA store (chain group only)
+//   M21  2x2 KB  -M21 (diag(1/kappa)) bf16 [32][32] without swizzle, by chunk parity
 // All shared-memory MMA operands use the 128-byte swizzle (TMA layout): 128-byte
 // rows, 8-row groups 1024 bytes apart, 64-column panels.
 // TMEM (512 columns): G 0-63, W 64-127, U[0] 128-191, U[1] 192-255 (Z^T accumulates
@@ -88,8 +89,9 @@ constexpr uint32_t OFF_P = OFF_R2 + 16384;           // 164864 (two 8 KB buffers
 constexpr uint32_t OFF_T = OFF_P + 16384;           // 181248 (Tinv*beta, Tinv*beta*gamma bf16)
 constexpr uint32_t OFF_Y = OFF_T + 16384;           // 197632 (solve scratch, 32 x LY fp32)
 constexpr uint32_t OFF_O = 203776;                   // o tile [64][dv] bf16 for the TMA store
-constexpr uint32_t kSmemUsed = OFF_O + 16384;        // 220160
-static_assert(OFF_O % 1024 == 0 && OFF_O >= OFF_Y + 32 * LY * 4, "o tile placement");
+constexpr uint32_t OFF_M21 = OFF_O + 16384;          // 220160 (two 2 KB coupling tiles)
+constexpr uint32_t kSmemUsed = OFF_M21 + 4096;       // 224256
+static_assert(OFF_O % 1024 == 0 && OFF_O >= OFF_Y + 32 * LY * 4 && OFF_M21 % 1024 == 0, "tile placement");
 static_assert(OFF_R2 % 1024 == 0 && OFF_P % 1024 == 0 && OFF_T % 1024 == 0 && kSmemUsed + 1024 <= 232448,
               "128-byte-swizzled MMA operands start on 1024-byte boundaries");
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
@@ -120,7 +122,8 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmO) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t bar_full[2], bar_g, bar_uw, bar_z, bar_o2, bar_ready, bar_wfree, bar_cdone[2], bar_drain[2];
+    __shared__ uint64_t bar_full[2], bar_g, bar_uw, bar_z, bar_cp, bar_o2, bar_ready, bar_wfree, bar_cdone[2],
+        bar_drain[2];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     // per-chunk gate arrays, by chunk index mod 4: while the prep group builds chunk
@@ -153,6 +156,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         mbar_init(&bar_g, 1);
         mbar_init(&bar_uw, 1);
         mbar_init(&bar_z, 1);
+        mbar_init(&bar_cp, 1);
         mbar_init(&bar_o2, 1);
         mbar_init(&bar_ready, 1);
         mbar_init(&bar_wfree, 1);
@@ -379,14 +383,17 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             }
         }
     };
-    // Tinv -> Tinv*beta, Tinv*beta*gamma into T (R1 and Y as scratch); warp 4 meanwhile
-    // turns the next chunk's raw gates into arrays
+    // the two 32-token halves' inverses diag(T11, T22) -> Tinv*beta, Tinv*beta*gamma into T,
+    // and the coupling -M21 (times 1/kappa in fold mode) into M21[c&1] (R1 and Y as scratch);
+    // warp 4 meanwhile turns the next chunk's raw gates into arrays
     auto solve = [&](int c) {
         const int gi = c & 3;
-        unit_lower_inverse(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_Y),
-                           sm + OFF_T, sm + OFF_T + 8192, g_beta[gi], g_gam[gi],
-                           [&]() { if (warp == 4 && c + 1 < nchunks) compute_gates(c + 1); },
-                           []() { named_sync(kBarPrep, kPrepThreads); }, []() { named_sync(kBarLo, 128); });
+        const bool fold = g_ell[gi][kC - 1] > kFoldLog;
+        unit_lower_inverse<true>(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_Y),
+                                 sm + OFF_T, sm + OFF_T + 8192, g_beta[gi], g_gam[gi],
+                                 [&]() { if (warp == 4 && c + 1 < nchunks) compute_gates(c + 1); },
+                                 []() { named_sync(kBarPrep, kPrepThreads); }, []() { named_sync(kBarLo, 128); },
+                                 sm + OFF_M21 + (c & 1) * 2048, fold ? g_gam[gi] : nullptr, g_igam[gi][kC - 1]);
     };
     // U^T = V^T T1^T into U[c&1], W^T = X^T T2^T
     auto issue_uw = [&](int c) {
@@ -462,24 +469,34 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                              idesc_bf16(128, 64, false, false), k > 0);
             }
     };
-    // Z^T (fp32, U[c&1]) -> Zt^T as packed bf16 pairs of tokens in the first 32 columns
-    // of U[c&1]; in fold mode Zt^T = Z^T diag(kappa)
-    auto zt_pack = [&](int c, bool fold) {
+    // 32 tokens of Z^T (fp32, columns 32 hf.. of U[c&1]) -> Zt^T as packed bf16 pairs into
+    // columns 16 hf.. of U[c&1]; in fold mode Zt^T = Z^T diag(kappa)
+    auto zt_pack = [&](int c, int hf2, bool fold) {
         const uint32_t tu = tl + TM_U + 64 * (uint32_t)(c & 1);
-        const float *kap = g_kap[c & 3];
-        float z[64];
-        tmem_ld32(tu, *reinterpret_cast<float(*)[32]>(z));
-        tmem_ld32(tu + 32, *reinterpret_cast<float(*)[32]>(z + 32));
+        const float *kap = g_kap[c & 3] + 32 * hf2;
+        float z[32];
+        tmem_ld32(tu + 32 * hf2, z);
         tmem_ld_wait();
-        uint32_t zp[32];
+        uint32_t zp[16];
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {              // no shared-memory stores here: kappa read as needed
+        for (int j = 0; j < 16; j += 2) {              // no shared-memory stores here: kappa read as needed
             const float4 kv = fold ? *reinterpret_cast<const float4 *>(kap + 2 * j) : make_float4(1.f, 1.f, 1.f, 1.f);
             zp[j] = pack_bf16x2(z[2 * j] * kv.x, z[2 * j + 1] * kv.y);
             zp[j + 1] = pack_bf16x2(z[2 * j + 2] * kv.z, z[2 * j + 3] * kv.w);
         }
-        tmem_st32(tu, zp);
+        tmem_st16(tu + 16 * hf2, zp);
         tmem_st_wait();
+    };
+    // the solve's coupling: Z^T of tokens 32-63 -= Zt^T(tokens 0-31) (M21 diag(1/kappa))^T
+    auto issue_couple = [&](int c) {
+        if (!c_issuer) return;
+        const uint32_t tu = tm + TM_U + 64 * (uint32_t)(c & 1);
+        const uint32_t sM = sbase + OFF_M21 + (uint32_t)(c & 1) * 2048;
+#pragma unroll
+        for (int k = 0; k < 2; ++k)                       // K = 16 tokens = two core matrices along K
+            umma_bf16_ta(tu + 32, tu + 8 * k, smem_desc_noswz(sM + k * 256, 128, 512),
+                         idesc_bf16(128, 32, false, false), 1);
+        umma_commit(&bar_cp);
     };
     // O += Zt^T Pt^T ; S += Zt^T (kappa K)  (S in TMEM already scaled by gamma_C); A = Zt^T in TMEM
     auto issue_mma2 = [&](int c) {
@@ -633,7 +650,11 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             if (c_issuer) mbar_arrive(&bar_wfree);
             issue_z_o(c);
             wait_mma(&bar_z, c);
-            zt_pack(c, fold);
+            zt_pack(c, 0, fold);
+            csync();
+            issue_couple(c);
+            wait_mma(&bar_cp, c);
+            zt_pack(c, 1, fold);
             if (c_issuer) tma_store_wait_read0();         // the o tile of chunk c-1 has been read
             csync();
             issue_mma2(c);

@@ -143,6 +143,13 @@ __device__ __forceinline__ void tile8_cab(float (&d)[4], const float *C, int ldc
     mma_tf32(d, a, b0, b1);
 }
 
+// Byte offset of bf16 element (row, col) of a [32][32] K-major MMA operand without
+// swizzle: 8x8 core matrices of 128 contiguous bytes (8 rows of 16 bytes), 128 bytes
+// apart along K (leading offset) and 512 bytes apart along the rows (stride offset).
+__device__ __forceinline__ uint32_t core_off(int row, int col) {
+    return (uint32_t)((row >> 3) * 512 + (col >> 3) * 128 + (row & 7) * 16 + (col & 7) * 2);
+}
+
 // bf16 outputs of the inverse: s * Tinv(row, col) * s1[col] into out1 and, unless
 // out2 is null, times s2[col] into out2 (null scales mean 1); col is even and
 // (v0, v1) are columns col and col + 1 of the row.
@@ -179,10 +186,18 @@ __device__ __forceinline__ void put_pair(uint8_t *out1, uint8_t *out2, const flo
 // Called by kThreads threads (thread indices 0..kThreads-1) that synchronise with
 // sync(); phases a-c run on warps 0-3 alone, which synchronise with sync_lo(), while
 // warps 4-7 run idle().
-template <typename Idle, typename Sync, typename SyncLo>
+//
+// With kCouple the last merge is left to the caller: phase d then computes only
+// M21 = T22 A21 (the 32x32 block coupling the two halves) and writes
+// -M21 diag(s3 * s3_mul) (null s3: -M21) as a bf16 [32][32] tile without swizzle
+// (core_off below) to out3; out1/out2 then hold the block-diagonal inverse
+// diag(T11, T22) with the same scalings.  Since T21 = -M21 T11, a solve (I + A) z = r is finished from the
+// block-diagonal one, zl = diag(T11, T22) r, by z_bot = zl_bot - M21 z_top.
+template <bool kCouple = false, typename Idle, typename Sync, typename SyncLo>
 __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *out1, uint8_t *out2,
                                                    const float *s1, const float *s2, Idle idle, Sync sync,
-                                                   SyncLo sync_lo) {
+                                                   SyncLo sync_lo, uint8_t *out3 = nullptr,
+                                                   const float *s3 = nullptr, float s3_mul = 1.f) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (warp >= 4) {
         idle();
@@ -251,6 +266,17 @@ __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *
         }
     }
     sync();
+    if (kCouple) {                    // M21 = A21 + T22s A21, warp w: rows 16 (w / 4), columns 8 (w % 4)
+        const int g = lane >> 2, t4 = lane & 3;
+        const int m0 = 16 * (warp >> 2), n0 = 8 * (warp & 3);
+        float d[4];
+        tile_cab<32>(d, M + (32 + m0) * LA + n0, LA, M + (32 + m0) * LA + 32, LA, M + 32 * LA + n0, LA);
+        const int c0 = n0 + 2 * t4;
+        const float f0 = s3 ? -s3[c0] * s3_mul : -1.f, f1 = s3 ? -s3[c0 + 1] * s3_mul : -1.f;
+        *reinterpret_cast<uint32_t *>(out3 + core_off(m0 + g, c0)) = pack_bf16x2(f0 * d[0], f1 * d[1]);
+        *reinterpret_cast<uint32_t *>(out3 + core_off(m0 + 8 + g, c0)) = pack_bf16x2(f0 * d[2], f1 * d[3]);
+        return;
+    }
     // 32 -> 64: warp w takes rows 16 (w / 4) and columns 8 (w % 4) of the 32x32 block
     {
         const int g = lane >> 2, t4 = lane & 3;
