@@ -76,7 +76,10 @@ size_t qdelta_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd
     return qd::qdelta_segment_workspace(B, H, qd::qdelta_segments(B, T, H, dk, dv, dtype));
 }
 
-size_t qed_workspace_bytes(int, int, int, int, int, int, qd_dtype) { return 0; }
+size_t qed_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype) {
+    if (B <= 0 || T <= 0 || H <= 0 || chunk != 64) return 0;
+    return qd::qdelta_segment_workspace(B, H, qd::qed_segments(B, T, H, dk, dv, dtype));
+}
 
 qd_status qdelta_fwd(const void *q, const void *k, const void *v, const void *alpha, const void *beta,
                      const void *lam, const float *S0, void *o, float *S_final, int B, int T, int H,
@@ -122,8 +125,13 @@ qd_status qed_fwd(const void *q, const void *k, const void *v, const void *g, co
     if (B == 0 || H == 0) { g_launches = 0; return QD_OK; }
     if (T == 0) { g_launches = 0; return empty_sequence(S0, S_final, B, H, dk, dv, stream); }
     qd::QedArgs a{q, k, v, g, b, w, lam_h, S0, o, S_final, B, T, H, dk, dv, workspace, workspace_bytes};
-    cudaError_t e = qd::qed_tc_supported(a, dtype) ? qd::launch_qed_chunk_tc(a, stream, &n)
-                                                   : qd::launch_qed_chunk_simt(a, dtype, stream, &n);
+    cudaError_t e;
+    if (qd::qed_tc_supported(a, dtype)) {
+        const int G = qd::qed_segments(B, T, H, dk, dv, dtype);
+        e = G > 1 ? qd::launch_qed_segmented(a, G, stream, &n) : qd::launch_qed_chunk_tc(a, stream, &n);
+    } else {
+        e = qd::launch_qed_chunk_simt(a, dtype, stream, &n);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "qed_fwd launch");
     g_launches = n;
     return QD_OK;

@@ -65,6 +65,7 @@ struct QedTcParams {
     const float *lam_h, *S0;
     float *S_final;
     int B, T, H;
+    int flags;   // kTcNoV | kTcS0Identity | kTcNoO (segment-scan passes)
 };
 
 struct QedMaps {
@@ -93,6 +94,11 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
     const bool producer = (tid == 0), issuer = (tid == 32);
     const float lam_h = p.lam_h[h];
     const int d_row = 32 * q4 + lane;
+    // flags of the segment-scan passes, read through opaque() inside the chunk loop
+    const uint32_t flags = (uint32_t)p.flags;
+    const bool s0_id = flags & kTcS0Identity;
+    auto no_v = [&]() { return (opaque(flags) & kTcNoV) != 0; };
+    auto no_o = [&]() { return (opaque(flags) & kTcNoO) != 0; };
 
     if (tid == 0) {
         mbar_init(&bar_gbw, 1);
@@ -104,7 +110,7 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
         tma_prefetch_desc(&mp.q);
         tma_prefetch_desc(&mp.k);
         tma_prefetch_desc(&mp.v);
-        tma_prefetch_desc(&mp.o);
+        if (!(p.flags & kTcNoO)) tma_prefetch_desc(&mp.o);
         tma_prefetch_desc(&mp.g);
         tma_prefetch_desc(&mp.b);
         tma_prefetch_desc(&mp.w);
@@ -117,7 +123,9 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
         reinterpret_cast<uint4 *>(sm + OFF_T)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async();                              // ... as the tensor core will read them
 
+    int n_gbw = 0, n_qv = 0, n_k = 0;                 // loads issued (producer), for a drain
     auto load_gbw = [&](int c) {
+        ++n_gbw;
         mbar_arrive_expect_tx(&bar_gbw, 3 * kC * kD * 2);
 #pragma unroll
         for (int pnl = 0; pnl < 2; ++pnl) {
@@ -127,14 +135,16 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
         }
     };
     auto load_qv = [&](int c) {
-        mbar_arrive_expect_tx(&bar_qv, 2 * kC * kD * 2);
+        ++n_qv;
+        mbar_arrive_expect_tx(&bar_qv, (no_v() ? 1 : 2) * kC * kD * 2);
 #pragma unroll
         for (int pnl = 0; pnl < 2; ++pnl) {
             tma_load_4d(sm + OFF_XQ + pnl * 16384 + 8192, &mp.q, &bar_qv, 64 * pnl, h, c * kC, b);
-            tma_load_4d(sm + OFF_V + pnl * 8192, &mp.v, &bar_qv, 64 * pnl, h, c * kC, b);
+            if (!no_v()) tma_load_4d(sm + OFF_V + pnl * 8192, &mp.v, &bar_qv, 64 * pnl, h, c * kC, b);
         }
     };
     auto load_k = [&](int c) {
+        ++n_k;
         mbar_arrive_expect_tx(&bar_k, kC * kD * 2);
 #pragma unroll
         for (int pnl = 0; pnl < 2; ++pnl)
@@ -165,6 +175,9 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
                                 : make_float4(0.f, 0.f, 0.f, 0.f);
                 sv[j] = v.x; sv[j + 1] = v.y; sv[j + 2] = v.z; sv[j + 3] = v.w;
             }
+            if (s0_id)
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sv[j] = (64 * hf + 32 * half + j == d_row) ? 1.f : 0.f;
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
                 float f[8];
@@ -226,6 +239,7 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
             for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
             if (lane == 0) g_ku[t] = acc;
         }
+        if (!no_v())
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const uint32_t off = (uint32_t)(tid + kThreads * r) << 4;   // both 8 KB panels
@@ -276,12 +290,13 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
                           smem_desc(sK + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), idesc_bf16(128, 64, false, false),
                           k > 0);
             }
+            if (!no_o())
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
-                umma_bf16(tm + TM_O1, smem_desc(sS + ko, 16, 1024), smem_desc(sXQ + ko + 8192, 16, 1024),
-                          idesc_bf16(128, 64, false, false), k > 0);
-            }
+                for (int k = 0; k < 8; ++k) {
+                    const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
+                    umma_bf16(tm + TM_O1, smem_desc(sS + ko, 16, 1024), smem_desc(sXQ + ko + 8192, 16, 1024),
+                              idesc_bf16(128, 64, false, false), k > 0);
+                }
             umma_commit(&bar_mma);
         }
         wait_mma();
@@ -347,10 +362,11 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
 
         // (7) U^T = (W*V)^T Tinv^T, W^T = Ae^T Tinv^T
         if (issuer) {
+            if (!no_v())                               // v taken as 0: U = 0 (Z starts from -S^ W^T)
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                umma_bf16(tm + TM_U, smem_desc(sV + k * 2048, 8192, 1024), smem_desc(sT + k * 32, 16, 1024),
-                          idesc_bf16(128, 64, true, false), k > 0);
+                for (int k = 0; k < 4; ++k)
+                    umma_bf16(tm + TM_U, smem_desc(sV + k * 2048, 8192, 1024), smem_desc(sT + k * 32, 16, 1024),
+                              idesc_bf16(128, 64, true, false), k > 0);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 umma_bf16(tm + TM_W, smem_desc(sXQ + k * 2048, 16384, 1024), smem_desc(sT + k * 32, 16, 1024),
@@ -378,7 +394,7 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
             for (int k = 0; k < 8; ++k) {
                 const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
                 umma_bf16(tm + TM_U, smem_desc(sS + ko, 16, 1024), smem_desc(sR2 + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024),
-                          idesc_bf16(128, 64, false, false), 1);
+                          idesc_bf16(128, 64, false, false), (no_v() && k == 0) ? 0u : 1u);
             }
             umma_commit(&bar_mma);
         }
@@ -401,10 +417,11 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
 
         // (11) O2 = Z^T P^T ; S^ += Z^T Kd
         if (issuer) {
+            if (!no_o())
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                umma_bf16(tm + TM_O2, smem_desc(sR2 + k * 32, 16, 1024), smem_desc(sP + k * 32, 16, 1024),
-                          idesc_bf16(128, 64, false, false), k > 0);
+                for (int k = 0; k < 4; ++k)
+                    umma_bf16(tm + TM_O2, smem_desc(sR2 + k * 32, 16, 1024), smem_desc(sP + k * 32, 16, 1024),
+                              idesc_bf16(128, 64, false, false), k > 0);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 umma_bf16(tm + TM_S, smem_desc(sR2 + k * 32, 16, 1024), smem_desc(sK + k * 2048, 8192, 1024),
@@ -416,15 +433,17 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
 
         // (12) o = O1 + O2 -> staging (R2); state -> bf16 S_in (and S_final after the last chunk)
         {
-            float o1[32], o2[32];
-            tmem_ld32(tl + TM_O1 + 32 * hf, o1);
-            tmem_ld32(tl + TM_O2 + 32 * hf, o2);
-            tmem_ld_wait();
-            uint8_t *dst = sm + OFF_R2 + (d_row >> 6) * 8192;
+            if (!no_o()) {
+                float o1[32], o2[32];
+                tmem_ld32(tl + TM_O1 + 32 * hf, o1);
+                tmem_ld32(tl + TM_O2 + 32 * hf, o2);
+                tmem_ld_wait();
+                uint8_t *dst = sm + OFF_R2 + (d_row >> 6) * 8192;
 #pragma unroll
-            for (int cc = 0; cc < 32; ++cc)
-                *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * hf + cc, d_row & 63)) =
-                    __float2bfloat16_rn(o1[cc] + o2[cc]);
+                for (int cc = 0; cc < 32; ++cc)
+                    *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * hf + cc, d_row & 63)) =
+                        __float2bfloat16_rn(o1[cc] + o2[cc]);
+            }
             const bool last = (c + 1 == nchunks);
             uint8_t *sp = sm + OFF_S + hf * 16384;
 #pragma unroll
@@ -447,7 +466,7 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
             }
         }
         sync_for_mma();
-        if (producer) {
+        if (producer && !no_o()) {
             tma_store_4d(&mp.o, sm + OFF_R2, 0, h, t0, b);
             tma_store_4d(&mp.o, sm + OFF_R2 + 8192, 64, h, t0, b);
             tma_store_commit();
@@ -457,9 +476,9 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
     if (producer) {
         tma_store_wait_all();
         if (abort_flag) {   // drain loads that may still be landing in shared memory
-            mbar_wait(&bar_gbw, 0, kWaitNs);
-            mbar_wait(&bar_qv, 0, kWaitNs);
-            mbar_wait(&bar_k, 0, kWaitNs);
+            if (n_gbw) mbar_wait(&bar_gbw, (uint32_t)((n_gbw - 1) & 1), kWaitNs);
+            if (n_qv) mbar_wait(&bar_qv, (uint32_t)((n_qv - 1) & 1), kWaitNs);
+            if (n_k) mbar_wait(&bar_k, (uint32_t)((n_k - 1) & 1), kWaitNs);
         }
     }
     if (issuer && abort_flag) {
@@ -478,17 +497,18 @@ bool qed_tc_supported(const QedArgs &a, int dtype) {
     return dtype == kBF16 && a.dk == kD && a.dv == kD && (long long)a.T * a.H * kD * 2 < (1ll << 40);
 }
 
-cudaError_t launch_qed_chunk_tc(const QedArgs &a, cudaStream_t s, int *nlaunch) {
+cudaError_t launch_qed_chunk_tc(const QedArgs &a, cudaStream_t s, int *nlaunch, int flags) {
     QedMaps m;
     if (!make_token_map(&m.q, a.q, a.B, a.T, a.H) || !make_token_map(&m.k, a.k, a.B, a.T, a.H) ||
-        !make_token_map(&m.v, a.v, a.B, a.T, a.H) || !make_token_map(&m.o, a.o, a.B, a.T, a.H) ||
-        !make_token_map(&m.g, a.g, a.B, a.T, a.H) || !make_token_map(&m.b, a.b, a.B, a.T, a.H) ||
-        !make_token_map(&m.w, a.w, a.B, a.T, a.H))
+        !make_token_map(&m.v, a.v, a.B, a.T, a.H) || !make_token_map(&m.g, a.g, a.B, a.T, a.H) ||
+        !make_token_map(&m.b, a.b, a.B, a.T, a.H) || !make_token_map(&m.w, a.w, a.B, a.T, a.H))
         return cudaErrorInvalidValue;
+    if (flags & kTcNoO) m.o = m.q;                    // not used
+    else if (!make_token_map(&m.o, a.o, a.B, a.T, a.H)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(qed_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    QedTcParams p{a.lam_h, a.S0, a.S_final, a.B, a.T, a.H};
+    QedTcParams p{a.lam_h, a.S0, a.S_final, a.B, a.T, a.H, flags};
     qed_fwd_tc_kernel<<<a.B * a.H, kThreads, kSmemBytes, s>>>(p, m);
     e = cudaGetLastError();
     if (e == cudaSuccess) *nlaunch += 1;

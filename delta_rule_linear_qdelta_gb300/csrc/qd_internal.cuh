@@ -64,15 +64,19 @@ cudaError_t launch_qdelta_step(const StepArgs &a, int dtype, cudaStream_t s, int
 enum { kTcNoV = 1, kTcS0Identity = 2, kTcNoO = 4 };
 bool qdelta_tc_supported(const QDeltaArgs &a, int dtype);
 cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nlaunch, int flags = 0);
-// Tensor-core (tcgen05) chunked QED forward: bf16, dk = dv = 128.
+// Tensor-core (tcgen05) chunked QED forward: bf16, dk = dv = 128; flags as above.
 bool qed_tc_supported(const QedArgs &a, int dtype);
-cudaError_t launch_qed_chunk_tc(const QedArgs &a, cudaStream_t s, int *nlaunch);
+cudaError_t launch_qed_chunk_tc(const QedArgs &a, cudaStream_t s, int *nlaunch, int flags = 0);
 // Segment scan of the tensor-core forward for long sequences over few (b, h)
 // streams: the number of segments for these sizes (1 = a single pass), its
 // workspace, and the launch (three passes of the forward kernel and a combine).
 int qdelta_segments(int B, int T, int H, int dk, int dv, int dtype);
 size_t qdelta_segment_workspace(int B, int H, int G);
 cudaError_t launch_qdelta_segmented(const QDeltaArgs &a, int G, cudaStream_t s, int *nlaunch);
+// The same for QED, whose per-chunk state map is also a right-multiplication of the
+// [dv][dk] state (S_out = S_in Phi + Psi); qed_segments is its own policy.
+int qed_segments(int B, int T, int H, int dk, int dv, int dtype);
+cudaError_t launch_qed_segmented(const QedArgs &a, int G, cudaStream_t s, int *nlaunch);
 // Reads and clears the device word the tensor-core kernels set when a bounded wait runs out.
 bool tc_read_and_clear_timeout();
 bool qed_tc_read_and_clear_timeout();

@@ -1,4 +1,4 @@
-// Segment scan for long sequences over few (b, h) streams.
+// Segment scan for long sequences over few (b, h) streams (Q-Delta and QED).
 //
 // A chunk of the Q-Delta recurrence maps its entering state linearly
 // ("Q-Delta: Beyond Key-Value Associative State Evolution", Sec. 3.3.2: with the
@@ -12,6 +12,9 @@
 //   combine (fp32, per (b, h), in segment order): S_start(g) = S, S <- S Phi_g + Psi_g
 //   pass 3  S0 = S_start(g)           ->  o, exactly as one pass over the whole sequence
 // The [B][T][H][d] layout makes the segment view free: [B][G*L][H][d] is [B*G][L][H][d].
+// QED ("The Query Knows What to Forget", Eqs. 4/6/8) keeps its state transposed,
+// S^ = S^T in [dv][dk], and S^_t = S^_{t-1} Diag(e^{g_t}) (I - a_t k_t^T) + (w_t*v_t) k_t^T
+// is the same kind of map, so the same passes and combine serve it.
 // The three per-segment state arrays live in caller-provided workspace.
 #include <cuda_runtime.h>
 
@@ -107,22 +110,35 @@ int qdelta_segments(int B, int T, int H, int dk, int dv, int dtype) {
     return G;
 }
 
+int qed_segments(int B, int T, int H, int dk, int dv, int dtype) {
+    // Each QED pass repeats the whole per-chunk preparation (the single-pass kernel is
+    // not warp-specialised), so three passes over G segments pay off only when very few
+    // streams leave most SMs idle: measured on the 32-stream QED workload (B=4, H=8,
+    // T=4096), four segments took 0.64 ms against 0.61 ms for one pass.
+    return (long long)B * H <= 16 ? qdelta_segments(B, T, H, dk, dv, dtype) : 1;
+}
+
 size_t qdelta_segment_workspace(int B, int H, int G) {
     return G > 1 ? 3 * (size_t)B * G * H * kD * kD * sizeof(float) : 0;
 }
 
-cudaError_t launch_qdelta_segmented(const QDeltaArgs &a, int G, cudaStream_t s, int *nlaunch) {
+namespace {
+
+// The four launches of a segment scan; Args is QDeltaArgs or QedArgs and launch(args,
+// flags) runs one pass of the matching tensor-core kernel.
+template <typename Args, typename Launch>
+cudaError_t run_segmented(const Args &a, int G, cudaStream_t s, int *nlaunch, Launch launch) {
     const size_t n = (size_t)a.B * G * a.H * kD * kD;
     float *S_start = static_cast<float *>(a.ws), *Psi = S_start + n, *Phi = Psi + n;
-    QDeltaArgs seg = a;
+    Args seg = a;
     seg.B = a.B * G;
     seg.T = a.T / G;
     seg.S0 = nullptr;
     seg.S_final = Psi;
-    cudaError_t e = launch_qdelta_chunk_tc(seg, s, nlaunch, kTcNoO);
+    cudaError_t e = launch(seg, kTcNoO);
     if (e != cudaSuccess) return e;
     seg.S_final = Phi;
-    e = launch_qdelta_chunk_tc(seg, s, nlaunch, kTcNoO | kTcNoV | kTcS0Identity);
+    e = launch(seg, kTcNoO | kTcNoV | kTcS0Identity);
     if (e != cudaSuccess) return e;
     const size_t smem = 2 * kD * kLS * sizeof(float);
     e = cudaFuncSetAttribute(segment_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -133,7 +149,19 @@ cudaError_t launch_qdelta_segmented(const QDeltaArgs &a, int G, cudaStream_t s, 
     *nlaunch += 1;
     seg.S0 = S_start;
     seg.S_final = nullptr;
-    return launch_qdelta_chunk_tc(seg, s, nlaunch, 0);
+    return launch(seg, 0);
+}
+
+}  // namespace
+
+cudaError_t launch_qdelta_segmented(const QDeltaArgs &a, int G, cudaStream_t s, int *nlaunch) {
+    return run_segmented(a, G, s, nlaunch,
+                         [&](const QDeltaArgs &x, int f) { return launch_qdelta_chunk_tc(x, s, nlaunch, f); });
+}
+
+cudaError_t launch_qed_segmented(const QedArgs &a, int G, cudaStream_t s, int *nlaunch) {
+    return run_segmented(a, G, s, nlaunch,
+                         [&](const QedArgs &x, int f) { return launch_qed_chunk_tc(x, s, nlaunch, f); });
 }
 
 }  // namespace qd

@@ -100,6 +100,13 @@ QD_API qd_status qed_fwd(const void *q, const void *k, const void *v,
                   int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype,
                   void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* Bytes of device workspace qed_fwd needs for these sizes (0 if none).  As for
+ * qdelta_fwd, very few (b, h) streams (at most 16) carrying a long sequence are cut
+ * into segments
+ * that run in parallel (QED's per-chunk map of the transposed state is linear,
+ * S^ -> S^ Phi + Psi) and are stitched together in fp32; the workspace holds three
+ * d_v x d_k fp32 states per segment and calls sharing it must be ordered on one
+ * stream. */
 QD_API size_t qed_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype);
 
 /*

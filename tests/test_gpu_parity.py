@@ -265,6 +265,18 @@ def test_qed_lambda_zero_is_gdn2(qd):
     check(S, S_ref, "f32", "gdn2 S")
 
 
+def test_qed_segmented_long_sequence_all_outputs(qd):
+    """B=1, H=2, T=2048 with an initial state: few streams and a long sequence take
+    the segment scan for QED too (its transposed state also maps linearly)."""
+    d = synth.qed_inputs(1, 2048, 2, 128, 128, seed=57, dtype="bf16", s0_var=0.01)
+    assert qd.qed_workspace_bytes(1, 2048, 2, 128, 128) > 0
+    o, S = run_qed(qd, d)
+    assert qd.last_launch_count() == 4
+    o_ref, S_ref = oracle.qed_fwd(d["q"], d["k"], d["v"], d["g"], d["b"], d["w"], d["lam_h"], d["S0"])
+    check(o, o_ref, "bf16", "segmented qed o")
+    check(S, S_ref, "bf16", "segmented qed S")
+
+
 def test_qed_full_size_sampled(qd):
     """B=4, H=8, T=4096, d=128 bf16; 4 streams checked."""
     name, d = synth.qed_gdn2()
