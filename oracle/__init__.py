@@ -1,4 +1,4 @@
-"""Oracle: plain fp64 CPU reference of the Q-Delta / QED forward and decode step.
+"""Oracle: plain fp64 CPU reference of the Q-Delta / QED forwards and decode steps.
 
 TEST INFRASTRUCTURE.  Only `tests/`, `__graft_entry__.smoke()` and `bench.py`'s
 CPU-baseline / reference leg may import this package.  It shares no code with
@@ -45,7 +45,10 @@ def _load():
         lib.oracle_qdelta_fwd.argtypes = [I] * 5 + [P] * 9 + [I]
         lib.oracle_qed_fwd.argtypes = [I] * 5 + [P] * 10 + [I]
         lib.oracle_qdelta_step.argtypes = [I] * 4 + [P] * 8 + [I]
-        for f in (lib.oracle_qdelta_fwd, lib.oracle_qed_fwd, lib.oracle_qdelta_step):
+        lib.oracle_qed_fwd_variant.argtypes = [I] * 5 + [P] * 7 + [I] + [P] * 4 + [I]
+        lib.oracle_qed_step.argtypes = [I] * 4 + [P] * 8 + [I, P, P, I]
+        for f in (lib.oracle_qdelta_fwd, lib.oracle_qed_fwd, lib.oracle_qdelta_step, lib.oracle_qed_fwd_variant,
+                  lib.oracle_qed_step):
             f.restype = I
         _lib = lib
     return _lib
@@ -89,6 +92,42 @@ def qed_fwd(q, k, v, g, b, w, lam_h, S0=None, nthreads: int = 0):
     if rc:
         raise MemoryError("oracle_qed_fwd failed")
     return o, S
+
+
+QED_VARIANTS = {"full": 0, "nogate": 1, "nogate_noproj": 2, "rand": 3}
+
+
+def qed_fwd_variant(q, k, v, g, b, w, lam_h, variant="full", z=None, S0=None, nthreads: int = 0):
+    """QED forward for one ablation arm ("The Query Knows What to Forget", Table 1):
+    full, nogate, nogate_noproj or rand (z [H,dk] the per-head fixed vector)."""
+    vid = QED_VARIANTS[variant]
+    q, k, v, g, b, w, lam_h, z, S0 = map(_f64, (q, k, v, g, b, w, lam_h, z, S0))
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    o = np.zeros((B, T, H, dv))
+    S = np.zeros((B, H, dv, dk))
+    rc = _load().oracle_qed_fwd_variant(B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b),
+                                        _ptr(w), _ptr(lam_h), vid, _ptr(z), _ptr(S0), _ptr(o), _ptr(S), nthreads)
+    if rc:
+        raise ValueError(f"oracle_qed_fwd_variant failed ({rc})")
+    return o, S
+
+
+def qed_step(S, q, k, v, g, b, w, lam_h, variant="full", z=None, nthreads: int = 0):
+    """One QED decode step.  S [N,H,dv,dk] fp64 numpy array (QED's state transposed),
+    updated IN PLACE; q, k, g, b [N,H,dk]; v, w [N,H,dv]; lam_h [H].  Returns o [N,H,dv]."""
+    if not (isinstance(S, np.ndarray) and S.dtype == np.float64 and S.flags.c_contiguous):
+        raise TypeError("S must be a C-contiguous float64 numpy array (updated in place)")
+    vid = QED_VARIANTS[variant]
+    q, k, v, g, b, w, lam_h, z = map(_f64, (q, k, v, g, b, w, lam_h, z))
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    o = np.zeros((N, H, dv))
+    rc = _load().oracle_qed_step(N, H, dk, dv, _ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b),
+                                 _ptr(w), _ptr(lam_h), vid, _ptr(z), _ptr(o), nthreads)
+    if rc:
+        raise ValueError(f"oracle_qed_step failed ({rc})")
+    return o
 
 
 def qdelta_step(S, q, k, v, alpha, beta, lam, nthreads: int = 0):

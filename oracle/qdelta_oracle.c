@@ -23,7 +23,15 @@
  *      r = w*v - Sbar^T a;  S = Sbar + k r^T;  o = S^T q.
  *    d is formed with the given k as it is (the pages' projection assumes
  *    |k| = 1; no renormalisation is done here).
- *  - Decode step: one iteration of the Q-Delta loop per call, state in place.
+ *  - QED ablation arms: same page, Sec. 3.2 (Table 1), each a different term
+ *    added to the base erase vector b*k:
+ *      full          lambda_h P(b*q)          (the method above)
+ *      nogate        lambda_h P(q)            (the gate b removed from the new term only)
+ *      nogate-noproj lambda_h q               (no gate, no projection)
+ *      rand          lambda_h P(b*z_h)        (z_h a fixed unit vector per head)
+ *    with P(u) = u - k (k^T u).
+ *  - Decode steps: one iteration of the Q-Delta or the QED loop per call, the
+ *    state carried in and out in place.
  *
  * Storage of every state buffer, both methods: [B][H][d_v][d_k] row-major.  For
  * Q-Delta that is S itself; for QED it is S^T (QED's K x V state transposed), so
@@ -43,6 +51,8 @@ typedef struct {
     int B, T, H, dk, dv;
     const double *q, *k, *v, *alpha, *beta, *lam;   /* Q-Delta gates */
     const double *g, *bgate, *w, *lam_h;            /* QED gates */
+    int variant;                                     /* QED arm: 0 full, 1 nogate, 2 nogate-noproj, 3 rand */
+    const double *z;                                 /* rand arm: z_h [H][dk] */
     const double *S0;
     double *o, *S_final;
     int method;          /* 0 = Q-Delta, 1 = QED */
@@ -121,10 +131,16 @@ static int qed_stream(const job_t *J, int b, int h)
             double *Sc = S + (size_t)c * V;
             for (int j = 0; j < V; ++j) Sc[j] *= dc;
         }
+        /* the new term's input: b*q (full), q (nogate, nogate-noproj), b*z_h (rand) */
+        const double *zh = J->variant == 3 ? J->z + (size_t)h * K : NULL;
         double ku = 0.0;
-        for (int c = 0; c < K; ++c) { u[c] = bt[c] * qt[c]; ku += kt[c] * u[c]; }  /* u = b*q, k^T u */
         for (int c = 0; c < K; ++c) {
-            const double d = u[c] - kt[c] * ku;                            /* d = u - k (k^T u) */
+            const double x = zh ? zh[c] : qt[c];
+            u[c] = (J->variant == 1 || J->variant == 2) ? x : bt[c] * x;
+            ku += kt[c] * u[c];                                            /* k^T u */
+        }
+        for (int c = 0; c < K; ++c) {
+            const double d = J->variant == 2 ? u[c] : u[c] - kt[c] * ku;   /* d = u - k (k^T u) */
             a[c] = bt[c] * kt[c] + lam_h * d;                              /* a = b*k + lambda_h d */
         }
         for (int j = 0; j < V; ++j) {                                      /* r = w*v - Sbar^T a */
@@ -219,6 +235,35 @@ int oracle_qed_fwd(int B, int T, int H, int dk, int dv,
     J.q = q; J.k = k; J.v = v; J.g = g; J.bgate = b; J.w = w; J.lam_h = lam_h;
     J.S0 = S0; J.o = o; J.S_final = S_final; J.method = 1;
     return run(&J, nthreads);
+}
+
+/* QED forward for one of the ablation arms (variant 0 full, 1 nogate,
+ * 2 nogate-noproj, 3 rand with z_h [H][dk]).  Variant 0 is oracle_qed_fwd. */
+int oracle_qed_fwd_variant(int B, int T, int H, int dk, int dv,
+                           const double *q, const double *k, const double *v,
+                           const double *g, const double *b, const double *w, const double *lam_h,
+                           int variant, const double *z, const double *S0, double *o, double *S_final,
+                           int nthreads)
+{
+    if (variant < 0 || variant > 3 || (variant == 3 && !z)) return 2;
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.B = B; J.T = T; J.H = H; J.dk = dk; J.dv = dv;
+    J.q = q; J.k = k; J.v = v; J.g = g; J.bgate = b; J.w = w; J.lam_h = lam_h;
+    J.variant = variant; J.z = z;
+    J.S0 = S0; J.o = o; J.S_final = S_final; J.method = 1;
+    return run(&J, nthreads);
+}
+
+/* One QED decode step for N sequences x H heads: S [N][H][dv][dk] (QED's state
+ * transposed) updated in place, tokens [N][H][d], g, b [N][H][dk], w [N][H][dv],
+ * lambda_h [H], o [N][H][dv]; the T = 1 case of the forward. */
+int oracle_qed_step(int N, int H, int dk, int dv, double *S,
+                    const double *q, const double *k, const double *v,
+                    const double *g, const double *b, const double *w, const double *lam_h,
+                    int variant, const double *z, double *o, int nthreads)
+{
+    return oracle_qed_fwd_variant(N, 1, H, dk, dv, q, k, v, g, b, w, lam_h, variant, z, S, o, S, nthreads);
 }
 
 /* One Q-Delta decode step for N sequences x H heads: S [N][H][dv][dk] updated in

@@ -132,3 +132,68 @@ def test_oracle_passes_qed_pins():
                                   "lambda_on_base"])
 def test_qed_mutant_rejected(kind):
     assert not qed_pins_hold(_qed_mutant(kind))
+
+
+# the QED ablation arms (QED notes, sec. 3.2, Table 1): new erase term t added to b*k
+_ARM_2D = {"nogate": (1.52, 3.312), "nogate_noproj": (1.28, 3.168), "rand": (1.70, 3.42)}
+
+
+def oracle_qed_arm_step(arm):
+    def step(Sbar, q, k, b, w, v, lam, z):
+        K, V = Sbar.shape
+        sh = lambda x: np.asarray(x, dtype=np.float64).reshape(1, 1, 1, -1)
+        o, S = oracle.qed_fwd_variant(sh(q), sh(k), sh(v), sh(np.zeros(K)), sh(b), sh(w), np.array([lam]), arm,
+                                      np.asarray(z, dtype=np.float64).reshape(1, K), Sbar.T.reshape(1, 1, V, K))
+        return S[0, 0].T, o[0, 0, 0]
+    return step
+
+
+def _qed_arm_mutant(arm, kind):
+    def step(Sbar, q, k, b, w, v, lam, z):
+        P = lambda u: u - k * (k @ u)
+        t = {"nogate": P(q), "nogate_noproj": q, "rand": P(b * z)}[arm]
+        if kind == "gate_kept":
+            t = P(b * q) if arm != "rand" else P(b * q)
+        elif kind == "projection_kept":
+            t = P(q) if arm == "nogate_noproj" else t
+        elif kind == "rand_ungated":
+            t = P(z) if arm == "rand" else t
+        a = b * k + lam * t
+        r = w * v - Sbar.T @ a
+        S = Sbar + np.outer(k, r)
+        return S, S.T @ q
+    return step
+
+
+def qed_arm_pins_hold(arm, step):
+    """The arm's hand-derived values on the sec. 2.4 example, and Eqs. 11-12 with
+    the arm's own new term."""
+    S1, o1 = _ARM_2D[arm]
+    S, o = step(np.array([[2.0], [3.0]]), np.array([0.6, 0.8]), np.array([1.0, 0.0]), np.array([0.5, 0.5]),
+                np.ones(1), np.ones(1), 0.2, np.array([0.0, 1.0]))
+    if abs(o - o1) > 1e-12 or abs(S[0, 0] - S1) > 1e-12:
+        return False
+    K, V = 6, 4
+    for _ in range(3):
+        q, k, z = _unit(rng.standard_normal(K)), _unit(rng.standard_normal(K)), _unit(rng.standard_normal(K))
+        b, w = rng.uniform(0.1, 0.9, K), rng.uniform(0.1, 0.9, V)
+        v, Sbar, lam = rng.standard_normal(V), rng.standard_normal((K, V)), 0.45
+        Sa, oa = step(Sbar, q, k, b, w, v, lam, z)
+        Sg, og = step(Sbar, q, k, b, w, v, 0.0, z)
+        P = lambda u: u - k * (k @ u)
+        t = {"nogate": P(q), "nogate_noproj": q, "rand": P(b * z)}[arm]
+        if not np.allclose(Sa - Sg, -lam * np.outer(k, Sbar.T @ t), atol=1e-10):
+            return False
+    return True
+
+
+@pytest.mark.parametrize("arm", ["nogate", "nogate_noproj", "rand"])
+def test_oracle_passes_qed_arm_pins(arm):
+    assert qed_arm_pins_hold(arm, oracle_qed_arm_step(arm))
+
+
+@pytest.mark.parametrize("arm,kind", [("nogate", "gate_kept"), ("nogate_noproj", "projection_kept"),
+                                      ("nogate_noproj", "gate_kept"), ("rand", "gate_kept"),
+                                      ("rand", "rand_ungated")])
+def test_qed_arm_mutant_rejected(arm, kind):
+    assert not qed_arm_pins_hold(arm, _qed_arm_mutant(arm, kind))

@@ -173,6 +173,127 @@ def test_qed_decay_only():
     np.testing.assert_allclose(S[0, 0], S0[0, 0] * np.exp(g.sum(axis=1))[0, 0][None, :], atol=1e-14)
 
 
+# ------------------------------------------ QED ablation arms and decode (page 3)
+
+def _qed_variant_step(k, q, b, S_prev_KxV, w, v, lam_h, variant, z=None, g=None):
+    """One oracle step of a QED ablation arm from S0 = S_prev. Returns (S_KxV, o)."""
+    K, V = S_prev_KxV.shape
+    sh = lambda x: np.asarray(x, dtype=np.float64).reshape(1, 1, 1, -1)
+    g = np.zeros(K) if g is None else g
+    S0 = S_prev_KxV.T.reshape(1, 1, V, K)
+    zz = None if z is None else np.asarray(z, dtype=np.float64).reshape(1, K)
+    o, S = oracle.qed_fwd_variant(sh(q), sh(k), sh(v), sh(g), sh(b), sh(w), np.array([lam_h]), variant, zz, S0)
+    return S[0, 0].T, o[0, 0, 0]
+
+
+@pytest.mark.parametrize("variant,z,S_first,o", [
+    # the new erase term of each arm (QED notes, sec. 3.2, Table 1) on the sec. 2.4
+    # example, k=(1,0), q=(0.6,0.8), b=(0.5,0.5), Sbar=(2,3), w*v=1, lambda=0.2:
+    #   full:          d = P(b*q) = (0,0.4),  Sbar^T d = 1.2,  S_1 = 2 - 0.2*1.2 = 1.76
+    #   nogate:        d = P(q)   = (0,0.8),  Sbar^T d = 2.4,  S_1 = 2 - 0.48     = 1.52
+    #   nogate-noproj: a = b*k + 0.2 q = (0.62,0.16), r = 1 - (1.24+0.48) = -0.72,
+    #                  S_1 = 2 - 0.72 = 1.28
+    #   rand, z=(0,1): d = P(b*z) = (0,0.5),  Sbar^T d = 1.5,  S_1 = 2 - 0.3      = 1.70
+    # and o = 0.6 S_1 + 0.8 * 3 (the second coordinate never changes)
+    ("full", None, 1.76, 3.456),
+    ("nogate", None, 1.52, 3.312),
+    ("nogate_noproj", None, 1.28, 3.168),
+    ("rand", [0.0, 1.0], 1.70, 3.42),
+])
+def test_qed_ablation_arms_on_the_2d_example(variant, z, S_first, o):
+    S, out = _qed_variant_step([1.0, 0.0], [0.6, 0.8], [0.5, 0.5], np.array([[2.0], [3.0]]), [1.0], [1.0],
+                               0.2, variant, z)
+    np.testing.assert_allclose(S.ravel(), [S_first, 3.0], atol=1e-14)
+    assert abs(out - o) < 1e-14
+    assert abs(out - (0.6 * S_first + 2.4)) < 1e-14
+
+
+@pytest.mark.parametrize("variant", ["full", "nogate", "nogate_noproj", "rand"])
+def test_qed_ablation_arms_difference_identity(variant):
+    """QED notes, Eqs. 11-12 hold for every arm with its own new term t
+    (S_arm - S_GDN2 = -lambda k (Sbar^T t)^T, o_arm - o_GDN2 = -lambda rho Sbar^T t),
+    and the projected arms keep the erase factor's eigenvalue 1 - (b*k)^T k."""
+    K, V = 6, 5
+    k = _unit(rng.standard_normal(K))
+    q = _unit(rng.standard_normal(K))
+    z = _unit(rng.standard_normal(K))
+    b = rng.uniform(0.05, 0.95, K)
+    w = rng.uniform(0.05, 0.95, V)
+    v = rng.standard_normal(V)
+    g = -rng.uniform(0.0, 0.5, K)
+    S_prev = rng.standard_normal((K, V))
+    lam = 0.41
+    S_a, o_a = _qed_variant_step(k, q, b, S_prev, w, v, lam, variant, z, g)
+    S_g, o_g = _qed_variant_step(k, q, b, S_prev, w, v, 0.0, "full", None, g)
+    P = lambda u: u - k * np.dot(k, u)
+    t = {"full": P(b * q), "nogate": P(q), "nogate_noproj": q, "rand": P(b * z)}[variant]
+    Sbar = np.exp(g)[:, None] * S_prev
+    np.testing.assert_allclose(S_a - S_g, -lam * np.outer(k, Sbar.T @ t), atol=1e-13)
+    np.testing.assert_allclose(o_a - o_g, -lam * np.dot(q, k) * (Sbar.T @ t), atol=1e-13)
+    # erase factor M = I - k a^T read off with v = 0, S0 = I, g = 0
+    M, _ = _qed_variant_step(k, q, b, np.eye(K), np.ones(K), np.zeros(K), lam, variant, z)
+    ev = np.sort(np.linalg.eigvals(M).real)
+    shift = 0.0 if variant != "nogate_noproj" else lam * np.dot(k, q)
+    expect = np.sort(np.r_[np.ones(K - 1), 1.0 - np.sum(b * k * k) - shift])
+    np.testing.assert_allclose(ev, expect, atol=1e-10)
+
+
+def test_qed_ablation_arms_coincide_where_they_should():
+    """b = 1 makes full and nogate the same arm; q orthogonal to k makes nogate and
+    nogate-noproj the same; z_h equal to every token's q makes rand and full the same."""
+    B, T, H, K, V = 1, 12, 2, 6, 4
+    q = _unit(rng.standard_normal((B, T, H, K)))
+    k = _unit(rng.standard_normal((B, T, H, K)))
+    v = rng.standard_normal((B, T, H, V))
+    g = -rng.uniform(0.0, 0.2, (B, T, H, K))
+    b = rng.uniform(0.05, 0.95, (B, T, H, K))
+    w = rng.uniform(0.05, 0.95, (B, T, H, V))
+    lam = np.array([0.3, 0.9])
+    S0 = rng.standard_normal((B, H, V, K)) * 0.3
+    ones = np.ones_like(b)
+    o1, S1 = oracle.qed_fwd_variant(q, k, v, g, ones, w, lam, "full", None, S0)
+    o2, S2 = oracle.qed_fwd_variant(q, k, v, g, ones, w, lam, "nogate", None, S0)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(S1, S2)
+    q_perp = _unit(q - k * np.sum(k * q, axis=-1, keepdims=True))
+    o1, S1 = oracle.qed_fwd_variant(q_perp, k, v, g, b, w, lam, "nogate", None, S0)
+    o2, S2 = oracle.qed_fwd_variant(q_perp, k, v, g, b, w, lam, "nogate_noproj", None, S0)
+    np.testing.assert_allclose(o1, o2, atol=1e-12)
+    np.testing.assert_allclose(S1, S2, atol=1e-12)
+    zh = _unit(rng.standard_normal((H, K)))
+    q_const = np.broadcast_to(zh[None, None], (B, T, H, K)).copy()
+    o1, S1 = oracle.qed_fwd_variant(q_const, k, v, g, b, w, lam, "full", None, S0)
+    o2, S2 = oracle.qed_fwd_variant(q_const, k, v, g, b, w, lam, "rand", zh, S0)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(S1, S2)
+    # the full arm through the variant entry point is the QED forward itself
+    o1, S1 = oracle.qed_fwd_variant(q, k, v, g, b, w, lam, "full", None, S0)
+    o2, S2 = oracle.qed_fwd(q, k, v, g, b, w, lam, S0)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(S1, S2)
+
+
+@pytest.mark.parametrize("variant", ["full", "nogate_noproj", "rand"])
+def test_qed_step_sequence_equals_forward(variant):
+    """T decode steps carry the state exactly as one forward over the T tokens."""
+    N, T, H, K, V = 2, 5, 3, 6, 4
+    q = _unit(rng.standard_normal((N, T, H, K)))
+    k = _unit(rng.standard_normal((N, T, H, K)))
+    v = rng.standard_normal((N, T, H, V))
+    g = -rng.uniform(0.0, 0.2, (N, T, H, K))
+    b = rng.uniform(0.05, 0.95, (N, T, H, K))
+    w = rng.uniform(0.05, 0.95, (N, T, H, V))
+    lam = rng.uniform(0.0, 1.0, H)
+    z = _unit(rng.standard_normal((H, K)))
+    S0 = rng.standard_normal((N, H, V, K)) * 0.3
+    o_f, S_f = oracle.qed_fwd_variant(q, k, v, g, b, w, lam, variant, z, S0)
+    S = S0.copy()
+    for t in range(T):
+        o_t = oracle.qed_step(S, q[:, t], k[:, t], v[:, t], g[:, t], b[:, t], w[:, t], lam, variant, z)
+        np.testing.assert_array_equal(o_t, o_f[:, t])
+    np.testing.assert_array_equal(S, S_f)
+
+
 # ------------------------------------------------------------ Q-Delta (page 1)
 
 def test_deltanet_special_case():
