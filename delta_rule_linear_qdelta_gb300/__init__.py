@@ -6,7 +6,8 @@ calls the library on the current CUDA stream.  Every step of the computation
 runs in the library's CUDA kernels; there is no CPU path.  If the shared
 library is missing this module raises instead of computing anything.
 
-Functions keep the C names: qdelta_fwd, qed_fwd, qdelta_step, qdelta_fwd_static_scratch,
+Functions keep the C names: qdelta_fwd, qed_fwd (with its ablation arms, the C
+qed_fwd_variant), qdelta_step, qed_step, qdelta_fwd_static_scratch,
 qdelta_workspace_bytes, qed_workspace_bytes, qd_device_status, qd_last_error.
 """
 from __future__ import annotations
@@ -23,8 +24,10 @@ QD_OK, QD_ERR_ARG, QD_ERR_UNSUPPORTED, QD_ERR_CUDA, QD_ERR_TIMEOUT, QD_ERR_WORKS
 QD_F32, QD_BF16 = 0, 1
 STATUS_NAMES = {0: "QD_OK", 1: "QD_ERR_ARG", 2: "QD_ERR_UNSUPPORTED", 3: "QD_ERR_CUDA",
                 4: "QD_ERR_TIMEOUT", 5: "QD_ERR_WORKSPACE"}
-EXPORTS = ("qdelta_fwd", "qdelta_workspace_bytes", "qed_fwd", "qed_workspace_bytes", "qdelta_step",
-           "qdelta_fwd_static_scratch", "qd_device_status", "qd_last_error", "qd_last_launch_count")
+EXPORTS = ("qdelta_fwd", "qdelta_workspace_bytes", "qed_fwd", "qed_fwd_variant", "qed_workspace_bytes",
+           "qdelta_step", "qed_step", "qdelta_fwd_static_scratch", "qd_device_status", "qd_last_error",
+           "qd_last_launch_count")
+QED_VARIANTS = {"full": 0, "nogate": 1, "nogate_noproj": 2, "rand": 3}
 
 
 class QDError(RuntimeError):
@@ -50,11 +53,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qdelta_fwd_static_scratch.argtypes = [P] * 9 + [I] * 7 + [P]
     lib.qed_fwd.argtypes = [P] * 10 + [I] * 7 + [P, Z, P]
     lib.qdelta_step.argtypes = [P] * 8 + [I] * 5 + [P]
+    lib.qed_fwd_variant.argtypes = [P] * 10 + [I] * 8 + [P, P, Z, P]
+    lib.qed_step.argtypes = [P] * 9 + [I] * 6 + [P, P]
     lib.qdelta_workspace_bytes.argtypes = [I] * 7
     lib.qed_workspace_bytes.argtypes = [I] * 7
     lib.qd_device_status.argtypes = [P]
     for f in (lib.qdelta_fwd, lib.qed_fwd, lib.qdelta_step, lib.qdelta_fwd_static_scratch, lib.qd_device_status,
-              lib.qd_last_launch_count):
+              lib.qd_last_launch_count, lib.qed_fwd_variant, lib.qed_step):
         f.restype = I
     lib.qdelta_workspace_bytes.restype = Z
     lib.qed_workspace_bytes.restype = Z
@@ -190,9 +195,10 @@ def qdelta_fwd_static_scratch(q, k, v, alpha, beta, lam, S0=None, *, o=None, S_f
 
 
 def qed_fwd(q, k, v, g, b, w, lam_h, S0=None, *, o=None, S_final=None, return_final=True, chunk=64,
-            workspace=None, stream=None):
+            workspace=None, stream=None, variant="full", z=None):
     """Chunked QED forward.  q, k, g, b [B,T,H,dk]; v, w [B,T,H,dv]; lam_h [H] fp32;
-    S0 [B,H,dv,dk] fp32 (QED's K x V state transposed) or None.  Returns (o, S_final)."""
+    S0 [B,H,dv,dk] fp32 (QED's K x V state transposed) or None.  variant: the ablation
+    arm (full, nogate, nogate_noproj, rand; rand needs z [H,dk] fp32).  Returns (o, S_final)."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     dt = q.dtype
@@ -207,13 +213,38 @@ def qed_fwd(q, k, v, g, b, w, lam_h, S0=None, *, o=None, S_final=None, return_fi
     if S_final is None and return_final:
         S_final = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
     _need(S_final, "S_final", torch.float32, (B, H, dv, dk), optional=True)
+    vid = QED_VARIANTS[variant]
+    _need(z, "z", torch.float32, (H, dk), optional=vid != QED_VARIANTS["rand"])
     code = _dtype_code(q)
     workspace, wsb = _workspace(qed_workspace_bytes(B, T, H, dk, dv, chunk, code), workspace, q.device)
-    st = load_library().qed_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(w), _ptr(lam_h), _ptr(S0),
-                                _ptr(o), _ptr(S_final), B, T, H, dk, dv, chunk, code, _ptr(workspace), wsb,
-                                _stream(stream, q.device))
-    _check(st, "qed_fwd")
+    st = load_library().qed_fwd_variant(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(w), _ptr(lam_h),
+                                        _ptr(S0), _ptr(o), _ptr(S_final), B, T, H, dk, dv, chunk, code, vid,
+                                        _ptr(z), _ptr(workspace), wsb, _stream(stream, q.device))
+    _check(st, "qed_fwd_variant")
     return o, S_final
+
+
+def qed_step(S, q, k, v, g, b, w, lam_h, *, o=None, stream=None, variant="full", z=None):
+    """One QED decode step, S [N,H,dv,dk] fp32 (QED's state transposed) updated in place;
+    q, k, g, b [N,H,dk]; v, w [N,H,dv]; lam_h [H] fp32; variant / z as in qed_fwd.
+    Returns o [N,H,dv]."""
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    _need(S, "S", torch.float32, (N, H, dv, dk))
+    for name, t, shp in (("q", q, (N, H, dk)), ("k", k, (N, H, dk)), ("g", g, (N, H, dk)), ("b", b, (N, H, dk)),
+                         ("v", v, (N, H, dv)), ("w", w, (N, H, dv))):
+        _need(t, name, dt, shp)
+    _need(lam_h, "lam_h", torch.float32, (H,))
+    vid = QED_VARIANTS[variant]
+    _need(z, "z", torch.float32, (H, dk), optional=vid != QED_VARIANTS["rand"])
+    if o is None:
+        o = torch.empty((N, H, dv), dtype=dt, device=q.device)
+    _need(o, "o", dt, (N, H, dv))
+    st = load_library().qed_step(_ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(w), _ptr(lam_h),
+                                 _ptr(o), N, H, dk, dv, _dtype_code(q), vid, _ptr(z), _stream(stream, q.device))
+    _check(st, "qed_step")
+    return o
 
 
 def qdelta_step(S, q, k, v, alpha, beta, lam, *, o=None, stream=None):

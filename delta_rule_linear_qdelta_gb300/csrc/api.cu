@@ -109,22 +109,27 @@ qd_status qdelta_fwd(const void *q, const void *k, const void *v, const void *al
     return QD_OK;
 }
 
-qd_status qed_fwd(const void *q, const void *k, const void *v, const void *g, const void *b, const void *w,
-                  const float *lam_h, const float *S0, void *o, float *S_final, int B, int T, int H, int dk,
-                  int dv, int chunk, qd_dtype dtype, void *workspace, size_t workspace_bytes,
-                  cudaStream_t stream) {
+qd_status qed_fwd_variant(const void *q, const void *k, const void *v, const void *g, const void *b,
+                          const void *w, const float *lam_h, const float *S0, void *o, float *S_final, int B,
+                          int T, int H, int dk, int dv, int chunk, qd_dtype dtype, qd_qed_variant variant,
+                          const float *z_h, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     g_err[0] = 0;
+    if (variant < QD_QED_FULL || variant > QD_QED_RAND)
+        return fail(QD_ERR_ARG, "qed_fwd_variant: unknown variant %d", (int)variant);
     const void *req[] = {q, k, v, g, b, w, lam_h, o};
-    const void *opt[] = {S0, S_final, workspace};
-    qd_status st = check_fwd("qed_fwd", req, 8, opt, 3, B, T, H, dk, dv, chunk, dtype);
+    const void *opt[] = {S0, S_final, workspace, z_h};
+    qd_status st = check_fwd("qed_fwd", req, 8, opt, 4, B, T, H, dk, dv, chunk, dtype);
     if (st != QD_OK) return st;
+    if (variant == QD_QED_RAND && !z_h && B > 0 && H > 0 && T > 0)
+        return fail(QD_ERR_ARG, "qed_fwd_variant: the rand arm needs z_h [H][dk]");
     const size_t need = qed_workspace_bytes(B, T, H, dk, dv, chunk, dtype);
     if (need && (!workspace || workspace_bytes < need))
         return fail(QD_ERR_WORKSPACE, "qed_fwd: workspace of %zu bytes needed, %zu given", need, workspace_bytes);
     int n = 0;
     if (B == 0 || H == 0) { g_launches = 0; return QD_OK; }
     if (T == 0) { g_launches = 0; return empty_sequence(S0, S_final, B, H, dk, dv, stream); }
-    qd::QedArgs a{q, k, v, g, b, w, lam_h, S0, o, S_final, B, T, H, dk, dv, workspace, workspace_bytes};
+    qd::QedArgs a{q, k, v, g, b, w, lam_h, S0, o, S_final, B, T, H, dk, dv, workspace, workspace_bytes,
+                  (int)variant, z_h};
     cudaError_t e;
     if (qd::qed_tc_supported(a, dtype)) {
         const int G = qd::qed_segments(B, T, H, dk, dv, dtype);
@@ -133,6 +138,43 @@ qd_status qed_fwd(const void *q, const void *k, const void *v, const void *g, co
         e = qd::launch_qed_chunk_simt(a, dtype, stream, &n);
     }
     if (e != cudaSuccess) return cuda_fail(e, "qed_fwd launch");
+    g_launches = n;
+    return QD_OK;
+}
+
+qd_status qed_fwd(const void *q, const void *k, const void *v, const void *g, const void *b, const void *w,
+                  const float *lam_h, const float *S0, void *o, float *S_final, int B, int T, int H, int dk,
+                  int dv, int chunk, qd_dtype dtype, void *workspace, size_t workspace_bytes,
+                  cudaStream_t stream) {
+    return qed_fwd_variant(q, k, v, g, b, w, lam_h, S0, o, S_final, B, T, H, dk, dv, chunk, dtype, QD_QED_FULL,
+                           nullptr, workspace, workspace_bytes, stream);
+}
+
+qd_status qed_step(float *S, const void *q, const void *k, const void *v, const void *g, const void *b,
+                   const void *w, const float *lam_h, void *o, int N, int H, int dk, int dv, qd_dtype dtype,
+                   qd_qed_variant variant, const float *z_h, cudaStream_t stream) {
+    g_err[0] = 0;
+    if (N < 0 || H < 0) return fail(QD_ERR_ARG, "qed_step: negative size N=%d H=%d", N, H);
+    if (dtype != QD_F32 && dtype != QD_BF16) return fail(QD_ERR_UNSUPPORTED, "qed_step: unknown dtype");
+    if (variant < QD_QED_FULL || variant > QD_QED_RAND)
+        return fail(QD_ERR_ARG, "qed_step: unknown variant %d", (int)variant);
+    if (!head_dim_ok(dk) || !head_dim_ok(dv))
+        return fail(QD_ERR_UNSUPPORTED, "qed_step: head dims dk=%d dv=%d not in {16,32,64,128}", dk, dv);
+    if ((double)N * H > 2147483647.0) return fail(QD_ERR_ARG, "qed_step: N*H exceeds the grid limit");
+    const bool empty = (N == 0 || H == 0);
+    const void *req[] = {S, q, k, v, g, b, w, lam_h, o};
+    for (int i = 0; i < 9; ++i) {
+        if (!req[i] && !empty) return fail(QD_ERR_ARG, "qed_step: required pointer argument #%d is NULL", i);
+        if (!aligned16(req[i])) return fail(QD_ERR_ARG, "qed_step: pointer argument #%d not 16-byte aligned", i);
+    }
+    if (!aligned16(z_h)) return fail(QD_ERR_ARG, "qed_step: z_h not 16-byte aligned");
+    if (variant == QD_QED_RAND && !z_h && !empty) return fail(QD_ERR_ARG, "qed_step: the rand arm needs z_h [H][dk]");
+    g_launches = 0;
+    if (empty) return QD_OK;
+    int n = 0;
+    qd::QedStepArgs a{S, q, k, v, g, b, w, lam_h, o, N, H, dk, dv, (int)variant, z_h};
+    cudaError_t e = qd::launch_qed_step(a, dtype, stream, &n);
+    if (e != cudaSuccess) return cuda_fail(e, "qed_step launch");
     g_launches = n;
     return QD_OK;
 }

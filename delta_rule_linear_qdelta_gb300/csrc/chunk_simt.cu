@@ -220,6 +220,9 @@ __global__ void __launch_bounds__(kNT) qed_chunk_simt_kernel(QedArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const float lam_h = a.lam_h[h];
     const size_t s_base = (size_t)bh * dv * DK + (size_t)d0 * DK;
+    const bool gate = a.variant == kQedFull || a.variant == kQedRand;   // the new term keeps b
+    const bool proj = a.variant != kQedNogateNoproj;                    // ... and the projection
+    const float *zh = a.variant == kQedRand ? a.z + (size_t)h * DK : nullptr;
 
     for (int idx = tid; idx < DVT * DK; idx += kNT) {
         const int d = idx / DK, j = idx % DK;
@@ -246,15 +249,22 @@ __global__ void __launch_bounds__(kNT) qed_chunk_simt_kernel(QedArgs a) {
         __syncthreads();
         if (tid < DK)
             for (int t = 1; t < C; ++t) Gs[t * LK + tid] += Gs[(t - 1) * LK + tid];
-        // erase vector a_t = b*k + lam_h (b*q - k (k . b*q)); one warp per token
+        // erase vector a_t = b*k + lam_h P(u) (full: u = b*q), one warp per token; the
+        // ablation arms take u = q (nogate), u = q without P (nogate-noproj), u = b*z_h (rand)
         for (int t = warp; t < C; t += kNT / 32) {
+            auto u_of = [&](int j) {
+                const float x = zh ? zh[j] : Qs[t * LK + j];
+                return gate ? As[t * LK + j] * x : x;
+            };
             float ku = 0.f;
-            for (int j = lane; j < DK; j += 32) ku += Ks[t * LK + j] * As[t * LK + j] * Qs[t * LK + j];
+            if (proj) {
+                for (int j = lane; j < DK; j += 32) ku += Ks[t * LK + j] * u_of(j);
 #pragma unroll
-            for (int off = 16; off; off >>= 1) ku += __shfl_xor_sync(0xffffffffu, ku, off);
+                for (int off = 16; off; off >>= 1) ku += __shfl_xor_sync(0xffffffffu, ku, off);
+            }
             for (int j = lane; j < DK; j += 32) {
                 const float bj = As[t * LK + j], kj = Ks[t * LK + j];
-                const float u = bj * Qs[t * LK + j];
+                const float u = u_of(j);
                 As[t * LK + j] = bj * kj + lam_h * (u - kj * ku);
             }
         }

@@ -5,7 +5,9 @@
 // Recurrence ("The Query Knows What to Forget", Sec. 2.1-2.2: GDN-2 update of
 // Eqs. 4/8, erase vector of Eq. 6), with the state kept as S^ = S^T ([dv][dk]):
 //   S^_t = S^_{t-1} D_t (I - a_t k_t^T) + (w_t * v_t) k_t^T,   o_t = S^_t q_t,
-//   D_t = Diag(e^{g_t}),  a_t = b_t*k_t + lam_h (u_t - k_t (k_t^T u_t)),  u_t = b_t*q_t.
+//   D_t = Diag(e^{g_t}),  a_t = b_t*k_t + lam_h (u_t - k_t (k_t^T u_t)),  u_t = b_t*q_t
+//   (the ablation arms of Table 1 take u_t = q_t, u_t = q_t without the projection,
+//   or u_t = b_t*z_h; see qd_internal.cuh).
 // Per chunk, with the in-chunk cumulative log-decay G_t = sum_{j<=t} g_j (a vector
 // over the dk channels, anchored at the chunk start):
 //   Ae = A*e^G, Qe = Q*e^G, Ke = K*e^-G, Kd = K*e^{G_C - G}   (elementwise, per channel)
@@ -65,7 +67,9 @@ struct QedTcParams {
     const float *lam_h, *S0;
     float *S_final;
     int B, T, H;
-    int flags;   // kTcNoV | kTcS0Identity | kTcNoO (segment-scan passes)
+    int flags;      // kTcNoV | kTcS0Identity | kTcNoO (segment-scan passes)
+    int variant;    // kQed* ablation arm
+    const float *z; // [H][128] for kQedRand
 };
 
 struct QedMaps {
@@ -94,6 +98,10 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
     const bool producer = (tid == 0), issuer = (tid == 32);
     const float lam_h = p.lam_h[h];
     const int d_row = 32 * q4 + lane;
+    // the erase vector's new term (ablation arm): b gate kept, projection kept, z_h in place of q
+    const bool gate = p.variant == kQedFull || p.variant == kQedRand;
+    const bool proj = p.variant != kQedNogateNoproj;
+    const float *zrow = p.variant == kQedRand ? p.z + (size_t)h * kD : nullptr;
     // flags of the segment-scan passes, read through opaque() inside the chunk loop
     const uint32_t flags = (uint32_t)p.flags;
     const bool s0_id = flags & kTcS0Identity;
@@ -217,7 +225,9 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
         __syncthreads();
         if (abort_flag) break;
 
-        // (2) k_t . (b_t * q_t) per token (one warp per token) and W*V in place of V
+        // (2) k_t . u_t per token (one warp per token; u = b*q, or the ablation arm's
+        // q, b*z_h) and W*V in place of V
+        if (proj)
         for (int t = warp; t < kC; t += kThreads / 32) {
             const int j = 4 * lane;
             const uint32_t o8 = tile_off(t, j, 8192), o16 = tile_off(t, j, 16384);
@@ -231,9 +241,11 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const float2 kf = __bfloat1622float2(k2[e]), bf2 = __bfloat1622float2(b2[e]);
-                const float2 qf = __bfloat1622float2(q2[e]);
-                acc = fmaf(kf.x * bf2.x, qf.x, acc);
-                acc = fmaf(kf.y * bf2.y, qf.y, acc);
+                float2 xf = __bfloat1622float2(q2[e]);
+                if (zrow) xf = make_float2(zrow[j + 2 * e], zrow[j + 2 * e + 1]);
+                const float u0 = gate ? bf2.x * xf.x : xf.x, u1 = gate ? bf2.y * xf.y : xf.y;
+                acc = fmaf(kf.x, u0, acc);
+                acc = fmaf(kf.y, u1, acc);
             }
 #pragma unroll
             for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -264,6 +276,7 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
         {
             const int j = tid & 127, half = tid >> 7;
             float G = half ? g_ps[0][j] : 0.f;
+            const float zj = zrow ? zrow[j] : 0.f;
             for (int t = 32 * half; t < 32 * half + 32; ++t) {
                 const uint32_t o8 = tile_off(t, j, 8192), o16 = tile_off(t, j, 16384);
                 G += bf(*reinterpret_cast<const __nv_bfloat16 *>(sm + OFF_G + o8));
@@ -271,7 +284,9 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
                 const float qv = bf(*reinterpret_cast<const __nv_bfloat16 *>(sm + OFF_XQ + 8192 + o16));
                 const float kv = bf(*reinterpret_cast<const __nv_bfloat16 *>(sm + OFF_K + o8));
                 const float bv = bf(*reinterpret_cast<const __nv_bfloat16 *>(sm + OFF_BT + o8));
-                const float a = bv * kv + lam_h * (bv * qv - kv * g_ku[t]);
+                const float xv = zrow ? zj : qv;
+                const float u = gate ? bv * xv : xv;
+                const float a = bv * kv + lam_h * (proj ? u - kv * g_ku[t] : u);
                 *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_XQ + o16) = __float2bfloat16_rn(a * eG);
                 *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_XQ + 8192 + o16) = __float2bfloat16_rn(qv * eG);
                 *reinterpret_cast<__nv_bfloat16 *>(sm + OFF_K + o8) = __float2bfloat16_rn(kv * emG);
@@ -508,7 +523,7 @@ cudaError_t launch_qed_chunk_tc(const QedArgs &a, cudaStream_t s, int *nlaunch, 
     cudaError_t e = cudaFuncSetAttribute(qed_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    QedTcParams p{a.lam_h, a.S0, a.S_final, a.B, a.T, a.H, flags};
+    QedTcParams p{a.lam_h, a.S0, a.S_final, a.B, a.T, a.H, flags, a.variant, a.z};
     qed_fwd_tc_kernel<<<a.B * a.H, kThreads, kSmemBytes, s>>>(p, m);
     e = cudaGetLastError();
     if (e == cudaSuccess) *nlaunch += 1;

@@ -34,6 +34,12 @@ struct QDeltaArgs {
     size_t ws_bytes;
 };
 
+// QED ablation arms ("The Query Knows What to Forget", Table 1): the term added to
+// the base erase vector b*k, P(u) = u - k (k^T u):
+//   full lambda_h P(b*q); nogate lambda_h P(q); nogate-noproj lambda_h q;
+//   rand lambda_h P(b*z_h) with z_h [H][dk] fp32.  Values match qd_qed_variant.
+enum { kQedFull = 0, kQedNogate = 1, kQedNogateNoproj = 2, kQedRand = 3 };
+
 // Arguments of one QED forward.
 struct QedArgs {
     const void *q, *k, *v, *g, *b, *w;
@@ -43,6 +49,19 @@ struct QedArgs {
     int B, T, H, dk, dv;
     void *ws;
     size_t ws_bytes;
+    int variant;          // kQed*
+    const float *z;       // [H][dk] for kQedRand, else unused
+};
+
+// Arguments of one QED decode step.
+struct QedStepArgs {
+    float *S;
+    const void *q, *k, *v, *g, *b, *w;
+    const float *lam_h;
+    void *o;
+    int N, H, dk, dv;
+    int variant;
+    const float *z;
 };
 
 // Arguments of one decode step.
@@ -57,6 +76,7 @@ struct StepArgs {
 cudaError_t launch_qdelta_chunk_simt(const QDeltaArgs &a, int dtype, cudaStream_t s, int *nlaunch);
 cudaError_t launch_qed_chunk_simt(const QedArgs &a, int dtype, cudaStream_t s, int *nlaunch);
 cudaError_t launch_qdelta_step(const StepArgs &a, int dtype, cudaStream_t s, int *nlaunch);
+cudaError_t launch_qed_step(const QedStepArgs &a, int dtype, cudaStream_t s, int *nlaunch);
 
 // Tensor-core (tcgen05) chunked Q-Delta forward: bf16, dk = dv = 128.  flags select the
 // segment-scan passes: kTcNoV (v taken as 0, v not read), kTcS0Identity (S0 = I per

@@ -1,5 +1,5 @@
-// Decode step: one token of the gated Q-Delta recurrence per (sequence, head),
-// state updated in place.  Memory bound: the fp32 state is read once and
+// Decode steps: one token of the gated Q-Delta recurrence, or of QED, per
+// (sequence, head), state updated in place.  Memory bound: the fp32 state is read once and
 // written once; everything else is a few hundred bytes per head.
 //
 // Per state row s (length dk), with x = k + lambda q and kq = k . q
@@ -112,6 +112,108 @@ __global__ void __launch_bounds__(kStepThreads) qdelta_step_kernel(StepArgs a) {
     }
 }
 
+// QED decode step ("The Query Knows What to Forget", Eqs. 4/6/8), state S^ = S^T
+// ([dv][dk]) in place.  With eg = e^{g}, the erase vector a (or an ablation arm's),
+// ea = eg*a, eq = eg*q and kq = k . q, per state row s (a d_v index i):
+//   p = s . ea,  sq = s . eq,  r = w_i v_i - p
+//   s' = eg*s + r k,  o_i = sq + r kq            (o = S^_new q in one pass)
+// Same layout and row pipelining as the Q-Delta step above.
+template <typename TIn, int DK>
+__global__ void __launch_bounds__(kStepThreads) qed_step_kernel(QedStepArgs a) {
+    constexpr int VEC = DK >= 128 ? 4 : (DK >= 64 ? 2 : 1);
+    constexpr int LANES = DK / VEC;
+    constexpr int RPW = 32 / LANES;
+    constexpr int NW = kStepThreads / 32;
+    const int head = blockIdx.x;                // n * H + h
+    const int h = head % a.H;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int sub = lane / LANES, l = lane % LANES;
+    const int dv = a.dv;
+
+    const TIn *q = (const TIn *)a.q + (size_t)head * DK;
+    const TIn *k = (const TIn *)a.k + (size_t)head * DK;
+    const TIn *g = (const TIn *)a.g + (size_t)head * DK;
+    const TIn *bg = (const TIn *)a.b + (size_t)head * DK;
+    const TIn *v = (const TIn *)a.v + (size_t)head * dv;
+    const TIn *w = (const TIn *)a.w + (size_t)head * dv;
+    const float lam_h = a.lam_h[h];
+    const bool gate = a.variant == kQedFull || a.variant == kQedRand;
+    const bool proj = a.variant != kQedNogateNoproj;
+    const float *zh = a.variant == kQedRand ? a.z + (size_t)h * DK : nullptr;
+    TIn *o = (TIn *)a.o + (size_t)head * dv;
+    float *S = a.S + (size_t)head * dv * DK;
+
+    float qv[VEC], kv[VEC], bv[VEC], eg[VEC], u[VEC];
+    float kq = 0.f, ku = 0.f;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+        const int j = l * VEC + e;
+        qv[e] = to_f(q[j]);
+        kv[e] = to_f(k[j]);
+        bv[e] = to_f(bg[j]);
+        eg[e] = __expf(to_f(g[j]));
+        const float x = zh ? zh[j] : qv[e];
+        u[e] = gate ? bv[e] * x : x;
+        kq = fmaf(kv[e], qv[e], kq);
+        ku = fmaf(kv[e], u[e], ku);
+    }
+    kq = group_sum<LANES>(kq);
+    ku = proj ? group_sum<LANES>(ku) : 0.f;
+    float ea[VEC], eq[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+        ea[e] = eg[e] * (bv[e] * kv[e] + lam_h * (u[e] - kv[e] * ku));
+        eq[e] = eg[e] * qv[e];
+    }
+
+    const int row_step = NW * RPW;
+    for (int base = warp * RPW; base < dv; base += row_step * kUnroll) {   // warp-uniform
+        const int r0 = base + sub;
+        float s[kUnroll][VEC] = {};
+        float wv[kUnroll] = {};
+#pragma unroll
+        for (int uu = 0; uu < kUnroll; ++uu) {
+            const int row = r0 + uu * row_step;
+            if (row < dv) {
+                vload<VEC>(S + (size_t)row * DK + l * VEC, s[uu]);
+                wv[uu] = to_f(w[row]) * to_f(v[row]);
+            }
+        }
+#pragma unroll
+        for (int uu = 0; uu < kUnroll; ++uu) {
+            const int row = r0 + uu * row_step;
+            float p = 0.f, sq = 0.f;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                p = fmaf(s[uu][e], ea[e], p);
+                sq = fmaf(s[uu][e], eq[e], sq);
+            }
+            p = group_sum<LANES>(p);
+            sq = group_sum<LANES>(sq);
+            if (row < dv) {
+                const float r = wv[uu] - p;
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) s[uu][e] = fmaf(eg[e], s[uu][e], r * kv[e]);
+                vstore<VEC>(S + (size_t)row * DK + l * VEC, s[uu]);
+                if (l == 0) o[row] = from_f<TIn>(fmaf(r, kq, sq));
+            }
+        }
+    }
+}
+
+template <typename TIn>
+cudaError_t run_qed_step(const QedStepArgs &a, cudaStream_t s) {
+    const unsigned grid = (unsigned)((size_t)a.N * a.H);
+    switch (a.dk) {
+        case 16: qed_step_kernel<TIn, 16><<<grid, kStepThreads, 0, s>>>(a); break;
+        case 32: qed_step_kernel<TIn, 32><<<grid, kStepThreads, 0, s>>>(a); break;
+        case 64: qed_step_kernel<TIn, 64><<<grid, kStepThreads, 0, s>>>(a); break;
+        case 128: qed_step_kernel<TIn, 128><<<grid, kStepThreads, 0, s>>>(a); break;
+        default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
 template <typename TIn>
 cudaError_t run_step(const StepArgs &a, cudaStream_t s) {
     const unsigned grid = (unsigned)((size_t)a.N * a.H);
@@ -126,6 +228,12 @@ cudaError_t run_step(const StepArgs &a, cudaStream_t s) {
 }
 
 }  // namespace
+
+cudaError_t launch_qed_step(const QedStepArgs &a, int dtype, cudaStream_t s, int *nlaunch) {
+    cudaError_t e = dtype == kBF16 ? run_qed_step<__nv_bfloat16>(a, s) : run_qed_step<float>(a, s);
+    if (e == cudaSuccess) *nlaunch += 1;
+    return e;
+}
 
 cudaError_t launch_qdelta_step(const StepArgs &a, int dtype, cudaStream_t s, int *nlaunch) {
     cudaError_t e = dtype == kBF16 ? run_step<__nv_bfloat16>(a, s) : run_step<float>(a, s);

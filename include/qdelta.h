@@ -100,6 +100,41 @@ QD_API qd_status qed_fwd(const void *q, const void *k, const void *v,
                   int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype,
                   void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * qed_fwd_variant -- qed_fwd for one of the ablation arms of the QED notes
+ * ("The Query Knows What to Forget", Sec. 3.2, Table 1).  Each arm changes only
+ * the term added to the base erase vector b_t * k_t, with P(u) = u - k (k^T u):
+ *     QD_QED_FULL           lam_h P(b_t * q_t)   (qed_fwd)
+ *     QD_QED_NOGATE         lam_h P(q_t)         (b removed from the new term only)
+ *     QD_QED_NOGATE_NOPROJ  lam_h q_t            (no gate, no projection)
+ *     QD_QED_RAND           lam_h P(b_t * z_h)   (z_h: a fixed vector per head)
+ * z_h [H][dk] fp32 is required for QD_QED_RAND and ignored otherwise.  Every
+ * other argument, layout and the workspace rule are those of qed_fwd.
+ */
+typedef enum { QD_QED_FULL = 0, QD_QED_NOGATE = 1, QD_QED_NOGATE_NOPROJ = 2, QD_QED_RAND = 3 } qd_qed_variant;
+
+QD_API qd_status qed_fwd_variant(const void *q, const void *k, const void *v,
+                                 const void *g, const void *b, const void *w, const float *lam_h,
+                                 const float *S0, void *o, float *S_final,
+                                 int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype,
+                                 qd_qed_variant variant, const float *z_h,
+                                 void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * qed_step -- one decode step of QED (T = 1), state in place.  With the state
+ * stored transposed (S^ = S^T, [dv][dk]) and e = exp(g_t), per row i:
+ *     S^_i <- S^_i Diag(e) + (w_i v_i - (S^_i Diag(e)) . a_t) k_t,   o_i = S^_i q_t
+ * (the QED notes' Eqs. 4, 6, 8 for one token; a_t of the chosen arm, as in
+ * qed_fwd_variant).  Each state row is read once and written once.
+ *   S  [N][H][dv][dk] fp32, updated in place
+ *   q, k, g, b [N][H][dk]; v, w, o [N][H][dv] in the call's dtype; lam_h [H] fp32;
+ *   z_h [H][dk] fp32 (QD_QED_RAND only)
+ */
+QD_API qd_status qed_step(float *S, const void *q, const void *k, const void *v,
+                          const void *g, const void *b, const void *w, const float *lam_h, void *o,
+                          int N, int H, int dk, int dv, qd_dtype dtype,
+                          qd_qed_variant variant, const float *z_h, cudaStream_t stream);
+
 /* Bytes of device workspace qed_fwd needs for these sizes (0 if none).  As for
  * qdelta_fwd, very few (b, h) streams (at most 16) carrying a long sequence are cut
  * into segments

@@ -19,7 +19,7 @@ shapes stand in for their 340M-1.3B models and 2K-32K contexts):
   alpha  = exp(-softplus(N(mu, 0.5))), mu = -4 (alpha ~ 0.98) unless a mean alpha
            is requested, in which case mu is found by bisection on 1e6 fp64 draws
   QED:   g = -softplus(N(-5, 0.5)) per key channel; b, w = sigmoid(N(0,1));
-         lambda_h ~ U(0,1) per head
+         lambda_h ~ U(0,1) per head; the rand arm's z_h ~ N(0,1) per head, unit length
   S0     ~ N(0, s0_var) when an initial state is requested (variance, not std)
 """
 from __future__ import annotations
@@ -35,7 +35,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 # Fixed stream ids per tensor name.
 STREAMS = {
     "q": 1, "k": 2, "v": 3, "alpha": 4, "beta": 5, "lam": 6, "S0": 7,
-    "g": 8, "b": 9, "w": 10, "lam_h": 11, "alpha_mu": 12,
+    "g": 8, "b": 9, "w": 10, "lam_h": 11, "alpha_mu": 12, "z": 13,
 }
 
 _BLOCK = 1 << 22
@@ -174,9 +174,10 @@ def qed_inputs(B: int, T: int, H: int, dk: int, dv: int, seed: int, dtype: str =
     b = _sigmoid(normal(seed, STREAMS["b"], n_tok * dk)).reshape(B, T, H, dk)
     w = _sigmoid(normal(seed, STREAMS["w"], n_tok * dv)).reshape(B, T, H, dv)
     lam_h = uniform(seed, STREAMS["lam_h"], H)
+    z = _unit_rows(normal(seed, STREAMS["z"], H * dk).reshape(H, dk))
     out = {"q": round_to(q, dtype), "k": round_to(k, dtype), "v": round_to(v, dtype),
            "g": round_to(g, dtype), "b": round_to(b, dtype), "w": round_to(w, dtype),
-           "lam_h": round_to(lam_h, "f32"), "S0": None, "dtype": dtype,
+           "lam_h": round_to(lam_h, "f32"), "z": round_to(z, "f32"), "S0": None, "dtype": dtype,
            "shape": (B, T, H, dk, dv)}
     if s0_var is not None:
         s0 = normal(seed, STREAMS["S0"], B * H * dv * dk, std=math.sqrt(s0_var))
@@ -195,6 +196,21 @@ def decode_inputs(N: int, H: int, dk: int, dv: int, steps: int, seed: int, dtype
         "beta": d["beta"].reshape(steps, N, H), "lam": d["lam"].reshape(steps, N, H),
         "S0": None, "dtype": dtype, "shape": (N, H, dk, dv, steps),
     }
+    if s0_var is not None:
+        s0 = normal(seed, STREAMS["S0"], N * H * dv * dk, std=math.sqrt(s0_var))
+        out["S0"] = round_to(s0.reshape(N, H, dv, dk), "f32")
+    return out
+
+
+def qed_decode_inputs(N: int, H: int, dk: int, dv: int, steps: int, seed: int, dtype: str = "bf16",
+                      s0_var: float | None = 0.01) -> dict:
+    """Inputs of `steps` consecutive QED decode steps: q, k, g, b [steps,N,H,dk],
+    v, w [steps,N,H,dv]; lam_h [H], z [H,dk] fp32; state S0 [N,H,dv,dk] fp32."""
+    d = qed_inputs(steps, 1, N * H, dk, dv, seed, dtype)
+    out = {key: d[key].reshape(steps, N, H, -1) for key in ("q", "k", "v", "g", "b", "w")}
+    # one lambda_h / z_h per head: the first H of the N*H drawn
+    out.update({"lam_h": d["lam_h"][:H].copy(), "z": d["z"][:H].copy(), "S0": None, "dtype": dtype,
+                "shape": (N, H, dk, dv, steps)})
     if s0_var is not None:
         s0 = normal(seed, STREAMS["S0"], N * H * dv * dk, std=math.sqrt(s0_var))
         out["S0"] = round_to(s0.reshape(N, H, dv, dk), "f32")

@@ -77,3 +77,28 @@ def test_python_binding_refuses_cpu_tensors(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         qd.load_library(str(tmp_path / "nope.so"))
+
+
+def test_qed_arms_and_step_arguments_checked(lib):
+    g = ctypes.c_void_p(256)
+    # unknown arm, rand without z_h, misaligned z_h
+    st = lib.qed_fwd_variant(g, g, g, g, g, g, g, None, g, None, 1, 8, 1, 64, 64, 64, qd.QD_BF16, 7, None,
+                             None, 0, None)
+    assert st == qd.QD_ERR_ARG and "variant" in qd.qd_last_error()
+    st = lib.qed_fwd_variant(g, g, g, g, g, g, g, None, g, None, 1, 8, 1, 64, 64, 64, qd.QD_BF16,
+                             qd.QED_VARIANTS["rand"], None, None, 0, None)
+    assert st == qd.QD_ERR_ARG and "z_h" in qd.qd_last_error()
+    st = lib.qed_fwd_variant(g, g, g, g, g, g, g, None, g, None, 1, 8, 1, 64, 64, 64, qd.QD_BF16,
+                             qd.QED_VARIANTS["rand"], ctypes.c_void_p(260), None, 0, None)
+    assert st == qd.QD_ERR_ARG and "aligned" in qd.qd_last_error()
+    # the decode step: NULL gate, unknown arm, unsupported head dim; empty batch is a no-op
+    st = lib.qed_step(g, g, g, g, None, g, g, g, g, 1, 1, 64, 64, qd.QD_BF16, 0, None, None)
+    assert st == qd.QD_ERR_ARG and "NULL" in qd.qd_last_error()
+    st = lib.qed_step(g, g, g, g, g, g, g, g, g, 1, 1, 64, 64, qd.QD_BF16, 9, None, None)
+    assert st == qd.QD_ERR_ARG
+    st = lib.qed_step(g, g, g, g, g, g, g, g, g, 1, 1, 48, 64, qd.QD_BF16, 0, None, None)
+    assert st == qd.QD_ERR_UNSUPPORTED
+    st = lib.qed_step(g, g, g, g, g, g, g, g, g, 1, 1, 64, 64, qd.QD_BF16, qd.QED_VARIANTS["rand"], None, None)
+    assert st == qd.QD_ERR_ARG and "z_h" in qd.qd_last_error()
+    assert lib.qed_step(None, None, None, None, None, None, None, None, None, 0, 4, 64, 64, 1, 0, None,
+                        None) == qd.QD_OK

@@ -61,10 +61,12 @@ def run_qdelta(qd, d):
     return o.float().cpu().numpy(), S.cpu().numpy()
 
 
-def run_qed(qd, d):
+def run_qed(qd, d, variant="full"):
     dt = tdt(d)
+    z = dev(d["z"], torch.float32) if variant == "rand" else None
     o, S = qd.qed_fwd(dev(d["q"], dt), dev(d["k"], dt), dev(d["v"], dt), dev(d["g"], dt), dev(d["b"], dt),
-                      dev(d["w"], dt), dev(d["lam_h"], torch.float32), dev(d["S0"], torch.float32))
+                      dev(d["w"], dt), dev(d["lam_h"], torch.float32), dev(d["S0"], torch.float32),
+                      variant=variant, z=z)
     torch.cuda.synchronize()
     return o.float().cpu().numpy(), S.cpu().numpy()
 
@@ -277,6 +279,19 @@ def test_qed_segmented_long_sequence_all_outputs(qd):
     check(S, S_ref, "bf16", "segmented qed S")
 
 
+@pytest.mark.parametrize("variant", ["nogate", "nogate_noproj", "rand"])
+@pytest.mark.parametrize("dt,dh", [("f32", 64), ("bf16", 128)])
+def test_qed_ablation_arms_all_outputs(qd, variant, dt, dh):
+    """The QED notes' ablation arms (Table 1) on the CUDA-core path (fp32, d=64) and
+    the tensor-core path (bf16, d=128): 2 full chunks + a ragged tail, initial state."""
+    d = synth.qed_inputs(2, 150, 2, dh, dh, seed=61, dtype=dt, s0_var=0.01)
+    o, S = run_qed(qd, d, variant)
+    o_ref, S_ref = oracle.qed_fwd_variant(d["q"], d["k"], d["v"], d["g"], d["b"], d["w"], d["lam_h"], variant,
+                                          d["z"], d["S0"])
+    check(o, o_ref, dt, f"qed {variant} {dt} o")
+    check(S, S_ref, dt, f"qed {variant} {dt} S")
+
+
 def test_qed_full_size_sampled(qd):
     """B=4, H=8, T=4096, d=128 bf16; 4 streams checked."""
     name, d = synth.qed_gdn2()
@@ -361,6 +376,62 @@ def test_step_sequence_matches_forward(qd):
     torch.cuda.synchronize()
     check(o_step.cpu().numpy(), o_fwd.cpu().numpy(), "f32", "step vs fwd o")
     check(S.cpu().numpy(), S_fwd.cpu().numpy(), "f32", "step vs fwd S")
+
+
+def _qed_step_call(qd, S, d, t, dt, variant):
+    z = dev(d["z"], torch.float32) if variant == "rand" else None
+    return qd.qed_step(S, dev(d["q"][t], dt), dev(d["k"][t], dt), dev(d["v"][t], dt), dev(d["g"][t], dt),
+                       dev(d["b"][t], dt), dev(d["w"][t], dt), dev(d["lam_h"], torch.float32), variant=variant, z=z)
+
+
+@pytest.mark.parametrize("variant", ["full", "nogate", "nogate_noproj", "rand"])
+@pytest.mark.parametrize("dt,dh", [("f32", 64), ("bf16", 128), ("f32", 16)])
+def test_qed_decode_steps_all_outputs(qd, variant, dt, dh):
+    """QED decode step (the T = 1 recurrence, state in place) for every arm: 20 steps
+    from a random state, each step's output and the final state against the oracle."""
+    d = synth.qed_decode_inputs(3, 2, dh, dh, 20, seed=92, dtype=dt)
+    tt = torch.bfloat16 if dt == "bf16" else torch.float32
+    S = dev(d["S0"], torch.float32)
+    S_ref = d["S0"].astype(np.float64).copy()
+    for t in range(20):
+        o = _qed_step_call(qd, S, d, t, tt, variant)
+        o_ref = oracle.qed_step(S_ref, d["q"][t], d["k"][t], d["v"][t], d["g"][t], d["b"][t], d["w"][t],
+                                d["lam_h"], variant, d["z"])
+        check(o.float().cpu().numpy(), o_ref, dt, f"qed step {t} o")
+    check(S.cpu().numpy(), S_ref, "f32", "qed decode S")
+
+
+def test_qed_decode_64x8_30_steps(qd):
+    """64 sequences x 8 heads, 128x128 fp32 state, bf16 tokens, 30 steps in place:
+    every head against the oracle."""
+    d = synth.qed_decode_inputs(64, 8, 128, 128, 30, seed=93)
+    S = dev(d["S0"], torch.float32)
+    S_ref = d["S0"].astype(np.float64).copy()
+    for t in range(30):
+        o = _qed_step_call(qd, S, d, t, torch.bfloat16, "full")
+        o_ref = oracle.qed_step(S_ref, d["q"][t], d["k"][t], d["v"][t], d["g"][t], d["b"][t], d["w"][t],
+                                d["lam_h"], "full")
+        if t % 10 == 9:
+            check(o.float().cpu().numpy(), o_ref, "bf16", f"qed 64x8 step {t} o")
+    check(S.cpu().numpy(), S_ref, "f32", "qed 64x8 S after 30 steps")
+
+
+def test_qed_step_sequence_matches_forward(qd):
+    """T QED decode steps equal one QED forward over the T tokens (fp32, d=64)."""
+    d = synth.qed_inputs(2, 40, 2, 64, 64, seed=96, dtype="f32", s0_var=0.01)
+    f = torch.float32
+    o_fwd, S_fwd = qd.qed_fwd(dev(d["q"], f), dev(d["k"], f), dev(d["v"], f), dev(d["g"], f), dev(d["b"], f),
+                              dev(d["w"], f), dev(d["lam_h"], f), dev(d["S0"], f))
+    S = dev(d["S0"], f)
+    outs = []
+    for t in range(40):
+        outs.append(qd.qed_step(S, dev(d["q"][:, t], f), dev(d["k"][:, t], f), dev(d["v"][:, t], f),
+                                dev(d["g"][:, t], f), dev(d["b"][:, t], f), dev(d["w"][:, t], f),
+                                dev(d["lam_h"], f)))
+    o_step = torch.stack(outs, dim=1)
+    torch.cuda.synchronize()
+    check(o_step.cpu().numpy(), o_fwd.cpu().numpy(), "f32", "qed step vs fwd o")
+    check(S.cpu().numpy(), S_fwd.cpu().numpy(), "f32", "qed step vs fwd S")
 
 
 def test_device_status_ok(qd):
