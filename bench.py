@@ -12,6 +12,7 @@ B=8, H=16, T=2048, dk=dv=128, bf16 inputs, fp32 state, full Q-Delta gates
   roofline the dominant kernel against the measured HBM copy bandwidth
   tensor   its GEMM work against the measured bf16 tensor peak
   decode   qdelta_step on 512 sequences x 16 heads (fp32 128x128 state), GB/s
+  qed_decode  qed_step on the same shape, GB/s
   qed      qed_fwd at B=4, H=8, T=4096, d=128 bf16, tokens/s
   cpu_baseline  the fp64 oracle timed on this host's cores on a bounded sample
 
@@ -283,6 +284,36 @@ def time_decode(qd, steps=50, warmup=5, N=512):
             "bytes_per_step": nbytes, "GBps": nbytes / (ms * 1e-3) / 1e9}
 
 
+def time_qed_decode(qd, steps=50, warmup=5, N=512):
+    """qed_step on N sequences x 16 heads, fp32 128x128 state (the decode shape)."""
+    import torch
+    d = synth.qed_decode_inputs(N, 16, 128, 128, 4, seed=6, dtype="bf16", s0_var=None)
+    S = torch.empty(N, 16, 128, 128, dtype=torch.float32, device="cuda").normal_(0, 0.1)
+    tok = [{k: to_dev(d[k][i], torch.bfloat16) for k in ("q", "k", "v", "g", "b", "w")} for i in range(4)]
+    lam_h = to_dev(d["lam_h"], torch.float32)
+    o = torch.empty(N, 16, 128, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        t = tok[i % 4]
+        qd.qed_step(S, t["q"], t["k"], t["v"], t["g"], t["b"], t["w"], lam_h, o=o, stream=stream)
+
+    for i in range(warmup):
+        step(i)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(steps):
+        step(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    heads = N * 16
+    nbytes = heads * (2 * 128 * 128 * 4 + 2 * (4 * 128 + 3 * 128))
+    return {"workload": f"qed_step_bf16_N{N}_H16_d128", "ms_per_step": ms, "tokens_per_s": N / (ms * 1e-3),
+            "bytes_per_step": nbytes, "GBps": nbytes / (ms * 1e-3) / 1e9}
+
+
 def time_qed(qd, steps=20, warmup=3):
     import torch
     _, d = synth.qed_gdn2()
@@ -404,6 +435,9 @@ def main():
             dec = time_decode(qd)
             dec["frac_hbm"] = dec["GBps"] / hbm_peak
             extras["decode"] = dec
+            qdec = time_qed_decode(qd)
+            qdec["frac_hbm"] = qdec["GBps"] / hbm_peak
+            extras["qed_decode"] = qdec
             extras["qed"] = time_qed(qd)
     del sets
     torch.cuda.synchronize()
