@@ -47,8 +47,9 @@ def _load():
         lib.oracle_qdelta_step.argtypes = [I] * 4 + [P] * 8 + [I]
         lib.oracle_qed_fwd_variant.argtypes = [I] * 5 + [P] * 7 + [I] + [P] * 4 + [I]
         lib.oracle_qed_step.argtypes = [I] * 4 + [P] * 8 + [I, P, P, I]
+        lib.oracle_qdelta_fwd_prologue.argtypes = [I] * 5 + [P] * 9 + [I]
         for f in (lib.oracle_qdelta_fwd, lib.oracle_qed_fwd, lib.oracle_qdelta_step, lib.oracle_qed_fwd_variant,
-                  lib.oracle_qed_step):
+                  lib.oracle_qed_step, lib.oracle_qdelta_fwd_prologue):
             f.restype = I
         _lib = lib
     return _lib
@@ -91,6 +92,21 @@ def qed_fwd(q, k, v, g, b, w, lam_h, S0=None, nthreads: int = 0):
                                 _ptr(w), _ptr(lam_h), _ptr(S0), _ptr(o), _ptr(S), nthreads)
     if rc:
         raise MemoryError("oracle_qed_fwd failed")
+    return o, S
+
+
+def qdelta_fwd_prologue(q_raw, k_raw, v, a_logit, b_logit, l_logit, S0=None, nthreads: int = 0):
+    """Q-Delta forward from the projections: q, k = SiLU(x)/|SiLU(x)|, beta, lambda =
+    sigmoid(logit), alpha = exp(-softplus(logit)) (None logits: alpha 1, lambda 0)."""
+    q_raw, k_raw, v, a_logit, b_logit, l_logit, S0 = map(_f64, (q_raw, k_raw, v, a_logit, b_logit, l_logit, S0))
+    B, T, H, dk = q_raw.shape
+    dv = v.shape[-1]
+    o = np.zeros((B, T, H, dv))
+    S = np.zeros((B, H, dv, dk))
+    rc = _load().oracle_qdelta_fwd_prologue(B, T, H, dk, dv, _ptr(q_raw), _ptr(k_raw), _ptr(v), _ptr(a_logit),
+                                            _ptr(b_logit), _ptr(l_logit), _ptr(S0), _ptr(o), _ptr(S), nthreads)
+    if rc:
+        raise MemoryError("oracle_qdelta_fwd_prologue failed")
     return o, S
 
 

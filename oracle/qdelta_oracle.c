@@ -32,6 +32,11 @@
  *    with P(u) = u - k (k^T u).
  *  - Decode steps: one iteration of the Q-Delta or the QED loop per call, the
  *    state carried in and out in place.
+ *  - Prologue (the feature map and gates computed from the layer's projections):
+ *    DeltaNet notes sec. 3.8, q = SiLU(x_q)/|SiLU(x_q)|_2 and the same for k,
+ *    beta = sigmoid(x_beta); Q-Delta notes sec. 2.5 (App. B), lambda = sigmoid(x_lambda);
+ *    the decay alpha = exp(-softplus(x_alpha)), the parameterisation of the
+ *    workloads' decay gate.  Applied token by token, then the recurrence above.
  *
  * Storage of every state buffer, both methods: [B][H][d_v][d_k] row-major.  For
  * Q-Delta that is S itself; for QED it is S^T (QED's K x V state transposed), so
@@ -253,6 +258,48 @@ int oracle_qed_fwd_variant(int B, int T, int H, int dk, int dv,
     J.variant = variant; J.z = z;
     J.S0 = S0; J.o = o; J.S_final = S_final; J.method = 1;
     return run(&J, nthreads);
+}
+
+/* The prologue for one token-head: q = SiLU(x)/|SiLU(x)|, sigmoid and
+ * exp(-softplus) gates.  The norm of an all-zero SiLU row is taken as 1. */
+static void feature_map(const double *x, double *y, int d)
+{
+    double ss = 0.0;
+    for (int j = 0; j < d; ++j) {
+        y[j] = x[j] / (1.0 + exp(-x[j]));                  /* SiLU(x) = x sigmoid(x) */
+        ss += y[j] * y[j];
+    }
+    const double inv = ss > 0.0 ? 1.0 / sqrt(ss) : 1.0;
+    for (int j = 0; j < d; ++j) y[j] *= inv;
+}
+static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
+static double exp_neg_softplus(double x) { return exp(-log1p(exp(x))); }
+
+/* Q-Delta forward from the layer's projections: q_raw, k_raw [B][T][H][dk] go
+ * through the feature map, the gate logits [B][T][H] through their gates (NULL
+ * alpha / lambda logits: alpha = 1 / lambda = 0), then oracle_qdelta_fwd. */
+int oracle_qdelta_fwd_prologue(int B, int T, int H, int dk, int dv,
+                               const double *q_raw, const double *k_raw, const double *v,
+                               const double *a_logit, const double *b_logit, const double *l_logit,
+                               const double *S0, double *o, double *S_final, int nthreads)
+{
+    const size_t nt = (size_t)B * T * H;
+    double *q = malloc(sizeof(double) * nt * dk), *k = malloc(sizeof(double) * nt * dk);
+    double *al = a_logit ? malloc(sizeof(double) * nt) : NULL, *be = malloc(sizeof(double) * nt);
+    double *lm = l_logit ? malloc(sizeof(double) * nt) : NULL;
+    int rc = 1;
+    if (q && k && be && (!a_logit || al) && (!l_logit || lm)) {
+        for (size_t i = 0; i < nt; ++i) {
+            feature_map(q_raw + i * dk, q + i * dk, dk);
+            feature_map(k_raw + i * dk, k + i * dk, dk);
+            be[i] = sigmoid(b_logit[i]);
+            if (al) al[i] = exp_neg_softplus(a_logit[i]);
+            if (lm) lm[i] = sigmoid(l_logit[i]);
+        }
+        rc = oracle_qdelta_fwd(B, T, H, dk, dv, q, k, v, al, be, lm, S0, o, S_final, nthreads);
+    }
+    free(q); free(k); free(al); free(be); free(lm);
+    return rc;
 }
 
 /* One QED decode step for N sequences x H heads: S [N][H][dv][dk] (QED's state

@@ -197,3 +197,47 @@ def test_oracle_passes_qed_arm_pins(arm):
                                       ("rand", "rand_ungated")])
 def test_qed_arm_mutant_rejected(arm, kind):
     assert not qed_arm_pins_hold(arm, _qed_arm_mutant(arm, kind))
+
+
+# the prologue (DeltaNet notes sec. 3.8; Q-Delta notes sec. 2.5): feature map and gates
+def _prologue_mutant(kind):
+    def fmap(x):
+        s = x * (1.0 / (1.0 + np.exp(x))) if kind == "silu_sign" else x / (1.0 + np.exp(-x))
+        n = np.abs(s).sum(-1, keepdims=True) if kind == "l1_norm" else np.linalg.norm(s, axis=-1, keepdims=True)
+        return s / n
+    def gate_alpha(x):
+        return 1.0 / (1.0 + np.exp(-x)) if kind == "alpha_sigmoid" else np.exp(-np.log1p(np.exp(x)))
+    def fwd(q_raw, k_raw, v, a_l, b_l, l_l, S0):
+        return oracle.qdelta_fwd(fmap(q_raw), fmap(k_raw), v, gate_alpha(a_l), 1.0 / (1.0 + np.exp(-b_l)),
+                                 1.0 / (1.0 + np.exp(-l_l)), S0)
+    return fwd
+
+
+def oracle_prologue(q_raw, k_raw, v, a_l, b_l, l_l, S0):
+    return oracle.qdelta_fwd_prologue(q_raw, k_raw, v, a_l, b_l, l_l, S0)
+
+
+def prologue_pins_hold(fwd):
+    """SiLU's shape on (ln 3, -ln 3) -> (3, -1)/sqrt(10) and alpha = 1/(1 + e^x)."""
+    T, H = 3, 2
+    l3 = np.log(3.0)
+    raw = np.broadcast_to(np.array([l3, -l3, 0.0, 0.0]), (1, T, H, 4)).copy()
+    feat = np.broadcast_to(np.array([3.0, -1.0, 0.0, 0.0]) / np.sqrt(10.0), (1, T, H, 4)).copy()
+    v = rng.standard_normal((1, T, H, 4))
+    a_l = rng.uniform(-3, 3, (1, T, H))
+    b_l = rng.uniform(-3, 3, (1, T, H))
+    l_l = rng.uniform(-3, 3, (1, T, H))
+    S0 = rng.standard_normal((1, H, 4, 4)) * 0.3
+    o1, S1 = fwd(raw, raw, v, a_l, b_l, l_l, S0)
+    o2, S2 = oracle.qdelta_fwd(feat, feat, v, 1.0 / (1.0 + np.exp(a_l)), 1.0 / (1.0 + np.exp(-b_l)),
+                               1.0 / (1.0 + np.exp(-l_l)), S0)
+    return np.allclose(o1, o2, atol=1e-12) and np.allclose(S1, S2, atol=1e-12)
+
+
+def test_oracle_passes_prologue_pins():
+    assert prologue_pins_hold(oracle_prologue)
+
+
+@pytest.mark.parametrize("kind", ["silu_sign", "l1_norm", "alpha_sigmoid"])
+def test_prologue_mutant_rejected(kind):
+    assert not prologue_pins_hold(_prologue_mutant(kind))

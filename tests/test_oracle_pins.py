@@ -294,6 +294,71 @@ def test_qed_step_sequence_equals_forward(variant):
     np.testing.assert_array_equal(S, S_f)
 
 
+# ------------------------------------------------ prologue (DeltaNet 3.8, Q-Delta 2.5)
+
+def _plain_vs_prologue(q_raw, k_raw, q, k, a_logit, alpha, b_logit, beta, l_logit, lam, atol):
+    """The prologue forward on raw inputs equals the plain forward on the feature map's
+    and gates' closed-form values."""
+    T, H, d = q_raw.shape[1:]
+    v = rng.standard_normal((1, T, H, d))
+    S0 = rng.standard_normal((1, H, d, d)) * 0.3
+    o1, S1 = oracle.qdelta_fwd_prologue(q_raw, k_raw, v, a_logit, b_logit, l_logit, S0)
+    o2, S2 = oracle.qdelta_fwd(q, k, v, alpha, beta, lam, S0)
+    np.testing.assert_allclose(o1, o2, atol=atol)
+    np.testing.assert_allclose(S1, S2, atol=atol)
+
+
+def test_prologue_silu_shape_and_l2_norm():
+    """SiLU(x) = x sigmoid(x): sigmoid(ln 3) = 3/4 and sigmoid(-ln 3) = 1/4, so the raw row
+    (ln 3, -ln 3) maps to (3 ln3/4, -ln3/4) / |.| = (3, -1)/sqrt(10); a zero entry stays 0."""
+    T, H = 4, 2
+    l3 = np.log(3.0)
+    row = np.array([l3, -l3, 0.0, 0.0])
+    q_raw = np.broadcast_to(row, (1, T, H, 4)).copy()
+    k_raw = np.broadcast_to(row[[2, 0, 3, 1]], (1, T, H, 4)).copy()
+    q = np.broadcast_to(np.array([3.0, -1.0, 0.0, 0.0]) / np.sqrt(10.0), (1, T, H, 4)).copy()
+    k = np.broadcast_to(np.array([0.0, 3.0, 0.0, -1.0]) / np.sqrt(10.0), (1, T, H, 4)).copy()
+    z = np.zeros((1, T, H))
+    # logit 0: sigmoid(0) = 1/2 and exp(-softplus(0)) = exp(-ln 2) = 1/2
+    half = np.full((1, T, H), 0.5)
+    _plain_vs_prologue(q_raw, k_raw, q, k, z, half, z, half, z, half, atol=1e-14)
+
+
+def test_prologue_gates_closed_forms():
+    """exp(-softplus(x)) = 1/(1 + e^x) and sigmoid(x) = 1/(1 + e^-x) for the gate logits,
+    with one-hot features (one large entry, the others far negative: SiLU ~ 0)."""
+    T, H, d = 6, 3, 5
+    q_raw = np.full((1, T, H, d), -60.0)
+    k_raw = np.full((1, T, H, d), -60.0)
+    idx_q = rng.integers(0, d, (T, H))
+    idx_k = rng.integers(0, d, (T, H))
+    q = np.zeros((1, T, H, d))
+    k = np.zeros((1, T, H, d))
+    for t in range(T):
+        for h in range(H):
+            q_raw[0, t, h, idx_q[t, h]] = 2.5
+            k_raw[0, t, h, idx_k[t, h]] = 4.0
+            q[0, t, h, idx_q[t, h]] = 1.0
+            k[0, t, h, idx_k[t, h]] = 1.0
+    a_l, b_l, l_l = [rng.uniform(-4, 4, (1, T, H)) for _ in range(3)]
+    alpha = 1.0 / (1.0 + np.exp(a_l))
+    beta = 1.0 / (1.0 + np.exp(-b_l))
+    lam = 1.0 / (1.0 + np.exp(-l_l))
+    _plain_vs_prologue(q_raw, k_raw, q, k, a_l, alpha, b_l, beta, l_l, lam, atol=1e-12)
+    # absent alpha / lambda logits: alpha = 1, lambda = 0
+    _plain_vs_prologue(q_raw, k_raw, q, k, None, None, b_l, beta, None, None, atol=1e-12)
+
+
+def test_prologue_large_inputs_reduce_to_l2_normalisation():
+    """For large positive entries SiLU(x) = x (to 1e-17), so the feature map is x/|x|."""
+    T, H, d = 5, 2, 6
+    u = rng.uniform(1.0, 2.0, (1, T, H, d))
+    w = rng.uniform(1.0, 2.0, (1, T, H, d))
+    _plain_vs_prologue(60.0 * u, 60.0 * w, u / np.linalg.norm(u, axis=-1, keepdims=True),
+                       w / np.linalg.norm(w, axis=-1, keepdims=True), None, None,
+                       np.zeros((1, T, H)), np.full((1, T, H), 0.5), None, None, atol=1e-12)
+
+
 # ------------------------------------------------------------ Q-Delta (page 1)
 
 def test_deltanet_special_case():
