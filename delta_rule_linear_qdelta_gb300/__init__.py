@@ -24,9 +24,9 @@ QD_OK, QD_ERR_ARG, QD_ERR_UNSUPPORTED, QD_ERR_CUDA, QD_ERR_TIMEOUT, QD_ERR_WORKS
 QD_F32, QD_BF16 = 0, 1
 STATUS_NAMES = {0: "QD_OK", 1: "QD_ERR_ARG", 2: "QD_ERR_UNSUPPORTED", 3: "QD_ERR_CUDA",
                 4: "QD_ERR_TIMEOUT", 5: "QD_ERR_WORKSPACE"}
-EXPORTS = ("qdelta_fwd", "qdelta_workspace_bytes", "qed_fwd", "qed_fwd_variant", "qed_workspace_bytes",
-           "qdelta_step", "qed_step", "qdelta_fwd_static_scratch", "qd_device_status", "qd_last_error",
-           "qd_last_launch_count")
+EXPORTS = ("qdelta_fwd", "qdelta_fwd_prologue", "qdelta_workspace_bytes", "qed_fwd", "qed_fwd_variant",
+           "qed_workspace_bytes", "qdelta_step", "qdelta_step_prologue", "qed_step", "qdelta_fwd_static_scratch",
+           "qd_device_status", "qd_last_error", "qd_last_launch_count")
 QED_VARIANTS = {"full": 0, "nogate": 1, "nogate_noproj": 2, "rand": 3}
 
 
@@ -50,6 +50,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
     P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     lib.qdelta_fwd.argtypes = [P] * 9 + [I] * 7 + [P, Z, P]
+    lib.qdelta_fwd_prologue.argtypes = [P] * 9 + [I] * 7 + [P, Z, P]
+    lib.qdelta_step_prologue.argtypes = [P] * 8 + [I] * 5 + [P]
     lib.qdelta_fwd_static_scratch.argtypes = [P] * 9 + [I] * 7 + [P]
     lib.qed_fwd.argtypes = [P] * 10 + [I] * 7 + [P, Z, P]
     lib.qdelta_step.argtypes = [P] * 8 + [I] * 5 + [P]
@@ -59,7 +61,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qed_workspace_bytes.argtypes = [I] * 7
     lib.qd_device_status.argtypes = [P]
     for f in (lib.qdelta_fwd, lib.qed_fwd, lib.qdelta_step, lib.qdelta_fwd_static_scratch, lib.qd_device_status,
-              lib.qd_last_launch_count, lib.qed_fwd_variant, lib.qed_step):
+              lib.qd_last_launch_count, lib.qed_fwd_variant, lib.qed_step, lib.qdelta_fwd_prologue,
+              lib.qdelta_step_prologue):
         f.restype = I
     lib.qdelta_workspace_bytes.restype = Z
     lib.qed_workspace_bytes.restype = Z
@@ -137,9 +140,12 @@ def _workspace(nbytes, workspace, device):
 
 
 def qdelta_fwd(q, k, v, alpha, beta, lam, S0=None, *, o=None, S_final=None, return_final=True,
-               chunk=64, workspace=None, stream=None):
+               chunk=64, workspace=None, stream=None, prologue=False):
     """Chunked Q-Delta forward.  q, k [B,T,H,dk]; v [B,T,H,dv]; alpha, beta, lam [B,T,H]
-    (alpha None = 1, lam None = 0); S0 [B,H,dv,dk] fp32 or None.  Returns (o, S_final)."""
+    (alpha None = 1, lam None = 0); S0 [B,H,dv,dk] fp32 or None.  Returns (o, S_final).
+    prologue=True: q, k are projections and alpha, beta, lam logits; the feature map
+    SiLU(x)/|SiLU(x)| and the gates (exp(-softplus), sigmoid, sigmoid) are applied
+    inside (the C qdelta_fwd_prologue)."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     dt = q.dtype
@@ -158,10 +164,10 @@ def qdelta_fwd(q, k, v, alpha, beta, lam, S0=None, *, o=None, S_final=None, retu
     _need(S_final, "S_final", torch.float32, (B, H, dv, dk), optional=True)
     code = _dtype_code(q)
     workspace, wsb = _workspace(qdelta_workspace_bytes(B, T, H, dk, dv, chunk, code), workspace, q.device)
-    st = load_library().qdelta_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(lam), _ptr(S0),
-                                   _ptr(o), _ptr(S_final), B, T, H, dk, dv, chunk, code, _ptr(workspace),
-                                   wsb, _stream(stream, q.device))
-    _check(st, "qdelta_fwd")
+    fn = load_library().qdelta_fwd_prologue if prologue else load_library().qdelta_fwd
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(lam), _ptr(S0), _ptr(o), _ptr(S_final),
+            B, T, H, dk, dv, chunk, code, _ptr(workspace), wsb, _stream(stream, q.device))
+    _check(st, "qdelta_fwd_prologue" if prologue else "qdelta_fwd")
     return o, S_final
 
 
@@ -247,9 +253,9 @@ def qed_step(S, q, k, v, g, b, w, lam_h, *, o=None, stream=None, variant="full",
     return o
 
 
-def qdelta_step(S, q, k, v, alpha, beta, lam, *, o=None, stream=None):
+def qdelta_step(S, q, k, v, alpha, beta, lam, *, o=None, stream=None, prologue=False):
     """One decode step, S [N,H,dv,dk] fp32 updated in place; tokens [N,H,d]; gates [N,H]
-    (alpha None = 1, lam None = 0).  Returns o [N,H,dv]."""
+    (alpha None = 1, lam None = 0).  Returns o [N,H,dv].  prologue=True as in qdelta_fwd."""
     N, H, dk = q.shape
     dv = v.shape[-1]
     dt = q.dtype
@@ -263,9 +269,10 @@ def qdelta_step(S, q, k, v, alpha, beta, lam, *, o=None, stream=None):
     if o is None:
         o = torch.empty((N, H, dv), dtype=dt, device=q.device)
     _need(o, "o", dt, (N, H, dv))
-    st = load_library().qdelta_step(_ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(lam),
-                                    _ptr(o), N, H, dk, dv, _dtype_code(q), _stream(stream, q.device))
-    _check(st, "qdelta_step")
+    fn = load_library().qdelta_step_prologue if prologue else load_library().qdelta_step
+    st = fn(_ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(lam), _ptr(o), N, H, dk, dv,
+            _dtype_code(q), _stream(stream, q.device))
+    _check(st, "qdelta_step_prologue" if prologue else "qdelta_step")
     return o
 
 

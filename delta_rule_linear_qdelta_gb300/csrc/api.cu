@@ -81,22 +81,27 @@ size_t qed_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dt
     return qd::qdelta_segment_workspace(B, H, qd::qed_segments(B, T, H, dk, dv, dtype));
 }
 
-qd_status qdelta_fwd(const void *q, const void *k, const void *v, const void *alpha, const void *beta,
-                     const void *lam, const float *S0, void *o, float *S_final, int B, int T, int H,
-                     int dk, int dv, int chunk, qd_dtype dtype, void *workspace, size_t workspace_bytes,
-                     cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+qd_status qdelta_fwd_impl(const char *fn, int prologue, const void *q, const void *k, const void *v,
+                          const void *alpha, const void *beta, const void *lam, const float *S0, void *o,
+                          float *S_final, int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype,
+                          void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     g_err[0] = 0;
     const void *req[] = {q, k, v, beta, o};
     const void *opt[] = {alpha, lam, S0, S_final, workspace};
-    qd_status st = check_fwd("qdelta_fwd", req, 5, opt, 5, B, T, H, dk, dv, chunk, dtype);
+    qd_status st = check_fwd(fn, req, 5, opt, 5, B, T, H, dk, dv, chunk, dtype);
     if (st != QD_OK) return st;
     const size_t need = qdelta_workspace_bytes(B, T, H, dk, dv, chunk, dtype);
     if (need && (!workspace || workspace_bytes < need))
-        return fail(QD_ERR_WORKSPACE, "qdelta_fwd: workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+        return fail(QD_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need, workspace_bytes);
     int n = 0;
     if (B == 0 || H == 0) { g_launches = 0; return QD_OK; }
     if (T == 0) { g_launches = 0; return empty_sequence(S0, S_final, B, H, dk, dv, stream); }
-    qd::QDeltaArgs a{q, k, v, alpha, beta, lam, S0, o, S_final, B, T, H, dk, dv, workspace, workspace_bytes};
+    qd::QDeltaArgs a{q, k, v, alpha, beta, lam, S0, o, S_final, B, T, H, dk, dv, workspace, workspace_bytes,
+                     prologue};
     cudaError_t e;
     if (qd::qdelta_tc_supported(a, dtype)) {
         const int G = qd::qdelta_segments(B, T, H, dk, dv, dtype);
@@ -107,6 +112,52 @@ qd_status qdelta_fwd(const void *q, const void *k, const void *v, const void *al
     if (e != cudaSuccess) return cuda_fail(e, "qdelta_fwd launch");
     g_launches = n;
     return QD_OK;
+}
+
+qd_status qdelta_step_impl(const char *fn, int prologue, float *S, const void *q, const void *k,
+                           const void *v, const void *alpha, const void *beta, const void *lam, void *o, int N,
+                           int H, int dk, int dv, qd_dtype dtype, cudaStream_t stream) {
+    g_err[0] = 0;
+    if (N < 0 || H < 0) return fail(QD_ERR_ARG, "%s: negative size N=%d H=%d", fn, N, H);
+    if (dtype != QD_F32 && dtype != QD_BF16) return fail(QD_ERR_UNSUPPORTED, "%s: unknown dtype", fn);
+    if (!head_dim_ok(dk) || !head_dim_ok(dv))
+        return fail(QD_ERR_UNSUPPORTED, "%s: head dims dk=%d dv=%d not in {16,32,64,128}", fn, dk, dv);
+    if ((double)N * H > 2147483647.0) return fail(QD_ERR_ARG, "%s: N*H exceeds the grid limit", fn);
+    const bool empty = (N == 0 || H == 0);
+    const void *req[] = {S, q, k, v, beta, o};
+    for (int i = 0; i < 6; ++i) {
+        if (!req[i] && !empty) return fail(QD_ERR_ARG, "%s: required pointer argument #%d is NULL", fn, i);
+        if (!aligned16(req[i])) return fail(QD_ERR_ARG, "%s: pointer argument #%d not 16-byte aligned", fn, i);
+    }
+    if (!aligned16(alpha) || !aligned16(lam)) return fail(QD_ERR_ARG, "%s: gate pointer not 16-byte aligned", fn);
+    g_launches = 0;
+    if (empty) return QD_OK;
+    int n = 0;
+    qd::StepArgs a{S, q, k, v, alpha, beta, lam, o, N, H, dk, dv, prologue};
+    cudaError_t e = qd::launch_qdelta_step(a, dtype, stream, &n);
+    if (e != cudaSuccess) return cuda_fail(e, "qdelta_step launch");
+    g_launches = n;
+    return QD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+qd_status qdelta_fwd(const void *q, const void *k, const void *v, const void *alpha, const void *beta,
+                     const void *lam, const float *S0, void *o, float *S_final, int B, int T, int H,
+                     int dk, int dv, int chunk, qd_dtype dtype, void *workspace, size_t workspace_bytes,
+                     cudaStream_t stream) {
+    return qdelta_fwd_impl("qdelta_fwd", 0, q, k, v, alpha, beta, lam, S0, o, S_final, B, T, H, dk, dv, chunk,
+                           dtype, workspace, workspace_bytes, stream);
+}
+
+qd_status qdelta_fwd_prologue(const void *q_raw, const void *k_raw, const void *v, const void *a_logit,
+                              const void *b_logit, const void *l_logit, const float *S0, void *o, float *S_final,
+                              int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+    return qdelta_fwd_impl("qdelta_fwd_prologue", 1, q_raw, k_raw, v, a_logit, b_logit, l_logit, S0, o, S_final,
+                           B, T, H, dk, dv, chunk, dtype, workspace, workspace_bytes, stream);
 }
 
 qd_status qed_fwd_variant(const void *q, const void *k, const void *v, const void *g, const void *b,
@@ -182,27 +233,14 @@ qd_status qed_step(float *S, const void *q, const void *k, const void *v, const 
 qd_status qdelta_step(float *S, const void *q, const void *k, const void *v, const void *alpha,
                       const void *beta, const void *lam, void *o, int N, int H, int dk, int dv,
                       qd_dtype dtype, cudaStream_t stream) {
-    g_err[0] = 0;
-    if (N < 0 || H < 0) return fail(QD_ERR_ARG, "qdelta_step: negative size N=%d H=%d", N, H);
-    if (dtype != QD_F32 && dtype != QD_BF16) return fail(QD_ERR_UNSUPPORTED, "qdelta_step: unknown dtype");
-    if (!head_dim_ok(dk) || !head_dim_ok(dv))
-        return fail(QD_ERR_UNSUPPORTED, "qdelta_step: head dims dk=%d dv=%d not in {16,32,64,128}", dk, dv);
-    if ((double)N * H > 2147483647.0) return fail(QD_ERR_ARG, "qdelta_step: N*H exceeds the grid limit");
-    const bool empty = (N == 0 || H == 0);
-    const void *req[] = {S, q, k, v, beta, o};
-    for (int i = 0; i < 6; ++i) {
-        if (!req[i] && !empty) return fail(QD_ERR_ARG, "qdelta_step: required pointer argument #%d is NULL", i);
-        if (!aligned16(req[i])) return fail(QD_ERR_ARG, "qdelta_step: pointer argument #%d not 16-byte aligned", i);
-    }
-    if (!aligned16(alpha) || !aligned16(lam)) return fail(QD_ERR_ARG, "qdelta_step: gate pointer not 16-byte aligned");
-    g_launches = 0;
-    if (empty) return QD_OK;
-    int n = 0;
-    qd::StepArgs a{S, q, k, v, alpha, beta, lam, o, N, H, dk, dv};
-    cudaError_t e = qd::launch_qdelta_step(a, dtype, stream, &n);
-    if (e != cudaSuccess) return cuda_fail(e, "qdelta_step launch");
-    g_launches = n;
-    return QD_OK;
+    return qdelta_step_impl("qdelta_step", 0, S, q, k, v, alpha, beta, lam, o, N, H, dk, dv, dtype, stream);
+}
+
+qd_status qdelta_step_prologue(float *S, const void *q_raw, const void *k_raw, const void *v,
+                               const void *a_logit, const void *b_logit, const void *l_logit, void *o, int N,
+                               int H, int dk, int dv, qd_dtype dtype, cudaStream_t stream) {
+    return qdelta_step_impl("qdelta_step_prologue", 1, S, q_raw, k_raw, v, a_logit, b_logit, l_logit, o, N, H, dk,
+                            dv, dtype, stream);
 }
 
 qd_status qd_device_status(cudaStream_t stream) {

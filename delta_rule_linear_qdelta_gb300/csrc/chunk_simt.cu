@@ -115,11 +115,34 @@ __global__ void __launch_bounds__(kNT) qdelta_chunk_simt_kernel(QDeltaArgs a) {
             const int t = tid;
             const size_t tok = ((size_t)b * T + c0 + t) * H + h;
             const bool ok = t < n;
-            ell[t] = (ok && alpha) ? logf(to_f(alpha[tok])) : 0.f;
-            bet[t] = ok ? to_f(beta[tok]) : 0.f;
-            lmb[t] = (ok && lam) ? to_f(lam[tok]) : 0.f;
+            if (a.prologue) {                             // gates from their logits
+                ell[t] = (ok && alpha) ? neg_softplus(to_f(alpha[tok])) : 0.f;
+                bet[t] = ok ? sigmoid_acc(to_f(beta[tok])) : 0.f;
+                lmb[t] = (ok && lam) ? sigmoid_acc(to_f(lam[tok])) : 0.f;
+            } else {
+                ell[t] = (ok && alpha) ? logf(to_f(alpha[tok])) : 0.f;
+                bet[t] = ok ? to_f(beta[tok]) : 0.f;
+                lmb[t] = (ok && lam) ? to_f(lam[tok]) : 0.f;
+            }
         }
         __syncthreads();
+        if (a.prologue) {                                 // q, k = SiLU(x)/|SiLU(x)|, a warp per row
+            const int lane = tid & 31, warp = tid >> 5;
+            for (int r = warp; r < 2 * C; r += kNT / 32) {
+                float *row = (r < C ? Qs : Ks) + (r % C) * LK;
+                float ss = 0.f;
+                for (int j = lane; j < DK; j += 32) {
+                    const float y = silu_acc(row[j]);
+                    row[j] = y;
+                    ss = fmaf(y, y, ss);
+                }
+#pragma unroll
+                for (int off = 16; off; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                const float inv = ss > 0.f ? 1.f / sqrtf(ss) : 1.f;   // padding rows stay zero
+                for (int j = lane; j < DK; j += 32) row[j] *= inv;
+            }
+            __syncthreads();
+        }
         chunk_log_prefix(ell);
         for (int idx = tid; idx < C * DK; idx += kNT) {
             const int t = idx / DK, j = idx % DK;

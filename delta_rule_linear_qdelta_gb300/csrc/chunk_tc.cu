@@ -116,6 +116,9 @@ struct TcParams {
     int flags;   // kTcNoV | kTcS0Identity | kTcNoO (segment-scan passes)
 };
 
+// PRO: q, k, alpha, beta, lambda arrive as projections and logits (the prologue of
+// qdelta_fwd_prologue); a template parameter, so the plain kernel carries none of it.
+template <bool PRO>
 __global__ void __launch_bounds__(kAllThreads, 1)
 qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -149,6 +152,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     const bool s0_id = flags & kTcS0Identity;
     auto no_v = [&]() { return (opaque(flags) & kTcNoV) != 0; };
     auto no_o = [&]() { return (opaque(flags) & kTcNoO) != 0; };
+    constexpr bool prologue = PRO;
 
     if (tid == 0) {
         mbar_init(&bar_full[0], 1);
@@ -209,15 +213,23 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     auto compute_gates = [&](int c) {
         const int buf = c & 3;
         const bool has_a = opaque(p.alpha) != nullptr, has_l = opaque(p.lam) != nullptr;
-        float ga[2], gb[2], gl[2];
+        const bool pro = prologue;
+        float la[2], gb[2], gl[2];
 #pragma unroll
         for (int u = 0; u < 2; ++u) {                  // tokens past T: alpha 1, beta 0, lambda 0
             const bool ok = c * kC + 2 * lane + u < T;
-            ga[u] = (ok && has_a) ? bf(ra[u]) : 1.f;
-            gb[u] = ok ? bf(rb[u]) : 0.f;
-            gl[u] = (ok && has_l) ? bf(rl[u]) : 0.f;
+            if (pro) {                                 // gates from their logits
+                const float x = bf(ra[u]);
+                la[u] = (ok && has_a) ? -(fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)))) : 0.f;
+                gb[u] = ok ? sigmoid_fast(bf(rb[u])) : 0.f;
+                gl[u] = (ok && has_l) ? sigmoid_fast(bf(rl[u])) : 0.f;
+            } else {
+                la[u] = (ok && has_a) ? __logf(bf(ra[u])) : 0.f;
+                gb[u] = ok ? bf(rb[u]) : 0.f;
+                gl[u] = (ok && has_l) ? bf(rl[u]) : 0.f;
+            }
         }
-        const float l0 = __logf(ga[0]), l1 = __logf(ga[1]);
+        const float l0 = la[0], l1 = la[1];
         float sum = l0 + l1;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -281,7 +293,10 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     auto stage_addr = [&](int c) { return sbase + (uint32_t)(c & 1) * kStageBytes; };
 
     // ---------------------------------------------------------------- prep group
-    // X = K + lambda Q into rows 0-63 of the XQ panels of chunk c's stage
+    // X = K + lambda Q into rows 0-63 of the XQ panels of chunk c's stage.  From
+    // projections (prologue), K and Q first become SiLU(x)/|SiLU(x)| in place: the
+    // 16-byte chunks r = 0, 2 of a thread are token row tid/8 of both 64-column panels,
+    // r = 1, 3 row 32 + tid/8, and the eight threads of a row sum its squares by shuffles.
     auto x_pass = [&](int c) {
         uint8_t *st = sm + (c & 1) * kStageBytes;
         const float *lam = g_lam[c & 3];
@@ -295,6 +310,51 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             kr[r] = *reinterpret_cast<const uint4 *>(st + OFF_K + pnl * 8192 + off);
             qr[r] = *reinterpret_cast<const uint4 *>(st + OFF_XQ + pnl * 16384 + 8192 + off);
             lm[r] = lam[off >> 7];
+        }
+        if (prologue) {
+            float kf[4][8], qf[4][8], sk[2] = {0.f, 0.f}, sq[2] = {0.f, 0.f};
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                unpack8(kr[r], kf[r]);
+                unpack8(qr[r], qf[r]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    kf[r][e] = silu_fast(kf[r][e]);
+                    qf[r][e] = silu_fast(qf[r][e]);
+                    sk[r & 1] = fmaf(kf[r][e], kf[r][e], sk[r & 1]);
+                    sq[r & 1] = fmaf(qf[r][e], qf[r][e], sq[r & 1]);
+                }
+            }
+#pragma unroll
+            for (int off = 1; off < 8; off <<= 1)
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    sk[i] += __shfl_xor_sync(0xffffffffu, sk[i], off);
+                    sq[i] += __shfl_xor_sync(0xffffffffu, sq[i], off);
+                }
+            float ik[2], iq[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {                 // zero rows (past T) stay zero
+                ik[i] = sk[i] > 0.f ? rsqrtf(sk[i]) : 1.f;
+                iq[i] = sq[i] > 0.f ? rsqrtf(sq[i]) : 1.f;
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int u = tid + kPrepThreads * r;
+                const int pnl = u >> 9;
+                const uint32_t off = (uint32_t)(u & 511) << 4;
+                float xf[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    kf[r][e] *= ik[r & 1];
+                    qf[r][e] *= iq[r & 1];
+                    xf[e] = fmaf(lm[r], qf[r][e], kf[r][e]);
+                }
+                *reinterpret_cast<uint4 *>(st + OFF_K + pnl * 8192 + off) = pack8(kf[r]);
+                *reinterpret_cast<uint4 *>(st + OFF_XQ + pnl * 16384 + 8192 + off) = pack8(qf[r]);
+                *reinterpret_cast<uint4 *>(st + OFF_XQ + pnl * 16384 + off) = pack8(xf);
+            }
+            return;
         }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
@@ -708,12 +768,12 @@ cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nla
         return cudaErrorInvalidValue;
     if (flags & kTcNoO) mo = mq;                      // not used
     else if (!make_token_map(&mo, a.o, a.B, a.T, a.H)) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(qdelta_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+    auto kern = a.prologue ? qdelta_fwd_tc_kernel<true> : qdelta_fwd_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     TcParams p{(const __nv_bfloat16 *)a.alpha, (const __nv_bfloat16 *)a.beta, (const __nv_bfloat16 *)a.lam,
                a.S0, (__nv_bfloat16 *)a.o, a.S_final, a.B, a.T, a.H, flags};
-    qdelta_fwd_tc_kernel<<<a.B * a.H, kAllThreads, kSmemBytes, s>>>(p, mq, mk, mv, mo);
+    kern<<<a.B * a.H, kAllThreads, kSmemBytes, s>>>(p, mq, mk, mv, mo);
     e = cudaGetLastError();
     if (e == cudaSuccess) *nlaunch += 1;
     return e;

@@ -23,6 +23,23 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float
     return __float2bfloat16_rn(x);
 }
 
+// The prologue computed from the layer's projections ("Parallelizing Linear
+// Transformers with the Delta Rule over Sequence Length", sec. 3.8: q, k =
+// SiLU(x)/|SiLU(x)|_2, beta = sigmoid; Q-Delta notes sec. 2.5: lambda = sigmoid; the
+// decay alpha = exp(-softplus(x)), log alpha = -softplus(x)).  Accurate forms for the
+// fp32 paths; the tensor-core path uses the hardware tanh (sigmoid(x) =
+// (1 + tanh(x/2))/2), whose error is below the bf16 rounding its results get.
+__device__ __forceinline__ float silu_acc(float x) { return x / (1.f + expf(-x)); }
+__device__ __forceinline__ float sigmoid_acc(float x) { return 1.f / (1.f + expf(-x)); }
+__device__ __forceinline__ float neg_softplus(float x) { return -(fmaxf(x, 0.f) + log1pf(expf(-fabsf(x)))); }
+__device__ __forceinline__ float tanh_fast(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float sigmoid_fast(float x) { return fmaf(0.5f, tanh_fast(0.5f * x), 0.5f); }
+__device__ __forceinline__ float silu_fast(float x) { return x * sigmoid_fast(x); }
+
 // Arguments of one Q-Delta forward (layouts as in include/qdelta.h).
 struct QDeltaArgs {
     const void *q, *k, *v, *alpha, *beta, *lam;
@@ -32,6 +49,7 @@ struct QDeltaArgs {
     int B, T, H, dk, dv;
     void *ws;
     size_t ws_bytes;
+    int prologue;     // q, k, alpha, beta, lam are projections and logits (qdelta_fwd_prologue)
 };
 
 // QED ablation arms ("The Query Knows What to Forget", Table 1): the term added to
@@ -70,6 +88,7 @@ struct StepArgs {
     const void *q, *k, *v, *alpha, *beta, *lam;
     void *o;
     int N, H, dk, dv;
+    int prologue;     // as in QDeltaArgs
 };
 
 // Launchers.  Each returns the first CUDA error and adds its launches to *nlaunch.

@@ -59,18 +59,42 @@ __global__ void __launch_bounds__(kStepThreads) qdelta_step_kernel(StepArgs a) {
     const TIn *q = (const TIn *)a.q + (size_t)head * DK;
     const TIn *k = (const TIn *)a.k + (size_t)head * DK;
     const TIn *v = (const TIn *)a.v + (size_t)head * dv;
-    const float alpha = a.alpha ? to_f(((const TIn *)a.alpha)[head]) : 1.f;
-    const float beta = to_f(((const TIn *)a.beta)[head]);
-    const float lam = a.lam ? to_f(((const TIn *)a.lam)[head]) : 0.f;
+    float alpha = a.alpha ? to_f(((const TIn *)a.alpha)[head]) : 1.f;
+    float beta = to_f(((const TIn *)a.beta)[head]);
+    float lam = a.lam ? to_f(((const TIn *)a.lam)[head]) : 0.f;
     TIn *o = (TIn *)a.o + (size_t)head * dv;
     float *S = a.S + (size_t)head * dv * DK;
 
     float qv[VEC], kv[VEC], xv[VEC];
-    float kq = 0.f;
 #pragma unroll
     for (int e = 0; e < VEC; ++e) {
         qv[e] = to_f(q[l * VEC + e]);
         kv[e] = to_f(k[l * VEC + e]);
+    }
+    if (a.prologue) {                           // the feature map and gates from projections/logits
+        if (a.alpha) alpha = expf(neg_softplus(alpha));
+        beta = sigmoid_acc(beta);
+        if (a.lam) lam = sigmoid_acc(lam);
+        float sq = 0.f, sk = 0.f;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            qv[e] = silu_acc(qv[e]);
+            kv[e] = silu_acc(kv[e]);
+            sq = fmaf(qv[e], qv[e], sq);
+            sk = fmaf(kv[e], kv[e], sk);
+        }
+        sq = group_sum<LANES>(sq);
+        sk = group_sum<LANES>(sk);
+        const float iq = sq > 0.f ? 1.f / sqrtf(sq) : 1.f, ik = sk > 0.f ? 1.f / sqrtf(sk) : 1.f;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+            qv[e] *= iq;
+            kv[e] *= ik;
+        }
+    }
+    float kq = 0.f;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
         xv[e] = kv[e] + lam * qv[e];
         kq = fmaf(kv[e], qv[e], kq);
     }

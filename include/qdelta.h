@@ -157,6 +157,34 @@ QD_API qd_status qdelta_step(float *S, const void *q, const void *k, const void 
                       int N, int H, int dk, int dv, qd_dtype dtype, cudaStream_t stream);
 
 /*
+ * qdelta_fwd_prologue -- qdelta_fwd from the layer's projections: the feature map
+ * and the gates are computed inside the forward, with no separate pass over HBM.
+ * Per token-head, before the recurrence:
+ *     q = SiLU(q_raw) / |SiLU(q_raw)|_2,  k = SiLU(k_raw) / |SiLU(k_raw)|_2
+ *         ("Parallelizing Linear Transformers with the Delta Rule over Sequence
+ *          Length", sec. 3.8; an all-zero SiLU row stays zero)
+ *     beta = sigmoid(b_logit)             (same section)
+ *     lambda = sigmoid(l_logit)           (Q-Delta notes, sec. 2.5 / App. B; the bias
+ *                                          is part of the logit)
+ *     alpha = exp(-softplus(a_logit))     (the decay parameterisation of the workloads)
+ * a_logit == NULL means alpha = 1 and l_logit == NULL means lambda = 0.  Arguments,
+ * layouts and the workspace rule are those of qdelta_fwd, with q_raw, k_raw in place
+ * of q, k and the logits in place of the gates.  The bf16 tensor-core path evaluates
+ * sigmoid through the hardware tanh (relative error ~2^-11, below the bf16 rounding
+ * of q and k); the fp32 path uses the accurate functions.
+ */
+QD_API qd_status qdelta_fwd_prologue(const void *q_raw, const void *k_raw, const void *v,
+                                     const void *a_logit, const void *b_logit, const void *l_logit,
+                                     const float *S0, void *o, float *S_final,
+                                     int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype,
+                                     void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* qdelta_step with the same prologue (q_raw, k_raw [N][H][dk], logits [N][H]). */
+QD_API qd_status qdelta_step_prologue(float *S, const void *q_raw, const void *k_raw, const void *v,
+                                      const void *a_logit, const void *b_logit, const void *l_logit, void *o,
+                                      int N, int H, int dk, int dv, qd_dtype dtype, cudaStream_t stream);
+
+/*
  * qdelta_fwd_static_scratch -- qdelta_fwd for callers that cannot allocate device
  * memory at call time.  The pages have no counterpart: this is a property of the
  * library, not of the method.

@@ -161,6 +161,27 @@ def qdelta_inputs(B: int, T: int, H: int, dk: int, dv: int, seed: int, dtype: st
     return out
 
 
+def qdelta_raw_inputs(B: int, T: int, H: int, dk: int, dv: int, seed: int, dtype: str = "bf16",
+                      alpha_mu: float = -4.0, s0_var: float | None = None) -> dict:
+    """Inputs of one Q-Delta forward from projections (the prologue entry points): the
+    draws of qdelta_inputs before their maps, i.e. q_raw, k_raw ~ N(0,1) (not
+    normalised), a_logit ~ N(alpha_mu, 0.5), b_logit, l_logit ~ N(0,1); v, S0 as there."""
+    n_tok = B * T * H
+    out = {
+        "q": round_to(normal(seed, STREAMS["q"], n_tok * dk).reshape(B, T, H, dk), dtype),
+        "k": round_to(normal(seed, STREAMS["k"], n_tok * dk).reshape(B, T, H, dk), dtype),
+        "v": round_to(normal(seed, STREAMS["v"], n_tok * dv).reshape(B, T, H, dv), dtype),
+        "alpha": round_to(normal(seed, STREAMS["alpha"], n_tok, mean=alpha_mu, std=0.5).reshape(B, T, H), dtype),
+        "beta": round_to(normal(seed, STREAMS["beta"], n_tok).reshape(B, T, H), dtype),
+        "lam": round_to(normal(seed, STREAMS["lam"], n_tok).reshape(B, T, H), dtype),
+        "S0": None, "dtype": dtype, "shape": (B, T, H, dk, dv),
+    }
+    if s0_var is not None:
+        s0 = normal(seed, STREAMS["S0"], B * H * dv * dk, std=math.sqrt(s0_var))
+        out["S0"] = round_to(s0.reshape(B, H, dv, dk), "f32")
+    return out
+
+
 def qed_inputs(B: int, T: int, H: int, dk: int, dv: int, seed: int, dtype: str = "bf16",
                g_mu: float = -5.0, s0_var: float | None = None) -> dict:
     """Inputs of one QED forward: q, k [B,T,H,dk]; v [B,T,H,dv]; g, b [B,T,H,dk];

@@ -102,3 +102,23 @@ def test_qed_arms_and_step_arguments_checked(lib):
     assert st == qd.QD_ERR_ARG and "z_h" in qd.qd_last_error()
     assert lib.qed_step(None, None, None, None, None, None, None, None, None, 0, 4, 64, 64, 1, 0, None,
                         None) == qd.QD_OK
+
+
+def test_prologue_entry_points_checked(lib):
+    g = ctypes.c_void_p(256)
+    # missing b_logit, misaligned q_raw, unsupported head dim; empty batch is a no-op
+    st = lib.qdelta_fwd_prologue(g, g, g, None, None, None, None, g, None, 1, 8, 1, 64, 64, 64, qd.QD_BF16,
+                                 None, 0, None)
+    assert st == qd.QD_ERR_ARG and "qdelta_fwd_prologue" in qd.qd_last_error()
+    st = lib.qdelta_fwd_prologue(ctypes.c_void_p(258), g, g, None, g, None, None, g, None, 1, 8, 1, 64, 64, 64,
+                                 qd.QD_BF16, None, 0, None)
+    assert st == qd.QD_ERR_ARG and "aligned" in qd.qd_last_error()
+    st = lib.qdelta_fwd_prologue(g, g, g, None, g, None, None, g, None, 1, 8, 1, 48, 64, 64, qd.QD_BF16,
+                                 None, 0, None)
+    assert st == qd.QD_ERR_UNSUPPORTED
+    assert lib.qdelta_fwd_prologue(None, None, None, None, None, None, None, None, None, 0, 8, 4, 64, 64, 64, 1,
+                                   None, 0, None) == qd.QD_OK
+    st = lib.qdelta_step_prologue(g, g, g, g, None, None, None, g, 1, 1, 64, 64, qd.QD_BF16, None)
+    assert st == qd.QD_ERR_ARG and "qdelta_step_prologue" in qd.qd_last_error()
+    assert lib.qdelta_step_prologue(None, None, None, None, None, None, None, None, 0, 4, 64, 64, 1,
+                                    None) == qd.QD_OK

@@ -378,6 +378,59 @@ def test_step_sequence_matches_forward(qd):
     check(S.cpu().numpy(), S_fwd.cpu().numpy(), "f32", "step vs fwd S")
 
 
+# ---------------------------------------------------------------- prologue
+
+def run_prologue(qd, d, use_alpha=True, use_lam=True):
+    dt = tdt(d)
+    o, S = qd.qdelta_fwd(dev(d["q"], dt), dev(d["k"], dt), dev(d["v"], dt),
+                         dev(d["alpha"], dt) if use_alpha else None, dev(d["beta"], dt),
+                         dev(d["lam"], dt) if use_lam else None, dev(d["S0"], torch.float32), prologue=True)
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy(), S.cpu().numpy()
+
+
+@pytest.mark.parametrize("dt,dh,use_alpha,use_lam", [("bf16", 128, True, True), ("bf16", 128, False, False),
+                                                     ("f32", 64, True, True), ("f32", 32, True, False)])
+def test_prologue_forward_all_outputs(qd, dt, dh, use_alpha, use_lam):
+    """Forward from projections and logits (feature map and gates inside the kernel),
+    tensor-core (bf16, d=128) and CUDA-core (fp32) paths: 2 full chunks + a ragged tail."""
+    d = synth.qdelta_raw_inputs(2, 150, 2, dh, dh, seed=63, dtype=dt, s0_var=0.01)
+    o, S = run_prologue(qd, d, use_alpha, use_lam)
+    o_ref, S_ref = oracle.qdelta_fwd_prologue(d["q"], d["k"], d["v"], d["alpha"] if use_alpha else None, d["beta"],
+                                              d["lam"] if use_lam else None, d["S0"])
+    check(o, o_ref, dt, f"prologue {dt} o")
+    check(S, S_ref, dt, f"prologue {dt} S")
+
+
+def test_prologue_segmented_long_sequence(qd):
+    """B=1, H=2, T=4096 from projections through the segment scan (all passes apply
+    the prologue)."""
+    d = synth.qdelta_raw_inputs(1, 4096, 2, 128, 128, seed=64, dtype="bf16", s0_var=0.01)
+    o, S = run_prologue(qd, d)
+    assert qd.last_launch_count() == 4
+    o_ref, S_ref = oracle.qdelta_fwd_prologue(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["lam"], d["S0"])
+    check(o, o_ref, "bf16", "segmented prologue o")
+    check(S, S_ref, "bf16", "segmented prologue S")
+
+
+@pytest.mark.parametrize("dt,dh", [("f32", 64), ("bf16", 128)])
+def test_prologue_decode_steps(qd, dt, dh):
+    """Decode steps from projections and logits: 12 steps against the oracle's prologue
+    forward run token by token with the state carried."""
+    d = synth.qdelta_raw_inputs(3, 12, 2, dh, dh, seed=65, dtype=dt, s0_var=0.01)
+    tt = torch.bfloat16 if dt == "bf16" else torch.float32
+    S = dev(d["S0"], torch.float32)
+    S_ref = d["S0"].astype(np.float64).copy()
+    for t in range(12):
+        sl = slice(t, t + 1)
+        o = qd.qdelta_step(S, dev(d["q"][:, t], tt), dev(d["k"][:, t], tt), dev(d["v"][:, t], tt),
+                           dev(d["alpha"][:, t], tt), dev(d["beta"][:, t], tt), dev(d["lam"][:, t], tt), prologue=True)
+        o_ref, S_ref = oracle.qdelta_fwd_prologue(d["q"][:, sl], d["k"][:, sl], d["v"][:, sl], d["alpha"][:, sl],
+                                                  d["beta"][:, sl], d["lam"][:, sl], S_ref)
+        check(o.float().cpu().numpy(), o_ref[:, 0], dt, f"prologue step {t} o")
+    check(S.cpu().numpy(), S_ref, "f32", "prologue decode S")
+
+
 def _qed_step_call(qd, S, d, t, dt, variant):
     z = dev(d["z"], torch.float32) if variant == "rand" else None
     return qd.qed_step(S, dev(d["q"][t], dt), dev(d["k"][t], dt), dev(d["v"][t], dt), dev(d["g"][t], dt),
