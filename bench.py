@@ -14,6 +14,7 @@ B=8, H=16, T=2048, dk=dv=128, bf16 inputs, fp32 state, full Q-Delta gates
   decode   qdelta_step on 512 sequences x 16 heads (fp32 128x128 state), GB/s
   qed_decode  qed_step on the same shape, GB/s
   qed      qed_fwd at B=4, H=8, T=4096, d=128 bf16, tokens/s
+  prologue qdelta_fwd_prologue on the step's workload (projections and logits in)
   cpu_baseline  the fp64 oracle timed on this host's cores on a bounded sample
 
 --impl reference times the oracle itself (the CPU reference of this build) on
@@ -339,6 +340,30 @@ def time_qed(qd, steps=20, warmup=3):
             "tensor_TFLOPs": th * FLOPS_PER_TOKEN_HEAD / (ms * 1e-3) / 1e12}
 
 
+def time_prologue(qd, steps=20, warmup=3):
+    """qdelta_fwd_prologue on the headline workload: q, k projections and gate logits
+    in, feature map and gates computed inside the forward."""
+    import torch
+    d = synth.qdelta_raw_inputs(B, T, H, DK, DV, seed=7, dtype="bf16")
+    bf = torch.bfloat16
+    args = [to_dev(d[k], bf) for k in ("q", "k", "v", "alpha", "beta", "lam")]
+    o = torch.empty(B, T, H, DV, dtype=bf, device="cuda")
+    S = torch.empty(B, H, DV, DK, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        qd.qdelta_fwd(*args, None, o=o, S_final=S, stream=stream, prologue=True)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        qd.qdelta_fwd(*args, None, o=o, S_final=S, stream=stream, prologue=True)
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    return {"workload": f"qdelta_prologue_bf16_B{B}_H{H}_T{T}_d{DK}", "ms_per_step": ms,
+            "tokens_per_s": B * T / (ms * 1e-3), "GBps": ALG_BYTES / (ms * 1e-3) / 1e9}
+
+
 def oracle_sample(n_streams, seed=1, min_seconds=0.0):
     """Runs the fp64 oracle on n_streams (b, h) streams of the workload (full T) on
     all host cores, repeated until min_seconds have passed; returns
@@ -439,6 +464,7 @@ def main():
             qdec["frac_hbm"] = qdec["GBps"] / hbm_peak
             extras["qed_decode"] = qdec
             extras["qed"] = time_qed(qd)
+            extras["prologue"] = time_prologue(qd)
     del sets
     torch.cuda.synchronize()
 
