@@ -1,4 +1,5 @@
-"""Oracle: plain fp64 CPU reference of the Q-Delta / QED forwards and decode steps.
+"""Oracle: plain fp64 CPU reference of the Q-Delta / QED forwards, the Q-Delta
+backward and the decode steps.
 
 TEST INFRASTRUCTURE.  Only `tests/`, `__graft_entry__.smoke()` and `bench.py`'s
 CPU-baseline / reference leg may import this package.  It shares no code with
@@ -48,8 +49,9 @@ def _load():
         lib.oracle_qed_fwd_variant.argtypes = [I] * 5 + [P] * 7 + [I] + [P] * 4 + [I]
         lib.oracle_qed_step.argtypes = [I] * 4 + [P] * 8 + [I, P, P, I]
         lib.oracle_qdelta_fwd_prologue.argtypes = [I] * 5 + [P] * 9 + [I]
+        lib.oracle_qdelta_bwd.argtypes = [I] * 5 + [P] * 16 + [I]
         for f in (lib.oracle_qdelta_fwd, lib.oracle_qed_fwd, lib.oracle_qdelta_step, lib.oracle_qed_fwd_variant,
-                  lib.oracle_qed_step, lib.oracle_qdelta_fwd_prologue):
+                  lib.oracle_qed_step, lib.oracle_qdelta_fwd_prologue, lib.oracle_qdelta_bwd):
             f.restype = I
         _lib = lib
     return _lib
@@ -78,6 +80,24 @@ def qdelta_fwd(q, k, v, alpha, beta, lam, S0=None, nthreads: int = 0):
     if rc:
         raise MemoryError("oracle_qdelta_fwd failed")
     return o, S
+
+
+def qdelta_bwd(q, k, v, alpha, beta, lam, S0, dO, dS_final=None, nthreads: int = 0):
+    """Backward of qdelta_fwd: gradients of sum(dO * o) + sum(dS_final * S_final)
+    (dS_final None = 0).  Returns a dict dq, dk, dv, dalpha (None when alpha is None),
+    dbeta, dlam (None when lam is None), dS0, all fp64 in the inputs' shapes."""
+    q, k, v, alpha, beta, lam, S0, dO, dS_final = map(_f64, (q, k, v, alpha, beta, lam, S0, dO, dS_final))
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    g = {"dq": np.zeros_like(q), "dk": np.zeros_like(k), "dv": np.zeros_like(v),
+         "dalpha": None if alpha is None else np.zeros((B, T, H)), "dbeta": np.zeros((B, T, H)),
+         "dlam": None if lam is None else np.zeros((B, T, H)), "dS0": np.zeros((B, H, dv, dk))}
+    rc = _load().oracle_qdelta_bwd(B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(lam),
+                                   _ptr(S0), _ptr(dO), _ptr(dS_final), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
+                                   _ptr(g["dalpha"]), _ptr(g["dbeta"]), _ptr(g["dlam"]), _ptr(g["dS0"]), nthreads)
+    if rc:
+        raise MemoryError("oracle_qdelta_bwd failed")
+    return g
 
 
 def qed_fwd(q, k, v, g, b, w, lam_h, S0=None, nthreads: int = 0):

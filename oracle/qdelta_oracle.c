@@ -32,6 +32,15 @@
  *    with P(u) = u - k (k^T u).
  *  - Decode steps: one iteration of the Q-Delta or the QED loop per call, the
  *    state carried in and out in place.
+ *  - Backward of the Q-Delta forward: the gradients of the scalar
+ *    L = sum_t <dO_t, o_t> + <dS_final, S_T> with respect to q, k, v, alpha, beta,
+ *    lambda and S0, by reverse-mode differentiation of the sequential recurrence
+ *    above, one step at a time in reverse (the pages train the layer end to end,
+ *    "Parallelizing Linear Transformers with the Delta Rule over Sequence Length",
+ *    sec. 3, but print no backward; this is the adjoint of the stated forward).
+ *    Rows of S evolve independently given a token's q, k and gates, so each row's
+ *    states are recorded and walked back on their own; the row contributions to the
+ *    shared gradients are summed.
  *  - Prologue (the feature map and gates computed from the layer's projections):
  *    DeltaNet notes sec. 3.8, q = SiLU(x_q)/|SiLU(x_q)|_2 and the same for k,
  *    beta = sigmoid(x_beta); Q-Delta notes sec. 2.5 (App. B), lambda = sigmoid(x_lambda);
@@ -60,7 +69,9 @@ typedef struct {
     const double *z;                                 /* rand arm: z_h [H][dk] */
     const double *S0;
     double *o, *S_final;
-    int method;          /* 0 = Q-Delta, 1 = QED */
+    const double *dO, *dS_final;                     /* backward: incoming gradients */
+    double *dq, *dk_out, *dv_out, *dalpha, *dbeta, *dlam, *dS0;
+    int method;          /* 0 = Q-Delta, 1 = QED, 2 = Q-Delta backward */
     int first, stride;   /* this worker's (b,h) streams: first, first+stride, ... */
     int status;
 } job_t;
@@ -107,6 +118,85 @@ static int qdelta_stream(const job_t *J, int b, int h)
     }
     if (J->S_final) memcpy(J->S_final + sh, S, sizeof(double) * (size_t)dv * dk);
     free(S); free(x); free(e);
+    return 0;
+}
+
+/* Backward of one Q-Delta stream (b, h).  For row i of S (s = S[i][:]):
+ *   forward   sbar_t = alpha_t s_{t-1},  e_t = v_t[i] - sbar_t . x_t,
+ *             s_t = sbar_t + beta_t e_t k_t,  o_t[i] = s_t . q_t
+ *   adjoint   g = dL/ds_t, walked from t = T-1 down to 0:
+ *             g += dO_t[i] q_t                       dq_t += dO_t[i] s_t
+ *             ge = beta_t (g . k_t)  (dL/de_t)       dbeta_t += e_t (g . k_t)
+ *             dk_t += beta_t e_t g                   dv_t[i] = ge
+ *             gbar = g - ge x_t      (dL/dsbar_t)    dx = -ge sbar_t
+ *             dk_t += dx,  dq_t += lambda_t dx,      dlambda_t += q_t . dx
+ *             dalpha_t += gbar . s_{t-1}             g = alpha_t gbar
+ *   and dS0[i] = g at the end. */
+static int qdelta_bwd_stream(const job_t *J, int b, int h)
+{
+    const int T = J->T, H = J->H, dk = J->dk, dv = J->dv;
+    double *hist = malloc(sizeof(double) * (size_t)(T + 1) * dk);   /* s_0 .. s_T of one row */
+    double *x = malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * dk);
+    double *e = malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+    double *g = malloc(sizeof(double) * (size_t)dk), *gbar = malloc(sizeof(double) * (size_t)dk);
+    if (!hist || !x || !e || !g || !gbar) { free(hist); free(x); free(e); free(g); free(gbar); return 1; }
+    const size_t sh = ((size_t)b * H + h) * dv * dk;
+
+    for (int t = 0; t < T; ++t) {                                         /* x_t = k_t + lambda_t q_t */
+        const size_t tok = ((size_t)b * T + t) * H + h;
+        const double lam = J->lam ? J->lam[tok] : 0.0;
+        for (int j = 0; j < dk; ++j) x[(size_t)t * dk + j] = J->k[tok * dk + j] + lam * J->q[tok * dk + j];
+    }
+    for (int i = 0; i < dv; ++i) {
+        /* forward, recording this row's states */
+        for (int j = 0; j < dk; ++j) hist[j] = J->S0 ? J->S0[sh + (size_t)i * dk + j] : 0.0;
+        for (int t = 0; t < T; ++t) {
+            const size_t tok = ((size_t)b * T + t) * H + h;
+            const double alpha = J->alpha ? J->alpha[tok] : 1.0;
+            const double *sp = hist + (size_t)t * dk, *xt = x + (size_t)t * dk, *kt = J->k + tok * dk;
+            double *sn = hist + (size_t)(t + 1) * dk;
+            double acc = 0.0;
+            for (int j = 0; j < dk; ++j) acc += alpha * sp[j] * xt[j];
+            e[t] = J->v[tok * dv + i] - acc;
+            for (int j = 0; j < dk; ++j) sn[j] = alpha * sp[j] + J->beta[tok] * e[t] * kt[j];
+        }
+        /* adjoint, t = T-1 .. 0 */
+        for (int j = 0; j < dk; ++j) g[j] = J->dS_final ? J->dS_final[sh + (size_t)i * dk + j] : 0.0;
+        for (int t = T - 1; t >= 0; --t) {
+            const size_t tok = ((size_t)b * T + t) * H + h;
+            const double alpha = J->alpha ? J->alpha[tok] : 1.0;
+            const double beta = J->beta[tok];
+            const double lam = J->lam ? J->lam[tok] : 0.0;
+            const double *qt = J->q + tok * dk, *kt = J->k + tok * dk, *xt = x + (size_t)t * dk;
+            const double *sp = hist + (size_t)t * dk, *sn = hist + (size_t)(t + 1) * dk;
+            double *dqt = J->dq + tok * dk, *dkt = J->dk_out + tok * dk;
+            const double dot = J->dO[tok * dv + i];
+            for (int j = 0; j < dk; ++j) {                                /* o_t[i] = s_t . q_t */
+                g[j] += dot * qt[j];
+                dqt[j] += dot * sn[j];
+            }
+            double gk = 0.0;
+            for (int j = 0; j < dk; ++j) gk += g[j] * kt[j];
+            const double ge = beta * gk;                                  /* s_t = sbar + beta e k */
+            J->dbeta[tok] += e[t] * gk;
+            for (int j = 0; j < dk; ++j) dkt[j] += beta * e[t] * g[j];
+            J->dv_out[tok * dv + i] = ge;                                 /* e = v - sbar . x */
+            double dlam = 0.0, dal = 0.0;
+            for (int j = 0; j < dk; ++j) {
+                gbar[j] = g[j] - ge * xt[j];
+                const double dx = -ge * alpha * sp[j];
+                dkt[j] += dx;                                             /* x = k + lambda q */
+                dqt[j] += lam * dx;
+                dlam += qt[j] * dx;
+                dal += gbar[j] * sp[j];                                   /* sbar = alpha s_{t-1} */
+            }
+            if (J->dlam) J->dlam[tok] += dlam;
+            if (J->dalpha) J->dalpha[tok] += dal;
+            for (int j = 0; j < dk; ++j) g[j] = alpha * gbar[j];
+        }
+        if (J->dS0) for (int j = 0; j < dk; ++j) J->dS0[sh + (size_t)i * dk + j] = g[j];
+    }
+    free(hist); free(x); free(e); free(g); free(gbar);
     return 0;
 }
 
@@ -177,7 +267,8 @@ static void *worker(void *arg)
     const int n = J->B * J->H;
     for (int s = J->first; s < n; s += J->stride) {
         const int b = s / J->H, h = s % J->H;
-        int rc = J->method == 0 ? qdelta_stream(J, b, h) : qed_stream(J, b, h);
+        int rc = J->method == 0 ? qdelta_stream(J, b, h)
+               : J->method == 1 ? qed_stream(J, b, h) : qdelta_bwd_stream(J, b, h);
         if (rc) J->status = rc;
     }
     return NULL;
@@ -225,6 +316,35 @@ int oracle_qdelta_fwd(int B, int T, int H, int dk, int dv,
     J.B = B; J.T = T; J.H = H; J.dk = dk; J.dv = dv;
     J.q = q; J.k = k; J.v = v; J.alpha = alpha; J.beta = beta; J.lam = lam;
     J.S0 = S0; J.o = o; J.S_final = S_final; J.method = 0;
+    return run(&J, nthreads);
+}
+
+/* Q-Delta backward.  dO [B][T][H][dv]; dS_final [B][H][dv][dk] or NULL (= 0).
+ * Gradients: dq, dk [B][T][H][dk], dv [B][T][H][dv], dalpha, dbeta, dlam [B][T][H],
+ * dS0 [B][H][dv][dk].  dalpha (dlam) must be NULL when alpha (lam) is NULL and is
+ * then not computed; dS0 may be NULL.  All outputs are overwritten. */
+int oracle_qdelta_bwd(int B, int T, int H, int dk, int dv,
+                      const double *q, const double *k, const double *v,
+                      const double *alpha, const double *beta, const double *lam, const double *S0,
+                      const double *dO, const double *dS_final,
+                      double *dq, double *dk_out, double *dv_out, double *dalpha, double *dbeta,
+                      double *dlam, double *dS0, int nthreads)
+{
+    if ((dalpha && !alpha) || (dlam && !lam)) return 2;
+    const size_t nt = (size_t)B * T * H;
+    memset(dq, 0, sizeof(double) * nt * dk);
+    memset(dk_out, 0, sizeof(double) * nt * dk);
+    memset(dv_out, 0, sizeof(double) * nt * dv);
+    memset(dbeta, 0, sizeof(double) * nt);
+    if (dalpha) memset(dalpha, 0, sizeof(double) * nt);
+    if (dlam) memset(dlam, 0, sizeof(double) * nt);
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.B = B; J.T = T; J.H = H; J.dk = dk; J.dv = dv;
+    J.q = q; J.k = k; J.v = v; J.alpha = alpha; J.beta = beta; J.lam = lam; J.S0 = S0;
+    J.dO = dO; J.dS_final = dS_final;
+    J.dq = dq; J.dk_out = dk_out; J.dv_out = dv_out; J.dalpha = dalpha; J.dbeta = dbeta; J.dlam = dlam;
+    J.dS0 = dS0; J.method = 2;
     return run(&J, nthreads);
 }
 

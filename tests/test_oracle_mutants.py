@@ -241,3 +241,89 @@ def test_oracle_passes_prologue_pins():
 @pytest.mark.parametrize("kind", ["silu_sign", "l1_norm", "alpha_sigmoid"])
 def test_prologue_mutant_rejected(kind):
     assert not prologue_pins_hold(_prologue_mutant(kind))
+
+
+# ---------------------------------------------------------------- backward
+
+def _bwd_rowwise(kind=None):
+    """Single-stream adjoint (B = H = 1), row by row, with an optional planted mistake."""
+    def bwd(q, k, v, al, be, lm, S0, dO, dS):
+        T, dk = q.shape
+        dv = v.shape[1]
+        x = k + lm[:, None] * q
+        g = {"dq": np.zeros_like(q), "dk": np.zeros_like(k), "dv": np.zeros_like(v),
+             "dalpha": np.zeros(T), "dbeta": np.zeros(T), "dlam": np.zeros(T), "dS0": np.zeros_like(S0)}
+        for i in range(dv):
+            hist, e = [S0[i].copy()], np.zeros(T)
+            for t in range(T):
+                sb = al[t] * hist[-1]
+                e[t] = v[t, i] - sb @ x[t]
+                hist.append(sb + be[t] * e[t] * k[t])
+            gs = dS[i].copy()
+            for t in range(T - 1, -1, -1):
+                gs = gs + dO[t, i] * q[t]
+                g["dq"][t] += dO[t, i] * hist[t + 1]
+                gk = gs @ k[t]
+                ge = be[t] * gk
+                g["dbeta"][t] += (v[t, i] if kind == "dbeta_uses_value" else e[t]) * gk
+                if kind != "dk_drops_write_term":
+                    g["dk"][t] += be[t] * e[t] * gs
+                g["dv"][t, i] = ge
+                gbar = gs - ge * x[t]
+                dx = (1 if kind == "dx_sign" else -1) * ge * al[t] * hist[t]
+                g["dk"][t] += dx
+                if kind != "dq_drops_lambda_term":
+                    g["dq"][t] += lm[t] * dx
+                g["dlam"][t] += q[t] @ dx
+                g["dalpha"][t] += gbar @ (hist[t + 1] if kind == "dalpha_new_state" else hist[t])
+                gs = gbar if kind == "carry_without_decay" else al[t] * gbar
+            g["dS0"][i] = gs
+        return g
+    return bwd
+
+
+def backward_pins_hold(bwd):
+    """Central differences of the pinned forward oracle (the backward's pin)."""
+    T, dk, dv = 6, 4, 3
+    q, k = rng.standard_normal((T, dk)), rng.standard_normal((T, dk))
+    v = rng.standard_normal((T, dv))
+    al, be, lm = rng.uniform(0.5, 1.0, T), rng.uniform(0.1, 0.9, T), rng.uniform(0.1, 0.9, T)
+    S0, dS = rng.standard_normal((dv, dk)), rng.standard_normal((dv, dk))
+    dO = rng.standard_normal((T, dv))
+    g = bwd(q, k, v, al, be, lm, S0, dO, dS)
+    ex = lambda a: a[None, :, None]
+    args = {"q": q, "k": k, "v": v, "alpha": al, "beta": be, "lam": lm, "S0": S0}
+
+    def loss(a):
+        o, S = oracle.qdelta_fwd(ex(a["q"]), ex(a["k"]), ex(a["v"]), ex(a["alpha"]), ex(a["beta"]),
+                                 ex(a["lam"]), a["S0"][None, None])
+        return (o[0, :, 0] * dO).sum() + (S[0, 0] * dS).sum()
+
+    for name, x in args.items():
+        for idx in np.ndindex(x.shape):
+            a = dict(args)
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += 1e-6
+            xm[idx] -= 1e-6
+            a[name] = xp
+            lp = loss(a)
+            a[name] = xm
+            fd = (lp - loss(a)) / 2e-6
+            if abs(g["d" + name][idx] - fd) > 1e-6 * max(1.0, abs(fd)):
+                return False
+    return True
+
+
+def test_oracle_and_rowwise_adjoint_pass_backward_pins():
+    def via_oracle(q, k, v, al, be, lm, S0, dO, dS):
+        ex = lambda a: a[None, :, None]
+        g = oracle.qdelta_bwd(ex(q), ex(k), ex(v), ex(al), ex(be), ex(lm), S0[None, None], ex(dO), dS[None, None])
+        return {n: (a[0, :, 0] if n != "dS0" else a[0, 0]) for n, a in g.items()}
+    assert backward_pins_hold(via_oracle)
+    assert backward_pins_hold(_bwd_rowwise())
+
+
+@pytest.mark.parametrize("kind", ["dbeta_uses_value", "dk_drops_write_term", "dx_sign", "dq_drops_lambda_term",
+                                  "dalpha_new_state", "carry_without_decay"])
+def test_backward_mutant_rejected(kind):
+    assert not backward_pins_hold(_bwd_rowwise(kind))

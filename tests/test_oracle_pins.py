@@ -567,3 +567,115 @@ def test_heads_and_batches_independent_and_thread_count_invariant():
     sl = lambda x: x[b:b + 1, :, h:h + 1]
     o1, S1 = oracle.qdelta_fwd(sl(q), sl(k), sl(v), sl(alpha), sl(beta), sl(lam), S0[b:b + 1, h:h + 1])
     assert np.array_equal(o1[0, :, 0], o[b, :, h]) and np.array_equal(S1[0, 0], S[b, h])
+
+
+# ---------------------------------------------------------------- backward
+
+def _loss(q, k, v, alpha, beta, lam, S0, dO, dS):
+    o, S = oracle.qdelta_fwd(q, k, v, alpha, beta, lam, S0)
+    return float((o * dO).sum() + (S * dS).sum())
+
+
+def finite_difference_grads(q, k, v, alpha, beta, lam, S0, dO, dS, h=1e-6):
+    """Central differences of L = <dO, o> + <dS, S_T> through the (pinned) forward
+    oracle, for every element of every input."""
+    args = {"q": q, "k": k, "v": v, "alpha": alpha, "beta": beta, "lam": lam, "S0": S0}
+    out = {}
+    for name, x in args.items():
+        if x is None:
+            continue
+        fd = np.zeros_like(x)
+        for i in np.ndindex(x.shape):
+            a = dict(args)
+            xp, xm = x.copy(), x.copy()
+            xp[i] += h
+            xm[i] -= h
+            a[name] = xp
+            lp = _loss(**a, dO=dO, dS=dS)
+            a[name] = xm
+            lm = _loss(**a, dO=dO, dS=dS)
+            fd[i] = (lp - lm) / (2 * h)
+        out["d" + name] = fd
+    return out
+
+
+@pytest.mark.parametrize("mode", ["qdelta", "gdn", "deltanet"])
+def test_backward_equals_finite_differences(mode):
+    """Every gradient of the backward oracle is the derivative of the forward oracle
+    (central differences, h = 1e-6; truncation ~1e-12, cancellation ~1e-10)."""
+    q, k, v, alpha, beta, lam, S0 = _rand_qdelta(1, 7, 2, 4, 3, gated=mode != "deltanet", lam=mode == "qdelta",
+                                                 unit=False)
+    alpha = None if alpha is None else rng.uniform(0.5, 1.0, alpha.shape)
+    dO = rng.standard_normal(v.shape)
+    dS = rng.standard_normal(S0.shape)
+    g = oracle.qdelta_bwd(q, k, v, alpha, beta, lam, S0, dO, dS)
+    fd = finite_difference_grads(q, k, v, alpha, beta, lam, S0, dO, dS)
+    for name, ref in fd.items():
+        np.testing.assert_allclose(g[name], ref, atol=1e-6 * max(1.0, np.abs(ref).max()), err_msg=name)
+    assert (g["dalpha"] is None) == (alpha is None) and (g["dlam"] is None) == (lam is None)
+
+
+def test_backward_linear_in_values_and_initial_state():
+    """o and S_T are jointly linear in (v, S0) (each step is S_prior (I - beta x k^T)
+    + beta v k^T), so by Euler's identity <dv, v> + <dS0, S0> = L exactly."""
+    q, k, v, alpha, beta, lam, S0 = _rand_qdelta(2, 23, 3, 8, 6)
+    dO, dS = rng.standard_normal(v.shape), rng.standard_normal(S0.shape)
+    g = oracle.qdelta_bwd(q, k, v, alpha, beta, lam, S0, dO, dS)
+    L = _loss(q, k, v, alpha, beta, lam, S0, dO, dS)
+    assert abs((g["dv"] * v).sum() + (g["dS0"] * S0).sum() - L) <= 1e-11 * max(1.0, abs(L))
+
+
+def test_backward_linear_in_queries_without_lambda():
+    """lambda = 0: the states do not depend on q and o_t = S_t q_t is linear in it,
+    so <dq, q> = <dO, o> (with lambda != 0 the identity fails, as x carries q)."""
+    q, k, v, alpha, beta, _, S0 = _rand_qdelta(2, 17, 2, 8, 5, lam=False)
+    dO = rng.standard_normal(v.shape)
+    o, _ = oracle.qdelta_fwd(q, k, v, alpha, beta, None, S0)
+    g = oracle.qdelta_bwd(q, k, v, alpha, beta, None, S0, dO)
+    ref = (dO * o).sum()
+    assert abs((g["dq"] * q).sum() - ref) <= 1e-12 * max(1.0, abs(ref))
+    lam = rng.uniform(0.2, 0.8, beta.shape)
+    o2, _ = oracle.qdelta_fwd(q, k, v, alpha, beta, lam, S0)
+    g2 = oracle.qdelta_bwd(q, k, v, alpha, beta, lam, S0, dO)
+    assert abs((g2["dq"] * q).sum() - (dO * o2).sum()) > 1e-6
+
+
+def test_backward_beta_zero_closed_form():
+    """beta = 0: S_t = gamma_t S0.  The gradient reaching S_t is
+    G_t = sum_{tau>=t} (gamma_tau/gamma_t) dO_tau q_tau^T + (gamma_T/gamma_t) dS_T, so
+    dbeta_t = e_t^T G_t k_t with e_t = v_t - gamma_t S0 x_t; dq_t = gamma_t S0^T dO_t;
+    dk = dv = dlambda = 0; alpha_j dalpha_j = sum_{t>=j} gamma_t <dO_t, S0 q_t>
+    + gamma_T <dS_T, S0>; dS0 = sum_t gamma_t dO_t q_t^T + gamma_T dS_T."""
+    B, T, H, dk, dv = 1, 9, 2, 5, 4
+    q, k, v, alpha, beta, lam, S0 = _rand_qdelta(B, T, H, dk, dv)
+    beta = np.zeros_like(beta)
+    dO, dS = rng.standard_normal(v.shape), rng.standard_normal(S0.shape)
+    g = oracle.qdelta_bwd(q, k, v, alpha, beta, lam, S0, dO, dS)
+    for h in range(H):
+        gam = np.cumprod(alpha[0, :, h])
+        S0h, dSh = S0[0, h], dS[0, h]
+        Q, K, V, dOh = q[0, :, h], k[0, :, h], v[0, :, h], dO[0, :, h]
+        X = K + lam[0, :, h, None] * Q
+        for t in range(T):
+            G = sum(gam[u] / gam[t] * np.outer(dOh[u], Q[u]) for u in range(t, T)) + gam[-1] / gam[t] * dSh
+            e = V[t] - gam[t] * S0h @ X[t]
+            assert abs(g["dbeta"][0, t, h] - e @ G @ K[t]) <= 1e-12 * max(1.0, abs(e @ G @ K[t]))
+            np.testing.assert_allclose(g["dq"][0, t, h], gam[t] * S0h.T @ dOh[t], atol=1e-13)
+            ref = sum(gam[u] * dOh[u] @ S0h @ Q[u] for u in range(t, T)) + gam[-1] * (dSh * S0h).sum()
+            assert abs(alpha[0, t, h] * g["dalpha"][0, t, h] - ref) <= 1e-12 * max(1.0, abs(ref))
+        dS0 = sum(gam[u] * np.outer(dOh[u], Q[u]) for u in range(T)) + gam[-1] * dSh
+        np.testing.assert_allclose(g["dS0"][0, h], dS0, atol=1e-13)
+    assert np.all(g["dk"] == 0) and np.all(g["dv"] == 0) and np.all(g["dlam"] == 0)
+
+
+def test_backward_streams_independent_and_thread_count_invariant():
+    q, k, v, alpha, beta, lam, S0 = _rand_qdelta(2, 11, 3, 6, 5)
+    dO, dS = rng.standard_normal(v.shape), rng.standard_normal(S0.shape)
+    g1 = oracle.qdelta_bwd(q, k, v, alpha, beta, lam, S0, dO, dS, nthreads=1)
+    g4 = oracle.qdelta_bwd(q, k, v, alpha, beta, lam, S0, dO, dS, nthreads=4)
+    one = oracle.qdelta_bwd(q[1:, :, 2:], k[1:, :, 2:], v[1:, :, 2:], alpha[1:, :, 2:], beta[1:, :, 2:],
+                            lam[1:, :, 2:], S0[1:, 2:], dO[1:, :, 2:], dS[1:, 2:])
+    for name in g1:
+        assert np.array_equal(g1[name], g4[name]), name
+    np.testing.assert_array_equal(one["dq"], g1["dq"][1:, :, 2:])
+    np.testing.assert_array_equal(one["dS0"], g1["dS0"][1:, 2:])
