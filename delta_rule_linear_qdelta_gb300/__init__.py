@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "QD_OK", 1: "QD_ERR_ARG", 2: "QD_ERR_UNSUPPORTED", 3: "QD_ERR
                 4: "QD_ERR_TIMEOUT", 5: "QD_ERR_WORKSPACE"}
 EXPORTS = ("qdelta_fwd", "qdelta_fwd_prologue", "qdelta_workspace_bytes", "qed_fwd", "qed_fwd_variant",
            "qed_workspace_bytes", "qdelta_step", "qdelta_step_prologue", "qed_step", "qdelta_fwd_static_scratch",
-           "qd_device_status", "qd_last_error", "qd_last_launch_count")
+           "qdelta_bwd", "qdelta_bwd_workspace_bytes", "qd_device_status", "qd_last_error",
+           "qd_last_launch_count")
 QED_VARIANTS = {"full": 0, "nogate": 1, "nogate_noproj": 2, "rand": 3}
 
 
@@ -59,13 +60,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qed_step.argtypes = [P] * 9 + [I] * 6 + [P, P]
     lib.qdelta_workspace_bytes.argtypes = [I] * 7
     lib.qed_workspace_bytes.argtypes = [I] * 7
+    lib.qdelta_bwd.argtypes = [P] * 16 + [I] * 7 + [P, Z, P]
+    lib.qdelta_bwd_workspace_bytes.argtypes = [I] * 7
     lib.qd_device_status.argtypes = [P]
     for f in (lib.qdelta_fwd, lib.qed_fwd, lib.qdelta_step, lib.qdelta_fwd_static_scratch, lib.qd_device_status,
               lib.qd_last_launch_count, lib.qed_fwd_variant, lib.qed_step, lib.qdelta_fwd_prologue,
-              lib.qdelta_step_prologue):
+              lib.qdelta_step_prologue, lib.qdelta_bwd):
         f.restype = I
     lib.qdelta_workspace_bytes.restype = Z
     lib.qed_workspace_bytes.restype = Z
+    lib.qdelta_bwd_workspace_bytes.restype = Z
     lib.qd_last_error.restype = ctypes.c_char_p
     lib.qd_last_error.argtypes = []
     lib.qd_last_launch_count.argtypes = []
@@ -169,6 +173,43 @@ def qdelta_fwd(q, k, v, alpha, beta, lam, S0=None, *, o=None, S_final=None, retu
             B, T, H, dk, dv, chunk, code, _ptr(workspace), wsb, _stream(stream, q.device))
     _check(st, "qdelta_fwd_prologue" if prologue else "qdelta_fwd")
     return o, S_final
+
+
+def qdelta_bwd_workspace_bytes(B, T, H, dk, dv, chunk=64, dtype=QD_BF16) -> int:
+    return load_library().qdelta_bwd_workspace_bytes(B, T, H, dk, dv, chunk, dtype)
+
+
+def qdelta_bwd(q, k, v, alpha, beta, lam, S0, dO, dS_final=None, *, want_dS0=True, chunk=64, workspace=None,
+               stream=None):
+    """Backward of qdelta_fwd: gradients of sum(dO * o) + sum(dS_final * S_final)
+    (the C qdelta_bwd).  Inputs as for qdelta_fwd, dO [B,T,H,dv] in the inputs' dtype,
+    dS_final [B,H,dv,dk] fp32 or None.  Returns a dict dq, dk, dv, dalpha (None when
+    alpha is None), dbeta, dlam (None when lam is None), dS0 (fp32; None unless
+    want_dS0), the token and gate gradients in the inputs' dtype."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    _need(q, "q", dt, (B, T, H, dk))
+    _need(k, "k", dt, (B, T, H, dk))
+    _need(v, "v", dt, (B, T, H, dv))
+    _need(beta, "beta", dt, (B, T, H))
+    _need(alpha, "alpha", dt, (B, T, H), optional=True)
+    _need(lam, "lam", dt, (B, T, H), optional=True)
+    _need(S0, "S0", torch.float32, (B, H, dv, dk), optional=True)
+    _need(dO, "dO", dt, (B, T, H, dv))
+    _need(dS_final, "dS_final", torch.float32, (B, H, dv, dk), optional=True)
+    g = {"dq": torch.empty_like(q), "dk": torch.empty_like(k), "dv": torch.empty_like(v),
+         "dalpha": None if alpha is None else torch.empty_like(alpha), "dbeta": torch.empty_like(beta),
+         "dlam": None if lam is None else torch.empty_like(lam),
+         "dS0": torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device) if want_dS0 else None}
+    code = _dtype_code(q)
+    workspace, wsb = _workspace(qdelta_bwd_workspace_bytes(B, T, H, dk, dv, chunk, code), workspace, q.device)
+    st = load_library().qdelta_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(lam), _ptr(S0),
+                                   _ptr(dO), _ptr(dS_final), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
+                                   _ptr(g["dalpha"]), _ptr(g["dbeta"]), _ptr(g["dlam"]), _ptr(g["dS0"]),
+                                   B, T, H, dk, dv, chunk, code, _ptr(workspace), wsb, _stream(stream, q.device))
+    _check(st, "qdelta_bwd")
+    return g
 
 
 def qdelta_fwd_static_scratch(q, k, v, alpha, beta, lam, S0=None, *, o=None, S_final=None, return_final=True,

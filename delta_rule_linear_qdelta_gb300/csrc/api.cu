@@ -81,6 +81,39 @@ size_t qed_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dt
     return qd::qdelta_segment_workspace(B, H, qd::qed_segments(B, T, H, dk, dv, dtype));
 }
 
+size_t qdelta_bwd_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype) {
+    (void)dtype;
+    if (B <= 0 || T <= 0 || H <= 0 || chunk != 64 || !head_dim_ok(dk) || !head_dim_ok(dv)) return 0;
+    return qd::qdelta_bwd_workspace(B, T, H, dk, dv);
+}
+
+qd_status qdelta_bwd(const void *q, const void *k, const void *v, const void *alpha, const void *beta,
+                     const void *lam, const float *S0, const void *dO, const float *dS_final, void *dq,
+                     void *dk_out, void *dv_out, void *dalpha, void *dbeta, void *dlam, float *dS0, int B, int T,
+                     int H, int dk, int dv, int chunk, qd_dtype dtype, void *workspace, size_t workspace_bytes,
+                     cudaStream_t stream) {
+    g_err[0] = 0;
+    const void *req[] = {q, k, v, beta, dO, dq, dk_out, dv_out, dbeta};
+    const void *opt[] = {alpha, lam, S0, dS_final, dalpha, dlam, dS0, workspace};
+    qd_status st = check_fwd("qdelta_bwd", req, 9, opt, 8, B, T, H, dk, dv, chunk, dtype);
+    if (st != QD_OK) return st;
+    if ((double)B * H * ((T + 63) / 64) > 2147483647.0) return fail(QD_ERR_ARG, "qdelta_bwd: B*H*chunks exceeds the grid limit");
+    if (B == 0 || H == 0) { g_launches = 0; return QD_OK; }
+    if (T == 0) { g_launches = 0; return empty_sequence(dS_final, dS0, B, H, dk, dv, stream); }
+    const size_t need = qdelta_bwd_workspace_bytes(B, T, H, dk, dv, chunk, dtype);
+    if (!workspace || workspace_bytes < need)
+        return fail(QD_ERR_WORKSPACE, "qdelta_bwd: workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+    float *chk = static_cast<float *>(workspace);
+    const size_t half = need / 2 / sizeof(float);
+    qd::QDeltaBwdArgs a{q, k, v, alpha, beta, lam, S0, dO, dS_final, dq, dk_out, dv_out, dalpha, dbeta, dlam,
+                        dS0, B, T, H, dk, dv, chk, chk + half};
+    int n = 0;
+    cudaError_t e = qd::launch_qdelta_bwd(a, dtype, stream, &n);
+    if (e != cudaSuccess) return cuda_fail(e, "qdelta_bwd launch");
+    g_launches = n;
+    return QD_OK;
+}
+
 }  // extern "C"
 
 namespace {

@@ -96,9 +96,14 @@ __global__ void __launch_bounds__(kNT) qdelta_chunk_simt_kernel(QDeltaArgs a) {
         Ss[d * LK + j] = a.S0 ? a.S0[s_base + (size_t)d * DK + j] : 0.f;
     }
 
+    const int nchunk = (T + C - 1) / C;
     for (int c0 = 0; c0 < T; c0 += C) {
         const int n = min(C, T - c0);
         __syncthreads();
+        if (a.S_chk) {                                    // checkpoint: the state entering this chunk
+            float *chk = a.S_chk + ((size_t)bh * nchunk + c0 / C) * dv * DK + (size_t)d0 * DK;
+            for (int idx = tid; idx < DVT * DK; idx += kNT) chk[idx] = Ss[(idx / DK) * LK + idx % DK];
+        }
         for (int idx = tid; idx < C * DK; idx += kNT) {
             const int t = idx / DK, j = idx % DK;
             const size_t tok = ((size_t)b * T + c0 + t) * H + h;
@@ -185,10 +190,10 @@ __global__ void __launch_bounds__(kNT) qdelta_chunk_simt_kernel(QDeltaArgs a) {
         __syncthreads();
         forward_substitute<DVT>(Am, Zs);
         __syncthreads();
-        // O = gamma Q S^T + P Z
+        // O = gamma Q S^T + P Z  (skipped when only the states are wanted)
         for (int idx = tid; idx < C * DVT; idx += kNT) {
             const int t = idx / DVT, d = idx % DVT;
-            if (t < n) {
+            if (t < n && o) {
                 float acc = Ws[t * LV + d];
                 const float *pt = Pm + t * LC;
                 for (int i = 0; i <= t; ++i) acc = fmaf(pt[i], Zs[i * LV + d], acc);

@@ -50,6 +50,23 @@ struct QDeltaArgs {
     void *ws;
     size_t ws_bytes;
     int prologue;     // q, k, alpha, beta, lam are projections and logits (qdelta_fwd_prologue)
+    float *S_chk;     // CUDA-core path only: if set, the state entering every chunk of 64
+                      // tokens, [B*H][ceil(T/64)][dv][dk] fp32 (the backward's checkpoints)
+};
+
+// Arguments of one Q-Delta backward (layouts as in include/qdelta.h); nk, nv are
+// d_k, d_v.  S_chk and dS_chk are the two checkpoint arrays in the workspace, each
+// [B*H][ceil(T/64)][dv][dk] fp32: the state entering each chunk and the gradient
+// reaching the state leaving it.
+struct QDeltaBwdArgs {
+    const void *q, *k, *v, *alpha, *beta, *lam;
+    const float *S0;
+    const void *dO;
+    const float *dS_final;
+    void *dq, *dk, *dv, *dalpha, *dbeta, *dlam;
+    float *dS0;
+    int B, T, H, nk, nv;
+    float *S_chk, *dS_chk;
 };
 
 // QED ablation arms ("The Query Knows What to Forget", Table 1): the term added to
@@ -93,6 +110,10 @@ struct StepArgs {
 
 // Launchers.  Each returns the first CUDA error and adds its launches to *nlaunch.
 cudaError_t launch_qdelta_chunk_simt(const QDeltaArgs &a, int dtype, cudaStream_t s, int *nlaunch);
+// Backward of the chunked forward: checkpoint forward, reverse state-gradient sweep and
+// the per-chunk gradient kernel.  qdelta_bwd_workspace is the workspace it needs.
+size_t qdelta_bwd_workspace(int B, int T, int H, int dk, int dv);
+cudaError_t launch_qdelta_bwd(const QDeltaBwdArgs &a, int dtype, cudaStream_t s, int *nlaunch);
 cudaError_t launch_qed_chunk_simt(const QedArgs &a, int dtype, cudaStream_t s, int *nlaunch);
 cudaError_t launch_qdelta_step(const StepArgs &a, int dtype, cudaStream_t s, int *nlaunch);
 cudaError_t launch_qed_step(const QedStepArgs &a, int dtype, cudaStream_t s, int *nlaunch);

@@ -1,5 +1,6 @@
 /*
- * qdelta.h -- C ABI of the GB300 (sm_103a) Q-Delta / QED forward and decode step.
+ * qdelta.h -- C ABI of the GB300 (sm_103a) Q-Delta / QED forward, the Q-Delta
+ * backward and the decode steps.
  *
  * Every entry point takes plain device pointers and sizes; no C++ or framework
  * types cross this boundary.  All device buffers are owned by the caller.  Every
@@ -183,6 +184,39 @@ QD_API qd_status qdelta_fwd_prologue(const void *q_raw, const void *k_raw, const
 QD_API qd_status qdelta_step_prologue(float *S, const void *q_raw, const void *k_raw, const void *v,
                                       const void *a_logit, const void *b_logit, const void *l_logit, void *o,
                                       int N, int H, int dk, int dv, qd_dtype dtype, cudaStream_t stream);
+
+/*
+ * qdelta_bwd -- backward of qdelta_fwd: the gradients of
+ *     L = sum_{b,t,h} <dO_t, o_t> + sum_{b,h} <dS_final, S_T>
+ * with respect to q, k, v, alpha, beta, lam and S0, i.e. the adjoint of the
+ * recurrence qdelta_fwd computes (Sec. 3.3.1 of the Q-Delta notes, chunked as in
+ * Sec. 3.3.2).  The pages train the layer end to end ("Parallelizing Linear
+ * Transformers with the Delta Rule over Sequence Length", sec. 3) but state no
+ * backward; this is the derivative of the stated forward.
+ *
+ * Inputs: q, k, v, alpha, beta, lam, S0, dtype, sizes exactly as passed to
+ * qdelta_fwd (alpha NULL = 1, lam NULL = 0, S0 NULL = 0); dO [B][T][H][dv] in the
+ * call's dtype; dS_final [B][H][dv][dk] fp32 or NULL (= 0).
+ * Outputs, each overwritten, in the call's dtype unless stated:
+ *   dq, dk [B][T][H][dk]; dv [B][T][H][dv]; dbeta [B][T][H]   (required)
+ *   dalpha [B][T][H]: written when alpha and dalpha are both non-NULL
+ *   dlam [B][T][H]:   written when lam and dlam are both non-NULL
+ *   dS0 [B][H][dv][dk] fp32: written when non-NULL (also when S0 is NULL)
+ * No output may alias an input.  workspace: at least qdelta_bwd_workspace_bytes(...)
+ * bytes (two fp32 checkpoint arrays: the state entering, and the gradient reaching
+ * the state leaving, every chunk of 64 tokens).  T = 0 writes dS0 = dS_final (or 0)
+ * and nothing else.  Arithmetic in fp32 on CUDA cores for both dtypes.
+ * Errors as for qdelta_fwd.
+ */
+QD_API qd_status qdelta_bwd(const void *q, const void *k, const void *v,
+                            const void *alpha, const void *beta, const void *lam, const float *S0,
+                            const void *dO, const float *dS_final,
+                            void *dq, void *dk_out, void *dv_out, void *dalpha, void *dbeta, void *dlam,
+                            float *dS0, int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of device workspace qdelta_bwd needs for these sizes (never 0 when T > 0). */
+QD_API size_t qdelta_bwd_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype);
 
 /*
  * qdelta_fwd_static_scratch -- qdelta_fwd for callers that cannot allocate device

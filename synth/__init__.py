@@ -35,7 +35,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 # Fixed stream ids per tensor name.
 STREAMS = {
     "q": 1, "k": 2, "v": 3, "alpha": 4, "beta": 5, "lam": 6, "S0": 7,
-    "g": 8, "b": 9, "w": 10, "lam_h": 11, "alpha_mu": 12, "z": 13,
+    "g": 8, "b": 9, "w": 10, "lam_h": 11, "alpha_mu": 12, "z": 13, "dO": 14, "dS": 15,
 }
 
 _BLOCK = 1 << 22
@@ -159,6 +159,15 @@ def qdelta_inputs(B: int, T: int, H: int, dk: int, dv: int, seed: int, dtype: st
         s0 = normal(seed, STREAMS["S0"], B * H * dv * dk, std=math.sqrt(s0_var))
         out["S0"] = round_to(s0.reshape(B, H, dv, dk), "f32")
     return out
+
+
+def cotangents(B: int, T: int, H: int, dk: int, dv: int, seed: int, dtype: str = "bf16",
+               final_state: bool = True) -> dict:
+    """Incoming gradients of one backward: dO [B,T,H,dv] ~ N(0,1) in the input dtype
+    and dS_final [B,H,dv,dk] ~ N(0,1) fp32 (None unless final_state)."""
+    dO = round_to(normal(seed, STREAMS["dO"], B * T * H * dv).reshape(B, T, H, dv), dtype)
+    dS = round_to(normal(seed, STREAMS["dS"], B * H * dv * dk).reshape(B, H, dv, dk), "f32") if final_state else None
+    return {"dO": dO, "dS_final": dS}
 
 
 def qdelta_raw_inputs(B: int, T: int, H: int, dk: int, dv: int, seed: int, dtype: str = "bf16",

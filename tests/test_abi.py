@@ -122,3 +122,24 @@ def test_prologue_entry_points_checked(lib):
     assert st == qd.QD_ERR_ARG and "qdelta_step_prologue" in qd.qd_last_error()
     assert lib.qdelta_step_prologue(None, None, None, None, None, None, None, None, 0, 4, 64, 64, 1,
                                     None) == qd.QD_OK
+
+
+def test_backward_arguments_checked(lib):
+    g = ctypes.c_void_p(256)
+    args = lambda **kw: [kw.get(n, g) for n in ("q", "k", "v", "alpha", "beta", "lam", "S0", "dO", "dS",
+                                               "dq", "dk", "dv", "dal", "dbe", "dla", "dS0")]
+    # missing dbeta, misaligned dq, unsupported head dim, missing workspace
+    st = lib.qdelta_bwd(*args(dbe=None), 1, 8, 1, 64, 64, 64, qd.QD_BF16, g, 1 << 30, None)
+    assert st == qd.QD_ERR_ARG and "qdelta_bwd" in qd.qd_last_error()
+    st = lib.qdelta_bwd(*args(dq=ctypes.c_void_p(260)), 1, 8, 1, 64, 64, 64, qd.QD_BF16, g, 1 << 30, None)
+    assert st == qd.QD_ERR_ARG and "aligned" in qd.qd_last_error()
+    st = lib.qdelta_bwd(*args(), 1, 8, 1, 48, 64, 64, qd.QD_BF16, g, 1 << 30, None)
+    assert st == qd.QD_ERR_UNSUPPORTED
+    need = lib.qdelta_bwd_workspace_bytes(1, 8, 1, 64, 64, 64, qd.QD_BF16)
+    assert need == 2 * 64 * 64 * 4
+    st = lib.qdelta_bwd(*args(), 1, 8, 1, 64, 64, 64, qd.QD_BF16, g, need - 16, None)
+    assert st == qd.QD_ERR_WORKSPACE
+    assert lib.qdelta_bwd_workspace_bytes(2, 130, 3, 128, 64, 64, qd.QD_F32) == 2 * 2 * 3 * 3 * 64 * 128 * 4
+    assert lib.qdelta_bwd_workspace_bytes(2, 0, 3, 128, 64, 64, qd.QD_F32) == 0
+    # empty batch: no device call
+    assert lib.qdelta_bwd(*([None] * 16), 0, 8, 4, 64, 64, 64, 1, None, 0, None) == qd.QD_OK

@@ -489,3 +489,90 @@ def test_qed_step_sequence_matches_forward(qd):
 
 def test_device_status_ok(qd):
     assert qd.qd_device_status() == qd.QD_OK
+
+
+# ---------------------------------------------------------------- backward
+
+GRAD_NAMES = ("dq", "dk", "dv", "dalpha", "dbeta", "dlam", "dS0")
+
+
+def check_grad(got, ref, dtype, what):
+    """As check(), with the bf16 max-abs bound scaled by the gradient's own magnitude:
+    gradients come out in the input dtype, whose rounding alone is 2^-9 of |value|."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
+    mx = np.abs(got - ref).max() if got.size else 0.0
+    if dtype == "bf16":
+        bound = BF16_ABS * max(1.0, np.abs(ref).max())
+        assert rel <= BF16_REL and mx <= bound, f"{what}: rel L2 {rel:.3e}, max abs {mx:.3e} (bound {bound:.3e})"
+    else:
+        assert rel <= F32_REL, f"{what}: rel L2 {rel:.3e}, max abs {mx:.3e}"
+    return rel, mx
+
+
+def run_bwd(qd, d, c, want_dS0=True):
+    dt = tdt(d)
+    g = qd.qdelta_bwd(dev(d["q"], dt), dev(d["k"], dt), dev(d["v"], dt), dev(d["alpha"], dt), dev(d["beta"], dt),
+                      dev(d["lam"], dt), dev(d["S0"], torch.float32), dev(c["dO"], dt),
+                      dev(c["dS_final"], torch.float32), want_dS0=want_dS0)
+    torch.cuda.synchronize()
+    return {n: None if x is None else x.float().cpu().numpy() for n, x in g.items()}
+
+
+@pytest.mark.parametrize("dt,dk,dv,mode", [("f32", 64, 64, "qdelta"), ("f32", 64, 64, "gdn"),
+                                           ("f32", 64, 64, "deltanet"), ("f32", 32, 16, "qdelta"),
+                                           ("f32", 128, 128, "qdelta"), ("bf16", 128, 128, "qdelta"),
+                                           ("bf16", 64, 32, "gdn"), ("bf16", 16, 16, "qdelta")])
+def test_backward_all_gradients(qd, dt, dk, dv, mode):
+    """Every gradient against the oracle's adjoint: 2 full chunks + a ragged tail,
+    carried S0 and an incoming dS_final."""
+    d = synth.qdelta_inputs(2, 150, 2, dk, dv, seed=71, dtype=dt, mode=mode, s0_var=0.01)
+    c = synth.cotangents(2, 150, 2, dk, dv, seed=71, dtype=dt)
+    g = run_bwd(qd, d, c)
+    assert qd.last_launch_count() == 3
+    ref = oracle.qdelta_bwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["lam"], d["S0"], c["dO"],
+                            c["dS_final"])
+    for name in GRAD_NAMES:
+        if ref[name] is None:
+            assert g[name] is None, name
+            continue
+        check_grad(g[name], ref[name], dt, f"{dt} {mode} {name}")
+
+
+@pytest.mark.parametrize("T", [1, 63, 64, 128])
+def test_backward_edge_lengths_without_state(qd, T):
+    """T = 1, one short chunk, exactly one and two chunks; S0 = 0 and dS_final = 0."""
+    d = synth.qdelta_inputs(1, T, 3, 64, 64, seed=72, dtype="f32", mode="qdelta")
+    c = synth.cotangents(1, T, 3, 64, 64, seed=72, dtype="f32", final_state=False)
+    g = run_bwd(qd, d, c)
+    ref = oracle.qdelta_bwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["lam"], None, c["dO"])
+    for name in GRAD_NAMES:
+        check_grad(g[name], ref[name], "f32", f"T={T} {name}")
+
+
+def test_backward_empty_sequence_passes_state_gradient(qd):
+    d = synth.qdelta_inputs(2, 0, 2, 64, 64, seed=73, dtype="f32", mode="qdelta")
+    c = synth.cotangents(2, 0, 2, 64, 64, seed=73, dtype="f32")
+    g = run_bwd(qd, d, c)
+    assert qd.last_launch_count() == 0
+    np.testing.assert_array_equal(g["dS0"], c["dS_final"])
+
+
+def test_backward_full_size_sampled_streams(qd):
+    """The 1.3B-layer workload (B=8, H=16, T=2048, d=128, bf16) in one call; four
+    (b, h) streams compared with the oracle over the whole sequence."""
+    _, d = synth.layer_1p3b()
+    B, T, H = 8, 2048, 16
+    c = synth.cotangents(B, T, H, 128, 128, seed=74, dtype="bf16")
+    g = run_bwd(qd, d, c)
+    pairs = [(0, 0), (3, 7), (5, 11), (7, 15)]
+    ref = oracle.qdelta_bwd(sel(d["q"], pairs), sel(d["k"], pairs), sel(d["v"], pairs), sel(d["alpha"], pairs),
+                            sel(d["beta"], pairs), sel(d["lam"], pairs), None, sel(c["dO"], pairs),
+                            np.stack([c["dS_final"][b, h] for b, h in pairs])[:, None])
+    for name in GRAD_NAMES:
+        got = g[name]
+        got = np.stack([got[b, h] for b, h in pairs])[:, None] if name == "dS0" else sel(got, pairs)
+        check_grad(got, ref[name], "bf16", f"full-size {name}")
