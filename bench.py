@@ -15,6 +15,8 @@ B=8, H=16, T=2048, dk=dv=128, bf16 inputs, fp32 state, full Q-Delta gates
   qed_decode  qed_step on the same shape, GB/s
   qed      qed_fwd at B=4, H=8, T=4096, d=128 bf16, tokens/s
   prologue qdelta_fwd_prologue on the step's workload (projections and logits in)
+  backward qdelta_bwd on the step's workload (all input gradients), against the
+           FP32 CUDA-core peak its arithmetic runs on
   cpu_baseline  the fp64 oracle timed on this host's cores on a bounded sample
 
 --impl reference times the oracle itself (the CPU reference of this build) on
@@ -364,6 +366,52 @@ def time_prologue(qd, steps=20, warmup=3):
             "tokens_per_s": B * T / (ms * 1e-3), "GBps": ALG_BYTES / (ms * 1e-3) / 1e9}
 
 
+# Backward work per token-head (multiply-adds x 2), C = 64, d = dk = dv: the checkpoint
+# forward (X S^T, Z^T K: 4 d^2; Grams and solve-apply 5 C d), the reverse sweep (dZ,
+# dS update: 6 d^2; Grams, P^T dO, back substitution 7 C d) and the gradient kernel
+# (XS, QS, K dS^T, the three S/dS products: 12 d^2; Grams, Z, dZ, dR, dA, dP and the
+# four masked products: 22 C d).
+BWD_FLOPS_PER_TOKEN_HEAD = 22 * DK * DV + 34 * CHUNK * DK
+
+
+def fp32_alu_peak_tflops():
+    """FP32 CUDA-core peak from unit counts and clock: SMs x 128 FMA lanes x 2 flop x
+    the maximum SM clock (152 x 128 x 2 x 2.07 GHz = 80.5 TFLOP/s on GB300)."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return sms * 128 * 2 * 2.07e9 / 1e12
+
+
+def time_bwd(qd, steps=5, warmup=3):
+    """qdelta_bwd on the step's workload (B=8, H=16, T=2048, d=128, bf16), dO and
+    dS_final ~ N(0,1)."""
+    import torch
+    _, d = synth.layer_1p3b()
+    c = synth.cotangents(B, T, H, DK, DV, seed=8, dtype="bf16")
+    bf = torch.bfloat16
+    args = [to_dev(d[k], bf) for k in ("q", "k", "v", "alpha", "beta", "lam")]
+    dO, dS = to_dev(c["dO"], bf), to_dev(c["dS_final"], torch.float32)
+    ws = torch.empty(qd.qdelta_bwd_workspace_bytes(B, T, H, DK, DV), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        qd.qdelta_bwd(*args, None, dO, dS, workspace=ws, stream=stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        qd.qdelta_bwd(*args, None, dO, dS, workspace=ws, stream=stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    tflops = TOKEN_HEADS * BWD_FLOPS_PER_TOKEN_HEAD / (ms * 1e-3) / 1e12
+    peak = fp32_alu_peak_tflops()
+    return {"workload": f"qdelta_bwd_bf16_B{B}_H{H}_T{T}_d{DK}", "ms_per_step": ms,
+            "tokens_per_s": B * T / (ms * 1e-3), "launches": qd.last_launch_count(),
+            "roofline": {"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak, "peak_kind": "derived: SMs x 128 FP32 lanes x 2 x 2.07 GHz",
+                         "alg_flops_per_launch": TOKEN_HEADS * BWD_FLOPS_PER_TOKEN_HEAD}}
+
+
 def oracle_sample(n_streams, seed=1, min_seconds=0.0):
     """Runs the fp64 oracle on n_streams (b, h) streams of the workload (full T) on
     all host cores, repeated until min_seconds have passed; returns
@@ -465,6 +513,7 @@ def main():
             extras["qed_decode"] = qdec
             extras["qed"] = time_qed(qd)
             extras["prologue"] = time_prologue(qd)
+            extras["backward"] = time_bwd(qd)
     del sets
     torch.cuda.synchronize()
 

@@ -23,9 +23,11 @@
 //   d log alpha = reverse cumulative sum of dl within the chunk, dalpha = d log alpha / alpha.
 //
 // Three launches:
-//   1. the fp32 chunk forward, storing the state entering each chunk (S_chk);
-//   2. qdelta_bwd_dstate_kernel: the reverse sweep of dS over the chunks, one CTA per
-//      (b, h, d_v tile) (rows of dS evolve independently, as rows of S do), storing the
+//   1. the chunk forward without its output, storing the state entering each chunk
+//      (S_chk): the tcgen05 kernel for bf16 at d = 128, else the fp32 CUDA-core one;
+//   2. the reverse sweep of dS over the chunks (qdelta_bwd_dstate_kernel here, one CTA
+//      per (b, h, d_v tile), since rows of dS evolve independently as rows of S do; the
+//      warp tensor-core sweep of bwd_mma.cu for bf16 at d = 128), storing the
 //      gradient reaching the state leaving each chunk (dS_chk) and dS0.  It needs no
 //      forward state: dS_in depends only on dS_out, dO, q, k and the gates;
 //   3. qdelta_bwd_grad_kernel: every input gradient, one CTA per (b, h, chunk), all
@@ -520,13 +522,18 @@ constexpr size_t grad_smem() {
 }
 
 template <typename TIn, int DK, int DVT>
-cudaError_t run_bwd(const QDeltaBwdArgs &a, cudaStream_t s) {
-    auto ks = qdelta_bwd_dstate_kernel<TIn, DK, DVT>;
-    constexpr size_t sm_s = dstate_smem<DK, DVT>();
-    cudaError_t e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_s);
-    if (e != cudaSuccess) return e;
-    ks<<<dim3(a.B * a.H, a.nv / DVT), kNTs, sm_s, s>>>(a);
-    e = cudaGetLastError();
+cudaError_t run_bwd(const QDeltaBwdArgs &a, cudaStream_t s, bool mma_sweep) {
+    cudaError_t e;
+    if (mma_sweep) {
+        e = launch_qdelta_bwd_dstate_mma(a, s);
+    } else {
+        auto ks = qdelta_bwd_dstate_kernel<TIn, DK, DVT>;
+        constexpr size_t sm_s = dstate_smem<DK, DVT>();
+        e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_s);
+        if (e != cudaSuccess) return e;
+        ks<<<dim3(a.B * a.H, a.nv / DVT), kNTs, sm_s, s>>>(a);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     auto kg = qdelta_bwd_grad_kernel<TIn, DK>;
     constexpr size_t sm_g = grad_smem<DK>();
@@ -538,13 +545,13 @@ cudaError_t run_bwd(const QDeltaBwdArgs &a, cudaStream_t s) {
 }
 
 template <typename TIn>
-cudaError_t dispatch_bwd(const QDeltaBwdArgs &a, cudaStream_t s) {
+cudaError_t dispatch_bwd(const QDeltaBwdArgs &a, cudaStream_t s, bool m) {
     const bool wide = a.nv >= 32;
     switch (a.nk) {
-        case 16: return wide ? run_bwd<TIn, 16, 32>(a, s) : run_bwd<TIn, 16, 16>(a, s);
-        case 32: return wide ? run_bwd<TIn, 32, 32>(a, s) : run_bwd<TIn, 32, 16>(a, s);
-        case 64: return wide ? run_bwd<TIn, 64, 32>(a, s) : run_bwd<TIn, 64, 16>(a, s);
-        case 128: return wide ? run_bwd<TIn, 128, 32>(a, s) : run_bwd<TIn, 128, 16>(a, s);
+        case 16: return wide ? run_bwd<TIn, 16, 32>(a, s, m) : run_bwd<TIn, 16, 16>(a, s, m);
+        case 32: return wide ? run_bwd<TIn, 32, 32>(a, s, m) : run_bwd<TIn, 32, 16>(a, s, m);
+        case 64: return wide ? run_bwd<TIn, 64, 32>(a, s, m) : run_bwd<TIn, 64, 16>(a, s, m);
+        case 128: return wide ? run_bwd<TIn, 128, 32>(a, s, m) : run_bwd<TIn, 128, 16>(a, s, m);
     }
     return cudaErrorInvalidValue;
 }
@@ -557,13 +564,16 @@ size_t qdelta_bwd_workspace(int B, int T, int H, int dk, int dv) {
 }
 
 cudaError_t launch_qdelta_bwd(const QDeltaBwdArgs &a, int dtype, cudaStream_t s, int *nlaunch) {
-    // 1. forward over the chunks, keeping the state entering each
+    // 1. forward over the chunks, keeping the state entering each (the tensor-core
+    //    kernel where it applies, without its output)
     QDeltaArgs f{a.q, a.k, a.v, a.alpha, a.beta, a.lam, a.S0, nullptr, nullptr, a.B, a.T, a.H, a.nk, a.nv,
                  nullptr, 0, 0, a.S_chk};
-    cudaError_t e = launch_qdelta_chunk_simt(f, dtype, s, nlaunch);
+    cudaError_t e = qdelta_tc_supported(f, dtype) ? launch_qdelta_chunk_tc(f, s, nlaunch, kTcNoO)
+                                                  : launch_qdelta_chunk_simt(f, dtype, s, nlaunch);
     if (e != cudaSuccess) return e;
     // 2. reverse sweep of dS and 3. the per-chunk gradients
-    e = dtype == kBF16 ? dispatch_bwd<__nv_bfloat16>(a, s) : dispatch_bwd<float>(a, s);
+    const bool m = qdelta_bwd_mma_supported(a, dtype);
+    e = dtype == kBF16 ? dispatch_bwd<__nv_bfloat16>(a, s, m) : dispatch_bwd<float>(a, s, m);
     if (e == cudaSuccess) *nlaunch += 2;
     return e;
 }

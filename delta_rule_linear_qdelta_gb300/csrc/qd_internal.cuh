@@ -50,8 +50,9 @@ struct QDeltaArgs {
     void *ws;
     size_t ws_bytes;
     int prologue;     // q, k, alpha, beta, lam are projections and logits (qdelta_fwd_prologue)
-    float *S_chk;     // CUDA-core path only: if set, the state entering every chunk of 64
-                      // tokens, [B*H][ceil(T/64)][dv][dk] fp32 (the backward's checkpoints)
+    float *S_chk;     // if set, the state entering every chunk of 64 tokens,
+                      // [B*H][ceil(T/64)][dv][dk] fp32 (the backward's checkpoints); the
+                      // tensor-core kernel takes it only without the prologue
 };
 
 // Arguments of one Q-Delta backward (layouts as in include/qdelta.h); nk, nv are
@@ -114,6 +115,9 @@ cudaError_t launch_qdelta_chunk_simt(const QDeltaArgs &a, int dtype, cudaStream_
 // the per-chunk gradient kernel.  qdelta_bwd_workspace is the workspace it needs.
 size_t qdelta_bwd_workspace(int B, int T, int H, int dk, int dv);
 cudaError_t launch_qdelta_bwd(const QDeltaBwdArgs &a, int dtype, cudaStream_t s, int *nlaunch);
+// The reverse sweep on the warp tensor cores (TF32): bf16 with dk = dv = 128.
+bool qdelta_bwd_mma_supported(const QDeltaBwdArgs &a, int dtype);
+cudaError_t launch_qdelta_bwd_dstate_mma(const QDeltaBwdArgs &a, cudaStream_t s);
 cudaError_t launch_qed_chunk_simt(const QedArgs &a, int dtype, cudaStream_t s, int *nlaunch);
 cudaError_t launch_qdelta_step(const StepArgs &a, int dtype, cudaStream_t s, int *nlaunch);
 cudaError_t launch_qed_step(const QedStepArgs &a, int dtype, cudaStream_t s, int *nlaunch);
