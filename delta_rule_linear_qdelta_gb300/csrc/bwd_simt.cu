@@ -30,8 +30,9 @@
 //      warp tensor-core sweep of bwd_mma.cu for bf16 at d = 128), storing the
 //      gradient reaching the state leaving each chunk (dS_chk) and dS0.  It needs no
 //      forward state: dS_in depends only on dS_out, dO, q, k and the gates;
-//   3. qdelta_bwd_grad_kernel: every input gradient, one CTA per (b, h, chunk), all
-//      chunks in parallel, from the two checkpoints of its chunk.
+//   3. qdelta_bwd_grad_kernel (or its warp tensor-core version in bwd_mma.cu for bf16
+//      at d = 128): every input gradient, one CTA per (b, h, chunk), all chunks in
+//      parallel, from the two checkpoints of its chunk.
 // A ragged last chunk is padded with alpha = 1, beta = 0, lambda = 0 and zero tokens and
 // zero dO, which adds nothing to any gradient of a valid token.
 #include "qd_internal.cuh"
@@ -535,6 +536,7 @@ cudaError_t run_bwd(const QDeltaBwdArgs &a, cudaStream_t s, bool mma_sweep) {
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
+    if (mma_sweep) return launch_qdelta_bwd_grad_mma(a, s);
     auto kg = qdelta_bwd_grad_kernel<TIn, DK>;
     constexpr size_t sm_g = grad_smem<DK>();
     e = cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_g);

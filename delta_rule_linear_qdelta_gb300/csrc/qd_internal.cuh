@@ -115,9 +115,11 @@ cudaError_t launch_qdelta_chunk_simt(const QDeltaArgs &a, int dtype, cudaStream_
 // the per-chunk gradient kernel.  qdelta_bwd_workspace is the workspace it needs.
 size_t qdelta_bwd_workspace(int B, int T, int H, int dk, int dv);
 cudaError_t launch_qdelta_bwd(const QDeltaBwdArgs &a, int dtype, cudaStream_t s, int *nlaunch);
-// The reverse sweep on the warp tensor cores (TF32): bf16 with dk = dv = 128.
+// The reverse sweep and the per-chunk gradients on the warp tensor cores (TF32):
+// bf16 with dk = dv = 128.
 bool qdelta_bwd_mma_supported(const QDeltaBwdArgs &a, int dtype);
 cudaError_t launch_qdelta_bwd_dstate_mma(const QDeltaBwdArgs &a, cudaStream_t s);
+cudaError_t launch_qdelta_bwd_grad_mma(const QDeltaBwdArgs &a, cudaStream_t s);
 cudaError_t launch_qed_chunk_simt(const QedArgs &a, int dtype, cudaStream_t s, int *nlaunch);
 cudaError_t launch_qdelta_step(const StepArgs &a, int dtype, cudaStream_t s, int *nlaunch);
 cudaError_t launch_qed_step(const QedStepArgs &a, int dtype, cudaStream_t s, int *nlaunch);
