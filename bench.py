@@ -16,7 +16,7 @@ B=8, H=16, T=2048, dk=dv=128, bf16 inputs, fp32 state, full Q-Delta gates
   qed      qed_fwd at B=4, H=8, T=4096, d=128 bf16, tokens/s
   prologue qdelta_fwd_prologue on the step's workload (projections and logits in)
   backward qdelta_bwd on the step's workload (all input gradients), against the
-           FP32 CUDA-core peak its arithmetic runs on
+           TF32 tensor peak its products run on
   cpu_baseline  the fp64 oracle timed on this host's cores on a bounded sample
 
 --impl reference times the oracle itself (the CPU reference of this build) on
@@ -374,15 +374,12 @@ def time_prologue(qd, steps=20, warmup=3):
 BWD_FLOPS_PER_TOKEN_HEAD = 22 * DK * DV + 34 * CHUNK * DK
 
 
-def fp32_alu_peak_tflops():
-    """FP32 CUDA-core peak from unit counts and clock: SMs x 128 FMA lanes x 2 flop x
-    the maximum SM clock (152 x 128 x 2 x 2.07 GHz = 80.5 TFLOP/s on GB300)."""
-    import torch
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    return sms * 128 * 2 * 2.07e9 / 1e12
+# TF32 dense tensor peak: the measured bf16 peak times the nominal TF32 : bf16 ratio
+# of GB300 (1.1 : 2.25 PFLOP/s)
+TF32_OVER_BF16 = 1.1 / 2.25
 
 
-def time_bwd(qd, steps=5, warmup=3):
+def time_bwd(qd, tc_peak, steps=5, warmup=3):
     """qdelta_bwd on the step's workload (B=8, H=16, T=2048, d=128, bf16), dO and
     dS_final ~ N(0,1)."""
     import torch
@@ -404,11 +401,11 @@ def time_bwd(qd, steps=5, warmup=3):
     torch.cuda.synchronize()
     ms = start.elapsed_time(end) / steps
     tflops = TOKEN_HEADS * BWD_FLOPS_PER_TOKEN_HEAD / (ms * 1e-3) / 1e12
-    peak = fp32_alu_peak_tflops()
+    peak = tc_peak * TF32_OVER_BF16
     return {"workload": f"qdelta_bwd_bf16_B{B}_H{H}_T{T}_d{DK}", "ms_per_step": ms,
             "tokens_per_s": B * T / (ms * 1e-3), "launches": qd.last_launch_count(),
-            "roofline": {"bound": "alu", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
-                         "frac": tflops / peak, "peak_kind": "derived: SMs x 128 FP32 lanes x 2 x 2.07 GHz",
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tflops / peak, "peak_kind": "measured bf16 x nominal tf32/bf16 (1.1/2.25)",
                          "alg_flops_per_launch": TOKEN_HEADS * BWD_FLOPS_PER_TOKEN_HEAD}}
 
 
@@ -513,7 +510,7 @@ def main():
             extras["qed_decode"] = qdec
             extras["qed"] = time_qed(qd)
             extras["prologue"] = time_prologue(qd)
-            extras["backward"] = time_bwd(qd)
+            extras["backward"] = time_bwd(qd, tc_peak)
     del sets
     torch.cuda.synchronize()
 
