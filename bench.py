@@ -460,8 +460,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip the decode / QED / e2e / CPU legs")
-    ap.add_argument("--profile", action="store_true",
-                    help="profiling case: run warmup + steps forwards of the workload untimed, print no JSON line")
+    ap.add_argument("--profile", nargs="?", const="fwd", choices=["fwd", "bwd"],
+                    help="profiling case: run warmup + steps forwards (fwd) or backwards (bwd) of the "
+                         "workload untimed, print no JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -476,11 +477,15 @@ def main():
         build.build()
     rank, world, local = dist_setup(args.gpus)
     hbm_peak, tc_peak, tc_sustained, peak_kind = load_peaks()
-    if args.profile:
+    if args.profile == "fwd":
         sets = make_buffers(1, seed_base=1 + rank)
         time_device(qd, sets, args.steps, args.warmup, world)
         torch.cuda.synchronize()
         print(f"profile case done: {args.warmup + args.steps} forwards, status {qd.qd_device_status()}", flush=True)
+        return
+    if args.profile == "bwd":
+        time_bwd(qd, tc_peak, steps=args.steps, warmup=args.warmup)
+        print(f"profile case done: {args.warmup + args.steps} backwards, status {qd.qd_device_status()}", flush=True)
         return
 
     sets = make_buffers(N_BUFFERS, seed_base=1 + rank)

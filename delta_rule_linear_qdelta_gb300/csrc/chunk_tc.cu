@@ -114,13 +114,13 @@ struct TcParams {
     float *S_final;
     int B, T, H;
     int flags;   // kTcNoV | kTcS0Identity | kTcNoO (segment-scan passes)
-    float *S_chk;   // CHK: the state entering each chunk, [B*H][nchunks][dv][dk] fp32
 };
 
 // PRO: q, k, alpha, beta, lambda arrive as projections and logits (the prologue of
 // qdelta_fwd_prologue); a template parameter, so the plain kernel carries none of it.
-// CHK: the fp32 state entering every chunk is written to S_chk (the backward's
-// checkpoints), from the registers that already hold it on its way into TMEM.
+// CHK: the fp32 state entering every chunk is written to [B*H][nchunks][dv][dk] (the
+// backward's checkpoints), from the registers that already hold it on its way into
+// TMEM.  That instance runs without output (kTcNoO) and takes the array in p.o.
 template <bool PRO, bool CHK = false>
 __global__ void __launch_bounds__(kAllThreads, 1)
 qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
@@ -605,7 +605,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             tmem_ld32(tl + TM_S + 64 * half + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
             tmem_ld_wait();
             if (CHK && !last) {
-                float *dst = p.S_chk + (((size_t)bh * nchunks + c + 1) * kD + d_row) * kD + 64 * half;
+                float *dst = reinterpret_cast<float *>(p.o) + (((size_t)bh * nchunks + c + 1) * kD + d_row) * kD + 64 * half;
 #pragma unroll
                 for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
             }
@@ -704,7 +704,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
                     for (int j = 0; j < 64; ++j) sv[j] = (64 * half + j == d_row) ? 1.f : 0.f;
                 if (CHK) {
-                    float *dst = p.S_chk + ((size_t)bh * nchunks * kD + d_row) * kD + 64 * half;
+                    float *dst = reinterpret_cast<float *>(p.o) + ((size_t)bh * nchunks * kD + d_row) * kD + 64 * half;
 #pragma unroll
                     for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
                 }
@@ -783,11 +783,11 @@ cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nla
     else if (!make_token_map(&mo, a.o, a.B, a.T, a.H)) return cudaErrorInvalidValue;
     auto kern = a.S_chk ? qdelta_fwd_tc_kernel<false, true>
               : a.prologue ? qdelta_fwd_tc_kernel<true> : qdelta_fwd_tc_kernel<false>;
-    if (a.S_chk && a.prologue) return cudaErrorInvalidValue;
+    if (a.S_chk && (a.prologue || !(flags & kTcNoO))) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     TcParams p{(const __nv_bfloat16 *)a.alpha, (const __nv_bfloat16 *)a.beta, (const __nv_bfloat16 *)a.lam,
-               a.S0, (__nv_bfloat16 *)a.o, a.S_final, a.B, a.T, a.H, flags, a.S_chk};
+               a.S0, a.S_chk ? (__nv_bfloat16 *)a.S_chk : (__nv_bfloat16 *)a.o, a.S_final, a.B, a.T, a.H, flags};
     kern<<<a.B * a.H, kAllThreads, kSmemBytes, s>>>(p, mq, mk, mv, mo);
     e = cudaGetLastError();
     if (e == cudaSuccess) *nlaunch += 1;
