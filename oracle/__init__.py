@@ -1,5 +1,5 @@
-"""Oracle: plain fp64 CPU reference of the Q-Delta / QED forwards, the Q-Delta
-backward and the decode steps.
+"""Oracle: plain fp64 CPU reference of the Q-Delta / QED / EDA forwards, the
+Q-Delta backward and the decode steps.
 
 TEST INFRASTRUCTURE.  Only `tests/`, `__graft_entry__.smoke()` and `bench.py`'s
 CPU-baseline / reference leg may import this package.  It shares no code with
@@ -50,8 +50,9 @@ def _load():
         lib.oracle_qed_step.argtypes = [I] * 4 + [P] * 8 + [I, P, P, I]
         lib.oracle_qdelta_fwd_prologue.argtypes = [I] * 5 + [P] * 9 + [I]
         lib.oracle_qdelta_bwd.argtypes = [I] * 5 + [P] * 16 + [I]
+        lib.oracle_eda_fwd.argtypes = [I] * 5 + [P] * 8 + [I]
         for f in (lib.oracle_qdelta_fwd, lib.oracle_qed_fwd, lib.oracle_qdelta_step, lib.oracle_qed_fwd_variant,
-                  lib.oracle_qed_step, lib.oracle_qdelta_fwd_prologue, lib.oracle_qdelta_bwd):
+                  lib.oracle_qed_step, lib.oracle_qdelta_fwd_prologue, lib.oracle_qdelta_bwd, lib.oracle_eda_fwd):
             f.restype = I
         _lib = lib
     return _lib
@@ -98,6 +99,21 @@ def qdelta_bwd(q, k, v, alpha, beta, lam, S0, dO, dS_final=None, nthreads: int =
     if rc:
         raise MemoryError("oracle_qdelta_bwd failed")
     return g
+
+
+def eda_fwd(q, k, v, e, beta=None, S0=None, nthreads: int = 0):
+    """Sequential EDA forward (erase along e, then the Delta write along k; beta None
+    = the page's unit step).  Returns (o [B,T,H,dv], S_final [B,H,dv,dk] = M^T)."""
+    q, k, v, e, beta, S0 = map(_f64, (q, k, v, e, beta, S0))
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    o = np.zeros((B, T, H, dv))
+    S = np.zeros((B, H, dv, dk))
+    rc = _load().oracle_eda_fwd(B, T, H, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(e), _ptr(beta), _ptr(S0),
+                                _ptr(o), _ptr(S), nthreads)
+    if rc:
+        raise MemoryError("oracle_eda_fwd failed")
+    return o, S
 
 
 def qed_fwd(q, k, v, g, b, w, lam_h, S0=None, nthreads: int = 0):

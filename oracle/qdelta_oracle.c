@@ -1,6 +1,6 @@
 /*
- * Oracle for the Q-Delta / QED forward and the Q-Delta decode step:
- * plain fp64 sequential recurrences on the CPU.
+ * Oracle for the Q-Delta / QED / EDA forwards, the Q-Delta backward and the decode
+ * steps: plain fp64 sequential recurrences on the CPU.
  *
  * TEST INFRASTRUCTURE.  Only the tests, the package smoke check and the bench's
  * CPU-baseline / reference leg load this library.  It shares no code with the
@@ -41,6 +41,15 @@
  *    Rows of S evolve independently given a token's q, k and gates, so each row's
  *    states are recorded and walked back on their own; the row contributions to the
  *    shared gradients are summed.
+ *  - EDA, erase-then-delta ("Erase-then-Delta Attention", core method, the two
+ *    steps of its update): with the memory M (K x V), an erase direction e, then
+ *    the Delta write along the key,
+ *      M <- M - e (e^T M)                  (targeted erase; the printed "(e^T M) e" read
+ *                                           as the outer product that fits the shapes)
+ *      M <- M - beta k (k^T M - v^T)       (Delta write; the page's unit step is beta = 1)
+ *      o = M^T q                           (read-out after both steps)
+ *    Stored here as S = M^T ([dv][dk]): S <- S - (S e) e^T, S <- S - beta (S k - v) k^T,
+ *    o = S q.  e is used as given (the page's default e = q/|q| is the caller's).
  *  - Prologue (the feature map and gates computed from the layer's projections):
  *    DeltaNet notes sec. 3.8, q = SiLU(x_q)/|SiLU(x_q)|_2 and the same for k,
  *    beta = sigmoid(x_beta); Q-Delta notes sec. 2.5 (App. B), lambda = sigmoid(x_lambda);
@@ -71,7 +80,7 @@ typedef struct {
     double *o, *S_final;
     const double *dO, *dS_final;                     /* backward: incoming gradients */
     double *dq, *dk_out, *dv_out, *dalpha, *dbeta, *dlam, *dS0;
-    int method;          /* 0 = Q-Delta, 1 = QED, 2 = Q-Delta backward */
+    int method;          /* 0 = Q-Delta, 1 = QED, 2 = Q-Delta backward, 3 = EDA */
     int first, stride;   /* this worker's (b,h) streams: first, first+stride, ... */
     int status;
 } job_t;
@@ -200,6 +209,38 @@ static int qdelta_bwd_stream(const job_t *J, int b, int h)
     return 0;
 }
 
+/* One EDA stream (b, h), S = M^T in [dv][dk]; J->g holds e [B][T][H][dk] and
+ * J->beta the write strength (NULL = 1). */
+static int eda_stream(const job_t *J, int b, int h)
+{
+    const int T = J->T, H = J->H, dk = J->dk, dv = J->dv;
+    double *S = malloc(sizeof(double) * (size_t)dv * dk);
+    if (!S) return 1;
+    const size_t sh = ((size_t)b * H + h) * dv * dk;
+    if (J->S0) memcpy(S, J->S0 + sh, sizeof(double) * (size_t)dv * dk);
+    else memset(S, 0, sizeof(double) * (size_t)dv * dk);
+    for (int t = 0; t < T; ++t) {
+        const size_t tok = ((size_t)b * T + t) * H + h;
+        const double *qt = J->q + tok * dk, *kt = J->k + tok * dk, *et = J->g + tok * dk, *vt = J->v + tok * dv;
+        const double beta = J->beta ? J->beta[tok] : 1.0;
+        for (int i = 0; i < dv; ++i) {
+            double *Si = S + (size_t)i * dk;
+            double p = 0.0;                                                /* erase: (S e)_i */
+            for (int j = 0; j < dk; ++j) p += Si[j] * et[j];
+            for (int j = 0; j < dk; ++j) Si[j] -= p * et[j];
+            double r = -vt[i];                                             /* write: (S k - v)_i */
+            for (int j = 0; j < dk; ++j) r += Si[j] * kt[j];
+            for (int j = 0; j < dk; ++j) Si[j] -= beta * r * kt[j];
+            double acc = 0.0;                                              /* o = S q */
+            for (int j = 0; j < dk; ++j) acc += Si[j] * qt[j];
+            J->o[tok * dv + i] = acc;
+        }
+    }
+    if (J->S_final) memcpy(J->S_final + sh, S, sizeof(double) * (size_t)dv * dk);
+    free(S);
+    return 0;
+}
+
 /* One QED stream (b, h).  S is held K x V here (S[c*dv + j], c over keys). */
 static int qed_stream(const job_t *J, int b, int h)
 {
@@ -268,7 +309,8 @@ static void *worker(void *arg)
     for (int s = J->first; s < n; s += J->stride) {
         const int b = s / J->H, h = s % J->H;
         int rc = J->method == 0 ? qdelta_stream(J, b, h)
-               : J->method == 1 ? qed_stream(J, b, h) : qdelta_bwd_stream(J, b, h);
+               : J->method == 1 ? qed_stream(J, b, h)
+               : J->method == 2 ? qdelta_bwd_stream(J, b, h) : eda_stream(J, b, h);
         if (rc) J->status = rc;
     }
     return NULL;
@@ -345,6 +387,20 @@ int oracle_qdelta_bwd(int B, int T, int H, int dk, int dv,
     J.dO = dO; J.dS_final = dS_final;
     J.dq = dq; J.dk_out = dk_out; J.dv_out = dv_out; J.dalpha = dalpha; J.dbeta = dbeta; J.dlam = dlam;
     J.dS0 = dS0; J.method = 2;
+    return run(&J, nthreads);
+}
+
+/* EDA forward: q, k, e [B][T][H][dk], v [B][T][H][dv], beta [B][T][H] or NULL (= 1),
+ * S0, S_final [B][H][dv][dk] (M^T) or NULL. */
+int oracle_eda_fwd(int B, int T, int H, int dk, int dv,
+                   const double *q, const double *k, const double *v, const double *e, const double *beta,
+                   const double *S0, double *o, double *S_final, int nthreads)
+{
+    job_t J;
+    memset(&J, 0, sizeof J);
+    J.B = B; J.T = T; J.H = H; J.dk = dk; J.dv = dv;
+    J.q = q; J.k = k; J.v = v; J.g = e; J.beta = beta;
+    J.S0 = S0; J.o = o; J.S_final = S_final; J.method = 3;
     return run(&J, nthreads);
 }
 

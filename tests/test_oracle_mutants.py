@@ -327,3 +327,63 @@ def test_oracle_and_rowwise_adjoint_pass_backward_pins():
                                   "dalpha_new_state", "carry_without_decay"])
 def test_backward_mutant_rejected(kind):
     assert not backward_pins_hold(_bwd_rowwise(kind))
+
+
+# ---------------------------------------------------------------- EDA
+
+def oracle_eda_step(Sp, q, k, v, e, be):
+    sh = lambda x: np.asarray(x, dtype=np.float64).reshape(1, 1, 1, -1)
+    o, S = oracle.eda_fwd(sh(q), sh(k), sh(v), sh(e), np.array([[[be]]]), Sp[None, None])
+    return S[0, 0], o[0, 0, 0]
+
+
+def _eda_mutant(kind):
+    def step(Sp, q, k, v, e, be):
+        P = np.eye(len(e)) - (2.0 if kind == "reflection" else 1.0) * np.outer(e, e)
+        Se = Sp @ P
+        if kind == "erase_after_write":
+            S = (Sp - be * np.outer(Sp @ k - v, k)) @ P
+        elif kind == "residual_before_erase":
+            S = Se - be * np.outer(Sp @ k - v, k)
+        elif kind == "erase_along_key":
+            S = (Sp @ (np.eye(len(e)) - np.outer(k, k))) - be * np.outer(Sp @ k - v, k)
+        else:
+            S = Se - be * np.outer(Se @ k - v, k)
+        o = Se @ q if kind == "output_before_write" else S @ q
+        return S, o
+    return step
+
+
+def eda_pins_hold(step):
+    """Erase-only projection, unit-step retrieval, the e = k reduction to DeltaNet and
+    the transition-product form A = (I - e e^T)(I - beta k k^T)."""
+    d, dv = 6, 4
+    for _ in range(4):
+        q, k, e = (_unit(rng.standard_normal(d)) for _ in range(3))
+        v = rng.standard_normal(dv)
+        Sp = rng.standard_normal((dv, d))
+        be = rng.uniform(0.2, 0.9)
+        S, o = step(Sp, q, np.zeros(d), np.zeros(dv), e, be)
+        if not np.allclose(S, Sp @ (np.eye(d) - np.outer(e, e)), atol=1e-12):
+            return False
+        S, o = step(Sp, q, k, v, e, 1.0)
+        if not np.allclose(S @ k, v, atol=1e-12):
+            return False
+        S, o = step(Sp, q, k, v, k, 1.0)
+        if not np.allclose(S, Sp - np.outer(Sp @ k - v, k), atol=1e-12):
+            return False
+        S, o = step(Sp, q, k, v, e, be)
+        A = (np.eye(d) - np.outer(e, e)) @ (np.eye(d) - be * np.outer(k, k))
+        if not (np.allclose(S, Sp @ A + be * np.outer(v, k), atol=1e-12) and np.allclose(o, S @ q, atol=1e-12)):
+            return False
+    return True
+
+
+def test_oracle_passes_eda_pins():
+    assert eda_pins_hold(oracle_eda_step)
+
+
+@pytest.mark.parametrize("kind", ["reflection", "erase_after_write", "residual_before_erase", "erase_along_key",
+                                  "output_before_write"])
+def test_eda_mutant_rejected(kind):
+    assert not eda_pins_hold(_eda_mutant(kind))

@@ -679,3 +679,80 @@ def test_backward_streams_independent_and_thread_count_invariant():
         assert np.array_equal(g1[name], g4[name]), name
     np.testing.assert_array_equal(one["dq"], g1["dq"][1:, :, 2:])
     np.testing.assert_array_equal(one["dS0"], g1["dS0"][1:, 2:])
+
+
+# ---------------------------------------------------------------- EDA (erase-then-delta)
+
+def _rand_eda(B, T, H, dk, dv, beta=True):
+    q = _unit(rng.standard_normal((B, T, H, dk)))
+    k = _unit(rng.standard_normal((B, T, H, dk)))
+    e = _unit(rng.standard_normal((B, T, H, dk)))
+    v = rng.standard_normal((B, T, H, dv))
+    bt = rng.uniform(0.1, 1.0, (B, T, H)) if beta else None
+    S0 = rng.standard_normal((B, H, dv, dk)) * 0.3
+    return q, k, v, e, bt, S0
+
+
+def test_eda_erase_along_the_key_is_deltanet():
+    """e_t = k_t with unit keys: (I - k k^T)^2 = I - k k^T, so the erase adds nothing to
+    the Delta write and EDA with unit step is DeltaNet with beta = 1 (the page's two
+    steps then coincide with the standard Delta update it starts from)."""
+    q, k, v, _, _, S0 = _rand_eda(2, 13, 2, 6, 5, beta=False)
+    o, S = oracle.eda_fwd(q, k, v, k, None, S0)
+    o2, S2 = oracle.qdelta_fwd(q, k, v, None, np.ones(q.shape[:3]), None, S0)
+    np.testing.assert_allclose(o, o2, atol=1e-12)
+    np.testing.assert_allclose(S, S2, atol=1e-12)
+
+
+def test_eda_erase_only_projects_out_the_direction():
+    """Zero key and value: only the erase acts.  After one step the memory has no
+    component along e (S e = 0, i.e. e^T M = 0) and S = S0 (I - e e^T); with
+    orthonormal directions over the steps, S_T = S0 (I - sum_t e_t e_t^T)."""
+    d, dv, T = 8, 5, 4
+    Q, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    e = Q[:, :T].T.reshape(1, T, 1, d)
+    z = np.zeros((1, T, 1, d))
+    q = _unit(rng.standard_normal((1, T, 1, d)))
+    S0 = rng.standard_normal((1, 1, dv, d))
+    _, S1 = oracle.eda_fwd(q[:, :1], z[:, :1], np.zeros((1, 1, 1, dv)), e[:, :1], None, S0)
+    np.testing.assert_allclose(S1[0, 0] @ e[0, 0, 0], 0.0, atol=1e-13)
+    np.testing.assert_allclose(S1[0, 0], S0[0, 0] @ (np.eye(d) - np.outer(e[0, 0, 0], e[0, 0, 0])), atol=1e-13)
+    o, ST = oracle.eda_fwd(q, z, np.zeros((1, T, 1, dv)), e, None, S0)
+    P = np.eye(d) - sum(np.outer(e[0, t, 0], e[0, t, 0]) for t in range(T))
+    np.testing.assert_allclose(ST[0, 0], S0[0, 0] @ P, atol=1e-13)
+    np.testing.assert_allclose(o[0, -1, 0], ST[0, 0] @ q[0, -1, 0], atol=1e-13)
+
+
+def test_eda_unit_write_retrieves_the_value():
+    """beta = 1 and a unit key: after the write S_t k_t = v_t exactly, whatever was
+    erased before (the Delta write replaces the key's slot)."""
+    q, k, v, e, _, S0 = _rand_eda(1, 9, 3, 6, 4, beta=False)
+    for t in range(1, 10):
+        _, S = oracle.eda_fwd(q[:, :t], k[:, :t], v[:, :t], e[:, :t], None, S0)
+        for h in range(3):
+            np.testing.assert_allclose(S[0, h] @ k[0, t - 1, h], v[0, t - 1, h], atol=1e-12)
+
+
+@pytest.mark.parametrize("T", [1, 3, 6])
+def test_eda_bruteforce_transition_products(T):
+    """S_T = S0 prod_t A_t + sum_t beta_t v_t k_t^T prod_{u>t} A_u with
+    A_t = (I - e_t e_t^T)(I - beta_t k_t k_t^T), by explicit matrices, and every
+    o_t = S_t q_t."""
+    q, k, v, e, bt, S0 = _rand_eda(1, T, 1, 5, 3)
+    o, S = oracle.eda_fwd(q, k, v, e, bt, S0)
+    I = np.eye(5)
+    A = [(I - np.outer(e[0, t, 0], e[0, t, 0])) @ (I - bt[0, t, 0] * np.outer(k[0, t, 0], k[0, t, 0]))
+         for t in range(T)]
+    St = S0[0, 0].copy()
+    for t in range(T):
+        St = St @ A[t] + bt[0, t, 0] * np.outer(v[0, t, 0], k[0, t, 0])
+        np.testing.assert_allclose(o[0, t, 0], St @ q[0, t, 0], atol=1e-12)
+    ref = S0[0, 0].copy()
+    for t in range(T):
+        ref = ref @ A[t]
+    for t in range(T):
+        term = bt[0, t, 0] * np.outer(v[0, t, 0], k[0, t, 0])
+        for u in range(t + 1, T):
+            term = term @ A[u]
+        ref = ref + term
+    np.testing.assert_allclose(S[0, 0], ref, atol=1e-12)
