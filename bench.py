@@ -15,6 +15,7 @@ B=8, H=16, T=2048, dk=dv=128, bf16 inputs, fp32 state, full Q-Delta gates
   qed_decode  qed_step on the same shape, GB/s
   qed      qed_fwd at B=4, H=8, T=4096, d=128 bf16, tokens/s
   prologue qdelta_fwd_prologue on the step's workload (projections and logits in)
+  eda      eda_fwd (erase-then-delta) on the step's shape, tokens/s
   backward qdelta_bwd on the step's workload (all input gradients), against the
            TF32 tensor peak its products run on
   cpu_baseline  the fp64 oracle timed on this host's cores on a bounded sample
@@ -409,6 +410,32 @@ def time_bwd(qd, tc_peak, steps=5, warmup=3):
                          "alg_flops_per_launch": TOKEN_HEADS * BWD_FLOPS_PER_TOKEN_HEAD}}
 
 
+def time_eda(qd, steps=20, warmup=3):
+    """eda_fwd on the step's shape (B=8, H=16, T=2048, d=128, bf16; random unit erase
+    directions, beta = sigmoid(N(0,1)))."""
+    import torch
+    d = synth.eda_inputs(B, T, H, DK, DV, seed=9, dtype="bf16")
+    bf = torch.bfloat16
+    args = [to_dev(d[k], bf) for k in ("q", "k", "v", "e", "beta")]
+    o = torch.empty(B, T, H, DV, dtype=bf, device="cuda")
+    S = torch.empty(B, H, DV, DK, dtype=torch.float32, device="cuda")
+    ws = torch.empty(qd.eda_workspace_bytes(B, T, H, DK, DV), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        qd.eda_fwd(*args, None, o=o, S_final=S, workspace=ws, stream=stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        qd.eda_fwd(*args, None, o=o, S_final=S, workspace=ws, stream=stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    nbytes = TOKEN_HEADS * (5 * DK * 2 + 2) + B * H * DV * DK * 4     # q, k, v, e, o and beta; S_final
+    return {"workload": f"eda_bf16_B{B}_H{H}_T{T}_d{DK}", "ms_per_step": ms, "tokens_per_s": B * T / (ms * 1e-3),
+            "GBps": nbytes / (ms * 1e-3) / 1e9, "launches": qd.last_launch_count()}
+
+
 def oracle_sample(n_streams, seed=1, min_seconds=0.0):
     """Runs the fp64 oracle on n_streams (b, h) streams of the workload (full T) on
     all host cores, repeated until min_seconds have passed; returns
@@ -516,6 +543,7 @@ def main():
             extras["qed"] = time_qed(qd)
             extras["prologue"] = time_prologue(qd)
             extras["backward"] = time_bwd(qd, tc_peak)
+            extras["eda"] = time_eda(qd)
     del sets
     torch.cuda.synchronize()
 

@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "QD_OK", 1: "QD_ERR_ARG", 2: "QD_ERR_UNSUPPORTED", 3: "QD_ERR
                 4: "QD_ERR_TIMEOUT", 5: "QD_ERR_WORKSPACE"}
 EXPORTS = ("qdelta_fwd", "qdelta_fwd_prologue", "qdelta_workspace_bytes", "qed_fwd", "qed_fwd_variant",
            "qed_workspace_bytes", "qdelta_step", "qdelta_step_prologue", "qed_step", "qdelta_fwd_static_scratch",
-           "qdelta_bwd", "qdelta_bwd_workspace_bytes", "qd_device_status", "qd_last_error",
+           "qdelta_bwd", "qdelta_bwd_workspace_bytes", "eda_fwd", "eda_workspace_bytes", "qd_device_status",
+           "qd_last_error",
            "qd_last_launch_count")
 QED_VARIANTS = {"full": 0, "nogate": 1, "nogate_noproj": 2, "rand": 3}
 
@@ -62,6 +63,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qed_workspace_bytes.argtypes = [I] * 7
     lib.qdelta_bwd.argtypes = [P] * 16 + [I] * 7 + [P, Z, P]
     lib.qdelta_bwd_workspace_bytes.argtypes = [I] * 7
+    lib.eda_fwd.argtypes = [P] * 8 + [I] * 7 + [P, Z, P]
+    lib.eda_workspace_bytes.argtypes = [I] * 7
+    lib.eda_fwd.restype = I
+    lib.eda_workspace_bytes.restype = Z
     lib.qd_device_status.argtypes = [P]
     for f in (lib.qdelta_fwd, lib.qed_fwd, lib.qdelta_step, lib.qdelta_fwd_static_scratch, lib.qd_device_status,
               lib.qd_last_launch_count, lib.qed_fwd_variant, lib.qed_step, lib.qdelta_fwd_prologue,
@@ -210,6 +215,37 @@ def qdelta_bwd(q, k, v, alpha, beta, lam, S0, dO, dS_final=None, *, want_dS0=Tru
                                    B, T, H, dk, dv, chunk, code, _ptr(workspace), wsb, _stream(stream, q.device))
     _check(st, "qdelta_bwd")
     return g
+
+
+def eda_workspace_bytes(B, T, H, dk, dv, chunk=64, dtype=QD_BF16) -> int:
+    return load_library().eda_workspace_bytes(B, T, H, dk, dv, chunk, dtype)
+
+
+def eda_fwd(q, k, v, e, beta=None, S0=None, *, o=None, S_final=None, return_final=True, chunk=64, workspace=None,
+            stream=None):
+    """EDA forward (the C eda_fwd): erase along e, then the Delta write along k with
+    strength beta (None = 1), o_t read after both.  q, k, e [B,T,H,dk]; v [B,T,H,dv];
+    beta [B,T,H] or None; S0 [B,H,dv,dk] fp32 or None.  Returns (o, S_final)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    for t, name, shape in ((q, "q", (B, T, H, dk)), (k, "k", (B, T, H, dk)), (e, "e", (B, T, H, dk)),
+                           (v, "v", (B, T, H, dv))):
+        _need(t, name, dt, shape)
+    _need(beta, "beta", dt, (B, T, H), optional=True)
+    _need(S0, "S0", torch.float32, (B, H, dv, dk), optional=True)
+    if o is None:
+        o = torch.empty((B, T, H, dv), dtype=dt, device=q.device)
+    _need(o, "o", dt, (B, T, H, dv))
+    if S_final is None and return_final:
+        S_final = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
+    _need(S_final, "S_final", torch.float32, (B, H, dv, dk), optional=True)
+    code = _dtype_code(q)
+    workspace, wsb = _workspace(eda_workspace_bytes(B, T, H, dk, dv, chunk, code), workspace, q.device)
+    st = load_library().eda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(e), _ptr(beta), _ptr(S0), _ptr(o), _ptr(S_final),
+                                B, T, H, dk, dv, chunk, code, _ptr(workspace), wsb, _stream(stream, q.device))
+    _check(st, "eda_fwd")
+    return o, S_final
 
 
 def qdelta_fwd_static_scratch(q, k, v, alpha, beta, lam, S0=None, *, o=None, S_final=None, return_final=True,

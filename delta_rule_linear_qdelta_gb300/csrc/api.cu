@@ -118,6 +118,16 @@ qd_status qdelta_bwd(const void *q, const void *k, const void *v, const void *al
 
 namespace {
 
+// The chunked forward: tensor-core kernel (single pass or segment scan) where it
+// applies, else the CUDA-core kernel.
+cudaError_t run_forward(const qd::QDeltaArgs &a, qd_dtype dtype, cudaStream_t stream, int *n) {
+    if (qd::qdelta_tc_supported(a, dtype)) {
+        const int G = qd::qdelta_segments(a.B, a.T, a.H, a.dk, a.dv, dtype);
+        return G > 1 ? qd::launch_qdelta_segmented(a, G, stream, n) : qd::launch_qdelta_chunk_tc(a, stream, n);
+    }
+    return qd::launch_qdelta_chunk_simt(a, dtype, stream, n);
+}
+
 qd_status qdelta_fwd_impl(const char *fn, int prologue, const void *q, const void *k, const void *v,
                           const void *alpha, const void *beta, const void *lam, const float *S0, void *o,
                           float *S_final, int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype,
@@ -135,13 +145,7 @@ qd_status qdelta_fwd_impl(const char *fn, int prologue, const void *q, const voi
     if (T == 0) { g_launches = 0; return empty_sequence(S0, S_final, B, H, dk, dv, stream); }
     qd::QDeltaArgs a{q, k, v, alpha, beta, lam, S0, o, S_final, B, T, H, dk, dv, workspace, workspace_bytes,
                      prologue};
-    cudaError_t e;
-    if (qd::qdelta_tc_supported(a, dtype)) {
-        const int G = qd::qdelta_segments(B, T, H, dk, dv, dtype);
-        e = G > 1 ? qd::launch_qdelta_segmented(a, G, stream, &n) : qd::launch_qdelta_chunk_tc(a, stream, &n);
-    } else {
-        e = qd::launch_qdelta_chunk_simt(a, dtype, stream, &n);
-    }
+    cudaError_t e = run_forward(a, dtype, stream, &n);
     if (e != cudaSuccess) return cuda_fail(e, "qdelta_fwd launch");
     g_launches = n;
     return QD_OK;
@@ -183,6 +187,30 @@ qd_status qdelta_fwd(const void *q, const void *k, const void *v, const void *al
                      cudaStream_t stream) {
     return qdelta_fwd_impl("qdelta_fwd", 0, q, k, v, alpha, beta, lam, S0, o, S_final, B, T, H, dk, dv, chunk,
                            dtype, workspace, workspace_bytes, stream);
+}
+
+size_t eda_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype) {
+    (void)B; (void)T; (void)H; (void)dk; (void)dv; (void)chunk; (void)dtype;
+    return 0;
+}
+
+qd_status eda_fwd(const void *q, const void *k, const void *v, const void *e, const void *beta, const float *S0,
+                  void *o, float *S_final, int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype,
+                  void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    (void)workspace_bytes;
+    g_err[0] = 0;
+    const void *req[] = {q, k, v, e, o};
+    const void *opt[] = {beta, S0, S_final, workspace};
+    qd_status st = check_fwd("eda_fwd", req, 5, opt, 4, B, T, H, dk, dv, chunk, dtype);
+    if (st != QD_OK) return st;
+    if (B == 0 || H == 0) { g_launches = 0; return QD_OK; }
+    if (T == 0) { g_launches = 0; return empty_sequence(S0, S_final, B, H, dk, dv, stream); }
+    qd::EdaArgs a{q, k, v, e, beta, S0, o, S_final, B, T, H, dk, dv};
+    int n = 0;
+    cudaError_t err = qd::launch_eda(a, dtype, stream, &n);
+    if (err != cudaSuccess) return cuda_fail(err, "eda_fwd launch");
+    g_launches = n;
+    return QD_OK;
 }
 
 qd_status qdelta_fwd_prologue(const void *q_raw, const void *k_raw, const void *v, const void *a_logit,

@@ -70,6 +70,18 @@ struct QDeltaBwdArgs {
     float *S_chk, *dS_chk;
 };
 
+// Arguments of one EDA forward (erase along e, then the Delta write): q, k, e
+// [B][T][H][dk], v, o [B][T][H][dv], beta [B][T][H] or NULL (= 1).
+struct EdaArgs {
+    const void *q, *k, *v, *e, *beta;
+    const float *S0;
+    void *o;
+    float *S_final;
+    int B, T, H, dk, dv;
+};
+// The EDA forward: a recurrent fp32 kernel, one CTA per (b, h), dv <= 128.
+cudaError_t launch_eda(const EdaArgs &a, int dtype, cudaStream_t s, int *nlaunch);
+
 // QED ablation arms ("The Query Knows What to Forget", Table 1): the term added to
 // the base erase vector b*k, P(u) = u - k (k^T u):
 //   full lambda_h P(b*q); nogate lambda_h P(q); nogate-noproj lambda_h q;

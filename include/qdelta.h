@@ -1,6 +1,6 @@
 /*
- * qdelta.h -- C ABI of the GB300 (sm_103a) Q-Delta / QED forward, the Q-Delta
- * backward and the decode steps.
+ * qdelta.h -- C ABI of the GB300 (sm_103a) Q-Delta / QED / EDA forwards, the
+ * Q-Delta backward and the decode steps.
  *
  * Every entry point takes plain device pointers and sizes; no C++ or framework
  * types cross this boundary.  All device buffers are owned by the caller.  Every
@@ -217,6 +217,28 @@ QD_API qd_status qdelta_bwd(const void *q, const void *k, const void *v,
 
 /* Bytes of device workspace qdelta_bwd needs for these sizes (never 0 when T > 0). */
 QD_API size_t qdelta_bwd_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype);
+
+/*
+ * eda_fwd -- erase-then-delta forward ("Erase-then-Delta Attention", core method:
+ * a targeted erase along a direction e, then the Delta write along the key).  Per
+ * (b, h), with the memory M (d_k x d_v), stored as S = M^T in the state layout:
+ *     M <- M - e_t (e_t^T M)                       erase (the page's "(e^T M) e" read as
+ *                                                   the outer product that fits the shapes)
+ *     M <- M - beta_t k_t (k_t^T M - v_t^T)         Delta write (the page's unit step: beta = 1)
+ *     o_t = M^T q_t                                 read-out after both steps
+ * e [B][T][H][dk] in the call's dtype, used as given (the page's default is
+ * e = q/|q|; pass that to get it).  beta [B][T][H] or NULL (= 1).  Other arguments,
+ * layouts, state convention and errors as for qdelta_fwd.  Arithmetic and state in
+ * fp32 for both dtypes (token by token: with e = q the read-out cancels most of S q,
+ * which bf16 operands would not resolve).  workspace may be NULL: none is needed
+ * (eda_workspace_bytes returns 0; the argument keeps the forwards' signature).
+ */
+QD_API qd_status eda_fwd(const void *q, const void *k, const void *v, const void *e, const void *beta,
+                         const float *S0, void *o, float *S_final, int B, int T, int H, int dk, int dv,
+                         int chunk, qd_dtype dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of device workspace eda_fwd needs for these sizes. */
+QD_API size_t eda_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype);
 
 /*
  * qdelta_fwd_static_scratch -- qdelta_fwd for callers that cannot allocate device

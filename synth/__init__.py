@@ -35,7 +35,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 # Fixed stream ids per tensor name.
 STREAMS = {
     "q": 1, "k": 2, "v": 3, "alpha": 4, "beta": 5, "lam": 6, "S0": 7,
-    "g": 8, "b": 9, "w": 10, "lam_h": 11, "alpha_mu": 12, "z": 13, "dO": 14, "dS": 15,
+    "g": 8, "b": 9, "w": 10, "lam_h": 11, "alpha_mu": 12, "z": 13, "dO": 14, "dS": 15, "e": 16,
 }
 
 _BLOCK = 1 << 22
@@ -159,6 +159,22 @@ def qdelta_inputs(B: int, T: int, H: int, dk: int, dv: int, seed: int, dtype: st
         s0 = normal(seed, STREAMS["S0"], B * H * dv * dk, std=math.sqrt(s0_var))
         out["S0"] = round_to(s0.reshape(B, H, dv, dk), "f32")
     return out
+
+
+def eda_inputs(B: int, T: int, H: int, dk: int, dv: int, seed: int, dtype: str = "bf16", erase: str = "random",
+               beta: bool = True, s0_var: float | None = None) -> dict:
+    """Inputs of one EDA forward: q, k unit rows and v ~ N(0,1) as for Q-Delta; the erase
+    direction e a unit N(0,1) row ("random") or e = q ("query", the page's e = q/|q|);
+    beta = sigmoid(N(0,1)) or None (the page's unit step)."""
+    d = qdelta_inputs(B, T, H, dk, dv, seed, dtype, mode="deltanet", s0_var=s0_var)
+    if erase == "query":
+        e = d["q"].copy()
+    elif erase == "random":
+        e = round_to(_unit_rows(normal(seed, STREAMS["e"], B * T * H * dk).reshape(B, T, H, dk)), dtype)
+    else:
+        raise ValueError(f"unknown erase {erase!r}")
+    return {"q": d["q"], "k": d["k"], "v": d["v"], "e": e, "beta": d["beta"] if beta else None, "S0": d["S0"],
+            "dtype": dtype, "shape": (B, T, H, dk, dv)}
 
 
 def cotangents(B: int, T: int, H: int, dk: int, dv: int, seed: int, dtype: str = "bf16",

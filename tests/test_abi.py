@@ -143,3 +143,17 @@ def test_backward_arguments_checked(lib):
     assert lib.qdelta_bwd_workspace_bytes(2, 0, 3, 128, 64, 64, qd.QD_F32) == 0
     # empty batch: no device call
     assert lib.qdelta_bwd(*([None] * 16), 0, 8, 4, 64, 64, 64, 1, None, 0, None) == qd.QD_OK
+
+
+def test_eda_arguments_checked(lib):
+    g = ctypes.c_void_p(256)
+    st = lib.eda_fwd(g, g, g, None, None, None, g, None, 1, 8, 1, 64, 64, 64, qd.QD_BF16, g, 1 << 30, None)
+    assert st == qd.QD_ERR_ARG and "eda_fwd" in qd.qd_last_error()
+    st = lib.eda_fwd(g, g, g, g, ctypes.c_void_p(258), None, g, None, 1, 8, 1, 64, 64, 64, qd.QD_BF16, g, 1 << 30,
+                     None)
+    assert st == qd.QD_ERR_ARG and "aligned" in qd.qd_last_error()
+    assert lib.eda_workspace_bytes(1, 8, 1, 64, 64, 64, qd.QD_BF16) == 0
+    st = lib.eda_fwd(g, g, g, g, None, None, g, None, 1, 8, 1, 48, 64, 64, qd.QD_BF16, None, 0, None)
+    assert st == qd.QD_ERR_UNSUPPORTED
+    assert lib.eda_fwd(None, None, None, None, None, None, None, None, 0, 8, 4, 64, 64, 64, 1, None, 0,
+                       None) == qd.QD_OK

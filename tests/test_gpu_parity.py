@@ -576,3 +576,36 @@ def test_backward_full_size_sampled_streams(qd):
         got = g[name]
         got = np.stack([got[b, h] for b, h in pairs])[:, None] if name == "dS0" else sel(got, pairs)
         check_grad(got, ref[name], "bf16", f"full-size {name}")
+
+
+# ---------------------------------------------------------------- EDA
+
+def run_eda(qd, d):
+    dt = tdt(d)
+    o, S = qd.eda_fwd(dev(d["q"], dt), dev(d["k"], dt), dev(d["v"], dt), dev(d["e"], dt), dev(d["beta"], dt),
+                      dev(d["S0"], torch.float32))
+    torch.cuda.synchronize()
+    return o.float().cpu().numpy(), S.cpu().numpy()
+
+
+@pytest.mark.parametrize("dt,dh,erase,beta", [("bf16", 128, "random", True), ("bf16", 128, "query", False),
+                                              ("f32", 64, "random", True), ("f32", 32, "query", False),
+                                              ("f32", 16, "random", False), ("bf16", 64, "query", True)])
+def test_eda_forward_all_outputs(qd, dt, dh, erase, beta):
+    """EDA, bf16 and fp32 inputs, random erase directions and the page's e = q/|q|:
+    150 tokens (9 staged tiles + a ragged one), carried S0."""
+    d = synth.eda_inputs(2, 150, 2, dh, dh, seed=81, dtype=dt, erase=erase, beta=beta, s0_var=0.01)
+    o, S = run_eda(qd, d)
+    assert qd.last_launch_count() == 1
+    o_ref, S_ref = oracle.eda_fwd(d["q"], d["k"], d["v"], d["e"], d["beta"], d["S0"])
+    check(o, o_ref, dt, f"eda {dt} {erase} o")
+    check(S, S_ref, dt, f"eda {dt} {erase} S")
+
+
+def test_eda_long_sequence_query_erase(qd):
+    """B=1, H=2, T=2048 with e = q: the state carried over the whole sequence."""
+    d = synth.eda_inputs(1, 2048, 2, 128, 128, seed=82, dtype="bf16", erase="query", s0_var=0.01)
+    o, S = run_eda(qd, d)
+    o_ref, S_ref = oracle.eda_fwd(d["q"], d["k"], d["v"], d["e"], d["beta"], d["S0"])
+    check(o, o_ref, "bf16", "eda long o")
+    check(S, S_ref, "bf16", "eda long S")
