@@ -487,9 +487,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip the decode / QED / e2e / CPU legs")
-    ap.add_argument("--profile", nargs="?", const="fwd", choices=["fwd", "bwd"],
-                    help="profiling case: run warmup + steps forwards (fwd) or backwards (bwd) of the "
-                         "workload untimed, print no JSON line")
+    ap.add_argument("--profile", nargs="?", const="fwd", choices=["fwd", "bwd", "eda"],
+                    help="profiling case: run warmup + steps forwards (fwd), backwards (bwd) or EDA "
+                         "forwards (eda) of the workload untimed, print no JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -509,6 +509,11 @@ def main():
         time_device(qd, sets, args.steps, args.warmup, world)
         torch.cuda.synchronize()
         print(f"profile case done: {args.warmup + args.steps} forwards, status {qd.qd_device_status()}", flush=True)
+        return
+    if args.profile == "eda":
+        time_eda(qd, steps=args.steps, warmup=args.warmup)
+        print(f"profile case done: {args.warmup + args.steps} EDA forwards, status {qd.qd_device_status()}",
+              flush=True)
         return
     if args.profile == "bwd":
         time_bwd(qd, tc_peak, steps=args.steps, warmup=args.warmup)
