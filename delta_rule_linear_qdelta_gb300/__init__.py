@@ -27,6 +27,7 @@ STATUS_NAMES = {0: "QD_OK", 1: "QD_ERR_ARG", 2: "QD_ERR_UNSUPPORTED", 3: "QD_ERR
 EXPORTS = ("qdelta_fwd", "qdelta_fwd_prologue", "qdelta_workspace_bytes", "qed_fwd", "qed_fwd_variant",
            "qed_workspace_bytes", "qdelta_step", "qdelta_step_prologue", "qed_step", "qdelta_fwd_static_scratch",
            "qdelta_bwd", "qdelta_bwd_workspace_bytes", "eda_fwd", "eda_workspace_bytes", "qd_device_status",
+           "qd_selftest_bounded_wait",
            "qd_last_error",
            "qd_last_launch_count")
 QED_VARIANTS = {"full": 0, "nogate": 1, "nogate_noproj": 2, "rand": 3}
@@ -68,6 +69,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.eda_fwd.restype = I
     lib.eda_workspace_bytes.restype = Z
     lib.qd_device_status.argtypes = [P]
+    lib.qd_selftest_bounded_wait.argtypes = [ctypes.c_uint, P]
+    lib.qd_selftest_bounded_wait.restype = I
     for f in (lib.qdelta_fwd, lib.qed_fwd, lib.qdelta_step, lib.qdelta_fwd_static_scratch, lib.qd_device_status,
               lib.qd_last_launch_count, lib.qed_fwd_variant, lib.qed_step, lib.qdelta_fwd_prologue,
               lib.qdelta_step_prologue, lib.qdelta_bwd):

@@ -304,12 +304,23 @@ qd_status qdelta_step_prologue(float *S, const void *q_raw, const void *k_raw, c
                             dv, dtype, stream);
 }
 
+qd_status qd_selftest_bounded_wait(unsigned limit_us, cudaStream_t stream) {
+    g_err[0] = 0;
+    if (limit_us < 1 || limit_us > 1000000)
+        return fail(QD_ERR_ARG, "qd_selftest_bounded_wait: limit_us=%u not in [1, 1000000]", limit_us);
+    cudaError_t e = qd::launch_wait_selftest((uint64_t)limit_us * 1000ull, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "qd_selftest_bounded_wait launch");
+    g_launches = 1;
+    return QD_OK;
+}
+
 qd_status qd_device_status(cudaStream_t stream) {
     g_err[0] = 0;
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "qd_device_status");
     const bool t1 = qd::tc_read_and_clear_timeout(), t2 = qd::qed_tc_read_and_clear_timeout();
-    if (t1 || t2)
+    const bool t3 = qd::selftest_read_and_clear_timeout();
+    if (t1 || t2 || t3)
         return fail(QD_ERR_TIMEOUT, "a tensor-core kernel gave up a bounded wait (results of that call are invalid)");
     return QD_OK;
 }

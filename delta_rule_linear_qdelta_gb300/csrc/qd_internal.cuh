@@ -157,6 +157,10 @@ int qed_segments(int B, int T, int H, int dk, int dv, int dtype);
 cudaError_t launch_qed_segmented(const QedArgs &a, int G, cudaStream_t s, int *nlaunch);
 // Reads and clears the device word the tensor-core kernels set when a bounded wait runs out.
 bool tc_read_and_clear_timeout();
+// One CTA whose only mbarrier wait can never complete, bounded by limit_ns: sets its own
+// timeout word, read and cleared like the kernels' by selftest_read_and_clear_timeout.
+cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s);
+bool selftest_read_and_clear_timeout();
 bool qed_tc_read_and_clear_timeout();
 
 // Records `msg` as this host thread's last error (qd_last_error) and returns `status`.

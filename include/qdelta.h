@@ -271,6 +271,17 @@ QD_API qd_status qdelta_fwd_static_scratch(const void *q, const void *k, const v
  */
 QD_API qd_status qd_device_status(cudaStream_t stream);
 
+/*
+ * qd_selftest_bounded_wait -- test hook for the failure path above, not part of any
+ * computation.  Launches one CTA on `stream` whose only mbarrier wait can never
+ * complete (nothing arrives on it); the wait is the library's bounded wait with a
+ * limit of limit_us microseconds (1 .. 1000000), after which the CTA records the
+ * timeout exactly as a library kernel does and exits: no trap, no fault, no hang.
+ * The next qd_device_status(stream) then returns QD_ERR_TIMEOUT (and clears it);
+ * the context stays usable.  QD_ERR_ARG for a limit out of range.
+ */
+QD_API qd_status qd_selftest_bounded_wait(unsigned limit_us, cudaStream_t stream);
+
 /* Message of the last failed call on this host thread ("" if none). */
 QD_API const char *qd_last_error(void);
 

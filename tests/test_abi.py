@@ -157,3 +157,8 @@ def test_eda_arguments_checked(lib):
     assert st == qd.QD_ERR_UNSUPPORTED
     assert lib.eda_fwd(None, None, None, None, None, None, None, None, 0, 8, 4, 64, 64, 64, 1, None, 0,
                        None) == qd.QD_OK
+
+
+def test_bounded_wait_selftest_limit_checked(lib):
+    assert lib.qd_selftest_bounded_wait(0, None) == qd.QD_ERR_ARG
+    assert lib.qd_selftest_bounded_wait(2000000, None) == qd.QD_ERR_ARG
