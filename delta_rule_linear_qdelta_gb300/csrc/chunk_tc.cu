@@ -619,23 +619,36 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         if (!no_o()) {
             const bool gscale = g_ell[c & 3][kC - 1] > kSplitLog;
             const float *gam = g_gam[c & 3];
-            // [64 tokens][dv] tile, two 64-column panels (the previous tile's store has read it)
-            uint8_t *ot = sm + OFF_O + (d_row >> 6) * 8192;
+            // [64 tokens][dv] tile, two 64-column panels (the previous tile's store has read it).
+            // Each 16-lane half of this warp's TMEM quarter is read in the 16x256b shape, so a
+            // thread holds two adjacent tokens of d_v rows L + t/4 and L + 8 + t/4; the 8x8
+            // blocks (tokens x d_v) then go out as transposed stmatrix rows of 16 bytes.
+            const int t4 = lane & 3;
+            float2 gv[8];                                 // gamma of tokens 8j + 2 t4, + 1
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                gv[j] = gscale ? *reinterpret_cast<const float2 *>(gam + 8 * j + 2 * t4) : make_float2(1.f, 1.f);
 #pragma unroll 1
             for (int half = 0; half < 2; ++half) {
-                float ov[32], gv[32];
-#pragma unroll
-                for (int j = 0; j < 32; j += 4) {         // gamma read before this half's stores
-                    const float4 v = gscale ? *reinterpret_cast<const float4 *>(gam + 32 * half + j)
-                                            : make_float4(1.f, 1.f, 1.f, 1.f);
-                    gv[j] = v.x; gv[j + 1] = v.y; gv[j + 2] = v.z; gv[j + 3] = v.w;
-                }
-                tmem_ld32(tl + TM_O + 32 * half, ov);
+                const int L = 32 * q4 + 16 * half;        // first d_v row of these 16 lanes
+                float ov[32];
+                tmem_ld16x256_x8(tm + TM_O + ((uint32_t)L << 16), ov);
                 tmem_ld_wait();
+                uint32_t pk[16];                          // pk[2j + h]: rows L + 8h + r8, tokens 8j + 2 t4, + 1
 #pragma unroll
-                for (int cc = 0; cc < 32; ++cc)
-                    *reinterpret_cast<__nv_bfloat16 *>(ot + sw128_off(32 * half + cc, d_row & 63)) =
-                        __float2bfloat16_rn(gv[cc] * ov[cc]);
+                for (int j = 0; j < 8; ++j) {
+                    pk[2 * j] = pack_bf16x2(gv[j].x * ov[4 * j], gv[j].y * ov[4 * j + 1]);
+                    pk[2 * j + 1] = pack_bf16x2(gv[j].x * ov[4 * j + 2], gv[j].y * ov[4 * j + 3]);
+                }
+                // matrix m = lane / 8 of each store: tokens 8 (j + m/2) + lane%8, d_v L + 8 (m%2) ..
+                const int m = lane >> 3, col = L + 8 * (m & 1);
+                const uint32_t obase = sbase + OFF_O + (uint32_t)(col >> 6) * 8192;
+#pragma unroll
+                for (int j = 0; j < 8; j += 2) {
+                    const int tok = 8 * (j + (m >> 1)) + (lane & 7);
+                    stmatrix_x4_trans(obase + sw128_off(tok, col & 63), pk[2 * j], pk[2 * j + 1], pk[2 * j + 2],
+                                      pk[2 * j + 3]);
+                }
             }
             fence_proxy_async();
             named_sync(kBarChain, kChainThreads);

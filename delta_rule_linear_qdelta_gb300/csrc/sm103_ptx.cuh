@@ -170,6 +170,34 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 16 lanes x 64 columns from taddr (lane base a multiple of 16), in the 16x256b shape:
+// for j = 0..7, thread t receives r[4j..4j+1] = lane (base + t/4), columns 8j + 2(t%4) and
+// 8j + 2(t%4) + 1, and r[4j+2..4j+3] = the same columns of lane (base + 8 + t/4).
+__device__ __forceinline__ void tmem_ld16x256_x8(uint32_t taddr, float (&r)[32]) {
+    uint32_t *u = reinterpret_cast<uint32_t *>(r);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+          "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]),
+          "=r"(u[15]), "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]), "=r"(u[20]), "=r"(u[21]),
+          "=r"(u[22]), "=r"(u[23]), "=r"(u[24]), "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]),
+          "=r"(u[29]), "=r"(u[30]), "=r"(u[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Four 8x8 bf16 matrices to shared memory, transposed: thread t holds, in r[m], the
+// pair (row t/4, columns 2(t%4), 2(t%4)+1) of matrix m and gives the address of row
+// t%8 of matrix t/8 of the stored (transposed) matrices: 16 contiguous bytes each.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                                  uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(r0),
+                 "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
+}
+
 // Stores 32 consecutive columns of this thread's lane (the inverse of tmem_ld32).
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&r)[32]) {
     const uint32_t *u = reinterpret_cast<const uint32_t *>(r);
