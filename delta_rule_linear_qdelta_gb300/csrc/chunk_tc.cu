@@ -80,7 +80,6 @@ constexpr int kPrepThreads = kThreads;              // warps 0-7
 constexpr int kChainThreads = 128;                  // warps 8-11
 constexpr int kAllThreads = kPrepThreads + kChainThreads;
 constexpr int kBarPrep = 1, kBarChain = 2;          // named barrier ids (8-13: inside the solve)
-constexpr int kBarLo = 14;                          // prep warps 0-3
 constexpr uint32_t kStageBytes = 65536;
 constexpr uint32_t OFF_XQ = 0, OFF_K = 32768, OFF_V = 49152;
 constexpr uint32_t OFF_R1 = 2 * kStageBytes;         // 131072
@@ -455,7 +454,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         unit_lower_inverse<true>(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_Y),
                                  sm + OFF_T, sm + OFF_T + 8192, g_beta[gi], g_gam[gi],
                                  [&]() { if (warp == 4 && c + 1 < nchunks) compute_gates(c + 1); },
-                                 []() { named_sync(kBarPrep, kPrepThreads); }, []() { named_sync(kBarLo, 128); },
+                                 []() { named_sync(kBarPrep, kPrepThreads); },
                                  sm + OFF_M21 + (c & 1) * 2048, fold ? g_gam[gi] : nullptr, g_igam[gi][kC - 1]);
     };
     // U^T = V^T T1^T into U[c&1], W^T = X^T T2^T

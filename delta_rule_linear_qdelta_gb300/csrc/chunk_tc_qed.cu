@@ -371,8 +371,7 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
 
         // (6) Tinv = (I + At)^{-1} -> T (the U and W products read the same matrix)
         unit_lower_inverse(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_R2),
-                           sm + OFF_T, nullptr, nullptr, nullptr, []() {}, []() { __syncthreads(); },
-                           []() { named_sync(14, 128); });
+                           sm + OFF_T, nullptr, nullptr, nullptr, []() {}, []() { __syncthreads(); });
         sync_for_mma();
 
         // (7) U^T = (W*V)^T Tinv^T, W^T = Ae^T Tinv^T

@@ -171,8 +171,8 @@ __device__ __forceinline__ void put_pair(uint8_t *out1, uint8_t *out2, const flo
 // part of the inverse is zero and is never written).  Y is >= 32*LY floats of
 // scratch; M is overwritten with intermediate blocks.
 //   a) the eight 8x8 diagonal blocks by forward substitution, one column per lane,
-//      the block held in registers (warps 0-1)
-//   b) 8 -> 16:  T10 = -T11 (A10 T00), one warp per block pair
+//      the block held in registers (warp w < 4: blocks 2w and 2w+1, lanes 0-15)
+//   b) 8 -> 16:  T10 = -T11 (A10 T00), warp w merges its own two blocks
 //   c) 16 -> 32: the same on 16x16 blocks, one warp per (pair, 8-column tile)
 //   d) 32 -> 64: the same on the two 32x32 halves, one warp per 16x8 tile
 // Every inverted block keeps only the strict lower part of its inverse (the unit
@@ -181,11 +181,11 @@ __device__ __forceinline__ void put_pair(uint8_t *out1, uint8_t *out2, const flo
 // products only the warps that read the A21 being overwritten synchronise: the
 // warp itself (8 -> 16), the warp pair on named barrier 8 + pair (16 -> 32); in
 // 32 -> 64 nothing is overwritten and warps w, w + 4 share their Y tiles on named
-// barrier 10 + w (w < 4).  The caller orders the bf16 writes before their use (proxy
-// fence and barrier).
+// barrier 10 + w (w < 4).  Between the phases, too, only the producers of what a
+// warp reads next synchronise: a warp with itself (a -> b), a warp pair (b -> c).
+// The caller orders the bf16 writes before their use (proxy fence and barrier).
 // Called by kThreads threads (thread indices 0..kThreads-1) that synchronise with
-// sync(); phases a-c run on warps 0-3 alone, which synchronise with sync_lo(), while
-// warps 4-7 run idle().
+// sync(); phases a-c run on warps 0-3 alone while warps 4-7 run idle().
 //
 // With kCouple the last merge is left to the caller: phase d then computes only
 // M21 = T22 A21 (the 32x32 block coupling the two halves) and writes
@@ -193,18 +193,18 @@ __device__ __forceinline__ void put_pair(uint8_t *out1, uint8_t *out2, const flo
 // (core_off below) to out3; out1/out2 then hold the block-diagonal inverse
 // diag(T11, T22) with the same scalings.  Since T21 = -M21 T11, a solve (I + A) z = r is finished from the
 // block-diagonal one, zl = diag(T11, T22) r, by z_bot = zl_bot - M21 z_top.
-template <bool kCouple = false, typename Idle, typename Sync, typename SyncLo>
+template <bool kCouple = false, typename Idle, typename Sync>
 __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *out1, uint8_t *out2,
                                                    const float *s1, const float *s2, Idle idle, Sync sync,
-                                                   SyncLo sync_lo, uint8_t *out3 = nullptr,
-                                                   const float *s3 = nullptr, float s3_mul = 1.f) {
+                                                   uint8_t *out3 = nullptr, const float *s3 = nullptr,
+                                                   float s3_mul = 1.f) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (warp >= 4) {
         idle();
     } else {
         const int g = lane >> 2, t4 = lane & 3;
-        if (warp < 2) {
-            const int base = 8 * (4 * warp + (lane >> 3)), j = lane & 7;
+        if (lane < 16) {
+            const int base = 8 * (2 * warp + (lane >> 3)), j = lane & 7;
             float a[8][8];
 #pragma unroll
             for (int i = 1; i < 8; ++i) {                  // the block's rows 1-7, all loads first
@@ -236,8 +236,8 @@ __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *
                 if (out2) *reinterpret_cast<__nv_bfloat16 *>(out2 + off) = __float2bfloat16_rn(t[i] * c2);
             }
         }
-        sync_lo();
-        // 8 -> 16: warp w < 4 merges the 8x8 blocks at 16 w
+        __syncwarp();
+        // 8 -> 16: warp w < 4 merges the 8x8 blocks at 16 w (its own)
         {
             const int base = 16 * warp;
             float *Yw = Y + 8 * warp * LY;
@@ -249,7 +249,7 @@ __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *
             *reinterpret_cast<float2 *>(M + (base + 8 + g) * LA + base + 2 * t4) = make_float2(-d[0], -d[1]);
             put_pair(out1, out2, s1, s2, base + 8 + g, base + 2 * t4, -d[0], -d[1]);
         }
-        sync_lo();
+        named_sync(8 + (warp >> 1), 64);  // the pair's two 16x16 blocks are final
         // 16 -> 32: warp w < 4 takes pair p = w / 2 (blocks at 32 p) and 8-column tile w % 2
         {
             const int p = warp >> 1, n0 = 8 * (warp & 1), base = 32 * p;
