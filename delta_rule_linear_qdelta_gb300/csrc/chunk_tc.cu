@@ -410,9 +410,15 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             const float4 v = ones ? make_float4(1.f, 1.f, 1.f, 1.f) : *reinterpret_cast<const float4 *>(src + j);
             fi[j] = v.x; fi[j + 1] = v.y; fi[j + 2] = v.z; fi[j + 3] = v.w;
         }
-        if (split)                                    // uniform branches: no exp when not needed
+        if (split) {                                  // uniform branches: no exp when not needed
 #pragma unroll
-            for (int cc = 0; cc < 32; ++cc) g[cc] = (32 * hf + cc < lim) ? r * fi[cc] * g[cc] : 0.f;
+            for (int cc = 0; cc < 32; cc += 2) {
+                const float2 x = fmul2(fmul2(make_float2(r, r), make_float2(fi[cc], fi[cc + 1])),
+                                       make_float2(g[cc], g[cc + 1]));
+                g[cc] = (32 * hf + cc < lim) ? x.x : 0.f;
+                g[cc + 1] = (32 * hf + cc + 1 < lim) ? x.y : 0.f;
+            }
+        }
         else {
             const float lt = ell[t];
 #pragma unroll
@@ -543,8 +549,10 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
         for (int j = 0; j < 16; j += 2) {              // no shared-memory stores here: kappa read as needed
             const float4 kv = fold ? *reinterpret_cast<const float4 *>(kap + 2 * j) : make_float4(1.f, 1.f, 1.f, 1.f);
-            zp[j] = pack_bf16x2(z[2 * j] * kv.x, z[2 * j + 1] * kv.y);
-            zp[j + 1] = pack_bf16x2(z[2 * j + 2] * kv.z, z[2 * j + 3] * kv.w);
+            const float2 a = fmul2(make_float2(z[2 * j], z[2 * j + 1]), make_float2(kv.x, kv.y));
+            const float2 b = fmul2(make_float2(z[2 * j + 2], z[2 * j + 3]), make_float2(kv.z, kv.w));
+            zp[j] = pack_bf16x2(a.x, a.y);
+            zp[j + 1] = pack_bf16x2(b.x, b.y);
         }
         tmem_st16(tu + 16 * hf2, zp);
         tmem_st_wait();
@@ -585,7 +593,11 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         tmem_st32(tl + TM_SB + 32 * half, sp);
         if (store_back) {
 #pragma unroll
-            for (int e = 0; e < 64; ++e) sv[e] *= g;
+            for (int e = 0; e < 64; e += 2) {
+                const float2 x = fmul2(make_float2(sv[e], sv[e + 1]), make_float2(g, g));
+                sv[e] = x.x;
+                sv[e + 1] = x.y;
+            }
             tmem_st32(tl + TM_S + 64 * half, *reinterpret_cast<float(*)[32]>(sv));
             tmem_st32(tl + TM_S + 64 * half + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
         }
@@ -636,8 +648,10 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                 uint32_t pk[16];                          // pk[2j + h]: rows L + 8h + r8, tokens 8j + 2 t4, + 1
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    pk[2 * j] = pack_bf16x2(gv[j].x * ov[4 * j], gv[j].y * ov[4 * j + 1]);
-                    pk[2 * j + 1] = pack_bf16x2(gv[j].x * ov[4 * j + 2], gv[j].y * ov[4 * j + 3]);
+                    const float2 lo = fmul2(make_float2(ov[4 * j], ov[4 * j + 1]), gv[j]);
+                    const float2 hi = fmul2(make_float2(ov[4 * j + 2], ov[4 * j + 3]), gv[j]);
+                    pk[2 * j] = pack_bf16x2(lo.x, lo.y);
+                    pk[2 * j + 1] = pack_bf16x2(hi.x, hi.y);
                 }
                 // matrix m = lane / 8 of each store: tokens 8 (j + m/2) + lane%8, d_v L + 8 (m%2) ..
                 const int m = lane >> 3, col = L + 8 * (m & 1);
