@@ -367,7 +367,12 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             unpack8(kr[r], kf);
             unpack8(qr[r], qf);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xf[e] = fmaf(lm[r], qf[e], kf[e]);
+            for (int e = 0; e < 8; e += 2) {
+                const float2 x = ffma2(make_float2(lm[r], lm[r]), make_float2(qf[e], qf[e + 1]),
+                                       make_float2(kf[e], kf[e + 1]));
+                xf[e] = x.x;
+                xf[e + 1] = x.y;
+            }
             *reinterpret_cast<uint4 *>(st + OFF_XQ + pnl * 16384 + off) = pack8(xf);
         }
     };
@@ -489,11 +494,10 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         tmem_ld32(tl + TM_W + 32, *reinterpret_cast<float(*)[32]>(w + 32));
         tmem_ld_wait();
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-            float f[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = -w[8 * ch + e];
-            *reinterpret_cast<uint4 *>(sm + OFF_R2 + sw128_off(d_row, 8 * ch)) = pack8(f);
+        for (int ch = 0; ch < 8; ++ch) {                  // -W: the bf16 sign bits flipped after packing
+            uint4 u = pack8p(w + 8 * ch);
+            u.x ^= 0x80008000u; u.y ^= 0x80008000u; u.z ^= 0x80008000u; u.w ^= 0x80008000u;
+            *reinterpret_cast<uint4 *>(sm + OFF_R2 + sw128_off(d_row, 8 * ch)) = u;
         }
     };
     // K -> kappa K in place in chunk c's stage (the operand of the state product)
