@@ -8,7 +8,8 @@ B=8, H=16, T=2048, dk=dv=128, bf16 inputs, fp32 state, full Q-Delta gates
            exactly K steps on the launching stream, inputs resident in HBM and
            larger than L2, rotated over several buffer sets between steps
   e2e      the same metric through the C ABI with pinned HOST buffers: every step
-           copies its inputs host->device and its outputs (o, S_final) back
+           copies its inputs host->device and its outputs (o, S_final) back, steps
+           pipelined over three streams (copy in / compute / copy out)
   roofline the dominant kernel against the measured HBM copy bandwidth
   tensor   its GEMM work against the measured bf16 tensor peak
   decode   qdelta_step on 512 sequences x 16 heads (fp32 128x128 state), GB/s
@@ -223,41 +224,65 @@ def time_device(qd, sets, steps, warmup, world):
 
 
 def time_e2e(qd, steps, warmup, world):
-    """Host buffers in pinned memory; each step copies inputs in and results out."""
+    """Host buffers in pinned memory; every step copies its inputs in and its results
+    (o, S_final) out, all inside the timed region.  Steps are pipelined the way a
+    serving loop runs them: step i+1's inputs travel host -> device on one stream while
+    step i computes on a second and step i-1's results travel back on a third, with two
+    device buffer sets and events ordering each set's reuse."""
     import torch
     d = synth.qdelta_inputs(B, T, H, DK, DV, seed=5, dtype="bf16", mode="qdelta")
-    host = {k: torch.from_numpy(d[k]).to(torch.bfloat16).pin_memory() for k in ("q", "k", "v", "alpha", "beta", "lam")}
-    devb = {k: torch.empty_like(v, device="cuda") for k, v in host.items()}
-    o = torch.empty(B, T, H, DV, dtype=torch.bfloat16, device="cuda")
-    S = torch.empty(B, H, DV, DK, dtype=torch.float32, device="cuda")
-    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    S_h = torch.empty(S.shape, dtype=S.dtype).pin_memory()
+    names = ("q", "k", "v", "alpha", "beta", "lam")
+    host = {k: torch.from_numpy(d[k]).to(torch.bfloat16).pin_memory() for k in names}
+    devb = [{k: torch.empty_like(v, device="cuda") for k, v in host.items()} for _ in range(2)]
+    o = [torch.empty(B, T, H, DV, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    S = [torch.empty(B, H, DV, DK, dtype=torch.float32, device="cuda") for _ in range(2)]
+    o_h = [torch.empty(o[0].shape, dtype=o[0].dtype).pin_memory() for _ in range(2)]
+    S_h = [torch.empty(S[0].shape, dtype=S[0].dtype).pin_memory() for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = o.numel() * o.element_size() + S.numel() * S.element_size()
-    stream = torch.cuda.current_stream()
+    d2h = o[0].numel() * o[0].element_size() + S[0].numel() * S[0].element_size()
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    cmp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
 
-    def step():
-        for k in host:
-            devb[k].copy_(host[k], non_blocking=True)
-        qd.qdelta_fwd(devb["q"], devb["k"], devb["v"], devb["alpha"], devb["beta"], devb["lam"], None,
-                      o=o, S_final=S, stream=stream)
-        o_h.copy_(o, non_blocking=True)
-        S_h.copy_(S, non_blocking=True)
+    def step(i):
+        b = i % 2
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(cmp_done[b])              # step i-2 has read this input set
+            for k in names:
+                devb[b][k].copy_(host[k], non_blocking=True)
+            in_done[b].record(s_in)
+        s_cmp.wait_event(in_done[b])
+        if i >= 2:
+            s_cmp.wait_event(out_done[b])                 # step i-2's results have left this set
+        x = devb[b]
+        qd.qdelta_fwd(x["q"], x["k"], x["v"], x["alpha"], x["beta"], x["lam"], None, o=o[b], S_final=S[b],
+                      stream=s_cmp)
+        cmp_done[b].record(s_cmp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(cmp_done[b])
+            o_h[b].copy_(o[b], non_blocking=True)
+            S_h[b].copy_(S[b], non_blocking=True)
+            out_done[b].record(s_out)
 
-    for _ in range(warmup):
-        step()
+    for i in range(warmup):
+        step(i)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     barrier(world)
-    start.record(stream)
-    for _ in range(steps):
-        step()
-    end.record(stream)
+    start.record(s_in)
+    for i in range(steps):
+        step(warmup + i)
+    for b in range(2):
+        s_in.wait_event(out_done[b])                      # the end waits for every step's results
+    end.record(s_in)
     torch.cuda.synchronize()
     barrier(world)
     ms = max_over_ranks(start.elapsed_time(end) / steps, world)
     return {"value": B * T * world / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": ms}
+            "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "pipeline": "inputs in, compute, results out on three streams, two buffer sets"}
 
 
 def time_decode(qd, steps=50, warmup=5, N=512):
