@@ -88,7 +88,8 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
     __shared__ uint64_t bar_gbw, bar_qv, bar_k, bar_mma;
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
-    __shared__ float g_ku[kC], g_ps[2][kD], g_ecg[kD];
+    __shared__ float g_ku[kC], g_ps[2][kD];
+    __shared__ __align__(16) float g_ecg[kD];      // read as float2 pairs
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q4 = warp & 3, hf = warp >> 2;
@@ -215,6 +216,37 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
     const uint32_t sbase = smem_u32(sm);
     const uint32_t sXQ = sbase + OFF_XQ, sK = sbase + OFF_K, sV = sbase + OFF_V, sS = sbase + OFF_S;
     const uint32_t sT = sbase + OFF_T, sR2 = sbase + OFF_R2, sP = sbase + OFF_P;
+    // A [64 tokens][128] bf16 tile (two swizzled 64-column panels at dst) from this warp's
+    // TMEM lanes (the tile's columns) and columns 32 hf.. (its tokens): the accumulator at
+    // column c1, negated when c2 < 0, else plus the one at c2.  Each 16-lane half is read in
+    // the 16x256b shape, so a thread holds two adjacent tokens of rows L + t/4 and
+    // L + 8 + t/4, and the 8x8 blocks go out as transposed 16-byte stmatrix rows.
+    auto tile_out = [&](uint32_t c1, int c2, uint32_t dst) {
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+            const int L = 32 * q4 + 16 * half;
+            float a[16], b2[16];
+            tmem_ld16x256_x4(tm + c1 + 32 * hf + ((uint32_t)L << 16), a);
+            if (c2 >= 0) tmem_ld16x256_x4(tm + (uint32_t)c2 + 32 * hf + ((uint32_t)L << 16), b2);
+            tmem_ld_wait();
+            uint32_t pk[8];                                // pk[2j + h]: rows L + 8h + lane/4
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    float2 x = make_float2(a[4 * j + 2 * h2], a[4 * j + 2 * h2 + 1]);
+                    if (c2 >= 0) x = ffma2(make_float2(1.f, 1.f), make_float2(b2[4 * j + 2 * h2], b2[4 * j + 2 * h2 + 1]), x);
+                    uint32_t u = pack_bf16x2(x.x, x.y);
+                    pk[2 * j + h2] = c2 < 0 ? u ^ 0x80008000u : u;
+                }
+            const int m = lane >> 3, col = L + 8 * (m & 1);
+            const uint32_t base = dst + (uint32_t)(col >> 6) * 8192;
+#pragma unroll
+            for (int j = 0; j < 4; j += 2)
+                stmatrix_x4_trans(base + sw128_off(32 * hf + 8 * (j + (m >> 1)) + (lane & 7), col & 63), pk[2 * j],
+                                  pk[2 * j + 1], pk[2 * j + 2], pk[2 * j + 3]);
+        }
+    };
     for (int c = 0; c < nchunks; ++c) {
         const int t0 = c * kC;
         const uint32_t par = (uint32_t)(c & 1);
@@ -360,7 +392,12 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
                 tmem_ld32(tl + TM_S + 64 * hf + 32 * half, sv);
                 tmem_ld_wait();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) sv[e] *= g_ecg[64 * hf + 32 * half + e];
+                for (int e = 0; e < 32; e += 2) {
+                    const float2 x = fmul2(make_float2(sv[e], sv[e + 1]),
+                                           *reinterpret_cast<const float2 *>(g_ecg + 64 * hf + 32 * half + e));
+                    sv[e] = x.x;
+                    sv[e + 1] = x.y;
+                }
                 tmem_st32(tl + TM_S + 64 * hf + 32 * half, sv);
             }
             tmem_st_wait();
@@ -391,15 +428,7 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
         if (producer && c + 1 < nchunks) load_qv(c + 1);   // Qe, W*V and Ae are consumed
 
         // (8) -W -> R2 as [64 tokens][dk]
-        {
-            float w[32];
-            tmem_ld32(tl + TM_W + 32 * hf, w);
-            tmem_ld_wait();
-            uint8_t *dst = sm + OFF_R2 + (d_row >> 6) * 8192;
-#pragma unroll
-            for (int cc = 0; cc < 32; ++cc)
-                *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * hf + cc, d_row & 63)) = __float2bfloat16_rn(-w[cc]);
-        }
+        tile_out(TM_W, -1, sbase + OFF_R2);
         sync_for_mma();
 
         // (9) Z^T = U^T - S^ W^T
@@ -447,17 +476,7 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
 
         // (12) o = O1 + O2 -> staging (R2); state -> bf16 S_in (and S_final after the last chunk)
         {
-            if (!no_o()) {
-                float o1[32], o2[32];
-                tmem_ld32(tl + TM_O1 + 32 * hf, o1);
-                tmem_ld32(tl + TM_O2 + 32 * hf, o2);
-                tmem_ld_wait();
-                uint8_t *dst = sm + OFF_R2 + (d_row >> 6) * 8192;
-#pragma unroll
-                for (int cc = 0; cc < 32; ++cc)
-                    *reinterpret_cast<__nv_bfloat16 *>(dst + sw128_off(32 * hf + cc, d_row & 63)) =
-                        __float2bfloat16_rn(o1[cc] + o2[cc]);
-            }
+            if (!no_o()) tile_out(TM_O1, TM_O2, sbase + OFF_R2);
             const bool last = (c + 1 == nchunks);
             uint8_t *sp = sm + OFF_S + hf * 16384;
 #pragma unroll

@@ -188,6 +188,19 @@ __device__ __forceinline__ void tmem_ld16x256_x8(uint32_t taddr, float (&r)[32])
         : "memory");
 }
 
+// 16 lanes x 32 columns in the 16x256b shape (as tmem_ld16x256_x8, j = 0..3).
+__device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, float (&r)[16]) {
+    uint32_t *u = reinterpret_cast<uint32_t *>(r);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+          "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]),
+          "=r"(u[15])
+        : "r"(taddr)
+        : "memory");
+}
+
 // Four 8x8 bf16 matrices to shared memory, transposed: thread t holds, in r[m], the
 // pair (row t/4, columns 2(t%4), 2(t%4)+1) of matrix m and gives the address of row
 // t%8 of matrix t/8 of the stored (transposed) matrices: 16 contiguous bytes each.
