@@ -22,9 +22,12 @@
 // tensor-core path leave an error of 2^-9 |S| on a result often ten times smaller
 // than |S|.  The recurrence in fp32 has no such cancellation error.
 #include "qd_internal.cuh"
+#include "sm103_ptx.cuh"
 
 namespace qd {
 namespace {
+
+using ptx::ffma2;
 
 constexpr int kTile = 16;   // tokens per staged tile
 
@@ -130,30 +133,35 @@ __global__ void __launch_bounds__(TPR * 128, 1) eda_recurrent_kernel(EdaArgs a) 
         if (tid < nt) bv = beta ? to_f(beta[((size_t)b * T + t0 + tid) * H + h]) : 1.f;
         return bv;
     };
-    auto rowdot = [&](const TIn *x) {
-        float p0 = 0.f, p1 = 0.f;
+    auto rowdot = [&](const TIn *x) {                 // packed pairs: one instruction per two products
+        float2 pa = make_float2(0.f, 0.f), pb = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < NS; j += W) {
+            float w[W];
+            loadw<W>(x + j, w);
+#pragma unroll
+            for (int i = 0; i < W; i += 4) {
+                pa = ffma2(make_float2(S[j + i], S[j + i + 1]), make_float2(w[i], w[i + 1]), pa);
+                pb = ffma2(make_float2(S[j + i + 2], S[j + i + 3]), make_float2(w[i + 2], w[i + 3]), pb);
+            }
+        }
+        float p = (pa.x + pb.x) + (pa.y + pb.y);
+#pragma unroll
+        for (int off = 1; off < TPR; off <<= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+        return p;
+    };
+    auto axpy = [&](float c, const TIn *x) {          // S -= c x, in packed pairs
+        const float2 nc = make_float2(-c, -c);
 #pragma unroll
         for (int j = 0; j < NS; j += W) {
             float w[W];
             loadw<W>(x + j, w);
 #pragma unroll
             for (int i = 0; i < W; i += 2) {
-                p0 = fmaf(S[j + i], w[i], p0);
-                p1 = fmaf(S[j + i + 1], w[i + 1], p1);
+                const float2 r = ffma2(nc, make_float2(w[i], w[i + 1]), make_float2(S[j + i], S[j + i + 1]));
+                S[j + i] = r.x;
+                S[j + i + 1] = r.y;
             }
-        }
-        float p = p0 + p1;
-#pragma unroll
-        for (int off = 1; off < TPR; off <<= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
-        return p;
-    };
-    auto axpy = [&](float c, const TIn *x) {          // S -= c x
-#pragma unroll
-        for (int j = 0; j < NS; j += W) {
-            float w[W];
-            loadw<W>(x + j, w);
-#pragma unroll
-            for (int i = 0; i < W; ++i) S[j + i] = fmaf(-c, w[i], S[j + i]);
         }
     };
 
