@@ -9,7 +9,8 @@
 // that run side by side as a [B*G][T/G] batch of the same tensor-core kernel:
 //   pass 1  S0 = 0, v as given        ->  final state = Psi_g
 //   pass 2  S0 = I, v taken as 0      ->  final state = Phi_g
-//   combine (fp32, per (b, h), in segment order): S_start(g) = S, S <- S Phi_g + Psi_g
+//   combine (fp32, per (b, h) and 16 state rows, in segment order): S_start(g) = S,
+//           S <- S Phi_g + Psi_g
 //   pass 3  S0 = S_start(g)           ->  o, exactly as one pass over the whole sequence
 // The [B][T][H][d] layout makes the segment view free: [B][G*L][H][d] is [B*G][L][H][d].
 // QED ("The Query Knows What to Forget", Eqs. 4/6/8) keeps its state transposed,
@@ -26,69 +27,68 @@ namespace {
 constexpr int kD = 128;
 constexpr int kLS = 132;          // smem row stride (16-byte aligned rows)
 constexpr int kCombineThreads = 256;
+constexpr int kRows = 16;         // state rows per combine CTA
 
-// one CTA per (b, h): S [128][kLS] and Phi [128][kLS] in shared memory; thread owns
-// rows r0..r0+3 and columns c0..c0+15 of the product
+// One CTA per (b, h, 16 state rows): rows of S evolve independently under
+// S <- S Phi_g + Psi_g, so a head's 128 rows are spread over 8 CTAs.  Each holds its
+// rows of S and the whole Phi_g (fp32) in shared memory; thread t computes row t/16,
+// columns 8 (t%16) .. 8 (t%16) + 7 of the product.
 __global__ void __launch_bounds__(kCombineThreads)
 segment_combine_kernel(const float *S0, const float *Phi, const float *Psi, float *S_start, float *S_final,
                        int B, int H, int G) {
     extern __shared__ float sm[];
-    float *Ss = sm, *Ps = sm + kD * kLS;
+    float *Ss = sm, *Ps = sm + kRows * kLS;
     const int tid = threadIdx.x;
     const int bh = blockIdx.x, b = bh / H, h = bh % H;
-    const int r0 = 4 * (tid >> 3), c0 = 16 * (tid & 7);
+    const int row0 = blockIdx.y * kRows;
+    const int r = tid >> 4, c0 = 8 * (tid & 15);
     const size_t mat = (size_t)kD * kD;
-    for (int i = tid; i < kD * kD / 4; i += kCombineThreads) {
-        const int r = (4 * i) / kD, c = (4 * i) % kD;
-        const float4 v = S0 ? reinterpret_cast<const float4 *>(S0 + (size_t)bh * mat)[i] : make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4 *>(Ss + r * kLS + c) = v;
+    for (int i = tid; i < kRows * kD / 4; i += kCombineThreads) {
+        const int rr = (4 * i) / kD, c = (4 * i) % kD;
+        const float4 v = S0 ? *reinterpret_cast<const float4 *>(S0 + (size_t)bh * mat + (size_t)(row0 + rr) * kD + c)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4 *>(Ss + rr * kLS + c) = v;
     }
     __syncthreads();
     for (int g = 0; g < G; ++g) {
         const size_t seg = ((size_t)(b * G + g) * H + h) * mat;   // (b*G + g, h) in the segment batch
+        for (int i = tid; i < kRows * kD / 4; i += kCombineThreads) {
+            const int rr = (4 * i) / kD, c = (4 * i) % kD;
+            *reinterpret_cast<float4 *>(S_start + seg + (size_t)(row0 + rr) * kD + c) =
+                *reinterpret_cast<const float4 *>(Ss + rr * kLS + c);
+        }
         for (int i = tid; i < kD * kD / 4; i += kCombineThreads) {
-            const int r = (4 * i) / kD, c = (4 * i) % kD;
-            reinterpret_cast<float4 *>(S_start + seg)[i] = *reinterpret_cast<const float4 *>(Ss + r * kLS + c);
-            *reinterpret_cast<float4 *>(Ps + r * kLS + c) = reinterpret_cast<const float4 *>(Phi + seg)[i];
+            const int rr = (4 * i) / kD, c = (4 * i) % kD;
+            *reinterpret_cast<float4 *>(Ps + rr * kLS + c) = reinterpret_cast<const float4 *>(Phi + seg)[i];
+        }
+        float acc[8];
+        {
+            const float *src = Psi + seg + (size_t)(row0 + r) * kD + c0;
+            const float4 u = *reinterpret_cast<const float4 *>(src), w = *reinterpret_cast<const float4 *>(src + 4);
+            acc[0] = u.x; acc[1] = u.y; acc[2] = u.z; acc[3] = u.w;
+            acc[4] = w.x; acc[5] = w.y; acc[6] = w.z; acc[7] = w.w;
         }
         __syncthreads();
-        float acc[4][16];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 16; j += 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(Psi + seg + (size_t)(r0 + i) * kD + c0 + j);
-                acc[i][j] = v.x; acc[i][j + 1] = v.y; acc[i][j + 2] = v.z; acc[i][j + 3] = v.w;
-            }
+#pragma unroll 4
         for (int k = 0; k < kD; ++k) {
-            float a[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = Ss[(r0 + i) * kLS + k];
-#pragma unroll
-            for (int j = 0; j < 16; j += 4) {
-                const float4 p = *reinterpret_cast<const float4 *>(Ps + k * kLS + c0 + j);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    acc[i][j] = fmaf(a[i], p.x, acc[i][j]);
-                    acc[i][j + 1] = fmaf(a[i], p.y, acc[i][j + 1]);
-                    acc[i][j + 2] = fmaf(a[i], p.z, acc[i][j + 2]);
-                    acc[i][j + 3] = fmaf(a[i], p.w, acc[i][j + 3]);
-                }
-            }
+            const float a = Ss[r * kLS + k];
+            const float4 p0 = *reinterpret_cast<const float4 *>(Ps + k * kLS + c0);
+            const float4 p1 = *reinterpret_cast<const float4 *>(Ps + k * kLS + c0 + 4);
+            acc[0] = fmaf(a, p0.x, acc[0]); acc[1] = fmaf(a, p0.y, acc[1]);
+            acc[2] = fmaf(a, p0.z, acc[2]); acc[3] = fmaf(a, p0.w, acc[3]);
+            acc[4] = fmaf(a, p1.x, acc[4]); acc[5] = fmaf(a, p1.y, acc[5]);
+            acc[6] = fmaf(a, p1.z, acc[6]); acc[7] = fmaf(a, p1.w, acc[7]);
         }
         __syncthreads();
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 16; j += 4)
-                *reinterpret_cast<float4 *>(Ss + (r0 + i) * kLS + c0 + j) =
-                    make_float4(acc[i][j], acc[i][j + 1], acc[i][j + 2], acc[i][j + 3]);
+        *reinterpret_cast<float4 *>(Ss + r * kLS + c0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4 *>(Ss + r * kLS + c0 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
         __syncthreads();
     }
     if (S_final)
-        for (int i = tid; i < kD * kD / 4; i += kCombineThreads) {
-            const int r = (4 * i) / kD, c = (4 * i) % kD;
-            reinterpret_cast<float4 *>(S_final + (size_t)bh * mat)[i] = *reinterpret_cast<const float4 *>(Ss + r * kLS + c);
+        for (int i = tid; i < kRows * kD / 4; i += kCombineThreads) {
+            const int rr = (4 * i) / kD, c = (4 * i) % kD;
+            *reinterpret_cast<float4 *>(S_final + (size_t)bh * mat + (size_t)(row0 + rr) * kD + c) =
+                *reinterpret_cast<const float4 *>(Ss + rr * kLS + c);
         }
 }
 
@@ -140,10 +140,11 @@ cudaError_t run_segmented(const Args &a, int G, cudaStream_t s, int *nlaunch, La
     seg.S_final = Phi;
     e = launch(seg, kTcNoO | kTcNoV | kTcS0Identity);
     if (e != cudaSuccess) return e;
-    const size_t smem = 2 * kD * kLS * sizeof(float);
+    const size_t smem = (kRows + kD) * kLS * sizeof(float);
     e = cudaFuncSetAttribute(segment_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    segment_combine_kernel<<<a.B * a.H, kCombineThreads, smem, s>>>(a.S0, Phi, Psi, S_start, a.S_final, a.B, a.H, G);
+    segment_combine_kernel<<<dim3(a.B * a.H, kD / kRows), kCombineThreads, smem, s>>>(a.S0, Phi, Psi, S_start,
+                                                                                     a.S_final, a.B, a.H, G);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     *nlaunch += 1;
