@@ -111,11 +111,11 @@ int qdelta_segments(int B, int T, int H, int dk, int dv, int dtype) {
 }
 
 int qed_segments(int B, int T, int H, int dk, int dv, int dtype) {
-    // Each QED pass repeats the whole per-chunk preparation (the single-pass kernel is
-    // not warp-specialised), so three passes over G segments pay off only when very few
-    // streams leave most SMs idle: measured on the 32-stream QED workload (B=4, H=8,
-    // T=4096), four segments took 0.64 ms against 0.61 ms for one pass.
-    return (long long)B * H <= 16 ? qdelta_segments(B, T, H, dk, dv, dtype) : 1;
+    // The same policy as Q-Delta.  Each QED pass repeats the whole per-chunk preparation
+    // (its kernel is not warp-specialised), but with the combine spread over eight CTAs per
+    // head three passes still pay: on the 32-stream QED workload (B=4, H=8, T=4096) four
+    // segments take 0.55 ms against 0.62 ms for one pass.
+    return qdelta_segments(B, T, H, dk, dv, dtype);
 }
 
 size_t qdelta_segment_workspace(int B, int H, int G) {
