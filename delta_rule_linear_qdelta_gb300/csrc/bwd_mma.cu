@@ -257,7 +257,10 @@ __global__ void __launch_bounds__(kNT, 1) qdelta_bwd_grad_mma_kernel(QDeltaBwdAr
     float *dAm = Tm + kC * LA;                                        // [C][LA]    sum dR Z^T -> H * dM
     float *dPm = dAm + kC * LA;                                       // [C][LA]    sum dO Z^T -> H * dP
     float *ell = dPm + kC * LA, *la = ell + kC, *bet = la + kC, *lmb = bet + kC, *gam = lmb + kC;
-    float *wgt = gam + kC, *sb = wgt + kC, *srow = sb + kC, *wz = srow + kC, *dlm = wz + kC, *red = dlm + kC;
+    float *wgt = gam + kC, *sb = wgt + kC, *srow = sb + kC, *red = srow + kC;
+    // per-token partial sums of the four warps that share a row block (column group cg),
+    // added in a fixed order at the end so that results are run-to-run identical
+    float *part_s = red + kNT / 32, *part_z = part_s + 4 * kC, *part_l = part_z + 4 * kC;   // [4][kC] each
 
     const __nv_bfloat16 *q = (const __nv_bfloat16 *)a.q, *k = (const __nv_bfloat16 *)a.k;
     const __nv_bfloat16 *v = (const __nv_bfloat16 *)a.v, *dO = (const __nv_bfloat16 *)a.dO;
@@ -282,7 +285,7 @@ __global__ void __launch_bounds__(kNT, 1) qdelta_bwd_grad_mma_kernel(QDeltaBwdAr
         bet[t] = ok ? __bfloat162float(((const __nv_bfloat16 *)a.beta)[tok]) : 0.f;
         lmb[t] = (ok && a.lam) ? __bfloat162float(((const __nv_bfloat16 *)a.lam)[tok]) : 0.f;
         ell[t] = la[t];
-        sb[t] = srow[t] = wz[t] = dlm[t] = 0.f;
+        sb[t] = srow[t] = 0.f;
     }
     for (int i = tid; i < kC * LA; i += kNT) dAm[i] = dPm[i] = 0.f;
     __syncthreads();
@@ -505,7 +508,7 @@ __global__ void __launch_bounds__(kNT, 1) qdelta_bwd_grad_mma_kernel(QDeltaBwdAr
             colE += Pm[i * LA + t];
             dbm += Mm[t * LA + i];
         }
-        atomicAdd(&srow[t], rowE - colE);
+        srow[t] = rowE - colE;
         sb[t] += dbm;                                     // dbeta
     }
     {
@@ -530,10 +533,11 @@ __global__ void __launch_bounds__(kNT, 1) qdelta_bwd_grad_mma_kernel(QDeltaBwdAr
             z_hi += __shfl_xor_sync(0xffffffffu, z_hi, off);
         }
         if (tq == 0) {
-            atomicAdd(&srow[t_lo], s_lo);
-            atomicAdd(&srow[t_hi], s_hi);
-            atomicAdd(&wz[t_lo], wgt[t_lo] * z_lo);
-            atomicAdd(&wz[t_hi], wgt[t_hi] * z_hi);
+            const int cg = warp & 3;
+            part_s[cg * kC + t_lo] = s_lo;
+            part_s[cg * kC + t_hi] = s_hi;
+            part_z[cg * kC + t_lo] = wgt[t_lo] * z_lo;
+            part_z[cg * kC + t_hi] = wgt[t_hi] * z_hi;
         }
         // dX = (gamma dXS) S_in + (H * dM) K;  dQ = (gamma dO) S_in + (H * dP) K + lambda dX
         mma_strip<kC, 4>(aX, 0, [&](int r, int kk) { return dAm[(16 * rb + r) * LA + kk]; },
@@ -563,8 +567,8 @@ __global__ void __launch_bounds__(kNT, 1) qdelta_bwd_grad_mma_kernel(QDeltaBwdAr
             l_hi += __shfl_xor_sync(0xffffffffu, l_hi, off);
         }
         if (tq == 0) {
-            atomicAdd(&dlm[t_lo], l_lo);
-            atomicAdd(&dlm[t_hi], l_hi);
+            part_l[(warp & 3) * kC + t_lo] = l_lo;
+            part_l[(warp & 3) * kC + t_hi] = l_hi;
         }
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
@@ -587,8 +591,10 @@ __global__ void __launch_bounds__(kNT, 1) qdelta_bwd_grad_mma_kernel(QDeltaBwdAr
     if (tid < 32) {                                       // dl, then d log alpha by a suffix sum
         float tot = 0.f;
         for (int w = 0; w < kNT / 32; ++w) tot += red[w];
-        float x0 = srow[2 * tid] - wz[2 * tid], x1 = srow[2 * tid + 1] - wz[2 * tid + 1];
-        float wsum = wz[2 * tid] + wz[2 * tid + 1];
+        auto sum4 = [&](const float *pp, int t) { return ((pp[t] + pp[kC + t]) + pp[2 * kC + t]) + pp[3 * kC + t]; };
+        const float z0 = sum4(part_z, 2 * tid), z1 = sum4(part_z, 2 * tid + 1);
+        float x0 = srow[2 * tid] + sum4(part_s, 2 * tid) - z0, x1 = srow[2 * tid + 1] + sum4(part_s, 2 * tid + 1) - z1;
+        float wsum = z0 + z1;
 #pragma unroll
         for (int off = 16; off; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
         if (tid == 31) x1 += gam[kC - 1] * tot + wsum;
@@ -606,12 +612,14 @@ __global__ void __launch_bounds__(kNT, 1) qdelta_bwd_grad_mma_kernel(QDeltaBwdAr
         const size_t tok = tok_of(tid);
         ((__nv_bfloat16 *)a.dbeta)[tok] = __float2bfloat16_rn(sb[tid]);
         if (a.dalpha && a.alpha) ((__nv_bfloat16 *)a.dalpha)[tok] = __float2bfloat16_rn(srow[tid] / expf(la[tid]));
-        if (a.dlam && a.lam) ((__nv_bfloat16 *)a.dlam)[tok] = __float2bfloat16_rn(dlm[tid]);
+        if (a.dlam && a.lam)
+            ((__nv_bfloat16 *)a.dlam)[tok] =
+                __float2bfloat16_rn(((part_l[tid] + part_l[kC + tid]) + part_l[2 * kC + tid]) + part_l[3 * kC + tid]);
     }
 }
 
 constexpr size_t kGradSmem = (2 * kC * LQ + 2 * kC * LV4) * sizeof(__nv_bfloat16) +
-                             sizeof(float) * (2 * kQV * LS + 3 * kC * LR + 5 * kC * LA + 10 * kC + kNT / 32);
+                             sizeof(float) * (2 * kQV * LS + 3 * kC * LR + 5 * kC * LA + 8 * kC + kNT / 32 + 12 * kC);
 
 }  // namespace
 

@@ -542,9 +542,10 @@ def test_backward_all_gradients(qd, dt, dk, dv, mode):
         check_grad(g[name], ref[name], dt, f"{dt} {mode} {name}")
 
 
-@pytest.mark.parametrize("T", [1, 63, 64, 128])
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 100, 128])
 def test_backward_edge_lengths_without_state(qd, T):
-    """T = 1, one short chunk, exactly one and two chunks; S0 = 0 and dS_final = 0."""
+    """T = 1, one short chunk, exactly one chunk, one past it, a ragged second chunk, two
+    chunks; S0 = 0 and dS_final = 0."""
     d = synth.qdelta_inputs(1, T, 3, 64, 64, seed=72, dtype="f32", mode="qdelta")
     c = synth.cotangents(1, T, 3, 64, 64, seed=72, dtype="f32", final_state=False)
     g = run_bwd(qd, d, c)
@@ -609,3 +610,42 @@ def test_eda_long_sequence_query_erase(qd):
     o_ref, S_ref = oracle.eda_fwd(d["q"], d["k"], d["v"], d["e"], d["beta"], d["S0"])
     check(o, o_ref, "bf16", "eda long o")
     check(S, S_ref, "bf16", "eda long S")
+
+
+@pytest.mark.parametrize("dt,dh,cut", [("f32", 64, 64), ("f32", 64, 90), ("bf16", 128, 128)])
+def test_backward_split_call_chains_state_gradient(qd, dt, dh, cut):
+    """The state gradient is the backward's carry: the backward of tokens [cut, T) with
+    S0 = S_cut and the incoming dS_final, then the backward of [0, cut) with its dS0 as
+    dS_final, gives the one-call gradients (chunk-aligned and unaligned cuts)."""
+    T = 200
+    d = synth.qdelta_inputs(1, T, 2, dh, dh, seed=75, dtype=dt, mode="qdelta", s0_var=0.01)
+    c = synth.cotangents(1, T, 2, dh, dh, seed=75, dtype=dt)
+    tt = tdt(d)
+    cu = lambda x, a, b: None if x is None else dev(x[:, a:b], tt)
+    whole = run_bwd(qd, d, c)
+    _, S_cut = qd.qdelta_fwd(cu(d["q"], 0, cut), cu(d["k"], 0, cut), cu(d["v"], 0, cut), cu(d["alpha"], 0, cut),
+                             cu(d["beta"], 0, cut), cu(d["lam"], 0, cut), dev(d["S0"], torch.float32))
+    g2 = qd.qdelta_bwd(cu(d["q"], cut, T), cu(d["k"], cut, T), cu(d["v"], cut, T), cu(d["alpha"], cut, T),
+                       cu(d["beta"], cut, T), cu(d["lam"], cut, T), S_cut, cu(c["dO"], cut, T),
+                       dev(c["dS_final"], torch.float32))
+    g1 = qd.qdelta_bwd(cu(d["q"], 0, cut), cu(d["k"], 0, cut), cu(d["v"], 0, cut), cu(d["alpha"], 0, cut),
+                       cu(d["beta"], 0, cut), cu(d["lam"], 0, cut), dev(d["S0"], torch.float32),
+                       cu(c["dO"], 0, cut), g2["dS0"])
+    torch.cuda.synchronize()
+    for name in ("dq", "dk", "dv", "dalpha", "dbeta", "dlam"):
+        joined = np.concatenate([g1[name].float().cpu().numpy(), g2[name].float().cpu().numpy()], axis=1)
+        check_grad(joined, whole[name], "f32" if dt == "f32" else "bf16", f"split {name}")
+    check_grad(g1["dS0"].cpu().numpy(), whole["dS0"], "f32" if dt == "f32" else "bf16", "split dS0")
+
+
+def test_backward_and_eda_deterministic(qd):
+    """Repeated calls give bitwise-identical results (no atomics, no order-dependent sums)."""
+    d = synth.qdelta_inputs(2, 150, 2, 128, 128, seed=76, dtype="bf16", mode="qdelta", s0_var=0.01)
+    c = synth.cotangents(2, 150, 2, 128, 128, seed=76, dtype="bf16")
+    a, b = run_bwd(qd, d, c), run_bwd(qd, d, c)
+    for name in GRAD_NAMES:
+        assert np.array_equal(a[name], b[name]), name
+    e = synth.eda_inputs(2, 150, 2, 128, 128, seed=77, dtype="bf16", s0_var=0.01)
+    o1, S1 = run_eda(qd, e)
+    o2, S2 = run_eda(qd, e)
+    assert np.array_equal(o1, o2) and np.array_equal(S1, S2)
