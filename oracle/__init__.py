@@ -51,6 +51,8 @@ def _load():
         lib.oracle_qdelta_fwd_prologue.argtypes = [I] * 5 + [P] * 9 + [I]
         lib.oracle_qdelta_bwd.argtypes = [I] * 5 + [P] * 16 + [I]
         lib.oracle_eda_fwd.argtypes = [I] * 5 + [P] * 8 + [I]
+        lib.oracle_qdelta_bwd_prologue.argtypes = [I] * 5 + [P] * 16 + [I]
+        lib.oracle_qdelta_bwd_prologue.restype = I
         for f in (lib.oracle_qdelta_fwd, lib.oracle_qed_fwd, lib.oracle_qdelta_step, lib.oracle_qed_fwd_variant,
                   lib.oracle_qed_step, lib.oracle_qdelta_fwd_prologue, lib.oracle_qdelta_bwd, lib.oracle_eda_fwd):
             f.restype = I
@@ -98,6 +100,25 @@ def qdelta_bwd(q, k, v, alpha, beta, lam, S0, dO, dS_final=None, nthreads: int =
                                    _ptr(g["dalpha"]), _ptr(g["dbeta"]), _ptr(g["dlam"]), _ptr(g["dS0"]), nthreads)
     if rc:
         raise MemoryError("oracle_qdelta_bwd failed")
+    return g
+
+
+def qdelta_bwd_prologue(q_raw, k_raw, v, a_logit, b_logit, l_logit, S0, dO, dS_final=None, nthreads: int = 0):
+    """Backward of qdelta_fwd_prologue: gradients with respect to the projections and
+    gate logits (dq, dk are of q_raw, k_raw; dalpha, dbeta, dlam of the logits)."""
+    args = map(_f64, (q_raw, k_raw, v, a_logit, b_logit, l_logit, S0, dO, dS_final))
+    q_raw, k_raw, v, a_logit, b_logit, l_logit, S0, dO, dS_final = args
+    B, T, H, dk = q_raw.shape
+    dv = v.shape[-1]
+    g = {"dq": np.zeros_like(q_raw), "dk": np.zeros_like(k_raw), "dv": np.zeros_like(v),
+         "dalpha": None if a_logit is None else np.zeros((B, T, H)), "dbeta": np.zeros((B, T, H)),
+         "dlam": None if l_logit is None else np.zeros((B, T, H)), "dS0": np.zeros((B, H, dv, dk))}
+    rc = _load().oracle_qdelta_bwd_prologue(B, T, H, dk, dv, _ptr(q_raw), _ptr(k_raw), _ptr(v), _ptr(a_logit),
+                                            _ptr(b_logit), _ptr(l_logit), _ptr(S0), _ptr(dO), _ptr(dS_final),
+                                            _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dalpha"]),
+                                            _ptr(g["dbeta"]), _ptr(g["dlam"]), _ptr(g["dS0"]), nthreads)
+    if rc:
+        raise MemoryError("oracle_qdelta_bwd_prologue failed")
     return g
 
 

@@ -32,7 +32,8 @@
  *    with P(u) = u - k (k^T u).
  *  - Decode steps: one iteration of the Q-Delta or the QED loop per call, the
  *    state carried in and out in place.
- *  - Backward of the Q-Delta forward: the gradients of the scalar
+ *  - Backward of the Q-Delta forward (and of the forward from projections, through the
+ *    prologue's maps by the chain rule): the gradients of the scalar
  *    L = sum_t <dO_t, o_t> + <dS_final, S_T> with respect to q, k, v, alpha, beta,
  *    lambda and S0, by reverse-mode differentiation of the sequential recurrence
  *    above, one step at a time in reverse (the pages train the layer end to end,
@@ -475,6 +476,71 @@ int oracle_qdelta_fwd_prologue(int B, int T, int H, int dk, int dv,
         rc = oracle_qdelta_fwd(B, T, H, dk, dv, q, k, v, al, be, lm, S0, o, S_final, nthreads);
     }
     free(q); free(k); free(al); free(be); free(lm);
+    return rc;
+}
+
+/* Backward through the prologue's feature map for one token-head row: with
+ * s = SiLU(x), n = |s|, y = s / n and the incoming gradient dy, the gradient of x is
+ *     ds = (dy - y (y . dy)) / n,   dx = ds * SiLU'(x),  SiLU'(x) = sig(x) (1 + x (1 - sig(x))).
+ * An all-zero s (where the forward leaves y = 0) passes no gradient. */
+static void feature_map_bwd(const double *x, const double *dy, double *dx, int d)
+{
+    double ss = 0.0, ydy = 0.0;
+    for (int j = 0; j < d; ++j) {
+        const double sj = x[j] * sigmoid(x[j]);
+        ss += sj * sj;
+    }
+    if (!(ss > 0.0)) { for (int j = 0; j < d; ++j) dx[j] = 0.0; return; }
+    const double n = sqrt(ss);
+    for (int j = 0; j < d; ++j) ydy += (x[j] * sigmoid(x[j]) / n) * dy[j];
+    for (int j = 0; j < d; ++j) {
+        const double sg = sigmoid(x[j]), y = x[j] * sg / n;
+        dx[j] = (dy[j] - y * ydy) / n * (sg * (1.0 + x[j] * (1.0 - sg)));
+    }
+}
+
+/* Backward of oracle_qdelta_fwd_prologue: the inputs through the prologue, the
+ * recurrence's backward (oracle_qdelta_bwd) on them, then the chain rule back through
+ * the prologue: dq_raw, dk_raw by feature_map_bwd, d b_logit = dbeta beta (1 - beta),
+ * d l_logit = dlam lam (1 - lam), d a_logit = -dalpha alpha (1 - alpha) (alpha =
+ * exp(-softplus(a)) = sigmoid(-a)).  Outputs as oracle_qdelta_bwd with the logits'
+ * gradients in place of the gates'. */
+int oracle_qdelta_bwd_prologue(int B, int T, int H, int dk, int dv,
+                               const double *q_raw, const double *k_raw, const double *v,
+                               const double *a_logit, const double *b_logit, const double *l_logit,
+                               const double *S0, const double *dO, const double *dS_final,
+                               double *dq_raw, double *dk_raw, double *dv_out, double *da_logit,
+                               double *db_logit, double *dl_logit, double *dS0, int nthreads)
+{
+    if ((da_logit && !a_logit) || (dl_logit && !l_logit)) return 2;
+    const size_t nt = (size_t)B * T * H;
+    double *q = malloc(sizeof(double) * nt * dk), *k = malloc(sizeof(double) * nt * dk);
+    double *dq = malloc(sizeof(double) * nt * dk), *dkk = malloc(sizeof(double) * nt * dk);
+    double *al = a_logit ? malloc(sizeof(double) * nt) : NULL, *be = malloc(sizeof(double) * nt);
+    double *lm = l_logit ? malloc(sizeof(double) * nt) : NULL;
+    double *dal = a_logit ? malloc(sizeof(double) * nt) : NULL, *dbe = malloc(sizeof(double) * nt);
+    double *dlm = l_logit ? malloc(sizeof(double) * nt) : NULL;
+    int rc = 1;
+    if (q && k && dq && dkk && be && dbe && (!a_logit || (al && dal)) && (!l_logit || (lm && dlm))) {
+        for (size_t i = 0; i < nt; ++i) {
+            feature_map(q_raw + i * dk, q + i * dk, dk);
+            feature_map(k_raw + i * dk, k + i * dk, dk);
+            be[i] = sigmoid(b_logit[i]);
+            if (al) al[i] = exp_neg_softplus(a_logit[i]);
+            if (lm) lm[i] = sigmoid(l_logit[i]);
+        }
+        rc = oracle_qdelta_bwd(B, T, H, dk, dv, q, k, v, al, be, lm, S0, dO, dS_final, dq, dkk, dv_out,
+                               dal, dbe, dlm, dS0, nthreads);
+        if (!rc)
+            for (size_t i = 0; i < nt; ++i) {
+                feature_map_bwd(q_raw + i * dk, dq + i * dk, dq_raw + i * dk, dk);
+                feature_map_bwd(k_raw + i * dk, dkk + i * dk, dk_raw + i * dk, dk);
+                db_logit[i] = dbe[i] * be[i] * (1.0 - be[i]);
+                if (da_logit) da_logit[i] = -dal[i] * al[i] * (1.0 - al[i]);
+                if (dl_logit) dl_logit[i] = dlm[i] * lm[i] * (1.0 - lm[i]);
+            }
+    }
+    free(q); free(k); free(dq); free(dkk); free(al); free(be); free(lm); free(dal); free(dbe); free(dlm);
     return rc;
 }
 

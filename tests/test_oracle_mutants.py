@@ -387,3 +387,45 @@ def test_oracle_passes_eda_pins():
                                   "output_before_write"])
 def test_eda_mutant_rejected(kind):
     assert not eda_pins_hold(_eda_mutant(kind))
+
+
+# ---------------------------------------------------------------- prologue backward
+
+def _feature_map_bwd(kind=None):
+    """dx of y = SiLU(x)/|SiLU(x)| for an incoming dy, with an optional planted mistake."""
+    def bwd(x, dy):
+        sg = 1.0 / (1.0 + np.exp(-x))
+        s = x * sg
+        n = np.linalg.norm(s)
+        y = s / n
+        ds = dy / n if kind == "no_projection" else (dy - y * (y @ dy)) / (1.0 if kind == "no_norm" else n)
+        dsilu = sg if kind == "silu_derivative_is_sigmoid" else sg * (1.0 + x * (1.0 - sg))
+        return ds * dsilu
+    return bwd
+
+
+def feature_map_bwd_pins_hold(bwd):
+    """Central differences of the oracle's prologue forward at one token (T = 1, S0 = 0):
+    with beta = 1, v = e_1 and dO = e_1, o = (k . q) e_1, so dL/dq_raw = J_q^T k."""
+    d = 5
+    for _ in range(3):
+        xq, xk = rng.standard_normal(d), rng.standard_normal(d)
+        sh = lambda a: np.asarray(a, dtype=np.float64).reshape(1, 1, 1, -1)
+        v = np.zeros(d)
+        v[0] = 1.0
+        blog = np.array([[[50.0]]])                          # beta = 1 to double precision
+        fwd = lambda x: oracle.qdelta_fwd_prologue(sh(x), sh(xk), sh(v), None, blog, None, None)[0][0, 0, 0, 0]
+        fd = np.array([(fwd(xq + 1e-6 * np.eye(d)[i]) - fwd(xq - 1e-6 * np.eye(d)[i])) / 2e-6 for i in range(d)])
+        sk = xk / (1.0 + np.exp(-xk))
+        if not np.allclose(bwd(xq, sk / np.linalg.norm(sk)), fd, atol=1e-7):
+            return False
+    return True
+
+
+def test_correct_feature_map_backward_passes_pin():
+    assert feature_map_bwd_pins_hold(_feature_map_bwd())
+
+
+@pytest.mark.parametrize("kind", ["no_projection", "no_norm", "silu_derivative_is_sigmoid"])
+def test_feature_map_backward_mutant_rejected(kind):
+    assert not feature_map_bwd_pins_hold(_feature_map_bwd(kind))

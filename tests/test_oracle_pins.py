@@ -756,3 +756,40 @@ def test_eda_bruteforce_transition_products(T):
             term = term @ A[u]
         ref = ref + term
     np.testing.assert_allclose(S[0, 0], ref, atol=1e-12)
+
+
+def _loss_prologue(q_raw, k_raw, v, a_l, b_l, l_l, S0, dO, dS):
+    o, S = oracle.qdelta_fwd_prologue(q_raw, k_raw, v, a_l, b_l, l_l, S0)
+    return float((o * dO).sum() + (S * dS).sum())
+
+
+@pytest.mark.parametrize("gates", ["all", "beta_only"])
+def test_prologue_backward_equals_finite_differences(gates):
+    """The backward from projections is the derivative of the (pinned) prologue forward:
+    central differences for every element of q_raw, k_raw, v, the logits and S0."""
+    B, T, H, dk, dv = 1, 6, 2, 4, 3
+    q_raw, k_raw = rng.standard_normal((B, T, H, dk)), rng.standard_normal((B, T, H, dk))
+    v = rng.standard_normal((B, T, H, dv))
+    a_l = rng.normal(-1.0, 0.5, (B, T, H)) if gates == "all" else None
+    b_l = rng.standard_normal((B, T, H))
+    l_l = rng.standard_normal((B, T, H)) if gates == "all" else None
+    S0, dS = rng.standard_normal((B, H, dv, dk)) * 0.3, rng.standard_normal((B, H, dv, dk))
+    dO = rng.standard_normal((B, T, H, dv))
+    g = oracle.qdelta_bwd_prologue(q_raw, k_raw, v, a_l, b_l, l_l, S0, dO, dS)
+    args = {"q": q_raw, "k": k_raw, "v": v, "alpha": a_l, "beta": b_l, "lam": l_l, "S0": S0}
+    for name, x in args.items():
+        if x is None:
+            assert g["d" + name] is None
+            continue
+        fd = np.zeros_like(x)
+        for i in np.ndindex(x.shape):
+            a = dict(args)
+            xp, xm = x.copy(), x.copy()
+            xp[i] += 1e-6
+            xm[i] -= 1e-6
+            a[name] = xp
+            lp = _loss_prologue(a["q"], a["k"], a["v"], a["alpha"], a["beta"], a["lam"], a["S0"], dO, dS)
+            a[name] = xm
+            lm = _loss_prologue(a["q"], a["k"], a["v"], a["alpha"], a["beta"], a["lam"], a["S0"], dO, dS)
+            fd[i] = (lp - lm) / 2e-6
+        np.testing.assert_allclose(g["d" + name], fd, atol=1e-6 * max(1.0, np.abs(fd).max()), err_msg=name)
