@@ -26,7 +26,8 @@ STATUS_NAMES = {0: "QD_OK", 1: "QD_ERR_ARG", 2: "QD_ERR_UNSUPPORTED", 3: "QD_ERR
                 4: "QD_ERR_TIMEOUT", 5: "QD_ERR_WORKSPACE"}
 EXPORTS = ("qdelta_fwd", "qdelta_fwd_prologue", "qdelta_workspace_bytes", "qed_fwd", "qed_fwd_variant",
            "qed_workspace_bytes", "qdelta_step", "qdelta_step_prologue", "qed_step", "qdelta_fwd_static_scratch",
-           "qdelta_bwd", "qdelta_bwd_workspace_bytes", "eda_fwd", "eda_workspace_bytes", "qd_device_status",
+           "qdelta_bwd", "qdelta_bwd_workspace_bytes", "qdelta_bwd_prologue", "qdelta_bwd_prologue_workspace_bytes",
+           "eda_fwd", "eda_workspace_bytes", "qd_device_status",
            "qd_selftest_bounded_wait",
            "qd_last_error",
            "qd_last_launch_count")
@@ -64,6 +65,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qed_workspace_bytes.argtypes = [I] * 7
     lib.qdelta_bwd.argtypes = [P] * 16 + [I] * 7 + [P, Z, P]
     lib.qdelta_bwd_workspace_bytes.argtypes = [I] * 7
+    lib.qdelta_bwd_prologue.argtypes = [P] * 16 + [I] * 7 + [P, Z, P]
+    lib.qdelta_bwd_prologue.restype = I
+    lib.qdelta_bwd_prologue_workspace_bytes.argtypes = [I] * 7
+    lib.qdelta_bwd_prologue_workspace_bytes.restype = Z
     lib.eda_fwd.argtypes = [P] * 8 + [I] * 7 + [P, Z, P]
     lib.eda_workspace_bytes.argtypes = [I] * 7
     lib.eda_fwd.restype = I
@@ -188,12 +193,14 @@ def qdelta_bwd_workspace_bytes(B, T, H, dk, dv, chunk=64, dtype=QD_BF16) -> int:
 
 
 def qdelta_bwd(q, k, v, alpha, beta, lam, S0, dO, dS_final=None, *, want_dS0=True, chunk=64, workspace=None,
-               stream=None):
+               stream=None, prologue=False):
     """Backward of qdelta_fwd: gradients of sum(dO * o) + sum(dS_final * S_final)
     (the C qdelta_bwd).  Inputs as for qdelta_fwd, dO [B,T,H,dv] in the inputs' dtype,
     dS_final [B,H,dv,dk] fp32 or None.  Returns a dict dq, dk, dv, dalpha (None when
     alpha is None), dbeta, dlam (None when lam is None), dS0 (fp32; None unless
-    want_dS0), the token and gate gradients in the inputs' dtype."""
+    want_dS0), the token and gate gradients in the inputs' dtype.  prologue=True: the
+    backward of qdelta_fwd(..., prologue=True), i.e. q, k are projections and alpha, beta,
+    lam logits, and the gradients are theirs (the C qdelta_bwd_prologue)."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     dt = q.dtype
@@ -211,12 +218,15 @@ def qdelta_bwd(q, k, v, alpha, beta, lam, S0, dO, dS_final=None, *, want_dS0=Tru
          "dlam": None if lam is None else torch.empty_like(lam),
          "dS0": torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device) if want_dS0 else None}
     code = _dtype_code(q)
-    workspace, wsb = _workspace(qdelta_bwd_workspace_bytes(B, T, H, dk, dv, chunk, code), workspace, q.device)
-    st = load_library().qdelta_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(lam), _ptr(S0),
+    lib = load_library()
+    nbytes = (lib.qdelta_bwd_prologue_workspace_bytes if prologue else lib.qdelta_bwd_workspace_bytes)(
+        B, T, H, dk, dv, chunk, code)
+    workspace, wsb = _workspace(nbytes, workspace, q.device)
+    st = (lib.qdelta_bwd_prologue if prologue else lib.qdelta_bwd)(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(lam), _ptr(S0),
                                    _ptr(dO), _ptr(dS_final), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
                                    _ptr(g["dalpha"]), _ptr(g["dbeta"]), _ptr(g["dlam"]), _ptr(g["dS0"]),
                                    B, T, H, dk, dv, chunk, code, _ptr(workspace), wsb, _stream(stream, q.device))
-    _check(st, "qdelta_bwd")
+    _check(st, "qdelta_bwd_prologue" if prologue else "qdelta_bwd")
     return g
 
 

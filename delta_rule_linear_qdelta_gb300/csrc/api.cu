@@ -189,6 +189,51 @@ qd_status qdelta_fwd(const void *q, const void *k, const void *v, const void *al
                            dtype, workspace, workspace_bytes, stream);
 }
 
+size_t qdelta_bwd_prologue_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype) {
+    if (B <= 0 || T <= 0 || H <= 0 || chunk != 64 || !head_dim_ok(dk) || !head_dim_ok(dv)) return 0;
+    return qd::prologue_bwd_buffers(B, T, H, dk, dtype).bwd + qdelta_bwd_workspace_bytes(B, T, H, dk, dv, chunk, dtype);
+}
+
+qd_status qdelta_bwd_prologue(const void *q_raw, const void *k_raw, const void *v, const void *a_logit,
+                              const void *b_logit, const void *l_logit, const float *S0, const void *dO,
+                              const float *dS_final, void *dq_raw, void *dk_raw, void *dv_out, void *da_logit,
+                              void *db_logit, void *dl_logit, float *dS0, int B, int T, int H, int dk, int dv,
+                              int chunk, qd_dtype dtype, void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
+    g_err[0] = 0;
+    const void *req[] = {q_raw, k_raw, v, b_logit, dO, dq_raw, dk_raw, dv_out, db_logit};
+    const void *opt[] = {a_logit, l_logit, S0, dS_final, da_logit, dl_logit, dS0, workspace};
+    qd_status st = check_fwd("qdelta_bwd_prologue", req, 9, opt, 8, B, T, H, dk, dv, chunk, dtype);
+    if (st != QD_OK) return st;
+    if ((double)B * H * ((T + 63) / 64) > 2147483647.0)
+        return fail(QD_ERR_ARG, "qdelta_bwd_prologue: B*H*chunks exceeds the grid limit");
+    if (B == 0 || H == 0) { g_launches = 0; return QD_OK; }
+    if (T == 0) { g_launches = 0; return empty_sequence(dS_final, dS0, B, H, dk, dv, stream); }
+    const size_t need = qdelta_bwd_prologue_workspace_bytes(B, T, H, dk, dv, chunk, dtype);
+    if (!workspace || workspace_bytes < need)
+        return fail(QD_ERR_WORKSPACE, "qdelta_bwd_prologue: workspace of %zu bytes needed, %zu given", need,
+                    workspace_bytes);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    const qd::PrologueBwdBuffers w = qd::prologue_bwd_buffers(B, T, H, dk, dtype);
+    qd::QDeltaBwdArgs raw{q_raw, k_raw, v, a_logit, b_logit, l_logit, S0, dO, dS_final, dq_raw, dk_raw, dv_out,
+                          da_logit, db_logit, dl_logit, dS0, B, T, H, dk, dv, nullptr, nullptr};
+    int n = 0;
+    cudaError_t e = qd::launch_prologue_map(raw, dtype, ws, stream, &n);
+    if (e == cudaSuccess) {
+        float *chk = reinterpret_cast<float *>(ws + w.bwd);
+        const size_t half = qdelta_bwd_workspace_bytes(B, T, H, dk, dv, chunk, dtype) / 2 / sizeof(float);
+        qd::QDeltaBwdArgs m{ws + w.q, ws + w.k, v, a_logit ? ws + w.a : nullptr, ws + w.b,
+                            l_logit ? ws + w.l : nullptr, S0, dO, dS_final, ws + w.dq, ws + w.dk, dv_out,
+                            a_logit ? ws + w.da : nullptr, ws + w.db, l_logit ? ws + w.dl : nullptr, dS0,
+                            B, T, H, dk, dv, chk, chk + half, 1, 1, q_raw, k_raw, a_logit, b_logit, l_logit};
+        e = qd::launch_qdelta_bwd(m, dtype, stream, &n);
+    }
+    if (e == cudaSuccess) e = qd::launch_prologue_chain(raw, dtype, ws, stream, &n);
+    if (e != cudaSuccess) return cuda_fail(e, "qdelta_bwd_prologue launch");
+    g_launches = n;
+    return QD_OK;
+}
+
 size_t eda_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype) {
     (void)B; (void)T; (void)H; (void)dk; (void)dv; (void)chunk; (void)dtype;
     return 0;

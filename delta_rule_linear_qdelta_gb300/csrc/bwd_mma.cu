@@ -93,9 +93,9 @@ __global__ void __launch_bounds__(kNT, 1) qdelta_bwd_dstate_mma_kernel(QDeltaBwd
             const int t = tid;
             const bool ok = t < n;
             const size_t tok = ((size_t)b * T + c0 + (ok ? t : 0)) * H + h;
-            ell[t] = (ok && a.alpha) ? logf(__bfloat162float(((const __nv_bfloat16 *)a.alpha)[tok])) : 0.f;
-            bet[t] = ok ? __bfloat162float(((const __nv_bfloat16 *)a.beta)[tok]) : 0.f;
-            lmb[t] = (ok && a.lam) ? __bfloat162float(((const __nv_bfloat16 *)a.lam)[tok]) : 0.f;
+            ell[t] = (ok && a.alpha) ? logf(gate_val<__nv_bfloat16>(a.alpha, tok, a.gates_f32)) : 0.f;
+            bet[t] = ok ? gate_val<__nv_bfloat16>(a.beta, tok, a.gates_f32) : 0.f;
+            lmb[t] = (ok && a.lam) ? gate_val<__nv_bfloat16>(a.lam, tok, a.gates_f32) : 0.f;
         }
         __syncthreads();
         if (tid < 32) {                                   // inclusive prefix of log alpha
@@ -281,9 +281,9 @@ __global__ void __launch_bounds__(kNT, 1) qdelta_bwd_grad_mma_kernel(QDeltaBwdAr
         const int t = tid;
         const bool ok = t < n;
         const size_t tok = tok_of(ok ? t : 0);
-        la[t] = (ok && a.alpha) ? logf(__bfloat162float(((const __nv_bfloat16 *)a.alpha)[tok])) : 0.f;
-        bet[t] = ok ? __bfloat162float(((const __nv_bfloat16 *)a.beta)[tok]) : 0.f;
-        lmb[t] = (ok && a.lam) ? __bfloat162float(((const __nv_bfloat16 *)a.lam)[tok]) : 0.f;
+        la[t] = (ok && a.alpha) ? logf(gate_val<__nv_bfloat16>(a.alpha, tok, a.gates_f32)) : 0.f;
+        bet[t] = ok ? gate_val<__nv_bfloat16>(a.beta, tok, a.gates_f32) : 0.f;
+        lmb[t] = (ok && a.lam) ? gate_val<__nv_bfloat16>(a.lam, tok, a.gates_f32) : 0.f;
         ell[t] = la[t];
         sb[t] = srow[t] = 0.f;
     }
@@ -570,20 +570,20 @@ __global__ void __launch_bounds__(kNT, 1) qdelta_bwd_grad_mma_kernel(QDeltaBwdAr
             part_l[(warp & 3) * kC + t_lo] = l_lo;
             part_l[(warp & 3) * kC + t_hi] = l_hi;
         }
+        auto put2 = [&](void *base, size_t idx, float x0, float x1) {   // two adjacent gradient entries
+            if (a.grad_f32) *reinterpret_cast<float2 *>((float *)base + idx) = make_float2(x0, x1);
+            else *reinterpret_cast<__nv_bfloat162 *>((__nv_bfloat16 *)base + idx) = __floats2bfloat162_rn(x0, x1);
+        };
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
             const int j = cb + 8 * nt + 2 * tq;
             if (t_lo < n) {
-                *reinterpret_cast<__nv_bfloat162 *>((__nv_bfloat16 *)a.dq + tok_of(t_lo) * kD + j) =
-                    __floats2bfloat162_rn(aQ[nt][0], aQ[nt][1]);
-                *reinterpret_cast<__nv_bfloat162 *>((__nv_bfloat16 *)a.dk + tok_of(t_lo) * kD + j) =
-                    __floats2bfloat162_rn(aK[nt][0], aK[nt][1]);
+                put2(a.dq, tok_of(t_lo) * kD + j, aQ[nt][0], aQ[nt][1]);
+                put2(a.dk, tok_of(t_lo) * kD + j, aK[nt][0], aK[nt][1]);
             }
             if (t_hi < n) {
-                *reinterpret_cast<__nv_bfloat162 *>((__nv_bfloat16 *)a.dq + tok_of(t_hi) * kD + j) =
-                    __floats2bfloat162_rn(aQ[nt][2], aQ[nt][3]);
-                *reinterpret_cast<__nv_bfloat162 *>((__nv_bfloat16 *)a.dk + tok_of(t_hi) * kD + j) =
-                    __floats2bfloat162_rn(aK[nt][2], aK[nt][3]);
+                put2(a.dq, tok_of(t_hi) * kD + j, aQ[nt][2], aQ[nt][3]);
+                put2(a.dk, tok_of(t_hi) * kD + j, aK[nt][2], aK[nt][3]);
             }
         }
     }
@@ -610,11 +610,13 @@ __global__ void __launch_bounds__(kNT, 1) qdelta_bwd_grad_mma_kernel(QDeltaBwdAr
     __syncthreads();
     if (tid < n) {
         const size_t tok = tok_of(tid);
-        ((__nv_bfloat16 *)a.dbeta)[tok] = __float2bfloat16_rn(sb[tid]);
-        if (a.dalpha && a.alpha) ((__nv_bfloat16 *)a.dalpha)[tok] = __float2bfloat16_rn(srow[tid] / expf(la[tid]));
-        if (a.dlam && a.lam)
-            ((__nv_bfloat16 *)a.dlam)[tok] =
-                __float2bfloat16_rn(((part_l[tid] + part_l[kC + tid]) + part_l[2 * kC + tid]) + part_l[3 * kC + tid]);
+        auto put1 = [&](void *base, float x) {
+            if (a.grad_f32) ((float *)base)[tok] = x;
+            else ((__nv_bfloat16 *)base)[tok] = __float2bfloat16_rn(x);
+        };
+        put1(a.dbeta, sb[tid]);
+        if (a.dalpha && a.alpha) put1(a.dalpha, srow[tid] / expf(la[tid]));
+        if (a.dlam && a.lam) put1(a.dlam, ((part_l[tid] + part_l[kC + tid]) + part_l[2 * kC + tid]) + part_l[3 * kC + tid]);
     }
 }
 

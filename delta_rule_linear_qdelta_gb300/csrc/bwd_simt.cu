@@ -86,9 +86,9 @@ __device__ __forceinline__ void load_gates(const QDeltaBwdArgs &a, int b, int h,
         const int t = threadIdx.x;
         const bool ok = t < n;
         const size_t tok = ((size_t)b * a.T + c0 + (ok ? t : 0)) * a.H + h;
-        la[t] = (ok && a.alpha) ? logf(to_f(((const TIn *)a.alpha)[tok])) : 0.f;
-        bet[t] = ok ? to_f(((const TIn *)a.beta)[tok]) : 0.f;
-        lmb[t] = (ok && a.lam) ? to_f(((const TIn *)a.lam)[tok]) : 0.f;
+        la[t] = (ok && a.alpha) ? logf(gate_val<TIn>(a.alpha, tok, a.gates_f32)) : 0.f;
+        bet[t] = ok ? gate_val<TIn>(a.beta, tok, a.gates_f32) : 0.f;
+        lmb[t] = (ok && a.lam) ? gate_val<TIn>(a.lam, tok, a.gates_f32) : 0.f;
     }
 }
 
@@ -478,8 +478,13 @@ __global__ void __launch_bounds__(kNTg) qdelta_bwd_grad_kernel(QDeltaBwdArgs a) 
             dl_p = fmaf(dx, Qs[r * LK + j], dl_p);
             wz_p = fmaf(accK[m], Ks[r * LK + j], wz_p);
             if (r < n) {
-                ((TIn *)a.dq)[tok * DK + j] = from_f<TIn>(dq);
-                ((TIn *)a.dk)[tok * DK + j] = from_f<TIn>(dkk);
+                if (a.grad_f32) {
+                    ((float *)a.dq)[tok * DK + j] = dq;
+                    ((float *)a.dk)[tok * DK + j] = dkk;
+                } else {
+                    ((TIn *)a.dq)[tok * DK + j] = from_f<TIn>(dq);
+                    ((TIn *)a.dk)[tok * DK + j] = from_f<TIn>(dkk);
+                }
             }
         }
 #pragma unroll
@@ -489,7 +494,10 @@ __global__ void __launch_bounds__(kNTg) qdelta_bwd_grad_kernel(QDeltaBwdArgs a) 
         }
         if (jc == 0) {
             wz[r] = wC[r] * wz_p;
-            if (r < n && a.dlam && a.lam) ((TIn *)a.dlam)[tok] = from_f<TIn>(dl_p);
+            if (r < n && a.dlam && a.lam) {
+                if (a.grad_f32) ((float *)a.dlam)[tok] = dl_p;
+                else ((TIn *)a.dlam)[tok] = from_f<TIn>(dl_p);
+            }
         }
     }
     __syncthreads();
@@ -507,8 +515,14 @@ __global__ void __launch_bounds__(kNTg) qdelta_bwd_grad_kernel(QDeltaBwdArgs a) 
     __syncthreads();
     if (tid < n) {
         const size_t tok = ((size_t)b * T + c0 + tid) * H + h;
-        ((TIn *)a.dbeta)[tok] = from_f<TIn>(sb[tid]);
-        if (a.dalpha && a.alpha) ((TIn *)a.dalpha)[tok] = from_f<TIn>(sq[tid] / expf(la[tid]));
+        const float dal = sq[tid] / expf(la[tid]);
+        if (a.grad_f32) {
+            ((float *)a.dbeta)[tok] = sb[tid];
+            if (a.dalpha && a.alpha) ((float *)a.dalpha)[tok] = dal;
+        } else {
+            ((TIn *)a.dbeta)[tok] = from_f<TIn>(sb[tid]);
+            if (a.dalpha && a.alpha) ((TIn *)a.dalpha)[tok] = from_f<TIn>(dal);
+        }
     }
 }
 
@@ -568,8 +582,10 @@ size_t qdelta_bwd_workspace(int B, int T, int H, int dk, int dv) {
 cudaError_t launch_qdelta_bwd(const QDeltaBwdArgs &a, int dtype, cudaStream_t s, int *nlaunch) {
     // 1. forward over the chunks, keeping the state entering each (the tensor-core
     //    kernel where it applies, without its output)
-    QDeltaArgs f{a.q, a.k, a.v, a.alpha, a.beta, a.lam, a.S0, nullptr, nullptr, a.B, a.T, a.H, a.nk, a.nv,
-                 nullptr, 0, 0, a.S_chk};
+    const bool pro = a.raw_q != nullptr;              // from projections: the prologue forward
+    QDeltaArgs f{pro ? a.raw_q : a.q, pro ? a.raw_k : a.k, a.v, pro ? a.raw_a : a.alpha, pro ? a.raw_b : a.beta,
+                 pro ? a.raw_l : a.lam, a.S0, nullptr, nullptr, a.B, a.T, a.H, a.nk, a.nv, nullptr, 0, pro ? 1 : 0,
+                 a.S_chk};
     cudaError_t e = qdelta_tc_supported(f, dtype) ? launch_qdelta_chunk_tc(f, s, nlaunch, kTcNoO)
                                                   : launch_qdelta_chunk_simt(f, dtype, s, nlaunch);
     if (e != cudaSuccess) return e;

@@ -811,9 +811,9 @@ cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nla
         return cudaErrorInvalidValue;
     if (flags & kTcNoO) mo = mq;                      // not used
     else if (!make_token_map(&mo, a.o, a.B, a.T, a.H)) return cudaErrorInvalidValue;
-    auto kern = a.S_chk ? qdelta_fwd_tc_kernel<false, true>
+    auto kern = a.S_chk ? (a.prologue ? qdelta_fwd_tc_kernel<true, true> : qdelta_fwd_tc_kernel<false, true>)
               : a.prologue ? qdelta_fwd_tc_kernel<true> : qdelta_fwd_tc_kernel<false>;
-    if (a.S_chk && (a.prologue || !(flags & kTcNoO))) return cudaErrorInvalidValue;
+    if (a.S_chk && !(flags & kTcNoO)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     TcParams p{(const __nv_bfloat16 *)a.alpha, (const __nv_bfloat16 *)a.beta, (const __nv_bfloat16 *)a.lam,

@@ -68,7 +68,20 @@ struct QDeltaBwdArgs {
     float *dS0;
     int B, T, H, nk, nv;
     float *S_chk, *dS_chk;
+    int grad_f32;     // dq, dk, dalpha, dbeta, dlam written as fp32 whatever the dtype (for the
+                      // prologue's chain rule, which would otherwise see them rounded)
+    int gates_f32;    // alpha, beta, lam are fp32 arrays whatever the dtype (gates mapped from
+                      // logits: alpha near 1 rounded to bf16 would lose most of log alpha)
+    // backward from projections: the raw inputs, from which the checkpoint forward runs
+    // with the prologue (null otherwise)
+    const void *raw_q, *raw_k, *raw_a, *raw_b, *raw_l;
 };
+
+// A gate value of token `tok`: fp32 when f32, else the call's dtype.
+template <typename TIn>
+__device__ __forceinline__ float gate_val(const void *p, size_t tok, int f32) {
+    return f32 ? static_cast<const float *>(p)[tok] : to_f(static_cast<const TIn *>(p)[tok]);
+}
 
 // Arguments of one EDA forward (erase along e, then the Delta write): q, k, e
 // [B][T][H][dk], v, o [B][T][H][dv], beta [B][T][H] or NULL (= 1).
@@ -127,6 +140,17 @@ cudaError_t launch_qdelta_chunk_simt(const QDeltaArgs &a, int dtype, cudaStream_
 // the per-chunk gradient kernel.  qdelta_bwd_workspace is the workspace it needs.
 size_t qdelta_bwd_workspace(int B, int T, int H, int dk, int dv);
 cudaError_t launch_qdelta_bwd(const QDeltaBwdArgs &a, int dtype, cudaStream_t s, int *nlaunch);
+// Backward from projections: byte offsets in its workspace (the mapped inputs q, k,
+// alpha, beta, lambda; their gradients; the recurrence backward's own workspace from
+// `bwd` on), and the two kernels around qdelta_bwd.  `raw` carries the projections and
+// logits in q, k, alpha, beta, lam and the caller's outputs in dq, dk, dalpha, dbeta, dlam.
+struct PrologueBwdBuffers {
+    size_t q, k, a, b, l, dq, dk, da, db, dl, bwd;
+};
+PrologueBwdBuffers prologue_bwd_buffers(int B, int T, int H, int dk, int dtype);
+cudaError_t launch_prologue_map(const QDeltaBwdArgs &raw, int dtype, uint8_t *ws, cudaStream_t s, int *nlaunch);
+cudaError_t launch_prologue_chain(const QDeltaBwdArgs &raw, int dtype, const uint8_t *ws, cudaStream_t s,
+                                  int *nlaunch);
 // The reverse sweep and the per-chunk gradients on the warp tensor cores (TF32):
 // bf16 with dk = dv = 128.
 bool qdelta_bwd_mma_supported(const QDeltaBwdArgs &a, int dtype);

@@ -219,6 +219,30 @@ QD_API qd_status qdelta_bwd(const void *q, const void *k, const void *v,
 QD_API size_t qdelta_bwd_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype);
 
 /*
+ * qdelta_bwd_prologue -- backward of qdelta_fwd_prologue: the gradients of the same L
+ * as qdelta_bwd with respect to the projections q_raw, k_raw, v, the gate logits and
+ * S0.  The inputs go through the prologue's maps (see qdelta_fwd_prologue; fp32
+ * arithmetic, stored in the call's dtype), the recurrence's backward runs on them
+ * (qdelta_bwd), and the chain rule takes the gradients back through the maps:
+ *     with s = SiLU(x), n = |s|, y = s / n:  dx = ((dy - y (y . dy)) / n) * SiLU'(x)
+ *     d b_logit = dbeta beta (1 - beta),  d l_logit = dlam lam (1 - lam),
+ *     d a_logit = -dalpha alpha (1 - alpha)          (alpha = exp(-softplus) = sigmoid(-a))
+ * An all-zero SiLU row (left zero by the forward) passes no gradient.  Arguments and
+ * outputs as qdelta_bwd with the raw inputs and the logits' gradients in place of the
+ * mapped ones (dq_raw, dk_raw [B][T][H][dk]; da_logit, db_logit, dl_logit [B][T][H]).
+ * workspace: at least qdelta_bwd_prologue_workspace_bytes(...) bytes.
+ */
+QD_API qd_status qdelta_bwd_prologue(const void *q_raw, const void *k_raw, const void *v,
+                                     const void *a_logit, const void *b_logit, const void *l_logit,
+                                     const float *S0, const void *dO, const float *dS_final,
+                                     void *dq_raw, void *dk_raw, void *dv_out, void *da_logit, void *db_logit,
+                                     void *dl_logit, float *dS0, int B, int T, int H, int dk, int dv, int chunk,
+                                     qd_dtype dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of device workspace qdelta_bwd_prologue needs for these sizes. */
+QD_API size_t qdelta_bwd_prologue_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype);
+
+/*
  * eda_fwd -- erase-then-delta forward ("Erase-then-Delta Attention", core method:
  * a targeted erase along a direction e, then the Delta write along the key).  Per
  * (b, h), with the memory M (d_k x d_v), stored as S = M^T in the state layout:

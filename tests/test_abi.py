@@ -162,3 +162,16 @@ def test_eda_arguments_checked(lib):
 def test_bounded_wait_selftest_limit_checked(lib):
     assert lib.qd_selftest_bounded_wait(0, None) == qd.QD_ERR_ARG
     assert lib.qd_selftest_bounded_wait(2000000, None) == qd.QD_ERR_ARG
+
+
+def test_prologue_backward_arguments_checked(lib):
+    g = ctypes.c_void_p(256)
+    args = lambda **kw: [kw.get(n, g) for n in ("q", "k", "v", "a", "b", "l", "S0", "dO", "dS",
+                                               "dq", "dk", "dv", "da", "db", "dl", "dS0")]
+    st = lib.qdelta_bwd_prologue(*args(b=None), 1, 8, 1, 64, 64, 64, qd.QD_BF16, g, 1 << 30, None)
+    assert st == qd.QD_ERR_ARG and "qdelta_bwd_prologue" in qd.qd_last_error()
+    need = lib.qdelta_bwd_prologue_workspace_bytes(1, 8, 1, 64, 64, 64, qd.QD_BF16)
+    assert need > lib.qdelta_bwd_workspace_bytes(1, 8, 1, 64, 64, 64, qd.QD_BF16)
+    st = lib.qdelta_bwd_prologue(*args(), 1, 8, 1, 64, 64, 64, qd.QD_BF16, g, need - 16, None)
+    assert st == qd.QD_ERR_WORKSPACE
+    assert lib.qdelta_bwd_prologue(*([None] * 16), 0, 8, 4, 64, 64, 64, 1, None, 0, None) == qd.QD_OK

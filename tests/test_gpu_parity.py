@@ -649,3 +649,26 @@ def test_backward_and_eda_deterministic(qd):
     o1, S1 = run_eda(qd, e)
     o2, S2 = run_eda(qd, e)
     assert np.array_equal(o1, o2) and np.array_equal(S1, S2)
+
+
+@pytest.mark.parametrize("dt,dh,gates", [("bf16", 128, "all"), ("f32", 64, "all"), ("f32", 32, "beta_only")])
+def test_prologue_backward_all_gradients(qd, dt, dh, gates):
+    """Backward from projections and logits against the oracle's chain rule through the
+    prologue: 2 full chunks + a ragged tail, carried S0 and dS_final."""
+    d = synth.qdelta_raw_inputs(2, 150, 2, dh, dh, seed=78, dtype=dt, s0_var=0.01)
+    if gates == "beta_only":
+        d["alpha"], d["lam"] = None, None
+    c = synth.cotangents(2, 150, 2, dh, dh, seed=78, dtype=dt)
+    tt = tdt(d)
+    g = qd.qdelta_bwd(dev(d["q"], tt), dev(d["k"], tt), dev(d["v"], tt), dev(d["alpha"], tt), dev(d["beta"], tt),
+                      dev(d["lam"], tt), dev(d["S0"], torch.float32), dev(c["dO"], tt),
+                      dev(c["dS_final"], torch.float32), prologue=True)
+    torch.cuda.synchronize()
+    assert qd.last_launch_count() == 5
+    ref = oracle.qdelta_bwd_prologue(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["lam"], d["S0"], c["dO"],
+                                     c["dS_final"])
+    for name in GRAD_NAMES:
+        if ref[name] is None:
+            assert g[name] is None, name
+            continue
+        check_grad(g[name].float().cpu().numpy(), ref[name], dt, f"prologue bwd {dt} {name}")
