@@ -260,8 +260,9 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
         // (2) k_t . u_t per token (one warp per token; u = b*q, or the ablation arm's
         // q, b*z_h) and W*V in place of V
         if (proj)
-        for (int t = warp; t < kC; t += kThreads / 32) {
-            const int j = 4 * lane;
+#pragma unroll
+        for (int it = 0; it < kC / (kThreads / 32); ++it) {   // unrolled: the eight reductions overlap
+            const int t = warp + (kThreads / 32) * it, j = 4 * lane;
             const uint32_t o8 = tile_off(t, j, 8192), o16 = tile_off(t, j, 16384);
             const uint2 kk = *reinterpret_cast<const uint2 *>(sm + OFF_K + o8);
             const uint2 bb = *reinterpret_cast<const uint2 *>(sm + OFF_BT + o8);
