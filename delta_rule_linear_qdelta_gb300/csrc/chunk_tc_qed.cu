@@ -299,6 +299,7 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
         {
             const int j = tid & 127, half = tid >> 7;
             float sum = 0.f;
+#pragma unroll 8
             for (int t = 32 * half; t < 32 * half + 32; ++t)
                 sum += bf(*reinterpret_cast<const __nv_bfloat16 *>(sm + OFF_G + tile_off(t, j, 8192)));
             g_ps[half][j] = sum;
@@ -310,6 +311,7 @@ qed_fwd_tc_kernel(const QedTcParams p, const __grid_constant__ QedMaps mp) {
             const int j = tid & 127, half = tid >> 7;
             float G = half ? g_ps[0][j] : 0.f;
             const float zj = zrow ? zrow[j] : 0.f;
+#pragma unroll 8
             for (int t = 32 * half; t < 32 * half + 32; ++t) {
                 const uint32_t o8 = tile_off(t, j, 8192), o16 = tile_off(t, j, 16384);
                 G += bf(*reinterpret_cast<const __nv_bfloat16 *>(sm + OFF_G + o8));
