@@ -250,8 +250,9 @@ __global__ void __launch_bounds__(kNT, 1) qdelta_bwd_grad_mma_kernel(QDeltaBwdAr
     float *dSq = Sq + kQV * LS;                                       // [kQV][LS]  dS_out rows
     float *Rq = dSq + kQV * LS;                                       // [C][LR]    V - XS
     float *Zq = Rq + kC * LR;                                         // [C][LR]
-    float *dRq = Zq + kC * LR;                                        // [C][LR]    dZ, then dR
-    float *Mm = dRq + kC * LR;                                        // [C][LA]    M -> dA * M
+    float *dRq = Zq + kC * LR;                                        // [C][LR]    dR
+    float *dZq = dRq + kC * LR;                                       // [C][LR]    dZ
+    float *Mm = dZq + kC * LR;                                        // [C][LA]    M -> dA * M
     float *Pm = Mm + kC * LA;                                         // [C][LA]    P -> E
     float *Tm = Pm + kC * LA;                                         // [C][LA]    T, then dR scratch
     float *dAm = Tm + kC * LA;                                        // [C][LA]    sum dR Z^T -> H * dM
@@ -402,12 +403,12 @@ __global__ void __launch_bounds__(kNT, 1) qdelta_bwd_grad_mma_kernel(QDeltaBwdAr
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int t = r0 + g + 8 * (e >> 1), d = n0 + 8 * nt + 2 * tq + (e & 1);
-                        dRq[t * LR + d] = acc[nt][e];
+                        dZq[t * LR + d] = acc[nt][e];
                     }
             }
         }
         __syncthreads();
-        // warps 0-7: Z = T diag(beta) R; warps 8-15: dR = T^T dZ (into Tm's spare columns? no: registers)
+        // warps 0-7: Z = T diag(beta) R; warps 8-15: dR = T^T dZ (separate buffers: no barrier between)
         {
             const int w8 = warp & 7, r0 = 16 * (w8 >> 1), n0 = 16 * (w8 & 1);
             float acc[2][4] = {};
@@ -416,8 +417,7 @@ __global__ void __launch_bounds__(kNT, 1) qdelta_bwd_grad_mma_kernel(QDeltaBwdAr
                                  [&](int kk, int nn) { return bet[kk] * Rq[kk * LR + n0 + nn]; });
             else
                 mma_strip<kC, 2>(acc, r0, [&](int r, int kk) { return Tm[kk * LA + r0 + r]; },
-                                 [&](int kk, int nn) { return dRq[kk * LR + n0 + nn]; });
-            __syncthreads();                              // every read of dZ done before dR replaces it
+                                 [&](int kk, int nn) { return dZq[kk * LR + n0 + nn]; });
             float *dst = warp < 8 ? Zq : dRq;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
@@ -621,7 +621,7 @@ __global__ void __launch_bounds__(kNT, 1) qdelta_bwd_grad_mma_kernel(QDeltaBwdAr
 }
 
 constexpr size_t kGradSmem = (2 * kC * LQ + 2 * kC * LV4) * sizeof(__nv_bfloat16) +
-                             sizeof(float) * (2 * kQV * LS + 3 * kC * LR + 5 * kC * LA + 8 * kC + kNT / 32 + 12 * kC);
+                             sizeof(float) * (2 * kQV * LS + 4 * kC * LR + 5 * kC * LA + 8 * kC + kNT / 32 + 12 * kC);
 
 }  // namespace
 
