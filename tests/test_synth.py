@@ -41,3 +41,26 @@ def test_mean_alpha_bisection():
     z = synth.normal(9, 9, 200000, mean=mu, std=0.5)
     assert abs(np.mean(np.exp(-np.logaddexp(0, z))) - 0.995) < 2e-4
     assert -5.6 < mu < -5.2
+
+
+def test_backward_prologue_and_eda_generators():
+    """The cotangent, projection and EDA generators: seeded, of the stated shapes and
+    distributions, and independent of each other's streams."""
+    c1 = synth.cotangents(2, 10, 3, 16, 8, seed=5, dtype="bf16")
+    c2 = synth.cotangents(2, 10, 3, 16, 8, seed=5, dtype="bf16")
+    assert c1["dO"].shape == (2, 10, 3, 8) and c1["dS_final"].shape == (2, 3, 8, 16)
+    assert np.array_equal(c1["dO"], c2["dO"]) and np.array_equal(c1["dS_final"], c2["dS_final"])
+    assert synth.cotangents(1, 4, 1, 16, 16, seed=5, final_state=False)["dS_final"] is None
+    big = synth.cotangents(1, 512, 4, 64, 64, seed=6, dtype="f32")
+    assert abs(big["dO"].mean()) < 0.02 and abs(big["dO"].std() - 1.0) < 0.02
+
+    r = synth.qdelta_raw_inputs(1, 256, 4, 64, 64, seed=7, dtype="f32")
+    assert abs(np.linalg.norm(r["q"], axis=-1).mean() - 8.0) < 0.5           # raw: |q| ~ sqrt(64)
+    assert abs(r["alpha"].mean() + 4.0) < 0.05 and abs(r["alpha"].std() - 0.5) < 0.05
+    assert abs(r["beta"].mean()) < 0.1 and abs(r["beta"].std() - 1.0) < 0.1
+
+    e = synth.eda_inputs(1, 64, 2, 32, 32, seed=8, dtype="f32")
+    np.testing.assert_allclose(np.linalg.norm(e["e"], axis=-1), 1.0, atol=1e-6)
+    assert not np.allclose(e["e"], e["q"])
+    eq = synth.eda_inputs(1, 64, 2, 32, 32, seed=8, dtype="f32", erase="query", beta=False)
+    assert np.array_equal(eq["e"], eq["q"]) and eq["beta"] is None
