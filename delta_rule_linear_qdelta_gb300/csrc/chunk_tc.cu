@@ -40,6 +40,12 @@
 //               P[c&1], U[c&1] and chunk c's stage are free
 // The chain group also issues the TMA loads of chunk c+2 into chunk c's stage.
 //
+// Instruction economy on both groups (they share each SM sub-partition's issue slots):
+// the output accumulator leaves TMEM in the 16x256b shape, so a thread holds two
+// adjacent tokens of a d_v row and the o tile is written as transposed 16-byte
+// stmatrix rows; elementwise scalings (state rescale, Zt packing, masks, X = K + lambda Q)
+// use packed f32x2 arithmetic; -W is packed first and its bf16 sign bits flipped.
+//
 // Shared memory (offsets from a 1024-aligned base):
 //   stage s in {0,1}: XQ 32 KB (per 64-column panel: X rows 0-63 | Q rows 64-127),
 //                     K 16 KB (scaled in place to kappa*K under strong decay), V 16 KB
