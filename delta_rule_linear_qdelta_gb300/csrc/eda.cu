@@ -6,17 +6,20 @@
 // o = S q.
 //
 // A recurrent kernel in fp32, one CTA per (b, h): the state stays in registers for
-// the whole sequence, row i of S spread over TPR = 4 threads (8 measured slower: the
-// same issue count with one more shuffle level), and each token costs three row-dot
-// products (S e, S k, S q), each reduced over those threads by shuffles, and two
-// rank-one updates: 5 dv dk multiply-adds.  The token
+// the whole sequence, and each token costs three row-dot products (S e, S k, S q), each
+// reduced over the threads of a row by shuffles, and two rank-one updates: 5 dv dk
+// multiply-adds.  The kernel is issue bound, so the thread layout is chosen to spend the
+// fewest instructions beside those multiply-adds: for d_k >= 64 a thread holds two state
+// rows over 16 columns, so each token slice it unpacks from bf16 and each shared-memory
+// read serve two rows (7 % faster than one row over 32 columns at d_k = 128); one row
+// over 8 threads measured slower (one more shuffle level, no fewer unpacks).  The token
 // vectors are staged in shared memory a tile of 16 tokens at a time by asynchronous
 // copies (cp.async), the next tile's in flight while the current one is consumed, and
 // converted to fp32 as they are read (a separate fp32 tile measured slower: twice the
-// shared-memory reads).  The kernel is issue bound, not latency bound: folding the two
-// updates of a token into one (three row-dot products in one pass against the token
-// scalars e.k, e.q, k.q, computed once per tile) measured 13 % slower, as many
-// instructions plus a barrier per tile.
+// shared-memory reads).  Folding the two updates of a token into one (three row-dot
+// products in one pass against the token scalars e.k, e.q, k.q, computed once per tile)
+// shortens the dependency chain but measured 13 % slower: as many instructions plus a
+// barrier per tile.
 //
 // Why not the chunked tensor-core forward: EDA is the Delta rule over the 2T
 // sub-tokens (e_t, 0, beta 1), (k_t, v_t, beta_t), and that runs through the chunked
@@ -84,8 +87,13 @@ struct TokenLayout {
     }
 };
 
-template <typename TIn, int DK, int TPR>
-__global__ void __launch_bounds__(TPR * 128, 1) eda_recurrent_kernel(EdaArgs a) {
+// R state rows per thread (1 or 2) over TPR threads per row.  With R = 2 a thread holds
+// rows rg and rg + dv/2 (rg = tid / TPR) over the same d_k/TPR columns, so one unpacked
+// token slice serves two rows.  Its "own" row is the one whose reduction it completes:
+// the first for the lower half of the row's TPR threads, the second for the upper half.
+template <typename TIn, int DK, int TPR, int R>
+__global__ void __launch_bounds__(TPR * 128 / R, 1) eda_recurrent_kernel(EdaArgs a) {
+    static_assert(R == 1 || R == 2, "one or two rows per thread");
     using L = TokenLayout<TIn, DK, TPR>;
     constexpr int NS = L::NS, SL = L::SL, VS = L::VS, E = L::E;
     constexpr int P8 = 8 / E;                         // elements per 8-byte copy
@@ -97,18 +105,22 @@ __global__ void __launch_bounds__(TPR * 128, 1) eda_recurrent_kernel(EdaArgs a) 
     float *bet = reinterpret_cast<float *>(smraw + (size_t)2 * kTile * TS * E);   // [2][kTile]
     float *obuf = bet + 2 * kTile;                                                // [kTile][dv]
 
-    const int tid = threadIdx.x, row = tid / TPR, s = tid % TPR;
+    const int tid = threadIdx.x, rg = tid / TPR, s = tid % TPR;
+    const bool upper = R == 2 && (s & (TPR / 2));
+    const int row = upper ? rg + dv / 2 : rg;         // own row
+    const int row2 = upper ? rg : rg + dv / 2;        // the other row (R == 2)
     const int bh = blockIdx.x, b = bh / H, h = bh % H;
     const TIn *q = (const TIn *)a.q, *k = (const TIn *)a.k, *v = (const TIn *)a.v, *e = (const TIn *)a.e;
     const TIn *beta = (const TIn *)a.beta;
-    const int nthreads = TPR * dv;
+    const int nthreads = TPR * dv / R;
     const int per_tok = (3 * DK + dv) / P8;           // 8-byte copies per token
 
-    float S[NS];
-    {
-        const size_t base = ((size_t)bh * dv + row) * DK + s * NS;
+    float S[R][NS];                                   // S[0]: own row, S[1]: the other row
 #pragma unroll
-        for (int j = 0; j < NS; ++j) S[j] = a.S0 ? a.S0[base + j] : 0.f;
+    for (int r = 0; r < R; ++r) {
+        const size_t base = ((size_t)bh * dv + (r ? row2 : row)) * DK + s * NS;
+#pragma unroll
+        for (int j = 0; j < NS; ++j) S[r][j] = a.S0 ? a.S0[base + j] : 0.f;
     }
     // issue the asynchronous copies of tile `tile` into buffer `buf` (tokens past T are
     // not copied: their staged values are never read); beta of token tid of the tile is
@@ -136,6 +148,9 @@ __global__ void __launch_bounds__(TPR * 128, 1) eda_recurrent_kernel(EdaArgs a) 
         if (tid < nt) bv = beta ? to_f(beta[((size_t)b * T + t0 + tid) * H + h]) : 1.f;
         return bv;
     };
+    // the own row's dot product with x, reduced over the row's TPR threads.  With R = 2
+    // the first shuffle level also trades: a thread sends its partial of the other row
+    // and receives its partner's partial of its own row (the partner's other row).
     auto rowdot = [&](const TIn *x) {                 // packed pairs: one instruction per two products
         float2 pa = make_float2(0.f, 0.f), pb = make_float2(0.f, 0.f);
 #pragma unroll
@@ -144,26 +159,49 @@ __global__ void __launch_bounds__(TPR * 128, 1) eda_recurrent_kernel(EdaArgs a) 
             loadw<W>(x + j, w);
 #pragma unroll
             for (int i = 0; i < W; i += 4) {
-                pa = ffma2(make_float2(S[j + i], S[j + i + 1]), make_float2(w[i], w[i + 1]), pa);
-                pb = ffma2(make_float2(S[j + i + 2], S[j + i + 3]), make_float2(w[i + 2], w[i + 3]), pb);
+                if constexpr (R == 1) {
+                    pa = ffma2(make_float2(S[0][j + i], S[0][j + i + 1]), make_float2(w[i], w[i + 1]), pa);
+                    pb = ffma2(make_float2(S[0][j + i + 2], S[0][j + i + 3]), make_float2(w[i + 2], w[i + 3]), pb);
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 4; u += 2) {
+                        const float2 wu = make_float2(w[i + u], w[i + u + 1]);
+                        pa = ffma2(make_float2(S[0][j + i + u], S[0][j + i + u + 1]), wu, pa);
+                        pb = ffma2(make_float2(S[R - 1][j + i + u], S[R - 1][j + i + u + 1]), wu, pb);
+                    }
+                }
             }
         }
-        float p = (pa.x + pb.x) + (pa.y + pb.y);
-#pragma unroll
-        for (int off = 1; off < TPR; off <<= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+        float p;
+        int off = TPR / 2;
+        if constexpr (R == 1) {
+            p = (pa.x + pb.x) + (pa.y + pb.y);
+        } else {
+            p = (pa.x + pa.y) + __shfl_xor_sync(0xffffffffu, pb.x + pb.y, off);
+            off >>= 1;
+        }
+        for (; off; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
         return p;
     };
-    auto axpy = [&](float c, const TIn *x) {          // S -= c x, in packed pairs
-        const float2 nc = make_float2(-c, -c);
+    // the other row's copy of a per-row scalar: the partner's own row is this thread's other
+    auto other = [&](float c) { return R == 2 ? __shfl_xor_sync(0xffffffffu, c, TPR / 2) : 0.f; };
+    auto axpy = [&](float c, float c2, const TIn *x) {   // own row -= c x, other row -= c2 x
+        const float2 nc = make_float2(-c, -c), nc2 = make_float2(-c2, -c2);
 #pragma unroll
         for (int j = 0; j < NS; j += W) {
             float w[W];
             loadw<W>(x + j, w);
 #pragma unroll
             for (int i = 0; i < W; i += 2) {
-                const float2 r = ffma2(nc, make_float2(w[i], w[i + 1]), make_float2(S[j + i], S[j + i + 1]));
-                S[j + i] = r.x;
-                S[j + i + 1] = r.y;
+                const float2 wi = make_float2(w[i], w[i + 1]);
+                float2 r = ffma2(nc, wi, make_float2(S[0][j + i], S[0][j + i + 1]));
+                S[0][j + i] = r.x;
+                S[0][j + i + 1] = r.y;
+                if constexpr (R == 2) {
+                    r = ffma2(nc2, wi, make_float2(S[1][j + i], S[1][j + i + 1]));
+                    S[1][j + i] = r.x;
+                    S[1][j + i + 1] = r.y;
+                }
             }
         }
     };
@@ -185,10 +223,12 @@ __global__ void __launch_bounds__(TPR * 128, 1) eda_recurrent_kernel(EdaArgs a) 
             const TIn *tk = cur + t * TS;
             const TIn *ev = tk + s * SL, *kv = tk + VS + s * SL, *qv = tk + 2 * VS + s * SL;
             const float vi = to_f(tk[3 * VS + row]), bt = bcur[t];
-            axpy(rowdot(ev), ev);                     // erase: S <- S - (S e) e^T
-            axpy(bt * (rowdot(kv) - vi), kv);         // write: S <- S - beta (S k - v) k^T
+            const float ce = rowdot(ev);              // erase: S <- S - (S e) e^T
+            axpy(ce, other(ce), ev);
+            const float cw = bt * (rowdot(kv) - vi);  // write: S <- S - beta (S k - v) k^T
+            axpy(cw, other(cw), kv);
             const float o = rowdot(qv);               // o = S q
-            if (s == 0) obuf[t * dv + row] = o;
+            if ((s & (TPR / R - 1)) == 0) obuf[t * dv + row] = o;
         }
         if (tile + 1 < ntiles && tid < kTile) bet[((tile + 1) & 1) * kTile + tid] = bnext;
         __syncthreads();                              // outputs of the tile complete
@@ -199,29 +239,32 @@ __global__ void __launch_bounds__(TPR * 128, 1) eda_recurrent_kernel(EdaArgs a) 
         }
     }
     if (a.S_final) {
-        const size_t base = ((size_t)bh * dv + row) * DK + s * NS;
 #pragma unroll
-        for (int j = 0; j < NS; ++j) a.S_final[base + j] = S[j];
+        for (int r = 0; r < R; ++r) {
+            const size_t base = ((size_t)bh * dv + (r ? row2 : row)) * DK + s * NS;
+#pragma unroll
+            for (int j = 0; j < NS; ++j) a.S_final[base + j] = S[r][j];
+        }
     }
 }
 
-template <typename TIn, int DK, int TPR>
+template <typename TIn, int DK, int TPR, int R>
 cudaError_t run_eda(const EdaArgs &a, cudaStream_t s) {
     const size_t smem = TokenLayout<TIn, DK, TPR>::bytes(a.dv);
-    auto kern = eda_recurrent_kernel<TIn, DK, TPR>;
+    auto kern = eda_recurrent_kernel<TIn, DK, TPR, R>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<a.B * a.H, TPR * a.dv, smem, s>>>(a);
+    kern<<<a.B * a.H, TPR * a.dv / R, smem, s>>>(a);
     return cudaGetLastError();
 }
 
 template <typename TIn>
 cudaError_t dispatch_eda(const EdaArgs &a, cudaStream_t s) {
     switch (a.dk) {
-        case 16: return run_eda<TIn, 16, 4>(a, s);
-        case 32: return run_eda<TIn, 32, 4>(a, s);
-        case 64: return run_eda<TIn, 64, 4>(a, s);
-        case 128: return run_eda<TIn, 128, 4>(a, s);
+        case 16: return run_eda<TIn, 16, 4, 1>(a, s);
+        case 32: return run_eda<TIn, 32, 4, 1>(a, s);
+        case 64: return run_eda<TIn, 64, 4, 2>(a, s);       // 16 columns x 2 rows a thread
+        case 128: return run_eda<TIn, 128, 8, 2>(a, s);
     }
     return cudaErrorInvalidValue;
 }
