@@ -9,10 +9,11 @@
 // the whole sequence, and each token costs three row-dot products (S e, S k, S q), each
 // reduced over the threads of a row by shuffles, and two rank-one updates: 5 dv dk
 // multiply-adds.  The kernel is issue bound, so the thread layout is chosen to spend the
-// fewest instructions beside those multiply-adds: for d_k >= 64 a thread holds two state
-// rows over 16 columns, so each token slice it unpacks from bf16 and each shared-memory
-// read serve two rows (7 % faster than one row over 32 columns at d_k = 128); one row
-// over 8 threads measured slower (one more shuffle level, no fewer unpacks).  The token
+// fewest instructions beside those multiply-adds: for d_k >= 64 a thread holds four state
+// rows over 8 columns, so each token slice it unpacks from bf16 and each shared-memory
+// read serve four rows (at d_k = 128: 7 % faster than one row over 32 columns, and 0.5 %
+// faster than two rows over 16); one row over 8 threads measured slower (one more
+// shuffle level, no fewer unpacks).  The token
 // vectors are staged in shared memory a tile of 16 tokens at a time by asynchronous
 // copies (cp.async), the next tile's in flight while the current one is consumed, and
 // converted to fp32 as they are read (a separate fp32 tile measured slower: twice the
@@ -87,13 +88,17 @@ struct TokenLayout {
     }
 };
 
-// R state rows per thread (1 or 2) over TPR threads per row.  With R = 2 a thread holds
-// rows rg and rg + dv/2 (rg = tid / TPR) over the same d_k/TPR columns, so one unpacked
-// token slice serves two rows.  Its "own" row is the one whose reduction it completes:
-// the first for the lower half of the row's TPR threads, the second for the upper half.
+// R state rows per thread (1, 2 or 4) over TPR threads per row.  A thread holds rows
+// rg + rho dv/R, rho < R (rg = tid / TPR), over the same d_k/TPR columns, so one
+// unpacked token slice serves R rows.  Its own row rho* = s / (TPR/R) (s = tid % TPR) is
+// the one whose reduction it completes; its registers hold row rho* ^ m in slot m, so
+// the partner at lane offset TPR/2, TPR/4, ... (own row rho* ^ R/2, rho* ^ R/4, ...) holds
+// this thread's slot m in its slot m ^ R/2, m ^ R/4, ...: each of the first log2 R shuffle
+// levels keeps the lower half of the slots and adds the partner's upper half, with no
+// selects.
 template <typename TIn, int DK, int TPR, int R>
 __global__ void __launch_bounds__(TPR * 128 / R, 1) eda_recurrent_kernel(EdaArgs a) {
-    static_assert(R == 1 || R == 2, "one or two rows per thread");
+    static_assert((R == 1 || R == 2 || R == 4) && TPR % R == 0, "1, 2 or 4 rows per thread");
     using L = TokenLayout<TIn, DK, TPR>;
     constexpr int NS = L::NS, SL = L::SL, VS = L::VS, E = L::E;
     constexpr int P8 = 8 / E;                         // elements per 8-byte copy
@@ -106,19 +111,19 @@ __global__ void __launch_bounds__(TPR * 128 / R, 1) eda_recurrent_kernel(EdaArgs
     float *obuf = bet + 2 * kTile;                                                // [kTile][dv]
 
     const int tid = threadIdx.x, rg = tid / TPR, s = tid % TPR;
-    const bool upper = R == 2 && (s & (TPR / 2));
-    const int row = upper ? rg + dv / 2 : rg;         // own row
-    const int row2 = upper ? rg : rg + dv / 2;        // the other row (R == 2)
+    const int own = s / (TPR / R);                    // rho*
+    auto row_of = [&](int m) { return rg + (m ^ own) * (dv / R); };
+    const int row = row_of(0);                        // own row
     const int bh = blockIdx.x, b = bh / H, h = bh % H;
     const TIn *q = (const TIn *)a.q, *k = (const TIn *)a.k, *v = (const TIn *)a.v, *e = (const TIn *)a.e;
     const TIn *beta = (const TIn *)a.beta;
     const int nthreads = TPR * dv / R;
     const int per_tok = (3 * DK + dv) / P8;           // 8-byte copies per token
 
-    float S[R][NS];                                   // S[0]: own row, S[1]: the other row
+    float S[R][NS];                                   // slot m: row rho* ^ m
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-        const size_t base = ((size_t)bh * dv + (r ? row2 : row)) * DK + s * NS;
+        const size_t base = ((size_t)bh * dv + row_of(r)) * DK + s * NS;
 #pragma unroll
         for (int j = 0; j < NS; ++j) S[r][j] = a.S0 ? a.S0[base + j] : 0.f;
     }
@@ -148,45 +153,12 @@ __global__ void __launch_bounds__(TPR * 128 / R, 1) eda_recurrent_kernel(EdaArgs
         if (tid < nt) bv = beta ? to_f(beta[((size_t)b * T + t0 + tid) * H + h]) : 1.f;
         return bv;
     };
-    // the own row's dot product with x, reduced over the row's TPR threads.  With R = 2
-    // the first shuffle level also trades: a thread sends its partial of the other row
-    // and receives its partner's partial of its own row (the partner's other row).
+    // the own row's dot product with x, reduced over the row's TPR threads (the first
+    // log2 R levels trade slots, as above)
     auto rowdot = [&](const TIn *x) {                 // packed pairs: one instruction per two products
-        float2 pa = make_float2(0.f, 0.f), pb = make_float2(0.f, 0.f);
+        float2 acc[R == 1 ? 2 : R];
 #pragma unroll
-        for (int j = 0; j < NS; j += W) {
-            float w[W];
-            loadw<W>(x + j, w);
-#pragma unroll
-            for (int i = 0; i < W; i += 4) {
-                if constexpr (R == 1) {
-                    pa = ffma2(make_float2(S[0][j + i], S[0][j + i + 1]), make_float2(w[i], w[i + 1]), pa);
-                    pb = ffma2(make_float2(S[0][j + i + 2], S[0][j + i + 3]), make_float2(w[i + 2], w[i + 3]), pb);
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 4; u += 2) {
-                        const float2 wu = make_float2(w[i + u], w[i + u + 1]);
-                        pa = ffma2(make_float2(S[0][j + i + u], S[0][j + i + u + 1]), wu, pa);
-                        pb = ffma2(make_float2(S[R - 1][j + i + u], S[R - 1][j + i + u + 1]), wu, pb);
-                    }
-                }
-            }
-        }
-        float p;
-        int off = TPR / 2;
-        if constexpr (R == 1) {
-            p = (pa.x + pb.x) + (pa.y + pb.y);
-        } else {
-            p = (pa.x + pa.y) + __shfl_xor_sync(0xffffffffu, pb.x + pb.y, off);
-            off >>= 1;
-        }
-        for (; off; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
-        return p;
-    };
-    // the other row's copy of a per-row scalar: the partner's own row is this thread's other
-    auto other = [&](float c) { return R == 2 ? __shfl_xor_sync(0xffffffffu, c, TPR / 2) : 0.f; };
-    auto axpy = [&](float c, float c2, const TIn *x) {   // own row -= c x, other row -= c2 x
-        const float2 nc = make_float2(-c, -c), nc2 = make_float2(-c2, -c2);
+        for (int m = 0; m < (R == 1 ? 2 : R); ++m) acc[m] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < NS; j += W) {
             float w[W];
@@ -194,13 +166,47 @@ __global__ void __launch_bounds__(TPR * 128 / R, 1) eda_recurrent_kernel(EdaArgs
 #pragma unroll
             for (int i = 0; i < W; i += 2) {
                 const float2 wi = make_float2(w[i], w[i + 1]);
-                float2 r = ffma2(nc, wi, make_float2(S[0][j + i], S[0][j + i + 1]));
-                S[0][j + i] = r.x;
-                S[0][j + i + 1] = r.y;
-                if constexpr (R == 2) {
-                    r = ffma2(nc2, wi, make_float2(S[1][j + i], S[1][j + i + 1]));
-                    S[1][j + i] = r.x;
-                    S[1][j + i + 1] = r.y;
+                if constexpr (R == 1) {               // two chains over one row
+                    acc[(i >> 1) & 1] = ffma2(make_float2(S[0][j + i], S[0][j + i + 1]), wi, acc[(i >> 1) & 1]);
+                } else {
+#pragma unroll
+                    for (int m = 0; m < R; ++m)
+                        acc[m] = ffma2(make_float2(S[m][j + i], S[m][j + i + 1]), wi, acc[m]);
+                }
+            }
+        }
+        float p[R == 1 ? 2 : R];
+#pragma unroll
+        for (int m = 0; m < (R == 1 ? 2 : R); ++m) p[m] = acc[m].x + acc[m].y;
+        if constexpr (R == 1) p[0] += p[1];
+        int off = TPR / 2;
+#pragma unroll
+        for (int half = R / 2; half; half >>= 1, off >>= 1) {
+#pragma unroll
+            for (int m = 0; m < half; ++m) p[m] += __shfl_xor_sync(0xffffffffu, p[m + half], off);
+        }
+        for (; off; off >>= 1) p[0] += __shfl_xor_sync(0xffffffffu, p[0], off);
+        return p[0];
+    };
+    // a per-row scalar for every slot: slot m's row is the own row of lane s ^ m (TPR/R)
+    auto spread = [&](float c, float (&cs)[R]) {
+        cs[0] = c;
+#pragma unroll
+        for (int m = 1; m < R; ++m) cs[m] = __shfl_xor_sync(0xffffffffu, c, m * (TPR / R));
+    };
+    auto axpy = [&](const float (&cs)[R], const TIn *x) {   // slot m -= cs[m] x
+#pragma unroll
+        for (int j = 0; j < NS; j += W) {
+            float w[W];
+            loadw<W>(x + j, w);
+#pragma unroll
+            for (int i = 0; i < W; i += 2) {
+                const float2 wi = make_float2(w[i], w[i + 1]);
+#pragma unroll
+                for (int m = 0; m < R; ++m) {
+                    const float2 r = ffma2(make_float2(-cs[m], -cs[m]), wi, make_float2(S[m][j + i], S[m][j + i + 1]));
+                    S[m][j + i] = r.x;
+                    S[m][j + i + 1] = r.y;
                 }
             }
         }
@@ -223,10 +229,11 @@ __global__ void __launch_bounds__(TPR * 128 / R, 1) eda_recurrent_kernel(EdaArgs
             const TIn *tk = cur + t * TS;
             const TIn *ev = tk + s * SL, *kv = tk + VS + s * SL, *qv = tk + 2 * VS + s * SL;
             const float vi = to_f(tk[3 * VS + row]), bt = bcur[t];
-            const float ce = rowdot(ev);              // erase: S <- S - (S e) e^T
-            axpy(ce, other(ce), ev);
-            const float cw = bt * (rowdot(kv) - vi);  // write: S <- S - beta (S k - v) k^T
-            axpy(cw, other(cw), kv);
+            float cs[R];
+            spread(rowdot(ev), cs);                   // erase: S <- S - (S e) e^T
+            axpy(cs, ev);
+            spread(bt * (rowdot(kv) - vi), cs);       // write: S <- S - beta (S k - v) k^T
+            axpy(cs, kv);
             const float o = rowdot(qv);               // o = S q
             if ((s & (TPR / R - 1)) == 0) obuf[t * dv + row] = o;
         }
@@ -241,7 +248,7 @@ __global__ void __launch_bounds__(TPR * 128 / R, 1) eda_recurrent_kernel(EdaArgs
     if (a.S_final) {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const size_t base = ((size_t)bh * dv + (r ? row2 : row)) * DK + s * NS;
+            const size_t base = ((size_t)bh * dv + row_of(r)) * DK + s * NS;
 #pragma unroll
             for (int j = 0; j < NS; ++j) a.S_final[base + j] = S[r][j];
         }
@@ -263,8 +270,8 @@ cudaError_t dispatch_eda(const EdaArgs &a, cudaStream_t s) {
     switch (a.dk) {
         case 16: return run_eda<TIn, 16, 4, 1>(a, s);
         case 32: return run_eda<TIn, 32, 4, 1>(a, s);
-        case 64: return run_eda<TIn, 64, 4, 2>(a, s);       // 16 columns x 2 rows a thread
-        case 128: return run_eda<TIn, 128, 8, 2>(a, s);
+        case 64: return run_eda<TIn, 64, 8, 4>(a, s);       // 8 columns x 4 rows a thread
+        case 128: return run_eda<TIn, 128, 16, 4>(a, s);
     }
     return cudaErrorInvalidValue;
 }
