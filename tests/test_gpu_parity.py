@@ -603,6 +603,17 @@ def test_eda_forward_all_outputs(qd, dt, dh, erase, beta):
     check(S, S_ref, dt, f"eda {dt} {erase} S")
 
 
+@pytest.mark.parametrize("dt,dk,dv", [("bf16", 128, 16), ("bf16", 64, 128), ("f32", 128, 64), ("f32", 32, 128)])
+def test_eda_rectangular_state(qd, dt, dk, dv):
+    """EDA with d_k != d_v: the kernel spreads state rows (d_v) over threads and the
+    columns (d_k) over the threads of a row independently, one to four rows a thread."""
+    d = synth.eda_inputs(2, 70, 3, dk, dv, seed=83, dtype=dt, erase="random", s0_var=0.01)
+    o, S = run_eda(qd, d)
+    o_ref, S_ref = oracle.eda_fwd(d["q"], d["k"], d["v"], d["e"], d["beta"], d["S0"])
+    check(o, o_ref, dt, f"eda {dt} dk={dk} dv={dv} o")
+    check(S, S_ref, dt, f"eda {dt} dk={dk} dv={dv} S")
+
+
 def test_eda_long_sequence_query_erase(qd):
     """B=1, H=2, T=2048 with e = q: the state carried over the whole sequence."""
     d = synth.eda_inputs(1, 2048, 2, 128, 128, seed=82, dtype="bf16", erase="query", s0_var=0.01)
