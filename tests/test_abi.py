@@ -74,6 +74,37 @@ def test_python_binding_refuses_cpu_tensors(lib):
         qd.qdelta_fwd(x, x, x, gt, gt, gt)
 
 
+def _cpu_calls():
+    """Every Python entry point, called with CPU tensors of valid shapes and dtypes."""
+    import torch
+    bf, f32 = torch.bfloat16, torch.float32
+    B, T, H, d, N = 1, 4, 1, 16, 2
+    x = lambda *s, dt=bf: torch.zeros(*s, dtype=dt)
+    tok, gate, st = x(B, T, H, d), x(B, T, H), x(B, H, d, d, dt=f32)
+    stok, sgate, sst = x(N, H, d), x(N, H), x(N, H, d, d, dt=f32)
+    lam_h = x(H, dt=f32)
+    return {
+        "qdelta_fwd": lambda: qd.qdelta_fwd(tok, tok, tok, gate, gate, gate, st),
+        "qdelta_fwd prologue": lambda: qd.qdelta_fwd(tok, tok, tok, gate, gate, gate, st, prologue=True),
+        "qdelta_fwd_static_scratch": lambda: qd.qdelta_fwd_static_scratch(tok, tok, tok, gate, gate, gate, st),
+        "qdelta_bwd": lambda: qd.qdelta_bwd(tok, tok, tok, gate, gate, gate, st, tok, st),
+        "qdelta_bwd prologue": lambda: qd.qdelta_bwd(tok, tok, tok, gate, gate, gate, st, tok, st, prologue=True),
+        "qed_fwd": lambda: qd.qed_fwd(tok, tok, tok, tok, tok, tok, lam_h, st),
+        "qed_fwd nogate": lambda: qd.qed_fwd(tok, tok, tok, tok, tok, tok, lam_h, st, variant="nogate"),
+        "eda_fwd": lambda: qd.eda_fwd(tok, tok, tok, tok, gate, st),
+        "qdelta_step": lambda: qd.qdelta_step(sst, stok, stok, stok, sgate, sgate, sgate),
+        "qdelta_step prologue": lambda: qd.qdelta_step(sst, stok, stok, stok, sgate, sgate, sgate, prologue=True),
+        "qed_step": lambda: qd.qed_step(sst, stok, stok, stok, stok, stok, stok, lam_h),
+    }
+
+
+@pytest.mark.parametrize("name", sorted(_cpu_calls()))
+def test_every_entry_point_refuses_cpu_tensors(lib, name):
+    """No entry point has a CPU path: host tensors are refused before any launch."""
+    with pytest.raises(ValueError, match="CUDA"):
+        _cpu_calls()[name]()
+
+
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         qd.load_library(str(tmp_path / "nope.so"))
