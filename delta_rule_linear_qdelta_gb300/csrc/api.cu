@@ -63,6 +63,15 @@ qd_status empty_sequence(const float *S0, float *S_final, int B, int H, int dk, 
 
 namespace qd {
 qd_status report_error(qd_status status, const char *msg) { return fail(status, "%s", msg); }
+
+qd_status check_qdelta_fwd_args(const char *fn, const void *q, const void *k, const void *v, const void *alpha,
+                                const void *beta, const void *lam, const float *S0, void *o, float *S_final,
+                                int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype) {
+    g_err[0] = 0;
+    const void *req[] = {q, k, v, beta, o};
+    const void *opt[] = {alpha, lam, S0, S_final};
+    return check_fwd(fn, req, 5, opt, 4, B, T, H, dk, dv, chunk, dtype);
+}
 }  // namespace qd
 
 extern "C" {

@@ -189,5 +189,10 @@ bool qed_tc_read_and_clear_timeout();
 
 // Records `msg` as this host thread's last error (qd_last_error) and returns `status`.
 qd_status report_error(qd_status status, const char *msg);
+// The host-side argument checks of qdelta_fwd (pointers, alignment, sizes, head
+// dims, chunk, dtype), without the workspace check; no CUDA call.
+qd_status check_qdelta_fwd_args(const char *fn, const void *q, const void *k, const void *v, const void *alpha,
+                                const void *beta, const void *lam, const float *S0, void *o, float *S_final,
+                                int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype);
 
 }  // namespace qd

@@ -206,3 +206,19 @@ def test_prologue_backward_arguments_checked(lib):
     st = lib.qdelta_bwd_prologue(*args(), 1, 8, 1, 64, 64, 64, qd.QD_BF16, g, need - 16, None)
     assert st == qd.QD_ERR_WORKSPACE
     assert lib.qdelta_bwd_prologue(*([None] * 16), 0, 8, 4, 64, 64, 64, 1, None, 0, None) == qd.QD_OK
+
+
+def test_static_scratch_checks_arguments_before_any_device_call(lib):
+    """Sizes that would take the segment scan (and so the fixed scratch array) still
+    get QD_ERR_ARG for a NULL or misaligned pointer, from the host checks alone."""
+    P = ctypes.c_void_p
+    g = P(256)
+    st = lib.qdelta_fwd_static_scratch(None, g, g, None, g, None, None, g, None, 1, 4096, 2, 128, 128, 64,
+                                       qd.QD_BF16, None)
+    assert st == qd.QD_ERR_ARG and "NULL" in qd.qd_last_error()
+    st = lib.qdelta_fwd_static_scratch(g, g, P(264), None, g, None, None, g, None, 1, 4096, 2, 128, 128, 64,
+                                       qd.QD_BF16, None)
+    assert st == qd.QD_ERR_ARG and "aligned" in qd.qd_last_error()
+    st = lib.qdelta_fwd_static_scratch(g, g, g, None, g, None, None, g, None, 1, 4096, 2, 128, 128, 32,
+                                       qd.QD_BF16, None)
+    assert st == qd.QD_ERR_UNSUPPORTED

@@ -2,14 +2,17 @@
 device memory at call time (a caller with only input and output pointers and no
 device allocator, or a serving loop whose memory is reserved up front and must
 not call cudaMalloc mid-step).  Called through the C ABI and checked against
-qdelta_fwd, which takes a caller workspace, on two calls in a row.  The sizes used
-take the segment scan, so the library's fixed scratch array is really used."""
+qdelta_fwd, which takes a caller workspace, on two calls in a row.  Both run the
+same kernels on the same inputs, so their outputs must agree bit for bit; one of
+them is also held to the fp64 oracle at the bf16 tolerance.  The sizes used take
+the segment scan, so the library's fixed scratch array is really used."""
 import ctypes
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 
 pytestmark = pytest.mark.gpu
@@ -63,8 +66,12 @@ def test_static_scratch_matches_workspace_forward_two_calls(qd):
         assert qd.last_launch_count() == 4       # the segment scan ran on the static scratch
         torch.cuda.synchronize()
         assert qd.qd_device_status() == qd.QD_OK
-        _close(o, o_ref, f"o (call {seed})")
-        _close(S, S_ref, f"S_final (call {seed})")
+        assert torch.equal(o, o_ref), f"o (call {seed}) differs from qdelta_fwd's"
+        assert torch.equal(S, S_ref), f"S_final (call {seed}) differs from qdelta_fwd's"
+        if seed == 301:                          # and against the fp64 oracle
+            o64, S64 = oracle.qdelta_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["lam"], d["S0"])
+            _close(o, torch.from_numpy(o64), f"o vs oracle (call {seed})")
+            _close(S, torch.from_numpy(S64), f"S_final vs oracle (call {seed})")
 
 
 def test_static_scratch_rejects_sizes_beyond_its_array(qd):
