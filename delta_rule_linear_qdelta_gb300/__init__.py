@@ -132,6 +132,19 @@ def _need(t: torch.Tensor | None, name: str, dtype, shape, optional: bool = Fals
         raise ValueError(f"{name} must be contiguous")
 
 
+def _same_device(device, *tensors):
+    for t in tensors:
+        if t is not None and t.device != device:
+            raise ValueError(f"tensor on {t.device}, expected every argument on {device}")
+
+
+def _call(device, fn, *args):
+    """Runs one C call with `device` current: the library takes the SM count, the
+    TMA descriptors and the static scratch address from the current device."""
+    with torch.cuda.device(device):
+        return fn(*args)
+
+
 def _stream(stream, device):
     if stream is None:
         return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
@@ -181,9 +194,10 @@ def qdelta_fwd(q, k, v, alpha, beta, lam, S0=None, *, o=None, S_final=None, retu
     _need(S_final, "S_final", torch.float32, (B, H, dv, dk), optional=True)
     code = _dtype_code(q)
     workspace, wsb = _workspace(qdelta_workspace_bytes(B, T, H, dk, dv, chunk, code), workspace, q.device)
+    _same_device(q.device, k, v, alpha, beta, lam, S0, o, S_final, workspace)
     fn = load_library().qdelta_fwd_prologue if prologue else load_library().qdelta_fwd
-    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(lam), _ptr(S0), _ptr(o), _ptr(S_final),
-            B, T, H, dk, dv, chunk, code, _ptr(workspace), wsb, _stream(stream, q.device))
+    st = _call(q.device, fn, _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(lam), _ptr(S0), _ptr(o),
+               _ptr(S_final), B, T, H, dk, dv, chunk, code, _ptr(workspace), wsb, _stream(stream, q.device))
     _check(st, "qdelta_fwd_prologue" if prologue else "qdelta_fwd")
     return o, S_final
 
@@ -222,10 +236,11 @@ def qdelta_bwd(q, k, v, alpha, beta, lam, S0, dO, dS_final=None, *, want_dS0=Tru
     nbytes = (lib.qdelta_bwd_prologue_workspace_bytes if prologue else lib.qdelta_bwd_workspace_bytes)(
         B, T, H, dk, dv, chunk, code)
     workspace, wsb = _workspace(nbytes, workspace, q.device)
-    st = (lib.qdelta_bwd_prologue if prologue else lib.qdelta_bwd)(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(lam), _ptr(S0),
-                                   _ptr(dO), _ptr(dS_final), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
-                                   _ptr(g["dalpha"]), _ptr(g["dbeta"]), _ptr(g["dlam"]), _ptr(g["dS0"]),
-                                   B, T, H, dk, dv, chunk, code, _ptr(workspace), wsb, _stream(stream, q.device))
+    _same_device(q.device, k, v, alpha, beta, lam, S0, dO, dS_final, workspace)
+    st = _call(q.device, lib.qdelta_bwd_prologue if prologue else lib.qdelta_bwd, _ptr(q), _ptr(k), _ptr(v),
+               _ptr(alpha), _ptr(beta), _ptr(lam), _ptr(S0), _ptr(dO), _ptr(dS_final), _ptr(g["dq"]),
+               _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dalpha"]), _ptr(g["dbeta"]), _ptr(g["dlam"]), _ptr(g["dS0"]),
+               B, T, H, dk, dv, chunk, code, _ptr(workspace), wsb, _stream(stream, q.device))
     _check(st, "qdelta_bwd_prologue" if prologue else "qdelta_bwd")
     return g
 
@@ -255,8 +270,10 @@ def eda_fwd(q, k, v, e, beta=None, S0=None, *, o=None, S_final=None, return_fina
     _need(S_final, "S_final", torch.float32, (B, H, dv, dk), optional=True)
     code = _dtype_code(q)
     workspace, wsb = _workspace(eda_workspace_bytes(B, T, H, dk, dv, chunk, code), workspace, q.device)
-    st = load_library().eda_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(e), _ptr(beta), _ptr(S0), _ptr(o), _ptr(S_final),
-                                B, T, H, dk, dv, chunk, code, _ptr(workspace), wsb, _stream(stream, q.device))
+    _same_device(q.device, k, v, e, beta, S0, o, S_final, workspace)
+    st = _call(q.device, load_library().eda_fwd, _ptr(q), _ptr(k), _ptr(v), _ptr(e), _ptr(beta), _ptr(S0),
+               _ptr(o), _ptr(S_final), B, T, H, dk, dv, chunk, code, _ptr(workspace), wsb,
+               _stream(stream, q.device))
     _check(st, "eda_fwd")
     return o, S_final
 
@@ -283,9 +300,10 @@ def qdelta_fwd_static_scratch(q, k, v, alpha, beta, lam, S0=None, *, o=None, S_f
     if S_final is None and return_final:
         S_final = torch.empty((B, H, dv, dk), dtype=torch.float32, device=q.device)
     _need(S_final, "S_final", torch.float32, (B, H, dv, dk), optional=True)
-    st = load_library().qdelta_fwd_static_scratch(_ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(lam),
-                                                  _ptr(S0), _ptr(o), _ptr(S_final), B, T, H, dk, dv, chunk,
-                                                  _dtype_code(q), _stream(stream, q.device))
+    _same_device(q.device, k, v, alpha, beta, lam, S0, o, S_final)
+    st = _call(q.device, load_library().qdelta_fwd_static_scratch, _ptr(q), _ptr(k), _ptr(v), _ptr(alpha),
+               _ptr(beta), _ptr(lam), _ptr(S0), _ptr(o), _ptr(S_final), B, T, H, dk, dv, chunk, _dtype_code(q),
+               _stream(stream, q.device))
     _check(st, "qdelta_fwd_static_scratch")
     return o, S_final
 
@@ -313,9 +331,10 @@ def qed_fwd(q, k, v, g, b, w, lam_h, S0=None, *, o=None, S_final=None, return_fi
     _need(z, "z", torch.float32, (H, dk), optional=vid != QED_VARIANTS["rand"])
     code = _dtype_code(q)
     workspace, wsb = _workspace(qed_workspace_bytes(B, T, H, dk, dv, chunk, code), workspace, q.device)
-    st = load_library().qed_fwd_variant(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(w), _ptr(lam_h),
-                                        _ptr(S0), _ptr(o), _ptr(S_final), B, T, H, dk, dv, chunk, code, vid,
-                                        _ptr(z), _ptr(workspace), wsb, _stream(stream, q.device))
+    _same_device(q.device, k, v, g, b, w, lam_h, S0, o, S_final, z, workspace)
+    st = _call(q.device, load_library().qed_fwd_variant, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(w),
+               _ptr(lam_h), _ptr(S0), _ptr(o), _ptr(S_final), B, T, H, dk, dv, chunk, code, vid, _ptr(z),
+               _ptr(workspace), wsb, _stream(stream, q.device))
     _check(st, "qed_fwd_variant")
     return o, S_final
 
@@ -337,8 +356,9 @@ def qed_step(S, q, k, v, g, b, w, lam_h, *, o=None, stream=None, variant="full",
     if o is None:
         o = torch.empty((N, H, dv), dtype=dt, device=q.device)
     _need(o, "o", dt, (N, H, dv))
-    st = load_library().qed_step(_ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(w), _ptr(lam_h),
-                                 _ptr(o), N, H, dk, dv, _dtype_code(q), vid, _ptr(z), _stream(stream, q.device))
+    _same_device(q.device, S, k, v, g, b, w, lam_h, o, z)
+    st = _call(q.device, load_library().qed_step, _ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(b), _ptr(w),
+               _ptr(lam_h), _ptr(o), N, H, dk, dv, _dtype_code(q), vid, _ptr(z), _stream(stream, q.device))
     _check(st, "qed_step")
     return o
 
@@ -359,9 +379,10 @@ def qdelta_step(S, q, k, v, alpha, beta, lam, *, o=None, stream=None, prologue=F
     if o is None:
         o = torch.empty((N, H, dv), dtype=dt, device=q.device)
     _need(o, "o", dt, (N, H, dv))
+    _same_device(q.device, S, k, v, alpha, beta, lam, o)
     fn = load_library().qdelta_step_prologue if prologue else load_library().qdelta_step
-    st = fn(_ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(lam), _ptr(o), N, H, dk, dv,
-            _dtype_code(q), _stream(stream, q.device))
+    st = _call(q.device, fn, _ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(lam), _ptr(o), N,
+               H, dk, dv, _dtype_code(q), _stream(stream, q.device))
     _check(st, "qdelta_step_prologue" if prologue else "qdelta_step")
     return o
 
