@@ -205,7 +205,11 @@ QD_API qd_status qdelta_step_prologue(float *S, const void *q_raw, const void *k
  * No output may alias an input.  workspace: at least qdelta_bwd_workspace_bytes(...)
  * bytes (two fp32 checkpoint arrays: the state entering, and the gradient reaching
  * the state leaving, every chunk of 64 tokens).  T = 0 writes dS0 = dS_final (or 0)
- * and nothing else.  Arithmetic in fp32 on CUDA cores for both dtypes.
+ * and nothing else.  Precision: fp32 inputs, and head dims other than 128, run in
+ * fp32 on CUDA cores.  bf16 inputs at dk = dv = 128 run the state checkpoints on
+ * the bf16 tensor-core forward (fp32 state, bf16 operands) and the reverse sweep and
+ * per-chunk gradient products on TF32 tensor-core MMAs (fp32 accumulation, operands
+ * rounded to TF32, 10-bit mantissa); the recurrence's elementwise work stays fp32.
  * Errors as for qdelta_fwd.
  */
 QD_API qd_status qdelta_bwd(const void *q, const void *k, const void *v,
