@@ -4,8 +4,8 @@ Tolerances (element by element against the fp64 oracle on identical inputs):
   bf16 inputs, fp32 accumulation: relative L2 <= 5e-3 and max abs <= 2e-2
   fp32 path:                       relative L2 <= 1e-5
 Small cases compare every output; the full-size workloads run on the GPU in the
-same launch configuration the bench times, and compare sampled (b, h) streams
-that the oracle computes one by one over the full sequence.
+same launch configuration the bench times and compare every (b, h) stream over
+the full sequence, stream by stream and as a whole.
 """
 import numpy as np
 import pytest
@@ -138,28 +138,35 @@ def test_head_dims_bf16(qd, dk, dv):
     check(S, S_ref, "bf16", f"dk={dk} dv={dv} S")
 
 
+def check_every_stream(o, o_ref, S, S_ref, name):
+    """Each (b, h) stream of o [B,T,H,dv] and S [B,H,dv,dk] on its own, then the whole:
+    an error confined to one CTA's stream cannot hide in the others' norm."""
+    Bn, _, Hn, _ = o.shape
+    for b in range(Bn):
+        for h in range(Hn):
+            check(o[b, :, h], o_ref[b, :, h], "bf16", f"{name} o stream (b={b}, h={h})")
+            check(S[b, h], S_ref[b, h], "bf16", f"{name} S stream (b={b}, h={h})")
+    check(o, o_ref, "bf16", name + " o")
+    check(S, S_ref, "bf16", name + " S")
+
+
 @pytest.mark.parametrize("mode", ["qdelta", "gdn", "deltanet"])
-def test_layer_1p3b_full_size_sampled(qd, mode):
-    """B=8, H=16, T=2048, d=128 bf16: the benchmarked workload; 6 streams checked."""
+def test_layer_1p3b_full_size_every_stream(qd, mode):
+    """B=8, H=16, T=2048, d=128 bf16: the benchmarked workload in the launch
+    configuration the bench times; all 128 streams against the oracle."""
     name, d = synth.layer_1p3b(mode)
     o, S = run_qdelta(qd, d)
-    pairs = [(0, 0), (0, 15), (3, 7), (5, 2), (7, 9), (7, 15)]
-    o_ref, S_ref = oracle.qdelta_fwd(sel(d["q"], pairs), sel(d["k"], pairs), sel(d["v"], pairs),
-                                     sel(d["alpha"], pairs), sel(d["beta"], pairs), sel(d["lam"], pairs))
-    check(sel(o, pairs), o_ref, "bf16", name + " o")
-    check(np.stack([S[b, h] for b, h in pairs])[:, None], S_ref, "bf16", name + " S")
+    o_ref, S_ref = oracle.qdelta_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["lam"])
+    check_every_stream(o, o_ref, S, S_ref, name)
 
 
-def test_long_context_full_size_sampled(qd):
-    """B=1, H=16, T=32768, mean alpha 0.995, S0 ~ N(0, 0.01); 2 heads checked."""
+def test_long_context_full_size_every_stream(qd):
+    """B=1, H=16, T=32768, mean alpha 0.995, S0 ~ N(0, 0.01) (the segment scan); all
+    16 heads against the oracle."""
     name, d = synth.long_context()
     o, S = run_qdelta(qd, d)
-    pairs = [(0, 3), (0, 12)]
-    S0 = np.stack([d["S0"][b, h] for b, h in pairs])[:, None]
-    o_ref, S_ref = oracle.qdelta_fwd(sel(d["q"], pairs), sel(d["k"], pairs), sel(d["v"], pairs),
-                                     sel(d["alpha"], pairs), sel(d["beta"], pairs), sel(d["lam"], pairs), S0)
-    check(sel(o, pairs), o_ref, "bf16", name + " o")
-    check(np.stack([S[b, h] for b, h in pairs])[:, None], S_ref, "bf16", name + " S")
+    o_ref, S_ref = oracle.qdelta_fwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["lam"], d["S0"])
+    check_every_stream(o, o_ref, S, S_ref, name)
 
 
 @pytest.mark.parametrize("mode", ["qdelta", "deltanet"])
@@ -292,22 +299,13 @@ def test_qed_ablation_arms_all_outputs(qd, variant, dt, dh):
     check(S, S_ref, dt, f"qed {variant} {dt} S")
 
 
-def test_qed_full_size_sampled(qd):
-    """B=4, H=8, T=4096, d=128 bf16; 4 streams checked."""
+def test_qed_full_size_every_stream(qd):
+    """B=4, H=8, T=4096, d=128 bf16 (the QED bench workload); all 32 streams against
+    the oracle."""
     name, d = synth.qed_gdn2()
     o, S = run_qed(qd, d)
-    pairs = [(0, 0), (1, 5), (2, 7), (3, 3)]
-    lam = np.array([d["lam_h"][h] for _, h in pairs])
-    # the oracle takes one lambda_h per head: run each stream as its own head
-    o_ref = np.zeros((len(pairs), 4096, 1, 128))
-    S_ref = np.zeros((len(pairs), 1, 128, 128))
-    for i, (b, h) in enumerate(pairs):
-        s = [(b, h)]
-        o1, S1 = oracle.qed_fwd(sel(d["q"], s), sel(d["k"], s), sel(d["v"], s), sel(d["g"], s), sel(d["b"], s),
-                                sel(d["w"], s), lam[i:i + 1])
-        o_ref[i], S_ref[i] = o1[0], S1[0]
-    check(sel(o, pairs), o_ref, "bf16", name + " o")
-    check(np.stack([S[b, h] for b, h in pairs])[:, None], S_ref, "bf16", name + " S")
+    o_ref, S_ref = oracle.qed_fwd(d["q"], d["k"], d["v"], d["g"], d["b"], d["w"], d["lam_h"])
+    check_every_stream(o, o_ref, S, S_ref, name)
 
 
 # ------------------------------------------------------------------- decode
