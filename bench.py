@@ -14,12 +14,18 @@ B=8, H=16, T=2048, dk=dv=128, bf16 inputs, fp32 state, full Q-Delta gates
   tensor   its GEMM work against the measured bf16 tensor peak
   decode   qdelta_step on 512 sequences x 16 heads (fp32 128x128 state), GB/s
   qed_decode  qed_step on the same shape, GB/s
-  qed      qed_fwd at B=4, H=8, T=4096, d=128 bf16, tokens/s
+  qed      qed_fwd at B=4, H=8, T=4096, d=128 bf16, tokens/s, against HBM
+  deltanet, gdn  qdelta_fwd on the step's workload with alpha and lambda dropped
+           (DeltaNet) or lambda dropped (Gated DeltaNet), against HBM
+  long_context  qdelta_fwd at B=1, H=16, T=32768 (mean alpha 0.995, S0 != 0),
+           the segment scan, against HBM
   prologue qdelta_fwd_prologue on the step's workload (projections and logits in)
   eda      eda_fwd (erase-then-delta) on the step's shape, tokens/s
   backward qdelta_bwd on the step's workload (all input gradients), against the
            TF32 tensor peak its products run on
   cpu_baseline  the fp64 oracle timed on this host's cores on a bounded sample
+  clocks   nvidia-smi samples over the timed K steps and about 0.6 s of the same
+           back-to-back steps (untimed) on either side of them
 
 --impl reference times the oracle itself (the CPU reference of this build) on
 a bounded sample of the same workload each step, and prints the same line.
@@ -57,6 +63,15 @@ ALG_BYTES = TOKEN_HEADS * BYTES_PER_TOKEN_HEAD + B * H * DV * DK * 4
 FLOPS_PER_TOKEN_HEAD = 8 * CHUNK * DK + 6 * DK * DV
 ALG_FLOPS = TOKEN_HEADS * FLOPS_PER_TOKEN_HEAD
 N_BUFFERS = 3
+SOAK_S = 0.6     # untimed back-to-back steps around the timed region, for the clock samples
+
+
+def mode_bytes(mode, token_heads, heads):
+    """Algorithmic bytes of one forward in a gate mode: q, k, v, o in bf16, the gates the
+    mode reads (beta always; alpha unless DeltaNet; lambda only for Q-Delta) in bf16, and
+    the fp32 final state (plus the fp32 initial state when one is read)."""
+    gates = {"deltanet": 1, "gdn": 2, "qdelta": 3}[mode]
+    return token_heads * (2 * (DK + DK + DV + DV) + 2 * gates) + heads * DV * DK * 4
 DOMINANT_KERNEL_SOURCES = ["delta_rule_linear_qdelta_gb300/csrc/chunk_tc.cu",
                            "delta_rule_linear_qdelta_gb300/csrc/tc_common.cuh",
                            "delta_rule_linear_qdelta_gb300/csrc/sm103_ptx.cuh"]
@@ -188,16 +203,36 @@ def make_buffers(n_sets, seed_base=1):
     return sets
 
 
-def time_device(qd, sets, steps, warmup, world):
+def soak(step, seconds):
+    """Back-to-back untimed steps for about `seconds` of wall time (keeps the GPU under
+    the timed workload's load while the clocks are sampled)."""
+    import torch
+    if seconds <= 0:
+        return
+    t0 = time.time()
+    i = 0
+    while time.time() - t0 < seconds:
+        for _ in range(50):
+            step(i)
+            i += 1
+        torch.cuda.synchronize()
+
+
+def time_device(qd, sets, steps, warmup, world, mode="qdelta", soak_s=0.0):
+    """Times exactly `steps` forwards after `warmup` untimed ones (plus `soak_s` seconds
+    of untimed steps on either side when asked, for the clock samples).  Returns the
+    event-timed total, the mean per-launch time, the kernels launched and the wall
+    window (soak included)."""
     import torch
     o = torch.empty(B, T, H, DV, dtype=torch.bfloat16, device="cuda")
     S = torch.empty(B, H, DV, DK, dtype=torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
+    use_a, use_l = mode != "deltanet", mode == "qdelta"
 
     def step(i):
         s = sets[i % len(sets)]
-        qd.qdelta_fwd(s["q"], s["k"], s["v"], s["alpha"], s["beta"], s["lam"], None, o=o, S_final=S,
-                      stream=stream)
+        qd.qdelta_fwd(s["q"], s["k"], s["v"], s["alpha"] if use_a else None, s["beta"], s["lam"] if use_l else None,
+                      None, o=o, S_final=S, stream=stream)
         return qd.last_launch_count()
 
     for i in range(warmup):
@@ -205,10 +240,11 @@ def time_device(qd, sets, steps, warmup, world):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
+    t_wall0 = time.time()
+    soak(step, soak_s)
     barrier(world)
     torch.cuda.synchronize()
     launches = 0
-    t_wall0 = time.time()
     start.record(stream)
     for i in range(steps):
         ev[i][0].record(stream)
@@ -216,11 +252,75 @@ def time_device(qd, sets, steps, warmup, world):
         ev[i][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
-    t_wall1 = time.time()
     barrier(world)
+    soak(step, soak_s)
+    t_wall1 = time.time()
     total_ms = start.elapsed_time(end)
     per_launch_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
     return total_ms, per_launch_ms, launches, (t_wall0, t_wall1)
+
+
+def hbm_roofline(nbytes, kernel_ms, hbm_peak, peak_kind, flops=None, tc_peak=None):
+    gbs = nbytes / (kernel_ms * 1e-3) / 1e9
+    r = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+         "peak_kind": peak_kind, "alg_bytes_per_launch": nbytes, "kernel_ms": kernel_ms}
+    if flops is not None:
+        tf = flops / (kernel_ms * 1e-3) / 1e12
+        r["tensor"] = {"achieved": tf, "peak": tc_peak, "unit": "TFLOP/s", "frac": tf / tc_peak,
+                       "alg_flops_per_launch": flops}
+    return r
+
+
+def time_mode(qd, sets, mode, hbm_peak, tc_peak, peak_kind, steps=50, warmup=5):
+    """qdelta_fwd on the step's workload in one of the special-case gate modes."""
+    total_ms, launch_ms, launches, _ = time_device(qd, sets, steps, warmup, 1, mode=mode)
+    ms = total_ms / steps
+    nbytes = mode_bytes(mode, TOKEN_HEADS, B * H)
+    return {"workload": f"{mode}_bf16_B{B}_H{H}_T{T}_d{DK}", "ms_per_step": ms, "tokens_per_s": B * T / (ms * 1e-3),
+            "launches_per_step": launches / steps,
+            "roofline": hbm_roofline(nbytes, launch_ms, hbm_peak, peak_kind, TOKEN_HEADS * FLOPS_PER_TOKEN_HEAD,
+                                     tc_peak)}
+
+
+def time_long_context(qd, hbm_peak, tc_peak, peak_kind, steps=20, warmup=3):
+    """qdelta_fwd at B=1, H=16, T=32768, d=128 bf16, mean alpha 0.995, S0 ~ N(0, 0.01):
+    the segment scan (a workspace from the caller).  q, k, v, o are 128 MiB each, so
+    the inputs do not fit in L2."""
+    import torch
+    name, d = synth.long_context()
+    bf = torch.bfloat16
+    args = [to_dev(d[k], bf) for k in ("q", "k", "v", "alpha", "beta", "lam")]
+    S0 = to_dev(d["S0"], torch.float32)
+    Bl, Tl, Hl = d["q"].shape[:3]
+    o = torch.empty(Bl, Tl, Hl, DV, dtype=bf, device="cuda")
+    S = torch.empty(Bl, Hl, DV, DK, dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(1, qd.qdelta_workspace_bytes(Bl, Tl, Hl, DK, DV)), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        qd.qdelta_fwd(*args, S0, o=o, S_final=S, workspace=ws, stream=stream)
+
+    for _ in range(warmup):
+        step()
+    launches = qd.last_launch_count()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    call_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    th = Bl * Tl * Hl
+    nbytes = mode_bytes("qdelta", th, Bl * Hl) + Bl * Hl * DV * DK * 4     # + the fp32 S0 read
+    return {"workload": name, "ms_per_step": ms, "tokens_per_s": Bl * Tl / (ms * 1e-3),
+            "launches_per_step": launches,
+            "segments": max(1, ws.numel() // (3 * Bl * Hl * DV * DK * 4)) if launches > 1 else 1,
+            "roofline": hbm_roofline(nbytes, call_ms, hbm_peak, peak_kind, th * FLOPS_PER_TOKEN_HEAD, tc_peak)}
 
 
 def time_e2e(qd, steps, warmup, world):
@@ -343,7 +443,7 @@ def time_qed_decode(qd, steps=50, warmup=5, N=512):
             "bytes_per_step": nbytes, "GBps": nbytes / (ms * 1e-3) / 1e9}
 
 
-def time_qed(qd, steps=20, warmup=3):
+def time_qed(qd, hbm_peak, tc_peak, peak_kind, steps=20, warmup=3):
     import torch
     _, d = synth.qed_gdn2()
     bf = torch.bfloat16
@@ -362,10 +462,11 @@ def time_qed(qd, steps=20, warmup=3):
     torch.cuda.synchronize()
     ms = start.elapsed_time(end) / steps
     th = 4 * 4096 * 8
-    nbytes = th * (2 * (128 * 5 + 128)) + 4 * 8 * 128 * 128 * 4
+    # q, k, v, g, b, w and o in bf16 (seven d-vectors) per token-head, lambda_h, the fp32 final state
+    nbytes = th * (2 * 7 * 128) + 8 * 4 + 4 * 8 * 128 * 128 * 4
     return {"workload": "qed_bf16_B4_H8_T4096_d128", "ms_per_step": ms, "tokens_per_s": 4 * 4096 / (ms * 1e-3),
-            "GBps": nbytes / (ms * 1e-3) / 1e9,
-            "tensor_TFLOPs": th * FLOPS_PER_TOKEN_HEAD / (ms * 1e-3) / 1e12}
+            "GBps": nbytes / (ms * 1e-3) / 1e9, "launches_per_step": qd.last_launch_count(),
+            "roofline": hbm_roofline(nbytes, ms, hbm_peak, peak_kind, th * FLOPS_PER_TOKEN_HEAD, tc_peak)}
 
 
 def time_prologue(qd, steps=20, warmup=3):
@@ -512,9 +613,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip the decode / QED / e2e / CPU legs")
-    ap.add_argument("--profile", nargs="?", const="fwd", choices=["fwd", "bwd", "eda"],
-                    help="profiling case: run warmup + steps forwards (fwd), backwards (bwd) or EDA "
-                         "forwards (eda) of the workload untimed, print no JSON line")
+    ap.add_argument("--profile", nargs="?", const="fwd",
+                    choices=["fwd", "bwd", "eda", "decode", "qed_decode", "qed", "long"],
+                    help="profiling case: run warmup + steps calls of one leg untimed (fwd: the step's "
+                         "forward; bwd, eda, decode, qed_decode, qed, long: those legs' workloads), "
+                         "print no JSON line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -544,6 +647,16 @@ def main():
         time_bwd(qd, tc_peak, steps=args.steps, warmup=args.warmup)
         print(f"profile case done: {args.warmup + args.steps} backwards, status {qd.qd_device_status()}", flush=True)
         return
+    legs = {"decode": lambda: time_decode(qd, steps=args.steps, warmup=args.warmup),
+            "qed_decode": lambda: time_qed_decode(qd, steps=args.steps, warmup=args.warmup),
+            "qed": lambda: time_qed(qd, hbm_peak, tc_peak, peak_kind, steps=args.steps, warmup=args.warmup),
+            "long": lambda: time_long_context(qd, hbm_peak, tc_peak, peak_kind, steps=args.steps,
+                                              warmup=args.warmup)}
+    if args.profile in legs:
+        legs[args.profile]()
+        print(f"profile case done: {args.warmup + args.steps} calls of {args.profile}, "
+              f"status {qd.qd_device_status()}", flush=True)
+        return
 
     sets = make_buffers(N_BUFFERS, seed_base=1 + rank)
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
@@ -551,9 +664,11 @@ def main():
     sampler = ClockSampler(smi_index)
     sampler.start()
     time.sleep(0.3)
-    total_ms, launch_ms, launches, (tw0, tw1) = time_device(qd, sets, args.steps, args.warmup, world)
+    total_ms, launch_ms, launches, (tw0, tw1) = time_device(qd, sets, args.steps, args.warmup, world,
+                                                            soak_s=SOAK_S)
     sampler.stop()
     clocks = sampler.summary(tw0, tw1)
+    clocks["window"] = f"the {args.steps} timed steps and {SOAK_S} s of the same steps, untimed, on either side"
     ms_step = max_over_ranks(total_ms / args.steps, world)
     value = job_tokens_per_s(ms_step, world)
     launch_ms = max_over_ranks(launch_ms, world)
@@ -570,7 +685,10 @@ def main():
             qdec = time_qed_decode(qd)
             qdec["frac_hbm"] = qdec["GBps"] / hbm_peak
             extras["qed_decode"] = qdec
-            extras["qed"] = time_qed(qd)
+            extras["qed"] = time_qed(qd, hbm_peak, tc_peak, peak_kind)
+            extras["deltanet"] = time_mode(qd, sets, "deltanet", hbm_peak, tc_peak, peak_kind)
+            extras["gdn"] = time_mode(qd, sets, "gdn", hbm_peak, tc_peak, peak_kind)
+            extras["long_context"] = time_long_context(qd, hbm_peak, tc_peak, peak_kind)
             extras["prologue"] = time_prologue(qd)
             extras["backward"] = time_bwd(qd, tc_peak)
             extras["eda"] = time_eda(qd)
