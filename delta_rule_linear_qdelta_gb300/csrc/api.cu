@@ -87,7 +87,10 @@ size_t qdelta_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd
 
 size_t qed_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype) {
     if (B <= 0 || T <= 0 || H <= 0 || chunk != 64) return 0;
-    return qd::qdelta_segment_workspace(B, H, qd::qed_segments(B, T, H, dk, dv, dtype));
+    qd::QedArgs a{};
+    a.B = B; a.T = T; a.H = H; a.dk = dk; a.dv = dv;
+    if (!qd::qed_tc_supported(a, dtype)) return 0;     // the CUDA-core path needs none
+    return qd::qed_tc_workspace(B, T, H, qd::qed_segments(B, T, H, dk, dv, dtype));
 }
 
 size_t qdelta_bwd_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype) {
@@ -299,7 +302,7 @@ qd_status qed_fwd_variant(const void *q, const void *k, const void *v, const voi
     cudaError_t e;
     if (qd::qed_tc_supported(a, dtype)) {
         const int G = qd::qed_segments(B, T, H, dk, dv, dtype);
-        e = G > 1 ? qd::launch_qed_segmented(a, G, stream, &n) : qd::launch_qed_chunk_tc(a, stream, &n);
+        e = qd::launch_qed_tc(a, G, stream, &n);
     } else {
         e = qd::launch_qed_chunk_simt(a, dtype, stream, &n);
     }
@@ -372,9 +375,9 @@ qd_status qd_device_status(cudaStream_t stream) {
     g_err[0] = 0;
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "qd_device_status");
-    const bool t1 = qd::tc_read_and_clear_timeout(), t2 = qd::qed_tc_read_and_clear_timeout();
+    const bool t1 = qd::tc_read_and_clear_timeout();
     const bool t3 = qd::selftest_read_and_clear_timeout();
-    if (t1 || t2 || t3)
+    if (t1 || t3)
         return fail(QD_ERR_TIMEOUT, "a tensor-core kernel gave up a bounded wait (results of that call are invalid)");
     return QD_OK;
 }

@@ -119,6 +119,7 @@ struct TcParams {
     float *S_final;
     int B, T, H;
     int flags;   // kTcNoV | kTcS0Identity | kTcNoO (segment-scan passes)
+    const float *ecg;   // QED: e^{G_C} per chunk and channel, [B*H][nchunks][128]
 };
 
 // PRO: q, k, alpha, beta, lambda arrive as projections and logits (the prologue of
@@ -126,11 +127,16 @@ struct TcParams {
 // CHK: the fp32 state entering every chunk is written to [B*H][nchunks][dv][dk] (the
 // backward's checkpoints), from the registers that already hold it on its way into
 // TMEM.  That instance runs without output (kTcNoO) and takes the array in p.o.
-template <bool PRO, bool CHK = false>
+// QED: the chain of the QED forward (chunk_tc_qed.cu) over its derived operands: tmA,
+// tmQ, tmK, tmV map Ae, Qe, Ke, W*V, the X rows are loaded (Ae) instead of formed, every
+// gate is a unit (alpha = 1, beta = 1, lambda = 0: the products above then are QED's
+// Gram, masks, solve, U, W, Z, O and S + Z^T Ke), and the epilogue multiplies the state
+// by the chunk's e^{G_C} per channel (column of the [dv][dk] state).
+template <bool PRO, bool CHK = false, bool QED = false>
 __global__ void __launch_bounds__(kAllThreads, 1)
 qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                     const __grid_constant__ CUtensorMap tmO) {
+                     const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmA) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t bar_full[2], bar_g, bar_uw, bar_z, bar_cp, bar_o2, bar_ready, bar_wfree, bar_cdone[2],
@@ -182,6 +188,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         if (!(p.flags & kTcNoO)) tma_prefetch_desc(&tmO);
+        if (QED) tma_prefetch_desc(&tmA);
     }
     if (warp == 0) {
         tmem_alloc(&tmem_base, 512);
@@ -195,9 +202,10 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         const int s = c & 1;
         uint8_t *st = sm + s * kStageBytes;
         const int t0 = c * kC;
-        mbar_arrive_expect_tx(&bar_full[s], no_v() ? kTmaBytes / 3 * 2 : kTmaBytes);
+        mbar_arrive_expect_tx(&bar_full[s], (no_v() ? kTmaBytes / 3 * 2 : kTmaBytes) + (QED ? kTmaBytes / 3 : 0));
 #pragma unroll
         for (int pnl = 0; pnl < 2; ++pnl) {
+            if (QED) tma_load_4d(st + OFF_XQ + pnl * 16384, &tmA, &bar_full[s], 64 * pnl, h, t0, b);
             tma_load_4d(st + OFF_XQ + pnl * 16384 + 8192, &tmQ, &bar_full[s], 64 * pnl, h, t0, b);
             tma_load_4d(st + OFF_K + pnl * 8192, &tmK, &bar_full[s], 64 * pnl, h, t0, b);
             if (!no_v()) tma_load_4d(st + OFF_V + pnl * 8192, &tmV, &bar_full[s], 64 * pnl, h, t0, b);
@@ -207,6 +215,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     // bf16 registers that nothing reads until compute_gates, so they do not stall the warp.
     __nv_bfloat16 ra[2], rb[2], rl[2];
     auto load_gates = [&](int c) {
+        if (QED) return;                                  // unit gates
         const __nv_bfloat16 *pa = opaque(p.alpha), *pl = opaque(p.lam);
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
@@ -226,7 +235,11 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
         for (int u = 0; u < 2; ++u) {                  // tokens past T: alpha 1, beta 0, lambda 0
             const bool ok = c * kC + 2 * lane + u < T;
-            if (pro) {                                 // gates from their logits
+            if (QED) {                                 // alpha 1, beta 1, lambda 0
+                la[u] = 0.f;
+                gb[u] = ok ? 1.f : 0.f;
+                gl[u] = 0.f;
+            } else if (pro) {                          // gates from their logits
                 const float x = bf(ra[u]);
                 la[u] = (ok && has_a) ? -(fmaxf(x, 0.f) + __logf(1.f + __expf(-fabsf(x)))) : 0.f;
                 gb[u] = ok ? sigmoid_fast(bf(rb[u])) : 0.f;
@@ -625,6 +638,16 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             tmem_ld32(tl + TM_S + 64 * half, *reinterpret_cast<float(*)[32]>(sv));
             tmem_ld32(tl + TM_S + 64 * half + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
             tmem_ld_wait();
+            if (QED) {                                // S <- (S + Z^T Ke) diag(e^{G_C}), staged in R2
+                const float *ecg = reinterpret_cast<const float *>(sm + OFF_R2) + 64 * half;
+#pragma unroll
+                for (int e = 0; e < 64; e += 4) {
+                    const float4 f = *reinterpret_cast<const float4 *>(ecg + e);
+                    const float2 x = fmul2(make_float2(sv[e], sv[e + 1]), make_float2(f.x, f.y));
+                    const float2 y = fmul2(make_float2(sv[e + 2], sv[e + 3]), make_float2(f.z, f.w));
+                    sv[e] = x.x; sv[e + 1] = x.y; sv[e + 2] = y.x; sv[e + 3] = y.y;
+                }
+            }
             if (CHK && !last) {
                 float *dst = reinterpret_cast<float *>(p.o) + (((size_t)bh * nchunks + c + 1) * kD + d_row) * kD + 64 * half;
 #pragma unroll
@@ -688,7 +711,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     if (prep) {
         // chunk 0's X and Gram; afterwards chunk c+1's are issued under chunk c's U/W
         wait_on(&bar_full[0], 0);
-        x_pass(0);
+        if (!QED) x_pass(0);                          // QED: the X rows (Ae) are loaded
         psync();
         issue_gram(0);
         for (int c = 0; c < nchunks; ++c) {
@@ -712,8 +735,10 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             issue_uw(c);
             if (c + 1 < nchunks) {                        // TM_G was read by masks(c)
                 wait_on(&bar_full[(c + 1) & 1], (uint32_t)(((c + 1) >> 1) & 1));
-                x_pass(c + 1);
-                fence_proxy_async();
+                if (!QED) {
+                    x_pass(c + 1);
+                    fence_proxy_async();
+                }
             }
             tc_fence_before();
             const bool stop = named_sync_or(kBarPrep, kPrepThreads, abort_flag != 0);
@@ -750,6 +775,8 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         }
         csync();
         for (int c = 0; c < nchunks; ++c) {
+            // QED: this chunk's e^{G_C}, element d_row (into R2 once Z has read -W^T there)
+            const float ecg = QED ? p.ecg[((size_t)bh * nchunks + c) * kD + d_row] : 0.f;
             wait_on(&bar_ready, (uint32_t)(c & 1));
             wait_mma(&bar_uw, c);
             const bool fold = g_ell[c & 3][kC - 1] > kFoldLog;
@@ -759,6 +786,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             if (c_issuer) mbar_arrive(&bar_wfree);
             issue_z_o(c);
             wait_mma(&bar_z, c);
+            if (QED) reinterpret_cast<float *>(sm + OFF_R2)[d_row] = ecg;   // read after the csyncs below
             zt_pack(c, 0, fold);
             csync();
             issue_couple(c);
@@ -823,8 +851,26 @@ cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nla
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     TcParams p{(const __nv_bfloat16 *)a.alpha, (const __nv_bfloat16 *)a.beta, (const __nv_bfloat16 *)a.lam,
-               a.S0, a.S_chk ? (__nv_bfloat16 *)a.S_chk : (__nv_bfloat16 *)a.o, a.S_final, a.B, a.T, a.H, flags};
-    kern<<<a.B * a.H, kAllThreads, kSmemBytes, s>>>(p, mq, mk, mv, mo);
+               a.S0, a.S_chk ? (__nv_bfloat16 *)a.S_chk : (__nv_bfloat16 *)a.o, a.S_final, a.B, a.T, a.H, flags,
+               nullptr};
+    kern<<<a.B * a.H, kAllThreads, kSmemBytes, s>>>(p, mq, mk, mv, mo, mq);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) *nlaunch += 1;
+    return e;
+}
+
+cudaError_t launch_qed_chain_tc(const QedArgs &a, const QedDerived &d, cudaStream_t s, int *nlaunch, int flags) {
+    CUtensorMap ma, mq, mk, mv, mo;
+    if (!make_token_map(&ma, d.Ae, a.B, a.T, a.H) || !make_token_map(&mq, d.Qe, a.B, a.T, a.H) ||
+        !make_token_map(&mk, d.Ke, a.B, a.T, a.H) || !make_token_map(&mv, d.WV, a.B, a.T, a.H))
+        return cudaErrorInvalidValue;
+    if (flags & kTcNoO) mo = mq;                      // not used
+    else if (!make_token_map(&mo, a.o, a.B, a.T, a.H)) return cudaErrorInvalidValue;
+    auto kern = qdelta_fwd_tc_kernel<false, false, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    TcParams p{nullptr, nullptr, nullptr, a.S0, (__nv_bfloat16 *)a.o, a.S_final, a.B, a.T, a.H, flags, d.ecg};
+    kern<<<a.B * a.H, kAllThreads, kSmemBytes, s>>>(p, mq, mk, mv, mo, ma);
     e = cudaGetLastError();
     if (e == cudaSuccess) *nlaunch += 1;
     return e;

@@ -166,9 +166,22 @@ cudaError_t launch_qed_step(const QedStepArgs &a, int dtype, cudaStream_t s, int
 enum { kTcNoV = 1, kTcS0Identity = 2, kTcNoO = 4 };
 bool qdelta_tc_supported(const QDeltaArgs &a, int dtype);
 cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nlaunch, int flags = 0);
-// Tensor-core (tcgen05) chunked QED forward: bf16, dk = dv = 128; flags as above.
+// Tensor-core (tcgen05) chunked QED forward: bf16, dk = dv = 128; flags as above.  The
+// state-independent per-chunk operands are derived first (qed_derive_kernel) into the
+// workspace, over the same [B][T] view the chain kernel then runs on (a segment view
+// when segmented): Ae, Qe, Ke, W*V as [B][T][H][128] bf16 and e^{G_C} as
+// [B][H][nchunks][128] fp32.
+struct QedDerived {
+    void *Ae, *Qe, *Ke, *WV;
+    float *ecg;
+};
 bool qed_tc_supported(const QedArgs &a, int dtype);
-cudaError_t launch_qed_chunk_tc(const QedArgs &a, cudaStream_t s, int *nlaunch, int flags = 0);
+size_t qed_derived_bytes(int B, int T, int H, int G);
+QedDerived qed_derived_buffers(int B, int T, int H, void *ws);
+cudaError_t launch_qed_derive(const QedArgs &a, const QedDerived &d, int no_v, cudaStream_t s, int *nlaunch);
+// One pass of the chain kernel over derived operands (the QED instance of the Q-Delta
+// tensor-core kernel); a carries the view's sizes, S0, o and S_final.
+cudaError_t launch_qed_chain_tc(const QedArgs &a, const QedDerived &d, cudaStream_t s, int *nlaunch, int flags = 0);
 // Segment scan of the tensor-core forward for long sequences over few (b, h)
 // streams: the number of segments for these sizes (1 = a single pass), its
 // workspace, and the launch (three passes of the forward kernel and a combine).
@@ -178,14 +191,18 @@ cudaError_t launch_qdelta_segmented(const QDeltaArgs &a, int G, cudaStream_t s, 
 // The same for QED, whose per-chunk state map is also a right-multiplication of the
 // [dv][dk] state (S_out = S_in Phi + Psi); qed_segments is its own policy.
 int qed_segments(int B, int T, int H, int dk, int dv, int dtype);
-cudaError_t launch_qed_segmented(const QedArgs &a, int G, cudaStream_t s, int *nlaunch);
+cudaError_t launch_qed_segmented(const QedArgs &a, int G, const QedDerived &d, cudaStream_t s, int *nlaunch);
+// The whole tensor-core QED forward: derive over the (segment) view, then one chain pass
+// or the segment scan.  Workspace: qed_tc_workspace(B, T, H, G) bytes at a.ws (the
+// derived operands, then the segment states).
+size_t qed_tc_workspace(int B, int T, int H, int G);
+cudaError_t launch_qed_tc(const QedArgs &a, int G, cudaStream_t s, int *nlaunch);
 // Reads and clears the device word the tensor-core kernels set when a bounded wait runs out.
 bool tc_read_and_clear_timeout();
 // One CTA whose only mbarrier wait can never complete, bounded by limit_ns: sets its own
 // timeout word, read and cleared like the kernels' by selftest_read_and_clear_timeout.
 cudaError_t launch_wait_selftest(uint64_t limit_ns, cudaStream_t s);
 bool selftest_read_and_clear_timeout();
-bool qed_tc_read_and_clear_timeout();
 
 // Records `msg` as this host thread's last error (qd_last_error) and returns `status`.
 qd_status report_error(qd_status status, const char *msg);

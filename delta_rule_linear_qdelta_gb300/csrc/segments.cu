@@ -111,10 +111,10 @@ int qdelta_segments(int B, int T, int H, int dk, int dv, int dtype) {
 }
 
 int qed_segments(int B, int T, int H, int dk, int dv, int dtype) {
-    // The same policy as Q-Delta.  Each QED pass repeats the whole per-chunk preparation
-    // (its kernel is not warp-specialised), but with the combine spread over eight CTAs per
-    // head three passes still pay: on the 32-stream QED workload (B=4, H=8, T=4096) four
-    // segments take 0.55 ms against 0.62 ms for one pass.
+    // The Q-Delta policy, for at most 16 streams.  QED derives its operands once for all
+    // three passes, but each pass still repeats the chain; on the 32-stream QED workload
+    // (B=4, H=8, T=4096) one pass takes 0.325 ms against 0.372 ms for four segments.
+    if ((long long)B * H > 16) return 1;
     return qdelta_segments(B, T, H, dk, dv, dtype);
 }
 
@@ -160,9 +160,9 @@ cudaError_t launch_qdelta_segmented(const QDeltaArgs &a, int G, cudaStream_t s, 
                          [&](const QDeltaArgs &x, int f) { return launch_qdelta_chunk_tc(x, s, nlaunch, f); });
 }
 
-cudaError_t launch_qed_segmented(const QedArgs &a, int G, cudaStream_t s, int *nlaunch) {
+cudaError_t launch_qed_segmented(const QedArgs &a, int G, const QedDerived &d, cudaStream_t s, int *nlaunch) {
     return run_segmented(a, G, s, nlaunch,
-                         [&](const QedArgs &x, int f) { return launch_qed_chunk_tc(x, s, nlaunch, f); });
+                         [&](const QedArgs &x, int f) { return launch_qed_chain_tc(x, d, s, nlaunch, f); });
 }
 
 }  // namespace qd

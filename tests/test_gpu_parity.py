@@ -280,7 +280,7 @@ def test_qed_segmented_long_sequence_all_outputs(qd):
     d = synth.qed_inputs(1, 2048, 2, 128, 128, seed=57, dtype="bf16", s0_var=0.01)
     assert qd.qed_workspace_bytes(1, 2048, 2, 128, 128) > 0
     o, S = run_qed(qd, d)
-    assert qd.last_launch_count() == 4
+    assert qd.last_launch_count() == 5    # the operand derivation, three segment passes, the combine
     o_ref, S_ref = oracle.qed_fwd(d["q"], d["k"], d["v"], d["g"], d["b"], d["w"], d["lam_h"], d["S0"])
     check(o, o_ref, "bf16", "segmented qed o")
     check(S, S_ref, "bf16", "segmented qed S")
