@@ -375,9 +375,9 @@ qd_status qd_device_status(cudaStream_t stream) {
     g_err[0] = 0;
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "qd_device_status");
-    const bool t1 = qd::tc_read_and_clear_timeout();
+    const bool t1 = qd::tc_read_and_clear_timeout(), t2 = qd::bwd_tc_read_and_clear_timeout();
     const bool t3 = qd::selftest_read_and_clear_timeout();
-    if (t1 || t3)
+    if (t1 || t2 || t3)
         return fail(QD_ERR_TIMEOUT, "a tensor-core kernel gave up a bounded wait (results of that call are invalid)");
     return QD_OK;
 }

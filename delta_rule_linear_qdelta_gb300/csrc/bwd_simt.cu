@@ -540,7 +540,7 @@ template <typename TIn, int DK, int DVT>
 cudaError_t run_bwd(const QDeltaBwdArgs &a, cudaStream_t s, bool mma_sweep) {
     cudaError_t e;
     if (mma_sweep) {
-        e = launch_qdelta_bwd_dstate_mma(a, s);
+        e = launch_qdelta_bwd_dstate_tc(a, s);
     } else {
         auto ks = qdelta_bwd_dstate_kernel<TIn, DK, DVT>;
         constexpr size_t sm_s = dstate_smem<DK, DVT>();
