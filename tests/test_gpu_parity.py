@@ -560,21 +560,23 @@ def test_backward_empty_sequence_passes_state_gradient(qd):
     np.testing.assert_array_equal(g["dS0"], c["dS_final"])
 
 
-def test_backward_full_size_sampled_streams(qd):
-    """The 1.3B-layer workload (B=8, H=16, T=2048, d=128, bf16) in one call; four
-    (b, h) streams compared with the oracle over the whole sequence."""
+def test_backward_full_size_every_stream(qd):
+    """The 1.3B-layer workload (B=8, H=16, T=2048, d=128, bf16) in one call; every
+    gradient of every (b, h) stream compared with the oracle over the whole sequence,
+    stream by stream and as a whole."""
     _, d = synth.layer_1p3b()
     B, T, H = 8, 2048, 16
     c = synth.cotangents(B, T, H, 128, 128, seed=74, dtype="bf16")
     g = run_bwd(qd, d, c)
-    pairs = [(0, 0), (3, 7), (5, 11), (7, 15)]
-    ref = oracle.qdelta_bwd(sel(d["q"], pairs), sel(d["k"], pairs), sel(d["v"], pairs), sel(d["alpha"], pairs),
-                            sel(d["beta"], pairs), sel(d["lam"], pairs), None, sel(c["dO"], pairs),
-                            np.stack([c["dS_final"][b, h] for b, h in pairs])[:, None])
+    ref = oracle.qdelta_bwd(d["q"], d["k"], d["v"], d["alpha"], d["beta"], d["lam"], None, c["dO"],
+                            c["dS_final"])
     for name in GRAD_NAMES:
-        got = g[name]
-        got = np.stack([got[b, h] for b, h in pairs])[:, None] if name == "dS0" else sel(got, pairs)
-        check_grad(got, ref[name], "bf16", f"full-size {name}")
+        got, r = g[name], ref[name]
+        for b in range(B):
+            for h in range(H):
+                gs, rs = (got[b, h], r[b, h]) if name == "dS0" else (got[b, :, h], r[b, :, h])
+                check_grad(gs, rs, "bf16", f"full-size {name} stream (b={b}, h={h})")
+        check_grad(got, r, "bf16", f"full-size {name}")
 
 
 # ---------------------------------------------------------------- EDA
