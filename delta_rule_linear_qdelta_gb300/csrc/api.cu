@@ -376,8 +376,8 @@ qd_status qd_device_status(cudaStream_t stream) {
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return cuda_fail(e, "qd_device_status");
     const bool t1 = qd::tc_read_and_clear_timeout(), t2 = qd::bwd_tc_read_and_clear_timeout();
-    const bool t3 = qd::selftest_read_and_clear_timeout();
-    if (t1 || t2 || t3)
+    const bool t3 = qd::selftest_read_and_clear_timeout(), t4 = qd::grad_tc_read_and_clear_timeout();
+    if (t1 || t2 || t3 || t4)
         return fail(QD_ERR_TIMEOUT, "a tensor-core kernel gave up a bounded wait (results of that call are invalid)");
     return QD_OK;
 }

@@ -27,10 +27,10 @@
 //      (S_chk): the tcgen05 kernel for bf16 at d = 128, else the fp32 CUDA-core one;
 //   2. the reverse sweep of dS over the chunks (qdelta_bwd_dstate_kernel here, one CTA
 //      per (b, h, d_v tile), since rows of dS evolve independently as rows of S do; the
-//      warp tensor-core sweep of bwd_mma.cu for bf16 at d = 128), storing the
+//      tcgen05 sweep of bwd_tc.cu for bf16 at d = 128), storing the
 //      gradient reaching the state leaving each chunk (dS_chk) and dS0.  It needs no
 //      forward state: dS_in depends only on dS_out, dO, q, k and the gates;
-//   3. qdelta_bwd_grad_kernel (or its warp tensor-core version in bwd_mma.cu for bf16
+//   3. qdelta_bwd_grad_kernel (or its tcgen05 version in bwd_grad_tc.cu for bf16
 //      at d = 128): every input gradient, one CTA per (b, h, chunk), all chunks in
 //      parallel, from the two checkpoints of its chunk.
 // A ragged last chunk is padded with alpha = 1, beta = 0, lambda = 0 and zero tokens and
@@ -537,9 +537,9 @@ constexpr size_t grad_smem() {
 }
 
 template <typename TIn, int DK, int DVT>
-cudaError_t run_bwd(const QDeltaBwdArgs &a, cudaStream_t s, bool mma_sweep) {
+cudaError_t run_bwd(const QDeltaBwdArgs &a, cudaStream_t s, bool tc) {
     cudaError_t e;
-    if (mma_sweep) {
+    if (tc) {
         e = launch_qdelta_bwd_dstate_tc(a, s);
     } else {
         auto ks = qdelta_bwd_dstate_kernel<TIn, DK, DVT>;
@@ -550,7 +550,7 @@ cudaError_t run_bwd(const QDeltaBwdArgs &a, cudaStream_t s, bool mma_sweep) {
         e = cudaGetLastError();
     }
     if (e != cudaSuccess) return e;
-    if (mma_sweep) return launch_qdelta_bwd_grad_mma(a, s);
+    if (tc) return launch_qdelta_bwd_grad_tc(a, s);
     auto kg = qdelta_bwd_grad_kernel<TIn, DK>;
     constexpr size_t sm_g = grad_smem<DK>();
     e = cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_g);
@@ -590,7 +590,7 @@ cudaError_t launch_qdelta_bwd(const QDeltaBwdArgs &a, int dtype, cudaStream_t s,
                                                   : launch_qdelta_chunk_simt(f, dtype, s, nlaunch);
     if (e != cudaSuccess) return e;
     // 2. reverse sweep of dS and 3. the per-chunk gradients
-    const bool m = qdelta_bwd_mma_supported(a, dtype);
+    const bool m = qdelta_bwd_tc_supported(a, dtype);
     e = dtype == kBF16 ? dispatch_bwd<__nv_bfloat16>(a, s, m) : dispatch_bwd<float>(a, s, m);
     if (e == cudaSuccess) *nlaunch += 2;
     return e;

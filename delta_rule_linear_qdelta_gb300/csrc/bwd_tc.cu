@@ -558,6 +558,10 @@ qdelta_bwd_dstate_tc_kernel(const BwdTcParams p, const __grid_constant__ CUtenso
 
 }  // namespace
 
+bool qdelta_bwd_tc_supported(const QDeltaBwdArgs &a, int dtype) {
+    return dtype == kBF16 && a.nk == kD && a.nv == kD;
+}
+
 cudaError_t launch_qdelta_bwd_dstate_tc(const QDeltaBwdArgs &a, cudaStream_t s) {
     CUtensorMap mq, mk, md;
     if (!make_token_map(&mq, a.q, a.B, a.T, a.H) || !make_token_map(&mk, a.k, a.B, a.T, a.H) ||

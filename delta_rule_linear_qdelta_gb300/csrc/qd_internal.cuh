@@ -151,12 +151,13 @@ PrologueBwdBuffers prologue_bwd_buffers(int B, int T, int H, int dk, int dtype);
 cudaError_t launch_prologue_map(const QDeltaBwdArgs &raw, int dtype, uint8_t *ws, cudaStream_t s, int *nlaunch);
 cudaError_t launch_prologue_chain(const QDeltaBwdArgs &raw, int dtype, const uint8_t *ws, cudaStream_t s,
                                   int *nlaunch);
-// The per-chunk gradients on the warp tensor cores (TF32): bf16 with dk = dv = 128.
-bool qdelta_bwd_mma_supported(const QDeltaBwdArgs &a, int dtype);
-// The reverse sweep on the tcgen05 tensor cores (bf16, dk = dv = 128) and its timeout word.
+// The reverse sweep and the per-chunk gradients on the tcgen05 tensor cores (bf16,
+// dk = dv = 128: qdelta_bwd_tc_supported) and their timeout words.
+bool qdelta_bwd_tc_supported(const QDeltaBwdArgs &a, int dtype);
 cudaError_t launch_qdelta_bwd_dstate_tc(const QDeltaBwdArgs &a, cudaStream_t s);
+cudaError_t launch_qdelta_bwd_grad_tc(const QDeltaBwdArgs &a, cudaStream_t s);
 bool bwd_tc_read_and_clear_timeout();
-cudaError_t launch_qdelta_bwd_grad_mma(const QDeltaBwdArgs &a, cudaStream_t s);
+bool grad_tc_read_and_clear_timeout();
 cudaError_t launch_qed_chunk_simt(const QedArgs &a, int dtype, cudaStream_t s, int *nlaunch);
 cudaError_t launch_qdelta_step(const StepArgs &a, int dtype, cudaStream_t s, int *nlaunch);
 cudaError_t launch_qed_step(const QedStepArgs &a, int dtype, cudaStream_t s, int *nlaunch);

@@ -273,6 +273,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with A and B fp16 (kind::f16 takes both operands in one of the two types).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
 // Byte offset of element (row, col) in a 128B-swizzled tile of 64 bf16 columns
 // (128-byte rows, 1024-byte aligned base): 16-byte chunk index XOR (row mod 8).
 __device__ __forceinline__ uint32_t sw128_off(int row, int col) {

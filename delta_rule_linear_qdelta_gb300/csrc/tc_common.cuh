@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "sm103_ptx.cuh"
@@ -71,6 +72,41 @@ __device__ __forceinline__ uint4 pack8p(const float *f) {
     return u;
 }
 __device__ __forceinline__ uint4 pack8(const float (&f)[8]) { return pack8p(f); }
+
+// The same for fp16 (the operands of a kind::f16 product taken as f16)
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ void unpack8h(const uint4 &u, float (&f)[8]) {
+    const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 t = __half22float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+__device__ __forceinline__ uint4 pack8hp(const float *f) {
+    uint4 u;
+    u.x = pack_half2(f[0], f[1]);
+    u.y = pack_half2(f[2], f[3]);
+    u.z = pack_half2(f[4], f[5]);
+    u.w = pack_half2(f[6], f[7]);
+    return u;
+}
+// two 16-bit values of the chosen type
+template <bool kHalf> __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    return kHalf ? pack_half2(lo, hi) : pack_bf16x2(lo, hi);
+}
+template <bool kHalf> __device__ __forceinline__ uint16_t cvt16(float x) {
+    if (kHalf) {
+        __half v = __float2half_rn(x);
+        return *reinterpret_cast<uint16_t *>(&v);
+    }
+    __nv_bfloat16 v = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t *>(&v);
+}
 
 
 // ---------------------------------------------------------- warp-level TF32 MMA
@@ -150,22 +186,23 @@ __device__ __forceinline__ uint32_t core_off(int row, int col) {
     return (uint32_t)((row >> 3) * 512 + (col >> 3) * 128 + (row & 7) * 16 + (col & 7) * 2);
 }
 
-// bf16 outputs of the inverse: s * Tinv(row, col) * s1[col] into out1 and, unless
-// out2 is null, times s2[col] into out2 (null scales mean 1); col is even and
-// (v0, v1) are columns col and col + 1 of the row.
+// 16-bit outputs of the inverse (bf16, or fp16 with kHalf): s * Tinv(row, col) * s1[col]
+// into out1 and, unless out2 is null, times s2[col] into out2 (null scales mean 1); col is
+// even and (v0, v1) are columns col and col + 1 of the row.
+template <bool kHalf = false>
 __device__ __forceinline__ void put_pair(uint8_t *out1, uint8_t *out2, const float *s1, const float *s2, int row,
                                          int col, float v0, float v1) {
     const float a0 = s1 ? v0 * s1[col] : v0, a1 = s1 ? v1 * s1[col + 1] : v1;
     const uint32_t off = sw128_off(row, col);
-    *reinterpret_cast<uint32_t *>(out1 + off) = pack_bf16x2(a0, a1);
+    *reinterpret_cast<uint32_t *>(out1 + off) = pack2<kHalf>(a0, a1);
     if (out2)
         *reinterpret_cast<uint32_t *>(out2 + off) =
-            pack_bf16x2(s2 ? a0 * s2[col] : a0, s2 ? a1 * s2[col + 1] : a1);
+            pack2<kHalf>(s2 ? a0 * s2[col] : a0, s2 ? a1 * s2[col + 1] : a1);
 }
 
 // Tinv = (I + A)^{-1} for the 64x64 strictly lower fp32 matrix A held in M (row
 // stride LA, zero on and above the diagonal).  Writes Tinv diag(s1) to out1 and
-// Tinv diag(s1 s2) to out2 as bf16 [64][64] tiles in the 128-byte swizzle, each
+// Tinv diag(s1 s2) to out2 as bf16 (fp16 with kHalf) [64][64] tiles in the 128-byte swizzle, each
 // block as soon as it is final (null scales mean 1, null out2 skips it).  out1 and
 // out2 must not overlap M and must hold zeros above the 8x8 diagonal blocks (that
 // part of the inverse is zero and is never written).  Y is >= 32*LY floats of
@@ -193,7 +230,7 @@ __device__ __forceinline__ void put_pair(uint8_t *out1, uint8_t *out2, const flo
 // (core_off below) to out3; out1/out2 then hold the block-diagonal inverse
 // diag(T11, T22) with the same scalings.  Since T21 = -M21 T11, a solve (I + A) z = r is finished from the
 // block-diagonal one, zl = diag(T11, T22) r, by z_bot = zl_bot - M21 z_top.
-template <bool kCouple = false, typename Idle, typename Sync>
+template <bool kCouple = false, bool kHalf = false, typename Idle, typename Sync>
 __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *out1, uint8_t *out2,
                                                    const float *s1, const float *s2, Idle idle, Sync sync,
                                                    uint8_t *out3 = nullptr, const float *s3 = nullptr,
@@ -232,8 +269,8 @@ __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *
 #pragma unroll
             for (int i = 0; i < 8; ++i) {                  // the whole block, zeros above the diagonal
                 const uint32_t off = sw128_off(base + i, base + j);
-                *reinterpret_cast<__nv_bfloat16 *>(out1 + off) = __float2bfloat16_rn(t[i] * c1);
-                if (out2) *reinterpret_cast<__nv_bfloat16 *>(out2 + off) = __float2bfloat16_rn(t[i] * c2);
+                *reinterpret_cast<uint16_t *>(out1 + off) = cvt16<kHalf>(t[i] * c1);
+                if (out2) *reinterpret_cast<uint16_t *>(out2 + off) = cvt16<kHalf>(t[i] * c2);
             }
         }
         __syncwarp();
@@ -247,7 +284,7 @@ __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *
             __syncwarp();
             tile8_cab(d, Yw, LY, M + (base + 8) * LA + base + 8, LA, Yw, LY);
             *reinterpret_cast<float2 *>(M + (base + 8 + g) * LA + base + 2 * t4) = make_float2(-d[0], -d[1]);
-            put_pair(out1, out2, s1, s2, base + 8 + g, base + 2 * t4, -d[0], -d[1]);
+            put_pair<kHalf>(out1, out2, s1, s2, base + 8 + g, base + 2 * t4, -d[0], -d[1]);
         }
         named_sync(8 + (warp >> 1), 64);  // the pair's two 16x16 blocks are final
         // 16 -> 32: warp w < 4 takes pair p = w / 2 (blocks at 32 p) and 8-column tile w % 2
@@ -261,8 +298,8 @@ __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *
             named_sync(8 + p, 64);        // the pair's A10 has been read before T10 overwrites it
             tile_cab<16>(d, Yp + n0, LY, M + (base + 16) * LA + base + 16, LA, Yp + n0, LY);   // Y + T11s Y
             tile_store(M + (base + 16) * LA + base + n0, LA, d, -1.f);
-            put_pair(out1, out2, s1, s2, base + 16 + g, base + n0 + 2 * t4, -d[0], -d[1]);
-            put_pair(out1, out2, s1, s2, base + 24 + g, base + n0 + 2 * t4, -d[2], -d[3]);
+            put_pair<kHalf>(out1, out2, s1, s2, base + 16 + g, base + n0 + 2 * t4, -d[0], -d[1]);
+            put_pair<kHalf>(out1, out2, s1, s2, base + 24 + g, base + n0 + 2 * t4, -d[2], -d[3]);
         }
     }
     sync();
@@ -286,8 +323,8 @@ __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *
         tile_store(Y + m0 * LY + n0, LY, d, 1.f);
         named_sync(10 + (warp & 3), 64);   // warps w and w ^ 4: Y columns n0..n0+7, all 32 rows
         tile_cab<32>(d, Y + m0 * LY + n0, LY, M + (32 + m0) * LA + 32, LA, Y + n0, LY);    // Y + T22s Y
-        put_pair(out1, out2, s1, s2, 32 + m0 + g, n0 + 2 * t4, -d[0], -d[1]);
-        put_pair(out1, out2, s1, s2, 40 + m0 + g, n0 + 2 * t4, -d[2], -d[3]);
+        put_pair<kHalf>(out1, out2, s1, s2, 32 + m0 + g, n0 + 2 * t4, -d[0], -d[1]);
+        put_pair<kHalf>(out1, out2, s1, s2, 40 + m0 + g, n0 + 2 * t4, -d[2], -d[3]);
     }
 }
 

@@ -209,10 +209,11 @@ QD_API qd_status qdelta_step_prologue(float *S, const void *q_raw, const void *k
  * bytes (two fp32 checkpoint arrays: the state entering, and the gradient reaching
  * the state leaving, every chunk of 64 tokens).  T = 0 writes dS0 = dS_final (or 0)
  * and nothing else.  Precision: fp32 inputs, and head dims other than 128, run in
- * fp32 on CUDA cores.  bf16 inputs at dk = dv = 128 run the state checkpoints on
- * the bf16 tensor-core forward (fp32 state, bf16 operands) and the reverse sweep and
- * per-chunk gradient products on TF32 tensor-core MMAs (fp32 accumulation, operands
- * rounded to TF32, 10-bit mantissa); the recurrence's elementwise work stays fp32.
+ * fp32 on CUDA cores.  bf16 inputs at dk = dv = 128 run on the tensor cores with fp32
+ * accumulation and fp32 state and state gradient: the state checkpoints on the bf16
+ * forward, the reverse sweep of the state gradient with bf16 operands, and the
+ * per-chunk gradients with fp16 operands (10-bit mantissa; their intermediates stay
+ * far inside fp16's range at unit-scale inputs); the elementwise work is fp32.
  * Errors as for qdelta_fwd.
  */
 QD_API qd_status qdelta_bwd(const void *q, const void *k, const void *v,
