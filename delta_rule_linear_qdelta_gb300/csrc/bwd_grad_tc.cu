@@ -2,7 +2,9 @@
 // TMEM + TMA): bf16 inputs, dk = dv = 128, chunk C = 64.  One CTA of 8 warps per
 // (b, h, chunk), all chunks in parallel, from the two checkpoints of its chunk: the
 // state entering it (S = S_chk) and the gradient reaching the state leaving it
-// (dS = dS_chk).
+// (dS = dS_chk), each an fp16 [dv][dk] tile already in the operand layout (written so by
+// the forward's checkpoint instance and the reverse sweep), copied in with one bulk copy
+// each beside the q, k, v, dO tiles.
 //
 // The adjoint of the WY form ("Q-Delta: Beyond Key-Value Associative State Evolution",
 // Sec. 3.3.2; the formulas are in bwd_simt.cu's header).  Per chunk, with H the decay
@@ -28,6 +30,10 @@
 // this kernel's roundings the relative error of dlambda, the gradient with the most
 // cancellation, is 5e-4 with fp16 operands against 4e-3 with bf16 ones.  These values stay
 // far inside fp16's range (|x| < 65504) at the workloads' scales.
+// S X^T, dS K^T and dO^T P need neither the inverse nor each other: they are issued as
+// soon as the masks are written, and the warps the solve's first phases leave idle form
+// R^T and dZ^T from them while the inverse runs, so the Z and dR products start as soon
+// as it ends.
 // Operands that a product needs transposed are written transposed from TMEM (16x256b
 // loads, stmatrix.trans) in the 128-byte swizzle.  Sums over a head dimension (the row
 // sums of the gate gradients) are a butterfly over the warp's 32 lanes, each lane ending
@@ -36,7 +42,7 @@
 // Shared memory, by phase (offsets from a 1024-aligned base):
 //   XQ  0       32 KB  X rows 0-63 | Q rows 64-127 (two 64-column panels; bf16 from TMA, fp16 after)
 //   RO  32768   32 KB  dO rows 64-127 (TMA, then fp16); dR rows 0-63 later; then E (fp32)
-//   Sb  65536   32 KB  S as fp16 [dv][dk];  dSb 98304  32 KB  dS as fp16
+//   Sb  65536   32 KB  S as fp16 [dv][dk];  dSb 98304  32 KB  dS as fp16 (bulk copies)
 //   K   131072  16 KB
 //   V   147456  16 KB  | T 163840 8 KB | T1 172032 8 KB;  all three later RS (32 KB:
 //                       -gamma beta dR rows 0-63 | gamma dO rows 64-127), then dq/dk rows
@@ -74,13 +80,13 @@ constexpr uint32_t OFF_MP = 180224, OFF_R1 = 196608, OFF_Y = 214016, OFF_ZR = OF
 constexpr uint32_t kSmemUsed = OFF_Y + 32 * LY * 4;   // 218624
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;
 static_assert(OFF_MP % 1024 == 0 && OFF_R1 % 1024 == 0 && OFF_Y >= OFF_R1 + 64 * LA * 4, "tile placement");
-constexpr uint32_t kTmaBytes = 4 * kC * kD * 2;      // q, k, v, dO tiles
+constexpr uint32_t kTmaBytes = 4 * kC * kD * 2 + 2 * kChkTileBytes;   // q, k, v, dO tiles; S, dS
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t TM_G = 0, TM_A = 64, TM_RP = 128, TM_Z = 160, TM_B = 224, TM_DR = 288, TM_D6 = 352, TM_ZP = 480;
 
 struct GradTcParams {
     const void *alpha, *beta, *lam;
-    const float *S_chk, *dS_chk;
+    const uint8_t *S_chk, *dS_chk;                    // fp16 checkpoint tiles (chk_tile_off)
     void *dq, *dk, *dv, *dalpha, *dbeta, *dlam;
     int B, T, H;
     int grad_f32, gates_f32;
@@ -147,7 +153,7 @@ qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensor
     const int T = p.T, H = p.H, nchunks = (T + kC - 1) / kC;
     const int c = blockIdx.x % nchunks, bh = blockIdx.x / nchunks, b = bh / H, h = bh % H;
     const int c0 = c * kC, n = min(kC, T - c0);
-    const size_t chk = ((size_t)bh * nchunks + c) * kD * kD;
+    const size_t chk = ((size_t)bh * nchunks + c) * kChkTileBytes;
     const bool issuer = (tid == 0);
     const uint32_t sbase = smem_u32(sm);
     auto tok_of = [&](int t) { return ((size_t)b * T + c0 + t) * H + h; };
@@ -180,6 +186,8 @@ qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensor
             tma_load_4d(sm + OFF_V + pnl * 8192, &tmV, &bar_ld, 64 * pnl, h, c0, b);
             tma_load_4d(sm + OFF_RO + pnl * 16384 + 8192, &tmD, &bar_ld, 64 * pnl, h, c0, b);
         }
+        bulk_load(sm + OFF_SB, p.S_chk + chk, kChkTileBytes, &bar_ld);
+        bulk_load(sm + OFF_DSB, p.dS_chk + chk, kChkTileBytes, &bar_ld);
     }
     // gates (tokens past T: alpha 1, beta 0, lambda 0)
     if (tid < kC) {
@@ -189,28 +197,6 @@ qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensor
         g_la[tid] = logf(a);
         g_beta[tid] = ok ? gate_val<__nv_bfloat16>(p.beta, tok, p.gates_f32) : 0.f;
         g_lam[tid] = (ok && p.lam) ? gate_val<__nv_bfloat16>(p.lam, tok, p.gates_f32) : 0.f;
-    }
-    // S and dS (fp32 checkpoints) -> fp16 [dv][dk] tiles, and <dS, S>
-    {
-        float dot = 0.f;
-#pragma unroll 2
-        for (int i = tid; i < kD * kD / 8; i += kNT) {
-            const int v = i >> 4, j = (i & 15) * 8;
-            const float4 s0 = *reinterpret_cast<const float4 *>(p.S_chk + chk + (size_t)v * kD + j);
-            const float4 s1 = *reinterpret_cast<const float4 *>(p.S_chk + chk + (size_t)v * kD + j + 4);
-            const float4 d0 = *reinterpret_cast<const float4 *>(p.dS_chk + chk + (size_t)v * kD + j);
-            const float4 d1 = *reinterpret_cast<const float4 *>(p.dS_chk + chk + (size_t)v * kD + j + 4);
-            dot += s0.x * d0.x + s0.y * d0.y + s0.z * d0.z + s0.w * d0.w + s1.x * d1.x + s1.y * d1.y + s1.z * d1.z +
-                   s1.w * d1.w;
-            const float sf[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-            const float df[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-            const uint32_t off = (uint32_t)(j >> 6) * 16384 + sw128_off(v, j & 63);
-            *reinterpret_cast<uint4 *>(sm + OFF_SB + off) = pack8hp(sf);
-            *reinterpret_cast<uint4 *>(sm + OFF_DSB + off) = pack8hp(df);
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-        if (lane == 0) sdot[warp] = dot;
     }
     __syncthreads();
     if (warp == 0) {                                   // l = inclusive prefix of log alpha; gamma, w, e^{-l}
@@ -297,6 +283,23 @@ qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensor
                       idesc_f16(128, 64, false, false), k > 0);
         }
     }
+    // <dS, S> over the two checkpoint tiles (one layout: an elementwise product) while the
+    // Gram runs
+    {
+        float dot = 0.f;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+            const uint32_t off = (uint32_t)(tid + kNT * r) << 4;
+            float sf[8], df[8];
+            unpack8h(*reinterpret_cast<const uint4 *>(sm + OFF_SB + off), sf);
+            unpack8h(*reinterpret_cast<const uint4 *>(sm + OFF_DSB + off), df);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) dot = fmaf(sf[e], df[e], dot);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        if (lane == 0) sdot[warp] = dot;
+    }
     commit_wait();
     // masks: A = beta M (fp32, R1) for the solve; M (rows 0-63) and P (rows 64-127) fp16 in MP
     {
@@ -323,62 +326,68 @@ qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensor
                     make_float4(bt * g[4 * c4], bt * g[4 * c4 + 1], bt * g[4 * c4 + 2], bt * g[4 * c4 + 3]);
         }
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    // T = (I + beta M)^{-1} (fp16, zero above the diagonal blocks) and T1 = T diag(beta)
-    unit_lower_inverse<false, true>(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_Y),
-                              sm + OFF_TT, sm + OFF_T1, nullptr, g_beta, []() {}, []() { __syncthreads(); });
-    sync_mma();
-
-    // ------------------------------------- S X^T, dS K^T, dO^T P (lanes d_v), then R, dZ
+    sync_mma();                                        // M, P (and A) written; TM_G read
+    // S X^T (into A), dS K^T (into G), dO^T P (into B), lanes d_v: they need neither the
+    // inverse nor each other, so they run while the solve does
     if (issuer) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
             umma_bf16(tm + TM_A, smem_desc(sbase + OFF_SB + ko, 16, 1024), smem_desc(sbase + OFF_XQ + ko, 16, 1024),
-                      idesc_f16(128, 64, false, false), k > 0);
+                          idesc_f16(128, 64, false, false), k > 0);
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
             umma_bf16(tm + TM_G, smem_desc(sbase + OFF_DSB + ko, 16, 1024),
-                      smem_desc(sbase + OFF_K + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024),
-                      idesc_f16(128, 64, false, false), k > 0);
+                          smem_desc(sbase + OFF_K + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024),
+                          idesc_f16(128, 64, false, false), k > 0);
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k)
             umma_bf16(tm + TM_B, smem_desc(sbase + OFF_RO + 8192 + k * 2048, 16384, 1024),
-                      smem_desc(sbase + OFF_MP + 8192 + k * 2048, 8192, 1024), idesc_f16(128, 64, true, true), k > 0);
+                          smem_desc(sbase + OFF_MP + 8192 + k * 2048, 8192, 1024), idesc_f16(128, 64, true, true), k > 0);
+        umma_commit(&bar_mma);
     }
-    commit_wait();
-    // thread (row = d_v, 32 tokens from 32 hf): R^T = V^T - (S X^T) diag(gamma) (fp32 back
-    // into A, packed into RP); dZ^T = dO^T P + (dS K^T) diag(w), packed into ZP
-    {
-        float d1[32], gk[32], bb[32];
-        tmem_ld32(tl + TM_A + 32 * hf, d1);
-        tmem_ld32(tl + TM_G + 32 * hf, gk);
-        tmem_ld32(tl + TM_B + 32 * hf, bb);
-        tmem_ld_wait();
+    // R^T = V^T - (S X^T) diag(gamma) (fp32 back into A, packed into RP) and
+    // dZ^T = dO^T P + (dS K^T) diag(w) (packed into ZP), for this warp's lane quarter, by
+    // the warps the solve's first phases leave idle (4-7)
+    auto form_r_dz = [&]() {
+        if (!mbar_wait(&bar_mma, mma_phase, kWaitNs)) { ok = false; abort_flag = 1; }
+        tc_fence_after();
         const int vp = row >> 6, vc = row & 63;
-        uint32_t rp[16], zp[16];
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+            float d1[32], gk[32], bb[32];
+            tmem_ld32(tl + TM_A + 32 * h2, d1);
+            tmem_ld32(tl + TM_G + 32 * h2, gk);
+            tmem_ld32(tl + TM_B + 32 * h2, bb);
+            tmem_ld_wait();
+            uint32_t rp[16], zp[16];
 #pragma unroll
-        for (int cc = 0; cc < 32; ++cc) {
-            const int t = 32 * hf + cc;
-            const float vv = bf(*reinterpret_cast<const __nv_bfloat16 *>(sm + OFF_V + vp * 8192 + sw128_off(t, vc)));
-            d1[cc] = vv - g_gam[t] * d1[cc];
-            bb[cc] = fmaf(g_w[t], gk[cc], bb[cc]);
-        }
+            for (int cc = 0; cc < 32; ++cc) {
+                const int t = 32 * h2 + cc;
+                const float vv = bf(*reinterpret_cast<const __nv_bfloat16 *>(sm + OFF_V + vp * 8192 + sw128_off(t, vc)));
+                d1[cc] = vv - g_gam[t] * d1[cc];
+                bb[cc] = fmaf(g_w[t], gk[cc], bb[cc]);
+            }
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            rp[j] = pack_half2(d1[2 * j], d1[2 * j + 1]);
-            zp[j] = pack_half2(bb[2 * j], bb[2 * j + 1]);
+            for (int j = 0; j < 16; ++j) {
+                rp[j] = pack_half2(d1[2 * j], d1[2 * j + 1]);
+                zp[j] = pack_half2(bb[2 * j], bb[2 * j + 1]);
+            }
+            tmem_st32(tl + TM_A + 32 * h2, d1);
+            tmem_st16(tl + TM_RP + 16 * h2, rp);
+            tmem_st16(tl + TM_ZP + 16 * h2, zp);
         }
-        tmem_st32(tl + TM_A + 32 * hf, d1);
-        tmem_st16(tl + TM_RP + 16 * hf, rp);
-        tmem_st16(tl + TM_ZP + 16 * hf, zp);
         tmem_st_wait();
-    }
+        tc_fence_before();
+    };
+    // T = (I + beta M)^{-1} (fp16, zero above the diagonal blocks) and T1 = T diag(beta)
+    unit_lower_inverse<false, true>(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_Y),
+                                    sm + OFF_TT, sm + OFF_T1, nullptr, g_beta, form_r_dz,
+                                    []() { __syncthreads(); });
+    mma_phase ^= 1;                                    // the phase warps 4-7 waited on
     sync_mma();
     // Z^T = R^T T1^T, dR^T = dZ^T T (A operands packed in TMEM)
     if (issuer) {
@@ -721,7 +730,8 @@ cudaError_t launch_qdelta_bwd_grad_tc(const QDeltaBwdArgs &a, cudaStream_t s) {
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const int nchunks = (a.T + kC - 1) / kC;
-    GradTcParams p{a.alpha, a.beta, a.lam, a.S_chk, a.dS_chk, a.dq, a.dk, a.dv, a.dalpha, a.dbeta, a.dlam,
+    GradTcParams p{a.alpha, a.beta, a.lam, reinterpret_cast<const uint8_t *>(a.S_chk),
+                   reinterpret_cast<const uint8_t *>(a.dS_chk), a.dq, a.dk, a.dv, a.dalpha, a.dbeta, a.dlam,
                    a.B, a.T, a.H, a.grad_f32, a.gates_f32};
     qdelta_bwd_grad_tc_kernel<<<(unsigned)(a.B * a.H * nchunks), kNT, kSmemBytes, s>>>(p, mq, mk, mv, md);
     return cudaGetLastError();

@@ -586,11 +586,13 @@ cudaError_t launch_qdelta_bwd(const QDeltaBwdArgs &a, int dtype, cudaStream_t s,
     QDeltaArgs f{pro ? a.raw_q : a.q, pro ? a.raw_k : a.k, a.v, pro ? a.raw_a : a.alpha, pro ? a.raw_b : a.beta,
                  pro ? a.raw_l : a.lam, a.S0, nullptr, nullptr, a.B, a.T, a.H, a.nk, a.nv, nullptr, 0, pro ? 1 : 0,
                  a.S_chk};
-    cudaError_t e = qdelta_tc_supported(f, dtype) ? launch_qdelta_chunk_tc(f, s, nlaunch, kTcNoO)
-                                                  : launch_qdelta_chunk_simt(f, dtype, s, nlaunch);
+    //    The checkpoint format follows the backward kernels: fp16 operand tiles for the
+    //    tensor-core ones (whose conditions include the tensor-core forward's), fp32 rows
+    //    for the CUDA-core ones.
+    const bool m = qdelta_bwd_tc_supported(a, dtype);
+    cudaError_t e = m ? launch_qdelta_chunk_tc(f, s, nlaunch, kTcNoO) : launch_qdelta_chunk_simt(f, dtype, s, nlaunch);
     if (e != cudaSuccess) return e;
     // 2. reverse sweep of dS and 3. the per-chunk gradients
-    const bool m = qdelta_bwd_tc_supported(a, dtype);
     e = dtype == kBF16 ? dispatch_bwd<__nv_bfloat16>(a, s, m) : dispatch_bwd<float>(a, s, m);
     if (e == cudaSuccess) *nlaunch += 2;
     return e;

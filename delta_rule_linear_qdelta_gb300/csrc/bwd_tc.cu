@@ -12,7 +12,9 @@
 //   dRs^T = dZ^T T diag(beta gamma)                    (= (diag(gamma beta) T^T dZ)^T)
 //   dS   <- gamma_C dS + dO^T (gamma Q) - dRs^T X
 // and dS as it enters each chunk (the gradient reaching the state that leaves it) is
-// written to the backward's checkpoint array; after the first chunk it is dS0.
+// written to the backward's checkpoint array, as an fp16 tile in the layout of a
+// 128-byte-swizzled MMA operand (chk_tile_off, the format of the forward's state
+// checkpoints); after the first chunk it is dS0 (fp32).
 //
 // The layout follows the forward kernel (chunk_tc.cu): every product has M = 128 with
 // the TMEM lanes indexing d_v; a prep group (warps 0-7) does each chunk's
@@ -76,7 +78,8 @@ constexpr uint32_t TM_G = 0, TM_DZ = 64, TM_DR = 128, TM_SB = 192, TM_S = 256;
 struct BwdTcParams {
     const void *alpha, *beta, *lam;
     const float *dS_final;
-    float *dS_chk, *dS0;
+    uint8_t *dS_chk;                                  // fp16 checkpoint tiles (chk_tile_off)
+    float *dS0;
     int B, T, H;
     int gates_f32;
 };
@@ -419,9 +422,9 @@ qdelta_bwd_dstate_tc_kernel(const BwdTcParams p, const __grid_constant__ CUtenso
                          idesc_bf16(128, 128, false, true), 1);
         umma_commit(&bar_s);
     };
-    // dS of this thread's row -> dst (global, fp32), its bf16 copy into TM_SB, and (unless
-    // last) the master scaled by g
-    auto state_out = [&](float *dst, float g, bool last, bool from_tmem, const float *src) {
+    // dS of this thread's row -> dst32 (an fp32 row) or dst16 (a checkpoint tile, fp16), its
+    // bf16 copy into TM_SB, and (unless last) the master scaled by g
+    auto state_out = [&](float *dst32, uint8_t *dst16, float g, bool last, bool from_tmem, const float *src) {
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
             float sv[64];
@@ -437,10 +440,14 @@ qdelta_bwd_dstate_tc_kernel(const BwdTcParams p, const __grid_constant__ CUtenso
                     sv[j] = v.x; sv[j + 1] = v.y; sv[j + 2] = v.z; sv[j + 3] = v.w;
                 }
             }
-            if (dst && !abort_flag)
+            if (dst32 && !abort_flag)
 #pragma unroll
                 for (int j = 0; j < 64; j += 4)
-                    *reinterpret_cast<float4 *>(dst + 64 * half + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+                    *reinterpret_cast<float4 *>(dst32 + 64 * half + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+            if (dst16 && !abort_flag)
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    *reinterpret_cast<uint4 *>(dst16 + chk_tile_off(d_row, 64 * half + 8 * ch)) = pack8hp(sv + 8 * ch);
             if (!last) {
                 uint32_t sp[32];
 #pragma unroll
@@ -458,8 +465,8 @@ qdelta_bwd_dstate_tc_kernel(const BwdTcParams p, const __grid_constant__ CUtenso
         }
         tmem_st_wait();
     };
-    auto chk_row = [&](int c) {                       // row d_row of the checkpoint of chunk c
-        return p.dS_chk + (((size_t)bh * nchunks + c) * kD + d_row) * kD;
+    auto chk_tile = [&](int c) {                      // the checkpoint tile of chunk c
+        return p.dS_chk + ((size_t)bh * nchunks + c) * kChkTileBytes;
     };
 
     int loads_issued = nchunks > 1 ? 2 : 1;
@@ -502,7 +509,7 @@ qdelta_bwd_dstate_tc_kernel(const BwdTcParams p, const __grid_constant__ CUtenso
         // scaled by that chunk's gamma_C
         {
             const float *src = p.dS_final ? p.dS_final + ((size_t)bh * kD + d_row) * kD : nullptr;
-            state_out(chk_row(nchunks - 1), g_gam[0][kC - 1], false, false, src);
+            state_out(nullptr, chk_tile(nchunks - 1), g_gam[0][kC - 1], false, false, src);
         }
         csync();
         for (int i = 0; i < nchunks; ++i) {
@@ -529,8 +536,9 @@ qdelta_bwd_dstate_tc_kernel(const BwdTcParams p, const __grid_constant__ CUtenso
             }
             // dS entering chunk_of(i) = leaving chunk_of(i) - 1: its checkpoint (dS0 after
             // the first chunk) and the operands of the next index
-            float *dst = last ? (p.dS0 ? p.dS0 + ((size_t)bh * kD + d_row) * kD : nullptr) : chk_row(chunk_of(i) - 1);
-            state_out(dst, last ? 1.f : g_gam[(i + 1) & 3][kC - 1], last, true, nullptr);
+            float *d0 = last && p.dS0 ? p.dS0 + ((size_t)bh * kD + d_row) * kD : nullptr;
+            state_out(d0, last ? nullptr : chk_tile(chunk_of(i) - 1), last ? 1.f : g_gam[(i + 1) & 3][kC - 1], last,
+                      true, nullptr);
             tc_fence_before();
             const bool stop = named_sync_or(kBarChain, kChainThreads, abort_flag != 0);
             tc_fence_after();
@@ -559,7 +567,8 @@ qdelta_bwd_dstate_tc_kernel(const BwdTcParams p, const __grid_constant__ CUtenso
 }  // namespace
 
 bool qdelta_bwd_tc_supported(const QDeltaBwdArgs &a, int dtype) {
-    return dtype == kBF16 && a.nk == kD && a.nv == kD;
+    // the checkpoints come from the tensor-core forward (fp16 tiles): its conditions too
+    return dtype == kBF16 && a.nk == kD && a.nv == kD && a.T > 0 && (long long)a.T * a.H * kD * 2 < (1ll << 40);
 }
 
 cudaError_t launch_qdelta_bwd_dstate_tc(const QDeltaBwdArgs &a, cudaStream_t s) {
@@ -570,7 +579,7 @@ cudaError_t launch_qdelta_bwd_dstate_tc(const QDeltaBwdArgs &a, cudaStream_t s) 
     cudaError_t e = cudaFuncSetAttribute(qdelta_bwd_dstate_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    BwdTcParams p{a.alpha, a.beta, a.lam, a.dS_final, a.dS_chk, a.dS0, a.B, a.T, a.H, a.gates_f32};
+    BwdTcParams p{a.alpha, a.beta, a.lam, a.dS_final, reinterpret_cast<uint8_t *>(a.dS_chk), a.dS0, a.B, a.T, a.H, a.gates_f32};
     qdelta_bwd_dstate_tc_kernel<<<a.B * a.H, kAllThreads, kSmemBytes, s>>>(p, mq, mk, md);
     return cudaGetLastError();
 }

@@ -124,9 +124,11 @@ struct TcParams {
 
 // PRO: q, k, alpha, beta, lambda arrive as projections and logits (the prologue of
 // qdelta_fwd_prologue); a template parameter, so the plain kernel carries none of it.
-// CHK: the fp32 state entering every chunk is written to [B*H][nchunks][dv][dk] (the
-// backward's checkpoints), from the registers that already hold it on its way into
-// TMEM.  That instance runs without output (kTcNoO) and takes the array in p.o.
+// CHK: the state entering every chunk is written to the backward's checkpoint array,
+// from the registers that already hold it on its way into TMEM: per (b*H + h, chunk) a
+// 32 KB fp16 [dv][dk] tile in the layout of a 128-byte-swizzled MMA operand (two
+// 64-column panels of 128 rows, chk_tile_off), which the gradient kernel copies in one
+// piece.  That instance runs without output (kTcNoO) and takes the array in p.o.
 // QED: the chain of the QED forward (chunk_tc_qed.cu) over its derived operands: tmA,
 // tmQ, tmK, tmV map Ae, Qe, Ke, W*V, the X rows are loaded (Ae) instead of formed, every
 // gate is a unit (alpha = 1, beta = 1, lambda = 0: the products above then are QED's
@@ -649,9 +651,10 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                 }
             }
             if (CHK && !last) {
-                float *dst = reinterpret_cast<float *>(p.o) + (((size_t)bh * nchunks + c + 1) * kD + d_row) * kD + 64 * half;
+                uint8_t *dst = reinterpret_cast<uint8_t *>(p.o) + ((size_t)bh * nchunks + c + 1) * kChkTileBytes;
 #pragma unroll
-                for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+                for (int ch = 0; ch < 8; ++ch)
+                    *reinterpret_cast<uint4 *>(dst + chk_tile_off(d_row, 64 * half + 8 * ch)) = pack8hp(sv + 8 * ch);
             }
             if (last && opaque(p.S_final) && !abort_flag) {
                 float *dst = p.S_final + ((size_t)bh * kD + d_row) * kD + 64 * half;
@@ -765,9 +768,10 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
                     for (int j = 0; j < 64; ++j) sv[j] = (64 * half + j == d_row) ? 1.f : 0.f;
                 if (CHK) {
-                    float *dst = reinterpret_cast<float *>(p.o) + ((size_t)bh * nchunks * kD + d_row) * kD + 64 * half;
+                    uint8_t *dst = reinterpret_cast<uint8_t *>(p.o) + (size_t)bh * nchunks * kChkTileBytes;
 #pragma unroll
-                    for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4 *>(dst + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+                    for (int ch = 0; ch < 8; ++ch)
+                        *reinterpret_cast<uint4 *>(dst + chk_tile_off(d_row, 64 * half + 8 * ch)) = pack8hp(sv + 8 * ch);
                 }
                 state_half(half, sv, g0, true);
             }

@@ -50,15 +50,18 @@ struct QDeltaArgs {
     void *ws;
     size_t ws_bytes;
     int prologue;     // q, k, alpha, beta, lam are projections and logits (qdelta_fwd_prologue)
-    float *S_chk;     // if set, the state entering every chunk of 64 tokens,
-                      // [B*H][ceil(T/64)][dv][dk] fp32 (the backward's checkpoints); the
-                      // tensor-core kernel takes it only without the prologue
+    float *S_chk;     // if set, the state entering every chunk of 64 tokens (the backward's
+                      // checkpoints), per (b*H + h, chunk): an [dv][dk] fp32 array from the
+                      // CUDA-core kernel, a 32 KB fp16 operand tile (tc::chk_tile_off) from
+                      // the tensor-core kernel
 };
 
 // Arguments of one Q-Delta backward (layouts as in include/qdelta.h); nk, nv are
-// d_k, d_v.  S_chk and dS_chk are the two checkpoint arrays in the workspace, each
-// [B*H][ceil(T/64)][dv][dk] fp32: the state entering each chunk and the gradient
-// reaching the state leaving it.
+// d_k, d_v.  S_chk and dS_chk are the two checkpoint arrays in the workspace, one entry
+// per (b*H + h, chunk of 64): the state entering each chunk and the gradient reaching
+// the state leaving it -- [dv][dk] fp32 for the CUDA-core kernels, a 32 KB fp16 tile in
+// the 128-byte-swizzled operand layout (tc::chk_tile_off) for the tensor-core ones
+// (qdelta_bwd_tc_supported decides both the format and the forward that writes it).
 struct QDeltaBwdArgs {
     const void *q, *k, *v, *alpha, *beta, *lam;
     const float *S0;

@@ -328,6 +328,15 @@ __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *
     }
 }
 
+// The backward's checkpoints on the tensor-core path: per (b*H + h, chunk) one fp16
+// [128][128] state (or state gradient) tile laid out as a 128-byte-swizzled MMA operand,
+// two 64-column panels of 128 rows, so that it is copied to shared memory in one piece.
+constexpr uint32_t kChkTileBytes = 2 * kD * 128;
+// byte offset of element (row, col) (col a multiple of 8 for a 16-byte group)
+__device__ __forceinline__ uint32_t chk_tile_off(int row, int col) {
+    return (uint32_t)(col >> 6) * (kD * 128) + sw128_off(row, col & 63);
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
