@@ -137,7 +137,8 @@ __device__ __forceinline__ float2 warp_sum64(float (&x)[64]) {
 __global__ void __launch_bounds__(kNT, 1)
 qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensorMap tmQ,
                           const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                          const __grid_constant__ CUtensorMap tmD) {
+                          const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmDQ,
+                          const __grid_constant__ CUtensorMap tmDK, const __grid_constant__ CUtensorMap tmDV) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t bar_ld, bar_mma, bar_drain;
@@ -442,7 +443,7 @@ qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensor
         for (int e = 0; e < 8; ++e) f[e] *= gt;
         *reinterpret_cast<uint4 *>(sm + OFF_RS + pnl * 16384 + 8192 + off) = pack8hp(f);
     }
-    // dV = diag(beta) dR (row = d_v, 32 tokens from 32 hf), and sum_v dR R (dbeta, second term)
+    // sum_v dR R (dbeta, second term; row = d_v, 32 tokens from 32 hf)
     {
         float dr[32], rr[32];
         tmem_ld32(tl + TM_DR + 32 * hf, dr);
@@ -451,11 +452,6 @@ qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensor
         float pr[64];
 #pragma unroll
         for (int cc = 0; cc < 32; ++cc) {
-            const int t = 32 * hf + cc;
-            if (t < n) {
-                const float x = g_beta[t] * dr[cc];        // dv is in the call's dtype (grad_f32 or not)
-                static_cast<__nv_bfloat16 *>(p.dv)[tok_of(t) * kD + row] = __float2bfloat16_rn(x);
-            }
             pr[cc] = dr[cc] * rr[cc];
             pr[32 + cc] = 0.f;
         }
@@ -643,17 +639,45 @@ qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensor
             red[warp][2 * lane] = s2.x;
             red[warp][2 * lane + 1] = s2.y;
         }
-        // dk (hf 0) or dq (hf 1) row t, column j
-        void *dst = hf ? p.dq : p.dk;
-#pragma unroll 8
-        for (int t = 0; t < kC; ++t)
-            if (t < n) {
-                const size_t o = tok_of(t) * kD + j;
-                if (p.grad_f32) static_cast<float *>(dst)[o] = dd[t];
-                else static_cast<__nv_bfloat16 *>(dst)[o] = __float2bfloat16_rn(dd[t]);
-            }
+        // dk (hf 0) or dq (hf 1) column j: fp32 straight to global memory, bf16 into a
+        // [t][dk] tile (Sb's place: dk panels, then dq panels) for the TMA store
+        if (p.grad_f32) {
+            float *dst = static_cast<float *>(hf ? p.dq : p.dk);
+#pragma unroll
+            for (int t = 0; t < kC; ++t)
+                if (t < n) dst[tok_of(t) * kD + j] = dd[t];
+        } else {
+            uint8_t *st = sm + OFF_SB + (hf ? 16384 : 0) + jp * 8192;
+#pragma unroll
+            for (int t = 0; t < kC; ++t)
+                *reinterpret_cast<__nv_bfloat16 *>(st + sw128_off(t, jc)) = __float2bfloat16_rn(dd[t]);
+        }
     }
+    // dV = diag(beta) dR (row = d_v, 32 tokens from 32 hf; always bf16) -> [t][dv] tile in dSb's place
+    {
+        float dr[32];
+        tmem_ld32(tl + TM_DR + 32 * hf, dr);
+        tmem_ld_wait();
+        uint8_t *st = sm + OFF_DSB + (row >> 6) * 8192;
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc) {
+            const int t = 32 * hf + cc;
+            *reinterpret_cast<__nv_bfloat16 *>(st + sw128_off(t, row & 63)) = __float2bfloat16_rn(g_beta[t] * dr[cc]);
+        }
+    }
+    fence_proxy_async();
     __syncthreads();
+    if (issuer && !abort_flag) {                          // rows past T are clipped by the copies
+#pragma unroll
+        for (int pnl = 0; pnl < 2; ++pnl) {
+            tma_store_4d(&tmDV, sm + OFF_DSB + pnl * 8192, 64 * pnl, h, c0, b);
+            if (!p.grad_f32) {
+                tma_store_4d(&tmDK, sm + OFF_SB + pnl * 8192, 64 * pnl, h, c0, b);
+                tma_store_4d(&tmDQ, sm + OFF_SB + 16384 + pnl * 8192, 64 * pnl, h, c0, b);
+            }
+        }
+        tma_store_commit();
+    }
     // gate gradients: dlambda = rowsum(dX * Q); dl = (row sums) - w z (+ the last token's
     // gamma_C <dS, S> + sum w z); d log alpha its suffix sum; dalpha = d log alpha / alpha
     if (warp == 0) {
@@ -713,6 +737,7 @@ qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensor
         }
         if (lane == 0) atomicExch(&g_grad_tc_timeout, 1u);
     }
+    if (issuer) tma_store_wait_all();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 512);
@@ -722,10 +747,17 @@ qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensor
 }  // namespace
 
 cudaError_t launch_qdelta_bwd_grad_tc(const QDeltaBwdArgs &a, cudaStream_t s) {
-    CUtensorMap mq, mk, mv, md;
+    CUtensorMap mq, mk, mv, md, mdq, mdk, mdv;
     if (!make_token_map(&mq, a.q, a.B, a.T, a.H) || !make_token_map(&mk, a.k, a.B, a.T, a.H) ||
-        !make_token_map(&mv, a.v, a.B, a.T, a.H) || !make_token_map(&md, a.dO, a.B, a.T, a.H))
+        !make_token_map(&mv, a.v, a.B, a.T, a.H) || !make_token_map(&md, a.dO, a.B, a.T, a.H) ||
+        !make_token_map(&mdv, a.dv, a.B, a.T, a.H))
         return cudaErrorInvalidValue;
+    if (a.grad_f32) {                                 // dq, dk fp32: written directly, maps unused
+        mdq = mq;
+        mdk = mk;
+    } else if (!make_token_map(&mdq, a.dq, a.B, a.T, a.H) || !make_token_map(&mdk, a.dk, a.B, a.T, a.H)) {
+        return cudaErrorInvalidValue;
+    }
     cudaError_t e = cudaFuncSetAttribute(qdelta_bwd_grad_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -733,7 +765,7 @@ cudaError_t launch_qdelta_bwd_grad_tc(const QDeltaBwdArgs &a, cudaStream_t s) {
     GradTcParams p{a.alpha, a.beta, a.lam, reinterpret_cast<const uint8_t *>(a.S_chk),
                    reinterpret_cast<const uint8_t *>(a.dS_chk), a.dq, a.dk, a.dv, a.dalpha, a.dbeta, a.dlam,
                    a.B, a.T, a.H, a.grad_f32, a.gates_f32};
-    qdelta_bwd_grad_tc_kernel<<<(unsigned)(a.B * a.H * nchunks), kNT, kSmemBytes, s>>>(p, mq, mk, mv, md);
+    qdelta_bwd_grad_tc_kernel<<<(unsigned)(a.B * a.H * nchunks), kNT, kSmemBytes, s>>>(p, mq, mk, mv, md, mdq, mdk, mdv);
     return cudaGetLastError();
 }
 
