@@ -9,59 +9,73 @@
 //   G      = [X; Q] K^T                                   (one M=128 MMA)
 //   A      = strictly_lower(beta_t e^{l_t - l_i} (X K^T)_ti);  P = incl_lower(e^{l_t-l_i} (Q K^T)_ti)
 //   Tinv   = (I + A)^{-1}                                  (fp32, tc_common.cuh)
-//   U^T    = V^T (Tinv diag(beta))^T;   W^T = X^T (Tinv diag(beta gamma))^T
-//   Z^T    = U^T - S W^T                                   (S = state entering the chunk)
+//   U^T    = V^T T1^T,  T1 = Tinv diag(beta);   T2 = Tinv diag(beta gamma)
+//   Z^T    = U^T - (S X^T) T2^T                            (S = state entering the chunk;
+//                                                            (S X^T) T2^T = S W^T, W = T2 X)
 //   o_t    = gamma_t (S Q^T)_t + (Z^T P^T)_t
 //   S     <- gamma_C S + Z^T diag(kappa) K
 // Every product is written "transposed" so that the 128 TMEM lanes index d_v (or
-// d_k) and every MMA has M = 128.  The two output terms share one accumulator O:
-// the MMAs form O = S Q^T + Zt^T Pt^T and the epilogue multiplies token t by gamma_t,
-// with Zt, Pt chosen by the chunk's log-decay l_C:
+// d_k) and every MMA has M = 128.  S [X; Q]^T is one N = 128 product whose halves are
+// S X^T and S Q^T, the first output term.  The two output terms share one accumulator
+// O = S Q^T + Zt^T Pt^T and the epilogue multiplies token t by gamma_t, with Zt, Pt
+// chosen by the chunk's log-decay l_C:
 //   l_C > -30 (fold):  Zt = Z diag(kappa), Pt_ti = e^{-l_C} (Q K^T)_ti   (K used as loaded)
 //   l_C > -80 (split): Zt = Z, Pt_ti = e^{-l_i} (Q K^T)_ti, K scaled in place to kappa K
-//   otherwise:         Zt = Z, Pt = P, kappa K in place, Q scaled in place to gamma Q after
-//                      the Gram and no gamma_t in the epilogue (no factor can overflow)
+//   otherwise:         Zt = Z, Pt = P, kappa K in place, S Q^T scaled by gamma in TMEM
+//                      before Zt^T Pt^T accumulates onto it, and no gamma_t in the
+//                      epilogue (no factor can overflow)
 // since (Z^T diag(kappa)) (P diag(1/kappa))^T = Z^T P^T and P_ti / gamma_t = e^{-l_i} (Q K^T)_ti.
 // The master state stays in TMEM in fp32 (the MMA accumulates Zt^T (kappa) K onto it
-// after the epilogue has scaled it by the chunk's gamma_C).  Its bf16 copy, and the
-// bf16 Zt^T, also live in TMEM and are the A operands of the state-dependent
-// products, so those MMAs read only their B operand from shared memory.
+// after the epilogue has scaled it by the chunk's gamma_C).  Its bf16 copy, the bf16
+// -(S X^T) and the bf16 Zt^T also live in TMEM and are the A operands of the
+// state-dependent products, so those MMAs read only their B operand from shared memory.
 //
 // Warp specialisation: a prep group (warps 0-7) does the state-independent work of
-// each chunk -- X, its Gram, the decay masks, the solve, U and W -- and hands the
-// chunk to a chain group (warps 8-11) that carries the state: Z and O, Zt^T, the
-// output and state products, the epilogue.  The two groups run concurrently, so the
-// chunk period is the longer of the two instead of their sum.  Each group
-// synchronises on its own named barrier; hand-offs are mbarriers:
-//   ready       prep -> chain: P(c) and the gates are in place, U/W(c) issued (the chain
-//               waits on their commit, then writes -W^T itself)
-//   wfree       chain -> prep: W(c) has been read out of TMEM, so U/W(c+1) may be issued
-//   cdone[c&1]  chain -> prep: the output and state products of chunk c have run, so
-//               P[c&1], U[c&1] and chunk c's stage are free
-// The chain group also issues the TMA loads of chunk c+2 into chunk c's stage.
+// each chunk -- the decay masks, the solve, U, and X and the Gram of the next chunk --
+// and hands the chunk to a chain group (warps 8-11) that carries the state: S [X; Q]^T,
+// Z, the coupling, Zt^T, the output and state products, the epilogue.  The two groups
+// run concurrently, so the chunk period is the longer of the two instead of their sum.
+// Each group synchronises on its own named barrier; hand-offs are mbarriers:
+//   ready       prep -> chain: P(c), T2(c), the gates of chunk c+1 and X(c+1) in place
+//   taken       chain -> prep: the chain has passed `ready` and `uw` of chunk c, so U(c+1)
+//               may be issued and `ready` completed for chunk c+1 (the prep may run up to
+//               two chunks ahead and must not complete a phase twice before the chain
+//               has waited on the first)
+//   cdone[c&1]  chain -> prep: the products of chunk c have run, so P, U, T2 and M21
+//               of parity c&1 are free
+// Inside the prep group three threads issue at once after the solve: the hand-off, U(c)
+// and the Gram of chunk c+1; warps 4-7, idle in the solve's first phases, form X of
+// chunk c+1 meanwhile.  The chain issues S [X; Q]^T of chunk c as soon as the state of
+// chunk c-1 is final, before the chunk is handed over.
+// Loads: K sits in a three-slot ring, X/Q and V in two stages by chunk parity, so the
+// tiles of chunk c+2 go out while chunk c is still running -- K while the chain waits for
+// `ready` (its slot held chunk c-1's K and then that chunk's o tile, once the o store has
+// read it), Q and V as soon as S [X; Q]^T and U of chunk c have run -- and arrive in time
+// for X of chunk c+2 to be formed during the solve of chunk c+1.
 //
 // Instruction economy on both groups (they share each SM sub-partition's issue slots):
 // the output accumulator leaves TMEM in the 16x256b shape, so a thread holds two
 // adjacent tokens of a d_v row and the o tile is written as transposed 16-byte
 // stmatrix rows; elementwise scalings (state rescale, Zt packing, masks, X = K + lambda Q)
-// use packed f32x2 arithmetic; -W is packed first and its bf16 sign bits flipped.
+// use packed f32x2 arithmetic; -(S X^T) is packed first and its bf16 sign bits flipped.
 //
 // Shared memory (offsets from a 1024-aligned base):
-//   stage s in {0,1}: XQ 32 KB (per 64-column panel: X rows 0-63 | Q rows 64-127),
-//                     K 16 KB (scaled in place to kappa*K under strong decay), V 16 KB
+//   stage s in {0,1}: XQ 32 KB (per 64-column panel: X rows 0-63 | Q rows 64-127), V 16 KB
+//   K ring 3x16 KB   K of chunk c in slot c%3 (scaled in place to kappa*K under strong
+//                    decay), then o(c) [64][dv] bf16 for the TMA store
 //   R1   17 KB   A fp32 [64][68], overwritten by the solve's intermediate blocks
-//   R2   16 KB   -W^T(c) [dk][64] (chain group only)
 //   P    2x8 KB  bf16 Pt [64][64], by chunk parity
-//   T    16 KB   Tinv*beta, Tinv*beta*gamma (bf16 [64][64] each), written block by
-//                block by the solve; zero above the 8x8 diagonal blocks
+//   T1   8 KB    Tinv*beta (bf16 [64][64]); T2 2x8 KB Tinv*beta*gamma by chunk parity;
+//                written block by block by the solve, zero above the 8x8 diagonal blocks
 //   Y    4.5 KB  fp32 scratch of the solve (prep group only)
-//   O    16 KB   o(c) [64][dv] bf16 for the TMA store (chain group only)
 //   M21  2x2 KB  -M21 (diag(1/kappa)) bf16 [32][32] without swizzle, by chunk parity
+//   ECG  512 B   QED: the chunk's e^{G_C}
 // All shared-memory MMA operands use the 128-byte swizzle (TMA layout): 128-byte
 // rows, 8-row groups 1024 bytes apart, 64-column panels.
-// TMEM (512 columns): G 0-63, W 64-127, U[0] 128-191, U[1] 192-255 (Z^T accumulates
-// there; its first 32 columns then hold the packed bf16 Zt^T), O 256-319, packed
-// bf16 state 320-383, fp32 state 384-511.
+// TMEM (512 columns): G 0-63, U[0] 64-127, U[1] 128-191 (Z^T accumulates there; its
+// first 32 columns then hold the packed bf16 Zt^T), SK 192-255 and O 256-319 (the two
+// halves of S [X; Q]^T; SK's first 32 columns then hold -(S X^T) packed), packed bf16
+// state 320-383, fp32 state 384-511.
 //
 // Every wait is bounded; on a timeout the kernel sets the library's error word,
 // waits (bounded) for its own copies and MMAs, frees TMEM and returns.
@@ -85,19 +99,19 @@ using namespace tc;
 constexpr int kPrepThreads = kThreads;              // warps 0-7
 constexpr int kChainThreads = 128;                  // warps 8-11
 constexpr int kAllThreads = kPrepThreads + kChainThreads;
-constexpr int kBarPrep = 1, kBarChain = 2;          // named barrier ids (8-13: inside the solve)
-constexpr uint32_t kStageBytes = 65536;
-constexpr uint32_t OFF_XQ = 0, OFF_K = 32768, OFF_V = 49152;
-constexpr uint32_t OFF_R1 = 2 * kStageBytes;         // 131072
-constexpr uint32_t OFF_R2 = OFF_R1 + 17408;          // 148480
-constexpr uint32_t OFF_P = OFF_R2 + 16384;           // 164864 (two 8 KB buffers)
-constexpr uint32_t OFF_T = OFF_P + 16384;           // 181248 (Tinv*beta, Tinv*beta*gamma bf16)
-constexpr uint32_t OFF_Y = OFF_T + 16384;           // 197632 (solve scratch, 32 x LY fp32)
-constexpr uint32_t OFF_O = 203776;                   // o tile [64][dv] bf16 for the TMA store
-constexpr uint32_t OFF_M21 = OFF_O + 16384;          // 220160 (two 2 KB coupling tiles)
-constexpr uint32_t kSmemUsed = OFF_M21 + 4096;       // 224256
-static_assert(OFF_O % 1024 == 0 && OFF_O >= OFF_Y + 32 * LY * 4 && OFF_M21 % 1024 == 0, "tile placement");
-static_assert(OFF_R2 % 1024 == 0 && OFF_P % 1024 == 0 && OFF_T % 1024 == 0 && kSmemUsed + 1024 <= 232448,
+constexpr int kBarPrep = 1, kBarChain = 2, kBarX = 3;   // named barrier ids (8-13: inside the solve)
+constexpr uint32_t kStageBytes = 49152;              // XQ 32 KB + V 16 KB, by chunk parity
+constexpr uint32_t OFF_XQ = 0, OFF_V = 32768;
+constexpr uint32_t OFF_KR = 2 * kStageBytes;         // 98304: K ring, three 16 KB slots
+constexpr uint32_t OFF_R1 = OFF_KR + 3 * 16384;      // 147456
+constexpr uint32_t OFF_P = OFF_R1 + 17408;           // 164864 (two 8 KB buffers)
+constexpr uint32_t OFF_T = OFF_P + 16384;            // 181248 (T1, then T2 by parity; bf16)
+constexpr uint32_t OFF_Y = OFF_T + 24576;            // 205824 (solve scratch, 32 x LY fp32)
+constexpr uint32_t OFF_M21 = 210944;                 // two 2 KB coupling tiles
+constexpr uint32_t OFF_ECG = OFF_M21 + 4096;         // 215040 (QED: e^{G_C} of the chunk, 128 fp32)
+constexpr uint32_t kSmemUsed = OFF_ECG + 512;        // 215552
+static_assert(OFF_M21 >= OFF_Y + 32 * LY * 4 && OFF_M21 % 1024 == 0, "tile placement");
+static_assert(OFF_KR % 1024 == 0 && OFF_P % 1024 == 0 && OFF_T % 1024 == 0 && kSmemUsed + 1024 <= 232448,
               "128-byte-swizzled MMA operands start on 1024-byte boundaries");
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;    // + alignment slack
 constexpr uint32_t kTmaBytes = 3 * kC * kD * 2;      // Q, K, V tiles per chunk
@@ -110,7 +124,7 @@ constexpr float kFoldLog = -30.f;
 // one by one and Q carries gamma instead
 constexpr float kSplitLog = -80.f;
 
-constexpr uint32_t TM_G = 0, TM_W = 64, TM_U = 128, TM_O = 256, TM_SB = 320, TM_S = 384;
+constexpr uint32_t TM_G = 0, TM_U = 64, TM_SK = 192, TM_O = 256, TM_SB = 320, TM_S = 384;
 
 struct TcParams {
     const __nv_bfloat16 *alpha, *beta, *lam;
@@ -132,7 +146,7 @@ struct TcParams {
 // QED: the chain of the QED forward (chunk_tc_qed.cu) over its derived operands: tmA,
 // tmQ, tmK, tmV map Ae, Qe, Ke, W*V, the X rows are loaded (Ae) instead of formed, every
 // gate is a unit (alpha = 1, beta = 1, lambda = 0: the products above then are QED's
-// Gram, masks, solve, U, W, Z, O and S + Z^T Ke), and the epilogue multiplies the state
+// Gram, masks, solve, U, S [A; Q]^T, Z, O and S + Z^T Ke), and the epilogue multiplies the state
 // by the chunk's e^{G_C} per channel (column of the [dv][dk] state).
 template <bool PRO, bool CHK = false, bool QED = false>
 __global__ void __launch_bounds__(kAllThreads, 1)
@@ -141,8 +155,8 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmO, const __grid_constant__ CUtensorMap tmA) {
     extern __shared__ uint8_t smraw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
-    __shared__ uint64_t bar_full[2], bar_g, bar_uw, bar_z, bar_cp, bar_o2, bar_ready, bar_wfree, bar_cdone[2],
-        bar_drain[2];
+    __shared__ uint64_t bar_full[2], bar_g, bar_uw, bar_z, bar_zz, bar_cp, bar_o2, bar_ready, bar_taken, bar_cdone[2],
+        bar_drain[3];
     __shared__ uint32_t tmem_base;
     __shared__ int abort_flag;
     // per-chunk gate arrays, by chunk index mod 4: while the prep group builds chunk
@@ -160,7 +174,9 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
     const int T = p.T, H = p.H;
     const int nchunks = (T + kC - 1) / kC;
-    const bool p_issuer = (tid == 32), c_issuer = (tid == kPrepThreads);
+    // MMA issuers: U and the prep's hand-off (p), the next chunk's Gram (g, in parallel with
+    // U), the chain's products (c)
+    const bool p_issuer = (tid == 32), g_issuer = (tid == 64), c_issuer = (tid == kPrepThreads);
     const int d_row = 32 * q4 + lane;                  // this thread's TMEM lane / state row
     // flags of the segment-scan passes; read through opaque() where they are tested
     // inside the chunk loops (see tc_common.cuh)
@@ -179,11 +195,13 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         mbar_init(&bar_cp, 1);
         mbar_init(&bar_o2, 1);
         mbar_init(&bar_ready, 1);
-        mbar_init(&bar_wfree, 1);
+        mbar_init(&bar_taken, 1);
+        mbar_init(&bar_zz, 1);
         mbar_init(&bar_cdone[0], 1);
         mbar_init(&bar_cdone[1], 1);
         mbar_init(&bar_drain[0], 1);
         mbar_init(&bar_drain[1], 1);
+        mbar_init(&bar_drain[2], 1);
         abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmQ);
@@ -196,22 +214,33 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         tmem_alloc(&tmem_base, 512);
         tmem_relinquish();
     }
-    for (int i = tid; i < 16384 / 16; i += kAllThreads)   // T: zeros above the diagonal blocks
+    for (int i = tid; i < 24576 / 16; i += kAllThreads)   // T1, T2: zeros above the diagonal blocks
         reinterpret_cast<uint4 *>(sm + OFF_T)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async();                                  // ... as the tensor core will read them
 
-    auto issue_loads = [&](int c) {
+    // the tiles of chunk c on bar_full[c&1], in two parts: K into its slot (arming the
+    // barrier with the whole chunk's bytes), then Q (QED: and A) and V into the stage
+    auto issue_k = [&](int c) {
+        const int s = c & 1;
+        uint8_t *kb = sm + OFF_KR + (uint32_t)(c % 3) * 16384;
+        mbar_arrive_expect_tx(&bar_full[s], (no_v() ? kTmaBytes / 3 * 2 : kTmaBytes) + (QED ? kTmaBytes / 3 : 0));
+#pragma unroll
+        for (int pnl = 0; pnl < 2; ++pnl) tma_load_4d(kb + pnl * 8192, &tmK, &bar_full[s], 64 * pnl, h, c * kC, b);
+    };
+    auto issue_xqv = [&](int c) {
         const int s = c & 1;
         uint8_t *st = sm + s * kStageBytes;
         const int t0 = c * kC;
-        mbar_arrive_expect_tx(&bar_full[s], (no_v() ? kTmaBytes / 3 * 2 : kTmaBytes) + (QED ? kTmaBytes / 3 : 0));
 #pragma unroll
         for (int pnl = 0; pnl < 2; ++pnl) {
             if (QED) tma_load_4d(st + OFF_XQ + pnl * 16384, &tmA, &bar_full[s], 64 * pnl, h, t0, b);
             tma_load_4d(st + OFF_XQ + pnl * 16384 + 8192, &tmQ, &bar_full[s], 64 * pnl, h, t0, b);
-            tma_load_4d(st + OFF_K + pnl * 8192, &tmK, &bar_full[s], 64 * pnl, h, t0, b);
             if (!no_v()) tma_load_4d(st + OFF_V + pnl * 8192, &tmV, &bar_full[s], 64 * pnl, h, t0, b);
         }
+    };
+    auto issue_loads = [&](int c) {
+        issue_k(c);
+        issue_xqv(c);
     };
     // gates of a chunk: lane l of warp 4 holds tokens 2l and 2l+1.  The loads land in raw
     // bf16 registers that nothing reads until compute_gates, so they do not stall the warp.
@@ -312,95 +341,102 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         tc_fence_after();
     };
     const uint32_t sbase = smem_u32(sm);
-    const uint32_t sT = sbase + OFF_T, sR2 = sbase + OFF_R2;
+    const uint32_t sT = sbase + OFF_T;
     auto stage_addr = [&](int c) { return sbase + (uint32_t)(c & 1) * kStageBytes; };
+    auto kring = [&](int c) { return OFF_KR + (uint32_t)(c % 3) * 16384; };   // chunk c's K slot
 
     // ---------------------------------------------------------------- prep group
-    // X = K + lambda Q into rows 0-63 of the XQ panels of chunk c's stage.  From
-    // projections (prologue), K and Q first become SiLU(x)/|SiLU(x)| in place: the
-    // 16-byte chunks r = 0, 2 of a thread are token row tid/8 of both 64-column panels,
-    // r = 1, 3 row 32 + tid/8, and the eight threads of a row sum its squares by shuffles.
+    // X = K + lambda Q into rows 0-63 of the XQ panels of chunk c's stage, by warps 4-7
+    // (during the solve of the chunk before).  From projections (prologue), K and Q first
+    // become SiLU(x)/|SiLU(x)| in place.  Thread x = tid - 128 takes, in each of two rounds
+    // h2, the 16-byte chunks i = 0..3: panel i / 2, token row x/8 + 16 (2 h2 + i % 2); the
+    // eight threads of a row sum its squares by shuffles.
     auto x_pass = [&](int c) {
         uint8_t *st = sm + (c & 1) * kStageBytes;
+        uint8_t *kb = sm + kring(c);
         const float *lam = g_lam[c & 3];
-        uint4 kr[4], qr[4];
-        float lm[4];
+        const int xt = tid - 128;
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+            auto chunk_of_i = [&](int i) { return xt + 128 * (2 * h2 + (i & 1) + 4 * (i >> 1)); };
+            uint4 kr[4], qr[4];
+            float lm[4];
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {                     // all loads first
-            const int u = tid + kPrepThreads * r;         // 16-byte chunk index, 0..1023
-            const int pnl = u >> 9;
-            const uint32_t off = (uint32_t)(u & 511) << 4;
-            kr[r] = *reinterpret_cast<const uint4 *>(st + OFF_K + pnl * 8192 + off);
-            qr[r] = *reinterpret_cast<const uint4 *>(st + OFF_XQ + pnl * 16384 + 8192 + off);
-            lm[r] = lam[off >> 7];
-        }
-        if (prologue) {
-            float kf[4][8], qf[4][8], sk[2] = {0.f, 0.f}, sq[2] = {0.f, 0.f};
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                unpack8(kr[r], kf[r]);
-                unpack8(qr[r], qf[r]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    kf[r][e] = silu_fast(kf[r][e]);
-                    qf[r][e] = silu_fast(qf[r][e]);
-                    sk[r & 1] = fmaf(kf[r][e], kf[r][e], sk[r & 1]);
-                    sq[r & 1] = fmaf(qf[r][e], qf[r][e], sq[r & 1]);
-                }
-            }
-#pragma unroll
-            for (int off = 1; off < 8; off <<= 1)
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    sk[i] += __shfl_xor_sync(0xffffffffu, sk[i], off);
-                    sq[i] += __shfl_xor_sync(0xffffffffu, sq[i], off);
-                }
-            float ik[2], iq[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {                 // zero rows (past T) stay zero
-                ik[i] = sk[i] > 0.f ? rsqrtf(sk[i]) : 1.f;
-                iq[i] = sq[i] > 0.f ? rsqrtf(sq[i]) : 1.f;
-            }
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int u = tid + kPrepThreads * r;
+            for (int r = 0; r < 4; ++r) {                 // all loads first
+                const int u = chunk_of_i(r);              // 16-byte chunk index, 0..1023
                 const int pnl = u >> 9;
                 const uint32_t off = (uint32_t)(u & 511) << 4;
-                float xf[8];
+                kr[r] = *reinterpret_cast<const uint4 *>(kb + pnl * 8192 + off);
+                qr[r] = *reinterpret_cast<const uint4 *>(st + OFF_XQ + pnl * 16384 + 8192 + off);
+                lm[r] = lam[off >> 7];
+            }
+            if (prologue) {
+                float kf[4][8], qf[4][8], sk[2] = {0.f, 0.f}, sq[2] = {0.f, 0.f};
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    kf[r][e] *= ik[r & 1];
-                    qf[r][e] *= iq[r & 1];
-                    xf[e] = fmaf(lm[r], qf[r][e], kf[r][e]);
+                for (int r = 0; r < 4; ++r) {
+                    unpack8(kr[r], kf[r]);
+                    unpack8(qr[r], qf[r]);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        kf[r][e] = silu_fast(kf[r][e]);
+                        qf[r][e] = silu_fast(qf[r][e]);
+                        sk[r & 1] = fmaf(kf[r][e], kf[r][e], sk[r & 1]);
+                        sq[r & 1] = fmaf(qf[r][e], qf[r][e], sq[r & 1]);
+                    }
                 }
-                *reinterpret_cast<uint4 *>(st + OFF_K + pnl * 8192 + off) = pack8(kf[r]);
-                *reinterpret_cast<uint4 *>(st + OFF_XQ + pnl * 16384 + 8192 + off) = pack8(qf[r]);
+#pragma unroll
+                for (int off = 1; off < 8; off <<= 1)
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        sk[i] += __shfl_xor_sync(0xffffffffu, sk[i], off);
+                        sq[i] += __shfl_xor_sync(0xffffffffu, sq[i], off);
+                    }
+                float ik[2], iq[2];
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {             // zero rows (past T) stay zero
+                    ik[i] = sk[i] > 0.f ? rsqrtf(sk[i]) : 1.f;
+                    iq[i] = sq[i] > 0.f ? rsqrtf(sq[i]) : 1.f;
+                }
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int u = chunk_of_i(r);
+                    const int pnl = u >> 9;
+                    const uint32_t off = (uint32_t)(u & 511) << 4;
+                    float xf[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        kf[r][e] *= ik[r & 1];
+                        qf[r][e] *= iq[r & 1];
+                        xf[e] = fmaf(lm[r], qf[r][e], kf[r][e]);
+                    }
+                    *reinterpret_cast<uint4 *>(kb + pnl * 8192 + off) = pack8(kf[r]);
+                    *reinterpret_cast<uint4 *>(st + OFF_XQ + pnl * 16384 + 8192 + off) = pack8(qf[r]);
+                    *reinterpret_cast<uint4 *>(st + OFF_XQ + pnl * 16384 + off) = pack8(xf);
+                }
+                continue;
+            }
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int u = chunk_of_i(r);
+                const int pnl = u >> 9;
+                const uint32_t off = (uint32_t)(u & 511) << 4;
+                float kf[8], qf[8], xf[8];
+                unpack8(kr[r], kf);
+                unpack8(qr[r], qf);
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    const float2 x = ffma2(make_float2(lm[r], lm[r]), make_float2(qf[e], qf[e + 1]),
+                                           make_float2(kf[e], kf[e + 1]));
+                    xf[e] = x.x;
+                    xf[e + 1] = x.y;
+                }
                 *reinterpret_cast<uint4 *>(st + OFF_XQ + pnl * 16384 + off) = pack8(xf);
             }
-            return;
-        }
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            const int u = tid + kPrepThreads * r;
-            const int pnl = u >> 9;
-            const uint32_t off = (uint32_t)(u & 511) << 4;
-            float kf[8], qf[8], xf[8];
-            unpack8(kr[r], kf);
-            unpack8(qr[r], qf);
-#pragma unroll
-            for (int e = 0; e < 8; e += 2) {
-                const float2 x = ffma2(make_float2(lm[r], lm[r]), make_float2(qf[e], qf[e + 1]),
-                                       make_float2(kf[e], kf[e + 1]));
-                xf[e] = x.x;
-                xf[e + 1] = x.y;
-            }
-            *reinterpret_cast<uint4 *>(st + OFF_XQ + pnl * 16384 + off) = pack8(xf);
         }
     };
     // G = [X; Q] K^T
     auto issue_gram = [&](int c) {
-        if (!p_issuer) return;
-        const uint32_t sXQ = stage_addr(c) + OFF_XQ, sK = stage_addr(c) + OFF_K;
+        const uint32_t sXQ = stage_addr(c) + OFF_XQ, sK = sbase + kring(c);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
@@ -461,69 +497,91 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             for (int ch = 0; ch < 4; ++ch)
                 *reinterpret_cast<uint4 *>(P + sw128_off(t, 32 * hf + 8 * ch)) = pack8p(g + 8 * ch);
         }
-        if (!split) {                                 // Q -> gamma Q (the Gram has read Q)
-            uint8_t *st = sm + (c & 1) * kStageBytes;
-#pragma unroll 1
-            for (int r4 = 0; r4 < 4; ++r4) {
-                const int u = tid + kPrepThreads * r4;    // 16-byte chunk of the two Q panels
-                const uint32_t off = (uint32_t)(u & 511) << 4;
-                uint8_t *qp = st + OFF_XQ + (u >> 9) * 16384 + 8192 + off;
-                const float gq = gam[off >> 7];
-                float qf[8];
-                unpack8(*reinterpret_cast<const uint4 *>(qp), qf);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) qf[e] *= gq;
-                *reinterpret_cast<uint4 *>(qp) = pack8(qf);
-            }
-        }
     };
-    // the two 32-token halves' inverses diag(T11, T22) -> Tinv*beta, Tinv*beta*gamma into T,
-    // and the coupling -M21 (times 1/kappa in fold mode) into M21[c&1] (R1 and Y as scratch);
-    // warp 4 meanwhile turns the next chunk's raw gates into arrays
+    // the two 32-token halves' inverses diag(T11, T22) -> Tinv*beta into T1, Tinv*beta*gamma
+    // into T2[c&1], and the coupling -M21 (times 1/kappa in fold mode) into M21[c&1] (R1 and Y
+    // as scratch); warps 4-7, idle in the solve's first phases, meanwhile turn the next
+    // chunk's raw gates into arrays (warp 4) and form its X
+    auto next_x = [&](int c) {
+        if (c + 1 >= nchunks) return;
+        if (warp == 4) compute_gates(c + 1);
+        if (QED) return;                                  // QED: the X rows (Ae) are loaded
+        named_sync(kBarX, 128);                           // lambda of chunk c+1 in place
+        wait_on(&bar_full[(c + 1) & 1], (uint32_t)(((c + 1) >> 1) & 1));
+        x_pass(c + 1);
+        fence_proxy_async();                              // X before the Gram reads it
+    };
     auto solve = [&](int c) {
         const int gi = c & 3;
         const bool fold = g_ell[gi][kC - 1] > kFoldLog;
         unit_lower_inverse<true>(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_Y),
-                                 sm + OFF_T, sm + OFF_T + 8192, g_beta[gi], g_gam[gi],
-                                 [&]() { if (warp == 4 && c + 1 < nchunks) compute_gates(c + 1); },
+                                 sm + OFF_T, sm + OFF_T + 8192 + (c & 1) * 8192, g_beta[gi], g_gam[gi],
+                                 [&]() { next_x(c); },
                                  []() { named_sync(kBarPrep, kPrepThreads); },
                                  sm + OFF_M21 + (c & 1) * 2048, fold ? g_gam[gi] : nullptr, g_igam[gi][kC - 1]);
     };
-    // U^T = V^T T1^T into U[c&1], W^T = X^T T2^T
-    auto issue_uw = [&](int c) {
+    // U^T = V^T T1^T into U[c&1] (bar_uw completes even without V)
+    auto issue_u = [&](int c) {
         if (!p_issuer) return;
-        const uint32_t sXQ = stage_addr(c) + OFF_XQ, sV = stage_addr(c) + OFF_V;
+        const uint32_t sV = stage_addr(c) + OFF_V;
         const uint32_t tu = tm + TM_U + 64 * (uint32_t)(c & 1);
         if (!no_v())
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 umma_bf16(tu, smem_desc(sV + k * 2048, 8192, 1024), smem_desc(sT + k * 32, 16, 1024),
                           idesc_bf16(128, 64, true, false), k > 0);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            umma_bf16(tm + TM_W, smem_desc(sXQ + k * 2048, 16384, 1024), smem_desc(sT + 8192 + k * 32, 16, 1024),
-                      idesc_bf16(128, 64, true, false), k > 0);
         umma_commit(&bar_uw);
     };
 
     // --------------------------------------------------------------- chain group
     // each chain thread owns TMEM lane d_row (a d_v row) and all of its columns
-    // -W -> R2 as W^T [dk][64 tokens] (the MN-major B operand of Z); the TMEM lane is the dk index
-    auto w_store = [&]() {
-        float w[64];
-        tmem_ld32(tl + TM_W, *reinterpret_cast<float(*)[32]>(w));
-        tmem_ld32(tl + TM_W + 32, *reinterpret_cast<float(*)[32]>(w + 32));
-        tmem_ld_wait();
+    // [S X^T | S Q^T] = S [X; Q]^T into SK | O (A = the bf16 state in TMEM, B = the XQ panels)
+    auto issue_skq = [&](int c) {
+        if (!c_issuer) return;
+        wait_on(&bar_full[c & 1], (uint32_t)((c >> 1) & 1));
+        const uint32_t sXQ = stage_addr(c) + OFF_XQ;
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {                  // -W: the bf16 sign bits flipped after packing
-            uint4 u = pack8p(w + 8 * ch);
-            u.x ^= 0x80008000u; u.y ^= 0x80008000u; u.z ^= 0x80008000u; u.w ^= 0x80008000u;
-            *reinterpret_cast<uint4 *>(sm + OFF_R2 + sw128_off(d_row, 8 * ch)) = u;
+        for (int k = 0; k < 8; ++k) {
+            const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
+            umma_bf16_ta(tm + TM_SK, tm + TM_SB + 8 * k, smem_desc(sXQ + ko, 16, 1024),
+                         idesc_bf16(128, 128, false, false), k > 0);
         }
+        umma_commit(&bar_z);
     };
-    // K -> kappa K in place in chunk c's stage (the operand of the state product)
+    // -(S X^T) as packed bf16 pairs into SK's first 32 columns (the A operand of Z)
+    auto sx_pack = [&]() {
+        float x[64];
+        tmem_ld32(tl + TM_SK, *reinterpret_cast<float(*)[32]>(x));
+        tmem_ld32(tl + TM_SK + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+        tmem_ld_wait();
+        uint32_t xp[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) xp[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]) ^ 0x80008000u;
+        tmem_st32(tl + TM_SK, xp);
+        tmem_st_wait();
+    };
+    // strong decay: S Q^T <- (S Q^T) diag(gamma) in TMEM (gamma_t may underflow, the output
+    // then takes no gamma), before Zt^T Pt^T accumulates onto it
+    auto o_gamma = [&](int c) {
+        const float *gam = g_gam[c & 3];
+#pragma unroll 1
+        for (int h2 = 0; h2 < 2; ++h2) {
+            float y[32];
+            tmem_ld32(tl + TM_O + 32 * h2, y);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                const float2 v = fmul2(make_float2(y[j], y[j + 1]), *reinterpret_cast<const float2 *>(gam + 32 * h2 + j));
+                y[j] = v.x;
+                y[j + 1] = v.y;
+            }
+            tmem_st32(tl + TM_O + 32 * h2, y);
+        }
+        tmem_st_wait();
+    };
+    // K -> kappa K in place in chunk c's K slot (the operand of the state product)
     auto kappa_k = [&](int c) {
-        uint8_t *st = sm + (c & 1) * kStageBytes;
+        uint8_t *st = sm + kring(c);
         const float *kap = g_kap[c & 3];
         const int ct = tid - kPrepThreads;
         uint4 kr[8];
@@ -531,7 +589,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
         for (int r = 0; r < 8; ++r) {                     // all loads first
             const uint32_t off = (uint32_t)(ct + kChainThreads * r) << 4;   // both K panels
-            kr[r] = *reinterpret_cast<const uint4 *>(st + OFF_K + off);
+            kr[r] = *reinterpret_cast<const uint4 *>(st + off);
             ka[r] = kap[(off & 8191) >> 7];
         }
 #pragma unroll
@@ -541,26 +599,19 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             unpack8(kr[r], kf);
 #pragma unroll
             for (int e = 0; e < 8; ++e) kf[e] *= ka[r];
-            *reinterpret_cast<uint4 *>(st + OFF_K + off) = pack8(kf);
+            *reinterpret_cast<uint4 *>(st + off) = pack8(kf);
         }
     };
-    // Z^T = U^T - S W^T (accumulated into U[c&1]), then O = S Q^T; A = the bf16 state in TMEM
-    auto issue_z_o = [&](int c) {
+    // Z^T = U^T - (S X^T) T2^T = U^T - S W^T, accumulated into U[c&1] (A = -(S X^T) packed in TMEM)
+    auto issue_z = [&](int c) {
         if (!c_issuer) return;
-        const uint32_t sXQ = stage_addr(c) + OFF_XQ;
         const uint32_t tu = tm + TM_U + 64 * (uint32_t)(c & 1);
+        const uint32_t sT2 = sT + 8192 + (uint32_t)(c & 1) * 8192;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-            umma_bf16_ta(tu, tm + TM_SB + 8 * k, smem_desc(sR2 + k * 2048, 8192, 1024),
-                         idesc_bf16(128, 64, false, true), (no_v() && k == 0) ? 0u : 1u);
-        umma_commit(&bar_z);
-        if (!no_o())
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
-                umma_bf16_ta(tm + TM_O, tm + TM_SB + 8 * k, smem_desc(sXQ + ko + 8192, 16, 1024),
-                             idesc_bf16(128, 64, false, false), k > 0);
-            }
+        for (int k = 0; k < 4; ++k)
+            umma_bf16_ta(tu, tm + TM_SK + 8 * k, smem_desc(sT2 + k * 32, 16, 1024), idesc_bf16(128, 64, false, false),
+                         (no_v() && k == 0) ? 0u : 1u);
+        umma_commit(&bar_zz);
     };
     // 32 tokens of Z^T (fp32, columns 32 hf.. of U[c&1]) -> Zt^T as packed bf16 pairs into
     // columns 16 hf.. of U[c&1]; in fold mode Zt^T = Z^T diag(kappa)
@@ -596,7 +647,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     // O += Zt^T Pt^T ; S += Zt^T (kappa K)  (S in TMEM already scaled by gamma_C); A = Zt^T in TMEM
     auto issue_mma2 = [&](int c) {
         if (!c_issuer) return;
-        const uint32_t sK = stage_addr(c) + OFF_K, sP = sbase + OFF_P + (uint32_t)(c & 1) * 8192;
+        const uint32_t sK = sbase + kring(c), sP = sbase + OFF_P + (uint32_t)(c & 1) * 8192;
         const uint32_t tz = tm + TM_U + 64 * (uint32_t)(c & 1);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -640,8 +691,8 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             tmem_ld32(tl + TM_S + 64 * half, *reinterpret_cast<float(*)[32]>(sv));
             tmem_ld32(tl + TM_S + 64 * half + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
             tmem_ld_wait();
-            if (QED) {                                // S <- (S + Z^T Ke) diag(e^{G_C}), staged in R2
-                const float *ecg = reinterpret_cast<const float *>(sm + OFF_R2) + 64 * half;
+            if (QED) {                                // S <- (S + Z^T Ke) diag(e^{G_C}), staged in ECG
+                const float *ecg = reinterpret_cast<const float *>(sm + OFF_ECG) + 64 * half;
 #pragma unroll
                 for (int e = 0; e < 64; e += 4) {
                     const float4 f = *reinterpret_cast<const float4 *>(ecg + e);
@@ -691,7 +742,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                 }
                 // matrix m = lane / 8 of each store: tokens 8 (j + m/2) + lane%8, d_v L + 8 (m%2) ..
                 const int m = lane >> 3, col = L + 8 * (m & 1);
-                const uint32_t obase = sbase + OFF_O + (uint32_t)(col >> 6) * 8192;
+                const uint32_t obase = sbase + kring(c) + (uint32_t)(col >> 6) * 8192;
 #pragma unroll
                 for (int j = 0; j < 8; j += 2) {
                     const int tok = 8 * (j + (m >> 1)) + (lane & 7);
@@ -702,8 +753,8 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             fence_proxy_async();
             named_sync(kBarChain, kChainThreads);
             if (c_issuer) {                               // rows past T are clipped by the copy
-                tma_store_4d(&tmO, sm + OFF_O, 0, h, t0, b);
-                tma_store_4d(&tmO, sm + OFF_O + 8192, 64, h, t0, b);
+                tma_store_4d(&tmO, sm + kring(c), 0, h, t0, b);
+                tma_store_4d(&tmO, sm + kring(c) + 8192, 64, h, t0, b);
                 tma_store_commit();
             }
         }
@@ -714,9 +765,9 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     if (prep) {
         // chunk 0's X and Gram; afterwards chunk c+1's are issued under chunk c's U/W
         wait_on(&bar_full[0], 0);
-        if (!QED) x_pass(0);                          // QED: the X rows (Ae) are loaded
+        if (!QED && warp >= 4) x_pass(0);             // QED: the X rows (Ae) are loaded
         psync();
-        issue_gram(0);
+        if (g_issuer) issue_gram(0);
         for (int c = 0; c < nchunks; ++c) {
             if (warp == 4 && c + 1 < nchunks) load_gates(c + 1);   // arrays built in solve(c)
             wait_mma(&bar_g, c);
@@ -731,23 +782,17 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             if (c >= 1) wait_mma(&bar_uw, c - 1);         // T free: U/W of chunk c-1 have run
             solve(c);
             psync();
-            if (p_issuer && c >= 1) {                     // TM_W free: the chain has read W(c-1)
-                wait_on(&bar_wfree, (uint32_t)((c - 1) & 1));
-                tc_fence_after();
-            }
-            issue_uw(c);
-            if (c + 1 < nchunks) {                        // TM_G was read by masks(c)
+            // three threads at once: the hand-off, U(c), the Gram of chunk c+1
+            if ((tid == 0 || p_issuer) && c >= 1) wait_on(&bar_taken, (uint32_t)((c - 1) & 1));   // see `taken`
+            if (tid == 0) mbar_arrive(&bar_ready);        // P(c), T2(c), gates(c+1), X(c+1) in place
+            if (g_issuer && c + 1 < nchunks) {            // TM_G was read by masks(c), X(c+1) formed
                 wait_on(&bar_full[(c + 1) & 1], (uint32_t)(((c + 1) >> 1) & 1));
-                if (!QED) {
-                    x_pass(c + 1);
-                    fence_proxy_async();
-                }
+                issue_gram(c + 1);
             }
+            issue_u(c);
             tc_fence_before();
             const bool stop = named_sync_or(kBarPrep, kPrepThreads, abort_flag != 0);
             tc_fence_after();
-            if (tid == 0) mbar_arrive(&bar_ready);        // P(c), gates(c+1), U/W(c) issued
-            if (c + 1 < nchunks) issue_gram(c + 1);
             if (stop) break;
         }
     } else {
@@ -779,34 +824,46 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         }
         csync();
         for (int c = 0; c < nchunks; ++c) {
-            // QED: this chunk's e^{G_C}, element d_row (into R2 once Z has read -W^T there)
+            // QED: this chunk's e^{G_C}, element d_row
             const float ecg = QED ? p.ecg[((size_t)bh * nchunks + c) * kD + d_row] : 0.f;
+            // S [X; Q]^T as soon as the state of chunk c-1 is final (X of chunk c was formed
+            // before `ready` of chunk c-1; that of chunk 0 before `ready` of chunk 0)
+            // K of chunk c + 2 goes into the slot of chunk c - 1, whose o tile the store has read
+            if (c > 0) issue_skq(c);
+            if (c > 0 && c_issuer && c + 2 < nchunks) {
+                tma_store_wait_read0();
+                issue_k(c + 2);
+            }
             wait_on(&bar_ready, (uint32_t)(c & 1));
+            if (c == 0) {
+                issue_skq(0);
+                if (c_issuer && nchunks > 2) issue_k(2);
+            }
             wait_mma(&bar_uw, c);
-            const bool fold = g_ell[c & 3][kC - 1] > kFoldLog;
-            w_store();
-            if (!fold) kappa_k(c);
-            csync();
-            if (c_issuer) mbar_arrive(&bar_wfree);
-            issue_z_o(c);
+            if (c_issuer) mbar_arrive(&bar_taken);
+            const float lC = g_ell[c & 3][kC - 1];
+            const bool fold = lC > kFoldLog, split = lC > kSplitLog;
             wait_mma(&bar_z, c);
-            if (QED) reinterpret_cast<float *>(sm + OFF_R2)[d_row] = ecg;   // read after the csyncs below
+            if (c_issuer && c + 2 < nchunks) {            // S [X; Q]^T and U of chunk c have run
+                issue_xqv(c + 2);
+                ++loads_issued;
+            }
+            sx_pack();
+            if (!split) o_gamma(c);
+            if (!fold) kappa_k(c);
+            if (QED) reinterpret_cast<float *>(sm + OFF_ECG)[d_row] = ecg;   // read after the csyncs below
+            csync();
+            issue_z(c);
+            wait_mma(&bar_zz, c);
             zt_pack(c, 0, fold);
             csync();
             issue_couple(c);
             wait_mma(&bar_cp, c);
             zt_pack(c, 1, fold);
-            if (c_issuer) tma_store_wait_read0();         // the o tile of chunk c-1 has been read
             csync();
             issue_mma2(c);
             wait_mma(&bar_o2, c);
-            if (c_issuer) {
-                mbar_arrive(&bar_cdone[c & 1]);
-                if (c + 2 < nchunks) {                    // chunk c's stage is consumed
-                    issue_loads(c + 2);
-                    ++loads_issued;
-                }
-            }
+            if (c_issuer) mbar_arrive(&bar_cdone[c & 1]);
             epilogue(c);
             tc_fence_before();
             const bool stop = named_sync_or(kBarChain, kChainThreads, abort_flag != 0);
@@ -823,8 +880,8 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                 const int n_s = (loads_issued + 1 - s) / 2;   // loads issued into stage s
                 if (n_s > 0) mbar_wait(&bar_full[s], (uint32_t)((n_s - 1) & 1), kWaitNs);
             }
-        if (p_issuer || c_issuer) {
-            uint64_t *dr = &bar_drain[p_issuer ? 0 : 1];
+        if (p_issuer || g_issuer || c_issuer) {
+            uint64_t *dr = &bar_drain[p_issuer ? 0 : g_issuer ? 2 : 1];
             umma_commit(dr);
             mbar_wait(dr, 0, kWaitNs);
         }
