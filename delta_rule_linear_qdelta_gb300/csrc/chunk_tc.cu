@@ -346,19 +346,23 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     auto kring = [&](int c) { return OFF_KR + (uint32_t)(c % 3) * 16384; };   // chunk c's K slot
 
     // ---------------------------------------------------------------- prep group
-    // X = K + lambda Q into rows 0-63 of the XQ panels of chunk c's stage, by warps 4-7
-    // (during the solve of the chunk before).  From projections (prologue), K and Q first
-    // become SiLU(x)/|SiLU(x)| in place.  Thread x = tid - 128 takes, in each of two rounds
-    // h2, the 16-byte chunks i = 0..3: panel i / 2, token row x/8 + 16 (2 h2 + i % 2); the
-    // eight threads of a row sum its squares by shuffles.
+    // X = K + lambda Q into rows 0-63 of the XQ panels of chunk c's stage: by warps 4-7
+    // during the solve of the chunk before, or, from projections (prologue), where K and Q
+    // first become SiLU(x)/|SiLU(x)| in place, by the whole prep group after it.  Thread x
+    // (of n = 128 or 256) takes, in each of 256/n rounds h2, the 16-byte chunks i = 0..3:
+    // panel i / 2 and token row x/8 + 16 (2 h2 + i % 2) (n = 128) or x/8 + 32 (i % 2)
+    // (n = 256); the eight threads of a row sum its squares by shuffles.
     auto x_pass = [&](int c) {
         uint8_t *st = sm + (c & 1) * kStageBytes;
         uint8_t *kb = sm + kring(c);
         const float *lam = g_lam[c & 3];
-        const int xt = tid - 128;
+        constexpr int nx = prologue ? kPrepThreads : 128;
+        const int xt = prologue ? tid : tid - 128;
 #pragma unroll 1
-        for (int h2 = 0; h2 < 2; ++h2) {
-            auto chunk_of_i = [&](int i) { return xt + 128 * (2 * h2 + (i & 1) + 4 * (i >> 1)); };
+        for (int h2 = 0; h2 < 256 / nx; ++h2) {
+            auto chunk_of_i = [&](int i) {
+                return prologue ? xt + 256 * i : xt + 128 * (2 * h2 + (i & 1) + 4 * (i >> 1));
+            };
             uint4 kr[4], qr[4];
             float lm[4];
 #pragma unroll
@@ -501,11 +505,11 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     // the two 32-token halves' inverses diag(T11, T22) -> Tinv*beta into T1, Tinv*beta*gamma
     // into T2[c&1], and the coupling -M21 (times 1/kappa in fold mode) into M21[c&1] (R1 and Y
     // as scratch); warps 4-7, idle in the solve's first phases, meanwhile turn the next
-    // chunk's raw gates into arrays (warp 4) and form its X
+    // chunk's raw gates into arrays (warp 4) and (not from projections) form its X
     auto next_x = [&](int c) {
         if (c + 1 >= nchunks) return;
         if (warp == 4) compute_gates(c + 1);
-        if (QED) return;                                  // QED: the X rows (Ae) are loaded
+        if (QED || prologue) return;                      // QED: the X rows (Ae) are loaded
         named_sync(kBarX, 128);                           // lambda of chunk c+1 in place
         wait_on(&bar_full[(c + 1) & 1], (uint32_t)(((c + 1) >> 1) & 1));
         x_pass(c + 1);
@@ -765,7 +769,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     if (prep) {
         // chunk 0's X and Gram; afterwards chunk c+1's are issued under chunk c's U/W
         wait_on(&bar_full[0], 0);
-        if (!QED && warp >= 4) x_pass(0);             // QED: the X rows (Ae) are loaded
+        if (!QED && (prologue || warp >= 4)) x_pass(0);   // QED: the X rows (Ae) are loaded
         psync();
         if (g_issuer) issue_gram(0);
         for (int c = 0; c < nchunks; ++c) {
@@ -782,6 +786,11 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             if (c >= 1) wait_mma(&bar_uw, c - 1);         // T free: U/W of chunk c-1 have run
             solve(c);
             psync();
+            if (prologue && c + 1 < nchunks) {            // from projections: X(c+1) after the solve
+                wait_on(&bar_full[(c + 1) & 1], (uint32_t)(((c + 1) >> 1) & 1));
+                x_pass(c + 1);
+                psync();
+            }
             // three threads at once: the hand-off, U(c), the Gram of chunk c+1
             if ((tid == 0 || p_issuer) && c >= 1) wait_on(&bar_taken, (uint32_t)((c - 1) & 1));   // see `taken`
             if (tid == 0) mbar_arrive(&bar_ready);        // P(c), T2(c), gates(c+1), X(c+1) in place
