@@ -206,14 +206,16 @@ QD_API qd_status qdelta_step_prologue(float *S, const void *q_raw, const void *k
  *   dlam [B][T][H]:   written when lam and dlam are both non-NULL
  *   dS0 [B][H][dv][dk] fp32: written when non-NULL (also when S0 is NULL)
  * No output may alias an input.  workspace: at least qdelta_bwd_workspace_bytes(...)
- * bytes (two fp32 checkpoint arrays: the state entering, and the gradient reaching
- * the state leaving, every chunk of 64 tokens).  T = 0 writes dS0 = dS_final (or 0)
- * and nothing else.  Precision: fp32 inputs, and head dims other than 128, run in
- * fp32 on CUDA cores.  bf16 inputs at dk = dv = 128 run on the tensor cores with fp32
- * accumulation and fp32 state and state gradient: the state checkpoints on the bf16
- * forward, the reverse sweep of the state gradient with bf16 operands, and the
- * per-chunk gradients with fp16 operands (10-bit mantissa; their intermediates stay
- * far inside fp16's range at unit-scale inputs); the elementwise work is fp32.
+ * bytes (two checkpoint arrays: the state entering, and the gradient reaching the
+ * state leaving, every chunk of 64 tokens; fp32, or fp16 tiles in half of that space
+ * on the tensor-core path).  T = 0 writes dS0 = dS_final (or 0) and nothing else.
+ * Precision: fp32 inputs, and head dims other than 128, run in fp32 on CUDA cores.
+ * bf16 inputs at dk = dv = 128 run on the tensor cores with fp32 accumulation, and
+ * the state and its gradient carried across chunks in fp32: the checkpoint forward is
+ * the bf16 forward, the reverse sweep of the state gradient takes bf16 operands, and
+ * the per-chunk gradients take fp16 operands (10-bit mantissa; their intermediates
+ * stay far inside fp16's range at unit-scale inputs), the two checkpoints among them,
+ * stored as fp16; the elementwise work is fp32.
  * Errors as for qdelta_fwd.
  */
 QD_API qd_status qdelta_bwd(const void *q, const void *k, const void *v,
