@@ -84,6 +84,7 @@
 #include <math.h>
 
 #include "qd_internal.cuh"
+#include "qed_derive.cuh"
 #include "sm103_ptx.cuh"
 #include "tc_common.cuh"
 
@@ -134,6 +135,12 @@ struct TcParams {
     int B, T, H;
     int flags;   // kTcNoV | kTcS0Identity | kTcNoO (segment-scan passes)
     const float *ecg;   // QED: e^{G_C} per chunk and channel, [B*H][nchunks][128]
+    // fused QED (n_chain > 0): CTAs n_chain.. derive the operands that CTAs 0..n_chain-1
+    // consume; done[bh * nchunks + chunk] counts the derived halves of each chunk (zero at
+    // the launch)
+    int n_chain;
+    unsigned int *done;
+    QedDeriveParams dp;
 };
 
 // PRO: q, k, alpha, beta, lambda arrive as projections and logits (the prologue of
@@ -169,6 +176,25 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         g_igam[4][kC];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if constexpr (QED) {
+        // fused QED: the CTAs past the chains derive the operands, one 32-token half of one
+        // chunk at a time in chunk order over all streams, on 256 threads, and count each
+        // finished half in `done` (every writer fences its stores before the count)
+        if (p.n_chain > 0 && (int)blockIdx.x >= p.n_chain) {
+            if (tid >= kDeriveThreads) return;
+            const int nd = (int)gridDim.x - p.n_chain, bhn = p.B * p.H, nch = (p.T + kC - 1) / kC;
+            float (*s_part)[kGroups][kD] = reinterpret_cast<float (*)[kGroups][kD]>(sm);
+            for (long long i = (long long)blockIdx.x - p.n_chain; i < 2LL * nch * bhn; i += nd) {
+                const int chunk = (int)(i / (2 * bhn)), rem = (int)(i % (2 * bhn));
+                qed_derive_half(p.dp, chunk, rem & 1, rem >> 1, s_part,
+                                []() { named_sync(4, kDeriveThreads); });
+                __threadfence();
+                named_sync(4, kDeriveThreads);        // the half's stores are out; s_part is free
+                if (tid == 0) atomicAdd(p.done + (size_t)(rem >> 1) * nch + chunk, 1u);
+            }
+            return;
+        }
+    }
     const bool prep = tid < kPrepThreads;
     const int q4 = warp & 3, hf = (warp >> 2) & 1;    // TMEM lane quarter; column half (prep)
     const int bh = blockIdx.x, b = bh / p.H, h = bh % p.H;
@@ -218,11 +244,24 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         reinterpret_cast<uint4 *>(sm + OFF_T)[i] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async();                                  // ... as the tensor core will read them
 
+    // fused QED: both halves of chunk c derived (bounded acquire), and the derived tiles,
+    // written by generic stores, ordered before this thread's TMA reads of them
+    auto derived_wait = [&](int c) {
+        if (!(QED && p.n_chain > 0)) return;
+        const unsigned int *d = p.done + (size_t)bh * nchunks + c;
+        uint64_t t0 = 0;
+        while (ld_acquire_u32(d) < 2u) {
+            if (t0 == 0) t0 = globaltimer_ns();
+            else if (globaltimer_ns() - t0 > kWaitNs) { abort_flag = 1; break; }
+        }
+        fence_proxy_async_global();
+    };
     // the tiles of chunk c on bar_full[c&1], in two parts: K into its slot (arming the
     // barrier with the whole chunk's bytes), then Q (QED: and A) and V into the stage
     auto issue_k = [&](int c) {
         const int s = c & 1;
         uint8_t *kb = sm + OFF_KR + (uint32_t)(c % 3) * 16384;
+        derived_wait(c);                              // fused QED: chunk c derived
         mbar_arrive_expect_tx(&bar_full[s], (no_v() ? kTmaBytes / 3 * 2 : kTmaBytes) + (QED ? kTmaBytes / 3 : 0));
 #pragma unroll
         for (int pnl = 0; pnl < 2; ++pnl) tma_load_4d(kb + pnl * 8192, &tmK, &bar_full[s], 64 * pnl, h, c * kC, b);
@@ -942,6 +981,46 @@ cudaError_t launch_qed_chain_tc(const QedArgs &a, const QedDerived &d, cudaStrea
     TcParams p{nullptr, nullptr, nullptr, a.S0, (__nv_bfloat16 *)a.o, a.S_final, a.B, a.T, a.H, flags, d.ecg};
     kern<<<a.B * a.H, kAllThreads, kSmemBytes, s>>>(p, mq, mk, mv, mo, ma);
     e = cudaGetLastError();
+    if (e == cudaSuccess) *nlaunch += 1;
+    return e;
+}
+
+// One cooperative launch (all CTAs resident at once): the chains of the B*H streams and,
+// on the remaining SMs, the derive step feeding them chunk by chunk through `done`.
+cudaError_t launch_qed_fused_tc(const QedArgs &a, const QedDerived &d, unsigned int *done, cudaStream_t s,
+                                int *nlaunch) {
+    CUtensorMap ma, mq, mk, mv, mo;
+    if (!make_token_map(&ma, d.Ae, a.B, a.T, a.H) || !make_token_map(&mq, d.Qe, a.B, a.T, a.H) ||
+        !make_token_map(&mk, d.Ke, a.B, a.T, a.H) || !make_token_map(&mv, d.WV, a.B, a.T, a.H) ||
+        !make_token_map(&mo, a.o, a.B, a.T, a.H))
+        return cudaErrorInvalidValue;
+    auto kern = qdelta_fwd_tc_kernel<false, false, true>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    int per_sm = 0;
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kAllThreads, (size_t)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const int bhn = a.B * a.H, grid = sm_count() * per_sm, nchunks = (a.T + kC - 1) / kC;
+    if (grid <= bhn) return cudaErrorInvalidValue;    // qed_fused_supported
+    e = cudaMemsetAsync(done, 0, (size_t)bhn * nchunks * sizeof(unsigned int), s);
+    if (e != cudaSuccess) return e;
+    const QedDeriveParams dp{(const __nv_bfloat16 *)a.q, (const __nv_bfloat16 *)a.k, (const __nv_bfloat16 *)a.v,
+                             (const __nv_bfloat16 *)a.g, (const __nv_bfloat16 *)a.b, (const __nv_bfloat16 *)a.w,
+                             a.lam_h, a.z, (__nv_bfloat16 *)d.Ae, (__nv_bfloat16 *)d.Qe, (__nv_bfloat16 *)d.Ke,
+                             (__nv_bfloat16 *)d.WV, d.ecg, a.B, a.T, a.H, a.variant, 0};
+    const TcParams p{nullptr, nullptr, nullptr, a.S0, (__nv_bfloat16 *)a.o, a.S_final, a.B, a.T, a.H, 0, d.ecg,
+                     bhn, done, dp};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kAllThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, p, mq, mk, mv, mo, ma);
     if (e == cudaSuccess) *nlaunch += 1;
     return e;
 }

@@ -33,6 +33,7 @@
 #include <math.h>
 
 #include "qd_internal.cuh"
+#include "qed_derive.cuh"
 #include "tc_common.cuh"
 
 namespace qd {
@@ -40,150 +41,11 @@ namespace {
 
 using namespace tc;
 
-constexpr int kDeriveThreads = 256;
-
-struct QedDeriveParams {
-    const __nv_bfloat16 *q, *k, *v, *g, *b, *w;
-    const float *lam_h, *z;
-    __nv_bfloat16 *Ae, *Qe, *Ke, *WV;
-    float *ecg;          // [B][H][nchunks][128]: e^{G_C} per chunk and channel
-    int B, T, H;
-    int variant;
-    int no_v;            // v is not read and W*V not written
-};
-
-// Two CTAs per (chunk, b*H + h), one per 32-token half (blockIdx.x = 2 chunk + half).
-// Thread (cg, rg): channels 8 cg .. 8 cg + 7 (one 16-byte vector of each input) of the
-// half's tokens 2 rg and 2 rg + 1.  A token row's sixteen channel groups sit in one
-// half-warp, so k.u is reduced there by shuffles.  The per-channel prefix of g runs over
-// a thread's two tokens, then across the sixteen token groups through shared memory;
-// the second half also reads g of the first (its own prefix starts there, and it writes
-// e^{G_C}).  Every input vector is loaded before any arithmetic (12 loads of 16 bytes
-// in flight per thread); at most 128 registers a thread, so two CTAs share an SM.
-constexpr int kTokPerThread = 2, kGroups = 16;
+// Two CTAs per (chunk, b*H + h), one per 32-token half (blockIdx.x = 2 chunk + half),
+// two CTAs per SM (at most 128 registers a thread).
 __global__ void __launch_bounds__(kDeriveThreads, 2) qed_derive_kernel(const QedDeriveParams p) {
     __shared__ __align__(16) float s_part[2][kGroups][kD];   // [first half, own half][group][channel]
-    const int tid = threadIdx.x;
-    const int chunk = blockIdx.x >> 1, half = blockIdx.x & 1, bh = blockIdx.y, b = bh / p.H, h = bh % p.H;
-    const int t0 = chunk * kC, nt = min(kC, p.T - t0);
-    const int nchunks = (p.T + kC - 1) / kC;
-    const bool gate = p.variant == kQedFull || p.variant == kQedRand;
-    const bool proj = p.variant != kQedNogateNoproj;
-    const float *zrow = p.variant == kQedRand ? p.z + (size_t)h * kD : nullptr;
-    const float lam = p.lam_h[h];
-    const int cg = tid & 15, rg = tid >> 4, j0 = 8 * cg;
-    auto off = [&](int t) { return (((size_t)b * p.T + t0 + t) * p.H + h) * kD + j0; };
-    auto ld8 = [&](const __nv_bfloat16 *src, int t) {
-        return *reinterpret_cast<const uint4 *>(src + off(t));
-    };
-    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-    uint4 rq[kTokPerThread], rk[kTokPerThread], rb[kTokPerThread], rgv[kTokPerThread], rg0[kTokPerThread];
-    uint4 rv[kTokPerThread], rw[kTokPerThread];
-#pragma unroll
-    for (int i = 0; i < kTokPerThread; ++i) {          // all loads first
-        const int t = 32 * half + kTokPerThread * rg + i, t_first = kTokPerThread * rg + i;
-        const bool ok = t < nt;
-        rq[i] = ok ? ld8(p.q, t) : zero;
-        rk[i] = ok ? ld8(p.k, t) : zero;
-        rb[i] = ok ? ld8(p.b, t) : zero;
-        rgv[i] = ok ? ld8(p.g, t) : zero;
-        rg0[i] = (half && t_first < nt) ? ld8(p.g, t_first) : zero;
-        rv[i] = (ok && !p.no_v) ? ld8(p.v, t) : zero;
-        rw[i] = (ok && !p.no_v) ? ld8(p.w, t) : zero;
-    }
-    float zf[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) zf[e] = zrow ? zrow[j0 + e] : 0.f;
-    // per-channel sums of g over this thread's tokens (own half, and the first half)
-    float gs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, g0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < kTokPerThread; ++i) {
-        float gf[8], hf8[8];
-        unpack8(rgv[i], gf);
-        unpack8(rg0[i], hf8);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            gs[e] += gf[e];
-            g0[e] += hf8[e];
-        }
-    }
-    *reinterpret_cast<float4 *>(&s_part[1][rg][j0]) = make_float4(gs[0], gs[1], gs[2], gs[3]);
-    *reinterpret_cast<float4 *>(&s_part[1][rg][j0 + 4]) = make_float4(gs[4], gs[5], gs[6], gs[7]);
-    *reinterpret_cast<float4 *>(&s_part[0][rg][j0]) = make_float4(g0[0], g0[1], g0[2], g0[3]);
-    *reinterpret_cast<float4 *>(&s_part[0][rg][j0 + 4]) = make_float4(g0[4], g0[5], g0[6], g0[7]);
-    // k.u per token, reduced over the sixteen channel groups of the half-warp
-    float ku[kTokPerThread];
-#pragma unroll
-    for (int i = 0; i < kTokPerThread; ++i) {
-        float kf[8], bf8[8], xf[8];
-        unpack8(rk[i], kf);
-        unpack8(rb[i], bf8);
-        unpack8(rq[i], xf);
-        float acc = 0.f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float x = zrow ? zf[e] : xf[e];
-            acc = fmaf(kf[e], gate ? bf8[e] * x : x, acc);
-        }
-#pragma unroll
-        for (int o = 1; o < 16; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        ku[i] = proj ? acc : 0.f;
-    }
-    __syncthreads();
-    // G before this thread's first token: the first half's total (second half only),
-    // then the own half's groups before rg
-    float G[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int r = 0; r < kGroups + rg; ++r) {
-        if (r < kGroups && !half) continue;
-        const float *src = r < kGroups ? &s_part[0][r][j0] : &s_part[1][r - kGroups][j0];
-        const float4 x = *reinterpret_cast<const float4 *>(src);
-        const float4 y = *reinterpret_cast<const float4 *>(src + 4);
-        G[0] += x.x; G[1] += x.y; G[2] += x.z; G[3] += x.w;
-        G[4] += y.x; G[5] += y.y; G[6] += y.z; G[7] += y.w;
-    }
-    if (half && rg == kGroups - 1) {                   // e^{G_C}: G over the whole chunk
-        float ec[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ec[e] = __expf(G[e] + gs[e]);
-        float4 *dst = reinterpret_cast<float4 *>(p.ecg + ((size_t)bh * nchunks + chunk) * kD + j0);
-        dst[0] = make_float4(ec[0], ec[1], ec[2], ec[3]);
-        dst[1] = make_float4(ec[4], ec[5], ec[6], ec[7]);
-    }
-    // per token: G_t, the erase vector a_t, and the operands
-#pragma unroll
-    for (int i = 0; i < kTokPerThread; ++i) {
-        const int t = 32 * half + kTokPerThread * rg + i;
-        float qf[8], kf[8], bf8[8], gf[8], ae[8], qe[8], ke[8];
-        unpack8(rq[i], qf);
-        unpack8(rk[i], kf);
-        unpack8(rb[i], bf8);
-        unpack8(rgv[i], gf);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            G[e] += gf[e];
-            const float x = zrow ? zf[e] : qf[e];
-            const float u = gate ? bf8[e] * x : x;
-            const float a = bf8[e] * kf[e] + lam * (proj ? u - kf[e] * ku[i] : u);
-            const float eg = __expf(G[e]), ig = __expf(-G[e]);
-            ae[e] = a * eg;
-            qe[e] = qf[e] * eg;
-            ke[e] = kf[e] * ig;
-        }
-        if (t < nt) {
-            const size_t o = off(t);
-            *reinterpret_cast<uint4 *>(p.Ae + o) = pack8(ae);
-            *reinterpret_cast<uint4 *>(p.Qe + o) = pack8(qe);
-            *reinterpret_cast<uint4 *>(p.Ke + o) = pack8(ke);
-            if (!p.no_v) {
-                float vf[8], wf[8];
-                unpack8(rv[i], vf);
-                unpack8(rw[i], wf);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) vf[e] *= wf[e];
-                *reinterpret_cast<uint4 *>(p.WV + o) = pack8(vf);
-            }
-        }
-    }
+    qed_derive_half(p, blockIdx.x >> 1, blockIdx.x & 1, blockIdx.y, s_part, []() { __syncthreads(); });
 }
 
 }  // namespace
@@ -223,8 +85,14 @@ cudaError_t launch_qed_derive(const QedArgs &a, const QedDerived &d, int no_v, c
     return e;
 }
 
+namespace {
+size_t qed_done_bytes(int B, int T, int H) {          // the fused launch's hand-over counters
+    return ((size_t)B * H * ((T + kC - 1) / kC) * sizeof(unsigned int) + 255) & ~(size_t)255;
+}
+}  // namespace
+
 size_t qed_tc_workspace(int B, int T, int H, int G) {
-    return qed_derived_bytes(B, T, H, G) + qdelta_segment_workspace(B, H, G);
+    return qed_derived_bytes(B, T, H, G) + qdelta_segment_workspace(B, H, G) + qed_done_bytes(B, T, H);
 }
 
 cudaError_t launch_qed_tc(const QedArgs &a, int G, cudaStream_t s, int *nlaunch) {
@@ -232,6 +100,12 @@ cudaError_t launch_qed_tc(const QedArgs &a, int G, cudaStream_t s, int *nlaunch)
     view.B = a.B * G;
     view.T = a.T / G;
     const QedDerived d = qed_derived_buffers(view.B, view.T, a.H, a.ws);
+    if (G == 1 && (long long)a.B * a.H + 8 <= sm_count()) {
+        unsigned int *done = reinterpret_cast<unsigned int *>(static_cast<uint8_t *>(a.ws) +
+                                                              qed_derived_bytes(a.B, a.T, a.H, 1) +
+                                                              qdelta_segment_workspace(a.B, a.H, 1));
+        return launch_qed_fused_tc(a, d, done, s, nlaunch);
+    }
     cudaError_t e = launch_qed_derive(view, d, 0, s, nlaunch);
     if (e != cudaSuccess) return e;
     if (G == 1) return launch_qed_chain_tc(a, d, s, nlaunch, 0);

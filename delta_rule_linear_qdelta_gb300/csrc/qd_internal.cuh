@@ -187,6 +187,13 @@ cudaError_t launch_qed_derive(const QedArgs &a, const QedDerived &d, int no_v, c
 // One pass of the chain kernel over derived operands (the QED instance of the Q-Delta
 // tensor-core kernel); a carries the view's sizes, S0, o and S_final.
 cudaError_t launch_qed_chain_tc(const QedArgs &a, const QedDerived &d, cudaStream_t s, int *nlaunch, int flags = 0);
+// Derive and chain in one cooperative launch: the chains of the B*H streams on B*H SMs,
+// the derive step on the rest, handing each chunk over through `done` (B*H*ceil(T/64)
+// counters in device memory, cleared by the launch).  Needs B*H below the SM count.
+cudaError_t launch_qed_fused_tc(const QedArgs &a, const QedDerived &d, unsigned int *done, cudaStream_t s,
+                                int *nlaunch);
+// SMs of the current device (0 if unknown).
+int sm_count();
 // Segment scan of the tensor-core forward for long sequences over few (b, h)
 // streams: the number of segments for these sizes (1 = a single pass), its
 // workspace, and the launch (three passes of the forward kernel and a combine).
@@ -198,8 +205,10 @@ cudaError_t launch_qdelta_segmented(const QDeltaArgs &a, int G, cudaStream_t s, 
 int qed_segments(int B, int T, int H, int dk, int dv, int dtype);
 cudaError_t launch_qed_segmented(const QedArgs &a, int G, const QedDerived &d, cudaStream_t s, int *nlaunch);
 // The whole tensor-core QED forward: derive over the (segment) view, then one chain pass
-// or the segment scan.  Workspace: qed_tc_workspace(B, T, H, G) bytes at a.ws (the
-// derived operands, then the segment states).
+// or the segment scan; in one pass with the derive beside the chains (launch_qed_fused_tc)
+// when B*H leaves at least 8 SMs to the derive step.  Workspace: qed_tc_workspace(B, T,
+// H, G) bytes at a.ws (the derived operands, then the segment states, then the hand-over
+// counters).
 size_t qed_tc_workspace(int B, int T, int H, int G);
 cudaError_t launch_qed_tc(const QedArgs &a, int G, cudaStream_t s, int *nlaunch);
 // Reads and clears the device word the tensor-core kernels set when a bounded wait runs out.

@@ -92,14 +92,15 @@ segment_combine_kernel(const float *S0, const float *Phi, const float *Psi, floa
         }
 }
 
+
+}  // namespace
+
 int sm_count() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
     return n;
 }
-
-}  // namespace
 
 int qdelta_segments(int B, int T, int H, int dk, int dv, int dtype) {
     if (dtype != kBF16 || dk != kD || dv != kD) return 1;

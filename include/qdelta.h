@@ -137,15 +137,18 @@ QD_API qd_status qed_step(float *S, const void *q, const void *k, const void *v,
                           qd_qed_variant variant, const float *z_h, cudaStream_t stream);
 
 /* Bytes of device workspace qed_fwd needs for these sizes (0 if none).  The
- * tensor-core path (bf16, dk = dv = 128) first derives each chunk's decay-folded
- * operands (a*e^G, q*e^G, k*e^-G, w*v as bf16 [B][T][H][128], and e^{G_C} per chunk
- * and channel in fp32) into the workspace, 8 * B * T * H * 128 bytes and a little
- * more; the other paths need none.  As for qdelta_fwd, very few (b, h) streams (at
- * most 16) carrying a long sequence are further cut into segments that run in
- * parallel (QED's per-chunk map of the transposed state is linear, S^ -> S^ Phi + Psi)
- * and are stitched together in fp32, with three d_v x d_k fp32 states per segment
- * after the derived operands.  Calls sharing a workspace must be ordered on one
- * stream. */
+ * tensor-core path (bf16, dk = dv = 128) derives each chunk's decay-folded operands
+ * (a*e^G, q*e^G, k*e^-G, w*v as bf16 [B][T][H][128], and e^{G_C} per chunk and
+ * channel in fp32) into the workspace, 8 * B * T * H * 128 bytes and a little more
+ * (one hand-over counter per chunk and stream); the other paths need none.  While
+ * B * H leaves at least 8 SMs free, the derive step runs on those SMs beside the
+ * per-stream chains, in one cooperative launch, and hands each chunk over through its
+ * counter; otherwise it is a launch of its own before the chains.  As for qdelta_fwd,
+ * very few (b, h) streams (at most 16) carrying a long sequence are further cut into
+ * segments that run in parallel (QED's per-chunk map of the transposed state is
+ * linear, S^ -> S^ Phi + Psi) and are stitched together in fp32, with three d_v x d_k
+ * fp32 states per segment after the derived operands.  Calls sharing a workspace must
+ * be ordered on one stream. */
 QD_API size_t qed_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype);
 
 /*

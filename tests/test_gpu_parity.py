@@ -229,6 +229,19 @@ def test_qed_small_all_outputs(qd, T, dt):
     check(S, S_ref, dt, f"qed T={T} S")
 
 
+@pytest.mark.parametrize("B,H", [(2, 2), (1, 160)])
+def test_qed_fused_and_two_launch_paths(qd, B, H):
+    # One cooperative launch (the derive step on the SMs the B*H chains leave free) when
+    # B*H + 8 <= SMs; the derive kernel and then the chain kernel otherwise.
+    d = synth.qed_inputs(B, 130, H, 128, 128, seed=90 + H, dtype="bf16", s0_var=0.01)
+    o, S = run_qed(qd, d)
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    assert qd.last_launch_count() == (1 if B * H + 8 <= nsm else 2)
+    o_ref, S_ref = oracle.qed_fwd(d["q"], d["k"], d["v"], d["g"], d["b"], d["w"], d["lam_h"], d["S0"])
+    check(o, o_ref, "bf16", f"qed B={B} H={H} o")
+    check(S, S_ref, "bf16", f"qed B={B} H={H} S")
+
+
 @pytest.mark.parametrize("dk,dv", [(64, 64), (128, 64)])
 def test_qed_head_dims_bf16(qd, dk, dv):
     d = synth.qed_inputs(2, 150, 2, dk, dv, seed=75 + dk + dv, dtype="bf16", s0_var=0.01)
