@@ -264,7 +264,12 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         derived_wait(c);                              // fused QED: chunk c derived
         mbar_arrive_expect_tx(&bar_full[s], (no_v() ? kTmaBytes / 3 * 2 : kTmaBytes) + (QED ? kTmaBytes / 3 : 0));
 #pragma unroll
-        for (int pnl = 0; pnl < 2; ++pnl) tma_load_4d(kb + pnl * 8192, &tmK, &bar_full[s], 64 * pnl, h, c * kC, b);
+        if (QED) {                                    // QED's maps take whole tiles
+            tma_load_5d(kb, &tmK, &bar_full[s], 0, c * kC, 0, h, b);
+        } else {
+#pragma unroll
+            for (int pnl = 0; pnl < 2; ++pnl) tma_load_4d(kb + pnl * 8192, &tmK, &bar_full[s], 64 * pnl, h, c * kC, b);
+        }
     };
     auto issue_xqv = [&](int c) {
         const int s = c & 1;
@@ -274,8 +279,9 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         for (int pnl = 0; pnl < 2; ++pnl) {
             if (QED) tma_load_4d(st + OFF_XQ + pnl * 16384, &tmA, &bar_full[s], 64 * pnl, h, t0, b);
             tma_load_4d(st + OFF_XQ + pnl * 16384 + 8192, &tmQ, &bar_full[s], 64 * pnl, h, t0, b);
-            if (!no_v()) tma_load_4d(st + OFF_V + pnl * 8192, &tmV, &bar_full[s], 64 * pnl, h, t0, b);
+            if (!QED && !no_v()) tma_load_4d(st + OFF_V + pnl * 8192, &tmV, &bar_full[s], 64 * pnl, h, t0, b);
         }
+        if (QED && !no_v()) tma_load_5d(st + OFF_V, &tmV, &bar_full[s], 0, t0, 0, h, b);
     };
     auto issue_loads = [&](int c) {
         issue_k(c);
@@ -796,8 +802,12 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             fence_proxy_async();
             named_sync(kBarChain, kChainThreads);
             if (c_issuer) {                               // rows past T are clipped by the copy
-                tma_store_4d(&tmO, sm + kring(c), 0, h, t0, b);
-                tma_store_4d(&tmO, sm + kring(c) + 8192, 64, h, t0, b);
+                if (QED) {
+                    tma_store_5d(&tmO, sm + kring(c), 0, t0, 0, h, b);
+                } else {
+                    tma_store_4d(&tmO, sm + kring(c), 0, h, t0, b);
+                    tma_store_4d(&tmO, sm + kring(c) + 8192, 64, h, t0, b);
+                }
                 tma_store_commit();
             }
         }
@@ -971,10 +981,10 @@ cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nla
 cudaError_t launch_qed_chain_tc(const QedArgs &a, const QedDerived &d, cudaStream_t s, int *nlaunch, int flags) {
     CUtensorMap ma, mq, mk, mv, mo;
     if (!make_token_map(&ma, d.Ae, a.B, a.T, a.H) || !make_token_map(&mq, d.Qe, a.B, a.T, a.H) ||
-        !make_token_map(&mk, d.Ke, a.B, a.T, a.H) || !make_token_map(&mv, d.WV, a.B, a.T, a.H))
+        !make_token_map_tile(&mk, d.Ke, a.B, a.T, a.H) || !make_token_map_tile(&mv, d.WV, a.B, a.T, a.H))
         return cudaErrorInvalidValue;
     if (flags & kTcNoO) mo = mq;                      // not used
-    else if (!make_token_map(&mo, a.o, a.B, a.T, a.H)) return cudaErrorInvalidValue;
+    else if (!make_token_map_tile(&mo, a.o, a.B, a.T, a.H)) return cudaErrorInvalidValue;
     auto kern = qdelta_fwd_tc_kernel<false, false, true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
@@ -991,8 +1001,8 @@ cudaError_t launch_qed_fused_tc(const QedArgs &a, const QedDerived &d, unsigned 
                                 int *nlaunch) {
     CUtensorMap ma, mq, mk, mv, mo;
     if (!make_token_map(&ma, d.Ae, a.B, a.T, a.H) || !make_token_map(&mq, d.Qe, a.B, a.T, a.H) ||
-        !make_token_map(&mk, d.Ke, a.B, a.T, a.H) || !make_token_map(&mv, d.WV, a.B, a.T, a.H) ||
-        !make_token_map(&mo, a.o, a.B, a.T, a.H))
+        !make_token_map_tile(&mk, d.Ke, a.B, a.T, a.H) || !make_token_map_tile(&mv, d.WV, a.B, a.T, a.H) ||
+        !make_token_map_tile(&mo, a.o, a.B, a.T, a.H))
         return cudaErrorInvalidValue;
     auto kern = qdelta_fwd_tc_kernel<false, false, true>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);

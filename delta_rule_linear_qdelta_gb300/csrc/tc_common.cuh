@@ -355,6 +355,21 @@ inline EncodeTiledFn encode_fn() {
     return fn;
 }
 
+// The same tensor viewed as [B][H][2 panels][T][64]: one box is a whole 64-token tile
+// of one head, landing as its two 64-column panels one after the other (the layout of
+// the two 4-D boxes at panel offsets 0 and 8 KB), so one TMA instruction moves it.
+inline bool make_token_map_tile(CUtensorMap *m, const void *ptr, int B, int T, int H) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[5] = {64, (cuuint64_t)T, 2, (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[4] = {(cuuint64_t)H * kD * 2, 64 * 2, (cuuint64_t)kD * 2, (cuuint64_t)T * H * kD * 2};
+    cuuint32_t box[5] = {64, (cuuint32_t)kC, 2, 1, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // [B][T][H][128] bf16 tensor, boxes of 64 columns x 64 tokens of one head.
 inline bool make_token_map(CUtensorMap *m, const void *ptr, int B, int T, int H) {
     EncodeTiledFn fn = encode_fn();
