@@ -717,12 +717,13 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         for (int j = 0; j < 32; ++j) sp[j] = pack_bf16x2(sv[2 * j], sv[2 * j + 1]);
         tmem_st32(tl + TM_SB + 32 * half, sp);
         if (store_back) {
+            if (!QED)                                 // QED: unit gates, gamma_C = 1
 #pragma unroll
-            for (int e = 0; e < 64; e += 2) {
-                const float2 x = fmul2(make_float2(sv[e], sv[e + 1]), make_float2(g, g));
-                sv[e] = x.x;
-                sv[e + 1] = x.y;
-            }
+                for (int e = 0; e < 64; e += 2) {
+                    const float2 x = fmul2(make_float2(sv[e], sv[e + 1]), make_float2(g, g));
+                    sv[e] = x.x;
+                    sv[e + 1] = x.y;
+                }
             tmem_st32(tl + TM_S + 64 * half, *reinterpret_cast<float(*)[32]>(sv));
             tmem_st32(tl + TM_S + 64 * half + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
         }
@@ -902,7 +903,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             const float lC = g_ell[c & 3][kC - 1];
             const bool fold = lC > kFoldLog, split = lC > kSplitLog;
             wait_mma(&bar_z, c);
-            if (c_issuer && c + 2 < nchunks) {            // S [X; Q]^T and U of chunk c have run
+            if (!QED && c_issuer && c + 2 < nchunks) {    // S [X; Q]^T and U of chunk c have run
                 issue_xqv(c + 2);
                 ++loads_issued;
             }
@@ -920,6 +921,10 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             zt_pack(c, 1, fold);
             csync();
             issue_mma2(c);
+            if (QED && c_issuer && c + 2 < nchunks) {     // QED forms no X: the next tiles can wait
+                issue_xqv(c + 2);                         // until the issuer waits anyway
+                ++loads_issued;
+            }
             wait_mma(&bar_o2, c);
             if (c_issuer) mbar_arrive(&bar_cdone[c & 1]);
             epilogue(c);
