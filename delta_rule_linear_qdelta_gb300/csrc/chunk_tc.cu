@@ -817,7 +817,8 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
 
     int loads_issued = nchunks > 1 ? 2 : 1;             // the chain issuer's bookkeeping for a drain
     if (prep) {
-        // chunk 0's X and Gram; afterwards chunk c+1's are issued under chunk c's U/W
+        // chunk 0's X and Gram; afterwards chunk c+1's X is formed during solve(c) and its
+        // Gram issued beside U(c)
         wait_on(&bar_full[0], 0);
         if (!QED && (prologue || warp >= 4)) x_pass(0);   // QED: the X rows (Ae) are loaded
         psync();
@@ -833,7 +834,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             tc_fence_before();
             named_sync(kBarPrep, kPrepThreads);
             tc_fence_after();
-            if (c >= 1) wait_mma(&bar_uw, c - 1);         // T free: U/W of chunk c-1 have run
+            if (c >= 1) wait_mma(&bar_uw, c - 1);         // T1 free: U of chunk c-1 has run
             solve(c);
             psync();
             if (prologue && c + 1 < nchunks) {            // from projections: X(c+1) after the solve

@@ -11,24 +11,26 @@
 //   Ae = A*e^G, Qe = Q*e^G, Ke = K*e^-G                  (elementwise, per channel)
 //   G  = [Ae; Qe] Ke^T                 -> At = strictly_lower, P = incl_lower
 //   Tinv = (I + At)^{-1}
-//   U^T = (W*V)^T Tinv^T,  W^T = Ae^T Tinv^T,  Z^T = U^T - S^ W^T
+//   U^T = (W*V)^T Tinv^T,  Z^T = U^T - (S^ Ae^T) Tinv^T      (= U^T - S^ W^T, W = Tinv Ae)
 //   O^T = S^ Qe^T + Z^T P^T
 //   S^ <- S^ diag(e^{G_C}) + Z^T (K*e^{G_C - G}) = (S^ + Z^T Ke) diag(e^{G_C})
 // The last form reads the same Ke tile as the Gram and applies the chunk's
 // per-channel decay once, to the fp32 state, in the epilogue.  The factored decay
 // stays in fp32 range while every channel's log-decay summed over one chunk is >= -80.
 //
-// Two kernels:
-//   qed_derive_kernel (this file, CUDA cores): every chunk independently, in parallel
-//     over all chunks: k.u per token, the erase vector a, the per-channel prefix G and
-//     the operands Ae, Qe, Ke, W*V (bf16, the [B][T][H][128] token layout) and e^{G_C}
-//     per chunk (fp32) into the workspace.  It is bandwidth bound: it reads the six
-//     input vectors once and writes four.
+// Two steps:
+//   the derive step (qed_derive.cuh, CUDA cores): every chunk independently: k.u per
+//     token, the erase vector a, the per-channel prefix G and the operands Ae, Qe, Ke,
+//     W*V (bf16, the [B][T][H][128] token layout) and e^{G_C} per chunk (fp32) into the
+//     workspace.  It reads the six input vectors once and writes four.
 //   the chain: the warp-specialised tensor-core chunk kernel of chunk_tc.cu in its QED
 //     instance, which takes Ae, Qe, Ke, W*V where the Q-Delta instance takes X, Q, K, V,
 //     runs with unit gates and multiplies the state by e^{G_C} per channel in its
 //     epilogue.  With the state-independent operands prepared, its per-chunk critical
 //     path is that of the Q-Delta kernel.
+// They run in one cooperative launch (launch_qed_fused_tc: the derive step on the SMs the
+// B*H chains leave free, handing chunks over through counters) while B*H leaves at least
+// 8 SMs, else as qed_derive_kernel (this file) and then the chain kernel.
 #include <cuda_bf16.h>
 #include <math.h>
 
