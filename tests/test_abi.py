@@ -222,3 +222,18 @@ def test_static_scratch_checks_arguments_before_any_device_call(lib):
     st = lib.qdelta_fwd_static_scratch(g, g, g, None, g, None, None, g, None, 1, 4096, 2, 128, 128, 32,
                                        qd.QD_BF16, None)
     assert st == qd.QD_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("B,T,H", [(2, 130, 3), (8, 2048, 16), (4, 4096, 8)])
+def test_qed_workspace_covers_derived_operands_and_counters(lib, B, T, H):
+    """The tensor-core QED path keeps four bf16 [B][T][H][128] operand arrays, e^{G_C} per
+    chunk and channel in fp32, and one 32-bit hand-over counter per chunk and stream
+    (rounded up to 256 bytes); these sizes take no segment states."""
+    nch = (T + 63) // 64
+    derived = 4 * B * T * H * 128 * 2 + B * H * nch * 128 * 4
+    counters = (B * H * nch * 4 + 255) // 256 * 256
+    assert lib.qed_workspace_bytes(B, T, H, 128, 128, 64, qd.QD_BF16) == derived + counters
+    # the CUDA-core paths (fp32, head dim 64) and a chunk other than 64 need none
+    assert lib.qed_workspace_bytes(B, T, H, 128, 128, 64, qd.QD_F32) == 0
+    assert lib.qed_workspace_bytes(B, T, H, 64, 64, 64, qd.QD_BF16) == 0
+    assert lib.qed_workspace_bytes(B, T, H, 128, 128, 32, qd.QD_BF16) == 0
