@@ -25,71 +25,97 @@ namespace qd {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kLS = 132;          // smem row stride (16-byte aligned rows)
+constexpr int kLS = 132;          // smem row stride (16-byte aligned rows; 8 rows hit 8 distinct 16-byte banks)
 constexpr int kCombineThreads = 256;
 constexpr int kRows = 16;         // state rows per combine CTA
 
+__device__ __forceinline__ void cp_async16(float *dst, const float *src) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void fma4(float (&acc)[4], float a, const float4 &p) {
+    acc[0] = fmaf(a, p.x, acc[0]);
+    acc[1] = fmaf(a, p.y, acc[1]);
+    acc[2] = fmaf(a, p.z, acc[2]);
+    acc[3] = fmaf(a, p.w, acc[3]);
+}
+
 // One CTA per (b, h, 16 state rows): rows of S evolve independently under
 // S <- S Phi_g + Psi_g, so a head's 128 rows are spread over 8 CTAs.  Each holds its
-// rows of S and the whole Phi_g (fp32) in shared memory; thread t computes row t/16,
-// columns 8 (t%16) .. 8 (t%16) + 7 of the product.
+// rows of S (two buffers, read and written in alternation) and Phi_g (fp32, two buffers:
+// Phi_{g+1} is copied in by cp.async while Phi_g is used) in shared memory, so one
+// barrier per segment orders everything.  Warp w computes columns 16 w .. 16 w + 15 of
+// all 16 rows; lane l rows l/4 and l/4 + 8, columns 16 w + 4 (l%4) .. + 3, reading four
+// k at a time (a warp's Phi reads are 64 contiguous bytes, its S reads 8 rows in 8
+// distinct banks).  Psi_g is loaded into registers before the products and added after.
+// Each result goes from registers to the next segment's S_start (or to S_final).
 __global__ void __launch_bounds__(kCombineThreads)
 segment_combine_kernel(const float *S0, const float *Phi, const float *Psi, float *S_start, float *S_final,
                        int B, int H, int G) {
-    extern __shared__ float sm[];
-    float *Ss = sm, *Ps = sm + kRows * kLS;
-    const int tid = threadIdx.x;
+    extern __shared__ float4 sm4[];
+    float *sm = reinterpret_cast<float *>(sm4);
+    auto Ss = [&](int i) { return sm + i * kRows * kLS; };             // S buffers 0, 1
+    auto Ps = [&](int i) { return sm + 2 * kRows * kLS + i * kD * kLS; };  // Phi buffers 0, 1
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int bh = blockIdx.x, b = bh / H, h = bh % H;
     const int row0 = blockIdx.y * kRows;
-    const int r = tid >> 4, c0 = 8 * (tid & 15);
+    const int r0 = lane >> 2, n0 = 16 * warp + 4 * (lane & 3);
     const size_t mat = (size_t)kD * kD;
-    for (int i = tid; i < kRows * kD / 4; i += kCombineThreads) {
-        const int rr = (4 * i) / kD, c = (4 * i) % kD;
-        const float4 v = S0 ? *reinterpret_cast<const float4 *>(S0 + (size_t)bh * mat + (size_t)(row0 + rr) * kD + c)
+    auto seg = [&](int g) { return ((size_t)(b * G + g) * H + h) * mat; };   // (b*G + g, h) in the segment batch
+    auto load_phi = [&](int g) {
+        const float *src = Phi + seg(g);
+        float *dst = Ps(g & 1);
+        for (int i = tid; i < kD * kD / 4; i += kCombineThreads)
+            cp_async16(dst + (i >> 5) * kLS + 4 * (i & 31), src + 4 * i);
+        cp_async_commit();
+    };
+    load_phi(0);
+    for (int i = tid; i < kRows * kD / 4; i += kCombineThreads) {   // S_start(0) = S0 (or 0)
+        const int rr = i >> 5, c = 4 * (i & 31);
+        const size_t o = (size_t)(row0 + rr) * kD + c;
+        const float4 v = S0 ? *reinterpret_cast<const float4 *>(S0 + (size_t)bh * mat + o)
                             : make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4 *>(Ss + rr * kLS + c) = v;
+        *reinterpret_cast<float4 *>(Ss(0) + rr * kLS + c) = v;
+        *reinterpret_cast<float4 *>(S_start + seg(0) + o) = v;
     }
-    __syncthreads();
     for (int g = 0; g < G; ++g) {
-        const size_t seg = ((size_t)(b * G + g) * H + h) * mat;   // (b*G + g, h) in the segment batch
-        for (int i = tid; i < kRows * kD / 4; i += kCombineThreads) {
-            const int rr = (4 * i) / kD, c = (4 * i) % kD;
-            *reinterpret_cast<float4 *>(S_start + seg + (size_t)(row0 + rr) * kD + c) =
-                *reinterpret_cast<const float4 *>(Ss + rr * kLS + c);
-        }
-        for (int i = tid; i < kD * kD / 4; i += kCombineThreads) {
-            const int rr = (4 * i) / kD, c = (4 * i) % kD;
-            *reinterpret_cast<float4 *>(Ps + rr * kLS + c) = reinterpret_cast<const float4 *>(Phi + seg)[i];
-        }
-        float acc[8];
-        {
-            const float *src = Psi + seg + (size_t)(row0 + r) * kD + c0;
-            const float4 u = *reinterpret_cast<const float4 *>(src), w = *reinterpret_cast<const float4 *>(src + 4);
-            acc[0] = u.x; acc[1] = u.y; acc[2] = u.z; acc[3] = u.w;
-            acc[4] = w.x; acc[5] = w.y; acc[6] = w.z; acc[7] = w.w;
-        }
-        __syncthreads();
+        cp_async_wait_all();
+        __syncthreads();    // Phi_g and S_start(g) in place; iteration g-1 no longer reads its buffers
+        if (g + 1 < G) load_phi(g + 1);
+        const size_t o0 = (size_t)(row0 + r0) * kD + n0, o1 = o0 + 8 * kD;
+        const float4 psi0 = *reinterpret_cast<const float4 *>(Psi + seg(g) + o0);
+        const float4 psi1 = *reinterpret_cast<const float4 *>(Psi + seg(g) + o1);
+        const float *S = Ss(g & 1), *P = Ps(g & 1);
+        float a0[4] = {0.f, 0.f, 0.f, 0.f}, a1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
-        for (int k = 0; k < kD; ++k) {
-            const float a = Ss[r * kLS + k];
-            const float4 p0 = *reinterpret_cast<const float4 *>(Ps + k * kLS + c0);
-            const float4 p1 = *reinterpret_cast<const float4 *>(Ps + k * kLS + c0 + 4);
-            acc[0] = fmaf(a, p0.x, acc[0]); acc[1] = fmaf(a, p0.y, acc[1]);
-            acc[2] = fmaf(a, p0.z, acc[2]); acc[3] = fmaf(a, p0.w, acc[3]);
-            acc[4] = fmaf(a, p1.x, acc[4]); acc[5] = fmaf(a, p1.y, acc[5]);
-            acc[6] = fmaf(a, p1.z, acc[6]); acc[7] = fmaf(a, p1.w, acc[7]);
+        for (int k = 0; k < kD; k += 4) {
+            const float4 s0 = *reinterpret_cast<const float4 *>(S + r0 * kLS + k);
+            const float4 s1 = *reinterpret_cast<const float4 *>(S + (r0 + 8) * kLS + k);
+            const float4 p0 = *reinterpret_cast<const float4 *>(P + k * kLS + n0);
+            const float4 p1 = *reinterpret_cast<const float4 *>(P + (k + 1) * kLS + n0);
+            const float4 p2 = *reinterpret_cast<const float4 *>(P + (k + 2) * kLS + n0);
+            const float4 p3 = *reinterpret_cast<const float4 *>(P + (k + 3) * kLS + n0);
+            fma4(a0, s0.x, p0); fma4(a1, s1.x, p0);
+            fma4(a0, s0.y, p1); fma4(a1, s1.y, p1);
+            fma4(a0, s0.z, p2); fma4(a1, s1.z, p2);
+            fma4(a0, s0.w, p3); fma4(a1, s1.w, p3);
         }
-        __syncthreads();
-        *reinterpret_cast<float4 *>(Ss + r * kLS + c0) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        *reinterpret_cast<float4 *>(Ss + r * kLS + c0 + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
-        __syncthreads();
+        const float4 x0 = make_float4(a0[0] + psi0.x, a0[1] + psi0.y, a0[2] + psi0.z, a0[3] + psi0.w);
+        const float4 x1 = make_float4(a1[0] + psi1.x, a1[1] + psi1.y, a1[2] + psi1.z, a1[3] + psi1.w);
+        if (g + 1 < G) {
+            float *Sn = Ss((g + 1) & 1);
+            *reinterpret_cast<float4 *>(Sn + r0 * kLS + n0) = x0;
+            *reinterpret_cast<float4 *>(Sn + (r0 + 8) * kLS + n0) = x1;
+            *reinterpret_cast<float4 *>(S_start + seg(g + 1) + o0) = x0;
+            *reinterpret_cast<float4 *>(S_start + seg(g + 1) + o1) = x1;
+        } else if (S_final) {
+            *reinterpret_cast<float4 *>(S_final + (size_t)bh * mat + o0) = x0;
+            *reinterpret_cast<float4 *>(S_final + (size_t)bh * mat + o1) = x1;
+        }
     }
-    if (S_final)
-        for (int i = tid; i < kRows * kD / 4; i += kCombineThreads) {
-            const int rr = (4 * i) / kD, c = (4 * i) % kD;
-            *reinterpret_cast<float4 *>(S_final + (size_t)bh * mat + (size_t)(row0 + rr) * kD + c) =
-                *reinterpret_cast<const float4 *>(Ss + rr * kLS + c);
-        }
 }
 
 
@@ -141,7 +167,7 @@ cudaError_t run_segmented(const Args &a, int G, cudaStream_t s, int *nlaunch, La
     seg.S_final = Phi;
     e = launch(seg, kTcNoO | kTcNoV | kTcS0Identity);
     if (e != cudaSuccess) return e;
-    const size_t smem = (kRows + kD) * kLS * sizeof(float);
+    const size_t smem = 2 * (kRows + kD) * kLS * sizeof(float);
     e = cudaFuncSetAttribute(segment_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     segment_combine_kernel<<<dim3(a.B * a.H, kD / kRows), kCombineThreads, smem, s>>>(a.S0, Phi, Psi, S_start,
