@@ -247,14 +247,16 @@ qd_status qdelta_bwd_prologue(const void *q_raw, const void *k_raw, const void *
 }
 
 size_t eda_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype) {
-    (void)B; (void)T; (void)H; (void)dk; (void)dv; (void)chunk; (void)dtype;
-    return 0;
+    if (B <= 0 || T <= 0 || H <= 0 || chunk != 64) return 0;
+    qd::EdaArgs a{};
+    a.B = B; a.T = T; a.H = H; a.dk = dk; a.dv = dv;
+    if (!qd::eda_tc_supported(a, dtype)) return 0;     // the recurrent kernel needs none
+    return qd::eda_tc_workspace(B, T, H);
 }
 
 qd_status eda_fwd(const void *q, const void *k, const void *v, const void *e, const void *beta, const float *S0,
                   void *o, float *S_final, int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype,
                   void *workspace, size_t workspace_bytes, cudaStream_t stream) {
-    (void)workspace_bytes;
     g_err[0] = 0;
     const void *req[] = {q, k, v, e, o};
     const void *opt[] = {beta, S0, S_final, workspace};
@@ -263,8 +265,11 @@ qd_status eda_fwd(const void *q, const void *k, const void *v, const void *e, co
     if (B == 0 || H == 0) { g_launches = 0; return QD_OK; }
     if (T == 0) { g_launches = 0; return empty_sequence(S0, S_final, B, H, dk, dv, stream); }
     qd::EdaArgs a{q, k, v, e, beta, S0, o, S_final, B, T, H, dk, dv};
+    const size_t need = eda_workspace_bytes(B, T, H, dk, dv, chunk, dtype);
+    if (need && (!workspace || workspace_bytes < need))
+        return fail(QD_ERR_WORKSPACE, "eda_fwd: workspace of %zu bytes needed, %zu given", need, workspace_bytes);
     int n = 0;
-    cudaError_t err = qd::launch_eda(a, dtype, stream, &n);
+    cudaError_t err = need ? qd::launch_eda_tc(a, workspace, stream, &n) : qd::launch_eda(a, dtype, stream, &n);
     if (err != cudaSuccess) return cuda_fail(err, "eda_fwd launch");
     g_launches = n;
     return QD_OK;

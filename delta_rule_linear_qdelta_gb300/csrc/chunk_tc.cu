@@ -150,12 +150,16 @@ struct TcParams {
 // 32 KB fp16 [dv][dk] tile in the layout of a 128-byte-swizzled MMA operand (two
 // 64-column panels of 128 rows, chk_tile_off), which the gradient kernel copies in one
 // piece.  That instance runs without output (kTcNoO) and takes the array in p.o.
+// F16: q, k, v and o are fp16 instead of bf16, and so are every operand the kernel forms
+// (X, Pt, the inverse, -(S X^T), Zt, the state copy); alpha must be null (the decay
+// factors of the other regimes do not fit fp16's range).  The EDA forward (eda_tc.cu)
+// runs its sub-token sequence through this instance.
 // QED: the chain of the QED forward (chunk_tc_qed.cu) over its derived operands: tmA,
 // tmQ, tmK, tmV map Ae, Qe, Ke, W*V, the X rows are loaded (Ae) instead of formed, every
 // gate is a unit (alpha = 1, beta = 1, lambda = 0: the products above then are QED's
 // Gram, masks, solve, U, S [A; Q]^T, Z, O and S + Z^T Ke), and the epilogue multiplies the state
 // by the chunk's e^{G_C} per channel (column of the [dv][dk] state).
-template <bool PRO, bool CHK = false, bool QED = false>
+template <bool PRO, bool CHK = false, bool QED = false, bool F16 = false>
 __global__ void __launch_bounds__(kAllThreads, 1)
 qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                      const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -470,8 +474,8 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                 const int pnl = u >> 9;
                 const uint32_t off = (uint32_t)(u & 511) << 4;
                 float kf[8], qf[8], xf[8];
-                unpack8(kr[r], kf);
-                unpack8(qr[r], qf);
+                unpack8t<F16>(kr[r], kf);
+                unpack8t<F16>(qr[r], qf);
 #pragma unroll
                 for (int e = 0; e < 8; e += 2) {
                     const float2 x = ffma2(make_float2(lm[r], lm[r]), make_float2(qf[e], qf[e + 1]),
@@ -479,7 +483,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                     xf[e] = x.x;
                     xf[e + 1] = x.y;
                 }
-                *reinterpret_cast<uint4 *>(st + OFF_XQ + pnl * 16384 + off) = pack8(xf);
+                *reinterpret_cast<uint4 *>(st + OFF_XQ + pnl * 16384 + off) = pack8t<F16>(xf);
             }
         }
     };
@@ -490,7 +494,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         for (int k = 0; k < 8; ++k) {
             const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
             umma_bf16(tm + TM_G, smem_desc(sXQ + ko, 16, 1024), smem_desc(sK + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024),
-                      idesc_bf16(128, 64, false, false), k > 0);
+                      idesc_16<F16>(128, 64, false, false), k > 0);
         }
         umma_commit(&bar_g);
     };
@@ -544,7 +548,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             uint8_t *P = sm + OFF_P + (c & 1) * 8192;
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch)
-                *reinterpret_cast<uint4 *>(P + sw128_off(t, 32 * hf + 8 * ch)) = pack8p(g + 8 * ch);
+                *reinterpret_cast<uint4 *>(P + sw128_off(t, 32 * hf + 8 * ch)) = pack8t<F16>(g + 8 * ch);
         }
     };
     // the two 32-token halves' inverses diag(T11, T22) -> Tinv*beta into T1, Tinv*beta*gamma
@@ -563,7 +567,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     auto solve = [&](int c) {
         const int gi = c & 3;
         const bool fold = g_ell[gi][kC - 1] > kFoldLog;
-        unit_lower_inverse<true>(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_Y),
+        unit_lower_inverse<true, F16>(reinterpret_cast<float *>(sm + OFF_R1), reinterpret_cast<float *>(sm + OFF_Y),
                                  sm + OFF_T, sm + OFF_T + 8192 + (c & 1) * 8192, g_beta[gi], g_gam[gi],
                                  [&]() { next_x(c); },
                                  []() { named_sync(kBarPrep, kPrepThreads); },
@@ -578,7 +582,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 umma_bf16(tu, smem_desc(sV + k * 2048, 8192, 1024), smem_desc(sT + k * 32, 16, 1024),
-                          idesc_bf16(128, 64, true, false), k > 0);
+                          idesc_16<F16>(128, 64, true, false), k > 0);
         umma_commit(&bar_uw);
     };
 
@@ -593,7 +597,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         for (int k = 0; k < 8; ++k) {
             const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32;
             umma_bf16_ta(tm + TM_SK, tm + TM_SB + 8 * k, smem_desc(sXQ + ko, 16, 1024),
-                         idesc_bf16(128, 128, false, false), k > 0);
+                         idesc_16<F16>(128, 128, false, false), k > 0);
         }
         umma_commit(&bar_z);
     };
@@ -605,7 +609,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         tmem_ld_wait();
         uint32_t xp[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) xp[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]) ^ 0x80008000u;
+        for (int j = 0; j < 32; ++j) xp[j] = pack2<F16>(x[2 * j], x[2 * j + 1]) ^ 0x80008000u;
         tmem_st32(tl + TM_SK, xp);
         tmem_st_wait();
     };
@@ -645,10 +649,10 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         for (int r = 0; r < 8; ++r) {
             const uint32_t off = (uint32_t)(ct + kChainThreads * r) << 4;
             float kf[8];
-            unpack8(kr[r], kf);
+            unpack8t<F16>(kr[r], kf);
 #pragma unroll
             for (int e = 0; e < 8; ++e) kf[e] *= ka[r];
-            *reinterpret_cast<uint4 *>(st + off) = pack8(kf);
+            *reinterpret_cast<uint4 *>(st + off) = pack8t<F16>(kf);
         }
     };
     // Z^T = U^T - (S X^T) T2^T = U^T - S W^T, accumulated into U[c&1] (A = -(S X^T) packed in TMEM)
@@ -658,7 +662,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
         const uint32_t sT2 = sT + 8192 + (uint32_t)(c & 1) * 8192;
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-            umma_bf16_ta(tu, tm + TM_SK + 8 * k, smem_desc(sT2 + k * 32, 16, 1024), idesc_bf16(128, 64, false, false),
+            umma_bf16_ta(tu, tm + TM_SK + 8 * k, smem_desc(sT2 + k * 32, 16, 1024), idesc_16<F16>(128, 64, false, false),
                          (no_v() && k == 0) ? 0u : 1u);
         umma_commit(&bar_zz);
     };
@@ -676,8 +680,8 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             const float4 kv = fold ? *reinterpret_cast<const float4 *>(kap + 2 * j) : make_float4(1.f, 1.f, 1.f, 1.f);
             const float2 a = fmul2(make_float2(z[2 * j], z[2 * j + 1]), make_float2(kv.x, kv.y));
             const float2 b = fmul2(make_float2(z[2 * j + 2], z[2 * j + 3]), make_float2(kv.z, kv.w));
-            zp[j] = pack_bf16x2(a.x, a.y);
-            zp[j + 1] = pack_bf16x2(b.x, b.y);
+            zp[j] = pack2<F16>(a.x, a.y);
+            zp[j + 1] = pack2<F16>(b.x, b.y);
         }
         tmem_st16(tu + 16 * hf2, zp);
         tmem_st_wait();
@@ -690,7 +694,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
         for (int k = 0; k < 2; ++k)                       // K = 16 tokens = two core matrices along K
             umma_bf16_ta(tu + 32, tu + 8 * k, smem_desc_noswz(sM + k * 256, 128, 512),
-                         idesc_bf16(128, 32, false, false), 1);
+                         idesc_16<F16>(128, 32, false, false), 1);
         umma_commit(&bar_cp);
     };
     // O += Zt^T Pt^T ; S += Zt^T (kappa K)  (S in TMEM already scaled by gamma_C); A = Zt^T in TMEM
@@ -701,12 +705,12 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
         for (int k = 0; k < 4; ++k)
             umma_bf16_ta(tm + TM_S, tz + 8 * k, smem_desc(sK + k * 2048, 8192, 1024),
-                         idesc_bf16(128, 128, false, true), 1);
+                         idesc_16<F16>(128, 128, false, true), 1);
         if (!no_o())
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 umma_bf16_ta(tm + TM_O, tz + 8 * k, smem_desc(sP + k * 32, 16, 1024),
-                             idesc_bf16(128, 64, false, false), 1);
+                             idesc_16<F16>(128, 64, false, false), 1);
         umma_commit(&bar_o2);
     };
     // the state of this thread's row, 64 columns from column 64 h: packed bf16 copy into
@@ -714,7 +718,7 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
     auto state_half = [&](int half, float (&sv)[64], float g, bool store_back) {
         uint32_t sp[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sp[j] = pack_bf16x2(sv[2 * j], sv[2 * j + 1]);
+        for (int j = 0; j < 32; ++j) sp[j] = pack2<F16>(sv[2 * j], sv[2 * j + 1]);
         tmem_st32(tl + TM_SB + 32 * half, sp);
         if (store_back) {
             if (!QED)                                 // QED: unit gates, gamma_C = 1
@@ -787,8 +791,8 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
                 for (int j = 0; j < 8; ++j) {
                     const float2 lo = fmul2(make_float2(ov[4 * j], ov[4 * j + 1]), gv[j]);
                     const float2 hi = fmul2(make_float2(ov[4 * j + 2], ov[4 * j + 3]), gv[j]);
-                    pk[2 * j] = pack_bf16x2(lo.x, lo.y);
-                    pk[2 * j + 1] = pack_bf16x2(hi.x, hi.y);
+                    pk[2 * j] = pack2<F16>(lo.x, lo.y);
+                    pk[2 * j + 1] = pack2<F16>(hi.x, hi.y);
                 }
                 // matrix m = lane / 8 of each store: tokens 8 (j + m/2) + lane%8, d_v L + 8 (m%2) ..
                 const int m = lane >> 3, col = L + 8 * (m & 1);
@@ -970,7 +974,10 @@ cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nla
         return cudaErrorInvalidValue;
     if (flags & kTcNoO) mo = mq;                      // not used
     else if (!make_token_map(&mo, a.o, a.B, a.T, a.H)) return cudaErrorInvalidValue;
-    auto kern = a.S_chk ? (a.prologue ? qdelta_fwd_tc_kernel<true, true> : qdelta_fwd_tc_kernel<false, true>)
+    const bool f16 = (flags & kTcF16) != 0;
+    if (f16 && (a.S_chk || a.prologue || a.alpha)) return cudaErrorInvalidValue;   // no decay in fp16
+    auto kern = f16 ? qdelta_fwd_tc_kernel<false, false, false, true>
+              : a.S_chk ? (a.prologue ? qdelta_fwd_tc_kernel<true, true> : qdelta_fwd_tc_kernel<false, true>)
               : a.prologue ? qdelta_fwd_tc_kernel<true> : qdelta_fwd_tc_kernel<false>;
     if (a.S_chk && !(flags & kTcNoO)) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);

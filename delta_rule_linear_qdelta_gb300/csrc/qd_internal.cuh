@@ -97,6 +97,12 @@ struct EdaArgs {
 };
 // The EDA forward: a recurrent fp32 kernel, one CTA per (b, h), dv <= 128.
 cudaError_t launch_eda(const EdaArgs &a, int dtype, cudaStream_t s, int *nlaunch);
+// The EDA forward on the tensor cores (bf16, dk = dv = 128): a sub-token pass, the fp16
+// instance of the Q-Delta tensor-core forward over 2T+1 sub-tokens and a read-out pass,
+// in eda_tc_workspace(B, T, H) bytes of workspace.
+bool eda_tc_supported(const EdaArgs &a, int dtype);
+size_t eda_tc_workspace(int B, int T, int H);
+cudaError_t launch_eda_tc(const EdaArgs &a, void *ws, cudaStream_t s, int *nlaunch);
 
 // QED ablation arms ("The Query Knows What to Forget", Table 1): the term added to
 // the base erase vector b*k, P(u) = u - k (k^T u):
@@ -167,8 +173,9 @@ cudaError_t launch_qed_step(const QedStepArgs &a, int dtype, cudaStream_t s, int
 
 // Tensor-core (tcgen05) chunked Q-Delta forward: bf16, dk = dv = 128.  flags select the
 // segment-scan passes: kTcNoV (v taken as 0, v not read), kTcS0Identity (S0 = I per
-// head, needs dk = dv), kTcNoO (o not written).
-enum { kTcNoV = 1, kTcS0Identity = 2, kTcNoO = 4 };
+// head, needs dk = dv), kTcNoO (o not written); kTcF16 takes q, k, v, o as fp16 and forms
+// every operand in fp16 (alpha null, no prologue, no checkpoints).
+enum { kTcNoV = 1, kTcS0Identity = 2, kTcNoO = 4, kTcF16 = 8 };
 bool qdelta_tc_supported(const QDeltaArgs &a, int dtype);
 cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nlaunch, int flags = 0);
 // Tensor-core (tcgen05) chunked QED forward: bf16, dk = dv = 128; flags as above.  The

@@ -317,6 +317,11 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b
     return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
 }
+// One of the two by a compile-time choice (kHalf: fp16).
+template <bool kHalf>
+__host__ __device__ constexpr uint32_t idesc_16(int M, int N, bool a_mn, bool b_mn) {
+    return kHalf ? idesc_f16(M, N, a_mn, b_mn) : idesc_bf16(M, N, a_mn, b_mn);
+}
 
 // Byte offset of element (row, col) in a 128B-swizzled tile of 64 bf16 columns
 // (128-byte rows, 1024-byte aligned base): 16-byte chunk index XOR (row mod 8).

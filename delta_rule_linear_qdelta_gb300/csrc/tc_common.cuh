@@ -99,6 +99,14 @@ __device__ __forceinline__ uint4 pack8hp(const float *f) {
 template <bool kHalf> __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return kHalf ? pack_half2(lo, hi) : pack_bf16x2(lo, hi);
 }
+// eight 16-bit values of the chosen type to / from fp32
+template <bool kHalf> __device__ __forceinline__ void unpack8t(const uint4 &u, float (&f)[8]) {
+    if (kHalf) unpack8h(u, f);
+    else unpack8(u, f);
+}
+template <bool kHalf> __device__ __forceinline__ uint4 pack8t(const float *f) {
+    return kHalf ? pack8hp(f) : pack8p(f);
+}
 template <bool kHalf> __device__ __forceinline__ uint16_t cvt16(float x) {
     if (kHalf) {
         __half v = __float2half_rn(x);
@@ -226,7 +234,7 @@ __device__ __forceinline__ void put_pair(uint8_t *out1, uint8_t *out2, const flo
 //
 // With kCouple the last merge is left to the caller: phase d then computes only
 // M21 = T22 A21 (the 32x32 block coupling the two halves) and writes
-// -M21 diag(s3 * s3_mul) (null s3: -M21) as a bf16 [32][32] tile without swizzle
+// -M21 diag(s3 * s3_mul) (null s3: -M21) as a bf16 (fp16 with kHalf) [32][32] tile without swizzle
 // (core_off below) to out3; out1/out2 then hold the block-diagonal inverse
 // diag(T11, T22) with the same scalings.  Since T21 = -M21 T11, a solve (I + A) z = r is finished from the
 // block-diagonal one, zl = diag(T11, T22) r, by z_bot = zl_bot - M21 z_top.
@@ -310,8 +318,8 @@ __device__ __forceinline__ void unit_lower_inverse(float *M, float *Y, uint8_t *
         tile_cab<32>(d, M + (32 + m0) * LA + n0, LA, M + (32 + m0) * LA + 32, LA, M + 32 * LA + n0, LA);
         const int c0 = n0 + 2 * t4;
         const float f0 = s3 ? -s3[c0] * s3_mul : -1.f, f1 = s3 ? -s3[c0 + 1] * s3_mul : -1.f;
-        *reinterpret_cast<uint32_t *>(out3 + core_off(m0 + g, c0)) = pack_bf16x2(f0 * d[0], f1 * d[1]);
-        *reinterpret_cast<uint32_t *>(out3 + core_off(m0 + 8 + g, c0)) = pack_bf16x2(f0 * d[2], f1 * d[3]);
+        *reinterpret_cast<uint32_t *>(out3 + core_off(m0 + g, c0)) = pack2<kHalf>(f0 * d[0], f1 * d[1]);
+        *reinterpret_cast<uint32_t *>(out3 + core_off(m0 + 8 + g, c0)) = pack2<kHalf>(f0 * d[2], f1 * d[3]);
         return;
     }
     // 32 -> 64: warp w takes rows 16 (w / 4) and columns 8 (w % 4) of the 32x32 block

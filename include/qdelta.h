@@ -265,16 +265,22 @@ QD_API size_t qdelta_bwd_prologue_workspace_bytes(int B, int T, int H, int dk, i
  *     o_t = M^T q_t                                 read-out after both steps
  * e [B][T][H][dk] in the call's dtype, used as given (the page's default is
  * e = q/|q|; pass that to get it).  beta [B][T][H] or NULL (= 1).  Other arguments,
- * layouts, state convention and errors as for qdelta_fwd.  Arithmetic and state in
- * fp32 for both dtypes (token by token: with e = q the read-out cancels most of S q,
- * which bf16 operands would not resolve).  workspace may be NULL: none is needed
- * (eda_workspace_bytes returns 0; the argument keeps the forwards' signature).
+ * layouts, state convention and errors as for qdelta_fwd.
+ * bf16 with dk = dv = 128 runs on the tensor cores: o_t = S_{t-1} r_t + beta_t (k_t.q_t) v_t
+ * with r_t = (I - e e^T)(q_t - beta_t (k_t.q_t) k_t) formed in fp32 per token (the
+ * read-out's cancellation at e = q done before any rounding), then the Delta rule over
+ * 2T+1 sub-tokens (erase e_t, write k_t) in fp16 operands with fp32 accumulation and an
+ * fp32 state; inputs and states must lie inside fp16's range (|x| < 65504).  That path
+ * needs eda_workspace_bytes() of workspace (QD_ERR_WORKSPACE without it); fp32 inputs and
+ * other head dims run a recurrence in fp32 and need none (workspace may then be NULL).
  */
 QD_API qd_status eda_fwd(const void *q, const void *k, const void *v, const void *e, const void *beta,
                          const float *S0, void *o, float *S_final, int B, int T, int H, int dk, int dv,
                          int chunk, qd_dtype dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
-/* Bytes of device workspace eda_fwd needs for these sizes. */
+/* Bytes of device workspace eda_fwd needs for these sizes: for bf16 at dk = dv = 128 the
+ * fp16 sub-token keys, values, queries and outputs ([B][2T+1][H][128] each), their bf16
+ * strengths and one fp32 scalar per token-head, each rounded up to 256 bytes; 0 otherwise. */
 QD_API size_t eda_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype);
 
 /*

@@ -237,3 +237,22 @@ def test_qed_workspace_covers_derived_operands_and_counters(lib, B, T, H):
     assert lib.qed_workspace_bytes(B, T, H, 128, 128, 64, qd.QD_F32) == 0
     assert lib.qed_workspace_bytes(B, T, H, 64, 64, 64, qd.QD_BF16) == 0
     assert lib.qed_workspace_bytes(B, T, H, 128, 128, 32, qd.QD_BF16) == 0
+
+
+def test_eda_workspace_for_the_tensor_core_path(lib):
+    """bf16 at d_k = d_v = 128 takes the tensor-core path: four fp16 [B][2T+1][H][128]
+    sub-token arrays, their bf16 strengths and c_t (fp32 [B][T][H]), each rounded up to
+    256 bytes; a call without it is refused before any device work."""
+    r = lambda n: (n + 255) // 256 * 256
+    for B, T, H in [(2, 150, 2), (8, 2048, 16)]:
+        n = B * (2 * T + 1) * H
+        want = 4 * r(n * 128 * 2) + r(n * 2) + r(B * T * H * 4)
+        assert lib.eda_workspace_bytes(B, T, H, 128, 128, 64, qd.QD_BF16) == want
+        assert lib.eda_workspace_bytes(B, T, H, 128, 128, 64, qd.QD_F32) == 0
+        assert lib.eda_workspace_bytes(B, T, H, 128, 64, 64, qd.QD_BF16) == 0
+    g = ctypes.c_void_p(256)
+    st = lib.eda_fwd(g, g, g, g, None, None, g, None, 1, 8, 1, 128, 128, 64, qd.QD_BF16, None, 0, None)
+    assert st == qd.QD_ERR_WORKSPACE and "eda_fwd" in qd.qd_last_error()
+    need = lib.eda_workspace_bytes(1, 8, 1, 128, 128, 64, qd.QD_BF16)
+    st = lib.eda_fwd(g, g, g, g, None, None, g, None, 1, 8, 1, 128, 128, 64, qd.QD_BF16, g, need - 16, None)
+    assert st == qd.QD_ERR_WORKSPACE

@@ -79,3 +79,46 @@ def test_qdelta_chunked_backward_equals_sequential_adjoint(T, C, mode):
             continue
         r = r[0, 0] if name == "dS0" else r[0, :, 0]
         np.testing.assert_allclose(g[name], r, atol=1e-11 * max(1.0, np.abs(r).max()), err_msg=name)
+
+
+def eda_subtokens(q, k, v, e, beta):
+    """The sub-token sequence of the tensor-core EDA path ([T, d] arrays of one stream,
+    beta None = 1): keys, values, strengths and queries of 2T+1 Delta-rule sub-tokens
+    (a leading no-op carrying r_0, then per token the erase e_t (value 0, strength 1,
+    query 0) and the write k_t (v_t, beta_t, query r_{t+1})), and c_t = beta_t k_t.q_t."""
+    T, dk = q.shape
+    b = np.ones(T) if beta is None else beta
+    c = b * np.einsum("td,td->t", k, q)
+    y = q - c[:, None] * k
+    r = y - np.einsum("td,td->t", e, y)[:, None] * e
+    n = 2 * T + 1
+    K = np.zeros((n, dk)); V = np.zeros((n, v.shape[1])); Bs = np.zeros(n); Q = np.zeros((n, dk))
+    K[1::2], Bs[1::2] = e, 1.0
+    K[2::2], V[2::2], Bs[2::2] = k, v, b
+    Q[0:2 * T:2] = r
+    return K, V, Bs, Q, c
+
+
+@pytest.mark.parametrize("T", [1, 2, 33, 100])
+@pytest.mark.parametrize("erase", ["random", "query"])
+@pytest.mark.parametrize("unit_step", [False, True])
+def test_eda_is_a_delta_rule_over_subtokens(T, erase, unit_step):
+    """EDA ("Erase-then-Delta Attention": erase along e, then the Delta write) equals the
+    Delta rule over 2T+1 sub-tokens read one sub-token before each erase with
+    r_t = (I - e e^T)(q - c k), plus c_t v_t: the oracle's EDA against the oracle's
+    Q-Delta forward (alpha 1, lambda 0) over that sequence, both fp64."""
+    dk, dv = 8, 6
+    q = _unit(rng.standard_normal((1, T, 1, dk)))
+    k = _unit(rng.standard_normal((1, T, 1, dk)))
+    e = q.copy() if erase == "query" else _unit(rng.standard_normal((1, T, 1, dk)))
+    v = rng.standard_normal((1, T, 1, dv))
+    beta = None if unit_step else rng.uniform(0.05, 1.0, (1, T, 1))
+    S0 = rng.standard_normal((1, 1, dv, dk)) * 0.5
+    o_ref, S_ref = oracle.eda_fwd(q, k, v, e, beta, S0)
+    K, V, Bs, Q, c = eda_subtokens(q[0, :, 0], k[0, :, 0], v[0, :, 0], e[0, :, 0],
+                                   None if beta is None else beta[0, :, 0])
+    o_sub, S = oracle.qdelta_fwd(Q[None, :, None], K[None, :, None], V[None, :, None], None, Bs[None, :, None],
+                                 None, S0)
+    o = o_sub[0, 0:2 * T:2, 0] + c[:, None] * v[0, :, 0]
+    assert np.abs(o - o_ref[0, :, 0]).max() <= 1e-12 * max(1.0, np.abs(o_ref).max())
+    assert np.abs(S - S_ref).max() <= 1e-12 * max(1.0, np.abs(S_ref).max())

@@ -610,7 +610,8 @@ def test_eda_forward_all_outputs(qd, dt, dh, erase, beta):
     150 tokens (9 staged tiles + a ragged one), carried S0."""
     d = synth.eda_inputs(2, 150, 2, dh, dh, seed=81, dtype=dt, erase=erase, beta=beta, s0_var=0.01)
     o, S = run_eda(qd, d)
-    assert qd.last_launch_count() == 1
+    # bf16 at d = 128: sub-token pass, the fp16 tensor-core forward, read-out; else the recurrence
+    assert qd.last_launch_count() == (3 if (dt, dh) == ("bf16", 128) else 1)
     o_ref, S_ref = oracle.eda_fwd(d["q"], d["k"], d["v"], d["e"], d["beta"], d["S0"])
     check(o, o_ref, dt, f"eda {dt} {erase} o")
     check(S, S_ref, dt, f"eda {dt} {erase} S")
@@ -625,6 +626,35 @@ def test_eda_rectangular_state(qd, dt, dk, dv):
     o_ref, S_ref = oracle.eda_fwd(d["q"], d["k"], d["v"], d["e"], d["beta"], d["S0"])
     check(o, o_ref, dt, f"eda {dt} dk={dk} dv={dv} o")
     check(S, S_ref, dt, f"eda {dt} dk={dk} dv={dv} S")
+
+
+@pytest.mark.parametrize("erase", ["random", "query"])
+def test_eda_full_size_every_stream(qd, erase):
+    """The bench's EDA workload (B=8, H=16, T=2048, d=128, bf16, beta = sigmoid(N(0,1)),
+    carried S0) on the tensor-core path: every (b, h) stream against the oracle."""
+    d = synth.eda_inputs(8, 2048, 16, 128, 128, seed=84, dtype="bf16", erase=erase, s0_var=0.01)
+    o, S = run_eda(qd, d)
+    assert qd.last_launch_count() == 3
+    o_ref, S_ref = oracle.eda_fwd(d["q"], d["k"], d["v"], d["e"], d["beta"], d["S0"])
+    check_every_stream(o, o_ref, S, S_ref, f"eda full {erase}")
+
+
+def test_eda_tensor_core_short_and_empty_sequences(qd):
+    """T = 1 and T = 63 (one ragged chunk of 3 and of 127 sub-tokens), and T = 0 (the
+    final state is S0) on the tensor-core path."""
+    for T in (1, 63):
+        d = synth.eda_inputs(1, T, 3, 128, 128, seed=85 + T, dtype="bf16", erase="query", s0_var=0.01)
+        o, S = run_eda(qd, d)
+        o_ref, S_ref = oracle.eda_fwd(d["q"], d["k"], d["v"], d["e"], d["beta"], d["S0"])
+        check(o, o_ref, "bf16", f"eda T={T} o")
+        check(S, S_ref, "bf16", f"eda T={T} S")
+    d = synth.eda_inputs(1, 1, 3, 128, 128, seed=90, dtype="bf16", s0_var=0.01)
+    z = torch.empty(1, 0, 3, 128, dtype=torch.bfloat16, device="cuda")
+    S0 = dev(d["S0"], torch.float32)
+    o, S = qd.eda_fwd(z, z, z, z, None, S0)
+    torch.cuda.synchronize()
+    assert o.shape == (1, 0, 3, 128)
+    np.testing.assert_array_equal(S.cpu().numpy(), d["S0"])
 
 
 def test_eda_long_sequence_query_erase(qd):
