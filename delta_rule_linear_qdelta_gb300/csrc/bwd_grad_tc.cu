@@ -133,6 +133,21 @@ __device__ __forceinline__ float2 warp_sum64(float (&x)[64]) {
     }
     return make_float2(x[0], x[1]);
 }
+// The same for 32 values: lane l returns the total of entry l.
+__device__ __forceinline__ float warp_sum32(float (&x)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int w = 16; w >= 1; w >>= 1) {               // 32 -> 16 -> ... -> 1 entries a lane
+#pragma unroll
+        for (int i = 0; i < w; ++i) {
+            const bool hi = lane & w;
+            const float send = hi ? x[i] : x[w + i];
+            const float keep = hi ? x[w + i] : x[i];
+            x[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+        }
+    }
+    return x[0];
+}
 
 __global__ void __launch_bounds__(kNT, 1)
 qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensorMap tmQ,
@@ -240,8 +255,25 @@ qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensor
     };
     // e^{l_t - l_i} for i <= t (the decay mask H), factored while l_C > -80
     const bool split = g_ell[kC - 1] > -80.f;
-    auto hmask = [&](int t, int i) {
-        return split ? g_gam[t] * g_ig[i] : __expf(g_ell[t] - g_ell[i]);
+    // H[t][32 hf + cc] for cc < 32 into f (above the diagonal too; callers mask), the
+    // branch taken once for the whole row
+    auto hrow = [&](int t, float (&f)[32]) {
+        if (split) {
+            const float gt = g_gam[t];
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+                const float4 x = *reinterpret_cast<const float4 *>(g_ig + 32 * hf + 4 * c4);
+                f[4 * c4] = gt * x.x; f[4 * c4 + 1] = gt * x.y; f[4 * c4 + 2] = gt * x.z; f[4 * c4 + 3] = gt * x.w;
+            }
+        } else {
+            const float lt = g_ell[t];
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+                const float4 x = *reinterpret_cast<const float4 *>(g_ell + 32 * hf + 4 * c4);
+                f[4 * c4] = __expf(lt - x.x); f[4 * c4 + 1] = __expf(lt - x.y);
+                f[4 * c4 + 2] = __expf(lt - x.z); f[4 * c4 + 3] = __expf(lt - x.w);
+            }
+        }
     };
 
     // ------------------------------------------------------------- X and the Gram
@@ -309,10 +341,12 @@ qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensor
         tmem_ld_wait();
         const bool arow = q4 < 2;
         const int t = 32 * (arow ? q4 : q4 - 2) + lane;
+        float hf32[32];
+        hrow(t, hf32);
 #pragma unroll
         for (int cc = 0; cc < 32; ++cc) {
             const int i = 32 * hf + cc;
-            g[cc] = (arow ? i < t : i <= t) ? hmask(t, i) * g[cc] : 0.f;
+            g[cc] = (arow ? i < t : i <= t) ? hf32[cc] * g[cc] : 0.f;
         }
         uint8_t *mp = sm + OFF_MP + (arow ? 0 : 8192);
 #pragma unroll
@@ -449,17 +483,10 @@ qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensor
         tmem_ld32(tl + TM_DR + 32 * hf, dr);
         tmem_ld32(tl + TM_A + 32 * hf, rr);
         tmem_ld_wait();
-        float pr[64];
+        float pr[32];
 #pragma unroll
-        for (int cc = 0; cc < 32; ++cc) {
-            pr[cc] = dr[cc] * rr[cc];
-            pr[32 + cc] = 0.f;
-        }
-        const float2 s2 = warp_sum64(pr);                 // entries 2 lane, 2 lane + 1 (< 32 used)
-        if (lane < 16) {
-            red[warp][32 * hf + 2 * lane] = s2.x;
-            red[warp][32 * hf + 2 * lane + 1] = s2.y;
-        }
+        for (int cc = 0; cc < 32; ++cc) pr[cc] = dr[cc] * rr[cc];
+        red[warp][32 * hf + lane] = warp_sum32(pr);       // token 32 hf + lane
     }
     sync_mma();
     if (tid < kC) {                                    // sum over the four lane quarters of the half
@@ -509,22 +536,22 @@ qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensor
         }
         float hd[32], ev[32], dam = 0.f;
         const float bt = g_beta[t];
+        float hf32[32];
+        hrow(t, hf32);
+        // A rows: dA = -(dR Z^T) strictly lower, dM = beta dA;  P rows: dP = dO Z^T, lower.
+        // One loop for both (warp-uniform lim and f): x = the kept D5 entry, dM | dP = f x.
+        const int lim = arow ? t : t + 1;
+        const float f = arow ? -bt : 1.f;
 #pragma unroll
         for (int cc = 0; cc < 32; ++cc) {
             const int i = 32 * hf + cc;
-            const float hti = i <= t ? hmask(t, i) : 0.f;
-            if (arow) {                                   // dA = -(dR Z^T), strictly lower; dM = beta dA
-                const float da = i < t ? -d5[cc] : 0.f;
-                dam = fmaf(da, mv[cc], dam);              // rowsum(dA * M)
-                const float dm = bt * da;
-                ev[cc] = dm * mv[cc];
-                hd[cc] = hti * dm;
-            } else {                                      // dP = dO Z^T, lower
-                const float dp = i <= t ? d5[cc] : 0.f;
-                ev[cc] = dp * mv[cc];
-                hd[cc] = hti * dp;
-            }
+            const float x = i < lim ? d5[cc] : 0.f;
+            dam = fmaf(x, mv[cc], dam);                   // -rowsum(dA * M) on A rows
+            const float dm = f * x;
+            ev[cc] = dm * mv[cc];
+            hd[cc] = (i <= t ? hf32[cc] : 0.f) * dm;
         }
+        dam = -dam;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch)                    // H * dM | H * dP over M | P
             *reinterpret_cast<uint4 *>(mp + sw128_off(t, 32 * hf + 8 * ch)) = pack8hp(hd + 8 * ch);
@@ -555,6 +582,7 @@ qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensor
     if (tid < kC) {                                       // dbeta = rowsum(dA * M) + sum_v dR R
         s_db[tid] += red[tid >> 5][tid] + red[4 + (tid >> 5)][tid];
         float re = 0.f, ce = 0.f;
+#pragma unroll 8
         for (int i = 0; i < kC; ++i) {
             re += E[tid * LA + i];
             ce += E[i * LA + tid];
@@ -599,53 +627,48 @@ qdelta_bwd_grad_tc_kernel(const GradTcParams p, const __grid_constant__ CUtensor
     // ------------------------------------------------------ dq, dk, dlambda, w z
     {
         const int j = row, jp = j >> 6, jc = j & 63;
-        float dx[64], dd[64];
-        if (hf == 0) {                                    // dX^T (lanes d_k, tokens) and dK^T
-            tmem_ld32(tl + TM_D6, *reinterpret_cast<float(*)[32]>(dx));
-            tmem_ld32(tl + TM_D6 + 32, *reinterpret_cast<float(*)[32]>(dx + 32));
-        } else {                                          // dQ^T (without lambda dX^T), and dX^T
-            tmem_ld32(tl + TM_D6 + 64, *reinterpret_cast<float(*)[32]>(dd));
-            tmem_ld32(tl + TM_D6 + 96, *reinterpret_cast<float(*)[32]>(dd + 32));
-            tmem_ld32(tl + TM_D6, *reinterpret_cast<float(*)[32]>(dx));
-            tmem_ld32(tl + TM_D6 + 32, *reinterpret_cast<float(*)[32]>(dx + 32));
-        }
+        // one loop for both halves (warp-uniform operands):
+        //   hf 0: dK^T = w (Z dS)^T + D8 + dX^T,   row-sum term w_t K[t][j] (Z dS)[t][j]
+        //   hf 1: dQ^T = lambda dX^T + dQ^T',       row-sum term dX[t][j] Q[t][j]
+        // with a = (Z dS)^T (D7) or dX^T, b = D8 + dX^T or dQ^T' (D6 without lambda dX^T)
+        const bool kside = hf == 0;
+        float a[64], bb[64];
+        tmem_ld32(tl + (kside ? TM_A : TM_D6), *reinterpret_cast<float(*)[32]>(a));
+        tmem_ld32(tl + (kside ? TM_A : TM_D6) + 32, *reinterpret_cast<float(*)[32]>(a + 32));
+        tmem_ld32(tl + (kside ? TM_B : TM_D6 + 64), *reinterpret_cast<float(*)[32]>(bb));
+        tmem_ld32(tl + (kside ? TM_B : TM_D6 + 64) + 32, *reinterpret_cast<float(*)[32]>(bb + 32));
         tmem_ld_wait();
-        if (hf == 0) {
-            float d8[64], d7[64];
-            tmem_ld32(tl + TM_B, *reinterpret_cast<float(*)[32]>(d8));
-            tmem_ld32(tl + TM_B + 32, *reinterpret_cast<float(*)[32]>(d8 + 32));
-            tmem_ld32(tl + TM_A, *reinterpret_cast<float(*)[32]>(d7));
-            tmem_ld32(tl + TM_A + 32, *reinterpret_cast<float(*)[32]>(d7 + 32));
+        if (kside) {
+            float dx[64];
+            tmem_ld32(tl + TM_D6, *reinterpret_cast<float(*)[32]>(dx));
+            tmem_ld32(tl + TM_D6 + 32, *reinterpret_cast<float(*)[32]>(dx + 32));
             tmem_ld_wait();
-            float wz[64];
 #pragma unroll
-            for (int t = 0; t < kC; ++t) {
-                const float kv = __half2float(*reinterpret_cast<const __half *>(sm + OFF_K + jp * 8192 + sw128_off(t, jc)));
-                wz[t] = g_w[t] * kv * d7[t];              // w_t K[t][j] (Z dS)[t][j]
-                dd[t] = fmaf(g_w[t], d7[t], d8[t]) + dx[t];   // dK^T
-            }
-            const float2 s2 = warp_sum64(wz);
-            red[warp][2 * lane] = s2.x;
-            red[warp][2 * lane + 1] = s2.y;
-        } else {
-            float lq[64];
+            for (int t = 0; t < kC; ++t) bb[t] += dx[t];
+        }
+        const float *cf = kside ? g_w : g_lam;
+        const uint8_t *tile = kside ? sm + OFF_K + jp * 8192 : sm + OFF_XQ + jp * 16384 + 8192;
+        float ps[64], dd[64];                             // the row-sum terms; dK^T or dQ^T
 #pragma unroll
-            for (int t = 0; t < kC; ++t) {
-                const float qv = __half2float(*reinterpret_cast<const __half *>(sm + OFF_XQ + jp * 16384 + 8192 + sw128_off(t, jc)));
-                lq[t] = dx[t] * qv;                       // dX[t][j] Q[t][j]
-                dd[t] = fmaf(g_lam[t], dx[t], dd[t]);     // dQ^T
-            }
-            const float2 s2 = warp_sum64(lq);
+        for (int t = 0; t < kC; ++t) {
+            const float m = __half2float(*reinterpret_cast<const __half *>(tile + sw128_off(t, jc)));
+            const float c = cf[t];
+            ps[t] = (kside ? c * m : m) * a[t];
+            dd[t] = fmaf(c, a[t], bb[t]);
+        }
+        {
+            const float2 s2 = warp_sum64(ps);
             red[warp][2 * lane] = s2.x;
             red[warp][2 * lane + 1] = s2.y;
         }
         // dk (hf 0) or dq (hf 1) column j: fp32 straight to global memory, bf16 into a
         // [t][dk] tile (Sb's place: dk panels, then dq panels) for the TMA store
-        if (p.grad_f32) {
-            float *dst = static_cast<float *>(hf ? p.dq : p.dk);
+        if (p.grad_f32) {                                 // token t at dst + t H kD
+            float *dst = static_cast<float *>(hf ? p.dq : p.dk) + tok_of(0) * kD + j;
+            const int step = H * kD;
 #pragma unroll
             for (int t = 0; t < kC; ++t)
-                if (t < n) dst[tok_of(t) * kD + j] = dd[t];
+                if (t < n) dst[t * step] = dd[t];
         } else {
             uint8_t *st = sm + OFF_SB + (hf ? 16384 : 0) + jp * 8192;
 #pragma unroll

@@ -153,7 +153,10 @@ struct TcParams {
 // F16: q, k, v and o are fp16 instead of bf16, and so are every operand the kernel forms
 // (X, Pt, the inverse, -(S X^T), Zt, the state copy); alpha must be null (the decay
 // factors of the other regimes do not fit fp16's range).  The EDA forward (eda_tc.cu)
-// runs its sub-token sequence through this instance.
+// runs its 2T'+1 sub-tokens through this instance: k holds every sub-token, while q, v
+// and o are compact [B][T'][H][128] arrays read through pair maps (tc_common.cuh), so
+// that sub-token 2j + p is row j of q and o (p = 0; zero / not stored for p = 1) and row
+// j - 1 of v (p = 0; zero for p = 1 and j = 0).
 // QED: the chain of the QED forward (chunk_tc_qed.cu) over its derived operands: tmA,
 // tmQ, tmK, tmV map Ae, Qe, Ke, W*V, the X rows are loaded (Ae) instead of formed, every
 // gate is a unit (alpha = 1, beta = 1, lambda = 0: the products above then are QED's
@@ -282,6 +285,11 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
         for (int pnl = 0; pnl < 2; ++pnl) {
             if (QED) tma_load_4d(st + OFF_XQ + pnl * 16384, &tmA, &bar_full[s], 64 * pnl, h, t0, b);
+            if (F16) {                                // pair maps: sub-token 2j + p is compact row j (p = 0)
+                tma_load_5d(st + OFF_XQ + pnl * 16384 + 8192, &tmQ, &bar_full[s], 64 * pnl, 0, h, t0 / 2, b);
+                tma_load_5d(st + OFF_V + pnl * 8192, &tmV, &bar_full[s], 64 * pnl, 0, h, t0 / 2 - 1, b);
+                continue;
+            }
             tma_load_4d(st + OFF_XQ + pnl * 16384 + 8192, &tmQ, &bar_full[s], 64 * pnl, h, t0, b);
             if (!QED && !no_v()) tma_load_4d(st + OFF_V + pnl * 8192, &tmV, &bar_full[s], 64 * pnl, h, t0, b);
         }
@@ -809,6 +817,11 @@ qdelta_fwd_tc_kernel(const TcParams p, const __grid_constant__ CUtensorMap tmQ,
             if (c_issuer) {                               // rows past T are clipped by the copy
                 if (QED) {
                     tma_store_5d(&tmO, sm + kring(c), 0, t0, 0, h, b);
+                } else if (F16) {                         // odd sub-tokens fall outside the pair map;
+                    if (t0 / 2 < (T - 1) / 2) {           // a chunk holding only sub-token 2T' stores nothing
+                        tma_store_5d(&tmO, sm + kring(c), 0, 0, h, t0 / 2, b);
+                        tma_store_5d(&tmO, sm + kring(c) + 8192, 64, 0, h, t0 / 2, b);
+                    }
                 } else {
                     tma_store_4d(&tmO, sm + kring(c), 0, h, t0, b);
                     tma_store_4d(&tmO, sm + kring(c) + 8192, 64, h, t0, b);
@@ -969,13 +982,21 @@ bool qdelta_tc_supported(const QDeltaArgs &a, int dtype) {
 
 cudaError_t launch_qdelta_chunk_tc(const QDeltaArgs &a, cudaStream_t s, int *nlaunch, int flags) {
     CUtensorMap mq, mk, mv, mo;
-    if (!make_token_map(&mq, a.q, a.B, a.T, a.H) || !make_token_map(&mk, a.k, a.B, a.T, a.H) ||
-        !make_token_map(&mv, a.v, a.B, a.T, a.H))
-        return cudaErrorInvalidValue;
-    if (flags & kTcNoO) mo = mq;                      // not used
-    else if (!make_token_map(&mo, a.o, a.B, a.T, a.H)) return cudaErrorInvalidValue;
     const bool f16 = (flags & kTcF16) != 0;
-    if (f16 && (a.S_chk || a.prologue || a.alpha)) return cudaErrorInvalidValue;   // no decay in fp16
+    if (f16) {                                        // q, v, o compact over (a.T - 1) / 2 pair rows
+        if (a.S_chk || a.prologue || a.alpha || (flags & (kTcNoO | kTcNoV)) || a.T % 2 == 0)
+            return cudaErrorInvalidValue;             // no decay in fp16; the EDA sub-token layout
+        const int Tc = (a.T - 1) / 2;
+        if (!make_pair_map(&mq, a.q, a.B, Tc, a.H) || !make_token_map(&mk, a.k, a.B, a.T, a.H) ||
+            !make_pair_map(&mv, a.v, a.B, Tc, a.H) || !make_pair_map(&mo, a.o, a.B, Tc, a.H))
+            return cudaErrorInvalidValue;
+    } else {
+        if (!make_token_map(&mq, a.q, a.B, a.T, a.H) || !make_token_map(&mk, a.k, a.B, a.T, a.H) ||
+            !make_token_map(&mv, a.v, a.B, a.T, a.H))
+            return cudaErrorInvalidValue;
+        if (flags & kTcNoO) mo = mq;                  // not used
+        else if (!make_token_map(&mo, a.o, a.B, a.T, a.H)) return cudaErrorInvalidValue;
+    }
     auto kern = f16 ? qdelta_fwd_tc_kernel<false, false, false, true>
               : a.S_chk ? (a.prologue ? qdelta_fwd_tc_kernel<true, true> : qdelta_fwd_tc_kernel<false, true>)
               : a.prologue ? qdelta_fwd_tc_kernel<true> : qdelta_fwd_tc_kernel<false>;

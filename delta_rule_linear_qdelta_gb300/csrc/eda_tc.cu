@@ -28,7 +28,11 @@
 //
 // Three launches on the caller's stream: eda_subtoken_kernel (r_t, c_t and the sub-token
 // arrays), the fp16 instance of the Q-Delta tensor-core forward (chunk_tc.cu) over the
-// [B][2T+1] sub-token sequence, and eda_readout_kernel (o_t = o'_{2t} + c_t v_t).
+// [B][2T+1] sub-token sequence, and eda_readout_kernel (o_t = o'_{2t} + c_t v_t).  Only the
+// keys are stored per sub-token; queries, values and outputs are nonzero (needed) on one
+// sub-token of each pair, so they are compact [B][T][H][128] arrays (r_t, v_t, o'_{2t})
+// that the kernel reads and writes through pair maps, the other rows coming from the
+// maps' zero fill.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -46,25 +50,27 @@ using tc::unpack8h;
 
 constexpr int kThreads = 256;                       // 16 token-heads of 16 threads per block
 
-// The workspace: Ks, Vs, Rs, Os fp16 [B][2T+1][H][128]; beta_s bf16 [B][2T+1][H];
-// c fp32 [B][T][H]; each region 256-byte aligned.
+// The workspace: Ks fp16 [B][2T+1][H][128] (the sub-token keys); Vc, Rc, Oc fp16
+// [B][T][H][128] (v_t, r_t, o'_{2t}); beta_s bf16 [B][2T+1][H]; c fp32 [B][T][H]; each
+// region 256-byte aligned.
 struct EdaTcBuffers {
-    __half *Ks, *Vs, *Rs, *Os;
+    __half *Ks, *Vc, *Rc, *Oc;
     __nv_bfloat16 *bs;
     float *c;
 };
 size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
-size_t eda_rows_bytes(int B, int T, int H) { return round256((size_t)B * (2 * (size_t)T + 1) * H * kD * 2); }
+size_t eda_keys_bytes(int B, int T, int H) { return round256((size_t)B * (2 * (size_t)T + 1) * H * kD * 2); }
+size_t eda_rows_bytes(int B, int T, int H) { return round256((size_t)B * T * H * kD * 2); }
 EdaTcBuffers eda_tc_buffers(int B, int T, int H, void *ws) {
     uint8_t *p = static_cast<uint8_t *>(ws);
-    const size_t rows = eda_rows_bytes(B, T, H);
+    const size_t keys = eda_keys_bytes(B, T, H), rows = eda_rows_bytes(B, T, H);
     EdaTcBuffers w;
     w.Ks = reinterpret_cast<__half *>(p);
-    w.Vs = reinterpret_cast<__half *>(p + rows);
-    w.Rs = reinterpret_cast<__half *>(p + 2 * rows);
-    w.Os = reinterpret_cast<__half *>(p + 3 * rows);
-    w.bs = reinterpret_cast<__nv_bfloat16 *>(p + 4 * rows);
-    w.c = reinterpret_cast<float *>(p + 4 * rows + round256((size_t)B * (2 * (size_t)T + 1) * H * 2));
+    w.Vc = reinterpret_cast<__half *>(p + keys);
+    w.Rc = reinterpret_cast<__half *>(p + keys + rows);
+    w.Oc = reinterpret_cast<__half *>(p + keys + 2 * rows);
+    w.bs = reinterpret_cast<__nv_bfloat16 *>(p + keys + 3 * rows);
+    w.c = reinterpret_cast<float *>(p + keys + 3 * rows + round256((size_t)B * (2 * (size_t)T + 1) * H * 2));
     return w;
 }
 
@@ -116,17 +122,11 @@ eda_subtoken_kernel(const __nv_bfloat16 *q, const __nv_bfloat16 *k, const __nv_b
         *reinterpret_cast<uint4 *>(dst + row(s) * kD + j0) = pack8hp(f);
     };
     const float zf[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    put(w.Rs, 2 * t, rf);
-    put(w.Rs, 2 * t + 1, zf);
+    *reinterpret_cast<uint4 *>(w.Rc + (size_t)th * kD + j0) = pack8hp(rf);
+    *reinterpret_cast<uint4 *>(w.Vc + (size_t)th * kD + j0) = pack8hp(vf);
     put(w.Ks, 2 * t + 1, ef);
-    put(w.Vs, 2 * t + 1, zf);
     put(w.Ks, 2 * t + 2, kf);
-    put(w.Vs, 2 * t + 2, vf);
-    if (t == 0) {                                   // the leading sub-token changes nothing
-        put(w.Ks, 0, zf);
-        put(w.Vs, 0, zf);
-    }
-    if (t == T - 1) put(w.Rs, 2 * T, zf);
+    if (t == 0) put(w.Ks, 0, zf);                   // the leading sub-token changes nothing
     if (cg == 0) {
         w.bs[row(2 * t + 1)] = __float2bfloat16_rn(1.f);
         w.bs[row(2 * t + 2)] = __float2bfloat16_rn(bt);   // exact: a bf16 input or 1
@@ -142,12 +142,8 @@ eda_readout_kernel(const __nv_bfloat16 *v, EdaTcBuffers w, __nv_bfloat16 *o, int
     const long long th = (long long)blockIdx.x * (kThreads / 16) + (threadIdx.x >> 4);
     if (th >= n) return;
     const int j0 = 8 * (threadIdx.x & 15);
-    const long long bt_ = th / H;
-    const int h = (int)(th - bt_ * H), t = (int)(bt_ % T);
-    const long long b = bt_ / T;
-    const size_t sub = ((size_t)(b * (2 * T + 1) + 2 * t) * H + h) * kD + j0;
     float of[8], vf[8];
-    unpack8h(*reinterpret_cast<const uint4 *>(w.Os + sub), of);
+    unpack8h(*reinterpret_cast<const uint4 *>(w.Oc + (size_t)th * kD + j0), of);
     unpack8(*reinterpret_cast<const uint4 *>(v + (size_t)th * kD + j0), vf);
     const float c = w.c[th];
 #pragma unroll
@@ -163,8 +159,8 @@ bool eda_tc_supported(const EdaArgs &a, int dtype) {
 }
 
 size_t eda_tc_workspace(int B, int T, int H) {
-    return 4 * eda_rows_bytes(B, T, H) + round256((size_t)B * (2 * (size_t)T + 1) * H * 2) +
-           round256((size_t)B * T * H * 4);
+    return eda_keys_bytes(B, T, H) + 3 * eda_rows_bytes(B, T, H) +
+           round256((size_t)B * (2 * (size_t)T + 1) * H * 2) + round256((size_t)B * T * H * 4);
 }
 
 cudaError_t launch_eda_tc(const EdaArgs &a, void *ws, cudaStream_t s, int *nlaunch) {
@@ -178,12 +174,12 @@ cudaError_t launch_eda_tc(const EdaArgs &a, void *ws, cudaStream_t s, int *nlaun
     if (e != cudaSuccess) return e;
     *nlaunch += 1;
     QDeltaArgs sub{};
-    sub.q = w.Rs;
+    sub.q = w.Rc;                                     // compact: the kernel's pair maps
     sub.k = w.Ks;
-    sub.v = w.Vs;
+    sub.v = w.Vc;
     sub.beta = w.bs;
     sub.S0 = a.S0;
-    sub.o = w.Os;
+    sub.o = w.Oc;
     sub.S_final = a.S_final;
     sub.B = a.B;
     sub.T = 2 * a.T + 1;

@@ -378,6 +378,23 @@ inline bool make_token_map_tile(CUtensorMap *m, const void *ptr, int B, int T, i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A compact [B][Tc][H][128] 16-bit tensor seen as a sequence of 2 Tc sub-token rows, row j
+// of the tensor at sub-token 2j and nothing at 2j + 1: dims {128, 1, H, Tc, B} with boxes
+// {64, 2, 1, 32, 1}, so a box is 64 sub-token rows (32 pairs) of one head whose odd rows
+// fall outside the size-1 dimension (zero-filled on load, not written on store).
+inline bool make_pair_map(CUtensorMap *m, const void *ptr, int B, int Tc, int H) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[5] = {(cuuint64_t)kD, 1, (cuuint64_t)H, (cuuint64_t)Tc, (cuuint64_t)B};
+    cuuint64_t strides[4] = {(cuuint64_t)kD * 2, (cuuint64_t)kD * 2, (cuuint64_t)H * kD * 2,
+                             (cuuint64_t)Tc * H * kD * 2};
+    cuuint32_t box[5] = {64, 2, 1, (cuuint32_t)kC / 2, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 5, const_cast<void *>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // [B][T][H][128] bf16 tensor, boxes of 64 columns x 64 tokens of one head.
 inline bool make_token_map(CUtensorMap *m, const void *ptr, int B, int T, int H) {
     EncodeTiledFn fn = encode_fn();

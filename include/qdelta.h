@@ -279,8 +279,9 @@ QD_API qd_status eda_fwd(const void *q, const void *k, const void *v, const void
                          int chunk, qd_dtype dtype, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* Bytes of device workspace eda_fwd needs for these sizes: for bf16 at dk = dv = 128 the
- * fp16 sub-token keys, values, queries and outputs ([B][2T+1][H][128] each), their bf16
- * strengths and one fp32 scalar per token-head, each rounded up to 256 bytes; 0 otherwise. */
+ * fp16 sub-token keys ([B][2T+1][H][128]), the fp16 queries r_t, values and sub-token
+ * outputs ([B][T][H][128] each), the sub-tokens' bf16 strengths and one fp32 scalar per
+ * token-head, each rounded up to 256 bytes; 0 otherwise. */
 QD_API size_t eda_workspace_bytes(int B, int T, int H, int dk, int dv, int chunk, qd_dtype dtype);
 
 /*

@@ -240,13 +240,14 @@ def test_qed_workspace_covers_derived_operands_and_counters(lib, B, T, H):
 
 
 def test_eda_workspace_for_the_tensor_core_path(lib):
-    """bf16 at d_k = d_v = 128 takes the tensor-core path: four fp16 [B][2T+1][H][128]
-    sub-token arrays, their bf16 strengths and c_t (fp32 [B][T][H]), each rounded up to
-    256 bytes; a call without it is refused before any device work."""
+    """bf16 at d_k = d_v = 128 takes the tensor-core path: the fp16 sub-token keys
+    [B][2T+1][H][128], three compact fp16 [B][T][H][128] arrays (r_t, v_t, o'_2t), the
+    sub-tokens' bf16 strengths and c_t (fp32 [B][T][H]), each rounded up to 256 bytes; a
+    call without it is refused before any device work."""
     r = lambda n: (n + 255) // 256 * 256
     for B, T, H in [(2, 150, 2), (8, 2048, 16)]:
         n = B * (2 * T + 1) * H
-        want = 4 * r(n * 128 * 2) + r(n * 2) + r(B * T * H * 4)
+        want = r(n * 128 * 2) + 3 * r(B * T * H * 128 * 2) + r(n * 2) + r(B * T * H * 4)
         assert lib.eda_workspace_bytes(B, T, H, 128, 128, 64, qd.QD_BF16) == want
         assert lib.eda_workspace_bytes(B, T, H, 128, 128, 64, qd.QD_F32) == 0
         assert lib.eda_workspace_bytes(B, T, H, 128, 64, 64, qd.QD_BF16) == 0
