@@ -253,7 +253,9 @@ def eda_fwd(q, k, v, e, beta=None, S0=None, *, o=None, S_final=None, return_fina
             stream=None):
     """EDA forward (the C eda_fwd): erase along e, then the Delta write along k with
     strength beta (None = 1), o_t read after both.  q, k, e [B,T,H,dk]; v [B,T,H,dv];
-    beta [B,T,H] or None; S0 [B,H,dv,dk] fp32 or None.  Returns (o, S_final)."""
+    beta [B,T,H] or None; S0 [B,H,dv,dk] fp32 or None.  bf16 at dk = dv = 128 runs on the
+    tensor cores and needs eda_workspace_bytes() of workspace (allocated here when None).
+    Returns (o, S_final)."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
     dt = q.dtype
