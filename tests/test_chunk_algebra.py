@@ -122,3 +122,46 @@ def test_eda_is_a_delta_rule_over_subtokens(T, erase, unit_step):
     o = o_sub[0, 0:2 * T:2, 0] + c[:, None] * v[0, :, 0]
     assert np.abs(o - o_ref[0, :, 0]).max() <= 1e-12 * max(1.0, np.abs(o_ref).max())
     assert np.abs(S - S_ref).max() <= 1e-12 * max(1.0, np.abs(S_ref).max())
+
+
+def pair_map_box(compact, j0, C=64):
+    """A pair-map box as the tensor-core EDA path reads it: 64 sub-token rows whose row
+    2i + p is compact row j0 + i for p = 0 and zero for p = 1 (the size-1 dimension), zero
+    too where j0 + i falls outside [0, len(compact))."""
+    out = np.zeros((C, compact.shape[1]))
+    for i in range(C // 2):
+        j = j0 + i
+        if 0 <= j < len(compact):
+            out[2 * i] = compact[j]
+    return out
+
+
+@pytest.mark.parametrize("T", [1, 31, 32, 33, 100])
+def test_eda_pair_maps_give_the_subtoken_rows(T):
+    """The compact queries r_t and values v_t, read chunk by chunk through pair-map boxes
+    at row j0 = 32 c (queries) and 32 c - 1 (values), give exactly the sub-token query
+    and value rows; the even rows of the sub-token outputs are what a pair-map store at
+    row 32 c keeps (and a chunk starting at row T, holding only sub-token 2T, keeps none)."""
+    dk, dv = 8, 6
+    q = _unit(rng.standard_normal((T, dk)))
+    k = _unit(rng.standard_normal((T, dk)))
+    e = _unit(rng.standard_normal((T, dk)))
+    v = rng.standard_normal((T, dv))
+    beta = rng.uniform(0.05, 1.0, T)
+    K, V, Bs, Q, c = eda_subtokens(q, k, v, e, beta)
+    r = Q[0:2 * T:2]                                   # the compact queries
+    n = 2 * T + 1
+    nch = (n + 63) // 64
+    Qm = np.concatenate([pair_map_box(r, 32 * ch) for ch in range(nch)])[:n]
+    Vm = np.concatenate([pair_map_box(v, 32 * ch - 1) for ch in range(nch)])[:n]
+    np.testing.assert_array_equal(Qm, Q)
+    np.testing.assert_array_equal(Vm, V)
+    O = rng.standard_normal((nch * 64, dv))            # any sub-token outputs
+    kept = np.zeros((T, dv))
+    for ch in range(nch):
+        if 32 * ch >= T:                               # the kernel skips this store
+            continue
+        for i in range(32):
+            if 32 * ch + i < T:
+                kept[32 * ch + i] = O[64 * ch + 2 * i]
+    np.testing.assert_array_equal(kept, O[0:2 * T:2])
