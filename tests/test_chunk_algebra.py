@@ -100,7 +100,7 @@ def eda_subtokens(q, k, v, e, beta):
 
 
 @pytest.mark.parametrize("T", [1, 2, 33, 100])
-@pytest.mark.parametrize("erase", ["random", "query"])
+@pytest.mark.parametrize("erase", ["random", "query", "scaled"])
 @pytest.mark.parametrize("unit_step", [False, True])
 def test_eda_is_a_delta_rule_over_subtokens(T, erase, unit_step):
     """EDA ("Erase-then-Delta Attention": erase along e, then the Delta write) equals the
@@ -111,6 +111,8 @@ def test_eda_is_a_delta_rule_over_subtokens(T, erase, unit_step):
     q = _unit(rng.standard_normal((1, T, 1, dk)))
     k = _unit(rng.standard_normal((1, T, 1, dk)))
     e = q.copy() if erase == "query" else _unit(rng.standard_normal((1, T, 1, dk)))
+    if erase == "scaled":               # |e| != 1: the identity needs only (I - e e^T) symmetric
+        e = e * rng.uniform(0.5, 1.5, (1, T, 1, 1))
     v = rng.standard_normal((1, T, 1, dv))
     beta = None if unit_step else rng.uniform(0.05, 1.0, (1, T, 1))
     S0 = rng.standard_normal((1, 1, dv, dk)) * 0.5
